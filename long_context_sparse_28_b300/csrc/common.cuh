@@ -1,0 +1,163 @@
+// Shared device/host helpers of the CSA + HCA CUDA library (sm_103a).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+#include <stdint.h>
+
+#include "../../include/csa_hca.h"
+
+namespace csahca {
+
+// ------------------------------------------------------------------ error word / bookkeeping
+enum : unsigned { ERRBIT_BOUNDS = 1u, ERRBIT_TIMEOUT = 2u };
+
+// Device address of the error word on the current device (cached per device).
+unsigned* err_word();
+// Counts kernel launches enqueued by this library (per host thread).
+void count_launch(int n = 1);
+
+__device__ __forceinline__ void flag_error(unsigned* err, unsigned bit) { atomicOr(err, bit); }
+
+#define CSAHCA_CHECK_LAUNCH()                                        \
+    do {                                                             \
+        cudaError_t e_ = cudaGetLastError();                         \
+        if (e_ != cudaSuccess) return CSAHCA_ERR_CUDA;               \
+    } while (0)
+
+#define CSAHCA_REQUIRE(cond)                                         \
+    do {                                                             \
+        if (!(cond)) return CSAHCA_ERR_INVALID_ARG;                  \
+    } while (0)
+
+inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+int num_sms();
+
+// ------------------------------------------------------------------------- vector I/O
+// 8 consecutive elements <-> float[8]; p must be 16-byte (bf16) / 32-byte (f32) aligned.
+__device__ __forceinline__ void load8(const float* p, float (&o)[8]) {
+    float4 a = __ldg(reinterpret_cast<const float4*>(p));
+    float4 b = __ldg(reinterpret_cast<const float4*>(p) + 1);
+    o[0] = a.x; o[1] = a.y; o[2] = a.z; o[3] = a.w;
+    o[4] = b.x; o[5] = b.y; o[6] = b.z; o[7] = b.w;
+}
+__device__ __forceinline__ void load8(const __nv_bfloat16* p, float (&o)[8]) {
+    uint4 u = __ldg(reinterpret_cast<const uint4*>(p));
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        o[2 * i] = __uint_as_float(w[i] << 16);
+        o[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    }
+}
+// plain (non-__ldg) variant for buffers written earlier in the same kernel
+__device__ __forceinline__ void load8_rw(const float* p, float (&o)[8]) {
+    float4 a = *reinterpret_cast<const float4*>(p);
+    float4 b = *(reinterpret_cast<const float4*>(p) + 1);
+    o[0] = a.x; o[1] = a.y; o[2] = a.z; o[3] = a.w;
+    o[4] = b.x; o[5] = b.y; o[6] = b.z; o[7] = b.w;
+}
+__device__ __forceinline__ void load8_rw(const __nv_bfloat16* p, float (&o)[8]) {
+    uint4 u = *reinterpret_cast<const uint4*>(p);
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        o[2 * i] = __uint_as_float(w[i] << 16);
+        o[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    }
+}
+__device__ __forceinline__ void store8(float* p, const float (&v)[8]) {
+    reinterpret_cast<float4*>(p)[0] = make_float4(v[0], v[1], v[2], v[3]);
+    reinterpret_cast<float4*>(p)[1] = make_float4(v[4], v[5], v[6], v[7]);
+}
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);  // round to nearest even
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+__device__ __forceinline__ void store8(__nv_bfloat16* p, const float (&v)[8]) {
+    uint4 u;
+    u.x = pack_bf16x2(v[0], v[1]);
+    u.y = pack_bf16x2(v[2], v[3]);
+    u.z = pack_bf16x2(v[4], v[5]);
+    u.w = pack_bf16x2(v[6], v[7]);
+    *reinterpret_cast<uint4*>(p) = u;
+}
+__device__ __forceinline__ void store8(__nv_bfloat16* p, const float (&v)[8], int) { store8(p, v); }
+
+__device__ __forceinline__ float to_f32(float x) { return x; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+__device__ __forceinline__ void from_f32(float& d, float x) { d = x; }
+__device__ __forceinline__ void from_f32(__nv_bfloat16& d, float x) { d = __float2bfloat16_rn(x); }
+
+// --------------------------------------------------------------------------- warp utils
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// Block-wide exclusive prefix sum of one value per thread (blockDim.x a multiple of 32,
+// <= 1024).  `sh` must hold 33 ints.  Returns the exclusive prefix; *total gets the sum.
+__device__ __forceinline__ int block_exclusive_scan(int v, int* sh, int* total) {
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    int x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) sh[wid] = x;
+    __syncthreads();
+    if (wid == 0) {
+        int s = (lane < nw) ? sh[lane] : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            int y = __shfl_up_sync(0xffffffffu, s, o);
+            if (lane >= o) s += y;
+        }
+        if (lane < nw) sh[lane] = s;          // inclusive per-warp totals
+        if (lane == 31) sh[32] = s;
+    }
+    __syncthreads();
+    int warp_base = (wid > 0) ? sh[wid - 1] : 0;
+    int res = warp_base + x - v;
+    *total = sh[32];
+    __syncthreads();
+    return res;
+}
+
+// Monotone map float32 -> uint32 (larger float -> larger key); -0 and +0 map to the same key.
+__device__ __forceinline__ uint32_t ordered_key(float f) {
+    uint32_t u = __float_as_uint(f);
+    if (f == 0.0f) u = 0u;
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// --------------------------------------------------------------- internal launchers
+// Top-k over float32 scores (rows of `stride`, n_vis per row from q_pos or n_vis arrays).
+struct TopkWorkspace {
+    uint32_t* hist1;   // [R][4096]
+    uint32_t* hist2;   // [R][4096]
+    uint32_t* hist3;   // [R][256]
+    uint32_t* win;     // [R][words]
+    uint32_t* tie;     // [R][words]
+    int32_t* ties_needed;  // [R]
+    int64_t words;
+};
+size_t topk_workspace_bytes(int64_t R, int64_t stride);
+TopkWorkspace topk_carve(void* ws, int64_t R, int64_t stride);
+// n_vis for row r is either n_vis_arr[r] (if non-NULL) or min(Ncap, (q_pos[r]+1)/m).
+csahca_status topk_launch(const float* scores, int64_t stride, int R, const int64_t* n_vis_arr,
+                          const int64_t* q_pos, int m, int64_t Ncap, int k, int32_t* idx_out,
+                          const TopkWorkspace& tw, cudaStream_t stream);
+
+}  // namespace csahca

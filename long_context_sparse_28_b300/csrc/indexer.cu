@@ -1,0 +1,188 @@
+// a5: lightning-indexer scores I(t,s) = sum_h w[t,h] * ReLU(q[t,h] . khat_s) and the
+// csa_index_topk entry point (scores -> top-k).
+//
+// honbul.tistory.com/221 "CSA" (a small indexer finds the blocks related to the current
+// token); pogovet.com DeepSeek-V4 article, detail 4 (FP4 lightning indexer, top-k blocks per
+// query) and detail 5 (the indexer runs in FP4).
+//
+// Generic CUDA-core kernel: one thread per (query row, compressed entry).  The key codes are
+// decoded exactly (e4m3 / e2m1 code values are small integers times powers of two) and the
+// per-row (e4m3) or per-32 (e2m1) scale is applied to each 32-wide partial dot product, so
+// the only rounding is the fp32 accumulation.
+#include "common.cuh"
+#include "quant.cuh"
+
+namespace csahca {
+namespace {
+
+__device__ __forceinline__ float e2m1_value(uint32_t c) {
+    const uint32_t mag = c & 7u, e = mag >> 1, mt = mag & 1u;
+    const float v = (e == 0) ? 0.5f * (float)mt : ldexpf(1.0f + 0.5f * (float)mt, (int)e - 1);
+    return (c & 8u) ? -v : v;
+}
+
+// 8 consecutive code values (unscaled) of key row `row` starting at channel c0.
+__device__ __forceinline__ void key_codes8(const void* codes, int fmt, int d_I, int64_t row, int c0,
+                                           float (&kv)[8]) {
+    if (fmt == CSAHCA_F32) {
+        load8(static_cast<const float*>(codes) + row * d_I + c0, kv);
+    } else if (fmt == CSAHCA_BF16) {
+        load8(static_cast<const __nv_bfloat16*>(codes) + row * d_I + c0, kv);
+    } else if (fmt == CSAHCA_E4M3_ROWSCALE) {
+        const uint2 u = __ldg(reinterpret_cast<const uint2*>(static_cast<const uint8_t*>(codes) + row * d_I + c0));
+        const uint32_t w[2] = {u.x, u.y};
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const uint32_t byte = (w[i >> 2] >> (8 * (i & 3))) & 0xFFu;
+            const __half_raw h = __nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)byte, __NV_E4M3);
+            kv[i] = __half2float(__half(h));
+        }
+    } else {
+        const uint32_t u = __ldg(reinterpret_cast<const uint32_t*>(static_cast<const uint8_t*>(codes) + row * (d_I / 2) + c0 / 2));
+#pragma unroll
+        for (int i = 0; i < 8; ++i) kv[i] = e2m1_value((u >> (4 * i)) & 0xFu);
+    }
+}
+
+__device__ __forceinline__ float block_scale(const void* scales, int fmt, int d_I, int64_t row, int blk) {
+    if (fmt == CSAHCA_E4M3_ROWSCALE) return __ldg(static_cast<const float*>(scales) + row);
+    if (fmt == CSAHCA_E2M1_UE8M0) {
+        const int e = (int)__ldg(static_cast<const uint8_t*>(scales) + row * (d_I / 32) + blk) - 127;
+        return ldexpf(1.0f, e);
+    }
+    return 1.0f;
+}
+
+template <int MAXH>
+__global__ void __launch_bounds__(256) index_score_kernel(
+    const void* __restrict__ q_idx, int q_dtype, const float* __restrict__ w, const void* __restrict__ k_codes,
+    const void* __restrict__ k_scale, int fmt, int T, int H_I, int d_I, const int64_t* __restrict__ q_pos,
+    int64_t Ncap, int m, float* __restrict__ S) {
+    extern __shared__ float sh[];                 // q [H_I][d_I], then w [H_I]
+    float* qs = sh;
+    float* ws = sh + H_I * d_I;
+    const int r = blockIdx.y;
+    const int b = r / T;
+    const int64_t p = q_pos[r];
+    int64_t n = (p >= 0) ? (p + 1) / m : 0;
+    n = n < Ncap ? n : Ncap;
+    const int64_t s = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if ((int64_t)blockIdx.x * blockDim.x >= n) return;   // CTA-uniform
+    for (int i = threadIdx.x; i < H_I * d_I; i += blockDim.x) {
+        const int64_t off = (int64_t)r * H_I * d_I + i;
+        qs[i] = (q_dtype == CSAHCA_F32) ? static_cast<const float*>(q_idx)[off]
+                                        : __bfloat162float(static_cast<const __nv_bfloat16*>(q_idx)[off]);
+    }
+    for (int i = threadIdx.x; i < H_I; i += blockDim.x) ws[i] = w[(int64_t)r * H_I + i];
+    __syncthreads();
+    if (s >= n) return;
+    const int64_t row = (int64_t)b * Ncap + s;
+    float acc[MAXH];
+#pragma unroll
+    for (int h = 0; h < MAXH; ++h) acc[h] = 0.0f;
+    for (int blk = 0; blk < d_I / 32; ++blk) {
+        float part[MAXH];
+#pragma unroll
+        for (int h = 0; h < MAXH; ++h) part[h] = 0.0f;
+        for (int c0 = blk * 32; c0 < blk * 32 + 32; c0 += 8) {
+            float kv[8];
+            key_codes8(k_codes, fmt, d_I, row, c0, kv);
+#pragma unroll
+            for (int h = 0; h < MAXH; ++h) {
+                if (h < H_I) {
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) part[h] = fmaf(qs[h * d_I + c0 + c], kv[c], part[h]);
+                }
+            }
+        }
+        const float sc = block_scale(k_scale, fmt, d_I, row, blk);
+#pragma unroll
+        for (int h = 0; h < MAXH; ++h) acc[h] = fmaf(sc, part[h], acc[h]);
+    }
+    float score = 0.0f;
+#pragma unroll
+    for (int h = 0; h < MAXH; ++h)
+        if (h < H_I) score = fmaf(ws[h], fmaxf(acc[h], 0.0f), score);
+    S[(int64_t)r * Ncap + s] = score;
+}
+
+}  // namespace
+}  // namespace csahca
+
+using namespace csahca;
+
+extern "C" {
+
+size_t csa_index_topk_workspace(int B, int T, int64_t Ncap, int k) {
+    (void)k;
+    if (B <= 0 || T <= 0 || Ncap < 0) return 0;
+    const int64_t R = (int64_t)B * T;
+    return align256((size_t)R * Ncap * 4) + topk_workspace_bytes(R, Ncap);
+}
+
+static csahca_status index_validate(const void* q_idx, csahca_dtype q_dtype, const float* w, const void* k_codes,
+                                    const void* k_scale, csahca_dtype key_fmt, int B, int T, int H_I, int d_I,
+                                    const int64_t* q_pos, int64_t Ncap, int m) {
+    CSAHCA_REQUIRE(q_idx && w && k_codes && q_pos);
+    CSAHCA_REQUIRE(q_dtype == CSAHCA_F32 || q_dtype == CSAHCA_BF16);
+    CSAHCA_REQUIRE(key_fmt >= CSAHCA_F32 && key_fmt <= CSAHCA_E2M1_UE8M0);
+    CSAHCA_REQUIRE(B >= 1 && T >= 1 && (int64_t)B * T <= 65535 && H_I >= 1 && H_I <= 64);
+    CSAHCA_REQUIRE(d_I >= 32 && d_I <= 256 && d_I % 32 == 0 && H_I * d_I <= 4096);
+    CSAHCA_REQUIRE(m >= 1 && Ncap >= 1);
+    if (key_fmt >= CSAHCA_E4M3_ROWSCALE) CSAHCA_REQUIRE(k_scale != nullptr);
+    if (key_fmt == CSAHCA_F32) CSAHCA_REQUIRE(aligned(k_codes, 32));
+    else CSAHCA_REQUIRE(aligned(k_codes, 16));
+    return CSAHCA_OK;
+}
+
+static csahca_status index_scores_launch(const void* q_idx, csahca_dtype q_dtype, const float* w,
+                                         const void* k_codes, const void* k_scale, csahca_dtype key_fmt, int B,
+                                         int T, int H_I, int d_I, const int64_t* q_pos, int64_t Ncap, int m,
+                                         float* S, cudaStream_t st) {
+    const int R = B * T;
+    dim3 grid((unsigned)cdiv(Ncap, 256), (unsigned)R);
+    const size_t smem = (size_t)(H_I * d_I + H_I) * 4;
+    if (H_I <= 16)
+        index_score_kernel<16><<<grid, 256, smem, st>>>(q_idx, q_dtype, w, k_codes, k_scale, key_fmt, T, H_I, d_I,
+                                                        q_pos, Ncap, m, S);
+    else
+        index_score_kernel<64><<<grid, 256, smem, st>>>(q_idx, q_dtype, w, k_codes, k_scale, key_fmt, T, H_I, d_I,
+                                                        q_pos, Ncap, m, S);
+    count_launch();
+    CSAHCA_CHECK_LAUNCH();
+    return CSAHCA_OK;
+}
+
+csahca_status csa_index_scores(const void* q_idx, csahca_dtype q_dtype, const float* w, const void* k_codes,
+                               const void* k_scale, csahca_dtype key_fmt, int B, int T, int H_I, int d_I,
+                               const int64_t* q_pos, int64_t Ncap, int m, float* scores, csahca_stream_t stream) {
+    const csahca_status v = index_validate(q_idx, q_dtype, w, k_codes, k_scale, key_fmt, B, T, H_I, d_I, q_pos,
+                                           Ncap, m);
+    if (v != CSAHCA_OK) return v;
+    CSAHCA_REQUIRE(scores != nullptr);
+    return index_scores_launch(q_idx, q_dtype, w, k_codes, k_scale, key_fmt, B, T, H_I, d_I, q_pos, Ncap, m, scores,
+                               (cudaStream_t)stream);
+}
+
+csahca_status csa_index_topk(const void* q_idx, csahca_dtype q_dtype, const float* w, const void* k_codes,
+                             const void* k_scale, csahca_dtype key_fmt, int B, int T, int H_I, int d_I,
+                             const int64_t* q_pos, int64_t Ncap, int m, int k, int32_t* idx_out, float* scores_out,
+                             void* workspace, size_t ws_bytes, csahca_stream_t stream) {
+    const csahca_status v = index_validate(q_idx, q_dtype, w, k_codes, k_scale, key_fmt, B, T, H_I, d_I, q_pos,
+                                           Ncap, m);
+    if (v != CSAHCA_OK) return v;
+    CSAHCA_REQUIRE(idx_out != nullptr && k >= 1 && k <= 65536);
+    const int R = B * T;
+    if (!workspace || !aligned(workspace, 256) || ws_bytes < csa_index_topk_workspace(B, T, Ncap, k))
+        return CSAHCA_ERR_WORKSPACE;
+    char* ws = static_cast<char*>(workspace);
+    float* S = scores_out ? scores_out : reinterpret_cast<float*>(ws);
+    TopkWorkspace tw = topk_carve(ws + align256((size_t)R * Ncap * 4), R, Ncap);
+    cudaStream_t st = (cudaStream_t)stream;
+    const csahca_status e = index_scores_launch(q_idx, q_dtype, w, k_codes, k_scale, key_fmt, B, T, H_I, d_I, q_pos,
+                                                Ncap, m, S, st);
+    if (e != CSAHCA_OK) return e;
+    return topk_launch(S, Ncap, R, nullptr, q_pos, m, Ncap, k, idx_out, tw, st);
+}
+
+}  // extern "C"

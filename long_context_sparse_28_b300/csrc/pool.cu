@@ -1,0 +1,353 @@
+// a1/a2 softmax-gated pooling (bulk compress) and a3 cache append / ring write.
+//
+// Pooling (pogovet.com DeepSeek-V4 article, detail 4; honbul.tistory.com/221 "CSA", "HCA"):
+//   alpha_i = softmax_i(gate[j*m+i] + bias[i]);  C[j] = sum_i alpha_i X[j*m+i]  (X = K and V).
+// One warp pools one block: lanes compute the m softmax weights cooperatively, then each lane
+// owns 8 consecutive channels of K or V (16-byte loads for bf16) and walks the m tokens in
+// order, accumulating in fp32.  HBM-bound: the raw K/V are read once, the entries written once.
+//
+// Cache append (honbul.tistory.com/221 "KV cache를 줄이는 방식"): recent raw tokens live in a
+// ring (the window cache), which also holds the tail of the block being filled; a block is
+// pooled into the compressed cache the moment its last token arrives.
+#include "common.cuh"
+#include "quant.cuh"
+
+namespace csahca {
+namespace {
+
+constexpr int kMaxM = 256;
+
+// Softmax weights of one block, distributed over the warp: lane holds alpha of slots
+// lane + 32*r (r < 8).  `zsrc(i)` returns gate_i + bias_i.
+template <typename Z>
+__device__ __forceinline__ void block_weights(int m, Z zsrc, float (&a)[8]) {
+    const int lane = threadIdx.x & 31;
+    float zmax = -INFINITY;
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {
+        const int i = lane + 32 * r;
+        a[r] = (i < m) ? zsrc(i) : -INFINITY;
+        zmax = fmaxf(zmax, a[r]);
+    }
+    zmax = warp_max(zmax);
+    float zs = 0.0f;
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {
+        const int i = lane + 32 * r;
+        a[r] = (i < m) ? expf(a[r] - zmax) : 0.0f;
+        zs += a[r];
+    }
+    zs = warp_sum(zs);
+#pragma unroll
+    for (int r = 0; r < 8; ++r) a[r] = a[r] / zs;
+}
+
+__device__ __forceinline__ float alpha_of(const float (&a)[8], int i) {
+    float v = 0.0f;
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {
+        const float t = __shfl_sync(0xffffffffu, a[r], i & 31);
+        if ((i >> 5) == r) v = t;
+    }
+    return v;
+}
+
+// Pool one block with one warp.  rowptr(which, i) -> pointer to token i's row of K (which=0)
+// or V (which=1).  Writes ck_row / cv_row.
+template <typename T, typename RowPtr>
+__device__ __forceinline__ void pool_block_warp(int m, int d, const float (&a)[8], RowPtr rowptr,
+                                                T* ck_row, T* cv_row) {
+    const int lane = threadIdx.x & 31;
+    const int groups = d / 8;                 // 8-channel groups per tensor
+    for (int g0 = 0; g0 < 2 * groups; g0 += 32) {
+        const int g = g0 + lane;
+        const bool active = g < 2 * groups;
+        const int which = (g < groups) ? 0 : 1;
+        const int col = (g % groups) * 8;
+        float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+        for (int i = 0; i < m; ++i) {
+            const float al = alpha_of(a, i);  // warp-uniform loop: all lanes shuffle
+            if (active) {
+                float x[8];
+                load8_rw(rowptr(which, i) + col, x);
+#pragma unroll
+                for (int c = 0; c < 8; ++c) acc[c] = fmaf(al, x[c], acc[c]);
+            }
+        }
+        if (active) store8((which ? cv_row : ck_row) + col, acc);
+    }
+}
+
+template <typename T>
+__global__ void compress_kernel(const T* __restrict__ k_raw, const T* __restrict__ v_raw,
+                                const float* __restrict__ gate, int64_t raw_stride,
+                                const int64_t* __restrict__ raw_pos0, const int64_t* __restrict__ n_raw,
+                                const float* __restrict__ bias, int m, int B, int d, T* ck, T* cv,
+                                int64_t Ncap, int64_t max_blocks, unsigned* err) {
+    const int wpc = blockDim.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int64_t total = (int64_t)B * max_blocks;
+    for (int64_t wid = (int64_t)blockIdx.x * wpc + (threadIdx.x >> 5); wid < total;
+         wid += (int64_t)gridDim.x * wpc) {
+        const int b = (int)(wid / max_blocks);
+        const int64_t jl = wid % max_blocks;
+        const int64_t p0 = raw_pos0[b], n = n_raw[b];
+        const int64_t j = (p0 + m - 1) / m + jl;          // first block fully inside + jl
+        if ((j + 1) * m > p0 + n) continue;
+        if (j >= Ncap || (j + 1) * m - p0 > raw_stride || p0 < 0) {
+            if (lane == 0) flag_error(err, ERRBIT_BOUNDS);
+            continue;
+        }
+        const int64_t row0 = (int64_t)b * raw_stride + (j * m - p0);
+        const float* g = gate + row0;
+        float a[8];
+        block_weights(m, [&](int i) { return g[i] + bias[i]; }, a);
+        auto rowptr = [&](int which, int i) -> const T* {
+            return (which ? v_raw : k_raw) + (row0 + i) * (int64_t)d;
+        };
+        pool_block_warp<T>(m, d, a, rowptr, ck + ((int64_t)b * Ncap + j) * d, cv + ((int64_t)b * Ncap + j) * d);
+    }
+}
+
+// One CTA per sequence: pool completed blocks (reading old tokens from the ring), then write
+// the new tokens into the ring.
+template <typename T>
+__global__ void append_kernel(const T* __restrict__ k_new, const T* __restrict__ v_new,
+                              const float* __restrict__ gate_new, const void* kidx_new, int kidx_dtype,
+                              int kidx_rows, const int64_t* __restrict__ pos, int n_new, int d,
+                              const float* __restrict__ bias, int m, T* ring_k, T* ring_v,
+                              float* ring_gate, int ring_cap, T* ck, T* cv, int64_t Ncap,
+                              void* k_codes, void* k_scale, int key_fmt, int d_I, unsigned* err) {
+    const int b = blockIdx.x;
+    const int wpc = blockDim.x >> 5;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t p = pos[b];
+    if (p < 0) {
+        if (threadIdx.x == 0) flag_error(err, ERRBIT_BOUNDS);
+        return;
+    }
+    const int64_t j_lo = p / m, j_hi = (p + n_new) / m;   // completed blocks: [j_lo, j_hi)
+    const T* kn = k_new + (int64_t)b * n_new * d;
+    const T* vn = v_new + (int64_t)b * n_new * d;
+    const float* gn = gate_new + (int64_t)b * n_new;
+    const T* rk = ring_k + (int64_t)b * ring_cap * d;
+    const T* rv = ring_v + (int64_t)b * ring_cap * d;
+    const float* rg = ring_gate + (int64_t)b * ring_cap;
+    for (int64_t j = j_lo + warp; j < j_hi; j += wpc) {
+        if (j >= Ncap) {
+            if (lane == 0) flag_error(err, ERRBIT_BOUNDS);
+            continue;
+        }
+        const int64_t t0 = j * m;
+        auto gate_of = [&](int i) -> float {
+            const int64_t t = t0 + i;
+            return (t >= p) ? gn[t - p] : rg[t % ring_cap];
+        };
+        float a[8];
+        block_weights(m, [&](int i) { return gate_of(i) + bias[i]; }, a);
+        auto rowptr = [&](int which, int i) -> const T* {
+            const int64_t t = t0 + i;
+            if (t >= p) return (which ? vn : kn) + (t - p) * d;
+            return (which ? rv : rk) + (t % ring_cap) * (int64_t)d;
+        };
+        pool_block_warp<T>(m, d, a, rowptr, ck + ((int64_t)b * Ncap + j) * d, cv + ((int64_t)b * Ncap + j) * d);
+        if (k_codes != nullptr) {
+            const int r = (int)(j - j_lo);
+            const int E = d_I / 32;
+            const int64_t in_bytes = (kidx_dtype == CSAHCA_F32 ? 4 : 2);
+            const char* row = static_cast<const char*>(kidx_new) + (((int64_t)b * kidx_rows + r) * d_I) * in_bytes;
+            float x[8];
+            load_row_slice(row, kidx_dtype, E, x);
+            const int64_t er = (int64_t)b * Ncap + j;
+            quantize_row_warp(x, E, d_I, key_fmt,
+                              static_cast<char*>(k_codes) + er * key_row_bytes(key_fmt, d_I),
+                              k_scale ? static_cast<char*>(k_scale) + er * key_scale_bytes(key_fmt, d_I) : nullptr);
+        }
+    }
+    __syncthreads();
+    // write the last min(n_new, ring_cap) tokens into the ring
+    const int first = n_new > ring_cap ? n_new - ring_cap : 0;
+    const int vec = d / 8;
+    T* wk = ring_k + (int64_t)b * ring_cap * d;
+    T* wv = ring_v + (int64_t)b * ring_cap * d;
+    const int64_t items = (int64_t)(n_new - first) * vec;
+    for (int64_t it = threadIdx.x; it < items; it += blockDim.x) {
+        const int i = first + (int)(it / vec);
+        const int c = (int)(it % vec) * 8;
+        const int64_t slot = (p + i) % ring_cap;
+        float x[8];
+        load8_rw(kn + (int64_t)i * d + c, x);
+        store8(wk + slot * d + c, x);
+        load8_rw(vn + (int64_t)i * d + c, x);
+        store8(wv + slot * d + c, x);
+    }
+    for (int i = first + threadIdx.x; i < n_new; i += blockDim.x)
+        ring_gate[(int64_t)b * ring_cap + (p + i) % ring_cap] = gn[i];
+}
+
+template <typename T>
+__global__ void ring_write_kernel(const T* __restrict__ k_new, const T* __restrict__ v_new,
+                                  const float* __restrict__ gate_new, int64_t new_stride,
+                                  const int64_t* __restrict__ pos, int n_new, int d, T* ring_k,
+                                  T* ring_v, float* ring_gate, int ring_cap) {
+    const int b = blockIdx.y;
+    const int64_t p = pos[b];
+    if (p < 0) return;                     // no valid slot for a negative position
+    const int first = n_new > ring_cap ? n_new - ring_cap : 0;
+    const int vec = d / 8;
+    const int64_t items = (int64_t)(n_new - first) * vec;
+    for (int64_t it = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; it < items;
+         it += (int64_t)gridDim.x * blockDim.x) {
+        const int i = first + (int)(it / vec);
+        const int c = (int)(it % vec) * 8;
+        const int64_t slot = (p + i) % ring_cap;
+        float x[8];
+        load8(k_new + ((int64_t)b * new_stride + i) * d + c, x);
+        store8(ring_k + ((int64_t)b * ring_cap + slot) * d + c, x);
+        load8(v_new + ((int64_t)b * new_stride + i) * d + c, x);
+        store8(ring_v + ((int64_t)b * ring_cap + slot) * d + c, x);
+        if (c == 0) ring_gate[(int64_t)b * ring_cap + slot] = gate_new[(int64_t)b * new_stride + i];
+    }
+}
+
+bool kv_dtype_ok(csahca_dtype t) { return t == CSAHCA_F32 || t == CSAHCA_BF16; }
+
+csahca_status compress_impl(const void* k_raw, const void* v_raw, const float* gate, int64_t raw_stride,
+                            const int64_t* raw_pos0, const int64_t* n_raw, const float* bias, int m,
+                            int B, int d, csahca_dtype kv, void* ck, void* cv, int64_t Ncap,
+                            cudaStream_t stream) {
+    CSAHCA_REQUIRE(k_raw && v_raw && gate && raw_pos0 && n_raw && bias && ck && cv);
+    CSAHCA_REQUIRE(m >= 1 && m <= kMaxM && B >= 1 && d >= 8 && d <= 512 && d % 8 == 0);
+    CSAHCA_REQUIRE(raw_stride >= 0 && Ncap >= 0);
+    CSAHCA_REQUIRE(kv_dtype_ok(kv));
+    const size_t al = (kv == CSAHCA_F32) ? 32 : 16;
+    CSAHCA_REQUIRE(aligned(k_raw, al) && aligned(v_raw, al) && aligned(ck, al) && aligned(cv, al));
+    const int64_t max_blocks = raw_stride / m + 1;
+    const int64_t warps = (int64_t)B * max_blocks;
+    if (warps == 0 || Ncap == 0 || raw_stride == 0) return CSAHCA_OK;
+    const int threads = 256;
+    const int64_t want = cdiv(warps, threads / 32);
+    const int grid = (int)std::min<int64_t>(want, (int64_t)num_sms() * 16);
+    unsigned* err = err_word();
+    if (!err) return CSAHCA_ERR_CUDA;
+    if (kv == CSAHCA_F32)
+        compress_kernel<float><<<grid, threads, 0, stream>>>(
+            (const float*)k_raw, (const float*)v_raw, gate, raw_stride, raw_pos0, n_raw, bias, m, B, d,
+            (float*)ck, (float*)cv, Ncap, max_blocks, err);
+    else
+        compress_kernel<__nv_bfloat16><<<grid, threads, 0, stream>>>(
+            (const __nv_bfloat16*)k_raw, (const __nv_bfloat16*)v_raw, gate, raw_stride, raw_pos0, n_raw,
+            bias, m, B, d, (__nv_bfloat16*)ck, (__nv_bfloat16*)cv, Ncap, max_blocks, err);
+    count_launch();
+    CSAHCA_CHECK_LAUNCH();
+    return CSAHCA_OK;
+}
+
+csahca_status append_impl(const void* k_new, const void* v_new, const float* gate_new, const void* kidx_new,
+                          csahca_dtype kidx_dtype, const int64_t* pos, int B, int n_new, int d,
+                          csahca_dtype kv, const float* bias, int m, void* ring_k, void* ring_v,
+                          float* ring_gate, int ring_cap, void* ck, void* cv, int64_t Ncap, void* k_codes,
+                          void* k_scale, csahca_dtype key_fmt, int d_I, cudaStream_t stream) {
+    CSAHCA_REQUIRE(k_new && v_new && gate_new && pos && bias && ring_k && ring_v && ring_gate && ck && cv);
+    CSAHCA_REQUIRE(m >= 1 && m <= kMaxM && B >= 1 && n_new >= 0 && d >= 8 && d <= 512 && d % 8 == 0);
+    CSAHCA_REQUIRE(ring_cap >= 1 && ring_cap >= m - 1 && Ncap >= 0);
+    CSAHCA_REQUIRE(kv_dtype_ok(kv));
+    const size_t al = (kv == CSAHCA_F32) ? 32 : 16;
+    CSAHCA_REQUIRE(aligned(k_new, al) && aligned(v_new, al) && aligned(ring_k, al) && aligned(ring_v, al) &&
+                   aligned(ck, al) && aligned(cv, al));
+    if (k_codes) {
+        CSAHCA_REQUIRE(kidx_new && (kidx_dtype == CSAHCA_F32 || kidx_dtype == CSAHCA_BF16));
+        CSAHCA_REQUIRE(d_I >= 32 && d_I <= 256 && d_I % 32 == 0);
+        CSAHCA_REQUIRE(key_fmt >= CSAHCA_F32 && key_fmt <= CSAHCA_E2M1_UE8M0);
+        if (key_fmt == CSAHCA_E2M1_UE8M0) CSAHCA_REQUIRE(d_I % 64 == 0);
+        if (key_fmt >= CSAHCA_E4M3_ROWSCALE) CSAHCA_REQUIRE(k_scale != nullptr);
+    }
+    if (n_new == 0) return CSAHCA_OK;
+    unsigned* err = err_word();
+    if (!err) return CSAHCA_ERR_CUDA;
+    const int kidx_rows = n_new / m + 1;
+    const int threads = 256;
+    if (kv == CSAHCA_F32)
+        append_kernel<float><<<B, threads, 0, stream>>>(
+            (const float*)k_new, (const float*)v_new, gate_new, kidx_new, kidx_dtype, kidx_rows, pos, n_new, d,
+            bias, m, (float*)ring_k, (float*)ring_v, ring_gate, ring_cap, (float*)ck, (float*)cv, Ncap, k_codes,
+            k_scale, key_fmt, d_I, err);
+    else
+        append_kernel<__nv_bfloat16><<<B, threads, 0, stream>>>(
+            (const __nv_bfloat16*)k_new, (const __nv_bfloat16*)v_new, gate_new, kidx_new, kidx_dtype, kidx_rows,
+            pos, n_new, d, bias, m, (__nv_bfloat16*)ring_k, (__nv_bfloat16*)ring_v, ring_gate, ring_cap,
+            (__nv_bfloat16*)ck, (__nv_bfloat16*)cv, Ncap, k_codes, k_scale, key_fmt, d_I, err);
+    count_launch();
+    CSAHCA_CHECK_LAUNCH();
+    return CSAHCA_OK;
+}
+
+}  // namespace
+}  // namespace csahca
+
+using namespace csahca;
+
+extern "C" {
+
+csahca_status csa_compress(const void* k_raw, const void* v_raw, const float* gate, int64_t raw_stride,
+                           const int64_t* raw_pos0, const int64_t* n_raw, const float* slot_bias, int m,
+                           int B, int d, csahca_dtype kv_dtype, void* ck, void* cv, int64_t Ncap,
+                           csahca_stream_t stream) {
+    return compress_impl(k_raw, v_raw, gate, raw_stride, raw_pos0, n_raw, slot_bias, m, B, d, kv_dtype, ck, cv,
+                         Ncap, (cudaStream_t)stream);
+}
+
+csahca_status hca_compress(const void* k_raw, const void* v_raw, const float* gate, int64_t raw_stride,
+                           const int64_t* raw_pos0, const int64_t* n_raw, const float* slot_bias, int m,
+                           int B, int d, csahca_dtype kv_dtype, void* ck, void* cv, int64_t Ncap,
+                           csahca_stream_t stream) {
+    return compress_impl(k_raw, v_raw, gate, raw_stride, raw_pos0, n_raw, slot_bias, m, B, d, kv_dtype, ck, cv,
+                         Ncap, (cudaStream_t)stream);
+}
+
+csahca_status csa_cache_append(const void* k_new, const void* v_new, const float* gate_new, const void* kidx_new,
+                               csahca_dtype kidx_dtype, const int64_t* pos, int B, int n_new, int d,
+                               csahca_dtype kv_dtype, const float* slot_bias, int m, void* ring_k, void* ring_v,
+                               float* ring_gate, int ring_cap, void* ck, void* cv, int64_t Ncap, void* k_codes,
+                               void* k_scale, csahca_dtype key_fmt, int d_I, csahca_stream_t stream) {
+    if (!k_codes) return CSAHCA_ERR_INVALID_ARG;
+    return append_impl(k_new, v_new, gate_new, kidx_new, kidx_dtype, pos, B, n_new, d, kv_dtype, slot_bias, m,
+                       ring_k, ring_v, ring_gate, ring_cap, ck, cv, Ncap, k_codes, k_scale, key_fmt, d_I,
+                       (cudaStream_t)stream);
+}
+
+csahca_status hca_cache_append(const void* k_new, const void* v_new, const float* gate_new, const int64_t* pos,
+                               int B, int n_new, int d, csahca_dtype kv_dtype, const float* slot_bias, int m,
+                               void* ring_k, void* ring_v, float* ring_gate, int ring_cap, void* ck, void* cv,
+                               int64_t Ncap, csahca_stream_t stream) {
+    return append_impl(k_new, v_new, gate_new, nullptr, CSAHCA_BF16, pos, B, n_new, d, kv_dtype, slot_bias, m,
+                       ring_k, ring_v, ring_gate, ring_cap, ck, cv, Ncap, nullptr, nullptr, CSAHCA_BF16, 0,
+                       (cudaStream_t)stream);
+}
+
+csahca_status swa_ring_write(const void* k_new, const void* v_new, const float* gate_new, int64_t new_stride,
+                             const int64_t* pos, int B, int n_new, int d, csahca_dtype kv_dtype, void* ring_k,
+                             void* ring_v, float* ring_gate, int ring_cap, csahca_stream_t stream) {
+    CSAHCA_REQUIRE(k_new && v_new && gate_new && pos && ring_k && ring_v && ring_gate);
+    CSAHCA_REQUIRE(B >= 1 && n_new >= 0 && new_stride >= n_new && d >= 8 && d <= 512 && d % 8 == 0 && ring_cap >= 1);
+    CSAHCA_REQUIRE(kv_dtype_ok(kv_dtype));
+    const size_t al = (kv_dtype == CSAHCA_F32) ? 32 : 16;
+    CSAHCA_REQUIRE(aligned(k_new, al) && aligned(v_new, al) && aligned(ring_k, al) && aligned(ring_v, al));
+    if (n_new == 0) return CSAHCA_OK;
+    const int first = n_new > ring_cap ? n_new - ring_cap : 0;
+    const int64_t items = (int64_t)(n_new - first) * (d / 8);
+    dim3 grid((unsigned)std::max<int64_t>(1, std::min<int64_t>(cdiv(items, 256), 64)), B);
+    if (kv_dtype == CSAHCA_F32)
+        ring_write_kernel<float><<<grid, 256, 0, (cudaStream_t)stream>>>(
+            (const float*)k_new, (const float*)v_new, gate_new, new_stride, pos, n_new, d, (float*)ring_k,
+            (float*)ring_v, ring_gate, ring_cap);
+    else
+        ring_write_kernel<__nv_bfloat16><<<grid, 256, 0, (cudaStream_t)stream>>>(
+            (const __nv_bfloat16*)k_new, (const __nv_bfloat16*)v_new, gate_new, new_stride, pos, n_new, d,
+            (__nv_bfloat16*)ring_k, (__nv_bfloat16*)ring_v, ring_gate, ring_cap);
+    count_launch();
+    CSAHCA_CHECK_LAUNCH();
+    return CSAHCA_OK;
+}
+
+}  // extern "C"

@@ -195,3 +195,33 @@ def to_numpy(t: torch.Tensor) -> np.ndarray:
     if t.dtype == torch.float32:
         return t.numpy()
     return t.numpy()
+
+
+def prefill_inputs(w: Workload, device="cuda", b: int = 0):
+    """Inputs of one chunked-prefill problem for sequence b (synthetic prior state + chunk).
+
+    Prior state before the chunk (all values drawn, not computed): offset/m_csa CSA entries and
+    their index-key inputs, offset/m_hca HCA entries, and the W raw tokens before the chunk (the
+    window ring).  The chunk: T raw tokens (K, V, gate), T/m_csa index-key inputs for the CSA
+    entries it completes, and per query: CSA and HCA queries, indexer queries and head weights.
+    """
+    dt = torch_dtype(w.kv)
+    kdt = torch.float32 if w.key_fmt == "f32" else torch.bfloat16
+    n_csa, n_hca = w.offset // w.m_csa, w.offset // w.m_hca
+    std = _std(w.kv_std, w.d)
+    out = dict(
+        csa_ck=normal((n_csa, w.d), std, device, w.seed, "prior/csa/ck", b, dt),
+        csa_cv=normal((n_csa, w.d), std, device, w.seed, "prior/csa/cv", b, dt),
+        csa_kidx=normal((n_csa, w.d_I), _std(w.ki_std, w.d_I), device, w.seed, "prior/csa/kidx", b, kdt),
+        hca_ck=normal((n_hca, w.d), std, device, w.seed, "prior/hca/ck", b, dt),
+        hca_cv=normal((n_hca, w.d), std, device, w.seed, "prior/hca/cv", b, dt),
+        csa_bias=layer_bias(w, "csa", w.m_csa, device),
+        hca_bias=layer_bias(w, "hca", w.m_hca, device),
+    )
+    out["ring_k"], out["ring_v"], out["ring_gate"] = raw_tokens(w, "prior", b, w.W, device, tag="ring")
+    out["chunk_k"], out["chunk_v"], out["chunk_gate"] = raw_tokens(w, "chunk", b, w.T, device, pos0=w.offset)
+    out["chunk_kidx"] = index_key_inputs(w, "chunk", b, w.T // w.m_csa, device)
+    out["q_csa"] = queries(w, "csa", b, w.T, device)
+    out["q_hca"] = queries(w, "hca", b, w.T, device)
+    out["q_idx"], out["w"] = indexer_queries(w, "csa", b, w.T, device)
+    return out
