@@ -196,6 +196,29 @@ csahca_status hca_attend(const void* q, int B, int T, int H, int d, float scale,
                          float* lse, void* workspace, size_t ws_bytes, csahca_stream_t stream);
 size_t hca_attend_workspace(int B, int T, int H, int d, int64_t Ncap, int W, int splits);
 
+/* HCA dense attention without any caller workspace and without allocating.  (The method's
+ * pages have no counterpart: this serves callers that cannot allocate device memory when they
+ * run attention -- e.g. a runtime with a fixed memory budget or an embedding that only hands
+ * over its input/output buffers.)  Same arguments and results as hca_attend, minus the
+ * workspace: the split-K partial results live in one fixed device array of
+ * hca_attend_noalloc_scratch_bytes() bytes (16 MiB) inside the library, which every GPU that
+ * loads the library keeps until the process exits.  The split count is lowered until the
+ * partials fit; if one split per query (B*T*H*(d+1)*4 bytes plus alignment) does not fit,
+ * the call returns CSAHCA_ERR_WORKSPACE and enqueues nothing.  Nothing in the array needs to
+ * start at zero: every call writes all partials it reads.  All calls on a device share the
+ * array, so calls that may overlap on the GPU (different streams without ordering) race and
+ * must be serialised by the caller.  The first call on a device looks up the array's device
+ * address (cudaGetSymbolAddress, with that device current); make that first call before any
+ * stream capture.  Calls no cudaMalloc/cudaFree or allocating library routine. */
+csahca_status hca_attend_noalloc(const void* q, int B, int T, int H, int d, float scale,
+                                 const void* ck, const void* cv, int64_t Ncap, int m,
+                                 const void* ring_k, const void* ring_v, int ring_cap, int W,
+                                 const void* chunk_k, const void* chunk_v,
+                                 const int64_t* chunk_pos0, int64_t chunk_stride,
+                                 const int64_t* q_pos, int splits, csahca_dtype dtype, void* out,
+                                 float* lse, csahca_stream_t stream);
+size_t hca_attend_noalloc_scratch_bytes(void);
+
 /* --------------------------------------------------------- a3: compressed-KV cache append
  * Appends n_new raw tokens per sequence (positions pos[b] .. pos[b]+n_new-1, int64 device)
  * to the split cache of honbul.tistory.com/221 "KV cache를 줄이는 방식": the raw tokens go

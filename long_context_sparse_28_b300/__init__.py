@@ -37,6 +37,9 @@ _SIGS = {
     "hca_attend": ([_P, _I, _I, _I, _I, _F, _P, _P, _I64, _I, _P, _P, _I, _I, _P, _P, _P, _I64, _P, _I, _I, _P,
                     _P, _P, _SZ, _P], _I),
     "hca_attend_workspace": ([_I, _I, _I, _I, _I64, _I, _I], _SZ),
+    "hca_attend_noalloc": ([_P, _I, _I, _I, _I, _F, _P, _P, _I64, _I, _P, _P, _I, _I, _P, _P, _P, _I64, _P, _I, _I,
+                            _P, _P, _P], _I),
+    "hca_attend_noalloc_scratch_bytes": ([], _SZ),
     "csa_cache_append": ([_P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _P, _I, _P, _P, _P, _I, _P, _P, _I64, _P, _P,
                           _I, _I, _P], _I),
     "hca_cache_append": ([_P, _P, _P, _P, _I, _I, _I, _I, _P, _I, _P, _P, _P, _I, _P, _P, _I64, _P], _I),
@@ -238,6 +241,24 @@ def hca_attend(q, scale, ck, cv, m, ring_k, ring_v, W, q_pos, out, lse=None, chu
     _check(library().hca_attend(_p(q), B, T, H, d, float(scale), _p(ck), _p(cv), ck.shape[1], int(m), _p(ring_k),
                            _p(ring_v), ring_cap, int(W), _p(ck_), _p(cv_), _p(cp_), cs_, _p(q_pos), int(splits),
                            _dt(q), _p(out), _p(lse), _p(ws), nb, _stream(stream)), "hca_attend")
+
+
+def hca_attend_noalloc_scratch_bytes() -> int:
+    return int(library().hca_attend_noalloc_scratch_bytes())
+
+
+def hca_attend_noalloc(q, scale, ck, cv, m, ring_k, ring_v, W, q_pos, out, lse=None, chunk_k=None, chunk_v=None,
+                       chunk_pos0=None, splits=0, stream=None):
+    """hca_attend for callers that cannot allocate: no workspace argument; the split partials
+    live in the library's fixed device scratch (see include/csa_hca.h).  Calls that may
+    overlap on the GPU share that scratch and must be serialised by the caller."""
+    B, T, H, d = q.shape
+    ring_cap = ring_k.shape[1] if ring_k is not None else 0
+    ck_, cv_, cp_, cs_ = _chunk_args(chunk_k, chunk_v, chunk_pos0)
+    _check(library().hca_attend_noalloc(_p(q), B, T, H, d, float(scale), _p(ck), _p(cv), ck.shape[1], int(m),
+                                        _p(ring_k), _p(ring_v), ring_cap, int(W), _p(ck_), _p(cv_), _p(cp_), cs_,
+                                        _p(q_pos), int(splits), _dt(q), _p(out), _p(lse), _stream(stream)),
+           "hca_attend_noalloc")
 
 
 def csa_cache_append(k_new, v_new, gate_new, kidx_new, pos, slot_bias, m, ring_k, ring_v, ring_gate, ck, cv,

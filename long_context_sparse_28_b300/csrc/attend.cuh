@@ -95,6 +95,9 @@ struct SplitPlan {
 };
 SplitPlan plan_splits(int R, int64_t total_max, int splits_req);
 size_t attend_workspace_bytes(int R, int H, int d, const SplitPlan& sp);
+// Host-side argument checks and the split + merge launch sequence shared by the entry points.
+csahca_status attend_validate(const AttendArgs& a);
+csahca_status attend_run(const AttendArgs& a, int splits_req, void* workspace, size_t ws_bytes, cudaStream_t st);
 
 // Tensor-core path (bf16, d = 128): availability and launch of the split kernel.
 bool attend_tc_supported(const AttendArgs& a);
