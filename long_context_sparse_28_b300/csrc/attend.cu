@@ -125,28 +125,31 @@ __global__ void __launch_bounds__(256) attend_split_kernel(AttendArgs a, int kps
     }
 }
 
+// One CTA per (query, group of kMergeHeads heads), one thread per output channel.
+constexpr int kMergeHeads = 4;
+
 template <typename T>
-__global__ void __launch_bounds__(256) merge_kernel(int S, int H, int d, const float* __restrict__ o_part,
+__global__ void __launch_bounds__(512) merge_kernel(int S, int H, int d, const float* __restrict__ o_part,
                                                    const float* __restrict__ lse_part, T* __restrict__ out,
                                                    float* __restrict__ lse_out) {
-    const int r = blockIdx.x;
-    for (int i = threadIdx.x; i < H * d; i += blockDim.x) {
-        const int h = i / d, c = i % d;
+    const int r = blockIdx.y, c = threadIdx.x;
+    for (int hh = 0; hh < kMergeHeads; ++hh) {
+        const int h = blockIdx.x * kMergeHeads + hh;
+        if (h >= H) break;
+        const float* lp = lse_part + (int64_t)r * S * H + h;
         float mx = -INFINITY;
-        for (int s = 0; s < S; ++s) mx = fmaxf(mx, lse_part[((int64_t)r * S + s) * H + h]);
+        for (int s = 0; s < S; ++s) mx = fmaxf(mx, __ldg(lp + (int64_t)s * H));
         float tot = 0.0f, acc = 0.0f;
         if (mx != -INFINITY) {
             for (int s = 0; s < S; ++s) {
-                const int64_t base = ((int64_t)r * S + s) * H + h;
-                const float ls = lse_part[base];
+                const float ls = __ldg(lp + (int64_t)s * H);
                 if (ls == -INFINITY) continue;
                 const float e = expf(ls - mx);
                 tot += e;
-                acc = fmaf(e, o_part[base * d + c], acc);
+                acc = fmaf(e, __ldg(o_part + (((int64_t)r * S + s) * H + h) * d + c), acc);
             }
         }
-        const float val = tot > 0.0f ? acc / tot : 0.0f;
-        from_f32(out[((int64_t)r * H + h) * d + c], val);
+        from_f32(out[((int64_t)r * H + h) * d + c], tot > 0.0f ? acc / tot : 0.0f);
         if (c == 0 && lse_out) lse_out[(int64_t)r * H + h] = tot > 0.0f ? mx + logf(tot) : -INFINITY;
     }
 }
@@ -182,20 +185,19 @@ cudaError_t dispatch_generic(const AttendArgs& a, int S, int kps, float* o_part,
 }  // namespace
 
 SplitPlan plan_splits(int R, int64_t total_max, int splits_req) {
+    // Keys per split are a multiple of the 128-key tensor-core tile.  Automatic plan: splits of
+    // up to 4 tiles, shrunk until there are at least as many (query, split) items as SMs.
     SplitPlan sp;
     total_max = std::max<int64_t>(total_max, 1);
-    int64_t S;
+    int64_t kps;
     if (splits_req > 0) {
-        S = splits_req;
+        kps = cdiv(cdiv(total_max, splits_req), 128) * 128;
     } else {
-        const int64_t target = 2LL * num_sms();
-        S = std::max<int64_t>(1, cdiv(target, R));
+        kps = 512;
+        while (kps > 128 && (int64_t)R * cdiv(total_max, kps) < num_sms()) kps /= 2;
     }
-    S = std::min<int64_t>(S, cdiv(total_max, 32));
-    int64_t kps = cdiv(cdiv(total_max, S), 32) * 32;
-    S = cdiv(total_max, kps);
-    sp.S = (int)S;
     sp.kps = (int)kps;
+    sp.S = (int)cdiv(total_max, kps);
     return sp;
 }
 
@@ -224,11 +226,12 @@ csahca_status attend_run(const AttendArgs& a, int splits_req, void* workspace, s
     }
     count_launch();
     if (e != cudaSuccess) return CSAHCA_ERR_CUDA;
+    const dim3 mgrid((unsigned)cdiv(a.H, kMergeHeads), (unsigned)R);
     if (a.dtype == CSAHCA_F32)
-        merge_kernel<float><<<R, 256, 0, st>>>(sp.S, a.H, a.d, o_part, lse_part, (float*)a.out, a.lse);
+        merge_kernel<float><<<mgrid, a.d, 0, st>>>(sp.S, a.H, a.d, o_part, lse_part, (float*)a.out, a.lse);
     else
-        merge_kernel<__nv_bfloat16><<<R, 256, 0, st>>>(sp.S, a.H, a.d, o_part, lse_part, (__nv_bfloat16*)a.out,
-                                                       a.lse);
+        merge_kernel<__nv_bfloat16><<<mgrid, a.d, 0, st>>>(sp.S, a.H, a.d, o_part, lse_part,
+                                                           (__nv_bfloat16*)a.out, a.lse);
     count_launch();
     CSAHCA_CHECK_LAUNCH();
     return CSAHCA_OK;

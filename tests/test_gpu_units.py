@@ -178,7 +178,8 @@ def _rand_cache(B, Ncap, W, d, dt, seed):
     return ck, cv, rk, rv
 
 
-@pytest.mark.parametrize("dt,H,d", [("f32", 8, 64), ("bf16", 64, 128), ("bf16", 16, 128), ("bf16", 8, 64)])
+@pytest.mark.parametrize("dt,H,d", [("f32", 8, 64), ("bf16", 64, 128), ("bf16", 32, 128), ("bf16", 16, 128),
+                                    ("bf16", 8, 64)])
 def test_csa_attend_parity(dt, H, d):
     B, Ncap, W, k = 3, 300, 128, 70
     ck, cv, rk, rv = _rand_cache(B, Ncap, W, d, dt, 30)
@@ -202,7 +203,7 @@ def test_csa_attend_parity(dt, H, d):
 
 
 @pytest.mark.parametrize("splits", [0, 1, 3, 17])
-@pytest.mark.parametrize("dt,H,d", [("f32", 8, 64), ("bf16", 64, 128)])
+@pytest.mark.parametrize("dt,H,d", [("f32", 8, 64), ("bf16", 64, 128), ("bf16", 32, 128)])
 def test_hca_attend_parity(splits, dt, H, d):
     B, m, W = 3, 128, 128
     pos = np.array([128 * 40 + 5, 127, 300])                 # 40 entries; 1 entry; 2 entries
