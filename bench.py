@@ -228,7 +228,7 @@ class DecodeBench:
         self.lens = w.lengths()
         B = w.B
         grow = total_steps + 8
-        self.Ncap_c = (max(self.lens) + grow) // w.m_csa + 1
+        self.Ncap_c = ((max(self.lens) + grow) // w.m_csa + 1 + 7) // 8 * 8
         self.Ncap_h = (max(self.lens) + grow) // w.m_hca + 1
         fmt = L.KEY_FMT[w.key_fmt]
         self.csa = CSACache(B, self.Ncap_c, w.d, w.W, w.d_I, fmt, torch.bfloat16, device, m=w.m_csa)

@@ -33,7 +33,7 @@ __device__ __forceinline__ void flag_error(unsigned* err, unsigned bit) { atomic
 
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
-inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+__host__ __device__ inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 int num_sms();
 
@@ -143,6 +143,13 @@ __device__ __forceinline__ uint32_t ordered_key(float f) {
 }
 
 // --------------------------------------------------------------- internal launchers
+// Tensor-core indexer scores (low-precision keys, bf16 queries, d_I = 64, Ncap % 8 == 0).
+bool index_tc_supported(int q_dtype, int key_fmt, int H_I, int d_I, int64_t Ncap, const void* k_codes,
+                        const void* k_scale, int64_t R);
+cudaError_t index_tc_launch(const void* q_idx, const float* w, const void* k_codes, const void* k_scale, int key_fmt,
+                            int B, int T, int H_I, const int64_t* q_pos, int64_t Ncap, int m, float* S, unsigned* err,
+                            cudaStream_t st);
+
 // Top-k over float32 scores (rows of `stride`, n_vis per row from q_pos or n_vis arrays).
 struct TopkWorkspace {
     uint32_t* hist1;   // [R][4096]

@@ -140,6 +140,14 @@ static csahca_status index_scores_launch(const void* q_idx, csahca_dtype q_dtype
                                          int T, int H_I, int d_I, const int64_t* q_pos, int64_t Ncap, int m,
                                          float* S, cudaStream_t st) {
     const int R = B * T;
+    if (index_tc_supported(q_dtype, key_fmt, H_I, d_I, Ncap, k_codes, k_scale, R)) {
+        unsigned* err = err_word();
+        if (!err) return CSAHCA_ERR_CUDA;
+        const cudaError_t e = index_tc_launch(q_idx, w, k_codes, k_scale, key_fmt, B, T, H_I, q_pos, Ncap, m, S, err,
+                                              st);
+        count_launch();
+        return e == cudaSuccess ? CSAHCA_OK : CSAHCA_ERR_CUDA;
+    }
     dim3 grid((unsigned)cdiv(Ncap, 256), (unsigned)R);
     const size_t smem = (size_t)(H_I * d_I + H_I) * 4;
     if (H_I <= 16)

@@ -102,7 +102,7 @@ def csa_decode_case(w: wl.Workload, check_seqs, device="cuda", layer="csa", step
     wts = torch.cat(ww)[:, None]
     pos = torch.tensor([Lb - 1 for Lb in lengths], dtype=torch.int64, device=device)
     step = CSADecode(cache, w.H, w.H_I, w.k, bias, **(step_kwargs or {}))
-    scores = torch.full((B, 1, Ncap), float("nan"), dtype=torch.float32, device=device)
+    scores = torch.full((B, 1, cache.Ncap), float("nan"), dtype=torch.float32, device=device)
     out, lse, idx = step.step(pos, q, q_idx, wts, k_new, v_new, g_new, kidx_new, scores_out=scores)
     torch.cuda.synchronize()
     st = L.device_status()

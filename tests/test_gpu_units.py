@@ -137,10 +137,13 @@ def test_topk_from_scores_long_rows():
 
 
 # ------------------------------------------------------------------- a5 indexer scores
-@pytest.mark.parametrize("fmt,q_dt", [("f32", "f32"), ("bf16", "bf16"), ("e4m3", "bf16"), ("e2m1", "bf16")])
-def test_index_scores_and_topk_parity(fmt, q_dt):
-    B, T, H_I, d_I, m, k = 2, 3, 16, 64, 4, 96
-    Ncap = 700
+@pytest.mark.parametrize("fmt,q_dt,Ncap,H_I", [("f32", "f32", 700, 16), ("bf16", "bf16", 700, 16),
+                                               ("e4m3", "bf16", 700, 16), ("e2m1", "bf16", 700, 16),
+                                               ("e4m3", "bf16", 1000, 16), ("e2m1", "bf16", 1000, 16),
+                                               ("e2m1", "bf16", 1000, 32), ("e4m3", "bf16", 1000, 64)])
+def test_index_scores_and_topk_parity(fmt, q_dt, Ncap, H_I):
+    # Ncap % 8 == 0 (1000) runs the tensor-core indexer for e4m3/e2m1 keys; 700 the generic kernel
+    B, T, d_I, m, k = 2, 3, 64, 4, 96
     F = L.KEY_FMT[fmt]
     kin = rnd((B, Ncap, d_I), torch.float32, 21)
     kin[0, 17] *= 4
@@ -149,7 +152,7 @@ def test_index_scores_and_topk_parity(fmt, q_dt):
     L.csa_index_key_quantize(kin, F, codes, scales)
     q = rnd((B, T, H_I, d_I), DT[q_dt], 22, 0.125)
     w = torch.rand(B, T, H_I, generator=torch.Generator().manual_seed(23)).cuda()
-    pos = dev_i64([[2799, 1000, 30], [400, 2, 2799]])
+    pos = dev_i64([[4 * Ncap - 1, 1000, 30], [400, 2, 4 * Ncap + 50]])
     idx = torch.empty(B, T, k, dtype=torch.int32, device="cuda")
     sc = torch.full((B, T, Ncap), float("nan"), device="cuda")
     L.csa_index_topk(q, w, codes, scales, F, pos.reshape(-1), m, k, idx, scores_out=sc)
