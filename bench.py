@@ -43,13 +43,15 @@ UNIT = "queries/s"
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="decode_1m_b32_csa_hca")
     ap.add_argument("--cpu-seqs", type=int, default=0, help="sequences in the CPU-baseline sample (0 = auto)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--layers", default="both", choices=["both", "csa", "hca", "index"],
+                    help="restrict the step (profiling): csa / hca layer only, or the CSA indexer + top-k only")
     return ap.parse_args()
 
 
@@ -87,29 +89,37 @@ class Dist:
 
 # ------------------------------------------------------------------------- clock sampler
 class ClockSampler:
-    """Polls NVML (SM clock, max clock, power, clock-event reasons) in a thread."""
+    """Samples SM clock, max clock, power and clock-event reasons during the timed region:
+    NVML when the Python binding is importable, else ``nvidia-smi -lms`` in a subprocess."""
 
     REASONS = {
         "gpu_idle": 0x1, "applications_clocks_setting": 0x2, "sw_power_cap": 0x4, "hw_slowdown": 0x8,
         "sync_boost": 0x10, "sw_thermal_slowdown": 0x20, "hw_thermal_slowdown": 0x40,
         "hw_power_brake_slowdown": 0x80, "display_clock_setting": 0x100,
     }
+    SMI_FIELDS = ["clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active"]
 
     def __init__(self, index: int, period_s: float = 0.002):
         self.samples = []
         self.period = period_s
-        self.ok = False
+        self.index = index
+        self.mode = None
+        self.max_mhz = None
+        self.err = None
         try:
             import pynvml
             pynvml.nvmlInit()
             self.nv = pynvml
             self.h = pynvml.nvmlDeviceGetHandleByIndex(index)
             self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self.h, pynvml.NVML_CLOCK_SM)
-            self.ok = True
-        except Exception as e:  # pragma: no cover
-            self.err = str(e)
+            self.mode = "nvml"
+        except Exception as e:
+            self.err = f"nvml: {e}"
+            import shutil
+            if shutil.which("nvidia-smi"):
+                self.mode = "smi"
 
-    def _run(self):
+    def _run_nvml(self):
         nv, h = self.nv, self.h
         while not self._stop.is_set():
             try:
@@ -122,27 +132,46 @@ class ClockSampler:
             time.sleep(self.period)
 
     def __enter__(self):
-        if self.ok:
+        if self.mode == "nvml":
             self._stop = threading.Event()
-            self._t = threading.Thread(target=self._run, daemon=True)
+            self._t = threading.Thread(target=self._run_nvml, daemon=True)
             self._t.start()
+        elif self.mode == "smi":
+            import subprocess
+            self._p = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + ",".join(self.SMI_FIELDS),
+                 "--format=csv,noheader,nounits", "-lms", "20"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                text=True)
+            time.sleep(0.3)   # let the first sample land before the timed work starts
         return self
 
     def __exit__(self, *a):
-        if self.ok:
+        if self.mode == "nvml":
             self._stop.set()
             self._t.join()
+        elif self.mode == "smi":
+            time.sleep(0.05)
+            self._p.terminate()
+            out, _ = self._p.communicate(timeout=10)
+            for line in out.strip().splitlines():
+                f = [x.strip() for x in line.split(",")]
+                try:
+                    self.samples.append((float(f[0]), int(f[3], 16), float(f[2])))
+                    self.max_mhz = float(f[1])
+                except (ValueError, IndexError):
+                    continue
 
     def summary(self):
-        if not self.ok or not self.samples:
-            return {"sm_mhz": None, "sm_max_mhz": getattr(self, "max_mhz", None), "reasons": [], "samples": 0}
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": [], "samples": 0,
+                    "error": self.err or "no samples"}
         sm = [s[0] for s in self.samples]
         bits = 0
         for s in self.samples:
             bits |= s[1]
         reasons = [k for k, v in self.REASONS.items() if bits & v and k != "gpu_idle"]
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": self.max_mhz, "reasons": reasons,
-                "samples": len(sm), "power_w_max": round(max(s[2] for s in self.samples), 1)}
+                "samples": len(sm), "power_w_max": round(max(s[2] for s in self.samples), 1), "source": self.mode}
 
 
 # ---------------------------------------------------------------------------- ours
@@ -218,10 +247,10 @@ def make_step_inputs(w, step: int, lens, device, m_csa):
 class DecodeBench:
     """Caches + per-step calls of the CSA layer then the HCA layer."""
 
-    SUBSTEPS = ["csa_cache_append", "csa_index_scores", "csa_topk_from_scores", "csa_attend",
-                "hca_cache_append", "hca_attend"]
+    SUBSTEPS = ["csa_cache_append", "csa_index_topk", "csa_attend", "hca_cache_append", "hca_attend"]
 
-    def __init__(self, w, device, total_steps):
+    def __init__(self, w, device, total_steps, layers="both"):
+        import types
         import long_context_sparse_28_b300 as L
         from long_context_sparse_28_b300.layers import CSACache, HCACache
         self.L, self.w, self.dev = L, w, device
@@ -231,18 +260,31 @@ class DecodeBench:
         self.Ncap_c = ((max(self.lens) + grow) // w.m_csa + 1 + 7) // 8 * 8
         self.Ncap_h = (max(self.lens) + grow) // w.m_hca + 1
         fmt = L.KEY_FMT[w.key_fmt]
-        self.csa = CSACache(B, self.Ncap_c, w.d, w.W, w.d_I, fmt, torch.bfloat16, device, m=w.m_csa)
-        self.hca = HCACache(B, self.Ncap_h, w.d, w.W, torch.bfloat16, device, m=w.m_hca)
+        self.active = {"both": [0, 1, 2, 3, 4], "csa": [0, 1, 2], "hca": [3, 4], "index": [1]}[layers]
         self.cb = wl.layer_bias(w, "csa", w.m_csa, device)
         self.hb = wl.layer_bias(w, "hca", w.m_hca, device)
+        if layers in ("both", "csa"):
+            self.csa = CSACache(B, self.Ncap_c, w.d, w.W, w.d_I, fmt, torch.bfloat16, device, m=w.m_csa)
+        elif layers == "index":            # index keys only (no compressed K/V)
+            codes, scale = L.key_storage(B, self.Ncap_c, w.d_I, fmt, device)
+            self.csa = types.SimpleNamespace(k_codes=codes.zero_(), k_scale=scale.zero_(), key_fmt=fmt, m=w.m_csa)
+        if layers in ("both", "hca"):
+            self.hca = HCACache(B, self.Ncap_h, w.d, w.W, torch.bfloat16, device, m=w.m_hca)
         for b, Lb in enumerate(self.lens):
-            k, v, g = wl.raw_tokens(w, "csa", b, Lb - 1, device)
-            kin = wl.index_key_inputs(w, "csa", b, Lb // w.m_csa + 1, device)
-            self.csa.build_seq(b, k, v, g, self.cb, kin, Lb - 1)
-            del k, v, g, kin
-            k, v, g = wl.raw_tokens(w, "hca", b, Lb - 1, device)
-            self.hca.build_seq(b, k, v, g, self.hb, Lb - 1)
-            del k, v, g
+            if layers in ("both", "csa"):
+                k, v, g = wl.raw_tokens(w, "csa", b, Lb - 1, device)
+                kin = wl.index_key_inputs(w, "csa", b, Lb // w.m_csa + 1, device)
+                self.csa.build_seq(b, k, v, g, self.cb, kin, Lb - 1)
+                del k, v, g, kin
+            elif layers == "index":
+                n = (Lb - 1) // w.m_csa
+                kin = wl.index_key_inputs(w, "csa", b, n, device)
+                L.csa_index_key_quantize(kin, fmt, self.csa.k_codes[b, :n], self.csa.k_scale[b, :n])
+                del kin
+            if layers in ("both", "hca"):
+                k, v, g = wl.raw_tokens(w, "hca", b, Lb - 1, device)
+                self.hca.build_seq(b, k, v, g, self.hb, Lb - 1)
+                del k, v, g
         torch.cuda.synchronize()
         self.scores = torch.empty(B, 1, self.Ncap_c, dtype=torch.float32, device=device)
         self.idx = torch.empty(B, 1, w.k, dtype=torch.int32, device=device)
@@ -250,7 +292,8 @@ class DecodeBench:
         self.out_h = torch.empty(B, 1, w.H, w.d, dtype=torch.bfloat16, device=device)
         self.lse_c = torch.empty(B, 1, w.H, dtype=torch.float32, device=device)
         self.lse_h = torch.empty(B, 1, w.H, dtype=torch.float32, device=device)
-        self.ws_topk = torch.empty(L.csa_topk_workspace(B, self.Ncap_c, w.k), dtype=torch.uint8, device=device)
+        self.ws_topk = torch.empty(L.csa_index_topk_workspace(B, 1, self.Ncap_c, w.k), dtype=torch.uint8,
+                                   device=device)
         self.ws_ca = torch.empty(max(256, L.csa_attend_workspace(B, 1, w.H, w.d, w.k, w.W)), dtype=torch.uint8,
                                  device=device)
         self.ws_ha = torch.empty(max(256, L.hca_attend_workspace(B, 1, w.H, w.d, self.Ncap_h, w.W, 0)),
@@ -258,19 +301,17 @@ class DecodeBench:
         self.scale = 1.0 / math.sqrt(w.d)
 
     def substep(self, i, t):
-        L, w, c, h = self.L, self.w, self.csa, self.hca
+        L, w, c, h = self.L, self.w, getattr(self, "csa", None), getattr(self, "hca", None)
         if i == 0:
             L.csa_cache_append(t["c_k"], t["c_v"], t["c_g"], t["c_kidx"], t["pos"], self.cb, c.m, c.ring_k,
                                c.ring_v, c.ring_gate, c.ck, c.cv, c.k_codes, c.k_scale, c.key_fmt)
         elif i == 1:
-            L.csa_index_scores(t["c_qi"], t["c_w"], c.k_codes, c.k_scale, c.key_fmt, t["pos"], c.m, self.scores)
+            L.csa_index_topk(t["c_qi"], t["c_w"], c.k_codes, c.k_scale, c.key_fmt, t["pos"], c.m, w.k, self.idx,
+                             workspace=self.ws_topk)
         elif i == 2:
-            L.csa_topk_from_scores(self.scores.view(w.B, self.Ncap_c), t["nvis"], w.k, self.idx.view(w.B, w.k),
-                                   workspace=self.ws_topk)
-        elif i == 3:
             L.csa_attend(t["c_q"], self.scale, c.ck, c.cv, self.idx, c.ring_k, c.ring_v, w.W, t["pos"], self.out_c,
                          self.lse_c, workspace=self.ws_ca)
-        elif i == 4:
+        elif i == 3:
             L.hca_cache_append(t["h_k"], t["h_v"], t["h_g"], t["pos"], self.hb, h.m, h.ring_k, h.ring_v,
                                h.ring_gate, h.ck, h.cv)
         else:
@@ -278,7 +319,7 @@ class DecodeBench:
                          self.lse_h, workspace=self.ws_ha)
 
     def step(self, t):
-        for i in range(len(self.SUBSTEPS)):
+        for i in self.active:
             self.substep(i, t)
 
 
@@ -370,14 +411,17 @@ def run_ours(args, dist):
     K, Wm = args.steps, args.warmup
     total = K + Wm
     e2e_steps = 0 if args.no_e2e else min(K, 20)
-    bench = DecodeBench(w, dev, total + e2e_steps + 2)
+    if args.layers != "both":
+        e2e_steps = 0
+    bench = DecodeBench(w, dev, total + e2e_steps + 2, args.layers)
     lens = bench.lens
     stream = torch.cuda.Stream(device=dev)
     inputs = [make_step_inputs(w, s, lens, dev, w.m_csa) for s in range(total)]
     torch.cuda.synchronize()
 
     # launches per step (counted on an eager dry run into a scratch copy? no: count during capture)
-    nsub = len(DecodeBench.SUBSTEPS)
+    active = bench.active
+    nsub = len(active)
     evs = [_events(nsub + 1) for _ in range(total)]
     graphs = []
     launches_per_step = None
@@ -388,7 +432,7 @@ def run_ours(args, dist):
             with torch.cuda.graph(g, stream=stream, capture_error_mode="relaxed"):
                 for i in range(nsub):
                     _record_external(evs[s][i], stream)
-                    bench.substep(i, inputs[s].t)
+                    bench.substep(active[i], inputs[s].t)
                 _record_external(evs[s][nsub], stream)
             if launches_per_step is None:
                 launches_per_step = L.launch_count() - c0
@@ -440,10 +484,10 @@ def run_ours(args, dist):
     hbm_peak = peaks.get("hbm_gbs", 6400.0)
     peak_src = "measured" if "hbm_gbs" in peaks else "fallback"
     # dominant kernel with a defined algorithmic byte count
-    kern_bytes = {"csa_index_scores": parts["csa_index_keys"], "hca_attend": parts["hca_entries"] + parts["hca_window"],
+    kern_bytes = {"csa_index_topk": parts["csa_index_keys"], "hca_attend": parts["hca_entries"] + parts["hca_window"],
                   "csa_attend": parts["csa_gather"]}
-    per = {n: sub_ms[i] for i, n in enumerate(DecodeBench.SUBSTEPS)}
-    dom = max(kern_bytes, key=lambda n: per[n])
+    per = {DecodeBench.SUBSTEPS[a]: sub_ms[i] for i, a in enumerate(active)}
+    dom = max((n for n in kern_bytes if n in per), key=lambda n: per[n])
     dom_gbs = kern_bytes[dom] / (per[dom] / 1e3) / 1e9
     traffic = load_traffic(dom)
     roofline = {"bound": "hbm", "kernel": dom, "achieved": round(dom_gbs, 1), "peak": hbm_peak, "unit": "GB/s",
@@ -457,7 +501,7 @@ def run_ours(args, dist):
         e2e = run_e2e(bench, w, lens, total, e2e_steps, dev, dist)
 
     cpu = None
-    if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
+    if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline and args.layers == "both":
         cpu = cpu_baseline_decode(w, args.cpu_seqs or 6, dev)
 
     clocks = sampler.summary()

@@ -146,25 +146,28 @@ __device__ __forceinline__ uint32_t ordered_key(float f) {
 // Tensor-core indexer scores (low-precision keys, bf16 queries, d_I = 64, Ncap % 8 == 0).
 bool index_tc_supported(int q_dtype, int key_fmt, int H_I, int d_I, int64_t Ncap, const void* k_codes,
                         const void* k_scale, int64_t R);
+// hist1 (nullable): [B*T][4096] histogram of the top 12 bits of each visible score's ordered key.
 cudaError_t index_tc_launch(const void* q_idx, const float* w, const void* k_codes, const void* k_scale, int key_fmt,
-                            int B, int T, int H_I, const int64_t* q_pos, int64_t Ncap, int m, float* S, unsigned* err,
-                            cudaStream_t st);
+                            int B, int T, int H_I, const int64_t* q_pos, int64_t Ncap, int m, float* S,
+                            uint32_t* hist1, unsigned* err, cudaStream_t st);
 
 // Top-k over float32 scores (rows of `stride`, n_vis per row from q_pos or n_vis arrays).
 struct TopkWorkspace {
-    uint32_t* hist1;   // [R][4096]
-    uint32_t* hist2;   // [R][4096]
-    uint32_t* hist3;   // [R][256]
-    uint32_t* win;     // [R][words]
-    uint32_t* tie;     // [R][words]
-    int32_t* ties_needed;  // [R]
+    uint32_t* hist1;   // [R][4096] histogram of the top 12 bits (zeroed with cand_n)
+    int* cand_n;       // [R] candidate counts
+    uint2* cand;       // [R][cap] (ordered key, index)
+    uint32_t* win;     // [R][words] bitmap of entries above the threshold
+    uint32_t* tie;     // [R][words] bitmap of entries equal to the threshold
     int64_t words;
 };
 size_t topk_workspace_bytes(int64_t R, int64_t stride);
 TopkWorkspace topk_carve(void* ws, int64_t R, int64_t stride);
+// Bytes at the start of the workspace that must be zero before a histogram is accumulated.
+size_t topk_zero_bytes(int64_t R);
 // n_vis for row r is either n_vis_arr[r] (if non-NULL) or min(Ncap, (q_pos[r]+1)/m).
+// hist_ready: hist1/cand_n were zeroed and hist1 filled by the caller (the fused indexer).
 csahca_status topk_launch(const float* scores, int64_t stride, int R, const int64_t* n_vis_arr,
                           const int64_t* q_pos, int m, int64_t Ncap, int k, int32_t* idx_out,
-                          const TopkWorkspace& tw, cudaStream_t stream);
+                          const TopkWorkspace& tw, bool hist_ready, cudaStream_t stream);
 
 }  // namespace csahca

@@ -135,17 +135,21 @@ static csahca_status index_validate(const void* q_idx, csahca_dtype q_dtype, con
     return CSAHCA_OK;
 }
 
+// Launches the scores kernel; with a non-null hist1 the tensor-core kernel also accumulates the
+// top-k histogram (*hist_done = true), the generic kernel does not.
 static csahca_status index_scores_launch(const void* q_idx, csahca_dtype q_dtype, const float* w,
                                          const void* k_codes, const void* k_scale, csahca_dtype key_fmt, int B,
                                          int T, int H_I, int d_I, const int64_t* q_pos, int64_t Ncap, int m,
-                                         float* S, cudaStream_t st) {
+                                         float* S, uint32_t* hist1, bool* hist_done, cudaStream_t st) {
     const int R = B * T;
+    if (hist_done) *hist_done = false;
     if (index_tc_supported(q_dtype, key_fmt, H_I, d_I, Ncap, k_codes, k_scale, R)) {
         unsigned* err = err_word();
         if (!err) return CSAHCA_ERR_CUDA;
-        const cudaError_t e = index_tc_launch(q_idx, w, k_codes, k_scale, key_fmt, B, T, H_I, q_pos, Ncap, m, S, err,
-                                              st);
+        const cudaError_t e = index_tc_launch(q_idx, w, k_codes, k_scale, key_fmt, B, T, H_I, q_pos, Ncap, m, S,
+                                              hist1, err, st);
         count_launch();
+        if (hist_done) *hist_done = hist1 != nullptr;
         return e == cudaSuccess ? CSAHCA_OK : CSAHCA_ERR_CUDA;
     }
     dim3 grid((unsigned)cdiv(Ncap, 256), (unsigned)R);
@@ -169,7 +173,7 @@ csahca_status csa_index_scores(const void* q_idx, csahca_dtype q_dtype, const fl
     if (v != CSAHCA_OK) return v;
     CSAHCA_REQUIRE(scores != nullptr);
     return index_scores_launch(q_idx, q_dtype, w, k_codes, k_scale, key_fmt, B, T, H_I, d_I, q_pos, Ncap, m, scores,
-                               (cudaStream_t)stream);
+                               nullptr, nullptr, (cudaStream_t)stream);
 }
 
 csahca_status csa_index_topk(const void* q_idx, csahca_dtype q_dtype, const float* w, const void* k_codes,
@@ -187,10 +191,12 @@ csahca_status csa_index_topk(const void* q_idx, csahca_dtype q_dtype, const floa
     float* S = scores_out ? scores_out : reinterpret_cast<float*>(ws);
     TopkWorkspace tw = topk_carve(ws + align256((size_t)R * Ncap * 4), R, Ncap);
     cudaStream_t st = (cudaStream_t)stream;
+    if (cudaMemsetAsync(tw.hist1, 0, topk_zero_bytes(R), st) != cudaSuccess) return CSAHCA_ERR_CUDA;
+    bool hist_done = false;
     const csahca_status e = index_scores_launch(q_idx, q_dtype, w, k_codes, k_scale, key_fmt, B, T, H_I, d_I, q_pos,
-                                                Ncap, m, S, st);
+                                                Ncap, m, S, tw.hist1, &hist_done, st);
     if (e != CSAHCA_OK) return e;
-    return topk_launch(S, Ncap, R, nullptr, q_pos, m, Ncap, k, idx_out, tw, st);
+    return topk_launch(S, Ncap, R, nullptr, q_pos, m, Ncap, k, idx_out, tw, hist_done, st);
 }
 
 }  // extern "C"

@@ -22,8 +22,6 @@
 #include "tc_ptx.cuh"
 #include "quant.cuh"
 
-#include <cuda_fp4.h>
-
 #include <algorithm>
 
 namespace csahca {
@@ -40,7 +38,7 @@ struct IdxCfg {
     static constexpr int row_bytes = FMT == CSAHCA_E4M3_ROWSCALE ? 64 : 32;
     static constexpr int scale_bytes = FMT == CSAHCA_E4M3_ROWSCALE ? 4 : 2;
     static constexpr int tile_bytes = kKeys * row_bytes;
-    static constexpr int stages = FMT == CSAHCA_E4M3_ROWSCALE ? 6 : 8;
+    static constexpr int stages = 6;
     static constexpr int nacc = FMT == CSAHCA_E2M1_UE8M0 ? 2 : 1;
     static constexpr uint32_t a_cols = 32;
     static constexpr uint32_t d_cols = nacc * HI;
@@ -61,9 +59,11 @@ struct IdxMisc {
     uint32_t tmem_base;
     unsigned amax[2][64];
     float wq[2][64];
+    uint32_t hist[4096];   // top-12-bit histogram of the current item's scores (fused top-k pass)
 };
 
 struct Tile {          // one 128-key tile of one query row
+    int item;
     int r;
     int64_t s0;        // first key of the tile
     int64_t n;         // visible keys of the row
@@ -103,6 +103,7 @@ struct Cursor {
             n = n < Ncap ? n : Ncap;
             const int64_t s0 = (int64_t)c * kChunkTiles * kKeys;
             if (s0 < n) {
+                cur.item = item;
                 cur.r = r;
                 cur.s0 = s0;
                 cur.n = n;
@@ -124,7 +125,8 @@ __global__ void __launch_bounds__(128) index_tc_kernel(const __nv_bfloat16* __re
                                                        const uint8_t* __restrict__ k_codes,
                                                        const uint8_t* __restrict__ k_scale, int T,
                                                        const int64_t* __restrict__ q_pos, int64_t Ncap, int m,
-                                                       int R, float* __restrict__ S, unsigned* err) {
+                                                       int R, float* __restrict__ S, uint32_t* __restrict__ hist1,
+                                                       unsigned* err) {
     using C = IdxCfg<FMT, HI>;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -143,6 +145,7 @@ __global__ void __launch_bounds__(128) index_tc_kernel(const __nv_bfloat16* __re
         mbar_init(&ms.mma_done[1], 1);
         fence_mbar_init();
     }
+    for (int i = t; i < 4096; i += 128) ms.hist[i] = 0u;
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
@@ -178,7 +181,7 @@ __global__ void __launch_bounds__(128) index_tc_kernel(const __nv_bfloat16* __re
     cons.start(blockIdx.x, items, gridDim.x, R, Ncap, m, q_pos);
     int64_t g = 0;
     int qrow = -1, qbuf = 1;
-    Tile prev{0, 0, 0};
+    Tile prev{0, 0, 0, 0};
     int prev_qbuf = 0;
     float prev_sc0 = 0.0f, prev_sc1 = 0.0f;
     uint32_t ph_mma[2] = {0, 0};
@@ -213,7 +216,25 @@ __global__ void __launch_bounds__(128) index_tc_kernel(const __nv_bfloat16* __re
         if (C::nacc == 1) score *= sc0;
         const int64_t s = x.s0 + t;
         if (s < x.n) S[(int64_t)x.r * Ncap + s] = score;
+        if (hist1 != nullptr) {                        // warp-aggregated histogram update
+            const uint32_t bin = (s < x.n) ? (ordered_key(score) >> 20) : 0xFFFFFFFFu;
+            const uint32_t peers = __match_any_sync(0xffffffffu, bin);
+            if (bin != 0xFFFFFFFFu && (t & 31) == __ffs(peers) - 1) atomicAdd(&ms.hist[bin], (uint32_t)__popc(peers));
+        }
         fence_before_sync();
+    };
+    // adds the item's smem histogram to the row's global one and clears it
+    auto flush_hist = [&](int r) {
+        __syncthreads();
+        uint32_t* gh = hist1 + (int64_t)r * 4096;
+        for (int i = t; i < 4096; i += 128) {
+            const uint32_t v = ms.hist[i];
+            if (v) {
+                atomicAdd(&gh[i], v);
+                ms.hist[i] = 0u;
+            }
+        }
+        __syncthreads();
     };
 
     while (cons.valid) {
@@ -273,24 +294,25 @@ __global__ void __launch_bounds__(128) index_tc_kernel(const __nv_bfloat16* __re
             const uint4 u1 = *reinterpret_cast<const uint4*>(row + 16);
             const uint32_t wds[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                const __half2_raw h2 = __nv_cvt_fp4x2_to_halfraw2(
-                    (__nv_fp4x2_storage_t)((wds[i >> 2] >> (8 * (i & 3))) & 0xFFu), __NV_E2M1);
-                a[i] = (uint32_t)h2.x | ((uint32_t)h2.y << 16);
+            for (int i = 0; i < 8; ++i) {
+                uint32_t o[4];
+                cvt_e2m1x8_f16(wds[i], o);
+                a[4 * i] = o[0]; a[4 * i + 1] = o[1]; a[4 * i + 2] = o[2]; a[4 * i + 3] = o[3];
             }
-            const uint16_t e2 = *reinterpret_cast<const uint16_t*>(sm + C::off_scale + st * kKeys * 2 + t * 2);
-            sc0 = ldexpf(1.0f, (int)(e2 & 0xFF) - 127);
-            sc1 = ldexpf(1.0f, (int)(e2 >> 8) - 127);
+            const uint32_t e2 = *reinterpret_cast<const uint16_t*>(sm + C::off_scale + st * kKeys * 2 + t * 2);
+            sc0 = ue8m0_value(e2 & 0xFFu);
+            sc1 = ue8m0_value(e2 >> 8);
         } else {
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
                 const uint4 u = *reinterpret_cast<const uint4*>(row + 16 * c);
                 const uint32_t wds[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const __half2_raw h2 = __nv_cvt_fp8x2_to_halfraw2(
-                        (__nv_fp8x2_storage_t)((wds[i >> 1] >> (16 * (i & 1))) & 0xFFFFu), __NV_E4M3);
-                    a[8 * c + i] = (uint32_t)h2.x | ((uint32_t)h2.y << 16);
+                for (int i = 0; i < 4; ++i) {
+                    uint32_t o[2];
+                    cvt_e4m3x4_f16(wds[i], o);
+                    a[8 * c + 2 * i] = o[0];
+                    a[8 * c + 2 * i + 1] = o[1];
                 }
             }
             sc0 = *reinterpret_cast<const float*>(sm + C::off_scale + st * kKeys * 4 + t * 4);
@@ -314,7 +336,10 @@ __global__ void __launch_bounds__(128) index_tc_kernel(const __nv_bfloat16* __re
             }
             mma_commit(&ms.mma_done[g & 1]);
         }
-        if (g > 0) epilogue(g - 1, prev, prev_qbuf, prev_sc0, prev_sc1);
+        if (g > 0) {
+            epilogue(g - 1, prev, prev_qbuf, prev_sc0, prev_sc1);
+            if (hist1 != nullptr && prev.item != x.item) flush_hist(prev.r);
+        }
         prev = x;
         prev_qbuf = qbuf;
         prev_sc0 = sc0;
@@ -322,7 +347,10 @@ __global__ void __launch_bounds__(128) index_tc_kernel(const __nv_bfloat16* __re
         ++g;
         cons.advance();
     }
-    if (g > 0) epilogue(g - 1, prev, prev_qbuf, prev_sc0, prev_sc1);
+    if (g > 0) {
+        epilogue(g - 1, prev, prev_qbuf, prev_sc0, prev_sc1);
+        if (hist1 != nullptr) flush_hist(prev.r);
+    }
     __syncthreads();
     fence_after_sync();
     if (warp == 0) tmem_dealloc(tmem, C::tmem_cols);
@@ -330,11 +358,11 @@ __global__ void __launch_bounds__(128) index_tc_kernel(const __nv_bfloat16* __re
 
 template <int FMT, int HI>
 cudaError_t launch_index_tc(const void* q_idx, const float* w, const void* k_codes, const void* k_scale, int B,
-                            int T, const int64_t* q_pos, int64_t Ncap, int m, float* S, unsigned* err,
+                            int T, const int64_t* q_pos, int64_t Ncap, int m, float* S, uint32_t* hist1, unsigned* err,
                             cudaStream_t st) {
     using C = IdxCfg<FMT, HI>;
-    // one CTA per 1/ctas_per_sm of the SM's shared memory, so TMEM is never oversubscribed
-    const size_t per_cta = (size_t)(227 * 1024) / C::ctas_per_sm - 8 * 1024;
+    // shared memory sized so that at most ctas_per_sm CTAs fit on an SM (TMEM never oversubscribed)
+    const size_t per_cta = (size_t)(228 * 1024) / (C::ctas_per_sm + 1) + 1024 - sizeof(IdxMisc);
     const size_t smem = std::max<size_t>((size_t)C::total + 1024, per_cta);
     auto kern = index_tc_kernel<FMT, HI>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -343,7 +371,7 @@ cudaError_t launch_index_tc(const void* q_idx, const float* w, const void* k_cod
     const int64_t items = (int64_t)R * cdiv(Ncap, (int64_t)kChunkTiles * kKeys);
     const int grid = (int)std::min<int64_t>(items, (int64_t)num_sms() * C::ctas_per_sm);
     kern<<<grid, 128, smem, st>>>(static_cast<const __nv_bfloat16*>(q_idx), w, static_cast<const uint8_t*>(k_codes),
-                                  static_cast<const uint8_t*>(k_scale), T, q_pos, Ncap, m, R, S, err);
+                                  static_cast<const uint8_t*>(k_scale), T, q_pos, Ncap, m, R, S, hist1, err);
     return cudaGetLastError();
 }
 
@@ -357,11 +385,11 @@ bool index_tc_supported(int q_dtype, int key_fmt, int H_I, int d_I, int64_t Ncap
 }
 
 cudaError_t index_tc_launch(const void* q_idx, const float* w, const void* k_codes, const void* k_scale, int key_fmt,
-                            int B, int T, int H_I, const int64_t* q_pos, int64_t Ncap, int m, float* S, unsigned* err,
-                            cudaStream_t st) {
+                            int B, int T, int H_I, const int64_t* q_pos, int64_t Ncap, int m, float* S,
+                            uint32_t* hist1, unsigned* err, cudaStream_t st) {
 #define CSAHCA_IDX_CASE(F, HH)                                                                                  \
     if (key_fmt == F && H_I == HH)                                                                              \
-        return launch_index_tc<F, HH>(q_idx, w, k_codes, k_scale, B, T, q_pos, Ncap, m, S, err, st);
+        return launch_index_tc<F, HH>(q_idx, w, k_codes, k_scale, B, T, q_pos, Ncap, m, S, hist1, err, st);
     CSAHCA_IDX_CASE(CSAHCA_E2M1_UE8M0, 16)
     CSAHCA_IDX_CASE(CSAHCA_E2M1_UE8M0, 32)
     CSAHCA_IDX_CASE(CSAHCA_E2M1_UE8M0, 64)

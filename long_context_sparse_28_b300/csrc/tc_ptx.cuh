@@ -179,5 +179,26 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
         : "memory");
 }
 
+// Exact decodes of packed low-precision codes into f16x2 (hardware conversions): one 32-bit
+// word of eight e2m1 codes -> four f16x2 words; one word of four e4m3 codes -> two f16x2 words.
+// Element order is kept: the lower code lands in the lower half.
+__device__ __forceinline__ void cvt_e2m1x8_f16(uint32_t w, uint32_t (&o)[4]) {
+    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %4;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %0, b0;\n\tcvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %2, b2;\n\tcvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+        : "=r"(o[0]), "=r"(o[1]), "=r"(o[2]), "=r"(o[3])
+        : "r"(w));
+}
+__device__ __forceinline__ void cvt_e4m3x4_f16(uint32_t w, uint32_t (&o)[2]) {
+    asm("{\n\t.reg .b16 h0, h1;\n\tmov.b32 {h0, h1}, %2;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, h0;\n\tcvt.rn.f16x2.e4m3x2 %1, h1;\n\t}"
+        : "=r"(o[0]), "=r"(o[1])
+        : "r"(w));
+}
+// 2^(b - 127) for a UE8M0 byte b (b = 0 gives 2^-127, a float32 subnormal).
+__device__ __forceinline__ float ue8m0_value(uint32_t b) {
+    return b ? __uint_as_float(b << 23) : __uint_as_float(0x00400000u);
+}
+
 }  // namespace tc
 }  // namespace csahca
