@@ -125,33 +125,49 @@ __global__ void __launch_bounds__(256) attend_split_kernel(AttendArgs a, int kps
     }
 }
 
-// One CTA per (query, group of kMergeHeads heads), one thread per output channel.
-constexpr int kMergeHeads = 4;
+// One warp per (query, head): lanes first turn the S partial log-sum-exps into merge weights
+// (max-subtracted, fixed order), then stream the S partial outputs with 16-byte loads.
+constexpr int kMergeWarps = 8;
 
 template <typename T>
-__global__ void __launch_bounds__(512) merge_kernel(int S, int H, int d, const float* __restrict__ o_part,
-                                                   const float* __restrict__ lse_part, T* __restrict__ out,
-                                                   float* __restrict__ lse_out) {
-    const int r = blockIdx.y, c = threadIdx.x;
-    for (int hh = 0; hh < kMergeHeads; ++hh) {
-        const int h = blockIdx.x * kMergeHeads + hh;
-        if (h >= H) break;
-        const float* lp = lse_part + (int64_t)r * S * H + h;
-        float mx = -INFINITY;
-        for (int s = 0; s < S; ++s) mx = fmaxf(mx, __ldg(lp + (int64_t)s * H));
-        float tot = 0.0f, acc = 0.0f;
-        if (mx != -INFINITY) {
-            for (int s = 0; s < S; ++s) {
-                const float ls = __ldg(lp + (int64_t)s * H);
-                if (ls == -INFINITY) continue;
-                const float e = expf(ls - mx);
-                tot += e;
-                acc = fmaf(e, __ldg(o_part + (((int64_t)r * S + s) * H + h) * d + c), acc);
-            }
-        }
-        from_f32(out[((int64_t)r * H + h) * d + c], tot > 0.0f ? acc / tot : 0.0f);
-        if (c == 0 && lse_out) lse_out[(int64_t)r * H + h] = tot > 0.0f ? mx + logf(tot) : -INFINITY;
+__global__ void __launch_bounds__(32 * kMergeWarps) merge_kernel(int R, int S, int H, int d,
+                                                                 const float* __restrict__ o_part,
+                                                                 const float* __restrict__ lse_part,
+                                                                 T* __restrict__ out, float* __restrict__ lse_out) {
+    const int lane = threadIdx.x & 31;
+    const int64_t gw = (int64_t)blockIdx.x * kMergeWarps + (threadIdx.x >> 5);
+    if (gw >= (int64_t)R * H) return;
+    const int r = (int)(gw / H), h = (int)(gw % H);
+    const float* lp = lse_part + (int64_t)r * S * H + h;
+    float mx = -INFINITY;
+    for (int s = lane; s < S; s += 32) mx = fmaxf(mx, __ldg(lp + (int64_t)s * H));
+    mx = warp_max(mx);
+    float tot = 0.0f;
+    for (int s = lane; s < S; s += 32) {
+        const float ls = __ldg(lp + (int64_t)s * H);
+        tot += (ls == -INFINITY || mx == -INFINITY) ? 0.0f : expf(ls - mx);
     }
+    tot = warp_sum(tot);
+    const float inv = tot > 0.0f ? 1.0f / tot : 0.0f;
+    for (int c0 = lane * 4; c0 < d; c0 += 128) {
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int s = 0; s < S; ++s) {
+            const float ls = __ldg(lp + (int64_t)s * H);
+            if (ls == -INFINITY) continue;
+            const float e = expf(ls - mx) * inv;
+            const float4 o = __ldg(reinterpret_cast<const float4*>(o_part + (((int64_t)r * S + s) * H + h) * d + c0));
+            acc.x = fmaf(e, o.x, acc.x);
+            acc.y = fmaf(e, o.y, acc.y);
+            acc.z = fmaf(e, o.z, acc.z);
+            acc.w = fmaf(e, o.w, acc.w);
+        }
+        T* op = out + ((int64_t)r * H + h) * d + c0;
+        from_f32(op[0], acc.x);
+        from_f32(op[1], acc.y);
+        from_f32(op[2], acc.z);
+        from_f32(op[3], acc.w);
+    }
+    if (lane == 0 && lse_out) lse_out[(int64_t)r * H + h] = tot > 0.0f ? mx + logf(tot) : -INFINITY;
 }
 
 template <typename T, int HPW, int DPL>
@@ -226,12 +242,13 @@ csahca_status attend_run(const AttendArgs& a, int splits_req, void* workspace, s
     }
     count_launch();
     if (e != cudaSuccess) return CSAHCA_ERR_CUDA;
-    const dim3 mgrid((unsigned)cdiv(a.H, kMergeHeads), (unsigned)R);
+    const unsigned mgrid = (unsigned)cdiv((int64_t)R * a.H, kMergeWarps);
     if (a.dtype == CSAHCA_F32)
-        merge_kernel<float><<<mgrid, a.d, 0, st>>>(sp.S, a.H, a.d, o_part, lse_part, (float*)a.out, a.lse);
+        merge_kernel<float><<<mgrid, 32 * kMergeWarps, 0, st>>>(R, sp.S, a.H, a.d, o_part, lse_part, (float*)a.out,
+                                                                a.lse);
     else
-        merge_kernel<__nv_bfloat16><<<mgrid, a.d, 0, st>>>(sp.S, a.H, a.d, o_part, lse_part,
-                                                           (__nv_bfloat16*)a.out, a.lse);
+        merge_kernel<__nv_bfloat16><<<mgrid, 32 * kMergeWarps, 0, st>>>(R, sp.S, a.H, a.d, o_part, lse_part,
+                                                                        (__nv_bfloat16*)a.out, a.lse);
     count_launch();
     CSAHCA_CHECK_LAUNCH();
     return CSAHCA_OK;

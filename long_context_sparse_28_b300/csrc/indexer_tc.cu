@@ -23,6 +23,7 @@
 #include "quant.cuh"
 
 #include <algorithm>
+#include <cstddef>
 
 namespace csahca {
 namespace {
@@ -38,14 +39,14 @@ struct IdxCfg {
     static constexpr int row_bytes = FMT == CSAHCA_E4M3_ROWSCALE ? 64 : 32;
     static constexpr int scale_bytes = FMT == CSAHCA_E4M3_ROWSCALE ? 4 : 2;
     static constexpr int tile_bytes = kKeys * row_bytes;
-    static constexpr int stages = 6;
+    static constexpr int stages = 4;
     static constexpr int nacc = FMT == CSAHCA_E2M1_UE8M0 ? 2 : 1;
-    static constexpr uint32_t a_cols = 32;
+    static constexpr uint32_t a_cols = 32;                 // 64 16-bit values per key row
     static constexpr uint32_t d_cols = nacc * HI;
-    static constexpr uint32_t need_cols = 2 * a_cols + 2 * d_cols;
+    static constexpr uint32_t need_cols = a_cols + d_cols;
     static constexpr uint32_t tmem_cols = need_cols <= 32 ? 32 : need_cols <= 64 ? 64 : need_cols <= 128 ? 128
                                         : need_cols <= 256 ? 256 : 512;
-    static constexpr int ctas_per_sm = 512 / tmem_cols;
+    static constexpr int tmem_ctas = 512 / tmem_cols;
     // shared memory: code stages | scale stages | q buffers (2 x HI rows x 128 B)
     static constexpr uint32_t off_scale = stages * tile_bytes;
     static constexpr uint32_t off_q = (off_scale + stages * kKeys * scale_bytes + 1023) / 1024 * 1024;
@@ -54,13 +55,14 @@ struct IdxCfg {
 };
 
 struct IdxMisc {
-    uint64_t full[8];
-    uint64_t mma_done[2];
-    uint32_t tmem_base;
+    alignas(16) float wq[2][64];        // read as float4
+    alignas(16) uint32_t hist[4096];    // top-12-bit histogram of the current item's scores (fused top-k pass)
     unsigned amax[2][64];
-    float wq[2][64];
-    uint32_t hist[4096];   // top-12-bit histogram of the current item's scores (fused top-k pass)
+    uint64_t full[4];
+    uint64_t mma_done;
+    uint32_t tmem_base;
 };
+static_assert(offsetof(IdxMisc, wq) % 16 == 0, "wq is read with 16-byte loads");
 
 struct Tile {          // one 128-key tile of one query row
     int item;
@@ -141,8 +143,7 @@ __global__ void __launch_bounds__(128) index_tc_kernel(const __nv_bfloat16* __re
     }
     if (t == 0) {
         for (int s = 0; s < C::stages; ++s) mbar_init(&ms.full[s], 1);
-        mbar_init(&ms.mma_done[0], 1);
-        mbar_init(&ms.mma_done[1], 1);
+        mbar_init(&ms.mma_done, 1);
         fence_mbar_init();
     }
     for (int i = t; i < 4096; i += 128) ms.hist[i] = 0u;
@@ -181,48 +182,12 @@ __global__ void __launch_bounds__(128) index_tc_kernel(const __nv_bfloat16* __re
     cons.start(blockIdx.x, items, gridDim.x, R, Ncap, m, q_pos);
     int64_t g = 0;
     int qrow = -1, qbuf = 1;
-    Tile prev{0, 0, 0, 0};
-    int prev_qbuf = 0;
-    float prev_sc0 = 0.0f, prev_sc1 = 0.0f;
-    uint32_t ph_mma[2] = {0, 0};
+    int cur_item = -1, cur_r = 0;
+    uint32_t ph_mma = 0;
     const uint32_t id = idesc_f16(128, HI, 0, 0, 0);
+    const uint32_t abuf = tmem;
+    const uint32_t dbuf = tmem + C::a_cols;
 
-    auto epilogue = [&](int64_t gi, const Tile& x, int qb, float sc0, float sc1) {
-        const int dbuf = (int)(gi & 1);
-        mbar_wait(&ms.mma_done[dbuf], ph_mma[dbuf], err);
-        ph_mma[dbuf] ^= 1;
-        fence_after_sync();
-        const uint32_t dcol = tmem + 2 * C::a_cols + dbuf * C::d_cols + lane_off;
-        float score = 0.0f;
-#pragma unroll
-        for (int c0 = 0; c0 < HI; c0 += 16) {
-            uint32_t r0[16];
-            tmem_ld16(dcol + c0, r0);
-            if (C::nacc == 2) {
-                uint32_t r1[16];
-                tmem_ld16(dcol + HI + c0, r1);
-                tmem_wait_ld();
-#pragma unroll
-                for (int k = 0; k < 16; ++k) {
-                    const float v = fmaf(sc0, __uint_as_float(r0[k]), sc1 * __uint_as_float(r1[k]));
-                    score = fmaf(ms.wq[qb][c0 + k], fmaxf(v, 0.0f), score);
-                }
-            } else {
-                tmem_wait_ld();
-#pragma unroll
-                for (int k = 0; k < 16; ++k) score = fmaf(ms.wq[qb][c0 + k], fmaxf(__uint_as_float(r0[k]), 0.0f), score);
-            }
-        }
-        if (C::nacc == 1) score *= sc0;
-        const int64_t s = x.s0 + t;
-        if (s < x.n) S[(int64_t)x.r * Ncap + s] = score;
-        if (hist1 != nullptr) {                        // warp-aggregated histogram update
-            const uint32_t bin = (s < x.n) ? (ordered_key(score) >> 20) : 0xFFFFFFFFu;
-            const uint32_t peers = __match_any_sync(0xffffffffu, bin);
-            if (bin != 0xFFFFFFFFu && (t & 31) == __ffs(peers) - 1) atomicAdd(&ms.hist[bin], (uint32_t)__popc(peers));
-        }
-        fence_before_sync();
-    };
     // adds the item's smem histogram to the row's global one and clears it
     auto flush_hist = [&](int r) {
         __syncthreads();
@@ -240,6 +205,9 @@ __global__ void __launch_bounds__(128) index_tc_kernel(const __nv_bfloat16* __re
     while (cons.valid) {
         const Tile x = cons.cur;
         const int st = (int)(g % C::stages);
+        if (hist1 != nullptr && x.item != cur_item && cur_item >= 0) flush_hist(cur_r);
+        cur_item = x.item;
+        cur_r = x.r;
         // ---- query row for this tile (B operand, f16 scaled per head; w' = w * 2^-e)
         if (x.r != qrow) {
             qrow = x.r;
@@ -284,7 +252,7 @@ __global__ void __launch_bounds__(128) index_tc_kernel(const __nv_bfloat16* __re
             }
             fence_proxy_async();
         }
-        // ---- this thread's key row -> f16 -> TMEM (A buffer g & 1)
+        // ---- this thread's key row -> f16 -> TMEM (A operand)
         mbar_wait(&ms.full[st], (uint32_t)((g / C::stages) & 1), err);
         uint32_t a[32];
         const unsigned char* row = sm + st * C::tile_bytes + t * C::row_bytes;
@@ -317,15 +285,13 @@ __global__ void __launch_bounds__(128) index_tc_kernel(const __nv_bfloat16* __re
             }
             sc0 = *reinterpret_cast<const float*>(sm + C::off_scale + st * kKeys * 4 + t * 4);
         }
-        const uint32_t abuf = tmem + (uint32_t)(g & 1) * C::a_cols;
         tmem_st32(abuf + lane_off, a);
         tmem_wait_st();
         fence_before_sync();
-        __syncthreads();                         // stage st consumed, A written, q ready
+        __syncthreads();                         // stage st consumed, A written, q ready, D read
         if (t == 0) {
             if (prod.valid) produce();           // refill stage st with the tile NS steps ahead
             fence_after_sync();
-            const uint32_t dbuf = tmem + 2 * C::a_cols + (uint32_t)(g & 1) * C::d_cols;
             const uint32_t qb = sbase + C::off_q + qbuf * C::q_buf;
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
@@ -334,23 +300,52 @@ __global__ void __launch_bounds__(128) index_tc_kernel(const __nv_bfloat16* __re
                 const uint32_t acc = (C::nacc == 2) ? (uint32_t)(j & 1) : (uint32_t)(j > 0);
                 mma_ts(dst, abuf + j * 8, bd, id, acc);
             }
-            mma_commit(&ms.mma_done[g & 1]);
+            mma_commit(&ms.mma_done);
         }
-        if (g > 0) {
-            epilogue(g - 1, prev, prev_qbuf, prev_sc0, prev_sc1);
-            if (hist1 != nullptr && prev.item != x.item) flush_hist(prev.r);
+        // ---- epilogue: score = sum_h w'_h ReLU(scaled accumulators)
+        mbar_wait(&ms.mma_done, ph_mma, err);
+        ph_mma ^= 1;
+        fence_after_sync();
+        float score = 0.0f;
+        const float4* wq4 = reinterpret_cast<const float4*>(ms.wq[qbuf]);
+#pragma unroll
+        for (int c0 = 0; c0 < HI; c0 += 16) {
+            uint32_t r0[16];
+            tmem_ld16(dbuf + lane_off + c0, r0);
+            float wv[16];
+#pragma unroll
+            for (int k4 = 0; k4 < 4; ++k4) {
+                const float4 q4 = wq4[c0 / 4 + k4];
+                wv[4 * k4] = q4.x; wv[4 * k4 + 1] = q4.y; wv[4 * k4 + 2] = q4.z; wv[4 * k4 + 3] = q4.w;
+            }
+            if (C::nacc == 2) {
+                uint32_t r1[16];
+                tmem_ld16(dbuf + lane_off + HI + c0, r1);
+                tmem_wait_ld();
+#pragma unroll
+                for (int k = 0; k < 16; ++k) {
+                    const float v = fmaf(sc0, __uint_as_float(r0[k]), sc1 * __uint_as_float(r1[k]));
+                    score = fmaf(wv[k], fmaxf(v, 0.0f), score);
+                }
+            } else {
+                tmem_wait_ld();
+#pragma unroll
+                for (int k = 0; k < 16; ++k) score = fmaf(wv[k], fmaxf(__uint_as_float(r0[k]), 0.0f), score);
+            }
         }
-        prev = x;
-        prev_qbuf = qbuf;
-        prev_sc0 = sc0;
-        prev_sc1 = sc1;
+        if (C::nacc == 1) score *= sc0;
+        const int64_t s = x.s0 + t;
+        if (s < x.n) S[(int64_t)x.r * Ncap + s] = score;
+        if (hist1 != nullptr) {                        // warp-aggregated histogram update
+            const uint32_t bin = (s < x.n) ? (ordered_key(score) >> 20) : 0xFFFFFFFFu;
+            const uint32_t peers = __match_any_sync(0xffffffffu, bin);
+            if (bin != 0xFFFFFFFFu && (t & 31) == __ffs(peers) - 1) atomicAdd(&ms.hist[bin], (uint32_t)__popc(peers));
+        }
+        fence_before_sync();
         ++g;
         cons.advance();
     }
-    if (g > 0) {
-        epilogue(g - 1, prev, prev_qbuf, prev_sc0, prev_sc1);
-        if (hist1 != nullptr) flush_hist(prev.r);
-    }
+    if (hist1 != nullptr && cur_item >= 0) flush_hist(cur_r);
     __syncthreads();
     fence_after_sync();
     if (warp == 0) tmem_dealloc(tmem, C::tmem_cols);
@@ -361,15 +356,18 @@ cudaError_t launch_index_tc(const void* q_idx, const float* w, const void* k_cod
                             int T, const int64_t* q_pos, int64_t Ncap, int m, float* S, uint32_t* hist1, unsigned* err,
                             cudaStream_t st) {
     using C = IdxCfg<FMT, HI>;
-    // shared memory sized so that at most ctas_per_sm CTAs fit on an SM (TMEM never oversubscribed)
-    const size_t per_cta = (size_t)(228 * 1024) / (C::ctas_per_sm + 1) + 1024 - sizeof(IdxMisc);
+    // shared memory sized so that no more CTAs fit on an SM than TMEM can hold
+    const size_t per_cta = (size_t)(228 * 1024) / (C::tmem_ctas + 1) + 1024 - sizeof(IdxMisc);
     const size_t smem = std::max<size_t>((size_t)C::total + 1024, per_cta);
+    // CTAs per SM: limited by shared memory (228 KB per SM, 1 KB reserved per CTA) and TMEM
+    const size_t per_sm_cta = smem + sizeof(IdxMisc) + 1024;
+    const int occ = std::max(1, std::min((int)((size_t)(228 * 1024) / per_sm_cta), C::tmem_ctas));
     auto kern = index_tc_kernel<FMT, HI>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const int R = B * T;
     const int64_t items = (int64_t)R * cdiv(Ncap, (int64_t)kChunkTiles * kKeys);
-    const int grid = (int)std::min<int64_t>(items, (int64_t)num_sms() * C::ctas_per_sm);
+    const int grid = (int)std::min<int64_t>(items, (int64_t)num_sms() * occ);
     kern<<<grid, 128, smem, st>>>(static_cast<const __nv_bfloat16*>(q_idx), w, static_cast<const uint8_t*>(k_codes),
                                   static_cast<const uint8_t*>(k_scale), T, q_pos, Ncap, m, R, S, hist1, err);
     return cudaGetLastError();

@@ -110,20 +110,24 @@ __global__ void compress_kernel(const T* __restrict__ k_raw, const T* __restrict
 }
 
 // One CTA per sequence: pool completed blocks (reading old tokens from the ring), then write
-// the new tokens into the ring.
+// the new tokens into the ring.  A completed block is pooled by the whole CTA: warp 0 computes
+// the m softmax weights into shared memory, then every thread sums a subset of the m tokens for
+// 8 channels of K or V (loads unrolled), and the partial sums are added in a fixed order.
+constexpr int kAppendThreads = 256;
+
 template <typename T>
-__global__ void append_kernel(const T* __restrict__ k_new, const T* __restrict__ v_new,
-                              const float* __restrict__ gate_new, const void* kidx_new, int kidx_dtype,
-                              int kidx_rows, const int64_t* __restrict__ pos, int n_new, int d,
-                              const float* __restrict__ bias, int m, T* ring_k, T* ring_v,
-                              float* ring_gate, int ring_cap, T* ck, T* cv, int64_t Ncap,
-                              void* k_codes, void* k_scale, int key_fmt, int d_I, unsigned* err) {
+__global__ void __launch_bounds__(kAppendThreads) append_kernel(
+    const T* __restrict__ k_new, const T* __restrict__ v_new, const float* __restrict__ gate_new,
+    const void* kidx_new, int kidx_dtype, int kidx_rows, const int64_t* __restrict__ pos, int n_new, int d,
+    const float* __restrict__ bias, int m, T* ring_k, T* ring_v, float* ring_gate, int ring_cap, T* ck, T* cv,
+    int64_t Ncap, void* k_codes, void* k_scale, int key_fmt, int d_I, unsigned* err) {
+    __shared__ float alpha[kMaxM];
+    __shared__ float part[kAppendThreads * 8];
     const int b = blockIdx.x;
-    const int wpc = blockDim.x >> 5;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int64_t p = pos[b];
     if (p < 0) {
-        if (threadIdx.x == 0) flag_error(err, ERRBIT_BOUNDS);
+        if (tid == 0) flag_error(err, ERRBIT_BOUNDS);
         return;
     }
     const int64_t j_lo = p / m, j_hi = (p + n_new) / m;   // completed blocks: [j_lo, j_hi)
@@ -133,25 +137,70 @@ __global__ void append_kernel(const T* __restrict__ k_new, const T* __restrict__
     const T* rk = ring_k + (int64_t)b * ring_cap * d;
     const T* rv = ring_v + (int64_t)b * ring_cap * d;
     const float* rg = ring_gate + (int64_t)b * ring_cap;
-    for (int64_t j = j_lo + warp; j < j_hi; j += wpc) {
+    const int G = 2 * d / 8;                               // 8-channel groups of K then V
+    const int NS = G >= kAppendThreads ? 1 : kAppendThreads / G;   // token subsets
+    const int per = (m + NS - 1) / NS;
+    for (int64_t j = j_lo; j < j_hi; ++j) {
         if (j >= Ncap) {
-            if (lane == 0) flag_error(err, ERRBIT_BOUNDS);
+            if (tid == 0) flag_error(err, ERRBIT_BOUNDS);
             continue;
         }
         const int64_t t0 = j * m;
-        auto gate_of = [&](int i) -> float {
-            const int64_t t = t0 + i;
-            return (t >= p) ? gn[t - p] : rg[t % ring_cap];
-        };
-        float a[8];
-        block_weights(m, [&](int i) { return gate_of(i) + bias[i]; }, a);
-        auto rowptr = [&](int which, int i) -> const T* {
-            const int64_t t = t0 + i;
-            if (t >= p) return (which ? vn : kn) + (t - p) * d;
-            return (which ? rv : rk) + (t % ring_cap) * (int64_t)d;
-        };
-        pool_block_warp<T>(m, d, a, rowptr, ck + ((int64_t)b * Ncap + j) * d, cv + ((int64_t)b * Ncap + j) * d);
-        if (k_codes != nullptr) {
+        if (warp == 0) {
+            float a[8];
+            block_weights(m, [&](int i) {
+                const int64_t t = t0 + i;
+                return ((t >= p) ? gn[t - p] : rg[t % ring_cap]) + bias[i];
+            }, a);
+#pragma unroll
+            for (int r = 0; r < 8; ++r)
+                if (lane + 32 * r < m) alpha[lane + 32 * r] = a[r];
+        }
+        __syncthreads();
+        const int g = tid % G, ts = tid / G;
+        float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+        if (ts < NS) {
+            const int which = (g < G / 2) ? 0 : 1;
+            const int col = (g % (G / 2)) * 8;
+            const int i0 = ts * per, i1 = min(m, i0 + per);
+            int i = i0;
+            for (; i + 4 <= i1; i += 4) {
+                float x[4][8];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int64_t t = t0 + i + u;
+                    const T* src = (t >= p) ? (which ? vn : kn) + (t - p) * d
+                                            : (which ? rv : rk) + (t % ring_cap) * (int64_t)d;
+                    load8_rw(src + col, x[u]);
+                }
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) acc[c] = fmaf(alpha[i + u], x[u][c], acc[c]);
+            }
+            for (; i < i1; ++i) {
+                const int64_t t = t0 + i;
+                const T* src = (t >= p) ? (which ? vn : kn) + (t - p) * d
+                                        : (which ? rv : rk) + (t % ring_cap) * (int64_t)d;
+                float x[8];
+                load8_rw(src + col, x);
+#pragma unroll
+                for (int c = 0; c < 8; ++c) acc[c] = fmaf(alpha[i], x[c], acc[c]);
+            }
+        }
+#pragma unroll
+        for (int c = 0; c < 8; ++c) part[tid * 8 + c] = acc[c];
+        __syncthreads();
+        if (tid < G) {                                      // subsets added in order 0..NS-1
+            float o[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+            for (int q = 0; q < NS; ++q)
+#pragma unroll
+                for (int c = 0; c < 8; ++c) o[c] += part[(q * G + tid) * 8 + c];
+            const int which = (tid < G / 2) ? 0 : 1;
+            const int col = (tid % (G / 2)) * 8;
+            store8((which ? cv : ck) + ((int64_t)b * Ncap + j) * d + col, o);
+        }
+        if (k_codes != nullptr && warp == 1) {
             const int r = (int)(j - j_lo);
             const int E = d_I / 32;
             const int64_t in_bytes = (kidx_dtype == CSAHCA_F32 ? 4 : 2);
@@ -159,19 +208,18 @@ __global__ void append_kernel(const T* __restrict__ k_new, const T* __restrict__
             float x[8];
             load_row_slice(row, kidx_dtype, E, x);
             const int64_t er = (int64_t)b * Ncap + j;
-            quantize_row_warp(x, E, d_I, key_fmt,
-                              static_cast<char*>(k_codes) + er * key_row_bytes(key_fmt, d_I),
+            quantize_row_warp(x, E, d_I, key_fmt, static_cast<char*>(k_codes) + er * key_row_bytes(key_fmt, d_I),
                               k_scale ? static_cast<char*>(k_scale) + er * key_scale_bytes(key_fmt, d_I) : nullptr);
         }
+        __syncthreads();
     }
-    __syncthreads();
     // write the last min(n_new, ring_cap) tokens into the ring
     const int first = n_new > ring_cap ? n_new - ring_cap : 0;
     const int vec = d / 8;
     T* wk = ring_k + (int64_t)b * ring_cap * d;
     T* wv = ring_v + (int64_t)b * ring_cap * d;
     const int64_t items = (int64_t)(n_new - first) * vec;
-    for (int64_t it = threadIdx.x; it < items; it += blockDim.x) {
+    for (int64_t it = tid; it < items; it += blockDim.x) {
         const int i = first + (int)(it / vec);
         const int c = (int)(it % vec) * 8;
         const int64_t slot = (p + i) % ring_cap;
@@ -181,7 +229,7 @@ __global__ void append_kernel(const T* __restrict__ k_new, const T* __restrict__
         load8_rw(vn + (int64_t)i * d + c, x);
         store8(wv + slot * d + c, x);
     }
-    for (int i = first + threadIdx.x; i < n_new; i += blockDim.x)
+    for (int i = first + tid; i < n_new; i += blockDim.x)
         ring_gate[(int64_t)b * ring_cap + (p + i) % ring_cap] = gn[i];
 }
 
@@ -268,12 +316,12 @@ csahca_status append_impl(const void* k_new, const void* v_new, const float* gat
     const int kidx_rows = n_new / m + 1;
     const int threads = 256;
     if (kv == CSAHCA_F32)
-        append_kernel<float><<<B, threads, 0, stream>>>(
+        append_kernel<float><<<B, kAppendThreads, 0, stream>>>(
             (const float*)k_new, (const float*)v_new, gate_new, kidx_new, kidx_dtype, kidx_rows, pos, n_new, d,
             bias, m, (float*)ring_k, (float*)ring_v, ring_gate, ring_cap, (float*)ck, (float*)cv, Ncap, k_codes,
             k_scale, key_fmt, d_I, err);
     else
-        append_kernel<__nv_bfloat16><<<B, threads, 0, stream>>>(
+        append_kernel<__nv_bfloat16><<<B, kAppendThreads, 0, stream>>>(
             (const __nv_bfloat16*)k_new, (const __nv_bfloat16*)v_new, gate_new, kidx_new, kidx_dtype, kidx_rows,
             pos, n_new, d, bias, m, (__nv_bfloat16*)ring_k, (__nv_bfloat16*)ring_v, ring_gate, ring_cap,
             (__nv_bfloat16*)ck, (__nv_bfloat16*)cv, Ncap, k_codes, k_scale, key_fmt, d_I, err);
