@@ -106,6 +106,7 @@ __global__ void __launch_bounds__(128, 1) attend_tc_kernel(AttendArgs a, int S, 
     const uint32_t sbase = smem_u32(sm);
     uint32_t ph_s = 0, ph_o = 0;
     const float c_log2 = a.scale * 1.4426950408889634f;
+    const uint64_t pol_stream = l2_policy_evict_first();     // K/V rows are read once per step
     const uint32_t id_qk = idesc_f16(128, H, 1, 0, 0);
     const uint32_t id_pv = idesc_f16(128, H, 1, 1, 1);
 
@@ -144,7 +145,7 @@ __global__ void __launch_bounds__(128, 1) attend_tc_kernel(AttendArgs a, int S, 
                 const __nv_bfloat16* src = (lane < 16) ? ms.rowk[st][row] : ms.rowv[st][row];
                 const int cc = lane & 15;
                 const uint32_t dst = stb + (lane < 16 ? 0 : 2 * kHalf) + (cc >> 3) * kHalf + sw128(row, cc & 7);
-                if (src) cp_async16(dst, src + cc * 8, 16);
+                if (src) cp_async16_hint(dst, src + cc * 8, 16, pol_stream);
                 else cp_async16(dst, qr, 0);                 // zero fill (no bytes read)
             }
         };

@@ -155,6 +155,7 @@ cudaError_t index_tc_launch(const void* q_idx, const float* w, const void* k_cod
 struct TopkWorkspace {
     uint32_t* hist1;   // [R][4096] histogram of the top 12 bits (zeroed with cand_n)
     int* cand_n;       // [R] candidate counts
+    int4* thr1;        // [R] boundary bin of the top 12 bits, count above it, candidate-list flag
     uint2* cand;       // [R][cap] (ordered key, index)
     uint32_t* win;     // [R][words] bitmap of entries above the threshold
     uint32_t* tie;     // [R][words] bitmap of entries equal to the threshold

@@ -154,6 +154,9 @@ __global__ void __launch_bounds__(128) index_tc_kernel(const __nv_bfloat16* __re
     const uint32_t lane_off = (uint32_t)(32 * warp) << 16;
     const int items = R * (int)cdiv(Ncap, (int64_t)kChunkTiles * kKeys);
 
+    // key codes are read once per step: keep them from evicting the scores the top-k re-reads
+    const uint64_t pol_stream = l2_policy_evict_first();
+    const uint64_t pol_keep = l2_policy_evict_last();
     // producer (thread 0): issues the bulk copies of tile `pt` into stage pg % NS
     Cursor prod;
     int64_t pg = 0;
@@ -167,9 +170,9 @@ __global__ void __launch_bounds__(128) index_tc_kernel(const __nv_bfloat16* __re
         const uint32_t cb = (uint32_t)(rows * C::row_bytes);
         const uint32_t sb = (uint32_t)(srows * C::scale_bytes);
         mbar_arrive_expect_tx(&ms.full[st], cb + sb);
-        bulk_g2s(sbase + st * C::tile_bytes, k_codes + row0 * C::row_bytes, cb, &ms.full[st]);
-        bulk_g2s(sbase + C::off_scale + st * kKeys * C::scale_bytes, k_scale + row0 * C::scale_bytes, sb,
-                 &ms.full[st]);
+        bulk_g2s_hint(sbase + st * C::tile_bytes, k_codes + row0 * C::row_bytes, cb, &ms.full[st], pol_stream);
+        bulk_g2s_hint(sbase + C::off_scale + st * kKeys * C::scale_bytes, k_scale + row0 * C::scale_bytes, sb,
+                      &ms.full[st], pol_stream);
         ++pg;
         prod.advance();
     };
@@ -335,7 +338,7 @@ __global__ void __launch_bounds__(128) index_tc_kernel(const __nv_bfloat16* __re
         }
         if (C::nacc == 1) score *= sc0;
         const int64_t s = x.s0 + t;
-        if (s < x.n) S[(int64_t)x.r * Ncap + s] = score;
+        if (s < x.n) st_global_hint(S + (int64_t)x.r * Ncap + s, score, pol_keep);
         if (hist1 != nullptr) {                        // warp-aggregated histogram update
             const uint32_t bin = (s < x.n) ? (ordered_key(score) >> 20) : 0xFFFFFFFFu;
             const uint32_t peers = __match_any_sync(0xffffffffu, bin);

@@ -5,9 +5,10 @@
 // Exact radix select on the order-preserving 32-bit image of each score (12 + 12 + 8 bits):
 //   hist  : 4096-bin histogram of the top 12 bits per row -- fused into the indexer's
 //           tensor-core epilogue, or a separate pass over the scores;
-//   collect (slices x rows CTAs): every CTA finds the boundary bin b1 from the histogram; when
-//           the elements in bins >= b1 number at most kCap, they are appended (key, index) to a
-//           per-row candidate list;
+//   threshold (one CTA per row): the boundary bin b1 where the running count from the top
+//           reaches k;
+//   collect (slices x rows CTAs): when the elements in bins >= b1 number at most kCap, they are
+//           appended (key, index) to a per-row candidate list;
 //   finish (one CTA per row): resolves the remaining 20 bits on the candidates (or, for rows
 //           whose boundary bin is too full, on the whole row), marks "above the threshold" and
 //           "equal to the threshold" entries in two bitmaps, then scans the bitmaps in index
@@ -90,59 +91,123 @@ __global__ void __launch_bounds__(kThreads) topk_hist_kernel(const float* __rest
         if (sh[i]) atomicAdd(&gh[i], sh[i]);
 }
 
-// Appends every element of bins >= b1 to the row's candidate list when they fit.
-__global__ void __launch_bounds__(kThreads) topk_collect_kernel(const float* __restrict__ scores, int64_t stride,
-                                                                const int64_t* __restrict__ n_vis_arr,
-                                                                const int64_t* __restrict__ q_pos, int m,
-                                                                int64_t Ncap, int k, const uint32_t* __restrict__ hist1,
-                                                                uint2* __restrict__ cand, int* __restrict__ cand_n) {
+// Per row: the boundary bin b1 of the top-12-bit histogram, the count above it, and whether the
+// elements of bins >= b1 fit the candidate list (x = b1, y = above1, z = fits).
+__global__ void __launch_bounds__(kThreads) topk_threshold_kernel(const int64_t* __restrict__ n_vis_arr,
+                                                                  const int64_t* __restrict__ q_pos, int m,
+                                                                  int64_t Ncap, int64_t stride, int k,
+                                                                  const uint32_t* __restrict__ hist1,
+                                                                  int4* __restrict__ thr1) {
     __shared__ int sh_scan[33];
     __shared__ int sh_res[2];
-    const int r = blockIdx.y;
+    const int r = blockIdx.x;
     const int64_t n = min(row_nvis(r, n_vis_arr, q_pos, m, Ncap), stride);
-    const int64_t s0 = (int64_t)blockIdx.x * kSlice;
-    if (s0 >= n || n <= k) return;                       // CTA-uniform
+    if (n <= k) {
+        if (threadIdx.x == 0) thr1[r] = make_int4(0, 0, 0, 0);
+        return;
+    }
     int b1;
     uint32_t above1;
     const uint32_t* h = hist1 + (int64_t)r * kBins12;
     find_bin(h, kBins12, (uint32_t)k, sh_scan, sh_res, &b1, &above1);
-    if (above1 + h[b1] > (uint32_t)kCap) return;        // the finish kernel scans the whole row
-    const int64_t s1 = min(n, s0 + kSlice);
-    const float* row = scores + (int64_t)r * stride;
+    if (threadIdx.x == 0) thr1[r] = make_int4(b1, (int)above1, above1 + h[b1] <= (uint32_t)kCap ? 1 : 0, 0);
+}
+
+// Smallest float32 whose ordered key has top-12-bit bin b (inverse of ordered_key on b << 20).
+__device__ __forceinline__ float bin_floor_value(int b) {
+    const uint32_t key = (uint32_t)b << 20;
+    return __uint_as_float((key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key);
+}
+
+// Appends every element of bins >= b1 to the row's candidate list when they fit.  Warp-centric:
+// each warp owns 1024 consecutive scores (32 per lane, 16-byte loads), compares them with the
+// bin's floor value, reserves its range of the list with one atomic and writes its candidates.
+constexpr int kWarpSpan = 1024;
+
+__global__ void __launch_bounds__(kThreads) topk_collect_kernel(const float* __restrict__ scores, int64_t stride,
+                                                                const int64_t* __restrict__ n_vis_arr,
+                                                                const int64_t* __restrict__ q_pos, int m,
+                                                                int64_t Ncap, int k, const int4* __restrict__ thr1,
+                                                                uint2* __restrict__ cand, int* __restrict__ cand_n) {
+    const int r = blockIdx.y;
     const int lane = threadIdx.x & 31;
-    for (int64_t base = s0 + (threadIdx.x & ~31); base < s1; base += blockDim.x) {
-        const int64_t s = base + lane;
-        uint32_t key = 0;
-        bool take = false;
-        if (s < s1) {
-            key = ordered_key(row[s]);
-            take = (int)(key >> 20) >= b1;
+    const int64_t w0 = ((int64_t)blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5)) * kWarpSpan;
+    const int64_t n = min(row_nvis(r, n_vis_arr, q_pos, m, Ncap), stride);
+    if (w0 >= n || n <= k) return;                       // warp-uniform
+    const int4 th = thr1[r];
+    if (!th.z) return;                                   // the finish kernel scans the whole row
+    const float tv = bin_floor_value(th.x);
+    const int cnt_n = (int)min((int64_t)kWarpSpan, n - w0);   // valid scores in this warp's span
+    const float* row = scores + (int64_t)r * stride + w0;
+    const bool vec = ((reinterpret_cast<uintptr_t>(row) & 15) == 0) && cnt_n == kWarpSpan;
+    float v[32];
+    if (vec) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const float4 x = __ldg(reinterpret_cast<const float4*>(row) + j * 32 + lane);
+            v[4 * j] = x.x; v[4 * j + 1] = x.y; v[4 * j + 2] = x.z; v[4 * j + 3] = x.w;
         }
-        const uint32_t bal = __ballot_sync(0xffffffffu, take);
-        if (bal) {
-            int off = 0;
-            if (lane == 0) off = atomicAdd(&cand_n[r], __popc(bal));
-            off = __shfl_sync(0xffffffffu, off, 0);
-            if (take) cand[(int64_t)r * kCap + off + __popc(bal & ((1u << lane) - 1u))] = make_uint2(key, (uint32_t)s);
+    } else {
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const int i = (j * 32 + lane) * 4 + c;
+                v[4 * j + c] = i < cnt_n ? __ldg(row + i) : -INFINITY;
+            }
+    }
+    uint32_t bits = 0;
+#pragma unroll
+    for (int e = 0; e < 32; ++e) {
+        const int i = ((e >> 2) * 32 + lane) * 4 + (e & 3);
+        if (i < cnt_n && v[e] >= tv) bits |= 1u << e;
+    }
+    const int mine = __popc(bits);
+    int incl = mine;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+    }
+    const int total = __shfl_sync(0xffffffffu, incl, 31);
+    if (total == 0) return;
+    int base = 0;
+    if (lane == 0) base = atomicAdd(&cand_n[r], total);
+    base = __shfl_sync(0xffffffffu, base, 0) + incl - mine;
+    uint2* out = cand + (int64_t)r * kCap;
+#pragma unroll
+    for (int e = 0; e < 32; ++e) {
+        if (bits & (1u << e)) {
+            const int i = ((e >> 2) * 32 + lane) * 4 + (e & 3);
+            out[base++] = make_uint2(ordered_key(v[e]), (uint32_t)(w0 + i));
         }
     }
 }
 
-// One CTA per row: exact threshold, bitmaps, ascending compaction.
+// One CTA per row: exact threshold, bitmaps, ascending compaction.  Candidates and (for rows of
+// up to kSmemWords*32 entries) both bitmaps live in shared memory.
+constexpr int kSmemWords = 8192;
+constexpr size_t kFinishSmem = (size_t)kCap * 8 + 2 * (size_t)kSmemWords * 4 + (size_t)kBins12 * 4;
+
 __global__ void __launch_bounds__(kFinishThreads) topk_finish_kernel(
     const float* __restrict__ scores, int64_t stride, const int64_t* __restrict__ n_vis_arr,
     const int64_t* __restrict__ q_pos, int m, int64_t Ncap, int k, const uint32_t* __restrict__ hist1,
-    const uint2* __restrict__ cand, const int* __restrict__ cand_n, uint32_t* __restrict__ win,
-    uint32_t* __restrict__ tie, int64_t words, int32_t* __restrict__ idx_out) {
-    __shared__ uint32_t sh_hist[kBins12];
+    const int4* __restrict__ thr1, const uint2* __restrict__ cand, const int* __restrict__ cand_n,
+    uint32_t* __restrict__ win, uint32_t* __restrict__ tie, int64_t words, int32_t* __restrict__ idx_out) {
+    extern __shared__ __align__(16) unsigned char fsm[];
+    uint2* cs = reinterpret_cast<uint2*>(fsm);
+    uint32_t* swin = reinterpret_cast<uint32_t*>(fsm + (size_t)kCap * 8);
+    uint32_t* stie = swin + kSmemWords;
+    uint32_t* sh_hist = stie + kSmemWords;
     __shared__ int sh_scan[33];
     __shared__ int sh_res[2];
     const int r = blockIdx.x;
     const int tid = threadIdx.x, nthr = blockDim.x, lane = tid & 31, warp = tid >> 5, nw = nthr >> 5;
     const int64_t n = min(row_nvis(r, n_vis_arr, q_pos, m, Ncap), min(stride, words * 32));
     const int64_t nwords = (n + 31) / 32;
-    uint32_t* wr = win + (int64_t)r * words;
-    uint32_t* tr = tie + (int64_t)r * words;
+    const bool smem_bits = nwords <= kSmemWords;
+    uint32_t* wr = smem_bits ? swin : win + (int64_t)r * words;
+    uint32_t* tr = smem_bits ? stie : tie + (int64_t)r * words;
     const float* row = scores + (int64_t)r * stride;
     int ties_needed = 0;
 
@@ -153,27 +218,28 @@ __global__ void __launch_bounds__(kFinishThreads) topk_finish_kernel(
             tr[w] = 0u;
         }
     } else {
-        int b1;
-        uint32_t above1;
-        const uint32_t* h1 = hist1 + (int64_t)r * kBins12;
-        find_bin(h1, kBins12, (uint32_t)k, sh_scan, sh_res, &b1, &above1);
-        const bool fast = above1 + h1[b1] <= (uint32_t)kCap;
-        const int nc = fast ? cand_n[r] : 0;
-        const uint2* cr = cand + (int64_t)r * kCap;
+        const int4 th = thr1[r];
+        const int b1 = th.x;
+        const uint32_t above1 = (uint32_t)th.y;
+        const bool fast = th.z != 0;
+        const int nc = fast ? min(cand_n[r], kCap) : 0;
+        if (fast)
+            for (int i = tid; i < nc; i += nthr) cs[i] = cand[(int64_t)r * kCap + i];
+        for (int64_t w = tid; w < nwords; w += nthr) {
+            wr[w] = 0u;
+            tr[w] = 0u;
+        }
+        for (int i = tid; i < kBins12; i += nthr) sh_hist[i] = 0;
+        __syncthreads();
         // visits (key, index) of the source: the candidate list, or the whole row
         auto for_each = [&](auto&& f) {
             if (fast) {
-                for (int i = tid; i < nc; i += nthr) {
-                    const uint2 e = cr[i];
-                    f(e.x, (int64_t)e.y);
-                }
+                for (int i = tid; i < nc; i += nthr) f(cs[i].x, (int64_t)cs[i].y);
             } else {
                 for (int64_t s = tid; s < n; s += nthr) f(ordered_key(row[s]), s);
             }
         };
         // bits 19..8 inside the boundary bin
-        for (int i = tid; i < kBins12; i += nthr) sh_hist[i] = 0;
-        __syncthreads();
         for_each([&](uint32_t key, int64_t) {
             if ((int)(key >> 20) == b1) atomicAdd(&sh_hist[(key >> 8) & 0xFFFu], 1u);
         });
@@ -197,13 +263,8 @@ __global__ void __launch_bounds__(kFinishThreads) topk_finish_kernel(
         ties_needed = (int)((uint32_t)k - above1 - above2 - above3);
         // bitmaps
         if (fast) {
-            for (int64_t w = tid; w < nwords; w += nthr) {
-                wr[w] = 0u;
-                tr[w] = 0u;
-            }
-            __syncthreads();
             for (int i = tid; i < nc; i += nthr) {
-                const uint2 e = cr[i];
+                const uint2 e = cs[i];
                 if (e.x > thr) atomicOr(&wr[e.y >> 5], 1u << (e.y & 31));
                 else if (e.x == thr) atomicOr(&tr[e.y >> 5], 1u << (e.y & 31));
             }
@@ -261,8 +322,8 @@ __global__ void __launch_bounds__(kFinishThreads) topk_finish_kernel(
 
 size_t topk_workspace_bytes(int64_t R, int64_t stride) {
     const int64_t words = (stride + 31) / 32;
-    return align256((size_t)R * kBins12 * 4) + align256((size_t)R * 4) + align256((size_t)R * kCap * 8) +
-           align256((size_t)R * words * 4) * 2;
+    return align256((size_t)R * kBins12 * 4) + align256((size_t)R * 4) + align256((size_t)R * 16) +
+           align256((size_t)R * kCap * 8) + align256((size_t)R * words * 4) * 2;
 }
 
 TopkWorkspace topk_carve(void* ws, int64_t R, int64_t stride) {
@@ -271,6 +332,7 @@ TopkWorkspace topk_carve(void* ws, int64_t R, int64_t stride) {
     char* p = static_cast<char*>(ws);
     t.hist1 = reinterpret_cast<uint32_t*>(p); p += align256((size_t)R * kBins12 * 4);
     t.cand_n = reinterpret_cast<int*>(p); p += align256((size_t)R * 4);
+    t.thr1 = reinterpret_cast<int4*>(p); p += align256((size_t)R * 16);
     t.cand = reinterpret_cast<uint2*>(p); p += align256((size_t)R * kCap * 8);
     t.win = reinterpret_cast<uint32_t*>(p); p += align256((size_t)R * t.words * 4);
     t.tie = reinterpret_cast<uint32_t*>(p);
@@ -290,12 +352,26 @@ csahca_status topk_launch(const float* scores, int64_t stride, int R, const int6
         count_launch();
         CSAHCA_CHECK_LAUNCH();
     }
-    topk_collect_kernel<<<grid, kThreads, 0, stream>>>(scores, stride, n_vis_arr, q_pos, m, Ncap, k, tw.hist1,
-                                                       tw.cand, tw.cand_n);
+    topk_threshold_kernel<<<R, kThreads, 0, stream>>>(n_vis_arr, q_pos, m, Ncap, stride, k, tw.hist1, tw.thr1);
     count_launch();
     CSAHCA_CHECK_LAUNCH();
-    topk_finish_kernel<<<R, kFinishThreads, 0, stream>>>(scores, stride, n_vis_arr, q_pos, m, Ncap, k, tw.hist1,
-                                                         tw.cand, tw.cand_n, tw.win, tw.tie, tw.words, idx_out);
+    const dim3 cgrid((unsigned)std::max<int64_t>(1, cdiv(stride, (int64_t)kWarpSpan * (kThreads / 32))), (unsigned)R);
+    topk_collect_kernel<<<cgrid, kThreads, 0, stream>>>(scores, stride, n_vis_arr, q_pos, m, Ncap, k, tw.thr1,
+                                                        tw.cand, tw.cand_n);
+    count_launch();
+    CSAHCA_CHECK_LAUNCH();
+    static bool attr_set[64] = {false};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+        if (cudaFuncSetAttribute(topk_finish_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kFinishSmem) !=
+            cudaSuccess)
+            return CSAHCA_ERR_CUDA;
+        attr_set[dev] = true;
+    }
+    topk_finish_kernel<<<R, kFinishThreads, kFinishSmem, stream>>>(scores, stride, n_vis_arr, q_pos, m, Ncap, k,
+                                                                   tw.hist1, tw.thr1, tw.cand, tw.cand_n, tw.win,
+                                                                   tw.tie, tw.words, idx_out);
     count_launch();
     CSAHCA_CHECK_LAUNCH();
     return CSAHCA_OK;
