@@ -201,17 +201,15 @@ cudaError_t dispatch_generic(const AttendArgs& a, int S, int kps, float* o_part,
 }  // namespace
 
 SplitPlan plan_splits(int R, int64_t total_max, int splits_req) {
-    // Keys per split are a multiple of the 128-key tensor-core tile.  Automatic plan: splits of
-    // up to 4 tiles, shrunk until there are at least as many (query, split) items as SMs.
+    // Keys per split are whole 128-key tiles.  Automatic plan: as many splits per query as keep
+    // the (query, split) items within one wave of the SMs, so a persistent CTA runs one long
+    // item instead of several short ones (each item refills the load pipeline).
     SplitPlan sp;
     total_max = std::max<int64_t>(total_max, 1);
-    int64_t kps;
-    if (splits_req > 0) {
-        kps = cdiv(cdiv(total_max, splits_req), 128) * 128;
-    } else {
-        kps = 512;
-        while (kps > 128 && (int64_t)R * cdiv(total_max, kps) < num_sms()) kps /= 2;
-    }
+    const int64_t tiles = cdiv(total_max, 128);
+    int64_t s0 = splits_req > 0 ? splits_req : std::max<int64_t>(1, num_sms() / std::max(R, 1));
+    s0 = std::min(s0, tiles);
+    const int64_t kps = cdiv(tiles, s0) * 128;
     sp.kps = (int)kps;
     sp.S = (int)cdiv(total_max, kps);
     return sp;
@@ -281,13 +279,13 @@ extern "C" {
 
 size_t csa_attend_workspace(int B, int T, int H, int d, int k, int W) {
     if (B <= 0 || T <= 0 || H <= 0 || d <= 0 || k < 0 || W < 0) return 0;
-    const SplitPlan sp = plan_splits(B * T, (int64_t)k + W, 0);
+    const SplitPlan sp = plan_splits(B * T, tile_space_keys(k, W), 0);
     return attend_workspace_bytes(B * T, H, d, sp);
 }
 
 size_t hca_attend_workspace(int B, int T, int H, int d, int64_t Ncap, int W, int splits) {
     if (B <= 0 || T <= 0 || H <= 0 || d <= 0 || Ncap < 0 || W < 0) return 0;
-    const SplitPlan sp = plan_splits(B * T, Ncap + W, splits);
+    const SplitPlan sp = plan_splits(B * T, tile_space_keys(Ncap, W), splits);
     return attend_workspace_bytes(B * T, H, d, sp);
 }
 
@@ -302,7 +300,7 @@ csahca_status csa_attend(const void* q, int B, int T, int H, int d, float scale,
     a.idx = idx; a.k = k; a.m = 1; a.ring_k = ring_k; a.ring_v = ring_v; a.ring_cap = ring_cap; a.W = W;
     a.chunk_k = chunk_k; a.chunk_v = chunk_v; a.chunk_pos0 = chunk_pos0; a.chunk_stride = chunk_stride;
     a.q_pos = q_pos; a.dtype = dtype; a.out = out; a.lse = lse;
-    a.total_max = (int64_t)k + W;
+    a.total_max = tile_space_keys(k, W);
     const csahca_status v = attend_validate(a);
     if (v != CSAHCA_OK) return v;
     return attend_run(a, 0, workspace, ws_bytes, (cudaStream_t)stream);
@@ -319,7 +317,7 @@ csahca_status hca_attend(const void* q, int B, int T, int H, int d, float scale,
     a.idx = nullptr; a.k = 0; a.m = m; a.ring_k = ring_k; a.ring_v = ring_v; a.ring_cap = ring_cap; a.W = W;
     a.chunk_k = chunk_k; a.chunk_v = chunk_v; a.chunk_pos0 = chunk_pos0; a.chunk_stride = chunk_stride;
     a.q_pos = q_pos; a.dtype = dtype; a.out = out; a.lse = lse;
-    a.total_max = Ncap + W;
+    a.total_max = tile_space_keys(Ncap, W);
     if (splits < 0) return CSAHCA_ERR_INVALID_ARG;
     const csahca_status v = attend_validate(a);
     if (v != CSAHCA_OK) return v;

@@ -89,9 +89,13 @@ __device__ __forceinline__ void key_rows(const AttendArgs& a, const KeyList& kl,
     *vp = static_cast<const T*>(a.ring_v) + off;
 }
 
+// Upper bound of a query's keys in tile space (both attention paths size their split plan with
+// it): the compressed keys rounded up to whole 128-key tiles, then the window likewise.
+inline int64_t tile_space_keys(int64_t n_c_max, int64_t W) { return cdiv(n_c_max, 128) * 128 + cdiv(W, 128) * 128; }
+
 struct SplitPlan {
     int S;     // splits per query
-    int kps;   // keys per split (multiple of 32)
+    int kps;   // keys per split (multiple of 128)
 };
 SplitPlan plan_splits(int R, int64_t total_max, int splits_req);
 size_t attend_workspace_bytes(int R, int H, int d, const SplitPlan& sp);

@@ -1,99 +1,101 @@
 // Tensor-core split attention for bf16 and d = 128 (CSA: selected entries + window; HCA: every
-// visible entry + window), sm_103a tcgen05 + TMEM.
+// visible entry + window), sm_103a tcgen05 + TMEM + TMA.
 //
 // All H query heads of a query share one KV stream (honbul.tistory.com/221 "CSA"/"HCA";
 // pogovet.com detail 4), so one tile of 128 keys against all heads is a dense contraction:
 //   S^T[128 keys x H]  = K_tile[128 x 128] . Q^T          (A = K, K-major; B = Q, K-major)
 //   O^T[128 dims x H] += V_tile^T[128 x 128] . P[128 x H]  (A = V, MN-major; B = P, MN-major)
-// Keys are the M dimension, so every thread owns one key row of S^T (tcgen05.ld 32x32b) and
-// the V tile is used exactly as loaded (no transpose).  Softmax per head runs over the
-// columns: the per-tile column maximum is a warp transpose-reduction plus 4-way smem merge;
-// the running maximum is raised lazily (only when it grows by more than 2^8), and only then is
-// the O^T accumulator in TMEM rescaled.  Row sums are kept per thread and reduced once at the
-// end.  Each CTA is persistent over (query, key-split) items; K/V tiles are gathered row by
-// row with cp.async into 128-byte-swizzled shared memory, double-buffered, zero-filled for
-// empty slots.  Partial results (o normalised, lse) go to the split workspace and are merged
-// by the shared merge kernel.
+// Keys are the M dimension: a thread owns one key row of S^T (tcgen05.ld 32x32b) and the V tile
+// is used as loaded.  Two warpgroups split the heads.  Per tile, the per-head maximum over the
+// 128 keys is one warp reduction per head plus a 4-way shared-memory merge; the running maximum
+// is raised lazily (only when it grows by more than 2^8) and only then is the O^T accumulator in
+// TMEM rescaled; row sums stay per thread until the end of the work item.
+//
+// Keys are addressed in tile space: the compressed keys of a query fill tiles [0, nt_c), the
+// window fills tiles [nt_c, nt_c + nt_w).  A tile whose rows are contiguous in memory (HCA
+// entries; the decode window ring when it holds exactly 128 tokens) is fetched as two 2-D TMA
+// boxes (128-byte swizzle) by one thread; selected CSA entries and chunked-prefill windows are
+// gathered row by row with cp.async.  K and V tiles have their own two-slot rings: K(i+2) is
+// requested once MMA1(i) is done, V(i+1) once PV(i-1) is done, and MMA1(i+1) is issued before
+// the softmax of tile i, so loads, both MMAs and the softmax overlap.  Each CTA is persistent
+// over (query, key-split) items; partial results (o normalised, lse) go to the split workspace
+// and are merged by the shared merge kernel.
 #include "attend.cuh"
 #include "tc_ptx.cuh"
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <cstddef>
+#include <cstring>
+#include <mutex>
 
 namespace csahca {
 namespace {
 
 using namespace tc;
 
-constexpr int kKeys = 128;           // keys per tile (MMA M)
-constexpr int kD = 128;              // head dim
-constexpr int kStages = 2;
-constexpr uint32_t kHalf = kKeys * 128;   // one 64-column half of a [128][128] bf16 tile: 16 KB
-constexpr float kRescaleThreshold = 8.0f; // log2 units
+constexpr int kKeys = 128;                 // keys per tile (MMA M)
+constexpr int kD = 128;                    // head dim
+constexpr int kThreads = 256;              // two warpgroups
+constexpr uint32_t kHalf = kKeys * 128;    // [128 rows][64 bf16] swizzled half tile: 16 KB
+constexpr uint32_t kTile = 2 * kHalf;      // one K or V tile: 32 KB
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
 template <int H>
 struct Smem {
     static constexpr uint32_t q = 0;                                  // 2 halves x [H][128 B]
     static constexpr uint32_t q_half = H * 128;
-    static constexpr uint32_t p = 2 * q_half;                         // [128 keys][H bf16] (64-head regions)
+    static constexpr uint32_t p = 2 * q_half;                         // [128 keys][H] bf16
     static constexpr uint32_t p_region = kKeys * 128;
     static constexpr uint32_t p_bytes = ((H + 63) / 64) * p_region;
-    static constexpr uint32_t kv = (p + p_bytes + 1023) / 1024 * 1024;
-    static constexpr uint32_t stage = 4 * kHalf;                      // K halves, then V halves
-    static constexpr uint32_t total = kv + kStages * stage;
+    static constexpr uint32_t k = (p + p_bytes + 1023) / 1024 * 1024;  // two K slots
+    static constexpr uint32_t v = k + 2 * kTile;                      // two V slots
+    static constexpr uint32_t total = v + 2 * kTile;
 };
 
-struct Misc {
-    uint64_t bar_s, bar_o;
+struct alignas(16) Misc {
+    uint64_t kfull[2], vfull[2], sdone[2], odone;
     uint32_t tmem_base;
     int flag;
-    float red[4][128];
-    float mrun[128];
-    float alpha[128];
-    float linv[128];
-    const __nv_bfloat16* rowk[kStages][kKeys];
-    const __nv_bfloat16* rowv[kStages][kKeys];
-    unsigned char valid[kStages][kKeys];
+    alignas(16) float red[8][32];
+    alignas(16) float mrun[64];      // read as float4
+    alignas(16) float alpha[64];     // read as float4
+    float linv[64];
+    unsigned char valid[4][kKeys];   // per tile (ring of 4): row holds a key of this query
+};
+static_assert(offsetof(Misc, mrun) % 16 == 0 && offsetof(Misc, alpha) % 16 == 0, "float4 fields");
+
+struct Maps {
+    CUtensorMap ck, cv, rk, rv;
 };
 
-// Column (head) reduction of NV = H values per thread across the 32 lanes of a warp: after the
-// call lane l holds the result for heads [l*H/32, (l+1)*H/32) in v[0 .. H/32).
-template <int H, bool MAX>
-__device__ __forceinline__ void warp_col_reduce(float (&v)[H]) {
-    const int lane = threadIdx.x & 31;
-#pragma unroll
-    for (int off = 16, n = H; off >= 1; off >>= 1) {
-        const int half = n / 2;
-        if (half < H / 32) break;
-        const bool up = (lane & off) != 0;
-#pragma unroll
-        for (int j = 0; j < H / 2; ++j) {
-            if (j < half) {
-                const float send = up ? v[j] : v[j + half];
-                const float keep = up ? v[j + half] : v[j];
-                const float recv = __shfl_xor_sync(0xffffffffu, send, off);
-                v[j] = MAX ? fmaxf(keep, recv) : keep + recv;
-            }
-        }
-        n = half;
-    }
-}
-
 template <int H>
-__global__ void __launch_bounds__(128, 1) attend_tc_kernel(AttendArgs a, int S, int kps, float* __restrict__ o_part,
-                                                           float* __restrict__ lse_part, unsigned* err) {
+__global__ void __launch_bounds__(kThreads, 1)
+    attend_tc_kernel(AttendArgs a, int S, int kps, const __grid_constant__ Maps maps, int use_tma_c, int use_tma_w,
+                     float* __restrict__ o_part, float* __restrict__ lse_part, unsigned* err) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                          ~uintptr_t(1023));
     __shared__ Misc ms;
     using L = Smem<H>;
-    const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
-    constexpr uint32_t kCols = (2 * H <= 32) ? 32 : (2 * H <= 64 ? 64 : (2 * H <= 128 ? 128 : 256));
+    constexpr int HG = H / 2;                   // heads per warpgroup
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int wg = warp >> 2;                   // warpgroup: heads [wg*HG, wg*HG + HG)
+    const int row = tid & (kKeys - 1);          // key row of S^T / dim row of O^T = TMEM lane
+    constexpr uint32_t kCols = (3 * H <= 128) ? 128 : 256;   // S[2] + O
 
     if (warp == 0) {
         tmem_alloc(&ms.tmem_base, kCols);
         tmem_relinquish();
     }
-    if (t == 0) {
-        mbar_init(&ms.bar_s, 1);
-        mbar_init(&ms.bar_o, 1);
+    if (tid == 0) {
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&ms.kfull[i], kThreads);
+            mbar_init(&ms.vfull[i], kThreads);
+            mbar_init(&ms.sdone[i], 1);
+        }
+        mbar_init(&ms.odone, 1);
         fence_mbar_init();
         ms.flag = 0;
     }
@@ -101,208 +103,288 @@ __global__ void __launch_bounds__(128, 1) attend_tc_kernel(AttendArgs a, int S, 
     __syncthreads();
     fence_after_sync();
     const uint32_t tmem = ms.tmem_base;
-    const uint32_t t_s = tmem, t_o = tmem + H;
-    const uint32_t lane_off = (uint32_t)(32 * warp) << 16;
+    const uint32_t t_o = tmem + 2 * H;
+    const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
     const uint32_t sbase = smem_u32(sm);
-    uint32_t ph_s = 0, ph_o = 0;
-    const float c_log2 = a.scale * 1.4426950408889634f;
-    const uint64_t pol_stream = l2_policy_evict_first();     // K/V rows are read once per step
+    const float c_log2 = a.scale * 1.4426950408889634f;      // scale > 0 (checked on the host)
     const uint32_t id_qk = idesc_f16(128, H, 1, 0, 0);
     const uint32_t id_pv = idesc_f16(128, H, 1, 1, 1);
+    const uint64_t pol_stream = l2_policy_evict_first();     // K/V rows are read once per step
+    uint32_t g = 0;                                          // tiles processed so far by this CTA
 
     const int R = a.B * a.T;
     const int items = R * S;
+    const int tps = kps / kKeys;
     for (int item = blockIdx.x; item < items; item += gridDim.x) {
         const int r = item / S, split = item % S;
         const int b = r / a.T;
         const int64_t p = a.q_pos[r];
         const KeyList kl = key_list(a, r, b, p);
-        const int64_t k0 = (int64_t)split * kps;
-        const int64_t k1 = kl.total < k0 + kps ? kl.total : k0 + kps;
-        const int ntiles = k1 > k0 ? (int)((k1 - k0 + kKeys - 1) / kKeys) : 0;
+        const int nt_c = (int)cdiv(kl.n_c, kKeys);
+        const int nt_w = (int)cdiv(a.W, kKeys);
+        const int t0 = split * tps;
+        const int t1 = min(nt_c + nt_w, t0 + tps);
+        const int nt = t1 > t0 ? t1 - t0 : 0;
         const int64_t obase = ((int64_t)r * S + split) * H;
-
-        if (t < H) ms.mrun[t] = -INFINITY;
-        // queue Q (row r) for this item, 16-byte chunks into the swizzled K-major layout
         const __nv_bfloat16* qr = static_cast<const __nv_bfloat16*>(a.q) + (int64_t)r * H * kD;
-        for (int c = t; c < H * 16; c += 128) {
+
+        if (nt == 0) {
+            for (int i = tid; i < H * kD; i += kThreads) o_part[obase * kD + i] = 0.0f;
+            if (tid < H) lse_part[obase + tid] = -INFINITY;
+            continue;
+        }
+        if (tid < H) ms.mrun[tid] = -INFINITY;
+
+        // K (is_v = false) or V of item tile i into its ring slot; called by all threads.  Tile
+        // i's loads are the (g + i)-th of each ring, so slot = (g + i) & 1.
+        auto load_tile = [&](int i, bool is_v) {
+            const int ti = t0 + i;
+            const uint32_t seq = g + (uint32_t)i;
+            uint64_t* bar = is_v ? &ms.vfull[seq & 1] : &ms.kfull[seq & 1];
+            const uint32_t dst = sbase + (is_v ? L::v : L::k) + (seq & 1) * kTile;
+            const bool comp = ti < nt_c;
+            if (comp ? use_tma_c : use_tma_w) {
+                if (!is_v && tid < kKeys) {
+                    bool valid;
+                    if (comp) {
+                        valid = (int64_t)ti * kKeys + tid < kl.n_c;
+                    } else {   // ring slot `tid` holds the token t = tid (mod 128) of the last 128
+                        const int64_t back = ((p - tid) % kKeys + kKeys) % kKeys;
+                        valid = p - back >= 0;
+                    }
+                    ms.valid[seq & 3][tid] = valid;
+                }
+                if (tid == 0) {
+                    mbar_expect_tx(bar, kTile);
+                    const CUtensorMap* mp = comp ? (is_v ? &maps.cv : &maps.ck) : (is_v ? &maps.rv : &maps.rk);
+                    const int y = comp ? (int)((int64_t)b * a.Ncap + (int64_t)ti * kKeys) : b * a.ring_cap;
+                    tma_load_2d(dst, mp, 0, y, bar, pol_stream);
+                    tma_load_2d(dst + kHalf, mp, 64, y, bar, pol_stream);
+                }
+            } else {   // two threads per row, one 64-column half each
+                const int rr = tid >> 1, half = tid & 1;
+                int64_t key;
+                bool in;
+                if (comp) {
+                    key = (int64_t)ti * kKeys + rr;
+                    in = key < kl.n_c;
+                } else {
+                    key = kl.n_c + (int64_t)(ti - nt_c) * kKeys + rr;
+                    in = key < kl.total;
+                }
+                const __nv_bfloat16* kp = nullptr;
+                const __nv_bfloat16* vp = nullptr;
+                if (in) key_rows<__nv_bfloat16>(a, kl, r, b, p, key, &kp, &vp, err);
+                if (!is_v && half == 0) ms.valid[seq & 3][rr] = kp != nullptr;
+                const __nv_bfloat16* src = is_v ? vp : kp;
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    const uint32_t d = dst + half * kHalf + sw128(rr, c);
+                    if (src) cp_async16_hint(d, src + half * 64 + c * 8, 16, pol_stream);
+                    else cp_async16(d, qr, 0);                   // zero fill (no bytes read)
+                }
+            }
+            cp_async_arrive_noinc(bar);
+        };
+
+        // thread 0: S^T(i) = K(i) . Q^T into S buffer (g + i) & 1
+        auto issue_qk = [&](int i) {
+            const uint32_t seq = g + (uint32_t)i;
+            mbar_wait(&ms.kfull[seq & 1], (seq >> 1) & 1, err);
+            fence_proxy_async();
+            fence_after_sync();
+            const uint32_t kb = sbase + L::k + (seq & 1) * kTile;
+            const uint32_t sb = tmem + (seq & 1) * H;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const uint64_t ad = smem_desc(kb + (j >> 2) * kHalf + (j & 3) * 32, 16, 1024);
+                const uint64_t bd = smem_desc(sbase + L::q + (j >> 2) * L::q_half + (j & 3) * 32, 16, 1024);
+                mma_ss(sb, ad, bd, id_qk, j > 0);
+            }
+            mma_commit(&ms.sdone[seq & 1]);
+        };
+
+        // ---- prologue: Q, K(0), K(1), V(0) in flight; MMA1(0)
+        for (int c = tid; c < H * 16; c += kThreads) {
             const int h = c >> 4, cc = c & 15;
             cp_async16(sbase + L::q + (cc >> 3) * L::q_half + sw128(h, cc & 7), qr + h * kD + cc * 8, 16);
         }
+        load_tile(0, false);
+        if (nt > 1) load_tile(1, false);
+        load_tile(0, true);
+        if (tid == 0) issue_qk(0);
+        __syncthreads();                               // valid[] of tiles 0 and 1
 
-        // gathers tile `tile` of this item into stage `st`
-        auto issue_tile = [&](int tile, int st) {
-            const int64_t key = k0 + (int64_t)tile * kKeys + t;
-            const __nv_bfloat16* kp = nullptr;
-            const __nv_bfloat16* vp = nullptr;
-            if (key < k1) key_rows<__nv_bfloat16>(a, kl, r, b, p, key, &kp, &vp, err);
-            ms.rowk[st][t] = kp;
-            ms.rowv[st][t] = vp;
-            ms.valid[st][t] = kp != nullptr;
-            __syncthreads();
-            const uint32_t stb = sbase + L::kv + st * L::stage;
-            for (int row = warp; row < kKeys; row += 4) {
-                const __nv_bfloat16* src = (lane < 16) ? ms.rowk[st][row] : ms.rowv[st][row];
-                const int cc = lane & 15;
-                const uint32_t dst = stb + (lane < 16 ? 0 : 2 * kHalf) + (cc >> 3) * kHalf + sw128(row, cc & 7);
-                if (src) cp_async16_hint(dst, src + cc * 8, 16, pol_stream);
-                else cp_async16(dst, qr, 0);                 // zero fill (no bytes read)
-            }
-        };
-
-        float lsum[H];
+        float lsum[HG];
 #pragma unroll
-        for (int h = 0; h < H; ++h) lsum[h] = 0.0f;
+        for (int h = 0; h < HG; ++h) lsum[h] = 0.0f;
 
-        if (ntiles > 0) issue_tile(0, 0);
-        cp_async_commit();
-
-        for (int i = 0; i < ntiles; ++i) {
-            const int st = i % kStages;
-            if (i > 0) {                                     // PV(i-1) done: frees P, O and stage st^1
-                mbar_wait(&ms.bar_o, ph_o, err);
-                ph_o ^= 1;
-                fence_after_sync();
-            }
-            if (i + 1 < ntiles) issue_tile(i + 1, (i + 1) % kStages);
-            cp_async_commit();
-            cp_async_wait<1>();
-            fence_proxy_async();
-            __syncthreads();
-            // ---- S^T = K . Q^T
-            if (t == 0) {
-                fence_after_sync();
-                const uint32_t kb = sbase + L::kv + st * L::stage;
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const uint64_t ad = smem_desc(kb + (j >> 2) * kHalf + (j & 3) * 32, 16, 1024);
-                    const uint64_t bd = smem_desc(sbase + L::q + (j >> 2) * L::q_half + (j & 3) * 32, 16, 1024);
-                    mma_ss(t_s, ad, bd, id_qk, j > 0);
-                }
-                mma_commit(&ms.bar_s);
-            }
-            mbar_wait(&ms.bar_s, ph_s, err);
-            ph_s ^= 1;
+        for (int i = 0; i < nt; ++i) {
+            const uint32_t seq = g + (uint32_t)i;
+            const int ti = t0 + i;
+            if (tid == 0 && i + 1 < nt) issue_qk(i + 1);
+            mbar_wait(&ms.sdone[seq & 1], (seq >> 1) & 1, err);
             fence_after_sync();
-            const bool valid = ms.valid[st][t] != 0;
-            // ---- column maxima (the S tile stays in TMEM and is read again below)
-            {
-                float v[H];
+            // ---- S(i) of this warpgroup's heads -> registers (raw scores; invalid rows -inf)
+            const bool valid = ms.valid[seq & 3][row] != 0;
+            float v[HG];
 #pragma unroll
-                for (int c0 = 0; c0 < H; c0 += 16) {
-                    uint32_t rr[16];
-                    tmem_ld16(t_s + lane_off + c0, rr);
-                    tmem_wait_ld();
+            for (int c0 = 0; c0 < HG; c0 += 16) {
+                uint32_t rr[16];
+                tmem_ld16(tmem + (seq & 1) * H + wg * HG + c0 + lane_off, rr);
+                tmem_wait_ld();
 #pragma unroll
-                    for (int k = 0; k < 16; ++k) v[c0 + k] = valid ? __uint_as_float(rr[k]) * c_log2 : -INFINITY;
-                }
-                warp_col_reduce<H, true>(v);
-#pragma unroll
-                for (int j = 0; j < H / 32; ++j) ms.red[warp][lane * (H / 32) + j] = v[j];
+                for (int k = 0; k < 16; ++k) v[c0 + k] = valid ? __uint_as_float(rr[k]) : -INFINITY;
             }
+            // K slot of tile i is free (MMA1(i) complete)
+            if (i + 2 < nt) load_tile(i + 2, false);
+            // ---- per-warp maximum of each head over its 32 keys; lane h keeps head h
+            float mine = -INFINITY;
+#pragma unroll
+            for (int h = 0; h < HG; ++h) {
+                const float mx = redux_max_f32(v[h]);
+                mine = (lane == h) ? mx : mine;
+            }
+            ms.red[warp][lane] = mine;
+            fence_before_sync();
             __syncthreads();
-            if (t < H) {
-                const float tmax = fmaxf(fmaxf(ms.red[0][t], ms.red[1][t]), fmaxf(ms.red[2][t], ms.red[3][t]));
-                const float mo = ms.mrun[t];
+            if (tid < H) {
+                const int gq = tid / HG, hh = tid % HG;
+                const float traw = fmaxf(fmaxf(ms.red[4 * gq][hh], ms.red[4 * gq + 1][hh]),
+                                         fmaxf(ms.red[4 * gq + 2][hh], ms.red[4 * gq + 3][hh]));
+                const float tmax = traw * c_log2;
+                const float mo = ms.mrun[tid];
                 float al = 1.0f;
                 if (tmax > mo + kRescaleThreshold || (mo == -INFINITY && tmax != -INFINITY)) {
-                    al = (mo == -INFINITY) ? 0.0f : exp2f(mo - tmax);
-                    ms.mrun[t] = tmax;
+                    al = (mo == -INFINITY) ? 0.0f : ex2_approx(mo - tmax);
+                    ms.mrun[tid] = tmax;
                     ms.flag = 1;
                 }
-                ms.alpha[t] = al;
+                ms.alpha[tid] = al;
             }
             __syncthreads();
             const bool rescale = ms.flag != 0;
-            // ---- P = exp2(s - m), row sums, P tile (MN-major: [key][head]), 16 heads at a time
+            // ---- P = 2^(s c - m) for this warpgroup's heads, row sums
+            uint32_t pk[HG / 2];
 #pragma unroll
-            for (int c0 = 0; c0 < H; c0 += 16) {
-                uint32_t rr[16];
-                tmem_ld16(t_s + lane_off + c0, rr);
-                tmem_wait_ld();
-                uint32_t pk[8];
+            for (int h = 0; h < HG; h += 4) {
+                const float4 m4 = *reinterpret_cast<const float4*>(&ms.mrun[wg * HG + h]);
+                const float mm[4] = {m4.x, m4.y, m4.z, m4.w};
+                float pp[4];
 #pragma unroll
-                for (int k = 0; k < 16; k += 2) {
-                    const int h = c0 + k;
-                    const float s0 = valid ? __uint_as_float(rr[k]) * c_log2 : -INFINITY;
-                    const float s1 = valid ? __uint_as_float(rr[k + 1]) * c_log2 : -INFINITY;
-                    const float m0 = ms.mrun[h], m1 = ms.mrun[h + 1];
-                    const float p0 = (m0 == -INFINITY) ? 0.0f : exp2f(s0 - m0);
-                    const float p1 = (m1 == -INFINITY) ? 0.0f : exp2f(s1 - m1);
-                    lsum[h] = lsum[h] * ms.alpha[h] + p0;
-                    lsum[h + 1] = lsum[h + 1] * ms.alpha[h + 1] + p1;
-                    pk[k / 2] = pack_bf16x2(p0, p1);
+                for (int u = 0; u < 4; ++u)
+                    pp[u] = (mm[u] == -INFINITY) ? 0.0f : ex2_approx(fmaf(v[h + u], c_log2, -mm[u]));
+                if (rescale) {
+                    const float4 a4 = *reinterpret_cast<const float4*>(&ms.alpha[wg * HG + h]);
+                    lsum[h] = fmaf(lsum[h], a4.x, pp[0]);
+                    lsum[h + 1] = fmaf(lsum[h + 1], a4.y, pp[1]);
+                    lsum[h + 2] = fmaf(lsum[h + 2], a4.z, pp[2]);
+                    lsum[h + 3] = fmaf(lsum[h + 3], a4.w, pp[3]);
+                } else {
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) lsum[h + u] += pp[u];
                 }
+                pk[h / 2] = pack_bf16x2(pp[0], pp[1]);
+                pk[h / 2 + 1] = pack_bf16x2(pp[2], pp[3]);
+            }
+            // ---- PV(i-1) done: P, O and the V slot of tile i-1 are free
+            if (i > 0) {
+                mbar_wait(&ms.odone, (seq - 1) & 1, err);
+                fence_after_sync();
+            }
+            if (i + 1 < nt) load_tile(i + 1, true);
 #pragma unroll
-                for (int c = 0; c < 2; ++c) {
-                    const int chunk = c0 / 8 + c;
-                    const uint32_t dst = sbase + L::p + (chunk >> 3) * L::p_region + sw128(t, chunk & 7);
-                    asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(dst), "r"(pk[4 * c]),
-                                 "r"(pk[4 * c + 1]), "r"(pk[4 * c + 2]), "r"(pk[4 * c + 3])
-                                 : "memory");
-                }
+            for (int c = 0; c < HG / 8; ++c) {
+                const int chunk = wg * (HG / 8) + c;          // 8 heads per 16-byte chunk
+                const uint32_t dst = sbase + L::p + (chunk >> 3) * L::p_region + sw128(row, chunk & 7);
+                asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(dst), "r"(pk[4 * c]), "r"(pk[4 * c + 1]),
+                             "r"(pk[4 * c + 2]), "r"(pk[4 * c + 3])
+                             : "memory");
             }
             // ---- rescale the O^T accumulator (lane = dim) when some running maximum moved
             if (rescale && i > 0) {
 #pragma unroll
-                for (int c0 = 0; c0 < H; c0 += 16) {
+                for (int c0 = 0; c0 < HG; c0 += 16) {
                     uint32_t rr[16];
-                    tmem_ld16(t_o + lane_off + c0, rr);
+                    const uint32_t oa = t_o + wg * HG + c0 + lane_off;
+                    tmem_ld16(oa, rr);
                     tmem_wait_ld();
 #pragma unroll
-                    for (int k = 0; k < 16; ++k) rr[k] = __float_as_uint(__uint_as_float(rr[k]) * ms.alpha[c0 + k]);
-                    tmem_st16(t_o + lane_off + c0, rr);
+                    for (int k = 0; k < 16; ++k)
+                        rr[k] = __float_as_uint(__uint_as_float(rr[k]) * ms.alpha[wg * HG + c0 + k]);
+                    tmem_st16(oa, rr);
                 }
                 tmem_wait_st();
+            }
+            // ---- a TMA tile may hold rows that are not keys of this query (entries not yet
+            // visible, the next sequence, ring slots before token 0): zero their V rows, since
+            // P = 0 does not cancel a non-finite value.
+            const bool comp = ti < nt_c;
+            const bool vzero = comp ? (use_tma_c && (int64_t)(ti + 1) * kKeys > kl.n_c)
+                                    : (use_tma_w && p < kKeys - 1);
+            if (vzero) {
+                mbar_wait(&ms.vfull[seq & 1], (seq >> 1) & 1, err);
+                if (tid < kKeys && !valid) {
+                    const uint32_t vrow = sbase + L::v + (seq & 1) * kTile + row * 128;
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        asm volatile("st.shared.v4.b32 [%0], {%1,%1,%1,%1};" ::"r"(vrow + c * 16), "r"(0u) : "memory");
+                        asm volatile("st.shared.v4.b32 [%0], {%1,%1,%1,%1};" ::"r"(vrow + kHalf + c * 16), "r"(0u)
+                                     : "memory");
+                    }
+                }
             }
             fence_proxy_async();
             fence_before_sync();
             __syncthreads();
-            if (t == 0) ms.flag = 0;
-            // ---- O^T += V^T . P
-            if (t == 0) {
+            if (tid == 0) {
+                ms.flag = 0;
+                // ---- O^T += V^T . P
+                mbar_wait(&ms.vfull[seq & 1], (seq >> 1) & 1, err);
+                fence_proxy_async();
                 fence_after_sync();
-                const uint32_t vb = sbase + L::kv + st * L::stage + 2 * kHalf;
+                const uint32_t vb = sbase + L::v + (seq & 1) * kTile;
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
                     const uint64_t ad = smem_desc(vb + j * 2048, kHalf, 1024);
                     const uint64_t bd = smem_desc(sbase + L::p + j * 2048, L::p_region, 1024);
                     mma_ss(t_o, ad, bd, id_pv, (i > 0 || j > 0) ? 1u : 0u);
                 }
-                mma_commit(&ms.bar_o);
+                mma_commit(&ms.odone);
             }
         }
-        if (ntiles > 0) {
-            mbar_wait(&ms.bar_o, ph_o, err);
-            ph_o ^= 1;
-            fence_after_sync();
-        }
-        cp_async_wait<0>();
+        mbar_wait(&ms.odone, (g + (uint32_t)nt - 1) & 1, err);
+        fence_after_sync();
+        g += (uint32_t)nt;
         // ---- row sums across the 128 keys, partial lse, normalised partial output
-        warp_col_reduce<H, false>(lsum);
+        float mine = 0.0f;
 #pragma unroll
-        for (int j = 0; j < H / 32; ++j) ms.red[warp][lane * (H / 32) + j] = lsum[j];
+        for (int h = 0; h < HG; ++h) {
+            const float s = warp_sum(lsum[h]);
+            mine = (lane == h) ? s : mine;
+        }
+        ms.red[warp][lane] = mine;
         __syncthreads();
-        if (t < H) {
-            const float l = ms.red[0][t] + ms.red[1][t] + ms.red[2][t] + ms.red[3][t];
-            const float m = ms.mrun[t];
+        if (tid < H) {
+            const int gq = tid / HG, hh = tid % HG;
+            const float l = ms.red[4 * gq][hh] + ms.red[4 * gq + 1][hh] + ms.red[4 * gq + 2][hh] +
+                            ms.red[4 * gq + 3][hh];
+            const float m = ms.mrun[tid];
             const bool any = (l > 0.0f) && (m != -INFINITY);
-            ms.linv[t] = any ? 1.0f / l : 0.0f;
-            lse_part[obase + t] = any ? (m + log2f(l)) * 0.6931471805599453f : -INFINITY;
+            ms.linv[tid] = any ? 1.0f / l : 0.0f;
+            lse_part[obase + tid] = any ? (m + log2f(l)) * 0.6931471805599453f : -INFINITY;
         }
         __syncthreads();
-        if (ntiles > 0) {
 #pragma unroll
-            for (int c0 = 0; c0 < H; c0 += 16) {
-                uint32_t rr[16];
-                tmem_ld16(t_o + lane_off + c0, rr);
-                tmem_wait_ld();
+        for (int c0 = 0; c0 < HG; c0 += 16) {
+            uint32_t rr[16];
+            tmem_ld16(t_o + wg * HG + c0 + lane_off, rr);
+            tmem_wait_ld();
 #pragma unroll
-                for (int k = 0; k < 16; ++k)
-                    o_part[(obase + c0 + k) * kD + t] = __uint_as_float(rr[k]) * ms.linv[c0 + k];
+            for (int k = 0; k < 16; ++k) {
+                const int h = wg * HG + c0 + k;
+                o_part[(obase + h) * kD + row] = __uint_as_float(rr[k]) * ms.linv[h];
             }
-        } else {
-            for (int h = 0; h < H; ++h) o_part[(obase + h) * kD + t] = 0.0f;
         }
         fence_before_sync();
         __syncthreads();
@@ -311,23 +393,65 @@ __global__ void __launch_bounds__(128, 1) attend_tc_kernel(AttendArgs a, int S, 
     if (warp == 0) tmem_dealloc(tmem, kCols);
 }
 
+// --------------------------------------------------------------------------- host side
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    });
+    return fn;
+}
+
+// Tensor map over `rows` rows of 128 bf16 (256-byte pitch): box of 64 columns x 128 rows,
+// 128-byte swizzle (the layout of the MMA operands), zero fill past the last row.  False when
+// the map cannot be made; the caller then gathers rows instead.
+bool encode_rows(CUtensorMap* m, const void* base, int64_t rows) {
+    PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+    if (!fn || rows < kKeys || rows + kKeys >= ((int64_t)1 << 31) || !aligned(base, 16)) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)kD, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)kD * 2};
+    const cuuint32_t box[2] = {64, (cuuint32_t)kKeys};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <int H>
 cudaError_t launch_tc(const AttendArgs& a, int S, int kps, float* o_part, float* lse_part, unsigned* err,
                       cudaStream_t st) {
+    Maps maps;
+    std::memset(&maps, 0, sizeof maps);
+    int use_c = 0, use_w = 0;
+    // HCA entries of a sequence are contiguous; CSA entries are gathered through the index list.
+    if (!a.is_csa && encode_rows(&maps.ck, a.ck, (int64_t)a.B * a.Ncap) &&
+        encode_rows(&maps.cv, a.cv, (int64_t)a.B * a.Ncap))
+        use_c = 1;
+    // The decode window is the whole ring when it holds exactly one tile of tokens.
+    if (a.chunk_k == nullptr && a.W == kKeys && a.ring_cap == kKeys && a.ring_k != nullptr &&
+        encode_rows(&maps.rk, a.ring_k, (int64_t)a.B * a.ring_cap) &&
+        encode_rows(&maps.rv, a.ring_v, (int64_t)a.B * a.ring_cap))
+        use_w = 1;
     const size_t smem = Smem<H>::total + 1024;
     auto kern = attend_tc_kernel<H>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const int items = a.B * a.T * S;
     const int grid = items < num_sms() ? items : num_sms();
-    kern<<<grid, 128, smem, st>>>(a, S, kps, o_part, lse_part, err);
+    kern<<<grid, kThreads, smem, st>>>(a, S, kps, maps, use_c, use_w, o_part, lse_part, err);
     return cudaGetLastError();
 }
 
 }  // namespace
 
 bool attend_tc_supported(const AttendArgs& a) {
-    return a.dtype == CSAHCA_BF16 && a.d == 128 && (a.H == 32 || a.H == 64);
+    return a.dtype == CSAHCA_BF16 && a.d == 128 && (a.H == 32 || a.H == 64) && a.scale > 0.0f;
 }
 
 cudaError_t attend_tc_launch(const AttendArgs& a, int S, int kps, float* o_part, float* lse_part, unsigned* err,

@@ -63,7 +63,7 @@ csahca_status hca_attend_noalloc(const void* q, int B, int T, int H, int d, floa
     a.idx = nullptr; a.k = 0; a.m = m; a.ring_k = ring_k; a.ring_v = ring_v; a.ring_cap = ring_cap; a.W = W;
     a.chunk_k = chunk_k; a.chunk_v = chunk_v; a.chunk_pos0 = chunk_pos0; a.chunk_stride = chunk_stride;
     a.q_pos = q_pos; a.dtype = dtype; a.out = out; a.lse = lse;
-    a.total_max = Ncap + W;
+    a.total_max = tile_space_keys(Ncap, W);
     if (splits < 0) return CSAHCA_ERR_INVALID_ARG;
     const csahca_status v = attend_validate(a);
     if (v != CSAHCA_OK) return v;

@@ -42,7 +42,10 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsign
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
     while (!mbar_try_wait(bar, parity)) {
-        if (global_timer_ns() - t0 > limit_ns) {
+        const uint64_t dt = global_timer_ns() - t0;
+        // once some wait has given up, later waits give up after 20 ms instead of the full limit
+        if (dt > limit_ns ||
+            (dt > 20000000ull && (*reinterpret_cast<volatile unsigned*>(err) & ERRBIT_TIMEOUT))) {
             flag_error(err, ERRBIT_TIMEOUT);
             return false;
         }
@@ -228,6 +231,40 @@ __device__ __forceinline__ void cp_async16_hint(uint32_t dst, const void* src, u
 }
 __device__ __forceinline__ void st_global_hint(float* p, float v, uint64_t policy) {
     asm volatile("st.global.L2::cache_hint.f32 [%0], %1, %2;" ::"l"(p), "f"(v), "l"(policy) : "memory");
+}
+
+// Adds `bytes` to the transaction count of the current phase without arriving.
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+// One arrival on the mbarrier once every cp.async issued so far by this thread has landed (the
+// barrier's expected count must include this arrival).
+__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+// 2-D tiled TMA load of the box at element coordinates (x, y) of the tensor map `map` (a
+// __grid_constant__ kernel parameter) into shared memory, completion counted in bytes on `bar`.
+// x * element size must be a multiple of 16 bytes.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* map, int x, int y, uint64_t* bar,
+                                            uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3}], [%4], %5;"
+        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(policy)
+        : "memory");
+}
+// 2^x with the hardware approximation (flush-to-zero; 2^-inf = 0).
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+// Maximum of one float32 over the 32 lanes of a fully active warp.
+__device__ __forceinline__ float redux_max_f32(float v) {
+    float r;
+    asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
+    return r;
 }
 
 }  // namespace tc
