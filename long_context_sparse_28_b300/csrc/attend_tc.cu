@@ -23,12 +23,10 @@
 #include "attend.cuh"
 #include "tc_ptx.cuh"
 
-#include <cuda.h>
-#include <cudaTypedefs.h>
+#include "tmap.cuh"
 
 #include <cstddef>
 #include <cstring>
-#include <mutex>
 
 namespace csahca {
 namespace {
@@ -394,33 +392,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // --------------------------------------------------------------------------- host side
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void* f = nullptr;
-        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
-    });
-    return fn;
-}
-
-// Tensor map over `rows` rows of 128 bf16 (256-byte pitch): box of 64 columns x 128 rows,
-// 128-byte swizzle (the layout of the MMA operands), zero fill past the last row.  False when
-// the map cannot be made; the caller then gathers rows instead.
+// Map over `rows` rows of 128 bf16 (256-byte pitch), boxes of 64 columns x 128 rows (the layout of
+// the MMA operands).  False when the map cannot be made; the caller then gathers rows instead.
 bool encode_rows(CUtensorMap* m, const void* base, int64_t rows) {
-    PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
-    if (!fn || rows < kKeys || rows + kKeys >= ((int64_t)1 << 31) || !aligned(base, 16)) return false;
-    const cuuint64_t dims[2] = {(cuuint64_t)kD, (cuuint64_t)rows};
-    const cuuint64_t strides[1] = {(cuuint64_t)kD * 2};
-    const cuuint32_t box[2] = {64, (cuuint32_t)kKeys};
-    const cuuint32_t estr[2] = {1, 1};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    return rows > 0 && encode_tmap_2d(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, base, kD, (uint64_t)rows, kD * 2, 64, kKeys);
 }
 
 template <int H>

@@ -145,7 +145,8 @@ __device__ __forceinline__ uint32_t ordered_key(float f) {
 // --------------------------------------------------------------- internal launchers
 // Tensor-core indexer scores (low-precision keys, bf16 queries, d_I = 64, Ncap % 8 == 0).
 bool index_tc_supported(int q_dtype, int key_fmt, int H_I, int d_I, int64_t Ncap, const void* k_codes,
-                        const void* k_scale, int64_t R);
+                        const void* k_scale, int B, int64_t R);
+// cudaErrorNotSupported when the key tensor map cannot be built (the caller takes the generic path).
 // hist1 (nullable): [B*T][4096] histogram of the top 12 bits of each visible score's ordered key.
 cudaError_t index_tc_launch(const void* q_idx, const float* w, const void* k_codes, const void* k_scale, int key_fmt,
                             int B, int T, int H_I, const int64_t* q_pos, int64_t Ncap, int m, float* S,

@@ -143,14 +143,16 @@ static csahca_status index_scores_launch(const void* q_idx, csahca_dtype q_dtype
                                          float* S, uint32_t* hist1, bool* hist_done, cudaStream_t st) {
     const int R = B * T;
     if (hist_done) *hist_done = false;
-    if (index_tc_supported(q_dtype, key_fmt, H_I, d_I, Ncap, k_codes, k_scale, R)) {
+    if (index_tc_supported(q_dtype, key_fmt, H_I, d_I, Ncap, k_codes, k_scale, B, R)) {
         unsigned* err = err_word();
         if (!err) return CSAHCA_ERR_CUDA;
         const cudaError_t e = index_tc_launch(q_idx, w, k_codes, k_scale, key_fmt, B, T, H_I, q_pos, Ncap, m, S,
                                               hist1, err, st);
-        count_launch();
-        if (hist_done) *hist_done = hist1 != nullptr;
-        return e == cudaSuccess ? CSAHCA_OK : CSAHCA_ERR_CUDA;
+        if (e != cudaErrorNotSupported) {
+            count_launch();
+            if (hist_done) *hist_done = hist1 != nullptr;
+            return e == cudaSuccess ? CSAHCA_OK : CSAHCA_ERR_CUDA;
+        }
     }
     dim3 grid((unsigned)cdiv(Ncap, 256), (unsigned)R);
     const size_t smem = (size_t)(H_I * d_I + H_I) * 4;

@@ -1,354 +1,464 @@
-// Tensor-core lightning-indexer scores for low-precision keys (e4m3 + row scale, e2m1 + UE8M0
-// per 32 values), d_I = 64, one query row per item (decode).
+// Tensor-core lightning-indexer scores for low-precision keys (e2m1 + UE8M0 per 32 values,
+// e4m3 + fp32 row scale), d_I = 64, any number of query rows.
 //
 // I(t,s) = sum_h w[t,h] * ReLU(q[t,h] . khat_s)  (honbul.tistory.com/221 "CSA"; pogovet.com
 // DeepSeek-V4 article, detail 4 (FP4 lightning indexer) and detail 5).
 //
-// Per 128-key tile:  D[128 keys x H_I] = A[128 keys x 64] . Q^T  on tcgen05 (kind::f16):
-//   * key codes stream through shared memory with 1-D bulk async copies (an NS-stage ring fed by
-//     one producer thread, mbarrier transaction counts);
-//   * each thread owns one key row: it decodes its 64 codes exactly to f16 with the hardware
-//     e4m3/e2m1 -> f16x2 conversions (every code value is a small integer times a power of two)
-//     and writes the row into TMEM, where it is the MMA's A operand (no shared-memory round trip);
-//   * the query row is the B operand in shared memory (K-major, 128-byte swizzle): bf16 queries
-//     are scaled per head by a power of two 2^e_h into f16 range, exactly; the factor 2^-e_h is
-//     folded into the head weight w';
-//   * the per-row (e4m3) or per-32 (e2m1, two accumulators) key scales are applied to the fp32
-//     accumulators in the epilogue: score = sum_h w'_h ReLU(sum_blocks s_block D_block[h]).
-// The MMA of tile g overlaps the epilogue of tile g-1 (two A and two D buffers in TMEM).
-// CTAs are persistent over (row, chunk of 8 tiles) items and keep the copy ring running
-// across items.  Only the rounding of the fp32 accumulation differs from exact arithmetic.
+// The key codes are never decoded on the CUDA cores: the 5th-generation tensor core multiplies
+// them as they are stored (tcgen05.mma kind::f8f6f4, A = e2m1 or e4m3 codes).  A stage holds 256
+// keys of one query row: one 2-D TMA box of 128 rows x 128 codes, each row two consecutive keys
+// (packed e2m1 codes are expanded by the TMA into the 16-byte-per-16-codes shared-memory form the
+// MMA reads; e4m3 codes are copied as bytes), 128-byte swizzle.  With M = 128 rows, the MMA over
+// code columns [0, 64) gives the even keys and over [64, 128) the odd keys.
+//
+// The query must be an 8-bit operand too.  Each bf16 head vector is scaled by a power of two 2^e_h
+// (largest element into [2^7, 2^8)) and split exactly as q' = hi + 2^-5 lo with hi = e4m3(q') and
+// lo = 32 (q' - hi): the remainder has at most 3 significant bits, so lo is an e4m3 value.  The
+// B operand stacks the hi rows over the lo rows (N = 2 H_I), so one MMA per 32-code block gives
+// both parts and the epilogue forms D_hi + 2^-5 D_lo.  (Elements below 2^-13 of their head's
+// largest element are the exception: lo is then rounded, an error below 2^-20 of that largest
+// element.)  2^-e_h is folded into the head weight w'.  Block scales (e2m1: one per 32 codes, so
+// two accumulators per key) or the row scale (e4m3) are applied in the epilogue, on pairs of
+// heads with f32x2 arithmetic: score = sum_h w'_h ReLU(sum_blocks s_block (D_hi + 2^-5 D_lo)[h]).
+// Apart from that the result differs from exact arithmetic only by the rounding of the fp32
+// accumulation.
+//
+// Warp roles (persistent CTAs over (row, chunk of 8 stages) work items):
+//   warp 4     producer: per work item, the q image and folded head weights of its row into one of
+//              two query slots (the next item's row is loaded one item ahead); per stage (one lane)
+//              the stage's (row, first key, visible count, flags) record, the TMA box of codes and
+//              a bulk copy of the scales;
+//   warp 5     one thread issues the MMAs of a stage into a TMEM accumulator buffer (two buffers
+//              when they fit in the 512 columns);
+//   warps 0-3  epilogue: thread j owns TMEM lane j (keys 2j and 2j+1 of the stage): scores to
+//              global memory, and the top-12-bit histogram of the scores (the top-k's first pass),
+//              accumulated per item in shared memory and added to the row's global histogram.
 #include "common.cuh"
 #include "tc_ptx.cuh"
-#include "quant.cuh"
+#include "tmap.cuh"
 
 #include <algorithm>
 #include <cstddef>
+#include <cstring>
 
 namespace csahca {
 namespace {
 
 using namespace tc;
 
-constexpr int kKeys = 128;
+constexpr int kPair = 256;            // keys per stage (128 TMA rows of two keys)
 constexpr int kDI = 64;
-constexpr int kChunkTiles = 8;
+constexpr int kChunkStages = 8;       // stages per work item: 2048 keys of one query row
+constexpr int kMaxNS = 6;             // shared-memory stages (at most)
+constexpr int kEpi = 128;             // epilogue threads (warps 0-3)
+constexpr int kThreads = kEpi + 64;   // + producer warp + MMA warp
+constexpr int kTerm = 1, kLast = 2;   // stage flags: no more work / last stage of an item
+enum : uint32_t { kE4M3 = 0, kE2M1 = 5 };   // kind::f8f6f4 operand formats
+constexpr float kLoScale = 0.03125f;         // lo rows of the query operand carry 32 x the remainder
 
-template <int FMT, int HI>
-struct IdxCfg {
-    static constexpr int row_bytes = FMT == CSAHCA_E4M3_ROWSCALE ? 64 : 32;
-    static constexpr int scale_bytes = FMT == CSAHCA_E4M3_ROWSCALE ? 4 : 2;
-    static constexpr int tile_bytes = kKeys * row_bytes;
-    static constexpr int stages = 4;
-    static constexpr int nacc = FMT == CSAHCA_E2M1_UE8M0 ? 2 : 1;
-    static constexpr uint32_t a_cols = 32;                 // 64 16-bit values per key row
-    static constexpr uint32_t d_cols = nacc * HI;
-    static constexpr uint32_t need_cols = a_cols + d_cols;
-    static constexpr uint32_t tmem_cols = need_cols <= 32 ? 32 : need_cols <= 64 ? 64 : need_cols <= 128 ? 128
-                                        : need_cols <= 256 ? 256 : 512;
-    static constexpr int tmem_ctas = 512 / tmem_cols;
-    // shared memory: code stages | scale stages | q buffers (2 x HI rows x 128 B)
-    static constexpr uint32_t off_scale = stages * tile_bytes;
-    static constexpr uint32_t off_q = (off_scale + stages * kKeys * scale_bytes + 1023) / 1024 * 1024;
-    static constexpr uint32_t q_buf = HI * 128;
-    static constexpr uint32_t total = off_q + 2 * q_buf;
-};
-
-struct IdxMisc {
-    alignas(16) float wq[2][64];        // read as float4
-    alignas(16) uint32_t hist[4096];    // top-12-bit histogram of the current item's scores (fused top-k pass)
-    unsigned amax[2][64];
-    uint64_t full[4];
-    uint64_t mma_done;
+struct alignas(16) IdxMisc {
+    uint32_t hist[2048];                  // top-12-bit histogram of the item's scores: bin b is the
+                                          // 16-bit half (b & 1) of word b >> 1 (<= 2048 per item)
+    uint64_t full[kMaxNS], empty[kMaxNS], dfull[2], dfree[2], qfree[2];
     uint32_t tmem_base;
 };
-static_assert(offsetof(IdxMisc, wq) % 16 == 0, "wq is read with 16-byte loads");
-
-struct Tile {          // one 128-key tile of one query row
-    int item;
-    int r;
-    int64_t s0;        // first key of the tile
-    int64_t n;         // visible keys of the row
-};
-
-// Walks this CTA's items (row r = item % R, chunk c = item / R) tile by tile, skipping empty ones.
-struct Cursor {
-    int item, items, stride, R;
-    int64_t Ncap;
-    int m;
-    const int64_t* q_pos;
-    Tile cur;
-    int64_t s_end;
-    bool valid;
-
-    __device__ void start(int first, int nitems, int step, int rows, int64_t ncap, int mm, const int64_t* qp) {
-        item = first - step;
-        items = nitems;
-        stride = step;
-        R = rows;
-        Ncap = ncap;
-        m = mm;
-        q_pos = qp;
-        valid = true;
-        next_item();
-    }
-    __device__ void next_item() {
-        for (;;) {
-            item += stride;
-            if (item >= items) {
-                valid = false;
-                return;
-            }
-            const int r = item % R, c = item / R;
-            const int64_t p = q_pos[r];
-            int64_t n = (p >= 0) ? (p + 1) / m : 0;
-            n = n < Ncap ? n : Ncap;
-            const int64_t s0 = (int64_t)c * kChunkTiles * kKeys;
-            if (s0 < n) {
-                cur.item = item;
-                cur.r = r;
-                cur.s0 = s0;
-                cur.n = n;
-                const int64_t e = s0 + (int64_t)kChunkTiles * kKeys;
-                s_end = e < n ? e : n;
-                return;
-            }
-        }
-    }
-    __device__ void advance() {
-        cur.s0 += kKeys;
-        if (cur.s0 >= s_end) next_item();
-    }
-};
 
 template <int FMT, int HI>
-__global__ void __launch_bounds__(128) index_tc_kernel(const __nv_bfloat16* __restrict__ q_idx,
-                                                       const float* __restrict__ w,
-                                                       const uint8_t* __restrict__ k_codes,
-                                                       const uint8_t* __restrict__ k_scale, int T,
-                                                       const int64_t* __restrict__ q_pos, int64_t Ncap, int m,
-                                                       int R, float* __restrict__ S, uint32_t* __restrict__ hist1,
-                                                       unsigned* err) {
-    using C = IdxCfg<FMT, HI>;
+struct Cfg {
+    static constexpr bool fp4 = FMT == CSAHCA_E2M1_UE8M0;
+    static constexpr int nacc = fp4 ? 2 : 1;                         // accumulators per key
+    static constexpr uint32_t code_tx = fp4 ? kPair * 32 : kPair * 64;  // global code bytes per stage
+    static constexpr int scale_bytes = fp4 ? 2 : 4;                  // per key
+    // stage: codes (128 rows x 128 B, swizzled) | scales | record
+    static constexpr uint32_t off_scale = 16384;
+    static constexpr uint32_t off_meta = off_scale + kPair * 4;
+    static constexpr uint32_t stage = (off_meta + 16 + 1023) / 1024 * 1024;
+    // query slot (one per work item, two in flight): q image (2 HI rows x 128 B: hi rows, then
+    // lo rows, codes in the first 64 bytes) | w'
+    static constexpr uint32_t q_img = 2 * HI * 128;
+    static constexpr uint32_t q_slot = (q_img + HI * 4 + 1023) / 1024 * 1024;
+    // as many stages as leave room for two CTAs per SM (228 KB, 1 KB reserved per CTA, 1 KB
+    // alignment slack, the static shared memory)
+    static constexpr int ns_fit = (int)((114 * 1024 - 1024 - 1024 - sizeof(IdxMisc) - 2 * q_slot) / stage);
+    static constexpr int NS = ns_fit < 3 ? 3 : (ns_fit > kMaxNS ? kMaxNS : ns_fit);
+    static constexpr uint32_t off_qslots = NS * stage;
+    static constexpr uint32_t smem = off_qslots + 2 * q_slot;
+    static constexpr uint32_t acc_cols = 2 * HI;                     // one accumulator: hi | lo columns
+    static constexpr uint32_t d_cols = 2 * nacc * acc_cols;          // even + odd keys
+    static constexpr int nbuf = 2 * d_cols <= 512 ? 2 : 1;           // accumulator buffers
+    static constexpr uint32_t tmem_cols = nbuf * d_cols;
+    static_assert(tmem_cols >= 32 && tmem_cols <= 512 && (tmem_cols & (tmem_cols - 1)) == 0, "TMEM columns");
+    static_assert(HI % 16 == 0 && HI <= 64, "heads");
+    // the next item's query row is loaded one item ahead when its share fits in a few registers
+    static constexpr bool prefetch_q = HI <= 16;
+};
+
+
+// One lane's share of the q image of a row: unit (head h, half hf) = lane + 32 j covers 32
+// elements of head h and yields two 16-byte chunks of hi codes and two of lo codes (lo = 32 x the
+// remainder, e4m3); returns the folded weight w'_h in wq[j].  `raw` holds the unit's 32 values.
+template <int HI>
+__device__ __forceinline__ void make_q_image(const uint4 (&raw)[2 * HI / 32][4], const float* __restrict__ w_row,
+                                             int lane, uint4 (&img)[2 * HI / 32][4], float (&wq)[2 * HI / 32]) {
+    constexpr int kUnits = 2 * HI / 32;
+#pragma unroll
+    for (int j = 0; j < kUnits; ++j) {
+        const int h = (lane + 32 * j) >> 1;
+        float x[32];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            const uint32_t wd[4] = {raw[j][c].x, raw[j][c].y, raw[j][c].z, raw[j][c].w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                x[8 * c + 2 * i] = __uint_as_float(wd[i] << 16);
+                x[8 * c + 2 * i + 1] = __uint_as_float(wd[i] & 0xFFFF0000u);
+            }
+        }
+        float amax = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(x[i]));
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));   // other half of head h
+        int ex = 0;
+        if (amax > 0.0f) {
+            frexpf(amax, &ex);                  // amax in [2^(ex-1), 2^ex)
+            ex = 8 - ex;                        // amax * 2^ex in [2^7, 2^8)
+        }
+        uint32_t hw[8], lw[8];
+#pragma unroll
+        for (int i = 0; i < 32; i += 4) {
+            float y[4], hv[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) y[k] = ldexpf(x[i + k], ex);
+            const uint32_t h01 = cvt_e4m3x2(y[0], y[1]), h23 = cvt_e4m3x2(y[2], y[3]);
+            e4m3x2_to_f32(h01, hv[0], hv[1]);
+            e4m3x2_to_f32(h23, hv[2], hv[3]);
+            const uint32_t l01 = cvt_e4m3x2(32.0f * (y[0] - hv[0]), 32.0f * (y[1] - hv[1]));
+            const uint32_t l23 = cvt_e4m3x2(32.0f * (y[2] - hv[2]), 32.0f * (y[3] - hv[3]));
+            hw[i / 4] = h01 | (h23 << 16);
+            lw[i / 4] = l01 | (l23 << 16);
+        }
+        img[j][0] = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+        img[j][1] = make_uint4(hw[4], hw[5], hw[6], hw[7]);
+        img[j][2] = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+        img[j][3] = make_uint4(lw[4], lw[5], lw[6], lw[7]);
+        wq[j] = ldexpf(w_row[h], -ex);
+    }
+}
+
+template <int HI>
+__device__ __forceinline__ void load_q_raw(const __nv_bfloat16* __restrict__ q_row, int lane,
+                                           uint4 (&raw)[2 * HI / 32][4]) {
+#pragma unroll
+    for (int j = 0; j < 2 * HI / 32; ++j) {
+        const int unit = lane + 32 * j;
+        const uint4* src = reinterpret_cast<const uint4*>(q_row + (unit >> 1) * kDI + (unit & 1) * 32);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) raw[j][c] = __ldg(src + c);
+    }
+}
+
+template <int FMT, int HI>
+__global__ void __launch_bounds__(kThreads) index_tc_kernel(const __grid_constant__ CUtensorMap kmap,
+                                                            const __nv_bfloat16* __restrict__ q_idx,
+                                                            const float* __restrict__ w,
+                                                            const uint8_t* __restrict__ k_scale, int T,
+                                                            const int64_t* __restrict__ q_pos, int64_t Ncap, int m,
+                                                            int R, float* __restrict__ S,
+                                                            uint32_t* __restrict__ hist1, unsigned* err) {
+    using C = Cfg<FMT, HI>;
+    constexpr int kUnits = 2 * HI / 32;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                          ~uintptr_t(1023));
     __shared__ IdxMisc ms;
-    const int t = threadIdx.x, warp = t >> 5;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t sbase = smem_u32(sm);
 
     if (warp == 0) {
         tmem_alloc(&ms.tmem_base, C::tmem_cols);
         tmem_relinquish();
     }
-    if (t == 0) {
-        for (int s = 0; s < C::stages; ++s) mbar_init(&ms.full[s], 1);
-        mbar_init(&ms.mma_done, 1);
+    if (tid == 0) {
+        for (int s = 0; s < C::NS; ++s) {
+            mbar_init(&ms.full[s], 1);
+            mbar_init(&ms.empty[s], 5);       // MMA commit + 4 epilogue warps
+        }
+        for (int d = 0; d < 2; ++d) {
+            mbar_init(&ms.dfull[d], 1);
+            mbar_init(&ms.dfree[d], 4);
+            mbar_init(&ms.qfree[d], 5);       // MMA commit + 4 epilogue warps, once per item
+        }
         fence_mbar_init();
     }
-    for (int i = t; i < 4096; i += 128) ms.hist[i] = 0u;
+    if (tid < kEpi)
+        for (int i = tid; i < 2048; i += kEpi) ms.hist[i] = 0u;
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
     const uint32_t tmem = ms.tmem_base;
-    const uint32_t lane_off = (uint32_t)(32 * warp) << 16;
-    const int items = R * (int)cdiv(Ncap, (int64_t)kChunkTiles * kKeys);
+    const int items = R * (int)cdiv(Ncap, (int64_t)kChunkStages * kPair);
 
-    // key codes are read once per step: keep them from evicting the scores the top-k re-reads
-    const uint64_t pol_stream = l2_policy_evict_first();
-    const uint64_t pol_keep = l2_policy_evict_last();
-    // producer (thread 0): issues the bulk copies of tile `pt` into stage pg % NS
-    Cursor prod;
-    int64_t pg = 0;
-    auto produce = [&]() {
-        const int st = (int)(pg % C::stages);
-        const Tile& x = prod.cur;
-        const int b = x.r / T;
-        const int64_t rows = (x.n - x.s0) < kKeys ? (x.n - x.s0) : kKeys;
-        const int64_t srows = ((rows + 7) / 8) * 8;                 // stays within Ncap (Ncap % 8 == 0)
-        const int64_t row0 = (int64_t)b * Ncap + x.s0;
-        const uint32_t cb = (uint32_t)(rows * C::row_bytes);
-        const uint32_t sb = (uint32_t)(srows * C::scale_bytes);
-        mbar_arrive_expect_tx(&ms.full[st], cb + sb);
-        bulk_g2s_hint(sbase + st * C::tile_bytes, k_codes + row0 * C::row_bytes, cb, &ms.full[st], pol_stream);
-        bulk_g2s_hint(sbase + C::off_scale + st * kKeys * C::scale_bytes, k_scale + row0 * C::scale_bytes, sb,
-                      &ms.full[st], pol_stream);
-        ++pg;
-        prod.advance();
-    };
-    if (t == 0) {
-        prod.start(blockIdx.x, items, gridDim.x, R, Ncap, m, q_pos);
-        for (int i = 0; i < C::stages && prod.valid; ++i) produce();
-    }
-
-    Cursor cons;
-    cons.start(blockIdx.x, items, gridDim.x, R, Ncap, m, q_pos);
-    int64_t g = 0;
-    int qrow = -1, qbuf = 1;
-    int cur_item = -1, cur_r = 0;
-    uint32_t ph_mma = 0;
-    const uint32_t id = idesc_f16(128, HI, 0, 0, 0);
-    const uint32_t abuf = tmem;
-    const uint32_t dbuf = tmem + C::a_cols;
-
-    // adds the item's smem histogram to the row's global one and clears it
-    auto flush_hist = [&](int r) {
-        __syncthreads();
-        uint32_t* gh = hist1 + (int64_t)r * 4096;
-        for (int i = t; i < 4096; i += 128) {
-            const uint32_t v = ms.hist[i];
-            if (v) {
-                atomicAdd(&gh[i], v);
-                ms.hist[i] = 0u;
+    if (warp == 4) {
+        // ======================================================================== producer
+        const uint64_t pol_stream = l2_policy_evict_first();     // codes are read once per step
+        // candidate item, one ahead: its q_pos and (small HI) its query row are loaded early
+        int c_item = (int)blockIdx.x;
+        int64_t c_p = 0;
+        uint4 c_raw[kUnits][4];
+        auto prefetch = [&](int it) {
+            c_item = it;
+            if (it < items) {
+                const int rr = it % R;
+                c_p = q_pos[rr];
+                if (C::prefetch_q) load_q_raw<HI>(q_idx + (int64_t)rr * HI * kDI, lane, c_raw);
             }
-        }
-        __syncthreads();
-    };
-
-    while (cons.valid) {
-        const Tile x = cons.cur;
-        const int st = (int)(g % C::stages);
-        if (hist1 != nullptr && x.item != cur_item && cur_item >= 0) flush_hist(cur_r);
-        cur_item = x.item;
-        cur_r = x.r;
-        // ---- query row for this tile (B operand, f16 scaled per head; w' = w * 2^-e)
-        if (x.r != qrow) {
-            qrow = x.r;
-            qbuf ^= 1;
-            if (t < HI) ms.amax[qbuf][t] = 0u;
-            __syncthreads();
-            const __nv_bfloat16* qr = q_idx + (int64_t)qrow * HI * kDI;
-            for (int c = t; c < HI * 8; c += 128) {                 // 8 chunks of 8 values per head
-                const uint4 u = __ldg(reinterpret_cast<const uint4*>(qr) + c);
-                const uint32_t wds[4] = {u.x, u.y, u.z, u.w};
-                float amax = 0.0f;
+        };
+        prefetch(c_item);
+        uint32_t u = 0;                       // stages issued
+        for (uint32_t it = 0;; ++it) {
+            // next non-empty item
+            int r = 0;
+            int64_t n = 0, s0 = 0, s_end = 0;
+            uint4 raw[kUnits][4];
+            bool found = false;
+            while (c_item < items) {
+                const int item = c_item;
+                const int64_t p = c_p;
+                r = item % R;
+                if (C::prefetch_q) {
 #pragma unroll
-                for (int i = 0; i < 4; ++i)
-                    amax = fmaxf(amax, fmaxf(fabsf(__uint_as_float(wds[i] << 16)),
-                                             fabsf(__uint_as_float(wds[i] & 0xFFFF0000u))));
-                atomicMax(&ms.amax[qbuf][c >> 3], __float_as_uint(amax));
+                    for (int j = 0; j < kUnits; ++j)
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) raw[j][c] = c_raw[j][c];
+                }
+                prefetch(item + (int)gridDim.x);
+                int64_t nn = (p >= 0) ? (p + 1) / m : 0;
+                nn = nn < Ncap ? nn : Ncap;
+                s0 = (int64_t)(item / R) * kChunkStages * kPair;
+                if (s0 < nn) {
+                    n = nn;
+                    const int64_t e = s0 + (int64_t)kChunkStages * kPair;
+                    s_end = e < nn ? e : nn;
+                    found = true;
+                    break;
+                }
             }
-            __syncthreads();
-            for (int c = t; c < HI * 8; c += 128) {
-                const int h = c >> 3;
-                const float amax = __uint_as_float(ms.amax[qbuf][h]);
-                int ex = 0;
-                if (amax > 0.0f) {
-                    frexpf(amax, &ex);                              // amax in [2^(ex-1), 2^ex)
-                    ex = 15 - ex;                                   // amax * 2^e in [2^14, 2^15)
-                }
-                const uint4 u = __ldg(reinterpret_cast<const uint4*>(qr) + c);
-                const uint32_t wds[4] = {u.x, u.y, u.z, u.w};
-                uint32_t o[4];
+            if (!found) break;
+            // query slot of this item: free once the MMAs and epilogue of item it-2 are done
+            const uint32_t qs = it & 1;
+            if (it >= 2) mbar_wait(&ms.qfree[qs], ((it >> 1) + 1) & 1, err);
+            if (!C::prefetch_q) load_q_raw<HI>(q_idx + (int64_t)r * HI * kDI, lane, raw);
+            uint4 img[kUnits][4];
+            float wq[kUnits];
+            make_q_image<HI>(raw, w + (int64_t)r * HI, lane, img, wq);
+            unsigned char* qsl = sm + C::off_qslots + qs * C::q_slot;
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const float lo = ldexpf(__uint_as_float(wds[i] << 16), ex);
-                    const float hi = ldexpf(__uint_as_float(wds[i] & 0xFFFF0000u), ex);
-                    __half2 hh = __floats2half2_rn(lo, hi);
-                    o[i] = *reinterpret_cast<uint32_t*>(&hh);
-                }
-                const uint32_t dst = sbase + C::off_q + qbuf * C::q_buf + sw128(h, c & 7);
-                asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(dst), "r"(o[0]), "r"(o[1]), "r"(o[2]),
-                             "r"(o[3])
-                             : "memory");
-                if ((c & 7) == 0) ms.wq[qbuf][h] = ldexpf(w[(int64_t)qrow * HI + h], -ex);
+            for (int j = 0; j < kUnits; ++j) {
+                const int unit = lane + 32 * j, h = unit >> 1, hf = unit & 1;
+#pragma unroll
+                for (int c = 0; c < 4; ++c)                       // hi: row h, lo: row HI + h
+                    *reinterpret_cast<uint4*>(qsl + sw128(h + (c >> 1) * HI, 2 * hf + (c & 1))) = img[j][c];
+                if (hf == 0) reinterpret_cast<float*>(qsl + C::q_img)[h] = wq[j];
             }
             fence_proxy_async();
-        }
-        // ---- this thread's key row -> f16 -> TMEM (A operand)
-        mbar_wait(&ms.full[st], (uint32_t)((g / C::stages) & 1), err);
-        uint32_t a[32];
-        const unsigned char* row = sm + st * C::tile_bytes + t * C::row_bytes;
-        float sc0, sc1 = 0.0f;
-        if (FMT == CSAHCA_E2M1_UE8M0) {
-            const uint4 u0 = *reinterpret_cast<const uint4*>(row);
-            const uint4 u1 = *reinterpret_cast<const uint4*>(row + 16);
-            const uint32_t wds[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                uint32_t o[4];
-                cvt_e2m1x8_f16(wds[i], o);
-                a[4 * i] = o[0]; a[4 * i + 1] = o[1]; a[4 * i + 2] = o[2]; a[4 * i + 3] = o[3];
-            }
-            const uint32_t e2 = *reinterpret_cast<const uint16_t*>(sm + C::off_scale + st * kKeys * 2 + t * 2);
-            sc0 = ue8m0_value(e2 & 0xFFu);
-            sc1 = ue8m0_value(e2 >> 8);
-        } else {
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                const uint4 u = *reinterpret_cast<const uint4*>(row + 16 * c);
-                const uint32_t wds[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    uint32_t o[2];
-                    cvt_e4m3x4_f16(wds[i], o);
-                    a[8 * c + 2 * i] = o[0];
-                    a[8 * c + 2 * i + 1] = o[1];
+            __syncwarp();
+            // stages of the item (one lane)
+            if (lane == 0) {
+                const int b = r / T;
+                for (; s0 < s_end; s0 += kPair, ++u) {
+                    const uint32_t s = u % C::NS;
+                    if (u >= (uint32_t)C::NS) mbar_wait(&ms.empty[s], ((u / C::NS) + 1) & 1, err);
+                    unsigned char* st = sm + s * C::stage;
+                    const uint32_t sb = sbase + s * C::stage;
+                    const int flags = ((s0 + kPair >= s_end) ? kLast : 0) | (int)(qs << 8);
+                    *reinterpret_cast<int4*>(st + C::off_meta) = make_int4(r, (int)s0, (int)n, flags);
+                    const int64_t key0 = (int64_t)b * Ncap + s0;
+                    const int64_t nk = (Ncap - s0) < kPair ? (Ncap - s0) : kPair;   // Ncap % 8 == 0
+                    const uint32_t sbytes = (uint32_t)nk * C::scale_bytes;
+                    mbar_arrive_expect_tx(&ms.full[s], C::code_tx + sbytes);
+                    tma_load_2d(sb, &kmap, 0, (int)(key0 / 2), &ms.full[s], pol_stream);
+                    bulk_g2s_hint(sb + C::off_scale, k_scale + key0 * C::scale_bytes, sbytes, &ms.full[s],
+                                  pol_stream);
                 }
             }
-            sc0 = *reinterpret_cast<const float*>(sm + C::off_scale + st * kKeys * 4 + t * 4);
+            u = __shfl_sync(0xffffffffu, u, 0);
         }
-        tmem_st32(abuf + lane_off, a);
-        tmem_wait_st();
-        fence_before_sync();
-        __syncthreads();                         // stage st consumed, A written, q ready, D read
-        if (t == 0) {
-            if (prod.valid) produce();           // refill stage st with the tile NS steps ahead
+        if (lane == 0) {                      // end of work
+            const uint32_t s = u % C::NS;
+            if (u >= (uint32_t)C::NS) mbar_wait(&ms.empty[s], ((u / C::NS) + 1) & 1, err);
+            *reinterpret_cast<int4*>(sm + s * C::stage + C::off_meta) = make_int4(0, 0, 0, kTerm);
+            mbar_arrive(&ms.full[s]);
+        }
+        __syncwarp();
+    } else if (warp == 5) {
+        // ============================================================================= MMA
+        if (lane == 0) {
+            constexpr uint32_t af = C::fp4 ? kE2M1 : kE4M3;
+            const uint32_t id = idesc_f8f6f4(128, 2 * HI, af, kE4M3);
+            // descriptors of stage 0 and query slot 0; other addresses add (offset >> 4)
+            const uint64_t a_desc0 = smem_desc(sbase, 16, 1024);
+            const uint64_t b_desc0 = smem_desc(sbase + C::off_qslots, 16, 1024);
+            for (uint32_t u = 0;; ++u) {
+                const uint32_t s = u % C::NS;
+                mbar_wait(&ms.full[s], (u / C::NS) & 1, err);
+                const int4 meta = *reinterpret_cast<const int4*>(sm + s * C::stage + C::off_meta);
+                if (meta.w & kTerm) break;
+                const uint32_t d = u % C::nbuf, qs = (uint32_t)(meta.w >> 8) & 1u;
+                if (u >= (uint32_t)C::nbuf) mbar_wait(&ms.dfree[d], ((u / C::nbuf) + 1) & 1, err);
+                fence_after_sync();
+                const uint64_t ad0 = a_desc0 + ((s * C::stage) >> 4);
+                const uint64_t bd0 = b_desc0 + ((qs * C::q_slot) >> 4);
+                const uint32_t dbuf = tmem + d * C::d_cols;
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {            // even keys: code columns [0,64); odd: [64,128)
+#pragma unroll
+                    for (int blk = 0; blk < 2; ++blk) {  // 32-code blocks (one MMA K step each)
+                        const uint32_t dst = dbuf + (C::fp4 ? 2 * e + blk : e) * C::acc_cols;
+                        const uint64_t ad = ad0 + (uint64_t)(e * 4 + blk * 2);
+                        mma_f8f6f4(dst, ad, bd0 + (uint64_t)(blk * 2), id, C::fp4 ? 0u : (uint32_t)(blk > 0));
+                    }
+                }
+                mma_commit(&ms.dfull[d]);
+                mma_commit(&ms.empty[s]);
+                if (meta.w & kLast) mma_commit(&ms.qfree[qs]);
+            }
+        }
+        __syncwarp();
+    } else {
+        // ======================================================================== epilogue
+        const uint64_t pol_keep = l2_policy_evict_last();       // the top-k re-reads the scores
+        const uint32_t lane_off = (uint32_t)(32 * warp) << 16;
+        for (uint32_t u = 0;; ++u) {
+            const uint32_t s = u % C::NS;
+            mbar_wait(&ms.full[s], (u / C::NS) & 1, err);
+            const unsigned char* st = sm + s * C::stage;
+            const int4 meta = *reinterpret_cast<const int4*>(st + C::off_meta);
+            if (meta.w & kTerm) break;
+            const uint32_t d = u % C::nbuf, qs = (uint32_t)(meta.w >> 8) & 1u;
+            mbar_wait(&ms.dfull[d], (u / C::nbuf) & 1, err);
             fence_after_sync();
-            const uint32_t qb = sbase + C::off_q + qbuf * C::q_buf;
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const uint64_t bd = smem_desc(qb + j * 32, 16, 1024);
-                const uint32_t dst = (C::nacc == 2 && j >= 2) ? dbuf + HI : dbuf;
-                const uint32_t acc = (C::nacc == 2) ? (uint32_t)(j & 1) : (uint32_t)(j > 0);
-                mma_ts(dst, abuf + j * 8, bd, id, acc);
-            }
-            mma_commit(&ms.mma_done);
-        }
-        // ---- epilogue: score = sum_h w'_h ReLU(scaled accumulators)
-        mbar_wait(&ms.mma_done, ph_mma, err);
-        ph_mma ^= 1;
-        fence_after_sync();
-        float score = 0.0f;
-        const float4* wq4 = reinterpret_cast<const float4*>(ms.wq[qbuf]);
-#pragma unroll
-        for (int c0 = 0; c0 < HI; c0 += 16) {
-            uint32_t r0[16];
-            tmem_ld16(dbuf + lane_off + c0, r0);
-            float wv[16];
-#pragma unroll
-            for (int k4 = 0; k4 < 4; ++k4) {
-                const float4 q4 = wq4[c0 / 4 + k4];
-                wv[4 * k4] = q4.x; wv[4 * k4 + 1] = q4.y; wv[4 * k4 + 2] = q4.z; wv[4 * k4 + 3] = q4.w;
-            }
-            if (C::nacc == 2) {
-                uint32_t r1[16];
-                tmem_ld16(dbuf + lane_off + HI + c0, r1);
-                tmem_wait_ld();
-#pragma unroll
-                for (int k = 0; k < 16; ++k) {
-                    const float v = fmaf(sc0, __uint_as_float(r0[k]), sc1 * __uint_as_float(r1[k]));
-                    score = fmaf(wv[k], fmaxf(v, 0.0f), score);
-                }
+            float se0, se1 = 0.0f, so0, so1 = 0.0f;             // scales of keys 2j (e) and 2j+1 (o)
+            if (C::fp4) {
+                const uint32_t b4 = *reinterpret_cast<const uint32_t*>(st + C::off_scale + 4 * tid);
+                se0 = ue8m0_value(b4 & 0xFFu);
+                se1 = ue8m0_value((b4 >> 8) & 0xFFu);
+                so0 = ue8m0_value((b4 >> 16) & 0xFFu);
+                so1 = ue8m0_value(b4 >> 24);
             } else {
-                tmem_wait_ld();
+                const float2 f2 = *reinterpret_cast<const float2*>(st + C::off_scale + 8 * tid);
+                se0 = f2.x;
+                so0 = f2.y;
+            }
+            // the stage's record and scales are in registers: release it (with the MMA commit)
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ms.empty[s]);
+            const float4* wq4 = reinterpret_cast<const float4*>(sm + C::off_qslots + qs * C::q_slot + C::q_img);
+            const uint32_t dbuf = tmem + d * C::d_cols + lane_off;
+            // per key: pairs of heads (h, h+1) in f32x2 lanes; the fp4 block scales and the lo
+            // factor 2^-5 are broadcast pairs
+            uint64_t acc2[2] = {f2_pack(0.0f, 0.0f), f2_pack(0.0f, 0.0f)};
 #pragma unroll
-                for (int k = 0; k < 16; ++k) score = fmaf(wv[k], fmaxf(__uint_as_float(r0[k]), 0.0f), score);
+            for (int key = 0; key < 2; ++key) {
+                const float s0 = key ? so0 : se0, s1 = key ? so1 : se1;
+                const uint64_t S0 = f2_pack(s0, s0), S0l = f2_pack(s0 * kLoScale, s0 * kLoScale);
+                const uint64_t S1 = f2_pack(s1, s1), S1l = f2_pack(s1 * kLoScale, s1 * kLoScale);
+                const uint64_t Ll = f2_pack(kLoScale, kLoScale);
+                const uint32_t abase = dbuf + key * C::nacc * C::acc_cols;
+#pragma unroll
+                for (int c0 = 0; c0 < HI; c0 += 16) {
+                    uint64_t wv[8];
+#pragma unroll
+                    for (int k4 = 0; k4 < 4; ++k4) {
+                        const float4 q4 = wq4[c0 / 4 + k4];
+                        wv[2 * k4] = f2_pack(q4.x, q4.y);
+                        wv[2 * k4 + 1] = f2_pack(q4.z, q4.w);
+                    }
+                    uint32_t h0[16], l0[16];
+                    tmem_ld16(abase + c0, h0);
+                    tmem_ld16(abase + HI + c0, l0);
+                    if (C::fp4) {
+                        uint32_t h1[16], l1[16];
+                        tmem_ld16(abase + C::acc_cols + c0, h1);
+                        tmem_ld16(abase + C::acc_cols + HI + c0, l1);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int k = 0; k < 16; k += 2) {
+                            uint64_t v = f2_mul(S0l, f2_pack(__uint_as_float(l0[k]), __uint_as_float(l0[k + 1])));
+                            v = f2_fma(S0, f2_pack(__uint_as_float(h0[k]), __uint_as_float(h0[k + 1])), v);
+                            v = f2_fma(S1l, f2_pack(__uint_as_float(l1[k]), __uint_as_float(l1[k + 1])), v);
+                            v = f2_fma(S1, f2_pack(__uint_as_float(h1[k]), __uint_as_float(h1[k + 1])), v);
+                            float a0, a1;
+                            f2_unpack(v, a0, a1);
+                            acc2[key] = f2_fma(wv[k / 2], f2_pack(fmaxf(a0, 0.0f), fmaxf(a1, 0.0f)), acc2[key]);
+                        }
+                    } else {
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int k = 0; k < 16; k += 2) {
+                            const uint64_t v = f2_fma(Ll, f2_pack(__uint_as_float(l0[k]), __uint_as_float(l0[k + 1])),
+                                                      f2_pack(__uint_as_float(h0[k]), __uint_as_float(h0[k + 1])));
+                            float a0, a1;
+                            f2_unpack(v, a0, a1);
+                            acc2[key] = f2_fma(wv[k / 2], f2_pack(fmaxf(a0, 0.0f), fmaxf(a1, 0.0f)), acc2[key]);
+                        }
+                    }
+                }
+            }
+            float acc_e, acc_o;
+            {
+                float x0, x1;
+                f2_unpack(acc2[0], x0, x1);
+                acc_e = x0 + x1;
+                f2_unpack(acc2[1], x0, x1);
+                acc_o = x0 + x1;
+            }
+            if (!C::fp4) {
+                acc_e *= se0;
+                acc_o *= so0;
+            }
+            // accumulators and (at the item's end) query slot consumed
+            fence_before_sync();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(&ms.dfree[d]);
+                if (meta.w & kLast) mbar_arrive(&ms.qfree[qs]);
+            }
+            const int64_t key = (int64_t)meta.y + 2 * tid;
+            const bool v0 = key < meta.z, v1 = key + 1 < meta.z;
+            float* dst = S + (int64_t)meta.x * Ncap + key;
+            if (v1) st_global_v2_hint(dst, acc_e, acc_o, pol_keep);
+            else if (v0) st_global_hint(dst, acc_e, pol_keep);
+            if (hist1 != nullptr) {
+                if (v0) {
+                    const uint32_t bin = ordered_key(acc_e) >> 20;
+                    atomicAdd(&ms.hist[bin >> 1], 1u << ((bin & 1) * 16));
+                }
+                if (v1) {
+                    const uint32_t bin = ordered_key(acc_o) >> 20;
+                    atomicAdd(&ms.hist[bin >> 1], 1u << ((bin & 1) * 16));
+                }
+                if (meta.w & kLast) {                     // item done: add to the row's histogram
+                    named_barrier_sync(1, kEpi);
+                    uint32_t* gh = hist1 + (int64_t)meta.x * 4096;
+                    for (int i = 4 * tid; i < 2048; i += 4 * kEpi) {   // words of two 16-bit counts
+                        const uint4 v = *reinterpret_cast<const uint4*>(&ms.hist[i]);
+                        if (v.x | v.y | v.z | v.w) {
+                            const uint32_t wd[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                            for (int k = 0; k < 4; ++k) {
+                                if (wd[k] & 0xFFFFu) atomicAdd(&gh[2 * (i + k)], wd[k] & 0xFFFFu);
+                                if (wd[k] >> 16) atomicAdd(&gh[2 * (i + k) + 1], wd[k] >> 16);
+                            }
+                            *reinterpret_cast<uint4*>(&ms.hist[i]) = make_uint4(0u, 0u, 0u, 0u);
+                        }
+                    }
+                    named_barrier_sync(1, kEpi);
+                }
             }
         }
-        if (C::nacc == 1) score *= sc0;
-        const int64_t s = x.s0 + t;
-        if (s < x.n) st_global_hint(S + (int64_t)x.r * Ncap + s, score, pol_keep);
-        if (hist1 != nullptr) {                        // warp-aggregated histogram update
-            const uint32_t bin = (s < x.n) ? (ordered_key(score) >> 20) : 0xFFFFFFFFu;
-            const uint32_t peers = __match_any_sync(0xffffffffu, bin);
-            if (bin != 0xFFFFFFFFu && (t & 31) == __ffs(peers) - 1) atomicAdd(&ms.hist[bin], (uint32_t)__popc(peers));
-        }
-        fence_before_sync();
-        ++g;
-        cons.advance();
     }
-    if (hist1 != nullptr && cur_item >= 0) flush_hist(cur_r);
+    __syncwarp();
+    fence_before_sync();
     __syncthreads();
     fence_after_sync();
     if (warp == 0) tmem_dealloc(tmem, C::tmem_cols);
@@ -358,31 +468,37 @@ template <int FMT, int HI>
 cudaError_t launch_index_tc(const void* q_idx, const float* w, const void* k_codes, const void* k_scale, int B,
                             int T, const int64_t* q_pos, int64_t Ncap, int m, float* S, uint32_t* hist1, unsigned* err,
                             cudaStream_t st) {
-    using C = IdxCfg<FMT, HI>;
-    // shared memory sized so that no more CTAs fit on an SM than TMEM can hold
-    const size_t per_cta = (size_t)(228 * 1024) / (C::tmem_ctas + 1) + 1024 - sizeof(IdxMisc);
-    const size_t smem = std::max<size_t>((size_t)C::total + 1024, per_cta);
-    // CTAs per SM: limited by shared memory (228 KB per SM, 1 KB reserved per CTA) and TMEM
-    const size_t per_sm_cta = smem + sizeof(IdxMisc) + 1024;
-    const int occ = std::max(1, std::min((int)((size_t)(228 * 1024) / per_sm_cta), C::tmem_ctas));
+    using C = Cfg<FMT, HI>;
+    CUtensorMap kmap;
+    std::memset(&kmap, 0, sizeof kmap);
+    const uint64_t rows = (uint64_t)B * (uint64_t)Ncap / 2;          // two keys per row of 128 codes
+    const bool ok = C::fp4 ? encode_tmap_2d(&kmap, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, k_codes, 128, rows, 64, 128,
+                                            128)
+                           : encode_tmap_2d(&kmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, k_codes, 128, rows, 128, 128, 128);
+    if (!ok) return cudaErrorNotSupported;
+    const size_t smem = (size_t)C::smem + 1024;
+    // CTAs per SM: shared memory (228 KB per SM, 1 KB reserved per CTA) and TMEM (512 columns)
+    const size_t per_cta = smem + sizeof(IdxMisc) + 1024;
+    const int occ = std::max(1, std::min((int)((size_t)(228 * 1024) / per_cta), (int)(512 / C::tmem_cols)));
     auto kern = index_tc_kernel<FMT, HI>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const int R = B * T;
-    const int64_t items = (int64_t)R * cdiv(Ncap, (int64_t)kChunkTiles * kKeys);
+    const int64_t items = (int64_t)R * cdiv(Ncap, (int64_t)kChunkStages * kPair);
     const int grid = (int)std::min<int64_t>(items, (int64_t)num_sms() * occ);
-    kern<<<grid, 128, smem, st>>>(static_cast<const __nv_bfloat16*>(q_idx), w, static_cast<const uint8_t*>(k_codes),
-                                  static_cast<const uint8_t*>(k_scale), T, q_pos, Ncap, m, R, S, hist1, err);
+    kern<<<grid, kThreads, smem, st>>>(kmap, static_cast<const __nv_bfloat16*>(q_idx), w,
+                                       static_cast<const uint8_t*>(k_scale), T, q_pos, Ncap, m, R, S, hist1, err);
     return cudaGetLastError();
 }
 
 }  // namespace
 
 bool index_tc_supported(int q_dtype, int key_fmt, int H_I, int d_I, int64_t Ncap, const void* k_codes,
-                        const void* k_scale, int64_t R) {
+                        const void* k_scale, int B, int64_t R) {
     return q_dtype == CSAHCA_BF16 && (key_fmt == CSAHCA_E4M3_ROWSCALE || key_fmt == CSAHCA_E2M1_UE8M0) &&
-           d_I == kDI && (H_I == 16 || H_I == 32 || H_I == 64) && Ncap % 8 == 0 && aligned(k_codes, 16) &&
-           aligned(k_scale, 16) && R * cdiv(Ncap, (int64_t)kChunkTiles * kKeys) < (1LL << 31);
+           d_I == kDI && (H_I == 16 || H_I == 32 || H_I == 64) && Ncap % 8 == 0 && aligned(k_codes, 32) &&
+           aligned(k_scale, 16) && (int64_t)B * Ncap / 2 >= 128 && (int64_t)B * Ncap < (1LL << 31) &&
+           R * cdiv(Ncap, (int64_t)kChunkStages * kPair) < (1LL << 31);
 }
 
 cudaError_t index_tc_launch(const void* q_idx, const float* w, const void* k_codes, const void* k_scale, int key_fmt,
