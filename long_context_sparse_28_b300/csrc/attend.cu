@@ -201,13 +201,14 @@ cudaError_t dispatch_generic(const AttendArgs& a, int S, int kps, float* o_part,
 }  // namespace
 
 SplitPlan plan_splits(int R, int64_t total_max, int splits_req) {
-    // Keys per split are whole 128-key tiles.  Automatic plan: as many splits per query as keep
-    // the (query, split) items within one wave of the SMs, so a persistent CTA runs one long
-    // item instead of several short ones (each item refills the load pipeline).
+    // Keys per split are whole 128-key tiles.  Automatic plan: about two partial results per SM
+    // over all query rows (at most 16 per row): the tensor-core kernel balances the tiles of few
+    // rows over all SMs and needs spare partial slots for that; many rows get one split each.
     SplitPlan sp;
     total_max = std::max<int64_t>(total_max, 1);
     const int64_t tiles = cdiv(total_max, 128);
-    int64_t s0 = splits_req > 0 ? splits_req : std::max<int64_t>(1, num_sms() / std::max(R, 1));
+    int64_t s0 = splits_req > 0 ? splits_req
+                                : std::min<int64_t>(16, std::max<int64_t>(1, cdiv(2 * (int64_t)num_sms(), std::max(R, 1))));
     s0 = std::min(s0, tiles);
     const int64_t kps = cdiv(tiles, s0) * 128;
     sp.kps = (int)kps;

@@ -6,7 +6,9 @@
 //   S^T[128 keys x H]  = K_tile[128 x 128] . Q^T          (A = K, K-major; B = Q, K-major)
 //   O^T[128 dims x H] += V_tile^T[128 x 128] . P[128 x H]  (A = V, MN-major; B = P, MN-major)
 // Keys are the M dimension: a thread owns one key row of S^T (tcgen05.ld 32x32b) and the V tile
-// is used as loaded.  Two warpgroups split the heads.  Per tile, the per-head maximum over the
+// is used as loaded.  Two warpgroups split the heads; a ninth warp only issues the MMAs (an MMA
+// issue costs the issuing thread on the order of a hundred cycles, so the softmax warps never
+// wait on it; they hand over through mbarriers).  Per tile, the per-head maximum over the
 // 128 keys is one warp reduction per head plus a 4-way shared-memory merge; the running maximum
 // is raised lazily (only when it grows by more than 2^8) and only then is the O^T accumulator in
 // TMEM rescaled; row sums stay per thread until the end of the work item.
@@ -16,8 +18,8 @@
 // entries; the decode window ring when it holds exactly 128 tokens) is fetched as two 2-D TMA
 // boxes (128-byte swizzle) by one thread; selected CSA entries and chunked-prefill windows are
 // gathered row by row with cp.async.  K and V tiles have their own two-slot rings: K(i+2) is
-// requested once MMA1(i) is done, V(i+1) once PV(i-1) is done, and MMA1(i+1) is issued before
-// the softmax of tile i, so loads, both MMAs and the softmax overlap.  Each CTA is persistent
+// requested once MMA1(i) is done, V(i+1) once PV(i-1) is done, and the MMA warp issues MMA1(i+2)
+// right after PV(i), so loads, both MMAs and the softmax of the next tile overlap.  Each CTA is persistent
 // over (query, key-split) items; partial results (o normalised, lse) go to the split workspace
 // and are merged by the shared merge kernel.
 #include "attend.cuh"
@@ -35,10 +37,12 @@ using namespace tc;
 
 constexpr int kKeys = 128;                 // keys per tile (MMA M)
 constexpr int kD = 128;                    // head dim
-constexpr int kThreads = 256;              // two warpgroups
+constexpr int kSoft = 256;                 // softmax / load threads: two warpgroups
+constexpr int kThreads = kSoft + 32;       // + the MMA warp
 constexpr uint32_t kHalf = kKeys * 128;    // [128 rows][64 bf16] swizzled half tile: 16 KB
 constexpr uint32_t kTile = 2 * kHalf;      // one K or V tile: 32 KB
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
+constexpr int kSchedRows = 256;            // balanced schedule for up to this many query rows
 
 template <int H>
 struct Smem {
@@ -53,16 +57,24 @@ struct Smem {
 };
 
 struct alignas(16) Misc {
-    uint64_t kfull[2], vfull[2], sdone[2], odone;
+    uint64_t kfull[2], vfull[2], sdone[2], odone, pready;
     uint32_t tmem_base;
-    int flag;
+    int flag[2];                     // per tile (ring of 2): some running maximum moved
     alignas(16) float red[8][32];
     alignas(16) float mrun[64];      // read as float4
     alignas(16) float alpha[64];     // read as float4
     float linv[64];
     unsigned char valid[4][kKeys];   // per tile (ring of 4): row holds a key of this query
+    int qoff[kSchedRows + 1];        // balanced schedule: first global tile of each query row
+    int sched_len;                   // ... and tiles per CTA
 };
 static_assert(offsetof(Misc, mrun) % 16 == 0 && offsetof(Misc, alpha) % 16 == 0, "float4 fields");
+
+struct ItemTiles {
+    int r, b, nt_c, t0, nt, slot;
+    int64_t p;
+    KeyList kl;
+};
 
 struct Maps {
     CUtensorMap ck, cv, rk, rv;
@@ -77,10 +89,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                          ~uintptr_t(1023));
     __shared__ Misc ms;
     using L = Smem<H>;
-    constexpr int HG = H / 2;                   // heads per warpgroup
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int wg = warp >> 2;                   // warpgroup: heads [wg*HG, wg*HG + HG)
-    const int row = tid & (kKeys - 1);          // key row of S^T / dim row of O^T = TMEM lane
     constexpr uint32_t kCols = (3 * H <= 128) ? 128 : 256;   // S[2] + O
 
     if (warp == 0) {
@@ -89,304 +98,424 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (tid == 0) {
         for (int i = 0; i < 2; ++i) {
-            mbar_init(&ms.kfull[i], kThreads);
-            mbar_init(&ms.vfull[i], kThreads);
+            mbar_init(&ms.kfull[i], kSoft);
+            mbar_init(&ms.vfull[i], kSoft);
             mbar_init(&ms.sdone[i], 1);
+            ms.flag[i] = 0;
         }
         mbar_init(&ms.odone, 1);
+        mbar_init(&ms.pready, kSoft / 32);
         fence_mbar_init();
-        ms.flag = 0;
+    }
+    const int R = a.B * a.T;
+    const int items = R * S;
+    const int tps = kps / kKeys;
+    const int nt_w = (int)cdiv(a.W, kKeys);
+    // Balanced schedule (few query rows, S >= 2 partial slots per row): the tiles of all rows,
+    // row after row, are cut into gridDim.x equal ranges; a CTA's range covers pieces of one or
+    // more rows, and a row's pieces go to consecutive slots of its partial results.  The range
+    // length is at least ceil(tiles of the longest row / (S - 1)), so no row has more than S
+    // pieces.  Otherwise items are (row, split) pairs, split s holding tiles [s kps, (s+1) kps).
+    const bool balanced = R <= kSchedRows && S >= 2;
+    if (balanced && warp == 0) {
+        int carry = 0, ntmax = 0;
+        for (int base = 0; base < R; base += 32) {
+            const int q = base + lane;
+            int nt = 0;
+            if (q < R) {
+                const int64_t p = a.q_pos[q];
+                nt = (int)cdiv(key_list(a, q, q / a.T, p).n_c, kKeys) + nt_w;
+            }
+            int x = nt;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, x, o);
+                if (lane >= o) x += y;
+            }
+            if (q < R) ms.qoff[q + 1] = carry + x;
+            carry += __shfl_sync(0xffffffffu, x, 31);
+            ntmax = max(ntmax, nt);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) ntmax = max(ntmax, __shfl_xor_sync(0xffffffffu, ntmax, o));
+        if (lane == 0) {
+            ms.qoff[0] = 0;
+            const int len = max((int)cdiv(carry, gridDim.x), (int)cdiv(ntmax, S - 1));
+            ms.sched_len = max(len, 1);
+        }
     }
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
     const uint32_t tmem = ms.tmem_base;
     const uint32_t t_o = tmem + 2 * H;
-    const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
     const uint32_t sbase = smem_u32(sm);
-    const float c_log2 = a.scale * 1.4426950408889634f;      // scale > 0 (checked on the host)
-    const uint32_t id_qk = idesc_f16(128, H, 1, 0, 0);
-    const uint32_t id_pv = idesc_f16(128, H, 1, 1, 1);
-    const uint64_t pol_stream = l2_policy_evict_first();     // K/V rows are read once per step
-    uint32_t g = 0;                                          // tiles processed so far by this CTA
-
-    const int R = a.B * a.T;
-    const int items = R * S;
-    const int tps = kps / kKeys;
-    for (int item = blockIdx.x; item < items; item += gridDim.x) {
-        const int r = item / S, split = item % S;
-        const int b = r / a.T;
-        const int64_t p = a.q_pos[r];
-        const KeyList kl = key_list(a, r, b, p);
-        const int nt_c = (int)cdiv(kl.n_c, kKeys);
-        const int nt_w = (int)cdiv(a.W, kKeys);
-        const int t0 = split * tps;
-        const int t1 = min(nt_c + nt_w, t0 + tps);
-        const int nt = t1 > t0 ? t1 - t0 : 0;
-        const int64_t obase = ((int64_t)r * S + split) * H;
-        const __nv_bfloat16* qr = static_cast<const __nv_bfloat16*>(a.q) + (int64_t)r * H * kD;
-
-        if (nt == 0) {
-            for (int i = tid; i < H * kD; i += kThreads) o_part[obase * kD + i] = 0.0f;
-            if (tid < H) lse_part[obase + tid] = -INFINITY;
-            continue;
+    // next work item of this CTA (cursor `cur`: an item index, or a query row when balanced);
+    // tile range [t0, t0 + nt) of the row's tile space: compressed tiles first, then the window
+    auto next_item = [&](int& cur, ItemTiles& it) -> bool {
+        if (balanced) {
+            const int len = ms.sched_len, lo = (int)blockIdx.x * len, hi = min(ms.qoff[R], lo + len);
+            for (;; ++cur) {
+                if (cur >= R) return false;
+                const int qs = ms.qoff[cur], qe = ms.qoff[cur + 1];
+                if (qs >= hi) return false;
+                if (qe <= lo || qe == qs) continue;
+                it.r = cur;
+                it.slot = (int)blockIdx.x - qs / len;
+                it.t0 = max(lo, qs) - qs;
+                it.nt = min(hi, qe) - max(lo, qs);
+                ++cur;
+                break;
+            }
+        } else {
+            if (cur >= items) return false;
+            it.r = cur / S;
+            it.slot = cur % S;
+            it.t0 = it.slot * tps;
+            cur += gridDim.x;
         }
-        if (tid < H) ms.mrun[tid] = -INFINITY;
+        it.b = it.r / a.T;
+        it.p = a.q_pos[it.r];
+        it.kl = key_list(a, it.r, it.b, it.p);
+        it.nt_c = (int)cdiv(it.kl.n_c, kKeys);
+        if (!balanced) {
+            const int t1 = min(it.nt_c + nt_w, it.t0 + tps);
+            it.nt = t1 > it.t0 ? t1 - it.t0 : 0;
+        }
+        return true;
+    };
+    const int cur0 = balanced ? 0 : (int)blockIdx.x;
 
-        // K (is_v = false) or V of item tile i into its ring slot; called by all threads.  Tile
-        // i's loads are the (g + i)-th of each ring, so slot = (g + i) & 1.
-        auto load_tile = [&](int i, bool is_v) {
-            const int ti = t0 + i;
-            const uint32_t seq = g + (uint32_t)i;
-            uint64_t* bar = is_v ? &ms.vfull[seq & 1] : &ms.kfull[seq & 1];
-            const uint32_t dst = sbase + (is_v ? L::v : L::k) + (seq & 1) * kTile;
-            const bool comp = ti < nt_c;
-            if (comp ? use_tma_c : use_tma_w) {
-                if (!is_v && tid < kKeys) {
-                    bool valid;
-                    if (comp) {
-                        valid = (int64_t)ti * kKeys + tid < kl.n_c;
-                    } else {   // ring slot `tid` holds the token t = tid (mod 128) of the last 128
-                        const int64_t back = ((p - tid) % kKeys + kKeys) % kKeys;
-                        valid = p - back >= 0;
+    if (warp == kSoft / 32) {
+        // ========================================================================= MMA warp
+        // Order per item: MMA1(0), MMA1(1), then PV(i), MMA1(i+2) for each tile i.  MMA1(i+2)
+        // overwrites the S buffer of tile i, which the softmax has read once P(i) is ready.
+        if (lane == 0) {
+            const uint32_t id_qk = idesc_f16(128, H, 1, 0, 0);
+            const uint32_t id_pv = idesc_f16(128, H, 1, 1, 1);
+            const uint64_t q_desc = smem_desc(sbase + L::q, 16, 1024);
+            const uint64_t p_desc = smem_desc(sbase + L::p, L::p_region, 1024);
+            uint32_t g = 0;
+            ItemTiles it;
+            for (int cur = cur0; next_item(cur, it);) {
+                const int nt = it.nt;
+                if (nt == 0) continue;
+                auto qk = [&](int i) {       // S^T(i) = K(i) . Q^T into S buffer (g + i) & 1
+                    const uint32_t seq = g + (uint32_t)i;
+                    mbar_wait(&ms.kfull[seq & 1], (seq >> 1) & 1, err);
+                    fence_proxy_async();
+                    fence_after_sync();
+                    const uint64_t k_desc = smem_desc(sbase + L::k + (seq & 1) * kTile, 16, 1024);
+                    const uint32_t sb = tmem + (seq & 1) * H;
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        mma_ss(sb, k_desc + (uint64_t)(((j >> 2) * kHalf + (j & 3) * 32) >> 4),
+                               q_desc + (uint64_t)(((j >> 2) * L::q_half + (j & 3) * 32) >> 4), id_qk, j > 0);
+                    mma_commit(&ms.sdone[seq & 1]);
+                };
+                qk(0);
+                if (nt > 1) qk(1);
+                for (int i = 0; i < nt; ++i) {
+                    const uint32_t seq = g + (uint32_t)i;
+                    mbar_wait(&ms.pready, seq & 1, err);
+                    mbar_wait(&ms.vfull[seq & 1], (seq >> 1) & 1, err);
+                    fence_proxy_async();
+                    fence_after_sync();
+                    // O^T += V^T . P
+                    const uint64_t v_desc = smem_desc(sbase + L::v + (seq & 1) * kTile, kHalf, 1024);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        mma_ss(t_o, v_desc + (uint64_t)((j * 2048) >> 4), p_desc + (uint64_t)((j * 2048) >> 4), id_pv,
+                               (i > 0 || j > 0) ? 1u : 0u);
+                    mma_commit(&ms.odone);
+                    if (i + 2 < nt) qk(i + 2);
+                }
+                g += (uint32_t)nt;
+            }
+        }
+        __syncwarp();
+    } else {
+        // ==================================================================== softmax warps
+        constexpr int HG = H / 2;                   // heads per warpgroup
+        const int wg = warp >> 2;                   // warpgroup: heads [wg*HG, wg*HG + HG)
+        const int row = tid & (kKeys - 1);          // key row of S^T / dim row of O^T = TMEM lane
+        const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
+        const float c_log2 = a.scale * 1.4426950408889634f;      // scale > 0 (checked on the host)
+        const uint64_t pol_stream = l2_policy_evict_first();     // K/V rows are read once per step
+        uint32_t g = 0;                                          // tiles processed so far by this CTA
+
+        if (balanced) {       // partial slots no piece of this schedule writes: lse = -inf
+            const int len = ms.sched_len;
+            for (int q = 0; q < R; ++q) {
+                const int qs = ms.qoff[q], qe = ms.qoff[q + 1];
+                int first_free;
+                if (qe == qs) {
+                    if (q % (int)gridDim.x != (int)blockIdx.x) continue;
+                    first_free = 0;
+                } else {
+                    if (qs / len != (int)blockIdx.x) continue;
+                    first_free = (qe - 1) / len - qs / len + 1;
+                }
+                for (int sl = first_free; sl < S; ++sl)
+                    if (tid < H) lse_part[((int64_t)q * S + sl) * H + tid] = -INFINITY;
+            }
+        }
+        ItemTiles it;
+        for (int cur = cur0; next_item(cur, it);) {
+            const int r = it.r, b = it.b, nt_c = it.nt_c, t0 = it.t0, nt = it.nt;
+            const int64_t p = it.p;
+            const KeyList kl = it.kl;
+            const int64_t obase = ((int64_t)r * S + it.slot) * H;
+            const __nv_bfloat16* qr = static_cast<const __nv_bfloat16*>(a.q) + (int64_t)r * H * kD;
+
+            if (nt == 0) {
+                for (int i = tid; i < H * kD; i += kSoft) o_part[obase * kD + i] = 0.0f;
+                if (tid < H) lse_part[obase + tid] = -INFINITY;
+                continue;
+            }
+            if (tid < H) ms.mrun[tid] = -INFINITY;
+
+            // K (is_v = false) or V of item tile i into its ring slot; called by all softmax
+            // threads.  Tile i's loads are the (g + i)-th of each ring, so slot = (g + i) & 1.
+            auto load_tile = [&](int i, bool is_v) {
+                const int ti = t0 + i;
+                const uint32_t seq = g + (uint32_t)i;
+                uint64_t* bar = is_v ? &ms.vfull[seq & 1] : &ms.kfull[seq & 1];
+                const uint32_t dst = sbase + (is_v ? L::v : L::k) + (seq & 1) * kTile;
+                const bool comp = ti < nt_c;
+                if (comp ? use_tma_c : use_tma_w) {
+                    if (!is_v && tid < kKeys) {
+                        bool valid;
+                        if (comp) {
+                            valid = (int64_t)ti * kKeys + tid < kl.n_c;
+                        } else {   // ring slot `tid` holds the token t = tid (mod 128) of the last 128
+                            const int64_t back = ((p - tid) % kKeys + kKeys) % kKeys;
+                            valid = p - back >= 0;
+                        }
+                        ms.valid[seq & 3][tid] = valid;
                     }
-                    ms.valid[seq & 3][tid] = valid;
-                }
-                if (tid == 0) {
-                    mbar_expect_tx(bar, kTile);
-                    const CUtensorMap* mp = comp ? (is_v ? &maps.cv : &maps.ck) : (is_v ? &maps.rv : &maps.rk);
-                    const int y = comp ? (int)((int64_t)b * a.Ncap + (int64_t)ti * kKeys) : b * a.ring_cap;
-                    tma_load_2d(dst, mp, 0, y, bar, pol_stream);
-                    tma_load_2d(dst + kHalf, mp, 64, y, bar, pol_stream);
-                }
-            } else {   // two threads per row, one 64-column half each
-                const int rr = tid >> 1, half = tid & 1;
-                int64_t key;
-                bool in;
-                if (comp) {
-                    key = (int64_t)ti * kKeys + rr;
-                    in = key < kl.n_c;
-                } else {
-                    key = kl.n_c + (int64_t)(ti - nt_c) * kKeys + rr;
-                    in = key < kl.total;
-                }
-                const __nv_bfloat16* kp = nullptr;
-                const __nv_bfloat16* vp = nullptr;
-                if (in) key_rows<__nv_bfloat16>(a, kl, r, b, p, key, &kp, &vp, err);
-                if (!is_v && half == 0) ms.valid[seq & 3][rr] = kp != nullptr;
-                const __nv_bfloat16* src = is_v ? vp : kp;
+                    if (tid == 0) {
+                        mbar_expect_tx(bar, kTile);
+                        const CUtensorMap* mp = comp ? (is_v ? &maps.cv : &maps.ck) : (is_v ? &maps.rv : &maps.rk);
+                        const int y = comp ? (int)((int64_t)b * a.Ncap + (int64_t)ti * kKeys) : b * a.ring_cap;
+                        tma_load_2d(dst, mp, 0, y, bar, pol_stream);
+                        tma_load_2d(dst + kHalf, mp, 64, y, bar, pol_stream);
+                    }
+                } else {   // two threads per row, one 64-column half each
+                    const int rr = tid >> 1, half = tid & 1;
+                    int64_t key;
+                    bool in;
+                    if (comp) {
+                        key = (int64_t)ti * kKeys + rr;
+                        in = key < kl.n_c;
+                    } else {
+                        key = kl.n_c + (int64_t)(ti - nt_c) * kKeys + rr;
+                        in = key < kl.total;
+                    }
+                    const __nv_bfloat16* kp = nullptr;
+                    const __nv_bfloat16* vp = nullptr;
+                    if (in) key_rows<__nv_bfloat16>(a, kl, r, b, p, key, &kp, &vp, err);
+                    if (!is_v && half == 0) ms.valid[seq & 3][rr] = kp != nullptr;
+                    const __nv_bfloat16* src = is_v ? vp : kp;
 #pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    const uint32_t d = dst + half * kHalf + sw128(rr, c);
-                    if (src) cp_async16_hint(d, src + half * 64 + c * 8, 16, pol_stream);
-                    else cp_async16(d, qr, 0);                   // zero fill (no bytes read)
+                    for (int c = 0; c < 8; ++c) {
+                        const uint32_t d = dst + half * kHalf + sw128(rr, c);
+                        if (src) cp_async16_hint(d, src + half * 64 + c * 8, 16, pol_stream);
+                        else cp_async16(d, qr, 0);                   // zero fill (no bytes read)
+                    }
                 }
-            }
-            cp_async_arrive_noinc(bar);
-        };
+                cp_async_arrive_noinc(bar);
+            };
 
-        // thread 0: S^T(i) = K(i) . Q^T into S buffer (g + i) & 1
-        auto issue_qk = [&](int i) {
-            const uint32_t seq = g + (uint32_t)i;
-            mbar_wait(&ms.kfull[seq & 1], (seq >> 1) & 1, err);
-            fence_proxy_async();
-            fence_after_sync();
-            const uint32_t kb = sbase + L::k + (seq & 1) * kTile;
-            const uint32_t sb = tmem + (seq & 1) * H;
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const uint64_t ad = smem_desc(kb + (j >> 2) * kHalf + (j & 3) * 32, 16, 1024);
-                const uint64_t bd = smem_desc(sbase + L::q + (j >> 2) * L::q_half + (j & 3) * 32, 16, 1024);
-                mma_ss(sb, ad, bd, id_qk, j > 0);
+            // ---- prologue: Q, K(0), K(1), V(0) in flight (Q lands before K(0) completes)
+            for (int c = tid; c < H * 16; c += kSoft) {
+                const int h = c >> 4, cc = c & 15;
+                cp_async16(sbase + L::q + (cc >> 3) * L::q_half + sw128(h, cc & 7), qr + h * kD + cc * 8, 16);
             }
-            mma_commit(&ms.sdone[seq & 1]);
-        };
+            load_tile(0, false);
+            if (nt > 1) load_tile(1, false);
+            load_tile(0, true);
+            named_barrier_sync(1, kSoft);                  // valid[] of tiles 0 and 1
 
-        // ---- prologue: Q, K(0), K(1), V(0) in flight; MMA1(0)
-        for (int c = tid; c < H * 16; c += kThreads) {
-            const int h = c >> 4, cc = c & 15;
-            cp_async16(sbase + L::q + (cc >> 3) * L::q_half + sw128(h, cc & 7), qr + h * kD + cc * 8, 16);
-        }
-        load_tile(0, false);
-        if (nt > 1) load_tile(1, false);
-        load_tile(0, true);
-        if (tid == 0) issue_qk(0);
-        __syncthreads();                               // valid[] of tiles 0 and 1
+            float lsum[HG];
+#pragma unroll
+            for (int h = 0; h < HG; ++h) lsum[h] = 0.0f;
 
-        float lsum[HG];
-#pragma unroll
-        for (int h = 0; h < HG; ++h) lsum[h] = 0.0f;
-
-        for (int i = 0; i < nt; ++i) {
-            const uint32_t seq = g + (uint32_t)i;
-            const int ti = t0 + i;
-            if (tid == 0 && i + 1 < nt) issue_qk(i + 1);
-            mbar_wait(&ms.sdone[seq & 1], (seq >> 1) & 1, err);
-            fence_after_sync();
-            // ---- S(i) of this warpgroup's heads -> registers (raw scores; invalid rows -inf)
-            const bool valid = ms.valid[seq & 3][row] != 0;
-            float v[HG];
-#pragma unroll
-            for (int c0 = 0; c0 < HG; c0 += 16) {
-                uint32_t rr[16];
-                tmem_ld16(tmem + (seq & 1) * H + wg * HG + c0 + lane_off, rr);
-                tmem_wait_ld();
-#pragma unroll
-                for (int k = 0; k < 16; ++k) v[c0 + k] = valid ? __uint_as_float(rr[k]) : -INFINITY;
-            }
-            // K slot of tile i is free (MMA1(i) complete)
-            if (i + 2 < nt) load_tile(i + 2, false);
-            // ---- per-warp maximum of each head over its 32 keys; lane h keeps head h
-            float mine = -INFINITY;
-#pragma unroll
-            for (int h = 0; h < HG; ++h) {
-                const float mx = redux_max_f32(v[h]);
-                mine = (lane == h) ? mx : mine;
-            }
-            ms.red[warp][lane] = mine;
-            fence_before_sync();
-            __syncthreads();
-            if (tid < H) {
-                const int gq = tid / HG, hh = tid % HG;
-                const float traw = fmaxf(fmaxf(ms.red[4 * gq][hh], ms.red[4 * gq + 1][hh]),
-                                         fmaxf(ms.red[4 * gq + 2][hh], ms.red[4 * gq + 3][hh]));
-                const float tmax = traw * c_log2;
-                const float mo = ms.mrun[tid];
-                float al = 1.0f;
-                if (tmax > mo + kRescaleThreshold || (mo == -INFINITY && tmax != -INFINITY)) {
-                    al = (mo == -INFINITY) ? 0.0f : ex2_approx(mo - tmax);
-                    ms.mrun[tid] = tmax;
-                    ms.flag = 1;
-                }
-                ms.alpha[tid] = al;
-            }
-            __syncthreads();
-            const bool rescale = ms.flag != 0;
-            // ---- P = 2^(s c - m) for this warpgroup's heads, row sums
-            uint32_t pk[HG / 2];
-#pragma unroll
-            for (int h = 0; h < HG; h += 4) {
-                const float4 m4 = *reinterpret_cast<const float4*>(&ms.mrun[wg * HG + h]);
-                const float mm[4] = {m4.x, m4.y, m4.z, m4.w};
-                float pp[4];
-#pragma unroll
-                for (int u = 0; u < 4; ++u)
-                    pp[u] = (mm[u] == -INFINITY) ? 0.0f : ex2_approx(fmaf(v[h + u], c_log2, -mm[u]));
-                if (rescale) {
-                    const float4 a4 = *reinterpret_cast<const float4*>(&ms.alpha[wg * HG + h]);
-                    lsum[h] = fmaf(lsum[h], a4.x, pp[0]);
-                    lsum[h + 1] = fmaf(lsum[h + 1], a4.y, pp[1]);
-                    lsum[h + 2] = fmaf(lsum[h + 2], a4.z, pp[2]);
-                    lsum[h + 3] = fmaf(lsum[h + 3], a4.w, pp[3]);
-                } else {
-#pragma unroll
-                    for (int u = 0; u < 4; ++u) lsum[h + u] += pp[u];
-                }
-                pk[h / 2] = pack_bf16x2(pp[0], pp[1]);
-                pk[h / 2 + 1] = pack_bf16x2(pp[2], pp[3]);
-            }
-            // ---- PV(i-1) done: P, O and the V slot of tile i-1 are free
-            if (i > 0) {
-                mbar_wait(&ms.odone, (seq - 1) & 1, err);
+            for (int i = 0; i < nt; ++i) {
+                const uint32_t seq = g + (uint32_t)i;
+                const int ti = t0 + i;
+                mbar_wait(&ms.sdone[seq & 1], (seq >> 1) & 1, err);
                 fence_after_sync();
-            }
-            if (i + 1 < nt) load_tile(i + 1, true);
-#pragma unroll
-            for (int c = 0; c < HG / 8; ++c) {
-                const int chunk = wg * (HG / 8) + c;          // 8 heads per 16-byte chunk
-                const uint32_t dst = sbase + L::p + (chunk >> 3) * L::p_region + sw128(row, chunk & 7);
-                asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(dst), "r"(pk[4 * c]), "r"(pk[4 * c + 1]),
-                             "r"(pk[4 * c + 2]), "r"(pk[4 * c + 3])
-                             : "memory");
-            }
-            // ---- rescale the O^T accumulator (lane = dim) when some running maximum moved
-            if (rescale && i > 0) {
+                // ---- S(i) of this warpgroup's heads -> registers (raw scores; invalid rows -inf)
+                const bool valid = ms.valid[seq & 3][row] != 0;
+                float v[HG];
 #pragma unroll
                 for (int c0 = 0; c0 < HG; c0 += 16) {
                     uint32_t rr[16];
-                    const uint32_t oa = t_o + wg * HG + c0 + lane_off;
-                    tmem_ld16(oa, rr);
+                    tmem_ld16(tmem + (seq & 1) * H + wg * HG + c0 + lane_off, rr);
                     tmem_wait_ld();
 #pragma unroll
-                    for (int k = 0; k < 16; ++k)
-                        rr[k] = __float_as_uint(__uint_as_float(rr[k]) * ms.alpha[wg * HG + c0 + k]);
-                    tmem_st16(oa, rr);
+                    for (int k = 0; k < 16; ++k) v[c0 + k] = valid ? __uint_as_float(rr[k]) : -INFINITY;
                 }
-                tmem_wait_st();
-            }
-            // ---- a TMA tile may hold rows that are not keys of this query (entries not yet
-            // visible, the next sequence, ring slots before token 0): zero their V rows, since
-            // P = 0 does not cancel a non-finite value.
-            const bool comp = ti < nt_c;
-            const bool vzero = comp ? (use_tma_c && (int64_t)(ti + 1) * kKeys > kl.n_c)
-                                    : (use_tma_w && p < kKeys - 1);
-            if (vzero) {
-                mbar_wait(&ms.vfull[seq & 1], (seq >> 1) & 1, err);
-                if (tid < kKeys && !valid) {
-                    const uint32_t vrow = sbase + L::v + (seq & 1) * kTile + row * 128;
+                // K slot of tile i is free (MMA1(i) complete)
+                if (i + 2 < nt) load_tile(i + 2, false);
+                // ---- running maxima: only when some score of the tile exceeds its head's running
+                // maximum by more than the threshold (always on an item's first tile) are the tile's
+                // per-head maxima formed: a warp reduction per head, then a 4-way merge
+                bool need = false;
 #pragma unroll
-                    for (int c = 0; c < 8; ++c) {
-                        asm volatile("st.shared.v4.b32 [%0], {%1,%1,%1,%1};" ::"r"(vrow + c * 16), "r"(0u) : "memory");
-                        asm volatile("st.shared.v4.b32 [%0], {%1,%1,%1,%1};" ::"r"(vrow + kHalf + c * 16), "r"(0u)
-                                     : "memory");
+                for (int h = 0; h < HG; h += 4) {
+                    const float4 m4 = *reinterpret_cast<const float4*>(&ms.mrun[wg * HG + h]);
+                    need |= (v[h] * c_log2 > m4.x + kRescaleThreshold) | (v[h + 1] * c_log2 > m4.y + kRescaleThreshold) |
+                            (v[h + 2] * c_log2 > m4.z + kRescaleThreshold) | (v[h + 3] * c_log2 > m4.w + kRescaleThreshold);
+                }
+                const bool grow = named_barrier_or(1, kSoft, need);
+                if (tid == 0) ms.flag[(seq + 1) & 1] = 0;   // everyone is done with tile i-1's flag
+                bool rescale = false;
+                if (grow) {
+                    float mine = -INFINITY;
+#pragma unroll
+                    for (int h = 0; h < HG; ++h) {
+                        const float mx = redux_max_f32(v[h]);
+                        mine = (lane == h) ? mx : mine;
+                    }
+                    ms.red[warp][lane] = mine;
+                    named_barrier_sync(1, kSoft);
+                    if (tid < H) {
+                        const int gq = tid / HG, hh = tid % HG;
+                        const float traw = fmaxf(fmaxf(ms.red[4 * gq][hh], ms.red[4 * gq + 1][hh]),
+                                                 fmaxf(ms.red[4 * gq + 2][hh], ms.red[4 * gq + 3][hh]));
+                        const float tmax = traw * c_log2;
+                        const float mo = ms.mrun[tid];
+                        float al = 1.0f;
+                        if (tmax > mo + kRescaleThreshold || (mo == -INFINITY && tmax != -INFINITY)) {
+                            al = (mo == -INFINITY) ? 0.0f : ex2_approx(mo - tmax);
+                            ms.mrun[tid] = tmax;
+                            ms.flag[seq & 1] = 1;
+                        }
+                        ms.alpha[tid] = al;
+                    }
+                    named_barrier_sync(1, kSoft);
+                    rescale = ms.flag[seq & 1] != 0;
+                }
+                // ---- P = 2^(s c - m) for this warpgroup's heads, row sums
+                uint32_t pk[HG / 2];
+#pragma unroll
+                for (int h = 0; h < HG; h += 4) {
+                    const float4 m4 = *reinterpret_cast<const float4*>(&ms.mrun[wg * HG + h]);
+                    const float mm[4] = {m4.x, m4.y, m4.z, m4.w};
+                    float pp[4];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u)
+                        pp[u] = (mm[u] == -INFINITY) ? 0.0f : ex2_approx(fmaf(v[h + u], c_log2, -mm[u]));
+                    if (rescale) {
+                        const float4 a4 = *reinterpret_cast<const float4*>(&ms.alpha[wg * HG + h]);
+                        lsum[h] = fmaf(lsum[h], a4.x, pp[0]);
+                        lsum[h + 1] = fmaf(lsum[h + 1], a4.y, pp[1]);
+                        lsum[h + 2] = fmaf(lsum[h + 2], a4.z, pp[2]);
+                        lsum[h + 3] = fmaf(lsum[h + 3], a4.w, pp[3]);
+                    } else {
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) lsum[h + u] += pp[u];
+                    }
+                    pk[h / 2] = pack_bf16x2(pp[0], pp[1]);
+                    pk[h / 2 + 1] = pack_bf16x2(pp[2], pp[3]);
+                }
+                // ---- PV(i-1) done: P, O and the V slot of tile i-1 are free
+                if (i > 0) {
+                    mbar_wait(&ms.odone, (seq - 1) & 1, err);
+                    fence_after_sync();
+                }
+                if (i + 1 < nt) load_tile(i + 1, true);
+#pragma unroll
+                for (int c = 0; c < HG / 8; ++c) {
+                    const int chunk = wg * (HG / 8) + c;          // 8 heads per 16-byte chunk
+                    const uint32_t dst = sbase + L::p + (chunk >> 3) * L::p_region + sw128(row, chunk & 7);
+                    asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(dst), "r"(pk[4 * c]),
+                                 "r"(pk[4 * c + 1]), "r"(pk[4 * c + 2]), "r"(pk[4 * c + 3])
+                                 : "memory");
+                }
+                // ---- rescale the O^T accumulator (lane = dim) when some running maximum moved
+                if (rescale && i > 0) {
+#pragma unroll
+                    for (int c0 = 0; c0 < HG; c0 += 16) {
+                        uint32_t rr[16];
+                        const uint32_t oa = t_o + wg * HG + c0 + lane_off;
+                        tmem_ld16(oa, rr);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int k = 0; k < 16; ++k)
+                            rr[k] = __float_as_uint(__uint_as_float(rr[k]) * ms.alpha[wg * HG + c0 + k]);
+                        tmem_st16(oa, rr);
+                    }
+                    tmem_wait_st();
+                }
+                // ---- a TMA tile may hold rows that are not keys of this query (entries not yet
+                // visible, the next sequence, ring slots before token 0): zero their V rows, since
+                // P = 0 does not cancel a non-finite value.
+                const bool comp = ti < nt_c;
+                const bool vzero = comp ? (use_tma_c && (int64_t)(ti + 1) * kKeys > kl.n_c)
+                                        : (use_tma_w && p < kKeys - 1);
+                if (vzero) {
+                    mbar_wait(&ms.vfull[seq & 1], (seq >> 1) & 1, err);
+                    if (tid < kKeys && !valid) {
+                        const uint32_t vrow = sbase + L::v + (seq & 1) * kTile + row * 128;
+#pragma unroll
+                        for (int c = 0; c < 8; ++c) {
+                            asm volatile("st.shared.v4.b32 [%0], {%1,%1,%1,%1};" ::"r"(vrow + c * 16), "r"(0u)
+                                         : "memory");
+                            asm volatile("st.shared.v4.b32 [%0], {%1,%1,%1,%1};" ::"r"(vrow + kHalf + c * 16),
+                                         "r"(0u)
+                                         : "memory");
+                        }
                     }
                 }
-            }
-            fence_proxy_async();
-            fence_before_sync();
-            __syncthreads();
-            if (tid == 0) {
-                ms.flag = 0;
-                // ---- O^T += V^T . P
-                mbar_wait(&ms.vfull[seq & 1], (seq >> 1) & 1, err);
+                // ---- P(i) and O ready for PV(i)
                 fence_proxy_async();
-                fence_after_sync();
-                const uint32_t vb = sbase + L::v + (seq & 1) * kTile;
+                fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&ms.pready);
+            }
+            mbar_wait(&ms.odone, (g + (uint32_t)nt - 1) & 1, err);
+            fence_after_sync();
+            g += (uint32_t)nt;
+            // ---- row sums across the 128 keys, partial lse, normalised partial output
+            float mine = 0.0f;
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const uint64_t ad = smem_desc(vb + j * 2048, kHalf, 1024);
-                    const uint64_t bd = smem_desc(sbase + L::p + j * 2048, L::p_region, 1024);
-                    mma_ss(t_o, ad, bd, id_pv, (i > 0 || j > 0) ? 1u : 0u);
+            for (int h = 0; h < HG; ++h) {
+                const float sum = warp_sum(lsum[h]);
+                mine = (lane == h) ? sum : mine;
+            }
+            ms.red[warp][lane] = mine;
+            named_barrier_sync(1, kSoft);
+            if (tid < H) {
+                const int gq = tid / HG, hh = tid % HG;
+                const float l = ms.red[4 * gq][hh] + ms.red[4 * gq + 1][hh] + ms.red[4 * gq + 2][hh] +
+                                ms.red[4 * gq + 3][hh];
+                const float m = ms.mrun[tid];
+                const bool any = (l > 0.0f) && (m != -INFINITY);
+                ms.linv[tid] = any ? 1.0f / l : 0.0f;
+                lse_part[obase + tid] = any ? (m + log2f(l)) * 0.6931471805599453f : -INFINITY;
+            }
+            named_barrier_sync(1, kSoft);
+#pragma unroll
+            for (int c0 = 0; c0 < HG; c0 += 16) {
+                uint32_t rr[16];
+                tmem_ld16(t_o + wg * HG + c0 + lane_off, rr);
+                tmem_wait_ld();
+#pragma unroll
+                for (int k = 0; k < 16; ++k) {
+                    const int h = wg * HG + c0 + k;
+                    o_part[(obase + h) * kD + row] = __uint_as_float(rr[k]) * ms.linv[h];
                 }
-                mma_commit(&ms.odone);
             }
+            fence_before_sync();
+            named_barrier_sync(1, kSoft);
         }
-        mbar_wait(&ms.odone, (g + (uint32_t)nt - 1) & 1, err);
-        fence_after_sync();
-        g += (uint32_t)nt;
-        // ---- row sums across the 128 keys, partial lse, normalised partial output
-        float mine = 0.0f;
-#pragma unroll
-        for (int h = 0; h < HG; ++h) {
-            const float s = warp_sum(lsum[h]);
-            mine = (lane == h) ? s : mine;
-        }
-        ms.red[warp][lane] = mine;
-        __syncthreads();
-        if (tid < H) {
-            const int gq = tid / HG, hh = tid % HG;
-            const float l = ms.red[4 * gq][hh] + ms.red[4 * gq + 1][hh] + ms.red[4 * gq + 2][hh] +
-                            ms.red[4 * gq + 3][hh];
-            const float m = ms.mrun[tid];
-            const bool any = (l > 0.0f) && (m != -INFINITY);
-            ms.linv[tid] = any ? 1.0f / l : 0.0f;
-            lse_part[obase + tid] = any ? (m + log2f(l)) * 0.6931471805599453f : -INFINITY;
-        }
-        __syncthreads();
-#pragma unroll
-        for (int c0 = 0; c0 < HG; c0 += 16) {
-            uint32_t rr[16];
-            tmem_ld16(t_o + wg * HG + c0 + lane_off, rr);
-            tmem_wait_ld();
-#pragma unroll
-            for (int k = 0; k < 16; ++k) {
-                const int h = wg * HG + c0 + k;
-                o_part[(obase + h) * kD + row] = __uint_as_float(rr[k]) * ms.linv[h];
-            }
-        }
-        fence_before_sync();
-        __syncthreads();
     }
+    __syncwarp();
+    fence_before_sync();
+    __syncthreads();
     fence_after_sync();
     if (warp == 0) tmem_dealloc(tmem, kCols);
 }
