@@ -42,7 +42,8 @@ __device__ __forceinline__ KeyList key_list(const AttendArgs& a, int r, int b, i
     if (a.is_csa) {
         kl.n_c = a.k;
     } else {
-        const int64_t n = (p >= 0) ? (p + 1) / a.m : 0;
+        // (integer division is slow on the GPU: shift when the block size is a power of two)
+        const int64_t n = (p < 0) ? 0 : ((a.m & (a.m - 1)) == 0 ? (p + 1) >> (__ffs(a.m) - 1) : (p + 1) / a.m);
         kl.n_c = n < a.Ncap ? n : a.Ncap;
     }
     kl.total = kl.n_c + a.W;

@@ -19,9 +19,10 @@
 // boxes (128-byte swizzle) by one thread; selected CSA entries and chunked-prefill windows are
 // gathered row by row with cp.async.  K and V tiles have their own two-slot rings: K(i+2) is
 // requested once MMA1(i) is done, V(i+1) once PV(i-1) is done, and the MMA warp issues MMA1(i+2)
-// right after PV(i), so loads, both MMAs and the softmax of the next tile overlap.  Each CTA is persistent
-// over (query, key-split) items; partial results (o normalised, lse) go to the split workspace
-// and are merged by the shared merge kernel.
+// right after PV(i), so loads, both MMAs and the softmax of the next tile overlap.  With few
+// query rows each CTA takes one near-equal piece of one row's tiles (pieces sized from the rows'
+// actual lengths); otherwise CTAs are persistent over (row, key-split) items.  Partial results
+// (o normalised, lse) go to the split workspace and are merged by the shared merge kernel.
 #include "attend.cuh"
 #include "tc_ptx.cuh"
 
@@ -42,16 +43,16 @@ constexpr int kThreads = kSoft + 32;       // + the MMA warp
 constexpr uint32_t kHalf = kKeys * 128;    // [128 rows][64 bf16] swizzled half tile: 16 KB
 constexpr uint32_t kTile = 2 * kHalf;      // one K or V tile: 32 KB
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
-constexpr int kSchedRows = 256;            // balanced schedule for up to this many query rows
+constexpr int kSchedRows = 256;            // piece schedule for up to this many query rows
 
 template <int H>
 struct Smem {
     static constexpr uint32_t q = 0;                                  // 2 halves x [H][128 B]
     static constexpr uint32_t q_half = H * 128;
-    static constexpr uint32_t p = 2 * q_half;                         // [128 keys][H] bf16
+    static constexpr uint32_t p = 2 * q_half;                         // two P buffers [128 keys][H] bf16
     static constexpr uint32_t p_region = kKeys * 128;
     static constexpr uint32_t p_bytes = ((H + 63) / 64) * p_region;
-    static constexpr uint32_t k = (p + p_bytes + 1023) / 1024 * 1024;  // two K slots
+    static constexpr uint32_t k = (p + 2 * p_bytes + 1023) / 1024 * 1024;  // two K slots
     static constexpr uint32_t v = k + 2 * kTile;                      // two V slots
     static constexpr uint32_t total = v + 2 * kTile;
 };
@@ -65,8 +66,10 @@ struct alignas(16) Misc {
     alignas(16) float alpha[64];     // read as float4
     float linv[64];
     unsigned char valid[4][kKeys];   // per tile (ring of 4): row holds a key of this query
-    int qoff[kSchedRows + 1];        // balanced schedule: first global tile of each query row
-    int sched_len;                   // ... and tiles per CTA
+    int my_row, my_piece, my_t0, my_nt;  // piece schedule: this CTA's piece (row -1: none), its
+    int my_empty_row;                // row's slots [my_slots_from, S) it marks empty, a row
+    int my_slots_from;               // without tiles whose slots it marks empty (or -1), and
+    int64_t my_p;                    // the query position of its row
 };
 static_assert(offsetof(Misc, mrun) % 16 == 0 && offsetof(Misc, alpha) % 16 == 0, "float4 fields");
 
@@ -111,37 +114,79 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int items = R * S;
     const int tps = kps / kKeys;
     const int nt_w = (int)cdiv(a.W, kKeys);
-    // Balanced schedule (few query rows, S >= 2 partial slots per row): the tiles of all rows,
-    // row after row, are cut into gridDim.x equal ranges; a CTA's range covers pieces of one or
-    // more rows, and a row's pieces go to consecutive slots of its partial results.  The range
-    // length is at least ceil(tiles of the longest row / (S - 1)), so no row has more than S
-    // pieces.  Otherwise items are (row, split) pairs, split s holding tiles [s kps, (s+1) kps).
-    const bool balanced = R <= kSchedRows && S >= 2;
-    if (balanced && warp == 0) {
-        int carry = 0, ntmax = 0;
-        for (int base = 0; base < R; base += 32) {
-            const int q = base + lane;
-            int nt = 0;
+    // Piece schedule (no more query rows than CTAs, S >= 2 partial slots per row): every row is
+    // cut into ceil(tiles / L) pieces of near-equal length, L the smallest length >= the average
+    // tiles per CTA for which all pieces fit the grid and no row has more than S pieces; CTA c
+    // takes the c-th piece (row by row), whose partial result goes to slot = piece index.
+    // Otherwise items are (row, split) pairs, split s holding tiles [s kps, (s+1) kps).
+    const bool pieces = R <= kSchedRows && R <= (int)gridDim.x && S >= 2;
+    if (pieces && warp == 0) {
+        constexpr int kPer = kSchedRows / 32;
+        int nt[kPer];
+        int64_t pq[kPer];
+        int total = 0, ntmax = 0;
+#pragma unroll
+        for (int j = 0; j < kPer; ++j) {
+            const int q = lane + 32 * j;
+            nt[j] = 0;
+            pq[j] = -1;
             if (q < R) {
-                const int64_t p = a.q_pos[q];
-                nt = (int)cdiv(key_list(a, q, q / a.T, p).n_c, kKeys) + nt_w;
+                pq[j] = a.q_pos[q];
+                nt[j] = (int)cdiv(key_list(a, q, 0, pq[j]).n_c, kKeys) + nt_w;
             }
-            int x = nt;
+            total += nt[j];
+            ntmax = max(ntmax, nt[j]);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            total += __shfl_xor_sync(0xffffffffu, total, o);
+            ntmax = max(ntmax, __shfl_xor_sync(0xffffffffu, ntmax, o));
+        }
+        int len = max(max((int)cdiv(total, gridDim.x), (int)cdiv(ntmax, S)), 1);
+        int np[kPer];
+        for (;;) {                                  // usually one or two rounds
+            int cnt = 0;
+#pragma unroll
+            for (int j = 0; j < kPer; ++j) {
+                np[j] = 32 * j < R ? (nt[j] + len - 1) / len : 0;
+                cnt += np[j];
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
+            if (cnt <= (int)gridDim.x) break;
+            ++len;
+        }
+        // first CTA of each row: exclusive prefix of the piece counts, rows in order
+        int carry = 0;
+        if (lane == 0) {
+            ms.my_row = -1;
+            ms.my_slots_from = S;
+            ms.my_empty_row = -1;
+        }
+        __syncwarp();
+        const int c = (int)blockIdx.x;
+#pragma unroll
+        for (int j = 0; j < kPer; ++j) {
+            const int q = lane + 32 * j;
+            int x = np[j];
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
                 const int y = __shfl_up_sync(0xffffffffu, x, o);
                 if (lane >= o) x += y;
             }
-            if (q < R) ms.qoff[q + 1] = carry + x;
+            const int first = carry + x - np[j];
             carry += __shfl_sync(0xffffffffu, x, 31);
-            ntmax = max(ntmax, nt);
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) ntmax = max(ntmax, __shfl_xor_sync(0xffffffffu, ntmax, o));
-        if (lane == 0) {
-            ms.qoff[0] = 0;
-            const int len = max((int)cdiv(carry, gridDim.x), (int)cdiv(ntmax, S - 1));
-            ms.sched_len = max(len, 1);
+            if (q < R && np[j] > 0 && c >= first && c < first + np[j]) {
+                const int piece = c - first;
+                const int t0 = piece * nt[j] / np[j];
+                ms.my_row = q;
+                ms.my_piece = piece;
+                ms.my_t0 = t0;
+                ms.my_nt = (piece + 1) * nt[j] / np[j] - t0;
+                ms.my_p = pq[j];
+                if (piece == 0) ms.my_slots_from = np[j];
+            }
+            if (q < R && np[j] == 0 && q == c) ms.my_empty_row = q;   // R <= gridDim.x
         }
     }
     fence_before_sync();
@@ -150,41 +195,36 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = ms.tmem_base;
     const uint32_t t_o = tmem + 2 * H;
     const uint32_t sbase = smem_u32(sm);
-    // next work item of this CTA (cursor `cur`: an item index, or a query row when balanced);
-    // tile range [t0, t0 + nt) of the row's tile space: compressed tiles first, then the window
+    // next work item of this CTA (cursor `cur`: an item index; with the piece schedule 0 before
+    // and 1 after the CTA's piece); tile range [t0, t0 + nt) of the row's tile space:
+    // compressed tiles first, then the window
     auto next_item = [&](int& cur, ItemTiles& it) -> bool {
-        if (balanced) {
-            const int len = ms.sched_len, lo = (int)blockIdx.x * len, hi = min(ms.qoff[R], lo + len);
-            for (;; ++cur) {
-                if (cur >= R) return false;
-                const int qs = ms.qoff[cur], qe = ms.qoff[cur + 1];
-                if (qs >= hi) return false;
-                if (qe <= lo || qe == qs) continue;
-                it.r = cur;
-                it.slot = (int)blockIdx.x - qs / len;
-                it.t0 = max(lo, qs) - qs;
-                it.nt = min(hi, qe) - max(lo, qs);
-                ++cur;
-                break;
-            }
+        if (pieces) {
+            if (cur != 0 || ms.my_row < 0) return false;
+            cur = 1;
+            it.r = ms.my_row;
+            it.t0 = ms.my_t0;
+            it.nt = ms.my_nt;
+            it.slot = ms.my_piece;
+            it.p = ms.my_p;
         } else {
             if (cur >= items) return false;
             it.r = cur / S;
             it.slot = cur % S;
             it.t0 = it.slot * tps;
             cur += gridDim.x;
+            it.p = a.q_pos[it.r];
         }
         it.b = it.r / a.T;
-        it.p = a.q_pos[it.r];
         it.kl = key_list(a, it.r, it.b, it.p);
         it.nt_c = (int)cdiv(it.kl.n_c, kKeys);
-        if (!balanced) {
+        if (!pieces) {
             const int t1 = min(it.nt_c + nt_w, it.t0 + tps);
             it.nt = t1 > it.t0 ? t1 - it.t0 : 0;
         }
         return true;
     };
-    const int cur0 = balanced ? 0 : (int)blockIdx.x;
+    const int cur0 = pieces ? 0 : (int)blockIdx.x;
 
     if (warp == kSoft / 32) {
         // ========================================================================= MMA warp
@@ -223,9 +263,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     fence_after_sync();
                     // O^T += V^T . P
                     const uint64_t v_desc = smem_desc(sbase + L::v + (seq & 1) * kTile, kHalf, 1024);
+                    const uint64_t pb_desc = p_desc + (uint64_t)(((seq & 1) * L::p_bytes) >> 4);
 #pragma unroll
                     for (int j = 0; j < 8; ++j)
-                        mma_ss(t_o, v_desc + (uint64_t)((j * 2048) >> 4), p_desc + (uint64_t)((j * 2048) >> 4), id_pv,
+                        mma_ss(t_o, v_desc + (uint64_t)((j * 2048) >> 4), pb_desc + (uint64_t)((j * 2048) >> 4), id_pv,
                                (i > 0 || j > 0) ? 1u : 0u);
                     mma_commit(&ms.odone);
                     if (i + 2 < nt) qk(i + 2);
@@ -244,21 +285,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t pol_stream = l2_policy_evict_first();     // K/V rows are read once per step
         uint32_t g = 0;                                          // tiles processed so far by this CTA
 
-        if (balanced) {       // partial slots no piece of this schedule writes: lse = -inf
-            const int len = ms.sched_len;
-            for (int q = 0; q < R; ++q) {
-                const int qs = ms.qoff[q], qe = ms.qoff[q + 1];
-                int first_free;
-                if (qe == qs) {
-                    if (q % (int)gridDim.x != (int)blockIdx.x) continue;
-                    first_free = 0;
-                } else {
-                    if (qs / len != (int)blockIdx.x) continue;
-                    first_free = (qe - 1) / len - qs / len + 1;
-                }
-                for (int sl = first_free; sl < S; ++sl)
-                    if (tid < H) lse_part[((int64_t)q * S + sl) * H + tid] = -INFINITY;
-            }
+        if (pieces && tid < H) {    // partial slots no piece of this schedule writes: lse = -inf
+            if (ms.my_row >= 0)
+                for (int sl = ms.my_slots_from; sl < S; ++sl)
+                    lse_part[((int64_t)ms.my_row * S + sl) * H + tid] = -INFINITY;
+            if (ms.my_empty_row >= 0)
+                for (int sl = 0; sl < S; ++sl) lse_part[((int64_t)ms.my_empty_row * S + sl) * H + tid] = -INFINITY;
         }
         ItemTiles it;
         for (int cur = cur0; next_item(cur, it);) {
@@ -346,17 +378,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int ti = t0 + i;
                 mbar_wait(&ms.sdone[seq & 1], (seq >> 1) & 1, err);
                 fence_after_sync();
-                // ---- S(i) of this warpgroup's heads -> registers (raw scores; invalid rows -inf)
+                // The S tile is read from TMEM in chunks of 16 heads (raw scores; invalid rows -inf),
+                // once per pass, so no pass holds more than 16 scores.
                 const bool valid = ms.valid[seq & 3][row] != 0;
-                float v[HG];
-#pragma unroll
-                for (int c0 = 0; c0 < HG; c0 += 16) {
-                    uint32_t rr[16];
-                    tmem_ld16(tmem + (seq & 1) * H + wg * HG + c0 + lane_off, rr);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int k = 0; k < 16; ++k) v[c0 + k] = valid ? __uint_as_float(rr[k]) : -INFINITY;
-                }
+                const uint32_t scol = tmem + (seq & 1) * H + wg * HG + lane_off;
                 // K slot of tile i is free (MMA1(i) complete)
                 if (i + 2 < nt) load_tile(i + 2, false);
                 // ---- running maxima: only when some score of the tile exceeds its head's running
@@ -364,20 +389,35 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // per-head maxima formed: a warp reduction per head, then a 4-way merge
                 bool need = false;
 #pragma unroll
-                for (int h = 0; h < HG; h += 4) {
-                    const float4 m4 = *reinterpret_cast<const float4*>(&ms.mrun[wg * HG + h]);
-                    need |= (v[h] * c_log2 > m4.x + kRescaleThreshold) | (v[h + 1] * c_log2 > m4.y + kRescaleThreshold) |
-                            (v[h + 2] * c_log2 > m4.z + kRescaleThreshold) | (v[h + 3] * c_log2 > m4.w + kRescaleThreshold);
+                for (int c0 = 0; c0 < HG; c0 += 16) {
+                    uint32_t rr[16];
+                    tmem_ld16(scol + c0, rr);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int k = 0; k < 16; k += 4) {
+                        const float4 m4 = *reinterpret_cast<const float4*>(&ms.mrun[wg * HG + c0 + k]);
+                        need |= (__uint_as_float(rr[k]) * c_log2 > m4.x + kRescaleThreshold) |
+                                (__uint_as_float(rr[k + 1]) * c_log2 > m4.y + kRescaleThreshold) |
+                                (__uint_as_float(rr[k + 2]) * c_log2 > m4.z + kRescaleThreshold) |
+                                (__uint_as_float(rr[k + 3]) * c_log2 > m4.w + kRescaleThreshold);
+                    }
                 }
+                need = need && valid;
                 const bool grow = named_barrier_or(1, kSoft, need);
                 if (tid == 0) ms.flag[(seq + 1) & 1] = 0;   // everyone is done with tile i-1's flag
                 bool rescale = false;
                 if (grow) {
                     float mine = -INFINITY;
 #pragma unroll
-                    for (int h = 0; h < HG; ++h) {
-                        const float mx = redux_max_f32(v[h]);
-                        mine = (lane == h) ? mx : mine;
+                    for (int c0 = 0; c0 < HG; c0 += 16) {
+                        uint32_t rr[16];
+                        tmem_ld16(scol + c0, rr);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int k = 0; k < 16; ++k) {
+                            const float mx = redux_max_f32(valid ? __uint_as_float(rr[k]) : -INFINITY);
+                            mine = (lane == c0 + k) ? mx : mine;
+                        }
                     }
                     ms.red[warp][lane] = mine;
                     named_barrier_sync(1, kSoft);
@@ -398,43 +438,54 @@ __global__ void __launch_bounds__(kThreads, 1)
                     named_barrier_sync(1, kSoft);
                     rescale = ms.flag[seq & 1] != 0;
                 }
-                // ---- P = 2^(s c - m) for this warpgroup's heads, row sums
-                uint32_t pk[HG / 2];
+                // ---- P = 2^(s c - m) into P buffer (i & 1) ([key][head], 128-byte swizzle; PV(i-2),
+                // its last reader, is complete), row sums
+                const uint32_t pbuf = sbase + L::p + (seq & 1) * L::p_bytes;
 #pragma unroll
-                for (int h = 0; h < HG; h += 4) {
-                    const float4 m4 = *reinterpret_cast<const float4*>(&ms.mrun[wg * HG + h]);
-                    const float mm[4] = {m4.x, m4.y, m4.z, m4.w};
-                    float pp[4];
+                for (int c0 = 0; c0 < HG; c0 += 16) {
+                    uint32_t rr[16];
+                    tmem_ld16(scol + c0, rr);
+                    tmem_wait_ld();
+                    uint32_t pk[8];
 #pragma unroll
-                    for (int u = 0; u < 4; ++u)
-                        pp[u] = (mm[u] == -INFINITY) ? 0.0f : ex2_approx(fmaf(v[h + u], c_log2, -mm[u]));
-                    if (rescale) {
-                        const float4 a4 = *reinterpret_cast<const float4*>(&ms.alpha[wg * HG + h]);
-                        lsum[h] = fmaf(lsum[h], a4.x, pp[0]);
-                        lsum[h + 1] = fmaf(lsum[h + 1], a4.y, pp[1]);
-                        lsum[h + 2] = fmaf(lsum[h + 2], a4.z, pp[2]);
-                        lsum[h + 3] = fmaf(lsum[h + 3], a4.w, pp[3]);
-                    } else {
+                    for (int k = 0; k < 16; k += 4) {
+                        const int h = wg * HG + c0 + k;
+                        const float4 m4 = *reinterpret_cast<const float4*>(&ms.mrun[h]);
+                        const float mm[4] = {m4.x, m4.y, m4.z, m4.w};
+                        float pp[4];
 #pragma unroll
-                        for (int u = 0; u < 4; ++u) lsum[h + u] += pp[u];
+                        for (int u = 0; u < 4; ++u)
+                            pp[u] = (mm[u] == -INFINITY || !valid)
+                                        ? 0.0f
+                                        : ex2_approx(fmaf(__uint_as_float(rr[k + u]), c_log2, -mm[u]));
+                        if (rescale) {
+                            const float4 a4 = *reinterpret_cast<const float4*>(&ms.alpha[h]);
+                            lsum[c0 + k] = fmaf(lsum[c0 + k], a4.x, pp[0]);
+                            lsum[c0 + k + 1] = fmaf(lsum[c0 + k + 1], a4.y, pp[1]);
+                            lsum[c0 + k + 2] = fmaf(lsum[c0 + k + 2], a4.z, pp[2]);
+                            lsum[c0 + k + 3] = fmaf(lsum[c0 + k + 3], a4.w, pp[3]);
+                        } else {
+#pragma unroll
+                            for (int u = 0; u < 4; ++u) lsum[c0 + k + u] += pp[u];
+                        }
+                        pk[k / 2] = pack_bf16x2(pp[0], pp[1]);
+                        pk[k / 2 + 1] = pack_bf16x2(pp[2], pp[3]);
                     }
-                    pk[h / 2] = pack_bf16x2(pp[0], pp[1]);
-                    pk[h / 2 + 1] = pack_bf16x2(pp[2], pp[3]);
+#pragma unroll
+                    for (int c = 0; c < 2; ++c) {
+                        const int chunk = (wg * HG + c0) / 8 + c;        // 8 heads per 16-byte chunk
+                        const uint32_t dst = pbuf + (chunk >> 3) * L::p_region + sw128(row, chunk & 7);
+                        asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(dst), "r"(pk[4 * c]),
+                                     "r"(pk[4 * c + 1]), "r"(pk[4 * c + 2]), "r"(pk[4 * c + 3])
+                                     : "memory");
+                    }
                 }
-                // ---- PV(i-1) done: P, O and the V slot of tile i-1 are free
+                // ---- PV(i-1) done: O and the V slot of tile i-1 are free
                 if (i > 0) {
                     mbar_wait(&ms.odone, (seq - 1) & 1, err);
                     fence_after_sync();
                 }
                 if (i + 1 < nt) load_tile(i + 1, true);
-#pragma unroll
-                for (int c = 0; c < HG / 8; ++c) {
-                    const int chunk = wg * (HG / 8) + c;          // 8 heads per 16-byte chunk
-                    const uint32_t dst = sbase + L::p + (chunk >> 3) * L::p_region + sw128(row, chunk & 7);
-                    asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(dst), "r"(pk[4 * c]),
-                                 "r"(pk[4 * c + 1]), "r"(pk[4 * c + 2]), "r"(pk[4 * c + 3])
-                                 : "memory");
-                }
                 // ---- rescale the O^T accumulator (lane = dim) when some running maximum moved
                 if (rescale && i > 0) {
 #pragma unroll
