@@ -23,6 +23,8 @@ constexpr int kTile = 32;
 template <typename T, int HPW, int DPL>
 __global__ void __launch_bounds__(256) attend_split_kernel(AttendArgs a, int kps, float* __restrict__ o_part,
                                                            float* __restrict__ lse_part, unsigned* err) {
+    pdl_wait();
+    pdl_trigger();
     extern __shared__ float smem[];
     const int H = a.H, d = a.d;
     float* Qs = smem;                              // [H][d]
@@ -134,6 +136,8 @@ __global__ void __launch_bounds__(32 * kMergeWarps) merge_kernel(int R, int S, i
                                                                  const float* __restrict__ o_part,
                                                                  const float* __restrict__ lse_part,
                                                                  T* __restrict__ out, float* __restrict__ lse_out) {
+    pdl_wait();
+    pdl_trigger();
     const int lane = threadIdx.x & 31;
     const int64_t gw = (int64_t)blockIdx.x * kMergeWarps + (threadIdx.x >> 5);
     if (gw >= (int64_t)R * H) return;
@@ -178,7 +182,7 @@ cudaError_t launch_split(const AttendArgs& a, int S, int kps, float* o_part, flo
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     dim3 grid((unsigned)S, (unsigned)(a.B * a.T));
-    kern<<<grid, 256, smem, st>>>(a, kps, o_part, lse_part, err);
+    (void)launch_pdl(kern, dim3(grid), dim3(256), smem, st, a, kps, o_part, lse_part, err);
     return cudaGetLastError();
 }
 
@@ -243,10 +247,10 @@ csahca_status attend_run(const AttendArgs& a, int splits_req, void* workspace, s
     if (e != cudaSuccess) return CSAHCA_ERR_CUDA;
     const unsigned mgrid = (unsigned)cdiv((int64_t)R * a.H, kMergeWarps);
     if (a.dtype == CSAHCA_F32)
-        merge_kernel<float><<<mgrid, 32 * kMergeWarps, 0, st>>>(R, sp.S, a.H, a.d, o_part, lse_part, (float*)a.out,
+        (void)launch_pdl(merge_kernel<float>, dim3(mgrid), dim3(32 * kMergeWarps), 0, st, R, sp.S, a.H, a.d, o_part, lse_part, (float*)a.out,
                                                                 a.lse);
     else
-        merge_kernel<__nv_bfloat16><<<mgrid, 32 * kMergeWarps, 0, st>>>(R, sp.S, a.H, a.d, o_part, lse_part,
+        (void)launch_pdl(merge_kernel<__nv_bfloat16>, dim3(mgrid), dim3(32 * kMergeWarps), 0, st, R, sp.S, a.H, a.d, o_part, lse_part,
                                                                         (__nv_bfloat16*)a.out, a.lse);
     count_launch();
     CSAHCA_CHECK_LAUNCH();

@@ -87,6 +87,8 @@ template <int H>
 __global__ void __launch_bounds__(kThreads, 1)
     attend_tc_kernel(AttendArgs a, int S, int kps, const __grid_constant__ Maps maps, int use_tma_c, int use_tma_w,
                      float* __restrict__ o_part, float* __restrict__ lse_part, unsigned* err) {
+    pdl_wait();
+    pdl_trigger();
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                          ~uintptr_t(1023));
@@ -599,7 +601,7 @@ cudaError_t launch_tc(const AttendArgs& a, int S, int kps, float* o_part, float*
     if (e != cudaSuccess) return e;
     const int items = a.B * a.T * S;
     const int grid = items < num_sms() ? items : num_sms();
-    kern<<<grid, kThreads, smem, st>>>(a, S, kps, maps, use_c, use_w, o_part, lse_part, err);
+    (void)launch_pdl(kern, dim3(grid), dim3(kThreads), smem, st, a, S, kps, maps, use_c, use_w, o_part, lse_part, err);
     return cudaGetLastError();
 }
 

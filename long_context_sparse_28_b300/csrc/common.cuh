@@ -37,6 +37,35 @@ __host__ __device__ inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 
 
 int num_sms();
 
+// ------------------------------------------------------------- programmatic dependent launch
+// Every kernel of the library is launched with programmatic stream serialization: its CTAs may
+// be scheduled while the previous kernel in the stream is still running.  Each kernel therefore
+// starts with pdl_wait() (returns once the previous grid has completed and its memory is
+// visible; immediately when there is none) before it reads any global memory, then calls
+// pdl_trigger() so that the next kernel may be scheduled in turn.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                              Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+
+// Zeroes n 32-bit words (a kernel rather than a memset node, so the launch chain stays
+// programmatic).
+cudaError_t zero_words(uint32_t* p, size_t n, cudaStream_t st);
+
 // ------------------------------------------------------------------------- vector I/O
 // 8 consecutive elements <-> float[8]; p must be 16-byte (bf16) / 32-byte (f32) aligned.
 __device__ __forceinline__ void load8(const float* p, float (&o)[8]) {

@@ -58,6 +58,8 @@ __global__ void __launch_bounds__(256) index_score_kernel(
     const void* __restrict__ q_idx, int q_dtype, const float* __restrict__ w, const void* __restrict__ k_codes,
     const void* __restrict__ k_scale, int fmt, int T, int H_I, int d_I, const int64_t* __restrict__ q_pos,
     int64_t Ncap, int m, float* __restrict__ S) {
+    pdl_wait();
+    pdl_trigger();
     extern __shared__ float sh[];                 // q [H_I][d_I], then w [H_I]
     float* qs = sh;
     float* ws = sh + H_I * d_I;
@@ -157,10 +159,10 @@ static csahca_status index_scores_launch(const void* q_idx, csahca_dtype q_dtype
     dim3 grid((unsigned)cdiv(Ncap, 256), (unsigned)R);
     const size_t smem = (size_t)(H_I * d_I + H_I) * 4;
     if (H_I <= 16)
-        index_score_kernel<16><<<grid, 256, smem, st>>>(q_idx, q_dtype, w, k_codes, k_scale, key_fmt, T, H_I, d_I,
+        (void)launch_pdl(index_score_kernel<16>, dim3(grid), dim3(256), smem, st, q_idx, q_dtype, w, k_codes, k_scale, key_fmt, T, H_I, d_I,
                                                         q_pos, Ncap, m, S);
     else
-        index_score_kernel<64><<<grid, 256, smem, st>>>(q_idx, q_dtype, w, k_codes, k_scale, key_fmt, T, H_I, d_I,
+        (void)launch_pdl(index_score_kernel<64>, dim3(grid), dim3(256), smem, st, q_idx, q_dtype, w, k_codes, k_scale, key_fmt, T, H_I, d_I,
                                                         q_pos, Ncap, m, S);
     count_launch();
     CSAHCA_CHECK_LAUNCH();
@@ -193,7 +195,7 @@ csahca_status csa_index_topk(const void* q_idx, csahca_dtype q_dtype, const floa
     float* S = scores_out ? scores_out : reinterpret_cast<float*>(ws);
     TopkWorkspace tw = topk_carve(ws + align256((size_t)R * Ncap * 4), R, Ncap);
     cudaStream_t st = (cudaStream_t)stream;
-    if (cudaMemsetAsync(tw.hist1, 0, topk_zero_bytes(R), st) != cudaSuccess) return CSAHCA_ERR_CUDA;
+    if (zero_words(tw.hist1, topk_zero_bytes(R) / 4, st) != cudaSuccess) return CSAHCA_ERR_CUDA;
     bool hist_done = false;
     const csahca_status e = index_scores_launch(q_idx, q_dtype, w, k_codes, k_scale, key_fmt, B, T, H_I, d_I, q_pos,
                                                 Ncap, m, S, tw.hist1, &hist_done, st);

@@ -165,6 +165,8 @@ __global__ void __launch_bounds__(kThreads) index_tc_kernel(const __grid_constan
                                                             const int64_t* __restrict__ q_pos, int64_t Ncap, int m,
                                                             int R, float* __restrict__ S,
                                                             uint32_t* __restrict__ hist1, unsigned* err) {
+    pdl_wait();
+    pdl_trigger();
     using C = Cfg<FMT, HI>;
     constexpr int kUnits = 2 * HI / 32;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -486,7 +488,7 @@ cudaError_t launch_index_tc(const void* q_idx, const float* w, const void* k_cod
     const int R = B * T;
     const int64_t items = (int64_t)R * cdiv(Ncap, (int64_t)kChunkStages * kPair);
     const int grid = (int)std::min<int64_t>(items, (int64_t)num_sms() * occ);
-    kern<<<grid, kThreads, smem, st>>>(kmap, static_cast<const __nv_bfloat16*>(q_idx), w,
+    (void)launch_pdl(kern, dim3(grid), dim3(kThreads), smem, st, kmap, static_cast<const __nv_bfloat16*>(q_idx), w,
                                        static_cast<const uint8_t*>(k_scale), T, q_pos, Ncap, m, R, S, hist1, err);
     return cudaGetLastError();
 }

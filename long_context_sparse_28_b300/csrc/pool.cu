@@ -84,6 +84,8 @@ __global__ void compress_kernel(const T* __restrict__ k_raw, const T* __restrict
                                 const int64_t* __restrict__ raw_pos0, const int64_t* __restrict__ n_raw,
                                 const float* __restrict__ bias, int m, int B, int d, T* ck, T* cv,
                                 int64_t Ncap, int64_t max_blocks, unsigned* err) {
+    pdl_wait();
+    pdl_trigger();
     const int wpc = blockDim.x >> 5;
     const int lane = threadIdx.x & 31;
     const int64_t total = (int64_t)B * max_blocks;
@@ -121,6 +123,8 @@ __global__ void __launch_bounds__(kAppendThreads) append_kernel(
     const void* kidx_new, int kidx_dtype, int kidx_rows, const int64_t* __restrict__ pos, int n_new, int d,
     const float* __restrict__ bias, int m, T* ring_k, T* ring_v, float* ring_gate, int ring_cap, T* ck, T* cv,
     int64_t Ncap, void* k_codes, void* k_scale, int key_fmt, int d_I, unsigned* err) {
+    pdl_wait();
+    pdl_trigger();
     __shared__ float alpha[kMaxM];
     __shared__ float part[kAppendThreads * 8];
     const int b = blockIdx.x;
@@ -238,6 +242,8 @@ __global__ void ring_write_kernel(const T* __restrict__ k_new, const T* __restri
                                   const float* __restrict__ gate_new, int64_t new_stride,
                                   const int64_t* __restrict__ pos, int n_new, int d, T* ring_k,
                                   T* ring_v, float* ring_gate, int ring_cap) {
+    pdl_wait();
+    pdl_trigger();
     const int b = blockIdx.y;
     const int64_t p = pos[b];
     if (p < 0) return;                     // no valid slot for a negative position
@@ -279,11 +285,11 @@ csahca_status compress_impl(const void* k_raw, const void* v_raw, const float* g
     unsigned* err = err_word();
     if (!err) return CSAHCA_ERR_CUDA;
     if (kv == CSAHCA_F32)
-        compress_kernel<float><<<grid, threads, 0, stream>>>(
+        (void)launch_pdl(compress_kernel<float>, dim3(grid), dim3(threads), 0, stream, 
             (const float*)k_raw, (const float*)v_raw, gate, raw_stride, raw_pos0, n_raw, bias, m, B, d,
             (float*)ck, (float*)cv, Ncap, max_blocks, err);
     else
-        compress_kernel<__nv_bfloat16><<<grid, threads, 0, stream>>>(
+        (void)launch_pdl(compress_kernel<__nv_bfloat16>, dim3(grid), dim3(threads), 0, stream, 
             (const __nv_bfloat16*)k_raw, (const __nv_bfloat16*)v_raw, gate, raw_stride, raw_pos0, n_raw,
             bias, m, B, d, (__nv_bfloat16*)ck, (__nv_bfloat16*)cv, Ncap, max_blocks, err);
     count_launch();
@@ -316,12 +322,12 @@ csahca_status append_impl(const void* k_new, const void* v_new, const float* gat
     const int kidx_rows = n_new / m + 1;
     const int threads = 256;
     if (kv == CSAHCA_F32)
-        append_kernel<float><<<B, kAppendThreads, 0, stream>>>(
+        (void)launch_pdl(append_kernel<float>, dim3(B), dim3(kAppendThreads), 0, stream, 
             (const float*)k_new, (const float*)v_new, gate_new, kidx_new, kidx_dtype, kidx_rows, pos, n_new, d,
             bias, m, (float*)ring_k, (float*)ring_v, ring_gate, ring_cap, (float*)ck, (float*)cv, Ncap, k_codes,
             k_scale, key_fmt, d_I, err);
     else
-        append_kernel<__nv_bfloat16><<<B, kAppendThreads, 0, stream>>>(
+        (void)launch_pdl(append_kernel<__nv_bfloat16>, dim3(B), dim3(kAppendThreads), 0, stream, 
             (const __nv_bfloat16*)k_new, (const __nv_bfloat16*)v_new, gate_new, kidx_new, kidx_dtype, kidx_rows,
             pos, n_new, d, bias, m, (__nv_bfloat16*)ring_k, (__nv_bfloat16*)ring_v, ring_gate, ring_cap,
             (__nv_bfloat16*)ck, (__nv_bfloat16*)cv, Ncap, k_codes, k_scale, key_fmt, d_I, err);
@@ -386,11 +392,11 @@ csahca_status swa_ring_write(const void* k_new, const void* v_new, const float* 
     const int64_t items = (int64_t)(n_new - first) * (d / 8);
     dim3 grid((unsigned)std::max<int64_t>(1, std::min<int64_t>(cdiv(items, 256), 64)), B);
     if (kv_dtype == CSAHCA_F32)
-        ring_write_kernel<float><<<grid, 256, 0, (cudaStream_t)stream>>>(
+        (void)launch_pdl(ring_write_kernel<float>, dim3(grid), dim3(256), 0, (cudaStream_t)stream, 
             (const float*)k_new, (const float*)v_new, gate_new, new_stride, pos, n_new, d, (float*)ring_k,
             (float*)ring_v, ring_gate, ring_cap);
     else
-        ring_write_kernel<__nv_bfloat16><<<grid, 256, 0, (cudaStream_t)stream>>>(
+        (void)launch_pdl(ring_write_kernel<__nv_bfloat16>, dim3(grid), dim3(256), 0, (cudaStream_t)stream, 
             (const __nv_bfloat16*)k_new, (const __nv_bfloat16*)v_new, gate_new, new_stride, pos, n_new, d,
             (__nv_bfloat16*)ring_k, (__nv_bfloat16*)ring_v, ring_gate, ring_cap);
     count_launch();

@@ -7,6 +7,8 @@ namespace {
 
 __global__ void quantize_rows_kernel(const void* __restrict__ in, int in_dtype, int64_t rows, int d_I,
                                      int fmt, void* codes, void* scales) {
+    pdl_wait();
+    pdl_trigger();
     const int wpc = blockDim.x >> 5;
     const int E = d_I / 32;
     const int64_t in_row_bytes = (int64_t)d_I * (in_dtype == CSAHCA_F32 ? 4 : 2);
@@ -37,7 +39,7 @@ extern "C" csahca_status csa_index_key_quantize(const void* k_in, csahca_dtype i
     const int threads = 256;
     const int64_t want = cdiv(rows, threads / 32);
     const int grid = (int)std::min<int64_t>(want, (int64_t)num_sms() * 16);
-    quantize_rows_kernel<<<grid, threads, 0, (cudaStream_t)stream>>>(k_in, in_dtype, rows, d_I, key_fmt, k_codes,
+    (void)launch_pdl(quantize_rows_kernel, dim3(grid), dim3(threads), 0, (cudaStream_t)stream, k_in, in_dtype, rows, d_I, key_fmt, k_codes,
                                                                     k_scale);
     count_launch();
     CSAHCA_CHECK_LAUNCH();

@@ -43,6 +43,23 @@ int num_sms() {
 
 void count_launch(int n) { g_launches += (uint64_t)n; }
 
+namespace {
+__global__ void zero_words_kernel(uint32_t* __restrict__ p, size_t n) {
+    pdl_wait();
+    pdl_trigger();
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x)
+        p[i] = 0u;
+}
+}  // namespace
+
+cudaError_t zero_words(uint32_t* p, size_t n, cudaStream_t st) {
+    if (n == 0) return cudaSuccess;
+    const size_t blocks = (n + 255) / 256;
+    const unsigned grid = (unsigned)(blocks < (size_t)num_sms() * 4 ? blocks : (size_t)num_sms() * 4);
+    count_launch();
+    return launch_pdl(zero_words_kernel, dim3(grid), dim3(256), 0, st, p, n);
+}
+
 }  // namespace csahca
 
 extern "C" {

@@ -75,6 +75,8 @@ __global__ void __launch_bounds__(kThreads) topk_hist_kernel(const float* __rest
                                                              const int64_t* __restrict__ n_vis_arr,
                                                              const int64_t* __restrict__ q_pos, int m, int64_t Ncap,
                                                              uint32_t* __restrict__ hist1) {
+    pdl_wait();
+    pdl_trigger();
     __shared__ uint32_t sh[kBins12];
     const int r = blockIdx.y;
     const int64_t n = min(row_nvis(r, n_vis_arr, q_pos, m, Ncap), stride);
@@ -98,6 +100,8 @@ __global__ void __launch_bounds__(kThreads) topk_threshold_kernel(const int64_t*
                                                                   int64_t Ncap, int64_t stride, int k,
                                                                   const uint32_t* __restrict__ hist1,
                                                                   int4* __restrict__ thr1) {
+    pdl_wait();
+    pdl_trigger();
     __shared__ int sh_scan[33];
     __shared__ int sh_res[2];
     const int r = blockIdx.x;
@@ -129,6 +133,8 @@ __global__ void __launch_bounds__(kThreads) topk_collect_kernel(const float* __r
                                                                 const int64_t* __restrict__ q_pos, int m,
                                                                 int64_t Ncap, int k, const int4* __restrict__ thr1,
                                                                 uint2* __restrict__ cand, int* __restrict__ cand_n) {
+    pdl_wait();
+    pdl_trigger();
     const int r = blockIdx.y;
     const int lane = threadIdx.x & 31;
     const int64_t w0 = ((int64_t)blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5)) * kWarpSpan;
@@ -194,6 +200,8 @@ __global__ void __launch_bounds__(kFinishThreads) topk_finish_kernel(
     const int64_t* __restrict__ q_pos, int m, int64_t Ncap, int k, const uint32_t* __restrict__ hist1,
     const int4* __restrict__ thr1, const uint2* __restrict__ cand, const int* __restrict__ cand_n,
     uint32_t* __restrict__ win, uint32_t* __restrict__ tie, int64_t words, int32_t* __restrict__ idx_out) {
+    pdl_wait();
+    pdl_trigger();
     extern __shared__ __align__(16) unsigned char fsm[];
     uint2* cs = reinterpret_cast<uint2*>(fsm);
     uint32_t* swin = reinterpret_cast<uint32_t*>(fsm + (size_t)kCap * 8);
@@ -347,16 +355,16 @@ csahca_status topk_launch(const float* scores, int64_t stride, int R, const int6
     const int64_t P = std::max<int64_t>(1, cdiv(stride, kSlice));
     dim3 grid((unsigned)P, (unsigned)R);
     if (!hist_ready) {
-        if (cudaMemsetAsync(tw.hist1, 0, topk_zero_bytes(R), stream) != cudaSuccess) return CSAHCA_ERR_CUDA;
-        topk_hist_kernel<<<grid, kThreads, 0, stream>>>(scores, stride, n_vis_arr, q_pos, m, Ncap, tw.hist1);
+        if (zero_words(tw.hist1, topk_zero_bytes(R) / 4, stream) != cudaSuccess) return CSAHCA_ERR_CUDA;
+        (void)launch_pdl(topk_hist_kernel, dim3(grid), dim3(kThreads), 0, stream, scores, stride, n_vis_arr, q_pos, m, Ncap, tw.hist1);
         count_launch();
         CSAHCA_CHECK_LAUNCH();
     }
-    topk_threshold_kernel<<<R, kThreads, 0, stream>>>(n_vis_arr, q_pos, m, Ncap, stride, k, tw.hist1, tw.thr1);
+    (void)launch_pdl(topk_threshold_kernel, dim3(R), dim3(kThreads), 0, stream, n_vis_arr, q_pos, m, Ncap, stride, k, tw.hist1, tw.thr1);
     count_launch();
     CSAHCA_CHECK_LAUNCH();
     const dim3 cgrid((unsigned)std::max<int64_t>(1, cdiv(stride, (int64_t)kWarpSpan * (kThreads / 32))), (unsigned)R);
-    topk_collect_kernel<<<cgrid, kThreads, 0, stream>>>(scores, stride, n_vis_arr, q_pos, m, Ncap, k, tw.thr1,
+    (void)launch_pdl(topk_collect_kernel, dim3(cgrid), dim3(kThreads), 0, stream, scores, stride, n_vis_arr, q_pos, m, Ncap, k, tw.thr1,
                                                         tw.cand, tw.cand_n);
     count_launch();
     CSAHCA_CHECK_LAUNCH();
@@ -369,7 +377,7 @@ csahca_status topk_launch(const float* scores, int64_t stride, int R, const int6
             return CSAHCA_ERR_CUDA;
         attr_set[dev] = true;
     }
-    topk_finish_kernel<<<R, kFinishThreads, kFinishSmem, stream>>>(scores, stride, n_vis_arr, q_pos, m, Ncap, k,
+    (void)launch_pdl(topk_finish_kernel, dim3(R), dim3(kFinishThreads), kFinishSmem, stream, scores, stride, n_vis_arr, q_pos, m, Ncap, k,
                                                                    tw.hist1, tw.thr1, tw.cand, tw.cand_n, tw.win,
                                                                    tw.tie, tw.words, idx_out);
     count_launch();
