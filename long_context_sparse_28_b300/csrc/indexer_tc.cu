@@ -56,12 +56,18 @@ constexpr int kTerm = 1, kLast = 2;   // stage flags: no more work / last stage 
 enum : uint32_t { kE4M3 = 0, kE2M1 = 5 };   // kind::f8f6f4 operand formats
 constexpr float kLoScale = 0.03125f;         // lo rows of the query operand carry 32 x the remainder
 
+constexpr int kSchedRows = 256;       // balanced piece schedule for up to this many query rows
+
 struct alignas(16) IdxMisc {
-    uint32_t hist[2048];                  // top-12-bit histogram of the item's scores: bin b is the
-                                          // 16-bit half (b & 1) of word b >> 1 (<= 2048 per item)
+    alignas(16) uint32_t hist[2048];      // top-12-bit histogram of the item's scores: bin b is the
+                                          // 16-bit half (b & 1) of word b >> 1 (<= 2048 per item);
+                                          // read and cleared as uint4
     uint64_t full[kMaxNS], empty[kMaxNS], dfull[2], dfree[2], qfree[2];
     uint32_t tmem_base;
+    int soff[kSchedRows + 1];             // piece schedule: first stage of each row (producer only)
+    int nvis[kSchedRows];                 // and its visible entries
 };
+static_assert(offsetof(IdxMisc, hist) % 16 == 0 && offsetof(IdxMisc, full) % 8 == 0, "IdxMisc alignment");
 
 template <int FMT, int HI>
 struct Cfg {
@@ -203,50 +209,97 @@ __global__ void __launch_bounds__(kThreads) index_tc_kernel(const __grid_constan
     if (warp == 4) {
         // ======================================================================== producer
         const uint64_t pol_stream = l2_policy_evict_first();     // codes are read once per step
-        // candidate item, one ahead: its q_pos and (small HI) its query row are loaded early
-        int c_item = (int)blockIdx.x;
-        int64_t c_p = 0;
-        uint4 c_raw[kUnits][4];
-        auto prefetch = [&](int it) {
-            c_item = it;
-            if (it < items) {
-                const int rr = it % R;
-                c_p = q_pos[rr];
-                if (C::prefetch_q) load_q_raw<HI>(q_idx + (int64_t)rr * HI * kDI, lane, c_raw);
-            }
-        };
-        prefetch(c_item);
-        uint32_t u = 0;                       // stages issued
-        for (uint32_t it = 0;; ++it) {
-            // next non-empty item
-            int r = 0;
-            int64_t n = 0, s0 = 0, s_end = 0;
-            uint4 raw[kUnits][4];
-            bool found = false;
-            while (c_item < items) {
-                const int item = c_item;
-                const int64_t p = c_p;
-                r = item % R;
-                if (C::prefetch_q) {
-#pragma unroll
-                    for (int j = 0; j < kUnits; ++j)
-#pragma unroll
-                        for (int c = 0; c < 4; ++c) raw[j][c] = c_raw[j][c];
+        // Work pieces (row r, its visible count n, stage range [s0, s_end) of 256 keys each),
+        // produced one ahead.  Few rows: the rows' stages, concatenated, are cut into gridDim.x
+        // equal ranges and a CTA streams its range (a piece per row it overlaps).  Otherwise:
+        // (row, chunk of kChunkStages stages) items, round-robin over the CTAs.
+        const bool balanced = R <= kSchedRows;
+        int lo = 0, hi = 0, brow = 0;
+        if (balanced) {
+            int carry = 0;
+            for (int base = 0; base < R; base += 32) {
+                const int q = base + lane;
+                int ns = 0;
+                if (q < R) {
+                    const int64_t p = q_pos[q];
+                    int64_t nn = (p >= 0) ? (p + 1) / m : 0;
+                    nn = nn < Ncap ? nn : Ncap;
+                    ms.nvis[q] = (int)nn;
+                    ns = (int)((nn + kPair - 1) / kPair);
                 }
-                prefetch(item + (int)gridDim.x);
-                int64_t nn = (p >= 0) ? (p + 1) / m : 0;
-                nn = nn < Ncap ? nn : Ncap;
-                s0 = (int64_t)(item / R) * kChunkStages * kPair;
-                if (s0 < nn) {
-                    n = nn;
+                int x = ns;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const int y = __shfl_up_sync(0xffffffffu, x, o);
+                    if (lane >= o) x += y;
+                }
+                if (q < R) ms.soff[q + 1] = carry + x;
+                carry += __shfl_sync(0xffffffffu, x, 31);
+            }
+            if (lane == 0) ms.soff[0] = 0;
+            __syncwarp();
+            const int len = (carry + (int)gridDim.x - 1) / (int)gridDim.x;
+            lo = (int)blockIdx.x * len;
+            hi = min(carry, lo + len);
+        }
+        int c_item = (int)blockIdx.x;          // round-robin cursor
+        bool c_ok = false;                      // candidate next piece
+        int c_r = 0;
+        int64_t c_n = 0, c_s0 = 0, c_send = 0, c_p = 0;
+        uint4 c_raw[kUnits][4];
+        auto fetch_next = [&]() {               // fills the candidate; blocking only when round-robin
+            c_ok = false;
+            if (balanced) {
+                for (; brow < R; ++brow) {
+                    const int st0 = ms.soff[brow], st1 = ms.soff[brow + 1];
+                    if (st0 >= hi) break;
+                    if (st1 <= lo || st1 == st0) continue;
+                    c_r = brow;
+                    c_n = ms.nvis[brow];
+                    c_s0 = (int64_t)(max(lo, st0) - st0) * kPair;
+                    const int64_t e = (int64_t)(min(hi, st1) - st0) * kPair;
+                    c_send = e < c_n ? e : c_n;
+                    c_ok = true;
+                    ++brow;
+                    break;
+                }
+            } else {
+                for (; c_item < items; c_item += gridDim.x) {
+                    const int rr = c_item % R;
+                    const int64_t p = (c_item == (int)blockIdx.x) ? q_pos[rr] : c_p;
+                    int64_t nn = (p >= 0) ? (p + 1) / m : 0;
+                    nn = nn < Ncap ? nn : Ncap;
+                    const int64_t s0 = (int64_t)(c_item / R) * kChunkStages * kPair;
+                    const int nxt = c_item + (int)gridDim.x;
+                    c_p = nxt < items ? q_pos[nxt % R] : 0;          // the next candidate's position
+                    if (s0 >= nn) continue;
                     const int64_t e = s0 + (int64_t)kChunkStages * kPair;
-                    s_end = e < nn ? e : nn;
-                    found = true;
+                    c_r = rr;
+                    c_n = nn;
+                    c_s0 = s0;
+                    c_send = e < nn ? e : nn;
+                    c_ok = true;
+                    c_item = nxt;
                     break;
                 }
             }
-            if (!found) break;
-            // query slot of this item: free once the MMAs and epilogue of item it-2 are done
+            if (c_ok && C::prefetch_q) load_q_raw<HI>(q_idx + (int64_t)c_r * HI * kDI, lane, c_raw);
+        };
+        fetch_next();
+        uint32_t u = 0;                       // stages issued
+        for (uint32_t it = 0; c_ok; ++it) {
+            const int r = c_r;
+            const int64_t n = c_n, s_end = c_send;
+            int64_t s0 = c_s0;
+            uint4 raw[kUnits][4];
+            if (C::prefetch_q) {
+#pragma unroll
+                for (int j = 0; j < kUnits; ++j)
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) raw[j][c] = c_raw[j][c];
+            }
+            fetch_next();
+            // query slot of this piece: free once the MMAs and epilogue of piece it-2 are done
             const uint32_t qs = it & 1;
             if (it >= 2) mbar_wait(&ms.qfree[qs], ((it >> 1) + 1) & 1, err);
             if (!C::prefetch_q) load_q_raw<HI>(q_idx + (int64_t)r * HI * kDI, lane, raw);
@@ -264,7 +317,7 @@ __global__ void __launch_bounds__(kThreads) index_tc_kernel(const __grid_constan
             }
             fence_proxy_async();
             __syncwarp();
-            // stages of the item (one lane)
+            // stages of the piece (one lane)
             if (lane == 0) {
                 const int b = r / T;
                 for (; s0 < s_end; s0 += kPair, ++u) {
