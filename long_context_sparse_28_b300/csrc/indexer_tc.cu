@@ -410,54 +410,111 @@ __global__ void __launch_bounds__(kThreads) index_tc_kernel(const __grid_constan
             const float4* wq4 = reinterpret_cast<const float4*>(sm + C::off_qslots + qs * C::q_slot + C::q_img);
             const uint32_t dbuf = tmem + d * C::d_cols + lane_off;
             // per key: pairs of heads (h, h+1) in f32x2 lanes; the fp4 block scales and the lo
-            // factor 2^-5 are broadcast pairs
+            // factor 2^-5 are broadcast pairs.  When the stage's accumulators fit in registers
+            // they are all loaded first and the TMEM buffer is handed back to the MMA warp before
+            // the arithmetic.
             uint64_t acc2[2] = {f2_pack(0.0f, 0.0f), f2_pack(0.0f, 0.0f)};
+            if constexpr (C::d_cols <= 128) {
+                uint32_t dv[C::d_cols];
 #pragma unroll
-            for (int key = 0; key < 2; ++key) {
-                const float s0 = key ? so0 : se0, s1 = key ? so1 : se1;
-                const uint64_t S0 = f2_pack(s0, s0), S0l = f2_pack(s0 * kLoScale, s0 * kLoScale);
-                const uint64_t S1 = f2_pack(s1, s1), S1l = f2_pack(s1 * kLoScale, s1 * kLoScale);
-                const uint64_t Ll = f2_pack(kLoScale, kLoScale);
-                const uint32_t abase = dbuf + key * C::nacc * C::acc_cols;
+                for (int c = 0; c < (int)C::d_cols; c += 16) {
+                    uint32_t t16[16];
+                    tmem_ld16(dbuf + c, t16);
 #pragma unroll
-                for (int c0 = 0; c0 < HI; c0 += 16) {
-                    uint64_t wv[8];
+                    for (int k = 0; k < 16; ++k) dv[c + k] = t16[k];
+                }
+                tmem_wait_ld();
+                fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&ms.dfree[d]);
 #pragma unroll
-                    for (int k4 = 0; k4 < 4; ++k4) {
-                        const float4 q4 = wq4[c0 / 4 + k4];
-                        wv[2 * k4] = f2_pack(q4.x, q4.y);
-                        wv[2 * k4 + 1] = f2_pack(q4.z, q4.w);
-                    }
-                    uint32_t h0[16], l0[16];
-                    tmem_ld16(abase + c0, h0);
-                    tmem_ld16(abase + HI + c0, l0);
-                    if (C::fp4) {
-                        uint32_t h1[16], l1[16];
-                        tmem_ld16(abase + C::acc_cols + c0, h1);
-                        tmem_ld16(abase + C::acc_cols + HI + c0, l1);
-                        tmem_wait_ld();
+                for (int key = 0; key < 2; ++key) {
+                    const float s0 = key ? so0 : se0, s1 = key ? so1 : se1;
+                    const uint64_t S0 = f2_pack(s0, s0), S0l = f2_pack(s0 * kLoScale, s0 * kLoScale);
+                    const uint64_t S1 = f2_pack(s1, s1), S1l = f2_pack(s1 * kLoScale, s1 * kLoScale);
+                    const uint64_t Ll = f2_pack(kLoScale, kLoScale);
+                    const int ab = key * C::nacc * (int)C::acc_cols;
 #pragma unroll
-                        for (int k = 0; k < 16; k += 2) {
-                            uint64_t v = f2_mul(S0l, f2_pack(__uint_as_float(l0[k]), __uint_as_float(l0[k + 1])));
-                            v = f2_fma(S0, f2_pack(__uint_as_float(h0[k]), __uint_as_float(h0[k + 1])), v);
-                            v = f2_fma(S1l, f2_pack(__uint_as_float(l1[k]), __uint_as_float(l1[k + 1])), v);
-                            v = f2_fma(S1, f2_pack(__uint_as_float(h1[k]), __uint_as_float(h1[k + 1])), v);
-                            float a0, a1;
-                            f2_unpack(v, a0, a1);
-                            acc2[key] = f2_fma(wv[k / 2], f2_pack(fmaxf(a0, 0.0f), fmaxf(a1, 0.0f)), acc2[key]);
+                    for (int c0 = 0; c0 < HI; c0 += 16) {
+                        uint64_t wv[8];
+#pragma unroll
+                        for (int k4 = 0; k4 < 4; ++k4) {
+                            const float4 q4 = wq4[c0 / 4 + k4];
+                            wv[2 * k4] = f2_pack(q4.x, q4.y);
+                            wv[2 * k4 + 1] = f2_pack(q4.z, q4.w);
                         }
-                    } else {
-                        tmem_wait_ld();
 #pragma unroll
                         for (int k = 0; k < 16; k += 2) {
-                            const uint64_t v = f2_fma(Ll, f2_pack(__uint_as_float(l0[k]), __uint_as_float(l0[k + 1])),
-                                                      f2_pack(__uint_as_float(h0[k]), __uint_as_float(h0[k + 1])));
+                            const int h = ab + c0 + k, l = h + HI;
+                            uint64_t v;
+                            if (C::fp4) {
+                                const int h1 = h + (int)C::acc_cols, l1 = h1 + HI;
+                                v = f2_mul(S0l, f2_pack(__uint_as_float(dv[l]), __uint_as_float(dv[l + 1])));
+                                v = f2_fma(S0, f2_pack(__uint_as_float(dv[h]), __uint_as_float(dv[h + 1])), v);
+                                v = f2_fma(S1l, f2_pack(__uint_as_float(dv[l1]), __uint_as_float(dv[l1 + 1])), v);
+                                v = f2_fma(S1, f2_pack(__uint_as_float(dv[h1]), __uint_as_float(dv[h1 + 1])), v);
+                            } else {
+                                v = f2_fma(Ll, f2_pack(__uint_as_float(dv[l]), __uint_as_float(dv[l + 1])),
+                                           f2_pack(__uint_as_float(dv[h]), __uint_as_float(dv[h + 1])));
+                            }
                             float a0, a1;
                             f2_unpack(v, a0, a1);
                             acc2[key] = f2_fma(wv[k / 2], f2_pack(fmaxf(a0, 0.0f), fmaxf(a1, 0.0f)), acc2[key]);
                         }
                     }
                 }
+            } else {
+#pragma unroll
+                for (int key = 0; key < 2; ++key) {
+                    const float s0 = key ? so0 : se0, s1 = key ? so1 : se1;
+                    const uint64_t S0 = f2_pack(s0, s0), S0l = f2_pack(s0 * kLoScale, s0 * kLoScale);
+                    const uint64_t S1 = f2_pack(s1, s1), S1l = f2_pack(s1 * kLoScale, s1 * kLoScale);
+                    const uint64_t Ll = f2_pack(kLoScale, kLoScale);
+                    const uint32_t abase = dbuf + key * C::nacc * C::acc_cols;
+#pragma unroll
+                    for (int c0 = 0; c0 < HI; c0 += 16) {
+                        uint64_t wv[8];
+#pragma unroll
+                        for (int k4 = 0; k4 < 4; ++k4) {
+                            const float4 q4 = wq4[c0 / 4 + k4];
+                            wv[2 * k4] = f2_pack(q4.x, q4.y);
+                            wv[2 * k4 + 1] = f2_pack(q4.z, q4.w);
+                        }
+                        uint32_t h0[16], l0[16];
+                        tmem_ld16(abase + c0, h0);
+                        tmem_ld16(abase + HI + c0, l0);
+                        if (C::fp4) {
+                            uint32_t h1[16], l1[16];
+                            tmem_ld16(abase + C::acc_cols + c0, h1);
+                            tmem_ld16(abase + C::acc_cols + HI + c0, l1);
+                            tmem_wait_ld();
+#pragma unroll
+                            for (int k = 0; k < 16; k += 2) {
+                                uint64_t v = f2_mul(S0l, f2_pack(__uint_as_float(l0[k]), __uint_as_float(l0[k + 1])));
+                                v = f2_fma(S0, f2_pack(__uint_as_float(h0[k]), __uint_as_float(h0[k + 1])), v);
+                                v = f2_fma(S1l, f2_pack(__uint_as_float(l1[k]), __uint_as_float(l1[k + 1])), v);
+                                v = f2_fma(S1, f2_pack(__uint_as_float(h1[k]), __uint_as_float(h1[k + 1])), v);
+                                float a0, a1;
+                                f2_unpack(v, a0, a1);
+                                acc2[key] = f2_fma(wv[k / 2], f2_pack(fmaxf(a0, 0.0f), fmaxf(a1, 0.0f)), acc2[key]);
+                            }
+                        } else {
+                            tmem_wait_ld();
+#pragma unroll
+                            for (int k = 0; k < 16; k += 2) {
+                                const uint64_t v = f2_fma(Ll, f2_pack(__uint_as_float(l0[k]), __uint_as_float(l0[k + 1])),
+                                                          f2_pack(__uint_as_float(h0[k]), __uint_as_float(h0[k + 1])));
+                                float a0, a1;
+                                f2_unpack(v, a0, a1);
+                                acc2[key] = f2_fma(wv[k / 2], f2_pack(fmaxf(a0, 0.0f), fmaxf(a1, 0.0f)), acc2[key]);
+                            }
+                        }
+                    }
+                }
+
+                fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&ms.dfree[d]);
             }
             float acc_e, acc_o;
             {
@@ -471,13 +528,9 @@ __global__ void __launch_bounds__(kThreads) index_tc_kernel(const __grid_constan
                 acc_e *= se0;
                 acc_o *= so0;
             }
-            // accumulators and (at the item's end) query slot consumed
-            fence_before_sync();
+            // (at the piece's end) query slot consumed
             __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(&ms.dfree[d]);
-                if (meta.w & kLast) mbar_arrive(&ms.qfree[qs]);
-            }
+            if (lane == 0 && (meta.w & kLast)) mbar_arrive(&ms.qfree[qs]);
             const int64_t key = (int64_t)meta.y + 2 * tid;
             const bool v0 = key < meta.z, v1 = key + 1 < meta.z;
             float* dst = S + (int64_t)meta.x * Ncap + key;
