@@ -38,12 +38,20 @@ using namespace tc;
 
 constexpr int kKeys = 128;                 // keys per tile (MMA M)
 constexpr int kD = 128;                    // head dim
-constexpr int kSoft = 256;                 // softmax / load threads: two warpgroups
-constexpr int kThreads = kSoft + 32;       // + the MMA warp
+constexpr int kHG = 16;                    // heads per softmax warpgroup (one tcgen05.ld of 16 columns)
 constexpr uint32_t kHalf = kKeys * 128;    // [128 rows][64 bf16] swizzled half tile: 16 KB
 constexpr uint32_t kTile = 2 * kHalf;      // one K or V tile: 32 KB
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 constexpr int kSchedRows = 256;            // piece schedule for up to this many query rows
+
+// Softmax / load threads: one warpgroup (128 threads, one per key row) per 16 heads; then the
+// MMA warp.
+template <int H>
+struct Thr {
+    static_assert(H % kHG == 0, "heads in groups of 16");
+    static constexpr int kSoft = (H / kHG) * kKeys;
+    static constexpr int kThreads = kSoft + 32;
+};
 
 template <int H>
 struct Smem {
@@ -61,8 +69,9 @@ struct alignas(16) Misc {
     uint64_t kfull[2], vfull[2], sdone[2], odone, pready;
     uint32_t tmem_base;
     int flag[2];                     // per tile (ring of 2): some running maximum moved
-    alignas(16) float red[8][32];
+    alignas(16) float red[16][32];
     alignas(16) float mrun[64];      // read as float4
+    alignas(16) float mold[64];      // running maxima before the tile's update (float4)
     alignas(16) float alpha[64];     // read as float4
     float linv[64];
     unsigned char valid[4][kKeys];   // per tile (ring of 4): row holds a key of this query
@@ -71,7 +80,8 @@ struct alignas(16) Misc {
     int my_slots_from;               // without tiles whose slots it marks empty (or -1), and
     int64_t my_p;                    // the query position of its row
 };
-static_assert(offsetof(Misc, mrun) % 16 == 0 && offsetof(Misc, alpha) % 16 == 0, "float4 fields");
+static_assert(offsetof(Misc, mrun) % 16 == 0 && offsetof(Misc, mold) % 16 == 0 && offsetof(Misc, alpha) % 16 == 0,
+              "float4 fields");
 
 struct ItemTiles {
     int r, b, nt_c, t0, nt, slot;
@@ -84,24 +94,24 @@ struct Maps {
 };
 
 template <int H>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(Thr<H>::kThreads, 1)
     attend_tc_kernel(AttendArgs a, int S, int kps, const __grid_constant__ Maps maps, int use_tma_c, int use_tma_w,
                      float* __restrict__ o_part, float* __restrict__ lse_part, unsigned* err) {
-    pdl_wait();
-    pdl_trigger();
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                          ~uintptr_t(1023));
     __shared__ Misc ms;
     using L = Smem<H>;
+    constexpr int kSoft = Thr<H>::kSoft;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     constexpr uint32_t kCols = (3 * H <= 128) ? 128 : 256;   // S[2] + O
 
+    // TMEM and barriers touch no global memory: set up while the preceding kernel finishes
     if (warp == 0) {
         tmem_alloc(&ms.tmem_base, kCols);
         tmem_relinquish();
     }
-    if (tid == 0) {
+    if (tid == 32) {
         for (int i = 0; i < 2; ++i) {
             mbar_init(&ms.kfull[i], kSoft);
             mbar_init(&ms.vfull[i], kSoft);
@@ -112,6 +122,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(&ms.pready, kSoft / 32);
         fence_mbar_init();
     }
+    pdl_wait();
+    pdl_trigger();
     const int R = a.B * a.T;
     const int items = R * S;
     const int tps = kps / kKeys;
@@ -279,7 +291,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
     } else {
         // ==================================================================== softmax warps
-        constexpr int HG = H / 2;                   // heads per warpgroup
+        constexpr int HG = kHG;                     // heads per warpgroup
         const int wg = warp >> 2;                   // warpgroup: heads [wg*HG, wg*HG + HG)
         const int row = tid & (kKeys - 1);          // key row of S^T / dim row of O^T = TMEM lane
         const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
@@ -335,8 +347,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tma_load_2d(dst, mp, 0, y, bar, pol_stream);
                         tma_load_2d(dst + kHalf, mp, 64, y, bar, pol_stream);
                     }
-                } else {   // two threads per row, one 64-column half each
-                    const int rr = tid >> 1, half = tid & 1;
+                } else {   // kSoft / 128 threads per row, each an equal share of its 16-byte chunks
+                    constexpr int kTpr = kSoft / kKeys;
+                    constexpr int kCpt = 16 / kTpr;
+                    const int rr = tid / kTpr, part = tid % kTpr;
                     int64_t key;
                     bool in;
                     if (comp) {
@@ -349,12 +363,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const __nv_bfloat16* kp = nullptr;
                     const __nv_bfloat16* vp = nullptr;
                     if (in) key_rows<__nv_bfloat16>(a, kl, r, b, p, key, &kp, &vp, err);
-                    if (!is_v && half == 0) ms.valid[seq & 3][rr] = kp != nullptr;
+                    if (!is_v && part == 0) ms.valid[seq & 3][rr] = kp != nullptr;
                     const __nv_bfloat16* src = is_v ? vp : kp;
 #pragma unroll
-                    for (int c = 0; c < 8; ++c) {
-                        const uint32_t d = dst + half * kHalf + sw128(rr, c);
-                        if (src) cp_async16_hint(d, src + half * 64 + c * 8, 16, pol_stream);
+                    for (int c = 0; c < kCpt; ++c) {
+                        const int cc = part * kCpt + c;              // chunk of the row: half cc / 8
+                        const uint32_t d = dst + (cc >> 3) * kHalf + sw128(rr, cc & 7);
+                        if (src) cp_async16_hint(d, src + cc * 8, 16, pol_stream);
                         else cp_async16(d, qr, 0);                   // zero fill (no bytes read)
                     }
                 }
@@ -380,45 +395,66 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int ti = t0 + i;
                 mbar_wait(&ms.sdone[seq & 1], (seq >> 1) & 1, err);
                 fence_after_sync();
-                // The S tile is read from TMEM in chunks of 16 heads (raw scores; invalid rows -inf),
-                // once per pass, so no pass holds more than 16 scores.
+                // Each thread holds one key row of this warpgroup's 16 heads (raw scores; rows that
+                // are not keys of the query give p = 0).
                 const bool valid = ms.valid[seq & 3][row] != 0;
                 const uint32_t scol = tmem + (seq & 1) * H + wg * HG + lane_off;
+                // P buffer (i & 1): its last reader PV(i-2) precedes MMA1(i) and is complete
+                const uint32_t prow = sbase + L::p + (seq & 1) * L::p_bytes + ((wg * HG / 8) >> 3) * L::p_region;
+                const int pchunk = (wg * HG / 8) & 7;                 // 8 heads per 16-byte chunk
+                auto store_p = [&](const uint32_t* pk) {
+#pragma unroll
+                    for (int c = 0; c < 2; ++c)
+                        asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(prow + sw128(row, pchunk + c)),
+                                     "r"(pk[4 * c]), "r"(pk[4 * c + 1]), "r"(pk[4 * c + 2]), "r"(pk[4 * c + 3])
+                                     : "memory");
+                };
                 // K slot of tile i is free (MMA1(i) complete)
                 if (i + 2 < nt) load_tile(i + 2, false);
-                // ---- running maxima: only when some score of the tile exceeds its head's running
-                // maximum by more than the threshold (always on an item's first tile) are the tile's
-                // per-head maxima formed: a warp reduction per head, then a 4-way merge
-                bool need = false;
-#pragma unroll
-                for (int c0 = 0; c0 < HG; c0 += 16) {
-                    uint32_t rr[16];
-                    tmem_ld16(scol + c0, rr);
+                // ---- P = 2^(s c - m) with the running maxima m, exponents capped at the threshold.
+                // When some score exceeds its head's running maximum by more than the threshold
+                // (always on an item's first tile, which skips this pass) the maxima are raised
+                // and P is formed again below.
+                bool grow = true;
+                if (i > 0) {
+                    uint32_t rr[16], pk[8];
+                    tmem_ld16(scol, rr);
                     tmem_wait_ld();
+                    bool need = false;
 #pragma unroll
                     for (int k = 0; k < 16; k += 4) {
-                        const float4 m4 = *reinterpret_cast<const float4*>(&ms.mrun[wg * HG + c0 + k]);
-                        need |= (__uint_as_float(rr[k]) * c_log2 > m4.x + kRescaleThreshold) |
-                                (__uint_as_float(rr[k + 1]) * c_log2 > m4.y + kRescaleThreshold) |
-                                (__uint_as_float(rr[k + 2]) * c_log2 > m4.z + kRescaleThreshold) |
-                                (__uint_as_float(rr[k + 3]) * c_log2 > m4.w + kRescaleThreshold);
+                        const float4 m4 = *reinterpret_cast<const float4*>(&ms.mrun[wg * HG + k]);
+                        const float mm[4] = {m4.x, m4.y, m4.z, m4.w};
+                        float pp[4];
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            const float x = __uint_as_float(rr[k + u]) * c_log2;
+                            need |= x > mm[u] + kRescaleThreshold;
+                            pp[u] = (mm[u] == -INFINITY || !valid) ? 0.0f
+                                                                   : ex2_approx(fminf(x - mm[u], kRescaleThreshold));
+                            lsum[k + u] += pp[u];
+                        }
+                        pk[k / 2] = pack_bf16x2(pp[0], pp[1]);
+                        pk[k / 2 + 1] = pack_bf16x2(pp[2], pp[3]);
                     }
+                    store_p(pk);
+                    grow = named_barrier_or(1, kSoft, need && valid);
                 }
-                need = need && valid;
-                const bool grow = named_barrier_or(1, kSoft, need);
-                if (tid == 0) ms.flag[(seq + 1) & 1] = 0;   // everyone is done with tile i-1's flag
+                // everyone is done with tile i-1's flag (the barrier above, or on an item's first
+                // tile the previous item's closing barriers)
+                if (tid == 0) ms.flag[(seq + 1) & 1] = 0;
                 bool rescale = false;
                 if (grow) {
+                    // tile maxima per head: a warp reduction, then a 4-way merge over the warpgroup
                     float mine = -INFINITY;
-#pragma unroll
-                    for (int c0 = 0; c0 < HG; c0 += 16) {
+                    {
                         uint32_t rr[16];
-                        tmem_ld16(scol + c0, rr);
+                        tmem_ld16(scol, rr);
                         tmem_wait_ld();
 #pragma unroll
                         for (int k = 0; k < 16; ++k) {
                             const float mx = redux_max_f32(valid ? __uint_as_float(rr[k]) : -INFINITY);
-                            mine = (lane == c0 + k) ? mx : mine;
+                            mine = (lane == k) ? mx : mine;
                         }
                     }
                     ms.red[warp][lane] = mine;
@@ -435,52 +471,39 @@ __global__ void __launch_bounds__(kThreads, 1)
                             ms.mrun[tid] = tmax;
                             ms.flag[seq & 1] = 1;
                         }
+                        ms.mold[tid] = mo;
                         ms.alpha[tid] = al;
                     }
                     named_barrier_sync(1, kSoft);
                     rescale = ms.flag[seq & 1] != 0;
-                }
-                // ---- P = 2^(s c - m) into P buffer (i & 1) ([key][head], 128-byte swizzle; PV(i-2),
-                // its last reader, is complete), row sums
-                const uint32_t pbuf = sbase + L::p + (seq & 1) * L::p_bytes;
-#pragma unroll
-                for (int c0 = 0; c0 < HG; c0 += 16) {
-                    uint32_t rr[16];
-                    tmem_ld16(scol + c0, rr);
+                    // P again with the new maxima; the row sums drop the first pass's term
+                    // (recomputed exactly as it was added) and are rescaled
+                    uint32_t rr[16], pk[8];
+                    tmem_ld16(scol, rr);
                     tmem_wait_ld();
-                    uint32_t pk[8];
 #pragma unroll
                     for (int k = 0; k < 16; k += 4) {
-                        const int h = wg * HG + c0 + k;
+                        const int h = wg * HG + k;
                         const float4 m4 = *reinterpret_cast<const float4*>(&ms.mrun[h]);
-                        const float mm[4] = {m4.x, m4.y, m4.z, m4.w};
+                        const float4 o4 = *reinterpret_cast<const float4*>(&ms.mold[h]);
+                        const float4 a4 = *reinterpret_cast<const float4*>(&ms.alpha[h]);
+                        const float mn[4] = {m4.x, m4.y, m4.z, m4.w};
+                        const float mo[4] = {o4.x, o4.y, o4.z, o4.w};
+                        const float al[4] = {a4.x, a4.y, a4.z, a4.w};
                         float pp[4];
 #pragma unroll
-                        for (int u = 0; u < 4; ++u)
-                            pp[u] = (mm[u] == -INFINITY || !valid)
-                                        ? 0.0f
-                                        : ex2_approx(fmaf(__uint_as_float(rr[k + u]), c_log2, -mm[u]));
-                        if (rescale) {
-                            const float4 a4 = *reinterpret_cast<const float4*>(&ms.alpha[h]);
-                            lsum[c0 + k] = fmaf(lsum[c0 + k], a4.x, pp[0]);
-                            lsum[c0 + k + 1] = fmaf(lsum[c0 + k + 1], a4.y, pp[1]);
-                            lsum[c0 + k + 2] = fmaf(lsum[c0 + k + 2], a4.z, pp[2]);
-                            lsum[c0 + k + 3] = fmaf(lsum[c0 + k + 3], a4.w, pp[3]);
-                        } else {
-#pragma unroll
-                            for (int u = 0; u < 4; ++u) lsum[c0 + k + u] += pp[u];
+                        for (int u = 0; u < 4; ++u) {
+                            const float x = __uint_as_float(rr[k + u]) * c_log2;
+                            const float pold = (i == 0 || mo[u] == -INFINITY || !valid)
+                                                   ? 0.0f
+                                                   : ex2_approx(fminf(x - mo[u], kRescaleThreshold));
+                            pp[u] = (mn[u] == -INFINITY || !valid) ? 0.0f : ex2_approx(x - mn[u]);
+                            lsum[k + u] = fmaf(lsum[k + u] - pold, al[u], pp[u]);
                         }
                         pk[k / 2] = pack_bf16x2(pp[0], pp[1]);
                         pk[k / 2 + 1] = pack_bf16x2(pp[2], pp[3]);
                     }
-#pragma unroll
-                    for (int c = 0; c < 2; ++c) {
-                        const int chunk = (wg * HG + c0) / 8 + c;        // 8 heads per 16-byte chunk
-                        const uint32_t dst = pbuf + (chunk >> 3) * L::p_region + sw128(row, chunk & 7);
-                        asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(dst), "r"(pk[4 * c]),
-                                     "r"(pk[4 * c + 1]), "r"(pk[4 * c + 2]), "r"(pk[4 * c + 3])
-                                     : "memory");
-                    }
+                    store_p(pk);
                 }
                 // ---- PV(i-1) done: O and the V slot of tile i-1 are free
                 if (i > 0) {
@@ -601,7 +624,7 @@ cudaError_t launch_tc(const AttendArgs& a, int S, int kps, float* o_part, float*
     if (e != cudaSuccess) return e;
     const int items = a.B * a.T * S;
     const int grid = items < num_sms() ? items : num_sms();
-    (void)launch_pdl(kern, dim3(grid), dim3(kThreads), smem, st, a, S, kps, maps, use_c, use_w, o_part, lse_part, err);
+    (void)launch_pdl(kern, dim3(grid), dim3(Thr<H>::kThreads), smem, st, a, S, kps, maps, use_c, use_w, o_part, lse_part, err);
     return cudaGetLastError();
 }
 
