@@ -75,6 +75,7 @@ struct alignas(16) Misc {
     alignas(16) float alpha[64];     // read as float4
     float linv[64];
     unsigned char valid[4][kKeys];   // per tile (ring of 4): row holds a key of this query
+    int snt[kSchedRows];             // piece schedule: tiles of each query row
     int my_row, my_piece, my_t0, my_nt;  // piece schedule: this CTA's piece (row -1: none), its
     int my_empty_row;                // row's slots [my_slots_from, S) it marks empty, a row
     int my_slots_from;               // without tiles whose slots it marks empty (or -1), and
@@ -93,9 +94,126 @@ struct Maps {
     CUtensorMap ck, cv, rk, rv;
 };
 
+// Piece schedule, computed by one warp (no more query rows than CTAs, S >= 2 partial slots per
+// row): every row is cut into ceil(tiles / L) pieces of near-equal length, L the smallest length
+// >= the average tiles per CTA for which all pieces fit the grid and no row has more than S
+// pieces; CTA c takes the c-th piece (row by row), whose partial result goes to slot = piece
+// index.  Kept out of line: it runs once per CTA and its code should not crowd the tile loop.
+__device__ __noinline__ void piece_schedule(const AttendArgs& a, int S, int nt_w, Misc& ms, int lane) {
+    const int R = a.B * a.T;
+    const int G = (int)gridDim.x, c = (int)blockIdx.x;
+    int total = 0, ntmax = 0;
+#pragma unroll 1
+    for (int q = lane; q < R; q += 32) {
+        const int n = (int)cdiv(key_list(a, q, 0, a.q_pos[q]).n_c, kKeys) + nt_w;
+        ms.snt[q] = n;
+        total += n;
+        ntmax = max(ntmax, n);
+    }
+    for (int o = 16; o > 0; o >>= 1) {
+        total += __shfl_xor_sync(0xffffffffu, total, o);
+        ntmax = max(ntmax, __shfl_xor_sync(0xffffffffu, ntmax, o));
+    }
+    __syncwarp();
+    int len = max(max((int)cdiv(total, G), (int)cdiv(ntmax, S)), 1);
+    for (;;) {                                      // usually one or two rounds
+        int cnt = 0;
+#pragma unroll 1
+        for (int q = lane; q < R; q += 32) cnt += (ms.snt[q] + len - 1) / len;
+        for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
+        if (cnt <= G) break;
+        ++len;
+    }
+    if (lane == 0) {
+        ms.my_row = -1;
+        ms.my_slots_from = S;
+        ms.my_empty_row = -1;
+    }
+    __syncwarp();
+    // first CTA of each row: exclusive prefix of the piece counts, rows in order
+    int carry = 0;
+#pragma unroll 1
+    for (int q0 = 0; q0 < R; q0 += 32) {
+        const int q = q0 + lane;
+        const int nt = q < R ? ms.snt[q] : 0;
+        const int np = (nt + len - 1) / len;
+        int x = np;
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, x, o);
+            if (lane >= o) x += y;
+        }
+        const int first = carry + x - np;
+        carry += __shfl_sync(0xffffffffu, x, 31);
+        if (q < R && np > 0 && c >= first && c < first + np) {
+            const int piece = c - first;
+            const int t0 = piece * nt / np;
+            ms.my_row = q;
+            ms.my_piece = piece;
+            ms.my_t0 = t0;
+            ms.my_nt = (piece + 1) * nt / np - t0;
+            ms.my_p = a.q_pos[q];
+            if (piece == 0) ms.my_slots_from = np;
+        }
+        if (q < R && np == 0 && q == c) ms.my_empty_row = q;   // R <= gridDim.x
+    }
+}
+
+// One K (is_v = false) or V tile -- keys [ti * 128, ti * 128 + 128) of query row r's tile space --
+// into shared memory at `dst`; completion on `bar` counts kSoft arrivals plus the TMA bytes.
+// Called by all kSoft loading threads.  For a K tile, valid[row] records whether the row holds a
+// key of the query.  A tile of contiguous rows with a tensor map is two 2-D TMA boxes issued by
+// thread 0; otherwise the rows are gathered with cp.async (kSoft / 128 threads per row).  With
+// `track_cp` every thread's arrival waits for all its earlier cp.async copies (the query tile
+// loaded just before), else a TMA tile's arrivals are made at once by thread 0.
+template <int kSoft>
+__device__ __forceinline__ void load_tile(const AttendArgs& a, const Maps& maps, int use_tma_c, int use_tma_w, int r,
+                                       int b, int64_t p, int64_t n_c, int64_t total, int nt_c, int ti, bool is_v,
+                                       uint32_t dst, uint64_t* bar, unsigned char* valid, const void* zsrc,
+                                       uint64_t pol, bool track_cp, unsigned* err) {
+    const int tid = threadIdx.x;
+    const bool comp = ti < nt_c;
+    if (comp ? use_tma_c : use_tma_w) {
+        if (!is_v && tid < kKeys) {
+            // ring slot `tid` of the decode window holds token t = tid (mod 128) of the last 128
+            valid[tid] = comp ? ((int64_t)ti * kKeys + tid < n_c) : (p - ((p - tid) & (kKeys - 1)) >= 0);
+        }
+        if (tid == 0) {
+            mbar_expect_tx(bar, kTile);
+            const CUtensorMap* mp = comp ? (is_v ? &maps.cv : &maps.ck) : (is_v ? &maps.rv : &maps.rk);
+            const int y = comp ? (int)((int64_t)b * a.Ncap + (int64_t)ti * kKeys) : b * a.ring_cap;
+            tma_load_2d(dst, mp, 0, y, bar, pol);
+            tma_load_2d(dst + kHalf, mp, 64, y, bar, pol);
+            if (!track_cp) mbar_arrive_cnt(bar, kSoft);     // the arrivals of all loading threads
+        }
+        if (track_cp) cp_async_arrive_noinc(bar);
+        return;
+    }
+    constexpr int kTpr = kSoft / kKeys;
+    constexpr int kCpt = 16 / kTpr;
+    const int rr = tid / kTpr, part = tid % kTpr;
+    const int64_t key = comp ? (int64_t)ti * kKeys + rr : n_c + (int64_t)(ti - nt_c) * kKeys + rr;
+    const bool in = key < (comp ? n_c : total);
+    const __nv_bfloat16* kp = nullptr;
+    const __nv_bfloat16* vp = nullptr;
+    KeyList kl;
+    kl.n_c = n_c;
+    kl.total = total;
+    if (in) key_rows<__nv_bfloat16>(a, kl, r, b, p, key, &kp, &vp, err);
+    if (!is_v && part == 0) valid[rr] = kp != nullptr;
+    const __nv_bfloat16* src = is_v ? vp : kp;
+#pragma unroll
+    for (int c = 0; c < kCpt; ++c) {
+        const int cc = part * kCpt + c;              // 16-byte chunk of the row: half cc / 8
+        const uint32_t d = dst + (cc >> 3) * kHalf + sw128(rr, cc & 7);
+        if (src) cp_async16_hint(d, src + cc * 8, 16, pol);
+        else cp_async16(d, zsrc, 0);                 // zero fill (no bytes read)
+    }
+    cp_async_arrive_noinc(bar);
+}
+
 template <int H>
 __global__ void __launch_bounds__(Thr<H>::kThreads, 1)
-    attend_tc_kernel(AttendArgs a, int S, int kps, const __grid_constant__ Maps maps, int use_tma_c, int use_tma_w,
+    attend_tc_kernel(const __grid_constant__ AttendArgs a, int S, int kps, const __grid_constant__ Maps maps, int use_tma_c, int use_tma_w,
                      float* __restrict__ o_part, float* __restrict__ lse_part, unsigned* err) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -128,81 +246,10 @@ __global__ void __launch_bounds__(Thr<H>::kThreads, 1)
     const int items = R * S;
     const int tps = kps / kKeys;
     const int nt_w = (int)cdiv(a.W, kKeys);
-    // Piece schedule (no more query rows than CTAs, S >= 2 partial slots per row): every row is
-    // cut into ceil(tiles / L) pieces of near-equal length, L the smallest length >= the average
-    // tiles per CTA for which all pieces fit the grid and no row has more than S pieces; CTA c
-    // takes the c-th piece (row by row), whose partial result goes to slot = piece index.
-    // Otherwise items are (row, split) pairs, split s holding tiles [s kps, (s+1) kps).
+    // With few query rows each CTA takes one piece of one row (piece_schedule); otherwise items
+    // are (row, split) pairs, split s holding tiles [s kps, (s+1) kps).
     const bool pieces = R <= kSchedRows && R <= (int)gridDim.x && S >= 2;
-    if (pieces && warp == 0) {
-        constexpr int kPer = kSchedRows / 32;
-        int nt[kPer];
-        int64_t pq[kPer];
-        int total = 0, ntmax = 0;
-#pragma unroll
-        for (int j = 0; j < kPer; ++j) {
-            const int q = lane + 32 * j;
-            nt[j] = 0;
-            pq[j] = -1;
-            if (q < R) {
-                pq[j] = a.q_pos[q];
-                nt[j] = (int)cdiv(key_list(a, q, 0, pq[j]).n_c, kKeys) + nt_w;
-            }
-            total += nt[j];
-            ntmax = max(ntmax, nt[j]);
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            total += __shfl_xor_sync(0xffffffffu, total, o);
-            ntmax = max(ntmax, __shfl_xor_sync(0xffffffffu, ntmax, o));
-        }
-        int len = max(max((int)cdiv(total, gridDim.x), (int)cdiv(ntmax, S)), 1);
-        int np[kPer];
-        for (;;) {                                  // usually one or two rounds
-            int cnt = 0;
-#pragma unroll
-            for (int j = 0; j < kPer; ++j) {
-                np[j] = 32 * j < R ? (nt[j] + len - 1) / len : 0;
-                cnt += np[j];
-            }
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
-            if (cnt <= (int)gridDim.x) break;
-            ++len;
-        }
-        // first CTA of each row: exclusive prefix of the piece counts, rows in order
-        int carry = 0;
-        if (lane == 0) {
-            ms.my_row = -1;
-            ms.my_slots_from = S;
-            ms.my_empty_row = -1;
-        }
-        __syncwarp();
-        const int c = (int)blockIdx.x;
-#pragma unroll
-        for (int j = 0; j < kPer; ++j) {
-            const int q = lane + 32 * j;
-            int x = np[j];
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int y = __shfl_up_sync(0xffffffffu, x, o);
-                if (lane >= o) x += y;
-            }
-            const int first = carry + x - np[j];
-            carry += __shfl_sync(0xffffffffu, x, 31);
-            if (q < R && np[j] > 0 && c >= first && c < first + np[j]) {
-                const int piece = c - first;
-                const int t0 = piece * nt[j] / np[j];
-                ms.my_row = q;
-                ms.my_piece = piece;
-                ms.my_t0 = t0;
-                ms.my_nt = (piece + 1) * nt[j] / np[j] - t0;
-                ms.my_p = pq[j];
-                if (piece == 0) ms.my_slots_from = np[j];
-            }
-            if (q < R && np[j] == 0 && q == c) ms.my_empty_row = q;   // R <= gridDim.x
-        }
-    }
+    if (pieces && warp == 0) piece_schedule(a, S, nt_w, ms, lane);
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
@@ -254,36 +301,37 @@ __global__ void __launch_bounds__(Thr<H>::kThreads, 1)
             for (int cur = cur0; next_item(cur, it);) {
                 const int nt = it.nt;
                 if (nt == 0) continue;
-                auto qk = [&](int i) {       // S^T(i) = K(i) . Q^T into S buffer (g + i) & 1
-                    const uint32_t seq = g + (uint32_t)i;
-                    mbar_wait(&ms.kfull[seq & 1], (seq >> 1) & 1, err);
-                    fence_proxy_async();
-                    fence_after_sync();
-                    const uint64_t k_desc = smem_desc(sbase + L::k + (seq & 1) * kTile, 16, 1024);
-                    const uint32_t sb = tmem + (seq & 1) * H;
+                // step s: PV(s - 2) (s >= 2), then MMA1(s) (s < nt)
+#pragma unroll 1
+                for (int st = 0; st < nt + 2; ++st) {
+                    if (st >= 2) {              // O^T += V^T . P(i)
+                        const int i = st - 2;
+                        const uint32_t seq = g + (uint32_t)i;
+                        mbar_wait(&ms.pready, seq & 1, err);
+                        mbar_wait(&ms.vfull[seq & 1], (seq >> 1) & 1, err);
+                        fence_proxy_async();
+                        fence_after_sync();
+                        const uint64_t v_desc = smem_desc(sbase + L::v + (seq & 1) * kTile, kHalf, 1024);
+                        const uint64_t pb_desc = p_desc + (uint64_t)(((seq & 1) * L::p_bytes) >> 4);
 #pragma unroll
-                    for (int j = 0; j < 8; ++j)
-                        mma_ss(sb, k_desc + (uint64_t)(((j >> 2) * kHalf + (j & 3) * 32) >> 4),
-                               q_desc + (uint64_t)(((j >> 2) * L::q_half + (j & 3) * 32) >> 4), id_qk, j > 0);
-                    mma_commit(&ms.sdone[seq & 1]);
-                };
-                qk(0);
-                if (nt > 1) qk(1);
-                for (int i = 0; i < nt; ++i) {
-                    const uint32_t seq = g + (uint32_t)i;
-                    mbar_wait(&ms.pready, seq & 1, err);
-                    mbar_wait(&ms.vfull[seq & 1], (seq >> 1) & 1, err);
-                    fence_proxy_async();
-                    fence_after_sync();
-                    // O^T += V^T . P
-                    const uint64_t v_desc = smem_desc(sbase + L::v + (seq & 1) * kTile, kHalf, 1024);
-                    const uint64_t pb_desc = p_desc + (uint64_t)(((seq & 1) * L::p_bytes) >> 4);
+                        for (int j = 0; j < 8; ++j)
+                            mma_ss(t_o, v_desc + (uint64_t)((j * 2048) >> 4), pb_desc + (uint64_t)((j * 2048) >> 4),
+                                   id_pv, (i > 0 || j > 0) ? 1u : 0u);
+                        mma_commit(&ms.odone);
+                    }
+                    if (st < nt) {              // S^T(st) = K(st) . Q^T into S buffer (g + st) & 1
+                        const uint32_t seq = g + (uint32_t)st;
+                        mbar_wait(&ms.kfull[seq & 1], (seq >> 1) & 1, err);
+                        fence_proxy_async();
+                        fence_after_sync();
+                        const uint64_t k_desc = smem_desc(sbase + L::k + (seq & 1) * kTile, 16, 1024);
+                        const uint32_t sb = tmem + (seq & 1) * H;
 #pragma unroll
-                    for (int j = 0; j < 8; ++j)
-                        mma_ss(t_o, v_desc + (uint64_t)((j * 2048) >> 4), pb_desc + (uint64_t)((j * 2048) >> 4), id_pv,
-                               (i > 0 || j > 0) ? 1u : 0u);
-                    mma_commit(&ms.odone);
-                    if (i + 2 < nt) qk(i + 2);
+                        for (int j = 0; j < 8; ++j)
+                            mma_ss(sb, k_desc + (uint64_t)(((j >> 2) * kHalf + (j & 3) * 32) >> 4),
+                                   q_desc + (uint64_t)(((j >> 2) * L::q_half + (j & 3) * 32) >> 4), id_qk, j > 0);
+                        mma_commit(&ms.sdone[seq & 1]);
+                    }
                 }
                 g += (uint32_t)nt;
             }
@@ -301,9 +349,11 @@ __global__ void __launch_bounds__(Thr<H>::kThreads, 1)
 
         if (pieces && tid < H) {    // partial slots no piece of this schedule writes: lse = -inf
             if (ms.my_row >= 0)
+#pragma unroll 1
                 for (int sl = ms.my_slots_from; sl < S; ++sl)
                     lse_part[((int64_t)ms.my_row * S + sl) * H + tid] = -INFINITY;
             if (ms.my_empty_row >= 0)
+#pragma unroll 1
                 for (int sl = 0; sl < S; ++sl) lse_part[((int64_t)ms.my_empty_row * S + sl) * H + tid] = -INFINITY;
         }
         ItemTiles it;
@@ -315,81 +365,37 @@ __global__ void __launch_bounds__(Thr<H>::kThreads, 1)
             const __nv_bfloat16* qr = static_cast<const __nv_bfloat16*>(a.q) + (int64_t)r * H * kD;
 
             if (nt == 0) {
+#pragma unroll 1
                 for (int i = tid; i < H * kD; i += kSoft) o_part[obase * kD + i] = 0.0f;
                 if (tid < H) lse_part[obase + tid] = -INFINITY;
                 continue;
             }
             if (tid < H) ms.mrun[tid] = -INFINITY;
 
-            // K (is_v = false) or V of item tile i into its ring slot; called by all softmax
-            // threads.  Tile i's loads are the (g + i)-th of each ring, so slot = (g + i) & 1.
-            auto load_tile = [&](int i, bool is_v) {
-                const int ti = t0 + i;
+            // Tile i's loads are the (g + i)-th of each ring, so slot = (g + i) & 1.
+            auto load = [&](int i, bool is_v) {
                 const uint32_t seq = g + (uint32_t)i;
-                uint64_t* bar = is_v ? &ms.vfull[seq & 1] : &ms.kfull[seq & 1];
-                const uint32_t dst = sbase + (is_v ? L::v : L::k) + (seq & 1) * kTile;
-                const bool comp = ti < nt_c;
-                if (comp ? use_tma_c : use_tma_w) {
-                    if (!is_v && tid < kKeys) {
-                        bool valid;
-                        if (comp) {
-                            valid = (int64_t)ti * kKeys + tid < kl.n_c;
-                        } else {   // ring slot `tid` holds the token t = tid (mod 128) of the last 128
-                            const int64_t back = ((p - tid) % kKeys + kKeys) % kKeys;
-                            valid = p - back >= 0;
-                        }
-                        ms.valid[seq & 3][tid] = valid;
-                    }
-                    if (tid == 0) {
-                        mbar_expect_tx(bar, kTile);
-                        const CUtensorMap* mp = comp ? (is_v ? &maps.cv : &maps.ck) : (is_v ? &maps.rv : &maps.rk);
-                        const int y = comp ? (int)((int64_t)b * a.Ncap + (int64_t)ti * kKeys) : b * a.ring_cap;
-                        tma_load_2d(dst, mp, 0, y, bar, pol_stream);
-                        tma_load_2d(dst + kHalf, mp, 64, y, bar, pol_stream);
-                    }
-                } else {   // kSoft / 128 threads per row, each an equal share of its 16-byte chunks
-                    constexpr int kTpr = kSoft / kKeys;
-                    constexpr int kCpt = 16 / kTpr;
-                    const int rr = tid / kTpr, part = tid % kTpr;
-                    int64_t key;
-                    bool in;
-                    if (comp) {
-                        key = (int64_t)ti * kKeys + rr;
-                        in = key < kl.n_c;
-                    } else {
-                        key = kl.n_c + (int64_t)(ti - nt_c) * kKeys + rr;
-                        in = key < kl.total;
-                    }
-                    const __nv_bfloat16* kp = nullptr;
-                    const __nv_bfloat16* vp = nullptr;
-                    if (in) key_rows<__nv_bfloat16>(a, kl, r, b, p, key, &kp, &vp, err);
-                    if (!is_v && part == 0) ms.valid[seq & 3][rr] = kp != nullptr;
-                    const __nv_bfloat16* src = is_v ? vp : kp;
-#pragma unroll
-                    for (int c = 0; c < kCpt; ++c) {
-                        const int cc = part * kCpt + c;              // chunk of the row: half cc / 8
-                        const uint32_t d = dst + (cc >> 3) * kHalf + sw128(rr, cc & 7);
-                        if (src) cp_async16_hint(d, src + cc * 8, 16, pol_stream);
-                        else cp_async16(d, qr, 0);                   // zero fill (no bytes read)
-                    }
-                }
-                cp_async_arrive_noinc(bar);
+                load_tile<kSoft>(a, maps, use_tma_c, use_tma_w, r, b, p, kl.n_c, kl.total, nt_c, t0 + i, is_v,
+                                 sbase + (is_v ? L::v : L::k) + (seq & 1) * kTile,
+                                 is_v ? &ms.vfull[seq & 1] : &ms.kfull[seq & 1], ms.valid[seq & 3], qr, pol_stream,
+                                 i == 0 && !is_v, err);
             };
 
-            // ---- prologue: Q, K(0), K(1), V(0) in flight (Q lands before K(0) completes)
+            // ---- prologue: Q, K(0), K(1), V(0) in flight (K(0) completes only once Q has landed)
             for (int c = tid; c < H * 16; c += kSoft) {
                 const int h = c >> 4, cc = c & 15;
                 cp_async16(sbase + L::q + (cc >> 3) * L::q_half + sw128(h, cc & 7), qr + h * kD + cc * 8, 16);
             }
-            load_tile(0, false);
-            if (nt > 1) load_tile(1, false);
-            load_tile(0, true);
+            load(0, false);
+            if (nt > 1) load(1, false);
+            load(0, true);
             named_barrier_sync(1, kSoft);                  // valid[] of tiles 0 and 1
 
             float lsum[HG];
 #pragma unroll
             for (int h = 0; h < HG; ++h) lsum[h] = 0.0f;
 
+#pragma unroll 1
             for (int i = 0; i < nt; ++i) {
                 const uint32_t seq = g + (uint32_t)i;
                 const int ti = t0 + i;
@@ -410,7 +416,7 @@ __global__ void __launch_bounds__(Thr<H>::kThreads, 1)
                                      : "memory");
                 };
                 // K slot of tile i is free (MMA1(i) complete)
-                if (i + 2 < nt) load_tile(i + 2, false);
+                if (i + 2 < nt) load(i + 2, false);
                 // ---- P = 2^(s c - m) with the running maxima m, exponents capped at the threshold.
                 // When some score exceeds its head's running maximum by more than the threshold
                 // (always on an item's first tile, which skips this pass) the maxima are raised
@@ -510,7 +516,7 @@ __global__ void __launch_bounds__(Thr<H>::kThreads, 1)
                     mbar_wait(&ms.odone, (seq - 1) & 1, err);
                     fence_after_sync();
                 }
-                if (i + 1 < nt) load_tile(i + 1, true);
+                if (i + 1 < nt) load(i + 1, true);
                 // ---- rescale the O^T accumulator (lane = dim) when some running maximum moved
                 if (rescale && i > 0) {
 #pragma unroll
