@@ -32,7 +32,8 @@
 //              when they fit in the 512 columns);
 //   warps 0-3  epilogue: thread j owns TMEM lane j (keys 2j and 2j+1 of the stage): scores to
 //              global memory, and the top-12-bit histogram of the scores (the top-k's first pass),
-//              accumulated per item in shared memory and added to the row's global histogram.
+//              accumulated in shared memory (16-bit counts) and added to the row's global
+//              histogram at the end of each item and every 128 stages.
 #include "common.cuh"
 #include "tc_ptx.cuh"
 #include "tmap.cuh"
@@ -52,16 +53,19 @@ constexpr int kChunkStages = 8;       // stages per work item: 2048 keys of one 
 constexpr int kMaxNS = 6;             // shared-memory stages (at most)
 constexpr int kEpi = 128;             // epilogue threads (warps 0-3)
 constexpr int kThreads = kEpi + 64;   // + producer warp + MMA warp
-constexpr int kTerm = 1, kLast = 2;   // stage flags: no more work / last stage of an item
+// stage flags: no more work / last stage of an item / add the shared histogram to the global one
+// (every kFlushStages stages, so that no 16-bit count can overflow)
+constexpr int kTerm = 1, kLast = 2, kFlush = 4;
+constexpr int kFlushStages = 128;     // 32768 keys
 enum : uint32_t { kE4M3 = 0, kE2M1 = 5 };   // kind::f8f6f4 operand formats
 constexpr float kLoScale = 0.03125f;         // lo rows of the query operand carry 32 x the remainder
 
 constexpr int kSchedRows = 256;       // balanced piece schedule for up to this many query rows
 
 struct alignas(16) IdxMisc {
-    alignas(16) uint32_t hist[2048];      // top-12-bit histogram of the item's scores: bin b is the
-                                          // 16-bit half (b & 1) of word b >> 1 (<= 2048 per item);
-                                          // read and cleared as uint4
+    alignas(16) uint32_t hist[2048];      // top-12-bit histogram of the scores since the last flush:
+                                          // bin b is the 16-bit half (b & 1) of word b >> 1 (at most
+                                          // 128 x 256 keys per flush); read and cleared as uint4
     uint64_t full[kMaxNS], empty[kMaxNS], dfull[2], dfree[2], qfree[2];
     uint32_t tmem_base;
     int soff[kSchedRows + 1];             // piece schedule: first stage of each row (producer only)
@@ -320,12 +324,13 @@ __global__ void __launch_bounds__(kThreads) index_tc_kernel(const __grid_constan
             // stages of the piece (one lane)
             if (lane == 0) {
                 const int b = r / T;
-                for (; s0 < s_end; s0 += kPair, ++u) {
+                for (int j = 0; s0 < s_end; s0 += kPair, ++u, ++j) {
                     const uint32_t s = u % C::NS;
                     if (u >= (uint32_t)C::NS) mbar_wait(&ms.empty[s], ((u / C::NS) + 1) & 1, err);
                     unsigned char* st = sm + s * C::stage;
                     const uint32_t sb = sbase + s * C::stage;
-                    const int flags = ((s0 + kPair >= s_end) ? kLast : 0) | (int)(qs << 8);
+                    const int flags = ((s0 + kPair >= s_end) ? kLast : 0) |
+                                      ((j % kFlushStages == kFlushStages - 1) ? kFlush : 0) | (int)(qs << 8);
                     *reinterpret_cast<int4*>(st + C::off_meta) = make_int4(r, (int)s0, (int)n, flags);
                     const int64_t key0 = (int64_t)b * Ncap + s0;
                     const int64_t nk = (Ncap - s0) < kPair ? (Ncap - s0) : kPair;   // Ncap % 8 == 0
@@ -545,7 +550,7 @@ __global__ void __launch_bounds__(kThreads) index_tc_kernel(const __grid_constan
                     const uint32_t bin = ordered_key(acc_o) >> 20;
                     atomicAdd(&ms.hist[bin >> 1], 1u << ((bin & 1) * 16));
                 }
-                if (meta.w & kLast) {                     // item done: add to the row's histogram
+                if (meta.w & (kLast | kFlush)) {          // add to the row's histogram
                     named_barrier_sync(1, kEpi);
                     uint32_t* gh = hist1 + (int64_t)meta.x * 4096;
                     for (int i = 4 * tid; i < 2048; i += 4 * kEpi) {   // words of two 16-bit counts

@@ -172,6 +172,30 @@ def test_index_scores_and_topk_parity(fmt, q_dt, Ncap, H_I):
             check_index_set(npy(idx[b, t]), ref[t], S[t], int(nv[t]), k, f"b{b}t{t}")
 
 
+@pytest.mark.parametrize("fmt", ["e2m1", "e4m3"])
+def test_index_topk_one_bin_over_65536_keys_per_cta(fmt):
+    # 80 rows of 250000 identical index keys: all scores of a row are equal, so the exact top-k
+    # is the first k entries (ties to the lower index) and every key of a row lands in one
+    # histogram bin.  The tensor-core indexer's CTAs then stream more than 65536 keys of one row
+    # each, which its 16-bit shared-memory counts only survive by being flushed in between.
+    B, Ncap, d_I, H_I, m, k = 80, 250000, 64, 16, 4, 1024
+    F = L.KEY_FMT[fmt]
+    one = rnd((1, 8, d_I), torch.bfloat16, 31)
+    c1, s1 = L.key_storage(1, 8, d_I, F)
+    L.csa_index_key_quantize(one, F, c1, s1)
+    codes, scales = L.key_storage(B, Ncap, d_I, F)
+    codes.copy_(c1[:, :1].expand_as(codes))
+    scales.copy_(s1[:, :1].expand_as(scales))
+    q = rnd((B, 1, H_I, d_I), torch.bfloat16, 32, 0.125)
+    w = torch.rand(B, 1, H_I, generator=torch.Generator().manual_seed(33)).cuda()
+    pos = dev_i64([m * Ncap - 1] * B)
+    idx = torch.empty(B, 1, k, dtype=torch.int32, device="cuda")
+    L.csa_index_topk(q, w, codes, scales, F, pos, m, k, idx)
+    torch.cuda.synchronize()
+    assert L.device_status() == 0
+    np.testing.assert_array_equal(npy(idx).reshape(B, k), np.broadcast_to(np.arange(k, dtype=np.int32), (B, k)))
+
+
 # ------------------------------------------------------------------------ a7/a8 attention
 def _rand_cache(B, Ncap, W, d, dt, seed):
     ck = rnd((B, Ncap, d), DT[dt], seed)
