@@ -32,8 +32,8 @@
 //              when they fit in the 512 columns);
 //   warps 0-3  epilogue: thread j owns TMEM lane j (keys 2j and 2j+1 of the stage): scores to
 //              global memory, and the top-12-bit histogram of the scores (the top-k's first pass),
-//              accumulated in shared memory (16-bit counts) and added to the row's global
-//              histogram at the end of each item and every 128 stages.
+//              accumulated per piece in shared memory (16-bit counts; a piece has at most 128
+//              stages) and added to the row's global histogram.
 #include "common.cuh"
 #include "tc_ptx.cuh"
 #include "tmap.cuh"
@@ -53,10 +53,9 @@ constexpr int kChunkStages = 8;       // stages per work item: 2048 keys of one 
 constexpr int kMaxNS = 6;             // shared-memory stages (at most)
 constexpr int kEpi = 128;             // epilogue threads (warps 0-3)
 constexpr int kThreads = kEpi + 64;   // + producer warp + MMA warp
-// stage flags: no more work / last stage of an item / add the shared histogram to the global one
-// (every kFlushStages stages, so that no 16-bit count can overflow)
-constexpr int kTerm = 1, kLast = 2, kFlush = 4;
-constexpr int kFlushStages = 128;     // 32768 keys
+constexpr int kTerm = 1, kLast = 2;   // stage flags: no more work / last stage of a piece
+// Longest piece: its keys' histogram is kept in 16-bit shared-memory counts until the piece ends
+constexpr int kMaxPieceStages = 128;  // 32768 keys
 enum : uint32_t { kE4M3 = 0, kE2M1 = 5 };   // kind::f8f6f4 operand formats
 constexpr float kLoScale = 0.03125f;         // lo rows of the query operand carry 32 x the remainder
 
@@ -65,7 +64,7 @@ constexpr int kSchedRows = 256;       // balanced piece schedule for up to this 
 struct alignas(16) IdxMisc {
     alignas(16) uint32_t hist[2048];      // top-12-bit histogram of the scores since the last flush:
                                           // bin b is the 16-bit half (b & 1) of word b >> 1 (at most
-                                          // 128 x 256 keys per flush); read and cleared as uint4
+                                          // kMaxPieceStages x 256 keys); read and cleared as uint4
     uint64_t full[kMaxNS], empty[kMaxNS], dfull[2], dfree[2], qfree[2];
     uint32_t tmem_base;
     int soff[kSchedRows + 1];             // piece schedule: first stage of each row (producer only)
@@ -215,10 +214,12 @@ __global__ void __launch_bounds__(kThreads) index_tc_kernel(const __grid_constan
         const uint64_t pol_stream = l2_policy_evict_first();     // codes are read once per step
         // Work pieces (row r, its visible count n, stage range [s0, s_end) of 256 keys each),
         // produced one ahead.  Few rows: the rows' stages, concatenated, are cut into gridDim.x
-        // equal ranges and a CTA streams its range (a piece per row it overlaps).  Otherwise:
-        // (row, chunk of kChunkStages stages) items, round-robin over the CTAs.
+        // equal ranges and a CTA streams its range (a piece per row it overlaps, split into
+        // pieces of at most kMaxPieceStages stages).  Otherwise: (row, chunk of kChunkStages
+        // stages) items, round-robin over the CTAs.
         const bool balanced = R <= kSchedRows;
         int lo = 0, hi = 0, brow = 0;
+        int64_t bnext = 0;                      // balanced: next key of row brow to stream
         if (balanced) {
             int carry = 0;
             for (int base = 0; base < R; base += 32) {
@@ -254,17 +255,25 @@ __global__ void __launch_bounds__(kThreads) index_tc_kernel(const __grid_constan
         auto fetch_next = [&]() {               // fills the candidate; blocking only when round-robin
             c_ok = false;
             if (balanced) {
-                for (; brow < R; ++brow) {
+                for (; brow < R; ++brow, bnext = 0) {
                     const int st0 = ms.soff[brow], st1 = ms.soff[brow + 1];
                     if (st0 >= hi) break;
                     if (st1 <= lo || st1 == st0) continue;
                     c_r = brow;
                     c_n = ms.nvis[brow];
-                    c_s0 = (int64_t)(max(lo, st0) - st0) * kPair;
+                    const int64_t b0 = (int64_t)(max(lo, st0) - st0) * kPair;
                     const int64_t e = (int64_t)(min(hi, st1) - st0) * kPair;
-                    c_send = e < c_n ? e : c_n;
+                    const int64_t end = e < c_n ? e : c_n;
+                    c_s0 = bnext > b0 ? bnext : b0;
+                    const int64_t cap = c_s0 + (int64_t)kMaxPieceStages * kPair;
+                    c_send = end < cap ? end : cap;
                     c_ok = true;
-                    ++brow;
+                    if (c_send < end) {
+                        bnext = c_send;                 // the rest of this row's range follows
+                    } else {
+                        ++brow;
+                        bnext = 0;
+                    }
                     break;
                 }
             } else {
@@ -324,13 +333,12 @@ __global__ void __launch_bounds__(kThreads) index_tc_kernel(const __grid_constan
             // stages of the piece (one lane)
             if (lane == 0) {
                 const int b = r / T;
-                for (int j = 0; s0 < s_end; s0 += kPair, ++u, ++j) {
+                for (; s0 < s_end; s0 += kPair, ++u) {
                     const uint32_t s = u % C::NS;
                     if (u >= (uint32_t)C::NS) mbar_wait(&ms.empty[s], ((u / C::NS) + 1) & 1, err);
                     unsigned char* st = sm + s * C::stage;
                     const uint32_t sb = sbase + s * C::stage;
-                    const int flags = ((s0 + kPair >= s_end) ? kLast : 0) |
-                                      ((j % kFlushStages == kFlushStages - 1) ? kFlush : 0) | (int)(qs << 8);
+                    const int flags = ((s0 + kPair >= s_end) ? kLast : 0) | (int)(qs << 8);
                     *reinterpret_cast<int4*>(st + C::off_meta) = make_int4(r, (int)s0, (int)n, flags);
                     const int64_t key0 = (int64_t)b * Ncap + s0;
                     const int64_t nk = (Ncap - s0) < kPair ? (Ncap - s0) : kPair;   // Ncap % 8 == 0
@@ -550,7 +558,7 @@ __global__ void __launch_bounds__(kThreads) index_tc_kernel(const __grid_constan
                     const uint32_t bin = ordered_key(acc_o) >> 20;
                     atomicAdd(&ms.hist[bin >> 1], 1u << ((bin & 1) * 16));
                 }
-                if (meta.w & (kLast | kFlush)) {          // add to the row's histogram
+                if (meta.w & kLast) {                     // piece done: add to the row's histogram
                     named_barrier_sync(1, kEpi);
                     uint32_t* gh = hist1 + (int64_t)meta.x * 4096;
                     for (int i = 4 * tid; i < 2048; i += 4 * kEpi) {   // words of two 16-bit counts
