@@ -128,7 +128,8 @@ __global__ void __launch_bounds__(256) attend_split_kernel(AttendArgs a, int kps
 }
 
 // One warp per (query, head): lanes first turn the S partial log-sum-exps into merge weights
-// (max-subtracted, fixed order), then stream the S partial outputs with 16-byte loads.
+// (max-subtracted, fixed order), then stream the S partial outputs with 16-byte loads, four
+// splits in flight at a time.
 constexpr int kMergeWarps = 8;
 
 template <typename T>
@@ -143,33 +144,69 @@ __global__ void __launch_bounds__(32 * kMergeWarps) merge_kernel(int R, int S, i
     if (gw >= (int64_t)R * H) return;
     const int r = (int)(gw / H), h = (int)(gw % H);
     const float* lp = lse_part + (int64_t)r * S * H + h;
-    float mx = -INFINITY;
-    for (int s = lane; s < S; s += 32) mx = fmaxf(mx, __ldg(lp + (int64_t)s * H));
-    mx = warp_max(mx);
-    float tot = 0.0f;
-    for (int s = lane; s < S; s += 32) {
-        const float ls = __ldg(lp + (int64_t)s * H);
-        tot += (ls == -INFINITY || mx == -INFINITY) ? 0.0f : expf(ls - mx);
-    }
-    tot = warp_sum(tot);
-    const float inv = tot > 0.0f ? 1.0f / tot : 0.0f;
-    for (int c0 = lane * 4; c0 < d; c0 += 128) {
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int s = 0; s < S; ++s) {
-            const float ls = __ldg(lp + (int64_t)s * H);
-            if (ls == -INFINITY) continue;
-            const float e = expf(ls - mx) * inv;
-            const float4 o = __ldg(reinterpret_cast<const float4*>(o_part + (((int64_t)r * S + s) * H + h) * d + c0));
-            acc.x = fmaf(e, o.x, acc.x);
-            acc.y = fmaf(e, o.y, acc.y);
-            acc.z = fmaf(e, o.z, acc.z);
-            acc.w = fmaf(e, o.w, acc.w);
+    const float* op0 = o_part + ((int64_t)r * S * H + h) * d;
+    float mx = -INFINITY, tot = 0.0f;
+    if (S <= 32) {
+        // split s's lse and weight live in lane s; slots without keys (lse = -inf) get weight 0
+        // and their (unwritten) partial output is never used
+        const float ls = lane < S ? __ldg(lp + (int64_t)lane * H) : -INFINITY;
+        mx = warp_max(ls);
+        const float e = (ls == -INFINITY || mx == -INFINITY) ? 0.0f : expf(ls - mx);
+        tot = warp_sum(e);
+        const float wl = tot > 0.0f ? e / tot : 0.0f;
+        for (int c0 = lane * 4; c0 < d; c0 += 128) {
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int s0 = 0; s0 < S; s0 += 4) {
+                float4 o[4];
+                float ws[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    ws[u] = __shfl_sync(0xffffffffu, wl, (s0 + u) & 31);
+                    ws[u] = s0 + u < S ? ws[u] : 0.0f;
+                    o[u] = ws[u] != 0.0f ? __ldg(reinterpret_cast<const float4*>(op0 + (int64_t)(s0 + u) * H * d + c0))
+                                         : make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    acc.x = fmaf(ws[u], o[u].x, acc.x);
+                    acc.y = fmaf(ws[u], o[u].y, acc.y);
+                    acc.z = fmaf(ws[u], o[u].z, acc.z);
+                    acc.w = fmaf(ws[u], o[u].w, acc.w);
+                }
+            }
+            T* op = out + ((int64_t)r * H + h) * d + c0;
+            from_f32(op[0], acc.x);
+            from_f32(op[1], acc.y);
+            from_f32(op[2], acc.z);
+            from_f32(op[3], acc.w);
         }
-        T* op = out + ((int64_t)r * H + h) * d + c0;
-        from_f32(op[0], acc.x);
-        from_f32(op[1], acc.y);
-        from_f32(op[2], acc.z);
-        from_f32(op[3], acc.w);
+    } else {
+        for (int s = lane; s < S; s += 32) mx = fmaxf(mx, __ldg(lp + (int64_t)s * H));
+        mx = warp_max(mx);
+        for (int s = lane; s < S; s += 32) {
+            const float ls = __ldg(lp + (int64_t)s * H);
+            tot += (ls == -INFINITY || mx == -INFINITY) ? 0.0f : expf(ls - mx);
+        }
+        tot = warp_sum(tot);
+        const float inv = tot > 0.0f ? 1.0f / tot : 0.0f;
+        for (int c0 = lane * 4; c0 < d; c0 += 128) {
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int s = 0; s < S; ++s) {
+                const float ls = __ldg(lp + (int64_t)s * H);
+                if (ls == -INFINITY) continue;
+                const float e = expf(ls - mx) * inv;
+                const float4 o = __ldg(reinterpret_cast<const float4*>(op0 + (int64_t)s * H * d + c0));
+                acc.x = fmaf(e, o.x, acc.x);
+                acc.y = fmaf(e, o.y, acc.y);
+                acc.z = fmaf(e, o.z, acc.z);
+                acc.w = fmaf(e, o.w, acc.w);
+            }
+            T* op = out + ((int64_t)r * H + h) * d + c0;
+            from_f32(op[0], acc.x);
+            from_f32(op[1], acc.y);
+            from_f32(op[2], acc.z);
+            from_f32(op[3], acc.w);
+        }
     }
     if (lane == 0 && lse_out) lse_out[(int64_t)r * H + h] = tot > 0.0f ? mx + logf(tot) : -INFINITY;
 }

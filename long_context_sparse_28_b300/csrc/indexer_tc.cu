@@ -174,8 +174,6 @@ __global__ void __launch_bounds__(kThreads) index_tc_kernel(const __grid_constan
                                                             const int64_t* __restrict__ q_pos, int64_t Ncap, int m,
                                                             int R, float* __restrict__ S,
                                                             uint32_t* __restrict__ hist1, unsigned* err) {
-    pdl_wait();
-    pdl_trigger();
     using C = Cfg<FMT, HI>;
     constexpr int kUnits = 2 * HI / 32;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -203,6 +201,10 @@ __global__ void __launch_bounds__(kThreads) index_tc_kernel(const __grid_constan
     }
     if (tid < kEpi)
         for (int i = tid; i < 2048; i += kEpi) ms.hist[i] = 0u;
+    // TMEM, barriers and shared memory touch no global memory: set up while the preceding kernel
+    // finishes
+    pdl_wait();
+    pdl_trigger();
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
