@@ -114,7 +114,11 @@ __global__ void compress_kernel(const T* __restrict__ k_raw, const T* __restrict
 // One CTA per sequence: pool completed blocks (reading old tokens from the ring), then write
 // the new tokens into the ring.  A completed block is pooled by the whole CTA: warp 0 computes
 // the m softmax weights into shared memory, then every thread sums a subset of the m tokens for
-// 8 channels of K or V (loads unrolled), and the partial sums are added in a fixed order.
+// 8 channels of K or V, and the partial sums are added in a fixed order.  Loads that do not need
+// the weights -- a thread's tokens when its subset has at most 4, the block's index-key row
+// (warp 1) -- are issued before the weights' barrier, so a decode step's block costs about one
+// memory round trip after the position is known.  Ring slots are computed with 32-bit arithmetic
+// from one 64-bit remainder per block (ring_cap >= m - 1, so one conditional subtraction).
 constexpr int kAppendThreads = 256;
 
 template <typename T>
@@ -134,7 +138,10 @@ __global__ void __launch_bounds__(kAppendThreads) append_kernel(
         if (tid == 0) flag_error(err, ERRBIT_BOUNDS);
         return;
     }
-    const int64_t j_lo = p / m, j_hi = (p + n_new) / m;   // completed blocks: [j_lo, j_hi)
+    // completed blocks: [j_lo, j_hi) (shifts when m is a power of two)
+    const bool pow2 = (m & (m - 1)) == 0;
+    const int msh = __ffs(m) - 1;
+    const int64_t j_lo = pow2 ? (p >> msh) : p / m, j_hi = pow2 ? ((p + n_new) >> msh) : (p + n_new) / m;
     const T* kn = k_new + (int64_t)b * n_new * d;
     const T* vn = v_new + (int64_t)b * n_new * d;
     const float* gn = gate_new + (int64_t)b * n_new;
@@ -144,52 +151,77 @@ __global__ void __launch_bounds__(kAppendThreads) append_kernel(
     const int G = 2 * d / 8;                               // 8-channel groups of K then V
     const int NS = G >= kAppendThreads ? 1 : kAppendThreads / G;   // token subsets
     const int per = (m + NS - 1) / NS;
+    const int g = tid % G, ts = tid / G;
+    const int which = (g < G / 2) ? 0 : 1;
+    const int col = (g % (G / 2)) * 8;
+    const int i0 = ts * per, i1 = min(m, i0 + per);
     for (int64_t j = j_lo; j < j_hi; ++j) {
         if (j >= Ncap) {
             if (tid == 0) flag_error(err, ERRBIT_BOUNDS);
             continue;
         }
         const int64_t t0 = j * m;
+        const int t0r = (int)(t0 % ring_cap);
+        // row of token t0 + i of K (which = 0) or V: new tokens from the input, older ones from the ring
+        auto tok = [&](int i, int wh) -> const T* {
+            const int64_t t = t0 + i;
+            if (t >= p) return (wh ? vn : kn) + (t - p) * d;
+            int sl = t0r + i;
+            if (sl >= ring_cap) sl -= ring_cap;
+            return (wh ? rv : rk) + (int64_t)sl * d;
+        };
+        // loads independent of the weights first
+        float x[4][8];
+        const int nx = (ts < NS && per <= 4) ? i1 - i0 : 0;
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+            if (u < nx) load8_rw(tok(i0 + u, which) + col, x[u]);
+        float kx[8];
+        const bool quant = k_codes != nullptr && warp == 1;
+        if (quant) {
+            const int r = (int)(j - j_lo);
+            const int64_t in_bytes = (kidx_dtype == CSAHCA_F32 ? 4 : 2);
+            const char* row = static_cast<const char*>(kidx_new) + (((int64_t)b * kidx_rows + r) * d_I) * in_bytes;
+            load_row_slice(row, kidx_dtype, d_I / 32, kx);
+        }
         if (warp == 0) {
             float a[8];
             block_weights(m, [&](int i) {
                 const int64_t t = t0 + i;
-                return ((t >= p) ? gn[t - p] : rg[t % ring_cap]) + bias[i];
+                int sl = t0r + i;
+                if (sl >= ring_cap) sl -= ring_cap;
+                return ((t >= p) ? gn[t - p] : rg[sl]) + bias[i];
             }, a);
 #pragma unroll
             for (int r = 0; r < 8; ++r)
                 if (lane + 32 * r < m) alpha[lane + 32 * r] = a[r];
         }
         __syncthreads();
-        const int g = tid % G, ts = tid / G;
         float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
         if (ts < NS) {
-            const int which = (g < G / 2) ? 0 : 1;
-            const int col = (g % (G / 2)) * 8;
-            const int i0 = ts * per, i1 = min(m, i0 + per);
-            int i = i0;
-            for (; i + 4 <= i1; i += 4) {
-                float x[4][8];
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const int64_t t = t0 + i + u;
-                    const T* src = (t >= p) ? (which ? vn : kn) + (t - p) * d
-                                            : (which ? rv : rk) + (t % ring_cap) * (int64_t)d;
-                    load8_rw(src + col, x[u]);
-                }
+            if (per <= 4) {
 #pragma unroll
                 for (int u = 0; u < 4; ++u)
+                    if (u < nx)
 #pragma unroll
-                    for (int c = 0; c < 8; ++c) acc[c] = fmaf(alpha[i + u], x[u][c], acc[c]);
-            }
-            for (; i < i1; ++i) {
-                const int64_t t = t0 + i;
-                const T* src = (t >= p) ? (which ? vn : kn) + (t - p) * d
-                                        : (which ? rv : rk) + (t % ring_cap) * (int64_t)d;
-                float x[8];
-                load8_rw(src + col, x);
+                        for (int c = 0; c < 8; ++c) acc[c] = fmaf(alpha[i0 + u], x[u][c], acc[c]);
+            } else {
+                int i = i0;
+                for (; i + 4 <= i1; i += 4) {
+                    float y[4][8];
 #pragma unroll
-                for (int c = 0; c < 8; ++c) acc[c] = fmaf(alpha[i], x[c], acc[c]);
+                    for (int u = 0; u < 4; ++u) load8_rw(tok(i + u, which) + col, y[u]);
+#pragma unroll
+                    for (int u = 0; u < 4; ++u)
+#pragma unroll
+                        for (int c = 0; c < 8; ++c) acc[c] = fmaf(alpha[i + u], y[u][c], acc[c]);
+                }
+                for (; i < i1; ++i) {
+                    float y[8];
+                    load8_rw(tok(i, which) + col, y);
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) acc[c] = fmaf(alpha[i], y[c], acc[c]);
+                }
             }
         }
 #pragma unroll
@@ -200,41 +232,38 @@ __global__ void __launch_bounds__(kAppendThreads) append_kernel(
             for (int q = 0; q < NS; ++q)
 #pragma unroll
                 for (int c = 0; c < 8; ++c) o[c] += part[(q * G + tid) * 8 + c];
-            const int which = (tid < G / 2) ? 0 : 1;
-            const int col = (tid % (G / 2)) * 8;
-            store8((which ? cv : ck) + ((int64_t)b * Ncap + j) * d + col, o);
+            const int wh = (tid < G / 2) ? 0 : 1;
+            const int cl = (tid % (G / 2)) * 8;
+            store8((wh ? cv : ck) + ((int64_t)b * Ncap + j) * d + cl, o);
         }
-        if (k_codes != nullptr && warp == 1) {
-            const int r = (int)(j - j_lo);
+        if (quant) {
             const int E = d_I / 32;
-            const int64_t in_bytes = (kidx_dtype == CSAHCA_F32 ? 4 : 2);
-            const char* row = static_cast<const char*>(kidx_new) + (((int64_t)b * kidx_rows + r) * d_I) * in_bytes;
-            float x[8];
-            load_row_slice(row, kidx_dtype, E, x);
             const int64_t er = (int64_t)b * Ncap + j;
-            quantize_row_warp(x, E, d_I, key_fmt, static_cast<char*>(k_codes) + er * key_row_bytes(key_fmt, d_I),
+            quantize_row_warp(kx, E, d_I, key_fmt, static_cast<char*>(k_codes) + er * key_row_bytes(key_fmt, d_I),
                               k_scale ? static_cast<char*>(k_scale) + er * key_scale_bytes(key_fmt, d_I) : nullptr);
         }
         __syncthreads();
     }
-    // write the last min(n_new, ring_cap) tokens into the ring
+    // write the last min(n_new, ring_cap) tokens into the ring (32-bit indices: the host checks
+    // that n_new * d / 8 fits)
     const int first = n_new > ring_cap ? n_new - ring_cap : 0;
     const int vec = d / 8;
     T* wk = ring_k + (int64_t)b * ring_cap * d;
     T* wv = ring_v + (int64_t)b * ring_cap * d;
-    const int64_t items = (int64_t)(n_new - first) * vec;
-    for (int64_t it = tid; it < items; it += blockDim.x) {
-        const int i = first + (int)(it / vec);
-        const int c = (int)(it % vec) * 8;
-        const int64_t slot = (p + i) % ring_cap;
-        float x[8];
-        load8_rw(kn + (int64_t)i * d + c, x);
-        store8(wk + slot * d + c, x);
-        load8_rw(vn + (int64_t)i * d + c, x);
-        store8(wv + slot * d + c, x);
+    const int base = (int)(p % ring_cap);
+    const int items = (n_new - first) * vec;
+    for (int it = tid; it < items; it += blockDim.x) {
+        const int i = first + it / vec;
+        const int c = (it % vec) * 8;
+        const int64_t slot = (base + i) % ring_cap;
+        float y[8];
+        load8_rw(kn + (int64_t)i * d + c, y);
+        store8(wk + slot * d + c, y);
+        load8_rw(vn + (int64_t)i * d + c, y);
+        store8(wv + slot * d + c, y);
     }
     for (int i = first + tid; i < n_new; i += blockDim.x)
-        ring_gate[(int64_t)b * ring_cap + (p + i) % ring_cap] = gn[i];
+        ring_gate[(int64_t)b * ring_cap + (base + i) % ring_cap] = gn[i];
 }
 
 template <typename T>
@@ -304,6 +333,7 @@ csahca_status append_impl(const void* k_new, const void* v_new, const float* gat
                           void* k_scale, csahca_dtype key_fmt, int d_I, cudaStream_t stream) {
     CSAHCA_REQUIRE(k_new && v_new && gate_new && pos && bias && ring_k && ring_v && ring_gate && ck && cv);
     CSAHCA_REQUIRE(m >= 1 && m <= kMaxM && B >= 1 && n_new >= 0 && d >= 8 && d <= 512 && d % 8 == 0);
+    CSAHCA_REQUIRE((int64_t)n_new * (d / 8) < (1LL << 30) && (int64_t)n_new + ring_cap < (1LL << 30));
     CSAHCA_REQUIRE(ring_cap >= 1 && ring_cap >= m - 1 && Ncap >= 0);
     CSAHCA_REQUIRE(kv_dtype_ok(kv));
     const size_t al = (kv == CSAHCA_F32) ? 32 : 16;
@@ -320,7 +350,6 @@ csahca_status append_impl(const void* k_new, const void* v_new, const float* gat
     unsigned* err = err_word();
     if (!err) return CSAHCA_ERR_CUDA;
     const int kidx_rows = n_new / m + 1;
-    const int threads = 256;
     if (kv == CSAHCA_F32)
         (void)launch_pdl(append_kernel<float>, dim3(B), dim3(kAppendThreads), 0, stream, 
             (const float*)k_new, (const float*)v_new, gate_new, kidx_new, kidx_dtype, kidx_rows, pos, n_new, d,
