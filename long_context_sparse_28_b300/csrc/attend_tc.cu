@@ -28,6 +28,7 @@
 
 #include "tmap.cuh"
 
+#include <algorithm>
 #include <cstddef>
 #include <cstring>
 
@@ -214,7 +215,7 @@ __device__ __forceinline__ void load_tile(const AttendArgs& a, const Maps& maps,
 template <int H>
 __global__ void __launch_bounds__(Thr<H>::kThreads, 1)
     attend_tc_kernel(const __grid_constant__ AttendArgs a, int S, int kps, const __grid_constant__ Maps maps, int use_tma_c, int use_tma_w,
-                     float* __restrict__ o_part, float* __restrict__ lse_part, unsigned* err) {
+                     int fixed_np, float* __restrict__ o_part, float* __restrict__ lse_part, unsigned* err) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                          ~uintptr_t(1023));
@@ -249,7 +250,25 @@ __global__ void __launch_bounds__(Thr<H>::kThreads, 1)
     // With few query rows each CTA takes one piece of one row (piece_schedule); otherwise items
     // are (row, split) pairs, split s holding tiles [s kps, (s+1) kps).
     const bool pieces = R <= kSchedRows && R <= (int)gridDim.x && S >= 2;
-    if (pieces && warp == 0) piece_schedule(a, S, nt_w, ms, lane);
+    if (pieces && warp == 0) {
+        if (fixed_np > 0) {
+            // every row has the same tiles (CSA: k selected entries + the window); the host cut
+            // them into fixed_np pieces per row, so CTA c takes piece c % fixed_np of row c / fixed_np
+            if (lane == 0) {
+                const int c = (int)blockIdx.x, q = c / fixed_np, piece = c % fixed_np;
+                const int nt = (int)cdiv(a.k, kKeys) + nt_w;
+                ms.my_row = q < R ? q : -1;
+                ms.my_empty_row = -1;
+                ms.my_slots_from = piece == 0 ? fixed_np : S;
+                ms.my_piece = piece;
+                ms.my_t0 = piece * nt / fixed_np;
+                ms.my_nt = (piece + 1) * nt / fixed_np - ms.my_t0;
+                ms.my_p = q < R ? a.q_pos[q] : 0;
+            }
+        } else {
+            piece_schedule(a, S, nt_w, ms, lane);
+        }
+    }
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
@@ -628,9 +647,22 @@ cudaError_t launch_tc(const AttendArgs& a, int S, int kps, float* o_part, float*
     auto kern = attend_tc_kernel<H>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    const int items = a.B * a.T * S;
+    const int R = a.B * a.T;
+    const int items = R * S;
     const int grid = items < num_sms() ? items : num_sms();
-    (void)launch_pdl(kern, dim3(grid), dim3(Thr<H>::kThreads), smem, st, a, S, kps, maps, use_c, use_w, o_part, lse_part, err);
+    // CSA rows all hold k + W keys: the piece schedule is the same for every row and is made here
+    // (the kernel's own schedule, with all rows' tile counts equal)
+    int fixed_np = 0;
+    if (a.is_csa && R <= kSchedRows && R <= grid && S >= 2) {
+        const int nt = (int)(cdiv(a.k, kKeys) + cdiv(a.W, kKeys));
+        if (nt > 0) {
+            int len = std::max(std::max((int)cdiv((int64_t)R * nt, grid), (int)cdiv(nt, S)), 1);
+            while ((int64_t)R * cdiv(nt, len) > grid) ++len;
+            fixed_np = (int)cdiv(nt, len);
+        }
+    }
+    (void)launch_pdl(kern, dim3(grid), dim3(Thr<H>::kThreads), smem, st, a, S, kps, maps, use_c, use_w, fixed_np,
+                     o_part, lse_part, err);
     return cudaGetLastError();
 }
 
