@@ -6,12 +6,12 @@
 //   S^T[128 keys x H]  = K_tile[128 x 128] . Q^T          (A = K, K-major; B = Q, K-major)
 //   O^T[128 dims x H] += V_tile^T[128 x 128] . P[128 x H]  (A = V, MN-major; B = P, MN-major)
 // Keys are the M dimension: a thread owns one key row of S^T (tcgen05.ld 32x32b) and the V tile
-// is used as loaded.  Two warpgroups split the heads; a ninth warp only issues the MMAs (an MMA
-// issue costs the issuing thread on the order of a hundred cycles, so the softmax warps never
-// wait on it; they hand over through mbarriers).  Per tile, the per-head maximum over the
-// 128 keys is one warp reduction per head plus a 4-way shared-memory merge; the running maximum
-// is raised lazily (only when it grows by more than 2^8) and only then is the O^T accumulator in
-// TMEM rescaled; row sums stay per thread until the end of the work item.
+// is used as loaded.  One warpgroup per 16 heads forms P; one more warp only issues the MMAs
+// (16 per tile) and hands over through mbarriers, so no softmax barrier waits on MMA issue.  The
+// softmax makes one pass over S with the running maxima; only when some score exceeds its
+// head's running maximum by more than 2^8 (always on an item's first tile) are the tile maxima
+// formed, the maxima raised, P formed again and the O^T accumulator in TMEM rescaled; row sums
+// stay per thread until the end of the work item.
 //
 // Keys are addressed in tile space: the compressed keys of a query fill tiles [0, nt_c), the
 // window fills tiles [nt_c, nt_c + nt_w).  A tile whose rows are contiguous in memory (HCA
@@ -103,6 +103,49 @@ struct Maps {
 __device__ __noinline__ void piece_schedule(const AttendArgs& a, int S, int nt_w, Misc& ms, int lane) {
     const int R = a.B * a.T;
     const int G = (int)gridDim.x, c = (int)blockIdx.x;
+    if (R <= 32) {
+        // one row per lane (the decode batches): the same schedule in registers and shuffles
+        const bool in = lane < R;
+        const int64_t pq = in ? a.q_pos[lane] : 0;
+        const int nt = in ? (int)cdiv(key_list(a, lane, 0, pq).n_c, kKeys) + nt_w : 0;
+        int total = nt, ntmax = nt;
+        for (int o = 16; o > 0; o >>= 1) {
+            total += __shfl_xor_sync(0xffffffffu, total, o);
+            ntmax = max(ntmax, __shfl_xor_sync(0xffffffffu, ntmax, o));
+        }
+        int len = max(max((int)cdiv(total, G), (int)cdiv(ntmax, S)), 1);
+        for (;;) {
+            int cnt = (nt + len - 1) / len;
+            for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
+            if (cnt <= G) break;
+            ++len;
+        }
+        const int np = (nt + len - 1) / len;
+        int x = np;
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, x, o);
+            if (lane >= o) x += y;
+        }
+        const int first = x - np;
+        if (lane == 0) {
+            ms.my_row = -1;
+            ms.my_slots_from = S;
+            ms.my_empty_row = -1;
+        }
+        __syncwarp();
+        if (in && np > 0 && c >= first && c < first + np) {
+            const int piece = c - first;
+            const int t0 = piece * nt / np;
+            ms.my_row = lane;
+            ms.my_piece = piece;
+            ms.my_t0 = t0;
+            ms.my_nt = (piece + 1) * nt / np - t0;
+            ms.my_p = pq;
+            if (piece == 0) ms.my_slots_from = np;
+        }
+        if (in && np == 0 && lane == c) ms.my_empty_row = lane;   // R <= gridDim.x
+        return;
+    }
     int total = 0, ntmax = 0;
 #pragma unroll 1
     for (int q = lane; q < R; q += 32) {
