@@ -346,22 +346,33 @@ def _elapsed_ms(a, b):
     return ms
 
 
-def kernel_source_hash():
+# Sources each timed call's kernels are compiled from (its own files plus the shared headers and
+# the launch helpers); a DRAM-traffic figure stays valid while these files are unchanged.
+_SHARED_SOURCES = ["common.cuh", "tc_ptx.cuh", "tmap.cuh", "tmap.cu", "runtime.cu"]
+CALL_SOURCES = {
+    "csa_index_topk": ["indexer.cu", "indexer_tc.cu", "topk.cu", "quant.cuh"] + _SHARED_SOURCES,
+    "hca_attend": ["attend.cu", "attend_tc.cu", "attend.cuh"] + _SHARED_SOURCES,
+    "csa_attend": ["attend.cu", "attend_tc.cu", "attend.cuh"] + _SHARED_SOURCES,
+}
+
+
+def kernel_source_hash(call: str) -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "long_context_sparse_28_b300", "csrc")
-    for f in sorted(os.listdir(csrc)):
+    for f in sorted(CALL_SOURCES[call]):
+        h.update(f.encode())
         h.update(open(os.path.join(csrc, f), "rb").read())
     return h.hexdigest()[:16]
 
 
 def load_traffic(kernel: str):
-    """Per-launch DRAM bytes of a kernel from the committed ncu summary, if it was taken on the
-    current kernel sources."""
+    """Per-launch DRAM bytes of a call's kernels from the committed ncu summary, if it was taken
+    on the call's current kernel sources."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         d = json.load(open(p))
         e = d.get(kernel)
-        if e and e.get("source_hash") == kernel_source_hash():
+        if e and kernel in CALL_SOURCES and e.get("source_hash") == kernel_source_hash(kernel):
             return e
     except Exception:
         pass
