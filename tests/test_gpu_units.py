@@ -251,6 +251,41 @@ def test_hca_attend_parity(splits, dt, H, d):
         np.testing.assert_allclose(npy(lse[b, 0]), ls, rtol=1e-5, atol=1e-5)
 
 
+@pytest.mark.parametrize("B", [48, 140])
+def test_attend_piece_schedule_more_rows_than_a_warp(B):
+    # 33..256 decode rows take the shared-memory form of the piece schedule (HCA: rows of
+    # different lengths; CSA: the host-made schedule with more rows than a warp)
+    H, d, m, W, Ncap, k = 64, 128, 128, 128, 45, 200
+    rng = np.random.default_rng(B)
+    ck, cv, rk, rv = _rand_cache(B, Ncap, W, d, "bf16", 60)
+    q = rnd((B, 1, H, d), torch.bfloat16, 61, d ** -0.5)
+    pos = rng.integers(0, m * Ncap + 64, size=B)
+    pos[0], pos[1] = 5, m * (Ncap + 3)                       # window only; every entry visible
+    out = torch.empty(B, 1, H, d, dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty(B, 1, H, device="cuda")
+    L.hca_attend(q, d ** -0.5, ck, cv, m, rk, rv, W, dev_i64(pos), out, lse)
+    idx = np.full((B, 1, k), -1, dtype=np.int32)
+    for b in range(B):                                       # distinct entries, -1 padded
+        n = int(rng.integers(0, Ncap + 1))
+        idx[b, 0, :n] = np.sort(rng.choice(Ncap, n, replace=False))
+    out_c = torch.empty_like(out)
+    lse_c = torch.empty_like(lse)
+    L.csa_attend(q, d ** -0.5, ck, cv, torch.from_numpy(idx).cuda(), rk, rv, W, dev_i64(pos), out_c, lse_c)
+    torch.cuda.synchronize()
+    assert L.device_status() == 0
+    for b in range(B):
+        wp = np.arange(max(0, pos[b] - W + 1), pos[b] + 1) % W
+        nv = min(Ncap, (pos[b] + 1) // m)
+        o, ls = oracle.attend(npy(q[b, 0]), d ** -0.5, npy(ck[b]), npy(cv[b]), np.arange(nv), npy(rk[b]),
+                              npy(rv[b]), wp)
+        assert_close(out[b, 0], o, "bf16", f"hca b{b}")
+        np.testing.assert_allclose(npy(lse[b, 0]), ls, rtol=1e-5, atol=1e-5)
+        sel = idx[b, 0][idx[b, 0] >= 0]
+        o, ls = oracle.attend(npy(q[b, 0]), d ** -0.5, npy(ck[b]), npy(cv[b]), sel, npy(rk[b]), npy(rv[b]), wp)
+        assert_close(out_c[b, 0], o, "bf16", f"csa b{b}")
+        np.testing.assert_allclose(npy(lse_c[b, 0]), ls, rtol=1e-5, atol=1e-5)
+
+
 def test_attend_empty_key_set_gives_zero():
     B, H, d, Ncap = 1, 8, 64, 4
     ck, cv, rk, rv = _rand_cache(B, Ncap, 1, d, "f32", 50)
