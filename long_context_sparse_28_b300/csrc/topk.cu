@@ -25,7 +25,6 @@ constexpr int kBins8 = 256;
 constexpr int kSlice = 8192;       // candidates per collect CTA (multiple of 32)
 constexpr int kCap = 8192;         // candidate-list capacity per row
 constexpr int kThreads = 256;
-constexpr int kThresholdThreads = 1024;   // four histogram bins per thread: one round of loads
 constexpr int kFinishThreads = 1024;
 
 __device__ __forceinline__ int64_t row_nvis(int r, const int64_t* n_vis_arr, const int64_t* q_pos, int m,
@@ -96,7 +95,7 @@ __global__ void __launch_bounds__(kThreads) topk_hist_kernel(const float* __rest
 
 // Per row: the boundary bin b1 of the top-12-bit histogram, the count above it, and whether the
 // elements of bins >= b1 fit the candidate list (x = b1, y = above1, z = fits).
-__global__ void __launch_bounds__(kThresholdThreads) topk_threshold_kernel(const int64_t* __restrict__ n_vis_arr,
+__global__ void __launch_bounds__(kThreads) topk_threshold_kernel(const int64_t* __restrict__ n_vis_arr,
                                                                   const int64_t* __restrict__ q_pos, int m,
                                                                   int64_t Ncap, int64_t stride, int k,
                                                                   const uint32_t* __restrict__ hist1,
@@ -361,7 +360,7 @@ csahca_status topk_launch(const float* scores, int64_t stride, int R, const int6
         count_launch();
         CSAHCA_CHECK_LAUNCH();
     }
-    (void)launch_pdl(topk_threshold_kernel, dim3(R), dim3(kThresholdThreads), 0, stream, n_vis_arr, q_pos, m, Ncap, stride, k, tw.hist1, tw.thr1);
+    (void)launch_pdl(topk_threshold_kernel, dim3(R), dim3(kThreads), 0, stream, n_vis_arr, q_pos, m, Ncap, stride, k, tw.hist1, tw.thr1);
     count_launch();
     CSAHCA_CHECK_LAUNCH();
     const dim3 cgrid((unsigned)std::max<int64_t>(1, cdiv(stride, (int64_t)kWarpSpan * (kThreads / 32))), (unsigned)R);
