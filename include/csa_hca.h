@@ -22,8 +22,12 @@
  * Conventions (all entry points):
  *   - Every pointer argument is a DEVICE pointer owned by the caller, unless stated.  The
  *     library never frees, retains or allocates memory; scratch space is a caller-provided
- *     workspace sized by the matching *_workspace() function (256-byte aligned).
- *   - Work is enqueued asynchronously on `stream` (a cudaStream_t; NULL = legacy default).
+ *     workspace sized by the matching *_workspace() function (256-byte aligned).  The one
+ *     exception is hca_attend_noalloc, whose scratch is a fixed array inside the library.
+ *   - Work is enqueued asynchronously on `stream` (a cudaStream_t; NULL = legacy default),
+ *     in stream order.  Kernels are launched with programmatic dependent launch: a kernel may
+ *     start while the previous kernel on the stream finishes, but it reads and writes global
+ *     memory only after that kernel has completed.
  *   - Arguments are validated on the host before any launch; a rejected call returns
  *     CSAHCA_ERR_INVALID_ARG / _UNSUPPORTED / _WORKSPACE and enqueues nothing.
  *   - A failed launch returns CSAHCA_ERR_CUDA.  Errors found on the device (index out of
