@@ -37,7 +37,7 @@ _LIB_PATH = os.path.join(_HERE, "liboracle.so")
 _lock = threading.Lock()
 _lib = None
 
-F32, BF16 = 0, 1                      # storage dtype codes
+F32, BF16, F64 = 0, 1, 2              # storage dtype codes (F64: dequantised values passed back in)
 KEY_F32, KEY_BF16, KEY_E4M3, KEY_E2M1 = 0, 1, 2, 3   # index-key formats
 
 
@@ -92,7 +92,9 @@ def _dt(a: np.ndarray) -> int:
         return F32
     if a.dtype == np.uint16:
         return BF16
-    raise TypeError(f"oracle storage arrays are float32 or uint16 (bf16 bits), got {a.dtype}")
+    if a.dtype == np.float64:
+        return F64
+    raise TypeError(f"oracle storage arrays are float32, float64 or uint16 (bf16 bits), got {a.dtype}")
 
 
 def num_threads() -> int:
@@ -201,6 +203,20 @@ def dequant_keys(fmt: int, codes: np.ndarray, scales, d: int) -> np.ndarray:
     sp = _p(np.ascontiguousarray(scales)) if scales is not None else None
     _L().oc_dequant_keys(fmt, _p(codes), sp, rows, d, _p(out))
     return out
+
+
+def fp4_query(q_idx: np.ndarray) -> np.ndarray:
+    """Indexer queries in FP4, as the lightning indexer's query-key path runs it (honbul.tistory
+    .com/221, section on FP4 QAT of the CSA indexer's query-key path; pogovet.com detail 5, the
+    indexer runs in FP4): every run of 32 consecutive elements of a head's vector is quantised
+    with the same MX rule as the index keys -- e = the smallest integer with amax <= 6 * 2^e
+    (0 for an all-zero run), code = RNE_e2m1(x * 2^-e) -- and the query becomes 2^e * code.
+
+    q_idx: [T, H_I, d_I] (float32 or bf16 bits), d_I % 32 == 0.  Returns fp64 [T, H_I, d_I]."""
+    q_idx = np.ascontiguousarray(q_idx)
+    T, H_I, d_I = q_idx.shape
+    codes, se = quant_e2m1_ue8m0(q_idx.reshape(T * H_I, d_I))
+    return dequant_keys(KEY_E2M1, codes, se, d_I).reshape(T, H_I, d_I)
 
 
 # ------------------------------------------------------------ a5: indexer

@@ -40,8 +40,10 @@ static double bf16_bits_to_double(uint16_t h) {
     return (double)f;
 }
 
+/* dtype 0 = float32, 1 = bfloat16 bits, 2 = float64 (dequantised values handed back in) */
 static double load_elem(const void* p, int dtype, int64_t i) {
     if (dtype == 0) return (double)((const float*)p)[i];
+    if (dtype == 2) return ((const double*)p)[i];
     return bf16_bits_to_double(((const uint16_t*)p)[i]);
 }
 

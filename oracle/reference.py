@@ -20,7 +20,7 @@ from __future__ import annotations
 
 import numpy as np
 
-from . import (BF16, F32, attend, dequant_keys, index_scores, pool, quantize_keys,
+from . import (BF16, F32, attend, dequant_keys, fp4_query, index_scores, pool, quantize_keys,
                round_to, topk)
 
 __all__ = ["n_visible", "window_positions", "compress", "csa_queries", "hca_queries"]
@@ -56,14 +56,15 @@ def _window_rows(pos: int, W: int, raw_pos0: int):
 
 def csa_queries(q, q_idx, w, pos, ck, cv, key_codes, key_scales, key_fmt, raw_k, raw_v,
                 raw_pos0: int, m: int, k: int, W: int, scale: float, idx_override=None,
-                strict: bool = False):
+                strict: bool = False, q_fp4: bool = False):
     """CSA for T queries of one sequence.
 
     q: [T, H, d]; q_idx: [T, H_I, d_I]; w: [T, H_I]; pos: [T] query positions;
     ck, cv: compressed cache [N, d] (storage form); key_codes/key_scales/key_fmt: index
     keys of the N entries; raw_k/raw_v: raw tokens from position raw_pos0 on.
     ``idx_override`` ([T, k]) replaces the oracle's own top-k (used to evaluate attention
-    on another implementation's index set).
+    on another implementation's index set).  ``q_fp4``: the indexer queries are taken in FP4
+    (``fp4_query``) before scoring.
     Returns dict(o [T,H,d], lse [T,H], idx [T,k], scores [T,N]).
     """
     q = np.asarray(q)
@@ -73,7 +74,7 @@ def csa_queries(q, q_idx, w, pos, ck, cv, key_codes, key_scales, key_fmt, raw_k,
     nv = n_visible(pos, m, N, strict)
     d_I = q_idx.shape[-1]
     khat = dequant_keys(key_fmt, key_codes, key_scales, d_I)
-    S = index_scores(q_idx, w, khat, nv)
+    S = index_scores(fp4_query(q_idx) if q_fp4 else q_idx, w, khat, nv)
     idx = topk(S, nv, k) if idx_override is None else np.asarray(idx_override, dtype=np.int32)
     H, d = q.shape[1], q.shape[2]
     o = np.empty((T, H, d))

@@ -82,3 +82,60 @@ def test_topk_k_ge_visible_returns_all_visible():
 def test_topk_signed_zero_is_a_tie():
     S = np.array([[0.0, -0.0, 0.0, -0.0, 1.0]])
     assert list(oracle.topk(S, [5], 3)[0]) == [0, 1, 4]
+
+
+# ---------------------------------------------------------- FP4 indexer queries
+def _bf16(x):
+    import torch
+    return torch.tensor(np.asarray(x, dtype=np.float32)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+def test_fp4_query_worked_example():
+    from tests.golden import load
+    g = load("fp4_query_worked.txt")
+    d = 64
+    q = np.zeros((1, 1, d), np.float32)
+    q[0, 0, [int(i) for i in g["q_at"]]] = g["q"]
+    qb = _bf16(q)
+    qh = oracle.fp4_query(qb)
+    want = np.zeros(d)
+    want[[int(i) for i in g["q_at"]]] = g["q_hat"]
+    np.testing.assert_array_equal(qh[0, 0], want)
+    key = np.zeros((1, d))
+    key[0, [int(i) for i in g["key_at"]]] = g["key"]
+    S = oracle.index_scores(qh, np.array([[g["w"][0]]], np.float32), key, [1])
+    assert S[0, 0] == g["expected"][0]
+
+
+def test_fp4_query_of_representable_values_leaves_scores_unchanged():
+    # values that already are 2^e * e2m1 with e the MX exponent of their run survive the
+    # quantisation exactly, so the FP4-query scores equal the bf16-query scores
+    rng = _rng(11)
+    T, H, d, N = 2, 3, 64, 40
+    mags = np.array([0, 0.5, 1, 1.5, 2, 3, 4, 6], np.float32)
+    codes = rng.choice(mags, size=(T, H, d)) * rng.choice([-1, 1], size=(T, H, d))
+    codes[..., 0] = 6.0                                  # every run of 32 has amax 6 -> e = its scale
+    codes[..., 32] = -6.0
+    e = rng.integers(-6, 6, size=(T, H, 2)).astype(np.float32)
+    q = (codes.reshape(T, H, 2, 32) * np.exp2(e)[..., None]).reshape(T, H, d).astype(np.float32)
+    kh = rng.standard_normal((N, d))
+    w = rng.uniform(size=(T, H)).astype(np.float32)
+    np.testing.assert_array_equal(oracle.fp4_query(q), q.astype(np.float64))
+    np.testing.assert_array_equal(oracle.index_scores(oracle.fp4_query(q), w, kh, [N, 7]),
+                                  oracle.index_scores(q, w, kh, [N, 7]))
+
+
+def test_fp4_query_scales_each_run_of_32_on_its_own():
+    # a run of large values next to a run of small ones: with one scale per head the small run
+    # would round to zero; per-32 scales keep each run within half the largest E2M1 step of its
+    # own scale (the step 4 -> 6 is 2 x 2^e)
+    rng = _rng(12)
+    d = 64
+    q = np.concatenate([rng.uniform(50, 100, 32), rng.uniform(0.01, 0.02, 32)]).astype(np.float32)[None, None]
+    qh = oracle.fp4_query(q)[0, 0]
+    assert (qh[32:] != 0).all()
+    for r in (slice(0, 32), slice(32, 64)):
+        amax = np.abs(q[0, 0, r]).max()
+        e = int(np.ceil(np.log2(amax / 6.0)))
+        assert np.abs(qh[r] - q[0, 0, r]).max() <= 2.0 ** e
+        assert set(np.unique(np.abs(qh[r]) / 2.0 ** e)) <= {0, 0.5, 1, 1.5, 2, 3, 4, 6}
