@@ -38,6 +38,8 @@ import workloads as wl  # noqa: E402
 
 METRIC = "CSA+HCA decode queries/s and achieved HBM GB/s at 1M ctx on 1 B300"
 UNIT = "queries/s"
+# layers of a decode step per workload kind
+DEFAULT_LAYERS = {"hybrid_decode": "both", "csa_decode": "csa", "hca_decode": "hca"}
 
 
 def parse():
@@ -48,10 +50,12 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="decode_1m_b32_csa_hca")
     ap.add_argument("--cpu-seqs", type=int, default=0, help="sequences in the CPU-baseline sample (0 = auto)")
+    ap.add_argument("--cpu-rows", type=int, default=64, help="query rows in the prefill CPU-baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--layers", default="both", choices=["both", "csa", "hca", "index"],
-                    help="restrict the step (profiling): csa / hca layer only, or the CSA indexer + top-k only")
+    ap.add_argument("--layers", default=None, choices=["both", "csa", "hca", "index"],
+                    help="restrict the step (profiling): csa / hca layer only, or the CSA indexer + top-k only "
+                         "(default: the workload's layers)")
     return ap.parse_args()
 
 
@@ -175,19 +179,22 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------------------- ours
-def algorithmic_bytes(w, lens_csa_nvis, lens_hca_nvis):
+def algorithmic_bytes(w, lens_csa_nvis, lens_hca_nvis, layers="both"):
     """Minimum bytes one decode step must move (per the method): all visible CSA index keys
     (+ scales), the k selected + W window K/V rows, all visible HCA entries + window, and the
-    queries/outputs.  Returns dict of per-part bytes."""
+    queries/outputs -- of the layers the step runs.  Returns dict of per-part bytes."""
     d, H, B = w.d, w.H, w.B
     key_row = {"f32": 4 * w.d_I, "bf16": 2 * w.d_I, "e4m3": w.d_I + 4, "e2m1": w.d_I // 2 + w.d_I // 32}[w.key_fmt]
     kv_row = 2 * d * 2                                   # one K row + one V row, bf16
+    csa = layers in ("both", "csa", "index")
+    hca = layers in ("both", "hca")
     parts = {
-        "csa_index_keys": int(sum(lens_csa_nvis)) * key_row,
-        "csa_gather": B * (w.k + w.W) * kv_row,
-        "hca_entries": int(sum(lens_hca_nvis)) * kv_row,
-        "hca_window": B * w.W * kv_row,
-        "q_o": B * (4 * H * d * 2 + w.H_I * w.d_I * 2 + w.H_I * 4),
+        "csa_index_keys": int(sum(lens_csa_nvis)) * key_row if csa else 0,
+        "csa_gather": B * (w.k + w.W) * kv_row if layers in ("both", "csa") else 0,
+        "hca_entries": int(sum(lens_hca_nvis)) * kv_row if hca else 0,
+        "hca_window": B * w.W * kv_row if hca else 0,
+        "q_o": B * ((4 * H * d * 2 if layers in ("both", "csa") else 0) + (4 * H * d * 2 if hca else 0)
+                    + (w.H_I * w.d_I * 2 + w.H_I * 4 if csa else 0)),
     }
     parts["total"] = sum(parts.values())
     return parts
@@ -339,6 +346,12 @@ def _record_external(ev, stream):
     assert err == rt.cudaError_t.cudaSuccess, err
 
 
+def _record(ev, stream):
+    from cuda.bindings import runtime as rt
+    err, = rt.cudaEventRecord(ev, stream.cuda_stream)
+    assert err == rt.cudaError_t.cudaSuccess, err
+
+
 def _elapsed_ms(a, b):
     from cuda.bindings import runtime as rt
     err, ms = rt.cudaEventElapsedTime(a, b)
@@ -379,38 +392,45 @@ def load_traffic(kernel: str):
     return None
 
 
-def cpu_baseline_decode(w, seqs: int, device):
+def cpu_baseline_decode(w, seqs: int, device, layers="both"):
     """The oracle (as it stands) on `seqs` sequences of the workload: one decode query per
-    sequence through both layers.  Cache construction is setup and not timed."""
+    sequence through the step's layers.  Cache construction is setup and not timed."""
     import oracle
     lens = w.lengths()
     order = list(range(w.B))[:seqs]
+    fmt = {"f32": oracle.KEY_F32, "bf16": oracle.KEY_BF16, "e4m3": oracle.KEY_E4M3, "e2m1": oracle.KEY_E2M1}[w.key_fmt]
     ctx = []
     for b in order:
         Lb = lens[b]
-        k, v, g = wl.raw_tokens(w, "csa", b, Lb, device)
-        kin = wl.index_key_inputs(w, "csa", b, Lb // w.m_csa + 1, device)
-        K, V, G, KIN = (wl.to_numpy(x) for x in (k, v, g, kin))
-        hk, hv, hg = wl.raw_tokens(w, "hca", b, Lb, device)
-        HK, HV, HG = (wl.to_numpy(x) for x in (hk, hv, hg))
-        cb = wl.to_numpy(wl.layer_bias(w, "csa", w.m_csa, device))
-        hb = wl.to_numpy(wl.layer_bias(w, "hca", w.m_hca, device))
-        ck, cv = oracle.compress(K, V, G, cb, w.m_csa, oracle.BF16)
-        codes, sc = oracle.quantize_keys(KIN[: Lb // w.m_csa], oracle.KEY_E2M1)
-        hck, hcv = oracle.compress(HK, HV, HG, hb, w.m_hca, oracle.BF16)
+        K = V = ck = cv = codes = sc = HK = HV = hck = hcv = None
+        if layers in ("both", "csa"):
+            k, v, g = wl.raw_tokens(w, "csa", b, Lb, device)
+            kin = wl.index_key_inputs(w, "csa", b, Lb // w.m_csa + 1, device)
+            K, V, G, KIN = (wl.to_numpy(x) for x in (k, v, g, kin))
+            cb = wl.to_numpy(wl.layer_bias(w, "csa", w.m_csa, device))
+            ck, cv = oracle.compress(K, V, G, cb, w.m_csa, oracle.BF16)
+            codes, sc = oracle.quantize_keys(KIN[: Lb // w.m_csa], fmt)
+            del k, v, g, kin
+        if layers in ("both", "hca"):
+            hk, hv, hg = wl.raw_tokens(w, "hca", b, Lb, device)
+            HK, HV, HG = (wl.to_numpy(x) for x in (hk, hv, hg))
+            hb = wl.to_numpy(wl.layer_bias(w, "hca", w.m_hca, device))
+            hck, hcv = oracle.compress(HK, HV, HG, hb, w.m_hca, oracle.BF16)
+            del hk, hv, hg
         q = wl.to_numpy(wl.queries(w, "csa", b, 1, device))
         qh = wl.to_numpy(wl.queries(w, "hca", b, 1, device))
         qi, ww = (wl.to_numpy(x) for x in wl.indexer_queries(w, "csa", b, 1, device))
         ctx.append((Lb, K, V, ck, cv, codes, sc, HK, HV, hck, hcv, q, qh, qi, ww))
-        del k, v, g, hk, hv, hg
     t0 = time.perf_counter()
     for (Lb, K, V, ck, cv, codes, sc, HK, HV, hck, hcv, q, qh, qi, ww) in ctx:
-        oracle.csa_queries(q, qi, ww, [Lb - 1], ck, cv, codes, sc, oracle.KEY_E2M1, K, V, 0, w.m_csa, w.k, w.W,
-                           w.scale)
-        oracle.hca_queries(qh, [Lb - 1], hck, hcv, HK, HV, 0, w.m_hca, w.W, w.scale)
+        if layers in ("both", "csa"):
+            oracle.csa_queries(q, qi, ww, [Lb - 1], ck, cv, codes, sc, fmt, K, V, 0, w.m_csa, w.k, w.W, w.scale)
+        if layers in ("both", "hca"):
+            oracle.hca_queries(qh, [Lb - 1], hck, hcv, HK, HV, 0, w.m_hca, w.W, w.scale)
     dt = time.perf_counter() - t0
+    names = {"both": "the CSA and HCA layers", "csa": "the CSA layer", "hca": "the HCA layer"}[layers]
     return dict(value=len(ctx) / dt, unit=UNIT, cores=oracle.num_threads(), kind="oracle",
-                sample=f"{len(ctx)} of {w.B} sequences, one decode query each through the CSA and HCA layers "
+                sample=f"{len(ctx)} of {w.B} sequences, one decode query each through {names} "
                        f"(fp64 C oracle, OpenMP); cache construction untimed; {dt:.2f} s")
 
 
@@ -419,12 +439,14 @@ def run_ours(args, dist):
     dev = torch.device("cuda", dist.local)
     torch.cuda.set_device(dev)
     w = wl.shrink(wl.WORKLOADS[args.workload], seed=dist.rank) if dist.world > 1 else wl.WORKLOADS[args.workload]
+    full = DEFAULT_LAYERS[w.kind]
+    layers = args.layers or full
     K, Wm = args.steps, args.warmup
     total = K + Wm
     e2e_steps = 0 if args.no_e2e else min(K, 20)
-    if args.layers != "both":
+    if layers != full:
         e2e_steps = 0
-    bench = DecodeBench(w, dev, total + e2e_steps + 2, args.layers)
+    bench = DecodeBench(w, dev, total + e2e_steps + 2, layers)
     lens = bench.lens
     stream = torch.cuda.Stream(device=dev)
     inputs = [make_step_inputs(w, s, lens, dev, w.m_csa) for s in range(total)]
@@ -495,7 +517,7 @@ def run_ours(args, dist):
     # algorithmic bytes (average over timed steps)
     nv_c = [[min(bench.Ncap_c, (L0 + s) // w.m_csa) for L0 in lens] for s in range(Wm, total)]
     nv_h = [[min(bench.Ncap_h, (L0 + s) // w.m_hca) for L0 in lens] for s in range(Wm, total)]
-    parts_list = [algorithmic_bytes(w, a, b) for a, b in zip(nv_c, nv_h)]
+    parts_list = [algorithmic_bytes(w, a, b, layers) for a, b in zip(nv_c, nv_h)]
     parts = {k: statistics.mean(p[k] for p in parts_list) for k in parts_list[0]}
     queries = w.B * dist.world
     value = queries / (ms_per_step / 1e3)
@@ -526,18 +548,23 @@ def run_ours(args, dist):
         e2e = run_e2e(bench, w, lens, total, e2e_steps, dev, dist)
 
     cpu = None
-    if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline and args.layers == "both":
-        cpu = cpu_baseline_decode(w, args.cpu_seqs or 6, dev)
+    if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline and layers == full:
+        cpu = cpu_baseline_decode(w, args.cpu_seqs or min(w.B, 6), dev, layers)
 
     clocks = sampler.summary()
+    key_desc = {"e2m1": "e2m1+ue8m0/32", "e4m3": "e4m3+f32 row scale", "bf16": "bf16", "f32": "f32"}[w.key_fmt]
+    cfg = {"workload": w.name, "B": w.B,
+           "L": f"U[{w.L_range[0]},{w.L_range[1]}] seeded" if w.L_range else w.L[0] if len(set(w.L)) == 1 else list(w.L),
+           "H": w.H, "d": w.d, "layers": layers}
+    if layers in ("both", "csa", "index"):
+        cfg["csa"] = {"m": w.m_csa, "k": w.k, "W": w.W, "H_I": w.H_I, "d_I": w.d_I, "index_keys": key_desc}
+    if layers in ("both", "hca"):
+        cfg["hca"] = {"m": w.m_hca, "W": w.W}
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": dist.world, "steps": K, "warmup": Wm,
         "ms_per_step": round(ms_per_step, 5), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": w.name, "B": w.B, "L": f"U[{w.L_range[0]},{w.L_range[1]}] seeded", "H": w.H,
-                   "d": w.d, "csa": {"m": w.m_csa, "k": w.k, "W": w.W, "H_I": w.H_I, "d_I": w.d_I,
-                                     "index_keys": "e2m1+ue8m0/32"},
-                   "hca": {"m": w.m_hca, "W": w.W}, "parallelism": f"replicas x{dist.world}",
+        "config": {**cfg, "parallelism": f"replicas x{dist.world}",
                    "l2": "inputs larger than L2: %.0f MB read per step" % (parts["total"] / 1e6),
                    "hbm_gbs_step": round(step_gbs, 1), "algorithmic_bytes_per_step": int(parts["total"]),
                    "substep_ms": {n: round(v, 5) for n, v in per.items()},
@@ -628,6 +655,238 @@ def run_e2e(bench, w, lens, first_step, n, dev, dist):
                     "both layers' outputs; inputs and outputs double-buffered on copy streams"}
 
 
+# --------------------------------------------------------------------- chunked prefill
+PREFILL_METRIC = "CSA+HCA chunked-prefill query tokens/s on 1 B300"
+
+
+def prefill_flops(w):
+    """Tensor-core work of one chunk (multiply-adds x 2): the indexer over every causally visible
+    CSA entry, CSA attention over k selected entries + W window keys (QK and PV), HCA attention over
+    every visible HCA entry + W window keys."""
+    o, T = w.offset, w.T
+    p = np.arange(o, o + T, dtype=np.int64)
+    nv_c = (p + 1) // w.m_csa
+    nv_h = (p + 1) // w.m_hca
+    index = 2.0 * float(nv_c.sum()) * w.H_I * w.d_I
+    csa = 2.0 * 2.0 * T * (w.k + w.W) * w.H * w.d
+    hca = 2.0 * 2.0 * float((nv_h + w.W).sum()) * w.H * w.d
+    return {"csa_index_topk": index, "csa_attend": csa, "hca_attend": hca, "total": index + csa + hca}
+
+
+class PrefillBench:
+    """A CSA and an HCA layer cache holding a synthetic prior state (entries, index keys and the
+    window ring before the chunk, as drawn by the workload), and the chunk's inputs; a step = one
+    chunk through both layers.  Every timed step re-processes the same chunk at the same position
+    (identical work)."""
+
+    SUBSTEPS = ["compress+quantise", "csa_index_topk", "csa_attend", "hca_attend", "ring_write"]
+
+    def __init__(self, w, device):
+        import long_context_sparse_28_b300 as L
+        from long_context_sparse_28_b300.layers import CSACache, HCACache, HybridPrefill
+        self.L, self.w = L, w
+        x = wl.prefill_inputs(w, device)
+        o, T, W = w.offset, w.T, w.W
+        n_csa, n_hca = o // w.m_csa, o // w.m_hca
+        self.csa = CSACache(1, (o + T) // w.m_csa, w.d, W, w.d_I, L.KEY_FMT[w.key_fmt], torch.bfloat16, device)
+        self.hca = HCACache(1, (o + T) // w.m_hca, w.d, W, torch.bfloat16, device)
+        self.csa.ck[0, :n_csa] = x["csa_ck"]
+        self.csa.cv[0, :n_csa] = x["csa_cv"]
+        L.csa_index_key_quantize(x["csa_kidx"], self.csa.key_fmt, self.csa.k_codes[0, :n_csa],
+                                 None if self.csa.k_scale is None else self.csa.k_scale[0, :n_csa])
+        self.hca.ck[0, :n_hca] = x["hca_ck"]
+        self.hca.cv[0, :n_hca] = x["hca_cv"]
+        pos_ring = torch.tensor([o - W], dtype=torch.int64, device=device)
+        for c in (self.csa, self.hca):
+            L.swa_ring_write(x["ring_k"][None], x["ring_v"][None], x["ring_gate"][None], pos_ring, W, c.ring_k,
+                             c.ring_v, c.ring_gate)
+        self.x = x
+        self.step_ = HybridPrefill(self.csa, self.hca, T, w.H, w.k, x["csa_bias"], x["hca_bias"])
+        self.step_.set_position(o)
+        self.args = (x["chunk_k"][None], x["chunk_v"][None], x["chunk_gate"][None], x["chunk_kidx"][None],
+                     x["q_csa"][None], x["q_idx"][None], x["w"][None], x["q_hca"][None])
+
+    def step(self, args=None):
+        return self.step_.step(*(args or self.args))
+
+
+def cpu_baseline_prefill(w, rows: int):
+    """The oracle (as it stands) on `rows` seeded query rows of the chunk (CSA: indexer, top-k and
+    attention; HCA: dense attention), scaled to query tokens/s.  Pooling the chunk's blocks is
+    included; building the prior state is setup."""
+    import oracle
+    x = {k: wl.to_numpy(v) for k, v in wl.prefill_inputs(w, "cpu").items()}
+    o, T, W = w.offset, w.T, w.W
+    fmt = {"f32": oracle.KEY_F32, "bf16": oracle.KEY_BF16, "e4m3": oracle.KEY_E4M3, "e2m1": oracle.KEY_E2M1}[w.key_fmt]
+    sel = np.sort(np.random.default_rng(0).choice(T, rows, replace=False))
+    t0 = time.perf_counter()
+    cck, ccv = oracle.compress(x["chunk_k"], x["chunk_v"], x["chunk_gate"], x["csa_bias"], w.m_csa, oracle.BF16)
+    hck, hcv = oracle.compress(x["chunk_k"], x["chunk_v"], x["chunk_gate"], x["hca_bias"], w.m_hca, oracle.BF16)
+    ck, cv = np.concatenate([x["csa_ck"], cck]), np.concatenate([x["csa_cv"], ccv])
+    codes, sc = oracle.quantize_keys(np.concatenate([x["csa_kidx"], x["chunk_kidx"]]), fmt)
+    rawk, rawv = np.concatenate([x["ring_k"], x["chunk_k"]]), np.concatenate([x["ring_v"], x["chunk_v"]])
+    pos = o + sel
+    oracle.csa_queries(x["q_csa"][sel], x["q_idx"][sel], x["w"][sel], pos, ck, cv, codes, sc, fmt, rawk, rawv, o - W,
+                       w.m_csa, w.k, W, w.scale)
+    oracle.hca_queries(x["q_hca"][sel], pos, np.concatenate([x["hca_ck"], hck]), np.concatenate([x["hca_cv"], hcv]),
+                       rawk, rawv, o - W, w.m_hca, W, w.scale)
+    dt = time.perf_counter() - t0
+    return dict(value=rows / dt, unit="query tokens/s", cores=oracle.num_threads(), kind="oracle",
+                sample=f"{rows} of {T} query rows of the chunk through both layers (fp64 C oracle, OpenMP), the "
+                       f"chunk's pooling included, scaled by rows; {dt:.2f} s")
+
+
+def run_prefill(args, dist):
+    import long_context_sparse_28_b300 as L
+    dev = torch.device("cuda", dist.local)
+    torch.cuda.set_device(dev)
+    w = wl.shrink(wl.WORKLOADS[args.workload], seed=dist.rank) if dist.world > 1 else wl.WORKLOADS[args.workload]
+    K, Wm = args.steps, args.warmup
+    bench = PrefillBench(w, dev)
+    stream = torch.cuda.Stream(device=dev)
+    torch.cuda.synchronize()
+    # one graph of the chunk's calls; a second one with timing events between the calls
+    nsub = 5
+    evs = [_events(nsub + 1) for _ in range(K)]
+    g = torch.cuda.CUDAGraph()
+    c0 = L.launch_count()
+    with torch.cuda.stream(stream):
+        bench.step()                                   # first run outside capture (per-device set-up)
+        stream.synchronize()
+        c0 = L.launch_count()
+        with torch.cuda.graph(g, stream=stream, capture_error_mode="relaxed"):
+            bench.step()
+        launches = L.launch_count() - c0
+    torch.cuda.synchronize()
+    assert L.device_status() == 0
+    with torch.cuda.stream(stream):
+        for _ in range(Wm):
+            g.replay()
+    stream.synchronize()
+    dist.barrier()
+    torch.cuda.synchronize()
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(dev.index if dev.index is not None else 0)
+    with sampler:
+        with torch.cuda.stream(stream):
+            start.record(stream)
+            for _ in range(K):
+                g.replay()
+            stop.record(stream)
+        stream.synchronize()
+    torch.cuda.synchronize()
+    dist.barrier()
+    ms_per_step = dist.max(start.elapsed_time(stop)) / K
+    assert L.device_status(stream) == 0
+    # per-call durations, the calls run eagerly between events on the same stream
+    st = bench.step_
+    csa, hca = bench.csa, bench.hca
+    a = bench.args
+    calls = [
+        lambda: (L.csa_compress(a[0], a[1], a[2], st.p0, st.nT, st.csa_bias, csa.m, csa.ck, csa.cv),
+                 L.hca_compress(a[0], a[1], a[2], st.p0, st.nT, st.hca_bias, hca.m, hca.ck, hca.cv),
+                 L.csa_index_key_quantize(a[3][0, :w.T // w.m_csa], csa.key_fmt,
+                                          csa.k_codes[0, st.pos0 // csa.m:st.pos0 // csa.m + w.T // csa.m],
+                                          None if csa.k_scale is None else
+                                          csa.k_scale[0, st.pos0 // csa.m:st.pos0 // csa.m + w.T // csa.m])),
+        lambda: L.csa_index_topk(a[5], a[6], csa.k_codes, csa.k_scale, csa.key_fmt, st.q_pos, csa.m, w.k, st.idx,
+                                 workspace=st.ws_topk),
+        lambda: L.csa_attend(a[4], st.scale, csa.ck, csa.cv, st.idx, csa.ring_k, csa.ring_v, csa.W, st.q_pos, st.out_c,
+                             st.lse_c, chunk_k=a[0], chunk_v=a[1], chunk_pos0=st.p0, workspace=st.ws_ca),
+        lambda: L.hca_attend(a[7], st.scale, hca.ck, hca.cv, hca.m, hca.ring_k, hca.ring_v, hca.W, st.q_pos, st.out_h,
+                             st.lse_h, chunk_k=a[0], chunk_v=a[1], chunk_pos0=st.p0, workspace=st.ws_ha),
+        lambda: (L.swa_ring_write(a[0], a[1], a[2], st.p0, w.T, csa.ring_k, csa.ring_v, csa.ring_gate),
+                 L.swa_ring_write(a[0], a[1], a[2], st.p0, w.T, hca.ring_k, hca.ring_v, hca.ring_gate)),
+    ]
+    with torch.cuda.stream(stream):
+        for s in range(K):
+            for i in range(nsub):
+                _record(evs[s][i], stream)
+                calls[i]()
+            _record(evs[s][nsub], stream)
+    stream.synchronize()
+    sub_ms = [statistics.mean(_elapsed_ms(evs[s][i], evs[s][i + 1]) for s in range(K)) for i in range(nsub)]
+    per = dict(zip(PrefillBench.SUBSTEPS, sub_ms))
+    fl = prefill_flops(w)
+    peaks = {}
+    try:
+        peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+    except Exception:
+        pass
+    tf_peak = peaks.get("bf16_tflops_sustained", 1400.0)
+    dom = max(("csa_index_topk", "csa_attend", "hca_attend"), key=lambda n: per[n])
+    ach = fl[dom] / (per[dom] / 1e3) / 1e12
+    roofline = {"bound": "tensor", "kernel": dom, "achieved": round(ach, 1), "peak": tf_peak, "unit": "TFLOP/s",
+                "frac": round(ach / tf_peak, 4), "traffic": None, "algorithmic_flops_per_launch": fl[dom],
+                "avg_launch_ms": round(per[dom], 4),
+                "peak_source": "measured (sustained)" if "bf16_tflops_sustained" in peaks else "fallback",
+                "step_tflops": round(fl["total"] / (ms_per_step / 1e3) / 1e12, 1)}
+    e2e = None if args.no_e2e else run_e2e_prefill(bench, w, K, dev, dist)
+    cpu = None
+    if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline_prefill(w, args.cpu_rows)
+    return {
+        "metric": PREFILL_METRIC, "value": round(w.T * dist.world / (ms_per_step / 1e3), 1), "unit": "query tokens/s",
+        "n_gpus": dist.world, "steps": K, "warmup": Wm, "ms_per_step": round(ms_per_step, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.name, "T": w.T, "offset": w.offset, "H": w.H, "d": w.d,
+                   "csa": {"m": w.m_csa, "k": w.k, "W": w.W, "H_I": w.H_I, "d_I": w.d_I, "index_keys": w.key_fmt},
+                   "hca": {"m": w.m_hca, "W": w.W}, "parallelism": f"replicas x{dist.world}",
+                   "l2": "scores (1.09 GB) and gathered keys larger than L2; no flush",
+                   "tflop_per_step": round(fl["total"] / 1e12, 4),
+                   "substep_ms": {n: round(v, 4) for n, v in per.items()}},
+        "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": int(launches * K),
+        "clocks": sampler.summary(),
+    }
+
+
+def run_e2e_prefill(bench, w, n, dev, dist):
+    """The public API end to end: each step copies the chunk's inputs from pinned host memory,
+    runs the chunk's calls (one CUDA graph) and reads both layers' outputs back into pinned host
+    memory, all inside the timed region."""
+    L = bench.L
+    host = [t.to("cpu").pin_memory() for t in bench.args]
+    dev_in = [torch.empty_like(t) for t in bench.args]
+    out_host = [torch.empty(bench.step_.out_c.shape, dtype=torch.bfloat16, pin_memory=True) for _ in range(2)]
+    stream = torch.cuda.Stream(device=dev)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        for d_, h_ in zip(dev_in, host):
+            d_.copy_(h_)
+        bench.step(dev_in)
+        stream.synchronize()
+        with torch.cuda.graph(g, stream=stream, capture_error_mode="relaxed"):
+            bench.step(dev_in)
+    torch.cuda.synchronize()
+
+    def one():
+        for d_, h_ in zip(dev_in, host):
+            d_.copy_(h_, non_blocking=True)
+        g.replay()
+        out_host[0].copy_(bench.step_.out_c, non_blocking=True)
+        out_host[1].copy_(bench.step_.out_h, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            one()
+    torch.cuda.synchronize()
+    dist.barrier()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        t0.record(stream)
+        for _ in range(n):
+            one()
+        t1.record(stream)
+    torch.cuda.synchronize()
+    ms = dist.max(t0.elapsed_time(t1)) / n
+    assert L.device_status() == 0
+    return {"value": round(w.T * dist.world / (ms / 1e3), 1), "unit": "query tokens/s", "ms_per_step": round(ms, 4),
+            "h2d_bytes_per_step": int(sum(t.numel() * t.element_size() for t in host)),
+            "d2h_bytes_per_step": int(sum(t.numel() * t.element_size() for t in out_host)),
+            "path": "per step: H2D copy of the chunk's inputs from pinned host memory, the chunk's C-ABI calls "
+                    "(one CUDA graph), D2H copy of both layers' outputs, on one stream"}
+
+
 # ------------------------------------------------------------------------ reference arm
 def run_reference(args, dist):
     """The CPU oracle as it stands, on the host cores, on a bounded sample of the workload:
@@ -686,6 +945,8 @@ def main():
             if dist.rank != 0:
                 return
             line = run_reference(args, dist)
+        elif wl.WORKLOADS[args.workload].kind == "hybrid_prefill":
+            line = run_prefill(args, dist)
         else:
             line = run_ours(args, dist)
         if dist.rank == 0:

@@ -132,7 +132,8 @@ csahca_status csa_index_key_quantize(const void* k_in, csahca_dtype in_dtype, in
  *   scores_out: NULL, or [B][T][Ncap] float32 receiving the scores of the visible entries
  *               (entries >= n_vis are left untouched)
  *   workspace : csa_index_topk_workspace(B, T, Ncap, k) bytes
- * Supported: H_I*d_I <= 4096; d_I % 16 == 0; 1 <= k <= 4096.
+ * Supported: 1 <= H_I <= 64; 32 <= d_I <= 256, d_I % 32 == 0; H_I*d_I <= 4096; B*T <= 65535;
+ * 1 <= k <= 65536 (k larger than the visible entries pads with -1).
  */
 csahca_status csa_index_topk(const void* q_idx, csahca_dtype q_dtype, const float* w,
                              const void* k_codes, const void* k_scale, csahca_dtype key_fmt,
@@ -262,6 +263,13 @@ csahca_status swa_ring_write(const void* k_new, const void* v_new, const float* 
  * device (CSAHCA_OK, CSAHCA_ERR_BOUNDS or CSAHCA_ERR_TIMEOUT), or CSAHCA_ERR_CUDA. */
 csahca_status csahca_device_status(csahca_stream_t stream);
 const char* csahca_status_string(csahca_status s);
+/* Self-test of the bounded device waits (no counterpart on the method's pages): launches one warp
+ * that waits on a device barrier nothing ever completes, through the same wait routine the
+ * tensor-core kernels use.  After ~limit_ns (1 .. 1e9 ns) the wait gives up, records
+ * CSAHCA_ERR_TIMEOUT in the device error word and the kernel ends normally, so the context stays
+ * usable; csahca_device_status() then reports CSAHCA_ERR_TIMEOUT.  Returns INVALID_ARG for a
+ * limit outside the range, CUDA if the launch fails. */
+csahca_status csahca_selftest_bounded_wait(uint64_t limit_ns, csahca_stream_t stream);
 /* Number of kernel launches this library has enqueued on the calling host thread. */
 uint64_t csahca_launch_count(void);
 int csahca_version(void);

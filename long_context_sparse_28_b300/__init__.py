@@ -47,6 +47,7 @@ _SIGS = {
     "csahca_device_status": ([_P], _I),
     "csahca_status_string": ([_I], ctypes.c_char_p),
     "csahca_launch_count": ([], ctypes.c_uint64),
+    "csahca_selftest_bounded_wait": ([ctypes.c_uint64, _P], _I),
     "csahca_version": ([], _I),
 }
 
@@ -118,6 +119,12 @@ def status_string(st: int) -> str:
 def device_status(stream=None) -> int:
     """Synchronises the stream and returns (and clears) the device error word's status."""
     return int(library().csahca_device_status(_stream(stream)))
+
+
+def selftest_bounded_wait(limit_ns: int, stream=None) -> None:
+    """Runs the library's bounded-wait self-test (a device wait that nothing completes gives up
+    after ``limit_ns``); read the outcome with ``device_status()``."""
+    _check(library().csahca_selftest_bounded_wait(int(limit_ns), _stream(stream)), "csahca_selftest_bounded_wait")
 
 
 def launch_count() -> int:

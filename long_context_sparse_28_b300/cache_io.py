@@ -119,7 +119,44 @@ def read_header(path: str) -> tuple[dict, int]:
         header = json.loads(raw.decode())
     except (UnicodeDecodeError, json.JSONDecodeError) as e:
         raise ValueError(f"{path}: unreadable header ({e})") from None
+    _check_schema(path, header)
     return header, (16 + n + _ALIGN - 1) // _ALIGN * _ALIGN
+
+
+def _is_int(x) -> bool:
+    return isinstance(x, int) and not isinstance(x, bool)
+
+
+def _check_schema(path: str, h) -> None:
+    """Every field the loaders use is present, of the right type and in range."""
+    def bad(what):
+        raise ValueError(f"{path}: malformed header ({what})")
+    if not isinstance(h, dict):
+        bad("not an object")
+    if h.get("kind") not in ("csa", "hca"):
+        bad("kind")
+    if h.get("dtype") not in _DTYPES:
+        bad("dtype")
+    for key in ("m", "d", "W") + (("d_I", "key_fmt") if h["kind"] == "csa" else ()):
+        if not _is_int(h.get(key)) or h[key] < 0:
+            bad(key)
+    seqs, tensors = h.get("seqs"), h.get("tensors")
+    if not isinstance(seqs, list) or not isinstance(tensors, list):
+        bad("seqs / tensors")
+    for sq in seqs:
+        if not isinstance(sq, dict) or not _is_int(sq.get("n_ctx")) or not _is_int(sq.get("n_entries")) \
+                or sq["n_ctx"] < 0 or sq["n_entries"] < 0:
+            bad("sequence entry")
+    for e in tensors:
+        if not isinstance(e, dict) or not isinstance(e.get("name"), str) or e.get("dtype") not in _DTYPES:
+            bad("tensor entry")
+        if not _is_int(e.get("seq")) or not 0 <= e["seq"] < len(seqs):
+            bad("tensor sequence")
+        shape = e.get("shape")
+        if not isinstance(shape, list) or not all(_is_int(x) and x >= 0 for x in shape):
+            bad("tensor shape")
+        if not _is_int(e.get("offset")) or not _is_int(e.get("nbytes")) or e["offset"] < 0 or e["nbytes"] < 0:
+            bad("tensor offset / size")
 
 
 def _load_seq(path, header, start, i):

@@ -61,7 +61,8 @@ struct Smem {
     static constexpr uint32_t p = 2 * q_half;                         // two P buffers [128 keys][H] bf16
     static constexpr uint32_t p_region = kKeys * 128;
     static constexpr uint32_t p_bytes = ((H + 63) / 64) * p_region;
-    static constexpr uint32_t k = (p + 2 * p_bytes + 1023) / 1024 * 1024;  // two K slots
+    static constexpr uint32_t p_lo = p + 2 * p_bytes;                 // their low parts P - bf16(P)
+    static constexpr uint32_t k = (p_lo + 2 * p_bytes + 1023) / 1024 * 1024;  // two K slots
     static constexpr uint32_t v = k + 2 * kTile;                      // two V slots
     static constexpr uint32_t total = v + 2 * kTile;
 };
@@ -375,10 +376,12 @@ __global__ void __launch_bounds__(Thr<H>::kThreads, 1)
                         fence_after_sync();
                         const uint64_t v_desc = smem_desc(sbase + L::v + (seq & 1) * kTile, kHalf, 1024);
                         const uint64_t pb_desc = p_desc + (uint64_t)(((seq & 1) * L::p_bytes) >> 4);
+                        constexpr uint64_t lo_off = (uint64_t)((L::p_lo - L::p) >> 4);
 #pragma unroll
-                        for (int j = 0; j < 8; ++j)
-                            mma_ss(t_o, v_desc + (uint64_t)((j * 2048) >> 4), pb_desc + (uint64_t)((j * 2048) >> 4),
-                                   id_pv, (i > 0 || j > 0) ? 1u : 0u);
+                        for (int j = 0; j < 16; ++j)      // P = P_hi + P_lo: 8 K steps each
+                            mma_ss(t_o, v_desc + (uint64_t)(((j & 7) * 2048) >> 4),
+                                   pb_desc + (j >= 8 ? lo_off : 0) + (uint64_t)(((j & 7) * 2048) >> 4), id_pv,
+                                   (i > 0 || j > 0) ? 1u : 0u);
                         mma_commit(&ms.odone);
                     }
                     if (st < nt) {              // S^T(st) = K(st) . Q^T into S buffer (g + st) & 1
@@ -470,12 +473,26 @@ __global__ void __launch_bounds__(Thr<H>::kThreads, 1)
                 // P buffer (i & 1): its last reader PV(i-2) precedes MMA1(i) and is complete
                 const uint32_t prow = sbase + L::p + (seq & 1) * L::p_bytes + ((wg * HG / 8) >> 3) * L::p_region;
                 const int pchunk = (wg * HG / 8) & 7;                 // 8 heads per 16-byte chunk
-                auto store_p = [&](const uint32_t* pk) {
+                // P goes to the MMA as two bf16 parts, P_hi = bf16(P) and P_lo = bf16(P - P_hi), so the
+                // products P V keep about 16 significant bits of P
+                auto store_p = [&](const float* pp16) {
+                    uint32_t hi[8], lo[8];
 #pragma unroll
-                    for (int c = 0; c < 2; ++c)
+                    for (int k = 0; k < 8; ++k) {
+                        hi[k] = pack_bf16x2(pp16[2 * k], pp16[2 * k + 1]);
+                        lo[k] = pack_bf16x2(pp16[2 * k] - __uint_as_float(hi[k] << 16),
+                                            pp16[2 * k + 1] - __uint_as_float(hi[k] & 0xFFFF0000u));
+                    }
+#pragma unroll
+                    for (int c = 0; c < 2; ++c) {
                         asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(prow + sw128(row, pchunk + c)),
-                                     "r"(pk[4 * c]), "r"(pk[4 * c + 1]), "r"(pk[4 * c + 2]), "r"(pk[4 * c + 3])
+                                     "r"(hi[4 * c]), "r"(hi[4 * c + 1]), "r"(hi[4 * c + 2]), "r"(hi[4 * c + 3])
                                      : "memory");
+                        asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};"
+                                     ::"r"(prow + (L::p_lo - L::p) + sw128(row, pchunk + c)),
+                                     "r"(lo[4 * c]), "r"(lo[4 * c + 1]), "r"(lo[4 * c + 2]), "r"(lo[4 * c + 3])
+                                     : "memory");
+                    }
                 };
                 // K slot of tile i is free (MMA1(i) complete)
                 if (i + 2 < nt) load(i + 2, false);
@@ -485,7 +502,8 @@ __global__ void __launch_bounds__(Thr<H>::kThreads, 1)
                 // and P is formed again below.
                 bool grow = true;
                 if (i > 0) {
-                    uint32_t rr[16], pk[8];
+                    uint32_t rr[16];
+                    float pp[16];
                     tmem_ld16(scol, rr);
                     tmem_wait_ld();
                     bool need = false;
@@ -493,19 +511,16 @@ __global__ void __launch_bounds__(Thr<H>::kThreads, 1)
                     for (int k = 0; k < 16; k += 4) {
                         const float4 m4 = *reinterpret_cast<const float4*>(&ms.mrun[wg * HG + k]);
                         const float mm[4] = {m4.x, m4.y, m4.z, m4.w};
-                        float pp[4];
 #pragma unroll
                         for (int u = 0; u < 4; ++u) {
                             const float x = __uint_as_float(rr[k + u]) * c_log2;
                             need |= x > mm[u] + kRescaleThreshold;
-                            pp[u] = (mm[u] == -INFINITY || !valid) ? 0.0f
-                                                                   : ex2_approx(fminf(x - mm[u], kRescaleThreshold));
-                            lsum[k + u] += pp[u];
+                            pp[k + u] = (mm[u] == -INFINITY || !valid) ? 0.0f
+                                                                       : ex2_approx(fminf(x - mm[u], kRescaleThreshold));
+                            lsum[k + u] += pp[k + u];
                         }
-                        pk[k / 2] = pack_bf16x2(pp[0], pp[1]);
-                        pk[k / 2 + 1] = pack_bf16x2(pp[2], pp[3]);
                     }
-                    store_p(pk);
+                    store_p(pp);
                     grow = named_barrier_or(1, kSoft, need && valid);
                 }
                 // everyone is done with tile i-1's flag (the barrier above, or on an item's first
@@ -546,7 +561,8 @@ __global__ void __launch_bounds__(Thr<H>::kThreads, 1)
                     rescale = ms.flag[seq & 1] != 0;
                     // P again with the new maxima; the row sums drop the first pass's term
                     // (recomputed exactly as it was added) and are rescaled
-                    uint32_t rr[16], pk[8];
+                    uint32_t rr[16];
+                    float pp[16];
                     tmem_ld16(scol, rr);
                     tmem_wait_ld();
 #pragma unroll
@@ -558,20 +574,17 @@ __global__ void __launch_bounds__(Thr<H>::kThreads, 1)
                         const float mn[4] = {m4.x, m4.y, m4.z, m4.w};
                         const float mo[4] = {o4.x, o4.y, o4.z, o4.w};
                         const float al[4] = {a4.x, a4.y, a4.z, a4.w};
-                        float pp[4];
 #pragma unroll
                         for (int u = 0; u < 4; ++u) {
                             const float x = __uint_as_float(rr[k + u]) * c_log2;
                             const float pold = (i == 0 || mo[u] == -INFINITY || !valid)
                                                    ? 0.0f
                                                    : ex2_approx(fminf(x - mo[u], kRescaleThreshold));
-                            pp[u] = (mn[u] == -INFINITY || !valid) ? 0.0f : ex2_approx(x - mn[u]);
-                            lsum[k + u] = fmaf(lsum[k + u] - pold, al[u], pp[u]);
+                            pp[k + u] = (mn[u] == -INFINITY || !valid) ? 0.0f : ex2_approx(x - mn[u]);
+                            lsum[k + u] = fmaf(lsum[k + u] - pold, al[u], pp[k + u]);
                         }
-                        pk[k / 2] = pack_bf16x2(pp[0], pp[1]);
-                        pk[k / 2 + 1] = pack_bf16x2(pp[2], pp[3]);
                     }
-                    store_p(pk);
+                    store_p(pp);
                 }
                 // ---- PV(i-1) done: O and the V slot of tile i-1 are free
                 if (i > 0) {

@@ -181,11 +181,19 @@ cudaError_t index_tc_launch(const void* q_idx, const float* w, const void* k_cod
                             int B, int T, int H_I, const int64_t* q_pos, int64_t Ncap, int m, float* S,
                             uint32_t* hist1, unsigned* err, cudaStream_t st);
 
+// Tensor-core indexer scores for chunked prefill (bf16 keys and queries, d_I = 64, T a multiple of
+// 128 / H_I); hist1 as above.
+bool index_prefill_supported(int q_dtype, int key_fmt, int H_I, int d_I, int64_t Ncap, const void* q_idx,
+                             const void* k_codes, int B, int T);
+cudaError_t index_prefill_launch(const void* q_idx, const float* w, const void* k_codes, int B, int T, int H_I,
+                                 const int64_t* q_pos, int64_t Ncap, int m, float* S, uint32_t* hist1, unsigned* err,
+                                 cudaStream_t st);
+
 // Top-k over float32 scores (rows of `stride`, n_vis per row from q_pos or n_vis arrays).
 struct TopkWorkspace {
-    uint32_t* hist1;   // [R][4096] histogram of the top 12 bits (zeroed with cand_n)
+    uint32_t* hist1;   // [R][4096] histogram of the top 12 bits (zeroed with cand_n and done)
     int* cand_n;       // [R] candidate counts
-    int4* thr1;        // [R] boundary bin of the top 12 bits, count above it, candidate-list flag
+    int* done;         // [R] CTAs of the row that have finished collecting
     uint2* cand;       // [R][cap] (ordered key, index)
     uint32_t* win;     // [R][words] bitmap of entries above the threshold
     uint32_t* tie;     // [R][words] bitmap of entries equal to the threshold

@@ -156,6 +156,16 @@ static csahca_status index_scores_launch(const void* q_idx, csahca_dtype q_dtype
             return e == cudaSuccess ? CSAHCA_OK : CSAHCA_ERR_CUDA;
         }
     }
+    if (index_prefill_supported(q_dtype, key_fmt, H_I, d_I, Ncap, q_idx, k_codes, B, T)) {
+        unsigned* err = err_word();
+        if (!err) return CSAHCA_ERR_CUDA;
+        const cudaError_t e = index_prefill_launch(q_idx, w, k_codes, B, T, H_I, q_pos, Ncap, m, S, hist1, err, st);
+        if (e != cudaErrorNotSupported) {
+            count_launch();
+            if (hist_done) *hist_done = hist1 != nullptr;
+            return e == cudaSuccess ? CSAHCA_OK : CSAHCA_ERR_CUDA;
+        }
+    }
     dim3 grid((unsigned)cdiv(Ncap, 256), (unsigned)R);
     const size_t smem = (size_t)(H_I * d_I + H_I) * 4;
     if (H_I <= 16)

@@ -15,13 +15,20 @@
 // (largest element into [2^7, 2^8)) and split exactly as q' = hi + 2^-5 lo with hi = e4m3(q') and
 // lo = 32 (q' - hi): the remainder has at most 3 significant bits, so lo is an e4m3 value.  The
 // B operand stacks the hi rows over the lo rows (N = 2 H_I), so one MMA per 32-code block gives
-// both parts and the epilogue forms D_hi + 2^-5 D_lo.  (Elements below 2^-13 of their head's
-// largest element are the exception: lo is then rounded, an error below 2^-20 of that largest
-// element.)  2^-e_h is folded into the head weight w'.  Block scales (e2m1: one per 32 codes, so
-// two accumulators per key) or the row scale (e4m3) are applied in the epilogue, on pairs of
-// heads with f32x2 arithmetic: score = sum_h w'_h ReLU(sum_blocks s_block (D_hi + 2^-5 D_lo)[h]).
-// Apart from that the result differs from exact arithmetic only by the rounding of the fp32
-// accumulation.
+// both parts.  (Elements below 2^-13 of their head's largest element are the exception: lo is
+// then rounded, an error below 2^-20 of that largest element; so are heads whose largest element
+// is below 2^-114, whose exponent is capped.)
+//   e2m1 keys (UE8M0 per 32 codes): the MMA applies every scale (kind::mxf8f6f4 block_scale): a
+//     key's factor for its code block is the A scale of its row, 2^-e_h (hi rows) and 2^-(e_h+5)
+//     (lo rows) are the B scales, so the accumulator of a key holds D_hi + D_lo = q . khat per
+//     head directly and the epilogue forms score = sum_h w_h ReLU(D_hi[h] + D_lo[h]).  The scale
+//     factors reach TMEM with tcgen05.cp: the MMA warp rearranges a stage's 512 scale bytes into
+//     the 32-row x 16-byte form (row r's four bytes -- even key blocks 0/1, odd key blocks 0/1 --
+//     in word r / 32 of line r % 32), the producer writes the query's factors with its image.
+//   e4m3 keys (fp32 row scale): kind::f8f6f4; 2^-e_h is folded into the head weight w' and the
+//     row scale applied in the epilogue: score = s_key sum_h w'_h ReLU(D_hi[h] + 2^-5 D_lo[h]).
+// The epilogue works on pairs of heads with f32x2 arithmetic.  Apart from the exceptions above the
+// result differs from exact arithmetic only by the rounding of the fp32 accumulation.
 //
 // Warp roles (persistent CTAs over (row, chunk of 8 stages) work items):
 //   warp 4     producer: per work item, the q image and folded head weights of its row into one of
@@ -29,7 +36,8 @@
 //              the stage's (row, first key, visible count, flags) record, the TMA box of codes and
 //              a bulk copy of the scales;
 //   warp 5     one thread issues the MMAs of a stage into a TMEM accumulator buffer (two buffers
-//              when they fit in the 512 columns);
+//              when they fit in the 512 columns); with e2m1 keys the warp first lays out the
+//              stage's scale factors and copies them (and a new query's) into TMEM;
 //   warps 0-3  epilogue: thread j owns TMEM lane j (keys 2j and 2j+1 of the stage): scores to
 //              global memory, and the top-12-bit histogram of the scores (the top-k's first pass),
 //              accumulated per piece in shared memory (16-bit counts; a piece has at most 128
@@ -60,12 +68,13 @@ enum : uint32_t { kE4M3 = 0, kE2M1 = 5 };   // kind::f8f6f4 operand formats
 constexpr float kLoScale = 0.03125f;         // lo rows of the query operand carry 32 x the remainder
 
 constexpr int kSchedRows = 256;       // balanced piece schedule for up to this many query rows
+constexpr int kMaxBuf = 4;            // TMEM accumulator buffers (at most)
 
 struct alignas(16) IdxMisc {
     alignas(16) uint32_t hist[2048];      // top-12-bit histogram of the scores since the last flush:
                                           // bin b is the 16-bit half (b & 1) of word b >> 1 (at most
                                           // kMaxPieceStages x 256 keys); read and cleared as uint4
-    uint64_t full[kMaxNS], empty[kMaxNS], dfull[2], dfree[2], qfree[2];
+    uint64_t full[kMaxNS], empty[kMaxNS], dfull[kMaxBuf], dfree[kMaxBuf], qfree[2];
     uint32_t tmem_base;
     int soff[kSchedRows + 1];             // piece schedule: first stage of each row (producer only)
     int nvis[kSchedRows];                 // and its visible entries
@@ -74,18 +83,20 @@ static_assert(offsetof(IdxMisc, hist) % 16 == 0 && offsetof(IdxMisc, full) % 8 =
 
 template <int FMT, int HI>
 struct Cfg {
-    static constexpr bool fp4 = FMT == CSAHCA_E2M1_UE8M0;
-    static constexpr int nacc = fp4 ? 2 : 1;                         // accumulators per key
+    static constexpr bool fp4 = FMT == CSAHCA_E2M1_UE8M0;            // block scales applied by the MMA
     static constexpr uint32_t code_tx = fp4 ? kPair * 32 : kPair * 64;  // global code bytes per stage
     static constexpr int scale_bytes = fp4 ? 2 : 4;                  // per key
-    // stage: codes (128 rows x 128 B, swizzled) | scales | record
+    // stage: codes (128 rows x 128 B, swizzled) | scales (fp4: 512 B, then the 512-byte factor
+    // image the MMA warp builds; e4m3: 1 KB) | record
     static constexpr uint32_t off_scale = 16384;
+    static constexpr uint32_t off_sfa = off_scale + 512;
     static constexpr uint32_t off_meta = off_scale + kPair * 4;
     static constexpr uint32_t stage = (off_meta + 16 + 1023) / 1024 * 1024;
     // query slot (one per work item, two in flight): q image (2 HI rows x 128 B: hi rows, then
-    // lo rows, codes in the first 64 bytes) | w'
+    // lo rows, codes in the first 64 bytes) | head weights | (fp4) the B scale-factor image
     static constexpr uint32_t q_img = 2 * HI * 128;
-    static constexpr uint32_t q_slot = (q_img + HI * 4 + 1023) / 1024 * 1024;
+    static constexpr uint32_t off_sfb = (q_img + HI * 4 + 15) / 16 * 16;
+    static constexpr uint32_t q_slot = ((fp4 ? off_sfb + 512 : q_img + HI * 4) + 1023) / 1024 * 1024;
     // as many stages as leave room for two CTAs per SM (228 KB, 1 KB reserved per CTA, 1 KB
     // alignment slack, the static shared memory)
     static constexpr int ns_fit = (int)((114 * 1024 - 1024 - 1024 - sizeof(IdxMisc) - 2 * q_slot) / stage);
@@ -93,22 +104,34 @@ struct Cfg {
     static constexpr uint32_t off_qslots = NS * stage;
     static constexpr uint32_t smem = off_qslots + 2 * q_slot;
     static constexpr uint32_t acc_cols = 2 * HI;                     // one accumulator: hi | lo columns
-    static constexpr uint32_t d_cols = 2 * nacc * acc_cols;          // even + odd keys
-    static constexpr int nbuf = 2 * d_cols <= 512 ? 2 : 1;           // accumulator buffers
-    static constexpr uint32_t tmem_cols = nbuf * d_cols;
-    static_assert(tmem_cols >= 32 && tmem_cols <= 512 && (tmem_cols & (tmem_cols - 1)) == 0, "TMEM columns");
+    static constexpr uint32_t d_cols = 2 * acc_cols;                 // even + odd keys
+    // fp4: scale factors of A (4 columns per stage slot) and B (4 per query slot)
+    static constexpr uint32_t sf_cols = fp4 ? 4 * kMaxNS + 8 : 0;
+    // accumulator buffers: the MMA of a stage waits for the epilogue to have read the buffer of the
+    // stage nbuf earlier, so more buffers keep more stages between the two in flight; as many as
+    // fit in 256 columns (two CTAs per SM), else in 512
+    static constexpr int fit256 = (int)((256 - sf_cols) / d_cols), fit512 = (int)((512 - sf_cols) / d_cols);
+    static constexpr int nbuf = fit256 >= 2 ? (fit256 < kMaxBuf ? fit256 : kMaxBuf)
+                                            : (fit512 < kMaxBuf ? (fit512 < 1 ? 1 : fit512) : kMaxBuf);
+    static constexpr uint32_t sfa_col = nbuf * d_cols, sfb_col = sfa_col + 4 * kMaxNS;
+    static constexpr uint32_t used_cols = nbuf * d_cols + sf_cols;
+    static constexpr uint32_t tmem_cols = used_cols <= 32 ? 32 : used_cols <= 64 ? 64 : used_cols <= 128 ? 128
+                                          : used_cols <= 256 ? 256 : 512;
+    static_assert(used_cols <= 512, "TMEM columns");
     static_assert(HI % 16 == 0 && HI <= 64, "heads");
+    static_assert(!fp4 || off_sfa + 512 <= off_meta, "fp4 stage layout");
     // the next item's query row is loaded one item ahead when its share fits in a few registers
     static constexpr bool prefetch_q = HI <= 16;
 };
 
-
 // One lane's share of the q image of a row: unit (head h, half hf) = lane + 32 j covers 32
 // elements of head h and yields two 16-byte chunks of hi codes and two of lo codes (lo = 32 x the
-// remainder, e4m3); returns the folded weight w'_h in wq[j].  `raw` holds the unit's 32 values.
-template <int HI>
+// remainder, e4m3); returns the head's exponent e_h in exq[j] and its weight in wq[j] (with FOLD,
+// the folded weight w_h 2^-e_h).  `raw` holds the unit's 32 values.
+template <int HI, bool FOLD>
 __device__ __forceinline__ void make_q_image(const uint4 (&raw)[2 * HI / 32][4], const float* __restrict__ w_row,
-                                             int lane, uint4 (&img)[2 * HI / 32][4], float (&wq)[2 * HI / 32]) {
+                                             int lane, uint4 (&img)[2 * HI / 32][4], float (&wq)[2 * HI / 32],
+                                             int (&exq)[2 * HI / 32]) {
     constexpr int kUnits = 2 * HI / 32;
 #pragma unroll
     for (int j = 0; j < kUnits; ++j) {
@@ -130,7 +153,7 @@ __device__ __forceinline__ void make_q_image(const uint4 (&raw)[2 * HI / 32][4],
         int ex = 0;
         if (amax > 0.0f) {
             frexpf(amax, &ex);                  // amax in [2^(ex-1), 2^ex)
-            ex = 8 - ex;                        // amax * 2^ex in [2^7, 2^8)
+            ex = min(8 - ex, 122);              // amax * 2^ex in [2^7, 2^8) (capped: UE8M0 range)
         }
         uint32_t hw[8], lw[8];
 #pragma unroll
@@ -150,7 +173,8 @@ __device__ __forceinline__ void make_q_image(const uint4 (&raw)[2 * HI / 32][4],
         img[j][1] = make_uint4(hw[4], hw[5], hw[6], hw[7]);
         img[j][2] = make_uint4(lw[0], lw[1], lw[2], lw[3]);
         img[j][3] = make_uint4(lw[4], lw[5], lw[6], lw[7]);
-        wq[j] = ldexpf(w_row[h], -ex);
+        wq[j] = FOLD ? ldexpf(w_row[h], -ex) : w_row[h];
+        exq[j] = ex;
     }
 }
 
@@ -192,11 +216,11 @@ __global__ void __launch_bounds__(kThreads) index_tc_kernel(const __grid_constan
             mbar_init(&ms.full[s], 1);
             mbar_init(&ms.empty[s], 5);       // MMA commit + 4 epilogue warps
         }
-        for (int d = 0; d < 2; ++d) {
+        for (int d = 0; d < kMaxBuf; ++d) {
             mbar_init(&ms.dfull[d], 1);
             mbar_init(&ms.dfree[d], 4);
-            mbar_init(&ms.qfree[d], 5);       // MMA commit + 4 epilogue warps, once per item
         }
+        for (int d = 0; d < 2; ++d) mbar_init(&ms.qfree[d], 5);   // MMA commit + 4 epilogue warps, once per item
         fence_mbar_init();
     }
     if (tid < kEpi)
@@ -320,7 +344,8 @@ __global__ void __launch_bounds__(kThreads) index_tc_kernel(const __grid_constan
             if (!C::prefetch_q) load_q_raw<HI>(q_idx + (int64_t)r * HI * kDI, lane, raw);
             uint4 img[kUnits][4];
             float wq[kUnits];
-            make_q_image<HI>(raw, w + (int64_t)r * HI, lane, img, wq);
+            int exq[kUnits];
+            make_q_image<HI, !C::fp4>(raw, w + (int64_t)r * HI, lane, img, wq, exq);
             unsigned char* qsl = sm + C::off_qslots + qs * C::q_slot;
 #pragma unroll
             for (int j = 0; j < kUnits; ++j) {
@@ -328,7 +353,17 @@ __global__ void __launch_bounds__(kThreads) index_tc_kernel(const __grid_constan
 #pragma unroll
                 for (int c = 0; c < 4; ++c)                       // hi: row h, lo: row HI + h
                     *reinterpret_cast<uint4*>(qsl + sw128(h + (c >> 1) * HI, 2 * hf + (c & 1))) = img[j][c];
-                if (hf == 0) reinterpret_cast<float*>(qsl + C::q_img)[h] = wq[j];
+                if (hf == 0) {
+                    reinterpret_cast<float*>(qsl + C::q_img)[h] = wq[j];
+                    if (C::fp4) {
+                        // B scale factors (every K block alike): column n's byte in word n / 32 of
+                        // line n % 32; hi column h: 2^-e_h, lo column HI + h: 2^-(e_h + 5)
+                        uint32_t* sfb = reinterpret_cast<uint32_t*>(qsl + C::off_sfb);
+                        const int nl = HI + h;
+                        sfb[(h & 31) * 4 + (h >> 5)] = (uint32_t)(127 - exq[j]) * 0x01010101u;
+                        sfb[(nl & 31) * 4 + (nl >> 5)] = (uint32_t)(122 - exq[j]) * 0x01010101u;
+                    }
+                }
             }
             fence_proxy_async();
             __syncwarp();
@@ -340,7 +375,7 @@ __global__ void __launch_bounds__(kThreads) index_tc_kernel(const __grid_constan
                     if (u >= (uint32_t)C::NS) mbar_wait(&ms.empty[s], ((u / C::NS) + 1) & 1, err);
                     unsigned char* st = sm + s * C::stage;
                     const uint32_t sb = sbase + s * C::stage;
-                    const int flags = ((s0 + kPair >= s_end) ? kLast : 0) | (int)(qs << 8);
+                    const int flags = ((s0 + kPair >= s_end) ? kLast : 0) | (int)(qs << 8) | (int)((it & 0x7FFFu) << 16);
                     *reinterpret_cast<int4*>(st + C::off_meta) = make_int4(r, (int)s0, (int)n, flags);
                     const int64_t key0 = (int64_t)b * Ncap + s0;
                     const int64_t nk = (Ncap - s0) < kPair ? (Ncap - s0) : kPair;   // Ncap % 8 == 0
@@ -362,38 +397,63 @@ __global__ void __launch_bounds__(kThreads) index_tc_kernel(const __grid_constan
         __syncwarp();
     } else if (warp == 5) {
         // ============================================================================= MMA
-        if (lane == 0) {
-            constexpr uint32_t af = C::fp4 ? kE2M1 : kE4M3;
-            const uint32_t id = idesc_f8f6f4(128, 2 * HI, af, kE4M3);
-            // descriptors of stage 0 and query slot 0; other addresses add (offset >> 4)
-            const uint64_t a_desc0 = smem_desc(sbase, 16, 1024);
-            const uint64_t b_desc0 = smem_desc(sbase + C::off_qslots, 16, 1024);
-            for (uint32_t u = 0;; ++u) {
-                const uint32_t s = u % C::NS;
-                mbar_wait(&ms.full[s], (u / C::NS) & 1, err);
-                const int4 meta = *reinterpret_cast<const int4*>(sm + s * C::stage + C::off_meta);
-                if (meta.w & kTerm) break;
-                const uint32_t d = u % C::nbuf, qs = (uint32_t)(meta.w >> 8) & 1u;
+        constexpr uint32_t af = C::fp4 ? kE2M1 : kE4M3;
+        // descriptors of stage 0 and query slot 0; other addresses add (offset >> 4)
+        const uint64_t a_desc0 = smem_desc(sbase, 16, 1024);
+        const uint64_t b_desc0 = smem_desc(sbase + C::off_qslots, 16, 1024);
+        int prev_piece = -1;                      // piece (low 15 bits) of the previous stage
+        for (uint32_t u = 0;; ++u) {
+            const uint32_t s = u % C::NS;
+            mbar_wait(&ms.full[s], (u / C::NS) & 1, err);
+            const int4 meta = *reinterpret_cast<const int4*>(sm + s * C::stage + C::off_meta);
+            if (meta.w & kTerm) break;
+            const uint32_t d = u % C::nbuf, qs = (uint32_t)(meta.w >> 8) & 1u;
+            if (C::fp4) {
+                // A scale factors of the stage: row r (keys 2r, 2r+1) holds four UE8M0 bytes (even
+                // key blocks 0/1, odd key blocks 0/1); lane l gathers rows l, l+32, l+64, l+96
+                // into line l of the 32 x 16-byte image tcgen05.cp reads
+                const uint32_t* sc = reinterpret_cast<const uint32_t*>(sm + s * C::stage + C::off_scale);
+                *reinterpret_cast<uint4*>(sm + s * C::stage + C::off_sfa + 16 * lane) =
+                    make_uint4(sc[lane], sc[lane + 32], sc[lane + 64], sc[lane + 96]);
+                fence_proxy_async();
+            }
+            __syncwarp();
+            if (lane == 0) {
                 if (u >= (uint32_t)C::nbuf) mbar_wait(&ms.dfree[d], ((u / C::nbuf) + 1) & 1, err);
                 fence_after_sync();
                 const uint64_t ad0 = a_desc0 + ((s * C::stage) >> 4);
                 const uint64_t bd0 = b_desc0 + ((qs * C::q_slot) >> 4);
                 const uint32_t dbuf = tmem + d * C::d_cols;
+                if (C::fp4) {
+                    // factors reach TMEM before the MMAs that read them (issued in order by this thread)
+                    const uint32_t sfa = tmem + C::sfa_col + 4 * s, sfb = tmem + C::sfb_col + 4 * qs;
+                    if ((meta.w >> 16) != prev_piece)     // a new piece: its query's B factors
+                        tmem_cp_32x128b_x4(sfb, smem_desc(sbase + C::off_qslots + qs * C::q_slot + C::off_sfb, 16, 128, 0));
+                    tmem_cp_32x128b_x4(sfa, smem_desc(sbase + s * C::stage + C::off_sfa, 16, 128, 0));
 #pragma unroll
-                for (int e = 0; e < 2; ++e) {            // even keys: code columns [0,64); odd: [64,128)
+                    for (int e = 0; e < 2; ++e)              // even keys: code columns [0,64); odd: [64,128)
 #pragma unroll
-                    for (int blk = 0; blk < 2; ++blk) {  // 32-code blocks (one MMA K step each)
-                        const uint32_t dst = dbuf + (C::fp4 ? 2 * e + blk : e) * C::acc_cols;
-                        const uint64_t ad = ad0 + (uint64_t)(e * 4 + blk * 2);
-                        mma_f8f6f4(dst, ad, bd0 + (uint64_t)(blk * 2), id, C::fp4 ? 0u : (uint32_t)(blk > 0));
-                    }
+                        for (int blk = 0; blk < 2; ++blk)    // 32-code blocks (one MMA K step each)
+                            mma_mxf8f6f4_bs(dbuf + e * C::acc_cols, ad0 + (uint64_t)(e * 4 + blk * 2),
+                                            bd0 + (uint64_t)(blk * 2),
+                                            idesc_mxf8f6f4_bs(128, 2 * HI, af, kE4M3, 2 * e + blk, blk), sfa, sfb,
+                                            (uint32_t)(blk > 0));
+                } else {
+                    const uint32_t id = idesc_f8f6f4(128, 2 * HI, af, kE4M3);
+#pragma unroll
+                    for (int e = 0; e < 2; ++e)
+#pragma unroll
+                        for (int blk = 0; blk < 2; ++blk)
+                            mma_f8f6f4(dbuf + e * C::acc_cols, ad0 + (uint64_t)(e * 4 + blk * 2), bd0 + (uint64_t)(blk * 2),
+                                       id, (uint32_t)(blk > 0));
                 }
                 mma_commit(&ms.dfull[d]);
                 mma_commit(&ms.empty[s]);
                 if (meta.w & kLast) mma_commit(&ms.qfree[qs]);
             }
+            prev_piece = meta.w >> 16;
+            __syncwarp();
         }
-        __syncwarp();
     } else {
         // ======================================================================== epilogue
         const uint64_t pol_keep = l2_policy_evict_last();       // the top-k re-reads the scores
@@ -407,27 +467,41 @@ __global__ void __launch_bounds__(kThreads) index_tc_kernel(const __grid_constan
             const uint32_t d = u % C::nbuf, qs = (uint32_t)(meta.w >> 8) & 1u;
             mbar_wait(&ms.dfull[d], (u / C::nbuf) & 1, err);
             fence_after_sync();
-            float se0, se1 = 0.0f, so0, so1 = 0.0f;             // scales of keys 2j (e) and 2j+1 (o)
-            if (C::fp4) {
-                const uint32_t b4 = *reinterpret_cast<const uint32_t*>(st + C::off_scale + 4 * tid);
-                se0 = ue8m0_value(b4 & 0xFFu);
-                se1 = ue8m0_value((b4 >> 8) & 0xFFu);
-                so0 = ue8m0_value((b4 >> 16) & 0xFFu);
-                so1 = ue8m0_value(b4 >> 24);
-            } else {
+            float se = 1.0f, so = 1.0f;                      // e4m3: row scales of keys 2j (e), 2j+1 (o)
+            if (!C::fp4) {
                 const float2 f2 = *reinterpret_cast<const float2*>(st + C::off_scale + 8 * tid);
-                se0 = f2.x;
-                so0 = f2.y;
+                se = f2.x;
+                so = f2.y;
             }
-            // the stage's record and scales are in registers: release it (with the MMA commit)
+            // the stage's record (and scales) are in registers: release it (with the MMA commit)
             __syncwarp();
             if (lane == 0) mbar_arrive(&ms.empty[s]);
             const float4* wq4 = reinterpret_cast<const float4*>(sm + C::off_qslots + qs * C::q_slot + C::q_img);
             const uint32_t dbuf = tmem + d * C::d_cols + lane_off;
-            // per key: pairs of heads (h, h+1) in f32x2 lanes; the fp4 block scales and the lo
-            // factor 2^-5 are broadcast pairs.  When the stage's accumulators fit in registers
-            // they are all loaded first and the TMEM buffer is handed back to the MMA warp before
-            // the arithmetic.
+            // per key: pairs of heads (h, h+1) in f32x2 lanes, v = D_hi + D_lo (fp4: scaled by the
+            // MMA) or D_hi + 2^-5 D_lo (e4m3).  When the stage's accumulators fit in registers they
+            // are all loaded first and the TMEM buffer is handed back to the MMA warp before the
+            // arithmetic.
+            const uint64_t Ll = f2_pack(kLoScale, kLoScale);
+            auto head_pairs = [&](uint64_t& acc, const uint32_t* hv, const uint32_t* lv, const uint64_t* wv) {
+#pragma unroll
+                for (int k = 0; k < 16; k += 2) {
+                    const uint64_t hp = f2_pack(__uint_as_float(hv[k]), __uint_as_float(hv[k + 1]));
+                    const uint64_t lp = f2_pack(__uint_as_float(lv[k]), __uint_as_float(lv[k + 1]));
+                    const uint64_t v = C::fp4 ? f2_add(hp, lp) : f2_fma(Ll, lp, hp);
+                    float a0, a1;
+                    f2_unpack(v, a0, a1);
+                    acc = f2_fma(wv[k / 2], f2_pack(fmaxf(a0, 0.0f), fmaxf(a1, 0.0f)), acc);
+                }
+            };
+            auto weights16 = [&](int c0, uint64_t (&wv)[8]) {
+#pragma unroll
+                for (int k4 = 0; k4 < 4; ++k4) {
+                    const float4 q4 = wq4[c0 / 4 + k4];
+                    wv[2 * k4] = f2_pack(q4.x, q4.y);
+                    wv[2 * k4 + 1] = f2_pack(q4.z, q4.w);
+                }
+            };
             uint64_t acc2[2] = {f2_pack(0.0f, 0.0f), f2_pack(0.0f, 0.0f)};
             if constexpr (C::d_cols <= 128) {
                 uint32_t dv[C::d_cols];
@@ -443,90 +517,29 @@ __global__ void __launch_bounds__(kThreads) index_tc_kernel(const __grid_constan
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&ms.dfree[d]);
 #pragma unroll
-                for (int key = 0; key < 2; ++key) {
-                    const float s0 = key ? so0 : se0, s1 = key ? so1 : se1;
-                    const uint64_t S0 = f2_pack(s0, s0), S0l = f2_pack(s0 * kLoScale, s0 * kLoScale);
-                    const uint64_t S1 = f2_pack(s1, s1), S1l = f2_pack(s1 * kLoScale, s1 * kLoScale);
-                    const uint64_t Ll = f2_pack(kLoScale, kLoScale);
-                    const int ab = key * C::nacc * (int)C::acc_cols;
+                for (int key = 0; key < 2; ++key)
 #pragma unroll
                     for (int c0 = 0; c0 < HI; c0 += 16) {
                         uint64_t wv[8];
-#pragma unroll
-                        for (int k4 = 0; k4 < 4; ++k4) {
-                            const float4 q4 = wq4[c0 / 4 + k4];
-                            wv[2 * k4] = f2_pack(q4.x, q4.y);
-                            wv[2 * k4 + 1] = f2_pack(q4.z, q4.w);
-                        }
-#pragma unroll
-                        for (int k = 0; k < 16; k += 2) {
-                            const int h = ab + c0 + k, l = h + HI;
-                            uint64_t v;
-                            if (C::fp4) {
-                                const int h1 = h + (int)C::acc_cols, l1 = h1 + HI;
-                                v = f2_mul(S0l, f2_pack(__uint_as_float(dv[l]), __uint_as_float(dv[l + 1])));
-                                v = f2_fma(S0, f2_pack(__uint_as_float(dv[h]), __uint_as_float(dv[h + 1])), v);
-                                v = f2_fma(S1l, f2_pack(__uint_as_float(dv[l1]), __uint_as_float(dv[l1 + 1])), v);
-                                v = f2_fma(S1, f2_pack(__uint_as_float(dv[h1]), __uint_as_float(dv[h1 + 1])), v);
-                            } else {
-                                v = f2_fma(Ll, f2_pack(__uint_as_float(dv[l]), __uint_as_float(dv[l + 1])),
-                                           f2_pack(__uint_as_float(dv[h]), __uint_as_float(dv[h + 1])));
-                            }
-                            float a0, a1;
-                            f2_unpack(v, a0, a1);
-                            acc2[key] = f2_fma(wv[k / 2], f2_pack(fmaxf(a0, 0.0f), fmaxf(a1, 0.0f)), acc2[key]);
-                        }
+                        weights16(c0, wv);
+                        const int h = key * (int)C::acc_cols + c0;
+                        head_pairs(acc2[key], dv + h, dv + h + HI, wv);
                     }
-                }
             } else {
 #pragma unroll
                 for (int key = 0; key < 2; ++key) {
-                    const float s0 = key ? so0 : se0, s1 = key ? so1 : se1;
-                    const uint64_t S0 = f2_pack(s0, s0), S0l = f2_pack(s0 * kLoScale, s0 * kLoScale);
-                    const uint64_t S1 = f2_pack(s1, s1), S1l = f2_pack(s1 * kLoScale, s1 * kLoScale);
-                    const uint64_t Ll = f2_pack(kLoScale, kLoScale);
-                    const uint32_t abase = dbuf + key * C::nacc * C::acc_cols;
+                    const uint32_t abase = dbuf + key * C::acc_cols;
 #pragma unroll
                     for (int c0 = 0; c0 < HI; c0 += 16) {
                         uint64_t wv[8];
-#pragma unroll
-                        for (int k4 = 0; k4 < 4; ++k4) {
-                            const float4 q4 = wq4[c0 / 4 + k4];
-                            wv[2 * k4] = f2_pack(q4.x, q4.y);
-                            wv[2 * k4 + 1] = f2_pack(q4.z, q4.w);
-                        }
+                        weights16(c0, wv);
                         uint32_t h0[16], l0[16];
                         tmem_ld16(abase + c0, h0);
                         tmem_ld16(abase + HI + c0, l0);
-                        if (C::fp4) {
-                            uint32_t h1[16], l1[16];
-                            tmem_ld16(abase + C::acc_cols + c0, h1);
-                            tmem_ld16(abase + C::acc_cols + HI + c0, l1);
-                            tmem_wait_ld();
-#pragma unroll
-                            for (int k = 0; k < 16; k += 2) {
-                                uint64_t v = f2_mul(S0l, f2_pack(__uint_as_float(l0[k]), __uint_as_float(l0[k + 1])));
-                                v = f2_fma(S0, f2_pack(__uint_as_float(h0[k]), __uint_as_float(h0[k + 1])), v);
-                                v = f2_fma(S1l, f2_pack(__uint_as_float(l1[k]), __uint_as_float(l1[k + 1])), v);
-                                v = f2_fma(S1, f2_pack(__uint_as_float(h1[k]), __uint_as_float(h1[k + 1])), v);
-                                float a0, a1;
-                                f2_unpack(v, a0, a1);
-                                acc2[key] = f2_fma(wv[k / 2], f2_pack(fmaxf(a0, 0.0f), fmaxf(a1, 0.0f)), acc2[key]);
-                            }
-                        } else {
-                            tmem_wait_ld();
-#pragma unroll
-                            for (int k = 0; k < 16; k += 2) {
-                                const uint64_t v = f2_fma(Ll, f2_pack(__uint_as_float(l0[k]), __uint_as_float(l0[k + 1])),
-                                                          f2_pack(__uint_as_float(h0[k]), __uint_as_float(h0[k + 1])));
-                                float a0, a1;
-                                f2_unpack(v, a0, a1);
-                                acc2[key] = f2_fma(wv[k / 2], f2_pack(fmaxf(a0, 0.0f), fmaxf(a1, 0.0f)), acc2[key]);
-                            }
-                        }
+                        tmem_wait_ld();
+                        head_pairs(acc2[key], h0, l0, wv);
                     }
                 }
-
                 fence_before_sync();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&ms.dfree[d]);
@@ -535,13 +548,9 @@ __global__ void __launch_bounds__(kThreads) index_tc_kernel(const __grid_constan
             {
                 float x0, x1;
                 f2_unpack(acc2[0], x0, x1);
-                acc_e = x0 + x1;
+                acc_e = (x0 + x1) * se;
                 f2_unpack(acc2[1], x0, x1);
-                acc_o = x0 + x1;
-            }
-            if (!C::fp4) {
-                acc_e *= se0;
-                acc_o *= so0;
+                acc_o = (x0 + x1) * so;
             }
             // (at the piece's end) query slot consumed
             __syncwarp();

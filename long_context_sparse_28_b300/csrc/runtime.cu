@@ -1,5 +1,6 @@
 // Library runtime: the device error word, launch bookkeeping and status reporting.
 #include "common.cuh"
+#include "tc_ptx.cuh"
 
 #include <atomic>
 #include <mutex>
@@ -52,6 +53,21 @@ __global__ void zero_words_kernel(uint32_t* __restrict__ p, size_t n) {
 }
 }  // namespace
 
+namespace {
+// One warp waits on an mbarrier that nothing ever arrives on, through the same bounded wait the
+// tensor-core kernels use; the wait gives up after limit_ns, flags CSAHCA_ERR_TIMEOUT in the
+// error word and the kernel returns normally.
+__global__ void bounded_wait_kernel(uint64_t limit_ns, unsigned* err) {
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        tc::mbar_init(&bar, 1);
+        tc::fence_mbar_init();
+    }
+    __syncthreads();
+    (void)tc::mbar_wait(&bar, 0, err, limit_ns);
+}
+}  // namespace
+
 cudaError_t zero_words(uint32_t* p, size_t n, cudaStream_t st) {
     if (n == 0) return cudaSuccess;
     const size_t blocks = (n + 255) / 256;
@@ -90,6 +106,15 @@ const char* csahca_status_string(csahca_status s) {
 }
 
 uint64_t csahca_launch_count(void) { return csahca::g_launches; }
+
+csahca_status csahca_selftest_bounded_wait(uint64_t limit_ns, csahca_stream_t stream) {
+    if (limit_ns == 0 || limit_ns > 1000000000ull) return CSAHCA_ERR_INVALID_ARG;
+    unsigned* err = csahca::err_word();
+    if (!err) return CSAHCA_ERR_CUDA;
+    csahca::bounded_wait_kernel<<<1, 32, 0, (cudaStream_t)stream>>>(limit_ns, err);
+    csahca::count_launch();
+    return cudaGetLastError() == cudaSuccess ? CSAHCA_OK : CSAHCA_ERR_CUDA;
+}
 
 int csahca_version(void) { return 1; }
 

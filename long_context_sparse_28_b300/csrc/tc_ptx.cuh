@@ -357,3 +357,42 @@ __device__ __forceinline__ float redux_max_f32(float v) {
 
 }  // namespace tc
 }  // namespace csahca
+
+namespace csahca {
+namespace tc {
+
+// Copies a 32-row x 128-bit matrix from shared memory (described by `desc`, no swizzle) into
+// TMEM columns [taddr, taddr + 4), replicated into all four 32-lane quarters (warpx4).  This is
+// the form block-scale factors take in TMEM: for an M = 128 operand, row r's factor is byte k of
+// column (r / 32) in lane r % 32 (of every quarter), k the scale-factor id of the MMA.
+__device__ __forceinline__ void tmem_cp_32x128b_x4(uint32_t taddr, uint64_t desc) {
+    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(desc) : "memory");
+}
+// D[tmem] (+)= (A * 2^sfa) x (B * 2^sfb) with 8-, 6- or 4-bit operands and one UE8M0 scale per
+// row of A / column of B per 32-element K block (kind::mxf8f6f4, block_scale, scale_vec::1X).
+// sfa_tmem / sfb_tmem: TMEM addresses of the factor columns; the byte within each 32-bit factor
+// word is chosen by the ids in the instruction descriptor.
+__device__ __forceinline__ void mma_mxf8f6f4_bs(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                                uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%5], [%6], p;\n\t}"
+        ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(sfa_tmem), "r"(sfb_tmem)
+        : "memory");
+}
+// Instruction descriptor of kind::mxf8f6f4 with UE8M0 block scales, fp32 accumulator, both
+// operands K-major; a_id / b_id pick the factor byte (0..3) of A and B.
+__host__ __device__ constexpr uint32_t idesc_mxf8f6f4_bs(int M, int N, uint32_t a_fmt, uint32_t b_fmt, uint32_t a_id,
+                                                         uint32_t b_id) {
+    return (b_id << 4) | (a_fmt << 7) | (b_fmt << 10) | ((uint32_t)(N >> 3) << 17) | (1u << 23) |
+           ((uint32_t)(M >> 4) << 24) | (a_id << 29);
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+}  // namespace tc
+}  // namespace csahca

@@ -136,40 +136,66 @@ class HCADecode:
         return self.out, self.lse
 
 
+class HybridPrefill:
+    """Chunked prefill of chunks of T tokens through a CSA layer and an HCA layer (B sequences, all
+    at the same chunk position).  Per chunk: compress its complete blocks into both caches,
+    quantise the new index keys, run CSA (indexer, top-k, sparse attention with the causal
+    window) and HCA (dense, causal) for every query of the chunk, then move the chunk's last
+    tokens into both rings.  Outputs and workspaces are allocated once, so a chunk's calls can be
+    captured in a CUDA graph."""
+
+    def __init__(self, csa: CSACache, hca: HCACache, T, H, k, csa_bias, hca_bias, scale=None):
+        B, d, dev = csa.B, csa.d, csa.device
+        self.csa, self.hca, self.T, self.H, self.k = csa, hca, T, H, k
+        self.csa_bias, self.hca_bias = csa_bias, hca_bias
+        self.scale = 1.0 / math.sqrt(d) if scale is None else scale
+        self.q_pos = torch.empty(B * T, dtype=torch.int64, device=dev)
+        self.p0 = torch.empty(B, dtype=torch.int64, device=dev)
+        self.nT = torch.full((B,), T, dtype=torch.int64, device=dev)
+        self.idx = torch.empty(B, T, k, dtype=torch.int32, device=dev)
+        self.out_c = torch.empty(B, T, H, d, dtype=csa.dtype, device=dev)
+        self.lse_c = torch.empty(B, T, H, dtype=torch.float32, device=dev)
+        self.out_h = torch.empty(B, T, H, d, dtype=hca.dtype, device=dev)
+        self.lse_h = torch.empty(B, T, H, dtype=torch.float32, device=dev)
+        self.ws_topk = torch.empty(csa_index_topk_workspace(B, T, csa.Ncap, k), dtype=torch.uint8, device=dev)
+        self.ws_ca = torch.empty(max(256, csa_attend_workspace(B, T, H, d, k, csa.W)), dtype=torch.uint8, device=dev)
+        self.ws_ha = torch.empty(max(256, hca_attend_workspace(B, T, H, d, hca.Ncap, hca.W, 0)), dtype=torch.uint8,
+                                 device=dev)
+
+    def set_position(self, pos0):
+        """Position of the next chunk's first token (a multiple of both block sizes)."""
+        assert pos0 % self.csa.m == 0 and pos0 % self.hca.m == 0
+        B, T, dev = self.csa.B, self.T, self.csa.device
+        self.pos0 = int(pos0)
+        self.p0.fill_(pos0)
+        self.q_pos.copy_((torch.arange(T, device=dev, dtype=torch.int64)[None, :] + pos0).repeat(B, 1).reshape(-1))
+
+    def step(self, chunk_k, chunk_v, chunk_gate, kidx_chunk, q_csa, q_idx, w, q_hca, scores_out=None):
+        """chunk_k/v [B, T, d]; chunk_gate [B, T]; kidx_chunk [B, T // m_csa, d_I] (index keys of the
+        new CSA entries); q_csa/q_hca [B, T, H, d]; q_idx [B, T, H_I, d_I]; w [B, T, H_I]."""
+        csa, hca, T = self.csa, self.hca, self.T
+        csa_compress(chunk_k, chunk_v, chunk_gate, self.p0, self.nT, self.csa_bias, csa.m, csa.ck, csa.cv)
+        hca_compress(chunk_k, chunk_v, chunk_gate, self.p0, self.nT, self.hca_bias, hca.m, hca.ck, hca.cv)
+        j0, nb = self.pos0 // csa.m, T // csa.m
+        for b in range(csa.B):
+            csa_index_key_quantize(kidx_chunk[b, :nb], csa.key_fmt, csa.k_codes[b, j0:j0 + nb],
+                                   None if csa.k_scale is None else csa.k_scale[b, j0:j0 + nb])
+        csa_index_topk(q_idx, w, csa.k_codes, csa.k_scale, csa.key_fmt, self.q_pos, csa.m, self.k, self.idx,
+                       scores_out=scores_out, workspace=self.ws_topk)
+        csa_attend(q_csa, self.scale, csa.ck, csa.cv, self.idx, csa.ring_k, csa.ring_v, csa.W, self.q_pos,
+                   self.out_c, self.lse_c, chunk_k=chunk_k, chunk_v=chunk_v, chunk_pos0=self.p0, workspace=self.ws_ca)
+        hca_attend(q_hca, self.scale, hca.ck, hca.cv, hca.m, hca.ring_k, hca.ring_v, hca.W, self.q_pos, self.out_h,
+                   self.lse_h, chunk_k=chunk_k, chunk_v=chunk_v, chunk_pos0=self.p0, workspace=self.ws_ha)
+        swa_ring_write(chunk_k, chunk_v, chunk_gate, self.p0, T, csa.ring_k, csa.ring_v, csa.ring_gate)
+        swa_ring_write(chunk_k, chunk_v, chunk_gate, self.p0, T, hca.ring_k, hca.ring_v, hca.ring_gate)
+        return dict(idx=self.idx, csa_out=self.out_c, csa_lse=self.lse_c, hca_out=self.out_h, hca_lse=self.lse_h,
+                    q_pos=self.q_pos)
+
+
 def hybrid_prefill_chunk(csa: CSACache, hca: HCACache, pos0, T, chunk_k, chunk_v, chunk_gate, kidx_chunk,
                          q_csa, q_idx, w, q_hca, csa_bias, hca_bias, k, scale=None, scores_out=None):
-    """Chunked prefill of one chunk of T tokens starting at position pos0 (B sequences, same
-    pos0): compress the chunk's complete blocks into both caches, quantise the new index keys,
-    run CSA (indexer, top-k, sparse attention with the causal window) and HCA (dense, causal)
-    for every query of the chunk, then move the chunk's last tokens into both rings.
-
-    chunk_k/v [B, T, d]; chunk_gate [B, T]; kidx_chunk [B, T // m_csa, d_I] (index keys of the
-    new CSA entries); q_csa/q_hca [B, T, H, d]; q_idx [B, T, H_I, d_I]; w [B, T, H_I].
-    pos0 must be a multiple of both block sizes.  Returns dict of outputs."""
-    B, _, d = chunk_k.shape
-    dev = csa.device
-    scale = 1.0 / math.sqrt(d) if scale is None else scale
-    assert pos0 % csa.m == 0 and pos0 % hca.m == 0
-    p0 = _i64([pos0] * B, dev)
-    nT = _i64([T] * B, dev)
-    csa_compress(chunk_k, chunk_v, chunk_gate, p0, nT, csa_bias, csa.m, csa.ck, csa.cv)
-    hca_compress(chunk_k, chunk_v, chunk_gate, p0, nT, hca_bias, hca.m, hca.ck, hca.cv)
-    j0, nb = pos0 // csa.m, T // csa.m
-    for b in range(B):
-        csa_index_key_quantize(kidx_chunk[b, :nb].contiguous(), csa.key_fmt, csa.k_codes[b, j0:j0 + nb],
-                               None if csa.k_scale is None else csa.k_scale[b, j0:j0 + nb])
-    q_pos = (torch.arange(T, device=dev, dtype=torch.int64)[None, :] + pos0).repeat(B, 1).reshape(-1).contiguous()
-    H = q_csa.shape[2]
-    idx = torch.empty(B, T, k, dtype=torch.int32, device=dev)
-    csa_index_topk(q_idx, w, csa.k_codes, csa.k_scale, csa.key_fmt, q_pos, csa.m, k, idx, scores_out=scores_out)
-    out_c = torch.empty(B, T, H, d, dtype=csa.dtype, device=dev)
-    lse_c = torch.empty(B, T, H, dtype=torch.float32, device=dev)
-    csa_attend(q_csa, scale, csa.ck, csa.cv, idx, csa.ring_k, csa.ring_v, csa.W, q_pos, out_c, lse_c,
-               chunk_k=chunk_k, chunk_v=chunk_v, chunk_pos0=p0)
-    out_h = torch.empty(B, T, H, d, dtype=hca.dtype, device=dev)
-    lse_h = torch.empty(B, T, H, dtype=torch.float32, device=dev)
-    hca_attend(q_hca, scale, hca.ck, hca.cv, hca.m, hca.ring_k, hca.ring_v, hca.W, q_pos, out_h, lse_h,
-               chunk_k=chunk_k, chunk_v=chunk_v, chunk_pos0=p0)
-    swa_ring_write(chunk_k, chunk_v, chunk_gate, p0, T, csa.ring_k, csa.ring_v, csa.ring_gate)
-    swa_ring_write(chunk_k, chunk_v, chunk_gate, p0, T, hca.ring_k, hca.ring_v, hca.ring_gate)
-    return dict(idx=idx, csa_out=out_c, csa_lse=lse_c, hca_out=out_h, hca_lse=lse_h, q_pos=q_pos)
+    """One chunk of T tokens at position pos0 through both layers (see ``HybridPrefill``).
+    Returns dict of outputs."""
+    step = HybridPrefill(csa, hca, T, q_csa.shape[2], k, csa_bias, hca_bias, scale)
+    step.set_position(pos0)
+    return step.step(chunk_k, chunk_v, chunk_gate, kidx_chunk, q_csa, q_idx, w, q_hca, scores_out=scores_out)

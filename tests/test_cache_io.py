@@ -85,3 +85,49 @@ def test_damaged_or_mismatched_files_are_refused(tmp_path):
         cache_io.load_prefix_into(str(p), small, 0)
     with pytest.raises(ValueError, match="do not fit"):
         cache_io.save_prefix(str(tmp_path / "c.kv"), src, [4 * 17])
+
+
+def _rewrite_header(raw: bytes, header: dict) -> bytes:
+    """The file with its JSON header replaced (tensor data re-aligned after it)."""
+    import json
+    n = struct.unpack("<I", raw[12:16])[0]
+    start = (16 + n + 255) // 256 * 256
+    hdr = json.dumps(header).encode()
+    new_start = (16 + len(hdr) + 255) // 256 * 256
+    return raw[:12] + struct.pack("<I", len(hdr)) + hdr + b"\0" * (new_start - 16 - len(hdr)) + raw[start:]
+
+
+@pytest.mark.parametrize("edit", ["drop_seqs", "drop_dtype", "bad_kind", "tensor_no_seq", "negative_shape",
+                                  "seq_out_of_range", "shape_not_list", "not_object"])
+def test_malformed_headers_are_refused_with_value_error(tmp_path, edit):
+    src = _fill(HCACache(2, 8, 64, 16, torch.bfloat16, "cpu", m=128), 6)
+    p = tmp_path / "a.kv"
+    cache_io.save_prefix(str(p), src, [128 * 3, 128 * 2])
+    raw = p.read_bytes()
+    header, _ = cache_io.read_header(str(p))
+    h = dict(header)
+    t0 = dict(h["tensors"][0])
+    if edit == "drop_seqs":
+        del h["seqs"]
+    elif edit == "drop_dtype":
+        del h["dtype"]
+    elif edit == "bad_kind":
+        h["kind"] = "mla"
+    elif edit == "tensor_no_seq":
+        del t0["seq"]
+    elif edit == "negative_shape":
+        t0["shape"] = [-3, 64]
+    elif edit == "seq_out_of_range":
+        t0["seq"] = 5
+    elif edit == "shape_not_list":
+        t0["shape"] = "3x64"
+    h["tensors"] = [t0] + h["tensors"][1:]
+    if edit == "not_object":
+        h = [1, 2, 3]
+    bad = tmp_path / "bad.kv"
+    bad.write_bytes(_rewrite_header(raw, h))
+    with pytest.raises(ValueError):
+        cache_io.load_prefix(str(bad), device="cpu")
+    dst = HCACache(2, 8, 64, 16, torch.bfloat16, "cpu", m=128)
+    with pytest.raises(ValueError):
+        cache_io.load_prefix_into(str(bad), dst, 0)

@@ -136,6 +136,35 @@ def test_topk_from_scores_long_rows():
     np.testing.assert_array_equal(npy(idx), oracle.topk(S.astype(np.float64), nv, k))
 
 
+@pytest.mark.parametrize("k", [5000, 9000])
+def test_topk_from_scores_k_above_4096(k):
+    # k = 9000 exceeds the candidate list (8192), so the exact finish runs on whole rows
+    rng = np.random.default_rng(k)
+    R, N = 4, 40000
+    S = rng.standard_normal((R, N)).astype(np.float32)
+    S[1] = np.round(S[1] * 2) / 2                       # heavy ties at the boundary
+    nv = np.array([N, 30001, k - 3, k], dtype=np.int64)
+    idx = torch.empty(R, k, dtype=torch.int32, device="cuda")
+    L.csa_topk_from_scores(torch.from_numpy(S).cuda(), dev_i64(nv), k, idx)
+    np.testing.assert_array_equal(npy(idx), oracle.topk(S.astype(np.float64), nv, k))
+
+
+# ---------------------------------------------------------------- bounded device waits
+def test_bounded_wait_times_out_and_context_survives():
+    # a device wait that nothing completes gives up after its limit, reports a timeout through
+    # the error word, and leaves the context usable
+    torch.cuda.synchronize()
+    assert L.device_status() == 0
+    L.selftest_bounded_wait(2_000_000)
+    assert L.device_status() == 4                       # CSAHCA_ERR_TIMEOUT
+    assert L.device_status() == 0                       # read and cleared
+    S = torch.arange(64, dtype=torch.float32, device="cuda")[None]
+    idx = torch.empty(1, 8, dtype=torch.int32, device="cuda")
+    L.csa_topk_from_scores(S, dev_i64([64]), 8, idx)
+    assert L.device_status() == 0
+    np.testing.assert_array_equal(npy(idx)[0], np.arange(56, 64))
+
+
 # ------------------------------------------------------------------- a5 indexer scores
 @pytest.mark.parametrize("fmt,q_dt,Ncap,H_I", [("f32", "f32", 700, 16), ("bf16", "bf16", 700, 16),
                                                ("e4m3", "bf16", 700, 16), ("e2m1", "bf16", 700, 16),
@@ -169,6 +198,40 @@ def test_index_scores_and_topk_parity(fmt, q_dt, Ncap, H_I):
             got = npy(sc[b, t])[: nv[t]].astype(np.float64)
             scale = np.abs(S[t, : nv[t]]).max() if nv[t] else 1.0
             assert np.abs(got - S[t, : nv[t]]).max(initial=0) <= 1e-5 * scale + 1e-6
+            check_index_set(npy(idx[b, t]), ref[t], S[t], int(nv[t]), k, f"b{b}t{t}")
+
+
+@pytest.mark.parametrize("H_I,T", [(16, 24), (32, 12), (64, 6)])
+def test_prefill_indexer_tensor_core_parity(H_I, T):
+    # bf16 keys and queries with T a multiple of 128 / H_I: the tensor-core prefill kernel (query
+    # rows x heads as one MMA operand); rows straddle several 8192-key chunks and a ragged tail
+    from torch.profiler import ProfilerActivity, profile
+    B, Ncap, d_I, m, k = 2, 20000, 64, 4, 200
+    kin = rnd((B, Ncap, d_I), torch.bfloat16, 41)
+    codes, _ = L.key_storage(B, Ncap, d_I, L.BF16)
+    L.csa_index_key_quantize(kin, L.BF16, codes)
+    q = rnd((B, T, H_I, d_I), torch.bfloat16, 42, 0.125)
+    w = torch.rand(B, T, H_I, generator=torch.Generator().manual_seed(43)).cuda()
+    p0 = [4 * Ncap - T + 3, 4 * 8192 - 5]
+    pos = dev_i64([[p0[b] + t for t in range(T)] for b in range(B)])
+    idx = torch.empty(B, T, k, dtype=torch.int32, device="cuda")
+    sc = torch.full((B, T, Ncap), float("nan"), device="cuda")
+    with profile(activities=[ProfilerActivity.CUDA]) as prof:
+        L.csa_index_topk(q, w, codes, None, L.BF16, pos.reshape(-1), m, k, idx, scores_out=sc)
+        torch.cuda.synchronize()
+    names = [e.name for e in prof.events()]
+    assert any("index_prefill_kernel" in n for n in names), "tensor-core prefill kernel not used"
+    assert not any("index_score_kernel" in n for n in names)
+    assert L.device_status() == 0
+    for b in range(B):
+        khat = oracle.dequant_keys(oracle.KEY_BF16, npy(kin[b]), None, d_I)
+        nv = np.minimum(Ncap, (npy(pos[b]) + 1) // m)
+        S = oracle.index_scores(npy(q[b]), npy(w[b]), khat, nv)
+        ref = oracle.topk(S, nv, k)
+        for t in range(T):
+            got = npy(sc[b, t])[: nv[t]].astype(np.float64)
+            assert np.abs(got - S[t, : nv[t]]).max() <= 1e-5 * np.abs(S[t, : nv[t]]).max() + 1e-6
+            assert np.isnan(npy(sc[b, t])[nv[t]:]).all()         # entries a row does not see: untouched
             check_index_set(npy(idx[b, t]), ref[t], S[t], int(nv[t]), k, f"b{b}t{t}")
 
 

@@ -68,7 +68,8 @@ def test_hca_decode_b4_1m_bf16():
 def test_decode_1m_b32_csa_then_hca():
     w = wl.WORKLOADS["decode_1m_b32_csa_hca"]
     lens = w.lengths()
-    seqs = sorted({int(np.argmin(lens)), int(np.argmax(lens))})
+    order = np.argsort(lens)
+    seqs = sorted({int(order[0]), int(order[len(order) // 3]), int(order[2 * len(order) // 3]), int(order[-1])})
     csa = csa_decode_case(w, seqs, layer="csa")
     _check_csa(csa, seqs, "bf16")
     del csa
@@ -114,8 +115,10 @@ def test_hybrid_prefill_t4096_at_256k():
     rawk = np.concatenate([h["ring_k"], h["chunk_k"]])
     rawv = np.concatenate([h["ring_v"], h["chunk_v"]])
     rng = np.random.default_rng(0)
-    rows = np.unique(np.concatenate([[0, 1, 2, 3, 4, 127, 128, 129, 1023, 2047, 2048, 4095],
-                                     rng.choice(T, 20, replace=False)]))
+    edge = [0, 1, 2, 3, 4, 127, 128, 129, 1023, 2047, 2048, 4095]
+    rest = rng.choice(np.setdiff1d(np.arange(T), edge), 256 - len(edge), replace=False)
+    rows = np.unique(np.concatenate([edge, rest]))
+    assert len(rows) == 256
     pos = o + rows
     ores = oracle.csa_queries(h["q_csa"][rows], h["q_idx"][rows], h["w"][rows], pos, ck_all, cv_all, kidx_all, None,
                               oracle.KEY_BF16, rawk, rawv, o - W, w.m_csa, w.k, W, w.scale)
