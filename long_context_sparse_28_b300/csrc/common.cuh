@@ -191,12 +191,9 @@ cudaError_t index_prefill_launch(const void* q_idx, const float* w, const void* 
 
 // Top-k over float32 scores (rows of `stride`, n_vis per row from q_pos or n_vis arrays).
 struct TopkWorkspace {
-    uint32_t* hist1;   // [R][4096] histogram of the top 12 bits (zeroed with cand_n and done)
-    int* cand_n;       // [R] candidate counts
-    int* done;         // [R] CTAs of the row that have finished collecting
-    uint2* cand;       // [R][cap] (ordered key, index)
-    uint32_t* win;     // [R][words] bitmap of entries above the threshold
-    uint32_t* tie;     // [R][words] bitmap of entries equal to the threshold
+    uint32_t* hist1;   // [R][4096] histogram of the top 12 bits (zeroed before it is accumulated)
+    uint32_t* win;     // [R][words] bitmap of entries above the threshold (rows too long for
+    uint32_t* tie;     // [R][words] bitmap of entries equal to it          shared memory)
     int64_t words;
 };
 size_t topk_workspace_bytes(int64_t R, int64_t stride);

@@ -74,6 +74,7 @@ struct alignas(16) IdxMisc {
     alignas(16) uint32_t hist[2048];      // top-12-bit histogram of the scores since the last flush:
                                           // bin b is the 16-bit half (b & 1) of word b >> 1 (at most
                                           // kMaxPieceStages x 256 keys); read and cleared as uint4
+    alignas(16) int4 dmeta[kMaxBuf];      // record of the stage in each accumulator buffer
     uint64_t full[kMaxNS], empty[kMaxNS], dfull[kMaxBuf], dfree[kMaxBuf], qfree[2];
     uint32_t tmem_base;
     int soff[kSchedRows + 1];             // piece schedule: first stage of each row (producer only)
@@ -99,10 +100,13 @@ struct Cfg {
     static constexpr uint32_t q_slot = ((fp4 ? off_sfb + 512 : q_img + HI * 4) + 1023) / 1024 * 1024;
     // as many stages as leave room for two CTAs per SM (228 KB, 1 KB reserved per CTA, 1 KB
     // alignment slack, the static shared memory)
-    static constexpr int ns_fit = (int)((114 * 1024 - 1024 - 1024 - sizeof(IdxMisc) - 2 * q_slot) / stage);
+    static constexpr int ns_fit = (int)((114 * 1024 - 1024 - 1024 - sizeof(IdxMisc) - 2 * q_slot -
+                                         (fp4 ? 0 : kMaxBuf * kPair * 4)) / stage);
     static constexpr int NS = ns_fit < 3 ? 3 : (ns_fit > kMaxNS ? kMaxNS : ns_fit);
     static constexpr uint32_t off_qslots = NS * stage;
-    static constexpr uint32_t smem = off_qslots + 2 * q_slot;
+    // e4m3: the row scales of the stage in each accumulator buffer (copied by the MMA warp)
+    static constexpr uint32_t off_dscale = off_qslots + 2 * q_slot;
+    static constexpr uint32_t smem = off_dscale + (fp4 ? 0 : kMaxBuf * kPair * 4);
     static constexpr uint32_t acc_cols = 2 * HI;                     // one accumulator: hi | lo columns
     static constexpr uint32_t d_cols = 2 * acc_cols;                 // even + odd keys
     // fp4: scale factors of A (4 columns per stage slot) and B (4 per query slot)
@@ -214,10 +218,10 @@ __global__ void __launch_bounds__(kThreads) index_tc_kernel(const __grid_constan
     if (tid == 0) {
         for (int s = 0; s < C::NS; ++s) {
             mbar_init(&ms.full[s], 1);
-            mbar_init(&ms.empty[s], 5);       // MMA commit + 4 epilogue warps
+            mbar_init(&ms.empty[s], 1);       // the MMA commit: the epilogue never reads a stage
         }
         for (int d = 0; d < kMaxBuf; ++d) {
-            mbar_init(&ms.dfull[d], 1);
+            mbar_init(&ms.dfull[d], 2);       // the MMA commit + the MMA warp's record of the stage
             mbar_init(&ms.dfree[d], 4);
         }
         for (int d = 0; d < 2; ++d) mbar_init(&ms.qfree[d], 5);   // MMA commit + 4 epilogue warps, once per item
@@ -406,8 +410,16 @@ __global__ void __launch_bounds__(kThreads) index_tc_kernel(const __grid_constan
             const uint32_t s = u % C::NS;
             mbar_wait(&ms.full[s], (u / C::NS) & 1, err);
             const int4 meta = *reinterpret_cast<const int4*>(sm + s * C::stage + C::off_meta);
-            if (meta.w & kTerm) break;
             const uint32_t d = u % C::nbuf, qs = (uint32_t)(meta.w >> 8) & 1u;
+            if (meta.w & kTerm) {
+                // end of work: hand the record to the epilogue through the next buffer
+                if (u >= (uint32_t)C::nbuf) mbar_wait(&ms.dfree[d], ((u / C::nbuf) + 1) & 1, err);
+                if (lane == 0) {
+                    ms.dmeta[d] = meta;
+                    mbar_arrive_cnt(&ms.dfull[d], 2);
+                }
+                break;
+            }
             if (C::fp4) {
                 // A scale factors of the stage: row r (keys 2r, 2r+1) holds four UE8M0 bytes (even
                 // key blocks 0/1, odd key blocks 0/1); lane l gathers rows l, l+32, l+64, l+96
@@ -418,8 +430,18 @@ __global__ void __launch_bounds__(kThreads) index_tc_kernel(const __grid_constan
                 fence_proxy_async();
             }
             __syncwarp();
+            // the accumulator buffer (with its record slot) is free once the epilogue has read it
+            if (u >= (uint32_t)C::nbuf) mbar_wait(&ms.dfree[d], ((u / C::nbuf) + 1) & 1, err);
+            if (!C::fp4) {
+                const float4* src = reinterpret_cast<const float4*>(sm + s * C::stage + C::off_scale);
+                float4* dst = reinterpret_cast<float4*>(sm + C::off_dscale + d * kPair * 4);
+                dst[lane] = src[lane];
+                dst[lane + 32] = src[lane + 32];
+            }
+            if (lane == 0) ms.dmeta[d] = meta;
+            __syncwarp();
             if (lane == 0) {
-                if (u >= (uint32_t)C::nbuf) mbar_wait(&ms.dfree[d], ((u / C::nbuf) + 1) & 1, err);
+                mbar_arrive(&ms.dfull[d]);            // the record (the MMA commit is the other arrival)
                 fence_after_sync();
                 const uint64_t ad0 = a_desc0 + ((s * C::stage) >> 4);
                 const uint64_t bd0 = b_desc0 + ((qs * C::q_slot) >> 4);
@@ -459,23 +481,18 @@ __global__ void __launch_bounds__(kThreads) index_tc_kernel(const __grid_constan
         const uint64_t pol_keep = l2_policy_evict_last();       // the top-k re-reads the scores
         const uint32_t lane_off = (uint32_t)(32 * warp) << 16;
         for (uint32_t u = 0;; ++u) {
-            const uint32_t s = u % C::NS;
-            mbar_wait(&ms.full[s], (u / C::NS) & 1, err);
-            const unsigned char* st = sm + s * C::stage;
-            const int4 meta = *reinterpret_cast<const int4*>(st + C::off_meta);
-            if (meta.w & kTerm) break;
-            const uint32_t d = u % C::nbuf, qs = (uint32_t)(meta.w >> 8) & 1u;
+            const uint32_t d = u % C::nbuf;
             mbar_wait(&ms.dfull[d], (u / C::nbuf) & 1, err);
             fence_after_sync();
+            const int4 meta = ms.dmeta[d];
+            if (meta.w & kTerm) break;
+            const uint32_t qs = (uint32_t)(meta.w >> 8) & 1u;
             float se = 1.0f, so = 1.0f;                      // e4m3: row scales of keys 2j (e), 2j+1 (o)
             if (!C::fp4) {
-                const float2 f2 = *reinterpret_cast<const float2*>(st + C::off_scale + 8 * tid);
+                const float2 f2 = reinterpret_cast<const float2*>(sm + C::off_dscale + d * kPair * 4)[tid];
                 se = f2.x;
                 so = f2.y;
             }
-            // the stage's record (and scales) are in registers: release it (with the MMA commit)
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&ms.empty[s]);
             const float4* wq4 = reinterpret_cast<const float4*>(sm + C::off_qslots + qs * C::q_slot + C::q_img);
             const uint32_t dbuf = tmem + d * C::d_cols + lane_off;
             // per key: pairs of heads (h, h+1) in f32x2 lanes, v = D_hi + D_lo (fp4: scaled by the

@@ -5,17 +5,21 @@
 // Exact radix select on the order-preserving 32-bit image of each score (12 + 12 + 8 bits):
 //   hist   : 4096-bin histogram of the top 12 bits per row -- fused into the indexer's
 //            tensor-core epilogue, or a separate pass over the scores;
-//   select : one launch, P CTAs per row.  Every CTA of a row finds the boundary bin b1 where the
-//            running count from the top reaches k; when the elements of bins >= b1 number at
-//            most kCap, each CTA appends those of its slice of the row, (key, index), to the
-//            row's candidate list.  The last CTA of the row to finish (an arrival counter; no
-//            CTA waits for another) resolves the remaining 20 bits on the candidates (or, when
-//            the boundary bin is too full, on the whole row), marks "above the threshold" and
-//            "equal to the threshold" entries in two bitmaps, then scans the bitmaps in index
-//            order: every "above" bit plus the lowest-index "equal" bits needed to reach k.
+//   select : one launch; a row is handled by a cluster of P CTAs, CTA p owning the p-th slice of
+//            the row's entries (whole 32-entry words).  Every CTA finds the boundary bin b1 where
+//            the running count from the top reaches k; when the elements of bins >= b1 number at
+//            most kCap, each CTA gathers those of its slice, (key, index), into shared memory
+//            (otherwise it re-reads its slice for every pass).  The next 12 and 8 bits are
+//            resolved with histograms of the CTAs' candidates summed over the cluster through
+//            distributed shared memory; each CTA then marks its "above the threshold" and "equal
+//            to the threshold" entries in two bitmaps of its slice, learns from the others' counts
+//            how many of the lowest-index "equal" entries are its to take and where its output
+//            starts, and writes its selected indices in ascending order.
 // Output: indices ascending, -1 padded.  Ties go to the lower index; the result is exact and
 // deterministic for any non-NaN scores (-0 == +0).
 #include "common.cuh"
+
+#include <cooperative_groups.h>
 
 namespace csahca {
 namespace {
@@ -100,13 +104,15 @@ __device__ __forceinline__ float bin_floor_value(int b) {
 }
 
 constexpr int kWarpSpan = 1024;    // scores per warp and step of the collect pass (32 per lane)
-constexpr int kSmemWords = 8192;   // bitmaps in shared memory for rows of up to 262144 entries
-constexpr size_t kSelSmem = (size_t)kCap * 8 + 2 * (size_t)kSmemWords * 4 + (size_t)kBins12 * 4;
+constexpr int kSmemWords = 8192;   // bitmap words of a slice kept in shared memory (262144 entries)
+constexpr int kMaxCluster = 8;
+// shared memory: candidates | histogram of this CTA | cluster sums | two bitmaps
+constexpr size_t kSelSmem = (size_t)kCap * 8 + 2 * (size_t)kBins12 * 4 + 2 * (size_t)kSmemWords * 4;
 
-// Appends the elements >= tv of the warp's span [w0, w0 + cnt_n) of `row` to the candidate list
-// (16-byte loads when aligned and full, one atomic per warp).
-__device__ __forceinline__ void collect_span(const float* __restrict__ row, int64_t w0, int cnt_n, float tv,
-                                             uint2* cand_row, int* cand_cnt, int lane) {
+// Appends the elements >= tv of the warp's span [w0, w0 + cnt_n) of `row` to the shared
+// candidate list (16-byte loads when aligned and full, one shared atomic per warp).
+__device__ __forceinline__ void collect_span(const float* __restrict__ row, int64_t w0, int cnt_n, float tv, uint2* cs,
+                                             int* sh_nc, int lane) {
     const float* src = row + w0;
     const bool vec = ((reinterpret_cast<uintptr_t>(src) & 15) == 0) && cnt_n == kWarpSpan;
     float v[32];
@@ -141,146 +147,176 @@ __device__ __forceinline__ void collect_span(const float* __restrict__ row, int6
     const int total = __shfl_sync(0xffffffffu, incl, 31);
     if (total == 0) return;
     int base = 0;
-    if (lane == 0) base = atomicAdd(cand_cnt, total);
+    if (lane == 0) base = atomicAdd(sh_nc, total);
     base = __shfl_sync(0xffffffffu, base, 0) + incl - mine;
 #pragma unroll
     for (int e = 0; e < 32; ++e) {
         if (bits & (1u << e)) {
             const int i = ((e >> 2) * 32 + lane) * 4 + (e & 3);
-            if (base < kCap) cand_row[base] = make_uint2(ordered_key(v[e]), (uint32_t)(w0 + i));
+            if (base < kCap) cs[base] = make_uint2(ordered_key(v[e]), (uint32_t)(w0 + i));
             ++base;
         }
     }
 }
 
-// Grid (P, rows).  Threshold, collect and (last CTA of each row) exact finish; see the file
-// comment.  Candidates and, for rows of up to kSmemWords * 32 entries, both bitmaps live in
-// shared memory.
+// Sums bins [0, nb) of `hist` over the CTAs of the cluster (distributed shared memory) into `out`.
+__device__ __forceinline__ void cluster_sum(cooperative_groups::cluster_group& cl, uint32_t* hist, uint32_t* out,
+                                            int nb) {
+    const int P = (int)cl.num_blocks();
+    for (int i = threadIdx.x; i < nb; i += blockDim.x) {
+        uint32_t s = 0;
+        for (int q = 0; q < P; ++q) s += cl.map_shared_rank(hist, q)[i];
+        out[i] = s;
+    }
+}
+
+// Grid (P, rows), clusters of (P, 1, 1): the CTAs of a cluster share one row.
 __global__ void __launch_bounds__(kSelThreads, 1) topk_select_kernel(
     const float* __restrict__ scores, int64_t stride, const int64_t* __restrict__ n_vis_arr,
     const int64_t* __restrict__ q_pos, int m, int64_t Ncap, int k, const uint32_t* __restrict__ hist1,
-    uint2* cand, int* cand_n, int* done, uint32_t* __restrict__ win, uint32_t* __restrict__ tie, int64_t words,
-    int32_t* __restrict__ idx_out) {
+    uint32_t* __restrict__ win, uint32_t* __restrict__ tie, int64_t words, int32_t* __restrict__ idx_out) {
     pdl_wait();
     pdl_trigger();
+    namespace cg = cooperative_groups;
+    cg::cluster_group cl = cg::this_cluster();
     extern __shared__ __align__(16) unsigned char fsm[];
     uint2* cs = reinterpret_cast<uint2*>(fsm);
-    uint32_t* swin = reinterpret_cast<uint32_t*>(fsm + (size_t)kCap * 8);
+    uint32_t* hmine = reinterpret_cast<uint32_t*>(fsm + (size_t)kCap * 8);
+    uint32_t* hsum = hmine + kBins12;
+    uint32_t* swin = hsum + kBins12;
     uint32_t* stie = swin + kSmemWords;
-    uint32_t* sh_hist = stie + kSmemWords;
     __shared__ int sh_scan[33];
     __shared__ int sh_res[2];
-    __shared__ int sh_last;
-    const int r = blockIdx.y, P = gridDim.x;
+    __shared__ int sh_nc;
+    __shared__ int sh_cnt[2];                          // this CTA's "above" and "equal" counts
+    const int r = blockIdx.y, P = (int)cl.num_blocks(), p = (int)cl.block_rank();
     const int tid = threadIdx.x, nthr = blockDim.x, lane = tid & 31, warp = tid >> 5, nw = nthr >> 5;
     const int64_t n = min(row_nvis(r, n_vis_arr, q_pos, m, Ncap), min(stride, words * 32));
-    const int64_t nwords = (n + 31) / 32;
     int32_t* out = idx_out + (int64_t)r * k;
     if (n <= k) {                                   // every visible entry is selected, in order
-        if (blockIdx.x == 0)
+        if (p == 0)
             for (int j = tid; j < k; j += nthr) out[j] = j < n ? j : -1;
-        return;
+        return;                                     // (the whole cluster takes this branch)
     }
     const float* row = scores + (int64_t)r * stride;
-    // ---- boundary bin of the top 12 bits (every CTA of the row, from the same histogram)
+    // this CTA's slice: bitmap words [w_lo, w_hi), entries [s_lo, s_hi)
+    const int64_t nwords = (n + 31) / 32;
+    const int64_t w_lo = nwords * p / P, w_hi = nwords * (p + 1) / P;
+    const int64_t s_lo = w_lo * 32, s_hi = min(n, w_hi * 32);
+    const int64_t sw = w_hi - w_lo;
+    const bool smem_bits = sw <= kSmemWords;
+    uint32_t* wr = smem_bits ? swin : win + (int64_t)r * words + w_lo;
+    uint32_t* tr = smem_bits ? stie : tie + (int64_t)r * words + w_lo;
+    // ---- boundary bin of the top 12 bits (every CTA, from the row's histogram)
     const uint32_t* h = hist1 + (int64_t)r * kBins12;
     int b1;
     uint32_t above1;
     find_bin(h, kBins12, (uint32_t)k, sh_scan, sh_res, &b1, &above1);
     const bool fast = above1 + h[b1] <= (uint32_t)kCap;
-    // ---- collect: this CTA's spans of the row (span g of the row goes to CTA g % P)
-    uint2* cand_row = cand + (int64_t)r * kCap;
+    if (tid == 0) sh_nc = 0;
+    for (int i = tid; i < kBins12; i += nthr) hmine[i] = 0;
+    __syncthreads();
+    // ---- candidates of the slice (spans of 1024 entries)
     if (fast) {
         const float tv = bin_floor_value(b1);
-        for (int64_t g = (int64_t)blockIdx.x + (int64_t)P * warp; g * kWarpSpan < n; g += (int64_t)P * nw) {
-            const int64_t w0 = g * kWarpSpan;
-            collect_span(row, w0, (int)min((int64_t)kWarpSpan, n - w0), tv, cand_row, &cand_n[r], lane);
-        }
-    }
-    // ---- the last CTA of the row to get here resolves it
-    __syncthreads();
-    if (tid == 0) {
-        __threadfence();
-        sh_last = atomicAdd(&done[r], 1) == P - 1;
+        for (int64_t w0 = s_lo + (int64_t)warp * kWarpSpan; w0 < s_hi; w0 += (int64_t)nw * kWarpSpan)
+            collect_span(row, w0, (int)min((int64_t)kWarpSpan, s_hi - w0), tv, cs, &sh_nc, lane);
     }
     __syncthreads();
-    if (!sh_last) return;
-    __threadfence();
-    const bool smem_bits = nwords <= kSmemWords;
-    uint32_t* wr = smem_bits ? swin : win + (int64_t)r * words;
-    uint32_t* tr = smem_bits ? stie : tie + (int64_t)r * words;
-    const int nc = fast ? min(__ldcg(&cand_n[r]), kCap) : 0;
-    for (int i = tid; i < nc; i += nthr) cs[i] = __ldcg(&cand_row[i]);
-    for (int64_t w = tid; w < nwords; w += nthr) {
-        wr[w] = 0u;
-        tr[w] = 0u;
-    }
-    for (int i = tid; i < kBins12; i += nthr) sh_hist[i] = 0;
-    __syncthreads();
-    // visits (key, index) of the source: the candidate list, or the whole row
+    const int nc = fast ? min(sh_nc, kCap) : 0;
+    // visits (key, index) of this CTA's part: its candidates, or its whole slice
     auto for_each = [&](auto&& f) {
         if (fast) {
             for (int i = tid; i < nc; i += nthr) f(cs[i].x, (int64_t)cs[i].y);
         } else {
-            for (int64_t s = tid; s < n; s += nthr) f(ordered_key(row[s]), s);
+            for (int64_t s = s_lo + tid; s < s_hi; s += nthr) f(ordered_key(row[s]), s);
         }
     };
-    // bits 19..8 inside the boundary bin
+    // ---- bits 19..8 inside the boundary bin, summed over the cluster
     for_each([&](uint32_t key, int64_t) {
-        if ((int)(key >> 20) == b1) atomicAdd(&sh_hist[(key >> 8) & 0xFFFu], 1u);
+        if ((int)(key >> 20) == b1) atomicAdd(&hmine[(key >> 8) & 0xFFFu], 1u);
     });
-    __syncthreads();
+    cl.sync();
+    cluster_sum(cl, hmine, hsum, kBins12);
+    cl.sync();                                      // every CTA has read the others' histograms
     int b2;
     uint32_t above2;
-    find_bin(sh_hist, kBins12, (uint32_t)k - above1, sh_scan, sh_res, &b2, &above2);
-    // bits 7..0 inside the 24-bit prefix
+    find_bin(hsum, kBins12, (uint32_t)k - above1, sh_scan, sh_res, &b2, &above2);
+    // ---- bits 7..0 inside the 24-bit prefix
     const uint32_t pre = ((uint32_t)b1 << 12) | (uint32_t)b2;
-    for (int i = tid; i < kBins12; i += nthr) sh_hist[i] = 0;
+    for (int i = tid; i < kBins12; i += nthr) hmine[i] = 0;
     __syncthreads();
     for_each([&](uint32_t key, int64_t) {
-        if ((key >> 8) == pre) atomicAdd(&sh_hist[key & 0xFFu], 1u);
+        if ((key >> 8) == pre) atomicAdd(&hmine[key & 0xFFu], 1u);
     });
+    cl.sync();
+    const int nb3 = kBins8 < nthr ? nthr : kBins8;
+    cluster_sum(cl, hmine, hsum, nb3);
     __syncthreads();
     int b3;
     uint32_t above3;
-    find_bin(sh_hist, kBins8 < nthr ? nthr : kBins8, (uint32_t)k - above1 - above2, sh_scan, sh_res, &b3, &above3);
+    find_bin(hsum, nb3, (uint32_t)k - above1 - above2, sh_scan, sh_res, &b3, &above3);
     const uint32_t thr = (pre << 8) | (uint32_t)b3;
     const int ties_needed = (int)((uint32_t)k - above1 - above2 - above3);
-    // bitmaps
+    // ---- bitmaps of the slice
+    for (int64_t w = tid; w < sw; w += nthr) {
+        wr[w] = 0u;
+        tr[w] = 0u;
+    }
+    __syncthreads();
     if (fast) {
         for (int i = tid; i < nc; i += nthr) {
             const uint2 e = cs[i];
-            if (e.x > thr) atomicOr(&wr[e.y >> 5], 1u << (e.y & 31));
-            else if (e.x == thr) atomicOr(&tr[e.y >> 5], 1u << (e.y & 31));
+            const uint32_t li = e.y - (uint32_t)s_lo;
+            if (e.x > thr) atomicOr(&wr[li >> 5], 1u << (li & 31));
+            else if (e.x == thr) atomicOr(&tr[li >> 5], 1u << (li & 31));
         }
     } else {
-        for (int64_t g = (int64_t)warp * 32; g < n; g += (int64_t)nw * 32) {
+        for (int64_t g = s_lo + (int64_t)warp * 32; g < s_hi; g += (int64_t)nw * 32) {
             const int64_t s = g + lane;
-            const uint32_t key = s < n ? ordered_key(row[s]) : 0u;
-            const uint32_t wb = __ballot_sync(0xffffffffu, s < n && key > thr);
-            const uint32_t tb = __ballot_sync(0xffffffffu, s < n && key == thr);
+            const uint32_t key = s < s_hi ? ordered_key(row[s]) : 0u;
+            const uint32_t wb = __ballot_sync(0xffffffffu, s < s_hi && key > thr);
+            const uint32_t tb = __ballot_sync(0xffffffffu, s < s_hi && key == thr);
             if (lane == 0) {
-                wr[g / 32] = wb;
-                tr[g / 32] = tb;
+                wr[(g - s_lo) / 32] = wb;
+                tr[(g - s_lo) / 32] = tb;
             }
         }
     }
     __threadfence_block();
     __syncthreads();
-    // ascending compaction: all "above" bits, then the lowest-index "equal" bits
-    const int64_t per = (nwords + nthr - 1) / nthr;
-    const int64_t w0 = min(nwords, (int64_t)tid * per), w1 = min(nwords, w0 + per);
+    // ---- per-thread word ranges; this CTA's counts, shared with the cluster
+    const int64_t per = (sw + nthr - 1) / nthr;
+    const int64_t v0 = min(sw, (int64_t)tid * per), v1 = min(sw, v0 + per);
     int nwin = 0, ntie = 0;
-    for (int64_t w = w0; w < w1; ++w) {
+    for (int64_t w = v0; w < v1; ++w) {
         nwin += __popc(wr[w]);
         ntie += __popc(tr[w]);
     }
+    int tot_win, tot_tie;
+    const int tie_before_local = block_exclusive_scan(ntie, sh_scan, &tot_tie);
+    (void)block_exclusive_scan(nwin, sh_scan, &tot_win);
+    if (tid == 0) {
+        sh_cnt[0] = tot_win;
+        sh_cnt[1] = tot_tie;
+    }
+    cl.sync();
+    // ties go to the lowest indices: the CTAs before this one take theirs first
+    int ties_before = 0, out_off = 0;
+    for (int q = 0; q < p; ++q) {
+        const int* c = cl.map_shared_rank(sh_cnt, q);
+        const int aq = c[0], tq = c[1];
+        const int take_q = max(0, min(ties_needed - ties_before, tq));
+        out_off += aq + take_q;
+        ties_before += tq;
+    }
+    cl.sync();                                      // the last reads of another CTA's shared memory
+    const int my_ties = max(0, min(ties_needed - ties_before, tot_tie));
+    const int take = max(0, min(my_ties - tie_before_local, ntie));
     int tot;
-    const int tie_before = block_exclusive_scan(ntie, sh_scan, &tot);
-    const int take = max(0, min(ties_needed - tie_before, ntie));
     const int pos0 = block_exclusive_scan(nwin + take, sh_scan, &tot);
-    int pos = pos0, rem = take;
-    for (int64_t w = w0; w < w1; ++w) {
+    int pos = out_off + pos0, rem = take;
+    for (int64_t w = v0; w < v1; ++w) {
         uint32_t t = tr[w];
         uint32_t tsel = 0;
         while (t && rem > 0) {
@@ -292,7 +328,7 @@ __global__ void __launch_bounds__(kSelThreads, 1) topk_select_kernel(
         uint32_t bits = wr[w] | tsel;
         while (bits) {
             const int b = __ffs(bits) - 1;
-            if (pos < k) out[pos] = (int32_t)(w * 32 + b);
+            if (pos < k) out[pos] = (int32_t)(s_lo + (w * 32 + b));
             ++pos;
             bits &= bits - 1;
         }
@@ -303,8 +339,7 @@ __global__ void __launch_bounds__(kSelThreads, 1) topk_select_kernel(
 
 size_t topk_workspace_bytes(int64_t R, int64_t stride) {
     const int64_t words = (stride + 31) / 32;
-    return align256((size_t)R * kBins12 * 4) + align256((size_t)R * 8) + align256((size_t)R * kCap * 8) +
-           align256((size_t)R * words * 4) * 2;
+    return align256((size_t)R * kBins12 * 4) + align256((size_t)R * words * 4) * 2;
 }
 
 TopkWorkspace topk_carve(void* ws, int64_t R, int64_t stride) {
@@ -312,15 +347,12 @@ TopkWorkspace topk_carve(void* ws, int64_t R, int64_t stride) {
     t.words = (stride + 31) / 32;
     char* p = static_cast<char*>(ws);
     t.hist1 = reinterpret_cast<uint32_t*>(p); p += align256((size_t)R * kBins12 * 4);
-    t.cand_n = reinterpret_cast<int*>(p);
-    t.done = t.cand_n + R;                      p += align256((size_t)R * 8);
-    t.cand = reinterpret_cast<uint2*>(p); p += align256((size_t)R * kCap * 8);
     t.win = reinterpret_cast<uint32_t*>(p); p += align256((size_t)R * t.words * 4);
     t.tie = reinterpret_cast<uint32_t*>(p);
     return t;
 }
 
-size_t topk_zero_bytes(int64_t R) { return align256((size_t)R * kBins12 * 4) + align256((size_t)R * 8); }
+size_t topk_zero_bytes(int64_t R) { return align256((size_t)R * kBins12 * 4); }
 
 csahca_status topk_launch(const float* scores, int64_t stride, int R, const int64_t* n_vis_arr,
                           const int64_t* q_pos, int m, int64_t Ncap, int k, int32_t* idx_out,
@@ -338,17 +370,31 @@ csahca_status topk_launch(const float* scores, int64_t stride, int R, const int6
     cudaGetDevice(&dev);
     if (dev >= 0 && dev < 64 && !attr_set[dev]) {
         if (cudaFuncSetAttribute(topk_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSelSmem) !=
-            cudaSuccess)
+                cudaSuccess ||
+            cudaFuncSetAttribute(topk_select_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 0) != cudaSuccess)
             return CSAHCA_ERR_CUDA;
         attr_set[dev] = true;
     }
-    // CTAs per row: one wave over the SMs for few rows (each row is collected by P CTAs and
-    // finished by the last of them), one per row otherwise
+    // CTAs per row (one cluster per row): spread few rows over the SMs, one CTA per row otherwise
     const int64_t spans = std::max<int64_t>(1, cdiv(stride, (int64_t)kWarpSpan * (kSelThreads / 32)));
-    const int P = (int)std::max<int64_t>(1, std::min<int64_t>(std::min<int64_t>(num_sms() / R, 8), spans));
-    (void)launch_pdl(topk_select_kernel, dim3((unsigned)P, (unsigned)R), dim3(kSelThreads), kSelSmem, stream, scores,
-                     stride, n_vis_arr, q_pos, m, Ncap, k, tw.hist1, tw.cand, tw.cand_n, tw.done, tw.win, tw.tie,
-                     tw.words, idx_out);
+    int P = (int)std::max<int64_t>(1, std::min<int64_t>(std::min<int64_t>(num_sms() / R, kMaxCluster), spans));
+    while (P & (P - 1)) --P;                         // a power of two
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)P, (unsigned)R);
+    cfg.blockDim = dim3(kSelThreads);
+    cfg.dynamicSmemBytes = kSelSmem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = (unsigned)P;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    (void)cudaLaunchKernelEx(&cfg, topk_select_kernel, scores, stride, n_vis_arr, q_pos, m, Ncap, k,
+                             (const uint32_t*)tw.hist1, tw.win, tw.tie, tw.words, idx_out);
     count_launch();
     CSAHCA_CHECK_LAUNCH();
     return CSAHCA_OK;

@@ -67,8 +67,8 @@ def test_workspace_sizes_are_host_only(lib):
     lib.csa_index_topk_workspace.restype = ctypes.c_size_t
     lib.csa_index_topk_workspace.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int64, ctypes.c_int]
     n = lib.csa_index_topk_workspace(32, 1, 262144, 1024)
-    # scores (32 x 262144 fp32) + 3 histograms + 2 bitmaps + tie counts
-    assert n >= 32 * 262144 * 4 + 32 * (4096 * 2 + 256) * 4 + 2 * 32 * 8192 * 4
+    # scores (32 x 262144 fp32) + the 12-bit histograms + 2 bitmaps per row
+    assert n >= 32 * 262144 * 4 + 32 * 4096 * 4 + 2 * 32 * 8192 * 4
     lib.hca_attend_workspace.restype = ctypes.c_size_t
     lib.hca_attend_workspace.argtypes = [ctypes.c_int] * 4 + [ctypes.c_int64, ctypes.c_int, ctypes.c_int]
     assert lib.hca_attend_workspace(4, 1, 64, 128, 8192, 128, 8) == 4 * 8 * 64 * 128 * 4 + 4 * 8 * 64 * 4
