@@ -181,6 +181,10 @@ cudaError_t index_tc_launch(const void* q_idx, const float* w, const void* k_cod
                             int B, int T, int H_I, const int64_t* q_pos, int64_t Ncap, int m, float* S,
                             uint32_t* hist1, unsigned* err, cudaStream_t st);
 
+// Tensor-core indexer with FP4 queries (E2M1 codes + UE8M0 per 32, the keys' form) and e2m1 keys.
+cudaError_t index_tc_q4_launch(const void* q_codes, const void* q_scale, const float* w, const void* k_codes,
+                               const void* k_scale, int B, int T, int H_I, const int64_t* q_pos, int64_t Ncap, int m,
+                               float* S, uint32_t* hist1, unsigned* err, cudaStream_t st);
 // Tensor-core indexer scores for chunked prefill (bf16 keys and queries, d_I = 64, T a multiple of
 // 128 / H_I); hist1 as above.
 bool index_prefill_supported(int q_dtype, int key_fmt, int H_I, int d_I, int64_t Ncap, const void* q_idx,

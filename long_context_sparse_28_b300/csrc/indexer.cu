@@ -213,4 +213,33 @@ csahca_status csa_index_topk(const void* q_idx, csahca_dtype q_dtype, const floa
     return topk_launch(S, Ncap, R, nullptr, q_pos, m, Ncap, k, idx_out, tw, hist_done, st);
 }
 
+csahca_status csa_index_topk_fp4(const void* q_codes, const void* q_scale, const float* w, const void* k_codes,
+                                 const void* k_scale, int B, int T, int H_I, int d_I, const int64_t* q_pos,
+                                 int64_t Ncap, int m, int k, int32_t* idx_out, float* scores_out, void* workspace,
+                                 size_t ws_bytes, csahca_stream_t stream) {
+    CSAHCA_REQUIRE(q_codes && q_scale && w && k_codes && k_scale && q_pos && idx_out);
+    CSAHCA_REQUIRE(B >= 1 && T >= 1 && (int64_t)B * T <= 65535 && m >= 1 && Ncap >= 1 && k >= 1 && k <= 65536);
+    CSAHCA_REQUIRE(H_I >= 1 && d_I >= 32 && d_I % 32 == 0);
+    const int R = B * T;
+    if (!(d_I == 64 && (H_I == 16 || H_I == 32 || H_I == 64)) ||
+        !index_tc_supported(CSAHCA_BF16, CSAHCA_E2M1_UE8M0, H_I, d_I, Ncap, k_codes, k_scale, B, R) ||
+        !aligned(q_codes, 16) || !aligned(q_scale, 2))
+        return CSAHCA_ERR_UNSUPPORTED;
+    if (!workspace || !aligned(workspace, 256) || ws_bytes < csa_index_topk_workspace(B, T, Ncap, k))
+        return CSAHCA_ERR_WORKSPACE;
+    char* ws = static_cast<char*>(workspace);
+    float* S = scores_out ? scores_out : reinterpret_cast<float*>(ws);
+    TopkWorkspace tw = topk_carve(ws + align256((size_t)R * Ncap * 4), R, Ncap);
+    cudaStream_t st = (cudaStream_t)stream;
+    unsigned* err = err_word();
+    if (!err) return CSAHCA_ERR_CUDA;
+    if (zero_words(tw.hist1, topk_zero_bytes(R) / 4, st) != cudaSuccess) return CSAHCA_ERR_CUDA;
+    const cudaError_t e = index_tc_q4_launch(q_codes, q_scale, w, k_codes, k_scale, B, T, H_I, q_pos, Ncap, m, S,
+                                             tw.hist1, err, st);
+    count_launch();
+    if (e == cudaErrorNotSupported) return CSAHCA_ERR_UNSUPPORTED;
+    if (e != cudaSuccess) return CSAHCA_ERR_CUDA;
+    return topk_launch(S, Ncap, R, nullptr, q_pos, m, Ncap, k, idx_out, tw, true, st);
+}
+
 }  // extern "C"

@@ -82,9 +82,10 @@ struct alignas(16) IdxMisc {
 };
 static_assert(offsetof(IdxMisc, hist) % 16 == 0 && offsetof(IdxMisc, full) % 8 == 0, "IdxMisc alignment");
 
-template <int FMT, int HI>
+template <int FMT, int HI, bool Q4 = false>
 struct Cfg {
     static constexpr bool fp4 = FMT == CSAHCA_E2M1_UE8M0;            // block scales applied by the MMA
+    static constexpr int NQ = Q4 ? HI : 2 * HI;                      // B rows: FP4 queries, or hi + lo rows
     static constexpr uint32_t code_tx = fp4 ? kPair * 32 : kPair * 64;  // global code bytes per stage
     static constexpr int scale_bytes = fp4 ? 2 : 4;                  // per key
     // stage: codes (128 rows x 128 B, swizzled) | scales (fp4: 512 B, then the 512-byte factor
@@ -95,7 +96,7 @@ struct Cfg {
     static constexpr uint32_t stage = (off_meta + 16 + 1023) / 1024 * 1024;
     // query slot (one per work item, two in flight): q image (2 HI rows x 128 B: hi rows, then
     // lo rows, codes in the first 64 bytes) | head weights | (fp4) the B scale-factor image
-    static constexpr uint32_t q_img = 2 * HI * 128;
+    static constexpr uint32_t q_img = NQ * 128;
     static constexpr uint32_t off_sfb = (q_img + HI * 4 + 15) / 16 * 16;
     static constexpr uint32_t q_slot = ((fp4 ? off_sfb + 512 : q_img + HI * 4) + 1023) / 1024 * 1024;
     // as many stages as leave room for two CTAs per SM (228 KB, 1 KB reserved per CTA, 1 KB
@@ -107,7 +108,7 @@ struct Cfg {
     // e4m3: the row scales of the stage in each accumulator buffer (copied by the MMA warp)
     static constexpr uint32_t off_dscale = off_qslots + 2 * q_slot;
     static constexpr uint32_t smem = off_dscale + (fp4 ? 0 : kMaxBuf * kPair * 4);
-    static constexpr uint32_t acc_cols = 2 * HI;                     // one accumulator: hi | lo columns
+    static constexpr uint32_t acc_cols = NQ;                         // one accumulator: hi | lo columns (or FP4 q)
     static constexpr uint32_t d_cols = 2 * acc_cols;                 // even + odd keys
     // fp4: scale factors of A (4 columns per stage slot) and B (4 per query slot)
     static constexpr uint32_t sf_cols = fp4 ? 4 * kMaxNS + 8 : 0;
@@ -124,6 +125,7 @@ struct Cfg {
     static_assert(used_cols <= 512, "TMEM columns");
     static_assert(HI % 16 == 0 && HI <= 64, "heads");
     static_assert(!fp4 || off_sfa + 512 <= off_meta, "fp4 stage layout");
+    static_assert(!Q4 || fp4, "FP4 queries go with FP4 keys");
     // the next item's query row is loaded one item ahead when its share fits in a few registers
     static constexpr bool prefetch_q = HI <= 16;
 };
@@ -194,15 +196,16 @@ __device__ __forceinline__ void load_q_raw(const __nv_bfloat16* __restrict__ q_r
     }
 }
 
-template <int FMT, int HI>
+template <int FMT, int HI, bool Q4>
 __global__ void __launch_bounds__(kThreads) index_tc_kernel(const __grid_constant__ CUtensorMap kmap,
                                                             const __nv_bfloat16* __restrict__ q_idx,
+                                                            const uint8_t* __restrict__ q_scale,
                                                             const float* __restrict__ w,
                                                             const uint8_t* __restrict__ k_scale, int T,
                                                             const int64_t* __restrict__ q_pos, int64_t Ncap, int m,
                                                             int R, float* __restrict__ S,
                                                             uint32_t* __restrict__ hist1, unsigned* err) {
-    using C = Cfg<FMT, HI>;
+    using C = Cfg<FMT, HI, Q4>;
     constexpr int kUnits = 2 * HI / 32;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -326,7 +329,7 @@ __global__ void __launch_bounds__(kThreads) index_tc_kernel(const __grid_constan
                     break;
                 }
             }
-            if (c_ok && C::prefetch_q) load_q_raw<HI>(q_idx + (int64_t)c_r * HI * kDI, lane, c_raw);
+            if (c_ok && C::prefetch_q && !Q4) load_q_raw<HI>(q_idx + (int64_t)c_r * HI * kDI, lane, c_raw);
         };
         fetch_next();
         uint32_t u = 0;                       // stages issued
@@ -345,12 +348,31 @@ __global__ void __launch_bounds__(kThreads) index_tc_kernel(const __grid_constan
             // query slot of this piece: free once the MMAs and epilogue of piece it-2 are done
             const uint32_t qs = it & 1;
             if (it >= 2) mbar_wait(&ms.qfree[qs], ((it >> 1) + 1) & 1, err);
+            unsigned char* qsl = sm + C::off_qslots + qs * C::q_slot;
+            if constexpr (Q4) {
+                // FP4 queries (E2M1 codes, two per byte, and a UE8M0 byte per 32): unit (head h, half
+                // hf) = lane + 32 j holds 32 codes = two groups of 16, each stored as the MMA reads a
+                // 4-bit operand (the 8 packed bytes, then 8 bytes of padding); the B scale factors are
+                // the query's own scale bytes (byte k of column h: block k)
+                const uint8_t* qc = reinterpret_cast<const uint8_t*>(q_idx) + (int64_t)r * HI * (kDI / 2);
+#pragma unroll
+                for (int j = 0; j < kUnits; ++j) {
+                    const int unit = lane + 32 * j, h = unit >> 1, hf = unit & 1;
+                    const uint4 pk = __ldg(reinterpret_cast<const uint4*>(qc + h * (kDI / 2) + hf * 16));
+                    *reinterpret_cast<uint4*>(qsl + sw128(h, 2 * hf)) = make_uint4(pk.x, pk.y, 0u, 0u);
+                    *reinterpret_cast<uint4*>(qsl + sw128(h, 2 * hf + 1)) = make_uint4(pk.z, pk.w, 0u, 0u);
+                    if (hf == 0) {
+                        reinterpret_cast<float*>(qsl + C::q_img)[h] = w[(int64_t)r * HI + h];
+                        const uint32_t sc = __ldg(reinterpret_cast<const uint16_t*>(q_scale) + (int64_t)r * HI + h);
+                        reinterpret_cast<uint32_t*>(qsl + C::off_sfb)[(h & 31) * 4 + (h >> 5)] = sc | (sc << 16);
+                    }
+                }
+            } else {
             if (!C::prefetch_q) load_q_raw<HI>(q_idx + (int64_t)r * HI * kDI, lane, raw);
             uint4 img[kUnits][4];
             float wq[kUnits];
             int exq[kUnits];
             make_q_image<HI, !C::fp4>(raw, w + (int64_t)r * HI, lane, img, wq, exq);
-            unsigned char* qsl = sm + C::off_qslots + qs * C::q_slot;
 #pragma unroll
             for (int j = 0; j < kUnits; ++j) {
                 const int unit = lane + 32 * j, h = unit >> 1, hf = unit & 1;
@@ -368,6 +390,7 @@ __global__ void __launch_bounds__(kThreads) index_tc_kernel(const __grid_constan
                         sfb[(nl & 31) * 4 + (nl >> 5)] = (uint32_t)(122 - exq[j]) * 0x01010101u;
                     }
                 }
+            }
             }
             fence_proxy_async();
             __syncwarp();
@@ -458,7 +481,8 @@ __global__ void __launch_bounds__(kThreads) index_tc_kernel(const __grid_constan
                         for (int blk = 0; blk < 2; ++blk)    // 32-code blocks (one MMA K step each)
                             mma_mxf8f6f4_bs(dbuf + e * C::acc_cols, ad0 + (uint64_t)(e * 4 + blk * 2),
                                             bd0 + (uint64_t)(blk * 2),
-                                            idesc_mxf8f6f4_bs(128, 2 * HI, af, kE4M3, 2 * e + blk, blk), sfa, sfb,
+                                            idesc_mxf8f6f4_bs(128, C::NQ, af, Q4 ? kE2M1 : kE4M3, 2 * e + blk, blk),
+                                            sfa, sfb,
                                             (uint32_t)(blk > 0));
                 } else {
                     const uint32_t id = idesc_f8f6f4(128, 2 * HI, af, kE4M3);
@@ -504,8 +528,11 @@ __global__ void __launch_bounds__(kThreads) index_tc_kernel(const __grid_constan
 #pragma unroll
                 for (int k = 0; k < 16; k += 2) {
                     const uint64_t hp = f2_pack(__uint_as_float(hv[k]), __uint_as_float(hv[k + 1]));
-                    const uint64_t lp = f2_pack(__uint_as_float(lv[k]), __uint_as_float(lv[k + 1]));
-                    const uint64_t v = C::fp4 ? f2_add(hp, lp) : f2_fma(Ll, lp, hp);
+                    uint64_t v = hp;                                     // FP4 queries: one part
+                    if constexpr (!Q4) {
+                        const uint64_t lp = f2_pack(__uint_as_float(lv[k]), __uint_as_float(lv[k + 1]));
+                        v = C::fp4 ? f2_add(hp, lp) : f2_fma(Ll, lp, hp);
+                    }
                     float a0, a1;
                     f2_unpack(v, a0, a1);
                     acc = f2_fma(wv[k / 2], f2_pack(fmaxf(a0, 0.0f), fmaxf(a1, 0.0f)), acc);
@@ -540,7 +567,7 @@ __global__ void __launch_bounds__(kThreads) index_tc_kernel(const __grid_constan
                         uint64_t wv[8];
                         weights16(c0, wv);
                         const int h = key * (int)C::acc_cols + c0;
-                        head_pairs(acc2[key], dv + h, dv + h + HI, wv);
+                        head_pairs(acc2[key], dv + h, dv + h + (Q4 ? 0 : HI), wv);
                     }
             } else {
 #pragma unroll
@@ -552,7 +579,7 @@ __global__ void __launch_bounds__(kThreads) index_tc_kernel(const __grid_constan
                         weights16(c0, wv);
                         uint32_t h0[16], l0[16];
                         tmem_ld16(abase + c0, h0);
-                        tmem_ld16(abase + HI + c0, l0);
+                        if (!Q4) tmem_ld16(abase + HI + c0, l0);
                         tmem_wait_ld();
                         head_pairs(acc2[key], h0, l0, wv);
                     }
@@ -613,11 +640,11 @@ __global__ void __launch_bounds__(kThreads) index_tc_kernel(const __grid_constan
     if (warp == 0) tmem_dealloc(tmem, C::tmem_cols);
 }
 
-template <int FMT, int HI>
-cudaError_t launch_index_tc(const void* q_idx, const float* w, const void* k_codes, const void* k_scale, int B,
-                            int T, const int64_t* q_pos, int64_t Ncap, int m, float* S, uint32_t* hist1, unsigned* err,
-                            cudaStream_t st) {
-    using C = Cfg<FMT, HI>;
+template <int FMT, int HI, bool Q4 = false>
+cudaError_t launch_index_tc(const void* q_idx, const void* q_scale, const float* w, const void* k_codes,
+                            const void* k_scale, int B, int T, const int64_t* q_pos, int64_t Ncap, int m, float* S,
+                            uint32_t* hist1, unsigned* err, cudaStream_t st) {
+    using C = Cfg<FMT, HI, Q4>;
     CUtensorMap kmap;
     std::memset(&kmap, 0, sizeof kmap);
     const uint64_t rows = (uint64_t)B * (uint64_t)Ncap / 2;          // two keys per row of 128 codes
@@ -629,13 +656,14 @@ cudaError_t launch_index_tc(const void* q_idx, const float* w, const void* k_cod
     // CTAs per SM: shared memory (228 KB per SM, 1 KB reserved per CTA) and TMEM (512 columns)
     const size_t per_cta = smem + sizeof(IdxMisc) + 1024;
     const int occ = std::max(1, std::min((int)((size_t)(228 * 1024) / per_cta), (int)(512 / C::tmem_cols)));
-    auto kern = index_tc_kernel<FMT, HI>;
+    auto kern = index_tc_kernel<FMT, HI, Q4>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const int R = B * T;
     const int64_t items = (int64_t)R * cdiv(Ncap, (int64_t)kChunkStages * kPair);
     const int grid = (int)std::min<int64_t>(items, (int64_t)num_sms() * occ);
-    (void)launch_pdl(kern, dim3(grid), dim3(kThreads), smem, st, kmap, static_cast<const __nv_bfloat16*>(q_idx), w,
+    (void)launch_pdl(kern, dim3(grid), dim3(kThreads), smem, st, kmap, static_cast<const __nv_bfloat16*>(q_idx),
+                     static_cast<const uint8_t*>(q_scale), w,
                                        static_cast<const uint8_t*>(k_scale), T, q_pos, Ncap, m, R, S, hist1, err);
     return cudaGetLastError();
 }
@@ -655,7 +683,7 @@ cudaError_t index_tc_launch(const void* q_idx, const float* w, const void* k_cod
                             uint32_t* hist1, unsigned* err, cudaStream_t st) {
 #define CSAHCA_IDX_CASE(F, HH)                                                                                  \
     if (key_fmt == F && H_I == HH)                                                                              \
-        return launch_index_tc<F, HH>(q_idx, w, k_codes, k_scale, B, T, q_pos, Ncap, m, S, hist1, err, st);
+        return launch_index_tc<F, HH>(q_idx, nullptr, w, k_codes, k_scale, B, T, q_pos, Ncap, m, S, hist1, err, st);
     CSAHCA_IDX_CASE(CSAHCA_E2M1_UE8M0, 16)
     CSAHCA_IDX_CASE(CSAHCA_E2M1_UE8M0, 32)
     CSAHCA_IDX_CASE(CSAHCA_E2M1_UE8M0, 64)
@@ -664,6 +692,17 @@ cudaError_t index_tc_launch(const void* q_idx, const float* w, const void* k_cod
     CSAHCA_IDX_CASE(CSAHCA_E4M3_ROWSCALE, 64)
 #undef CSAHCA_IDX_CASE
     return cudaErrorNotSupported;
+}
+
+cudaError_t index_tc_q4_launch(const void* q_codes, const void* q_scale, const float* w, const void* k_codes,
+                               const void* k_scale, int B, int T, int H_I, const int64_t* q_pos, int64_t Ncap, int m,
+                               float* S, uint32_t* hist1, unsigned* err, cudaStream_t st) {
+    switch (H_I) {
+        case 16: return launch_index_tc<CSAHCA_E2M1_UE8M0, 16, true>(q_codes, q_scale, w, k_codes, k_scale, B, T, q_pos, Ncap, m, S, hist1, err, st);
+        case 32: return launch_index_tc<CSAHCA_E2M1_UE8M0, 32, true>(q_codes, q_scale, w, k_codes, k_scale, B, T, q_pos, Ncap, m, S, hist1, err, st);
+        case 64: return launch_index_tc<CSAHCA_E2M1_UE8M0, 64, true>(q_codes, q_scale, w, k_codes, k_scale, B, T, q_pos, Ncap, m, S, hist1, err, st);
+        default: return cudaErrorNotSupported;
+    }
 }
 
 }  // namespace csahca

@@ -201,6 +201,43 @@ def test_index_scores_and_topk_parity(fmt, q_dt, Ncap, H_I):
             check_index_set(npy(idx[b, t]), ref[t], S[t], int(nv[t]), k, f"b{b}t{t}")
 
 
+@pytest.mark.parametrize("H_I", [16, 32, 64])
+def test_index_fp4_queries_parity(H_I):
+    # both indexer operands in FP4: the queries quantised to MX E2M1 (bit-exact with the oracle's
+    # rule), then scores against the oracle's scores of the dequantised queries, and the top-k
+    B, T, Ncap, d_I, m, k = 3, 2, 5000, 64, 4, 300
+    kin = rnd((B, Ncap, d_I), torch.bfloat16, 51)
+    kin[1, 7] *= 4
+    codes, scales = L.key_storage(B, Ncap, d_I, L.E2M1_UE8M0)
+    L.csa_index_key_quantize(kin, L.E2M1_UE8M0, codes, scales)
+    q = rnd((B, T, H_I, d_I), torch.bfloat16, 52, 0.125)
+    q[0, 1, 3] *= 64                                    # a head with a much larger scale
+    q[2, 0, 5, :32] = 0                                 # an all-zero run of 32
+    qc = torch.empty(B, T, H_I, d_I // 2, dtype=torch.uint8, device="cuda")
+    qs = torch.empty(B, T, H_I, d_I // 32, dtype=torch.uint8, device="cuda")
+    L.csa_index_key_quantize(q, L.E2M1_UE8M0, qc, qs)
+    w = torch.rand(B, T, H_I, generator=torch.Generator().manual_seed(53)).cuda()
+    pos = dev_i64([[4 * Ncap - 1, 3000], [40, 4 * Ncap + 9], [9999, 17]])
+    idx = torch.empty(B, T, k, dtype=torch.int32, device="cuda")
+    sc = torch.full((B, T, Ncap), float("nan"), device="cuda")
+    L.csa_index_topk_fp4(qc, qs, w, codes, scales, pos.reshape(-1), m, k, idx, scores_out=sc)
+    torch.cuda.synchronize()
+    assert L.device_status() == 0
+    for b in range(B):
+        oc, os_ = oracle.quantize_keys(npy(q[b]).reshape(T * H_I, d_I), oracle.KEY_E2M1)
+        np.testing.assert_array_equal(npy(qc[b]).reshape(T * H_I, -1), oc)
+        np.testing.assert_array_equal(npy(qs[b]).reshape(T * H_I, -1), os_)
+        kc, ks = oracle.quantize_keys(npy(kin[b]), oracle.KEY_E2M1)
+        khat = oracle.dequant_keys(oracle.KEY_E2M1, kc, ks, d_I)
+        nv = np.minimum(Ncap, (npy(pos[b]) + 1) // m)
+        S = oracle.index_scores(oracle.fp4_query(npy(q[b])), npy(w[b]), khat, nv)
+        ref = oracle.topk(S, nv, k)
+        for t in range(T):
+            got = npy(sc[b, t])[: nv[t]].astype(np.float64)
+            assert np.abs(got - S[t, : nv[t]]).max() <= 1e-5 * np.abs(S[t, : nv[t]]).max() + 1e-6
+            check_index_set(npy(idx[b, t]), ref[t], S[t], int(nv[t]), k, f"b{b}t{t}")
+
+
 @pytest.mark.parametrize("H_I,T", [(16, 24), (32, 12), (64, 6)])
 def test_prefill_indexer_tensor_core_parity(H_I, T):
     # bf16 keys and queries with T a multiple of 128 / H_I: the tensor-core prefill kernel (query
