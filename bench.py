@@ -264,7 +264,7 @@ class DecodeBench:
         self.lens = w.lengths()
         B = w.B
         grow = total_steps + 8
-        self.Ncap_c = ((max(self.lens) + grow) // w.m_csa + 1 + 7) // 8 * 8
+        self.Ncap_c = ((max(self.lens) + grow) // w.m_csa + 1 + 255) // 256 * 256
         self.Ncap_h = (max(self.lens) + grow) // w.m_hca + 1
         fmt = L.KEY_FMT[w.key_fmt]
         self.active = {"both": [0, 1, 2, 3, 4], "csa": [0, 1, 2], "hca": [3, 4], "index": [1]}[layers]
@@ -301,6 +301,9 @@ class DecodeBench:
         self.lse_h = torch.empty(B, 1, w.H, dtype=torch.float32, device=device)
         self.ws_topk = torch.empty(L.csa_index_topk_workspace(B, 1, self.Ncap_c, w.k), dtype=torch.uint8,
                                    device=device)
+        if w.index_q == "e2m1":          # FP4 indexer queries: quantised every step
+            self.q4c = torch.empty(B, 1, w.H_I, w.d_I // 2, dtype=torch.uint8, device=device)
+            self.q4s = torch.empty(B, 1, w.H_I, w.d_I // 32, dtype=torch.uint8, device=device)
         self.ws_ca = torch.empty(max(256, L.csa_attend_workspace(B, 1, w.H, w.d, w.k, w.W)), dtype=torch.uint8,
                                  device=device)
         self.ws_ha = torch.empty(max(256, L.hca_attend_workspace(B, 1, w.H, w.d, self.Ncap_h, w.W, 0)),
@@ -312,6 +315,10 @@ class DecodeBench:
         if i == 0:
             L.csa_cache_append(t["c_k"], t["c_v"], t["c_g"], t["c_kidx"], t["pos"], self.cb, c.m, c.ring_k,
                                c.ring_v, c.ring_gate, c.ck, c.cv, c.k_codes, c.k_scale, c.key_fmt)
+        elif i == 1 and w.index_q == "e2m1":
+            L.csa_index_key_quantize(t["c_qi"], L.E2M1_UE8M0, self.q4c, self.q4s)
+            L.csa_index_topk_fp4(self.q4c, self.q4s, t["c_w"], c.k_codes, c.k_scale, t["pos"], c.m, w.k, self.idx,
+                                 workspace=self.ws_topk)
         elif i == 1:
             L.csa_index_topk(t["c_qi"], t["c_w"], c.k_codes, c.k_scale, c.key_fmt, t["pos"], c.m, w.k, self.idx,
                              workspace=self.ws_topk)
@@ -424,7 +431,8 @@ def cpu_baseline_decode(w, seqs: int, device, layers="both"):
     t0 = time.perf_counter()
     for (Lb, K, V, ck, cv, codes, sc, HK, HV, hck, hcv, q, qh, qi, ww) in ctx:
         if layers in ("both", "csa"):
-            oracle.csa_queries(q, qi, ww, [Lb - 1], ck, cv, codes, sc, fmt, K, V, 0, w.m_csa, w.k, w.W, w.scale)
+            oracle.csa_queries(q, qi, ww, [Lb - 1], ck, cv, codes, sc, fmt, K, V, 0, w.m_csa, w.k, w.W, w.scale,
+                               q_fp4=w.index_q == "e2m1")
         if layers in ("both", "hca"):
             oracle.hca_queries(qh, [Lb - 1], hck, hcv, HK, HV, 0, w.m_hca, w.W, w.scale)
     dt = time.perf_counter() - t0
@@ -557,7 +565,8 @@ def run_ours(args, dist):
            "L": f"U[{w.L_range[0]},{w.L_range[1]}] seeded" if w.L_range else w.L[0] if len(set(w.L)) == 1 else list(w.L),
            "H": w.H, "d": w.d, "layers": layers}
     if layers in ("both", "csa", "index"):
-        cfg["csa"] = {"m": w.m_csa, "k": w.k, "W": w.W, "H_I": w.H_I, "d_I": w.d_I, "index_keys": key_desc}
+        cfg["csa"] = {"m": w.m_csa, "k": w.k, "W": w.W, "H_I": w.H_I, "d_I": w.d_I, "index_keys": key_desc,
+                      "index_queries": "e2m1+ue8m0/32" if w.index_q == "e2m1" else "bf16"}
     if layers in ("both", "hca"):
         cfg["hca"] = {"m": w.m_hca, "W": w.W}
     line = {

@@ -22,9 +22,12 @@
 //     key's factor for its code block is the A scale of its row, 2^-e_h (hi rows) and 2^-(e_h+5)
 //     (lo rows) are the B scales, so the accumulator of a key holds D_hi + D_lo = q . khat per
 //     head directly and the epilogue forms score = sum_h w_h ReLU(D_hi[h] + D_lo[h]).  The scale
-//     factors reach TMEM with tcgen05.cp: the MMA warp rearranges a stage's 512 scale bytes into
-//     the 32-row x 16-byte form (row r's four bytes -- even key blocks 0/1, odd key blocks 0/1 --
-//     in word r / 32 of line r % 32), the producer writes the query's factors with its image.
+//     factors reach TMEM with tcgen05.cp, which wants an M = 128 operand's factors as 32 lines of
+//     16 bytes (row r's four bytes -- even key blocks 0/1, odd key blocks 0/1 -- in word r / 32 of
+//     line r % 32).  The codes are therefore loaded with a 4-D TMA map that puts TMA row 4 l + j
+//     of a stage into MMA row 32 j + l: the stage's 512 scale bytes, bulk-copied as they are
+//     stored, are then already that image (keys need Ncap % 256 == 0).  The producer writes the
+//     query's factors with its image.
 //   e4m3 keys (fp32 row scale): kind::f8f6f4; 2^-e_h is folded into the head weight w' and the
 //     row scale applied in the epilogue: score = s_key sum_h w'_h ReLU(D_hi[h] + 2^-5 D_lo[h]).
 // The epilogue works on pairs of heads with f32x2 arithmetic.  Apart from the exceptions above the
@@ -35,10 +38,10 @@
 //              two query slots (the next item's row is loaded one item ahead); per stage (one lane)
 //              the stage's (row, first key, visible count, flags) record, the TMA box of codes and
 //              a bulk copy of the scales;
-//   warp 5     one thread issues the MMAs of a stage into a TMEM accumulator buffer (two buffers
-//              when they fit in the 512 columns); with e2m1 keys the warp first lays out the
-//              stage's scale factors and copies them (and a new query's) into TMEM;
-//   warps 0-3  epilogue: thread j owns TMEM lane j (keys 2j and 2j+1 of the stage): scores to
+//   warp 5     hands the stage's record to the epilogue through the accumulator buffer's slot, then
+//              one thread copies the stage's scale factors (and a new query's) into TMEM and issues
+//              the MMAs into the buffer (up to four buffers, as TMEM allows);
+//   warps 0-3  epilogue: thread j owns TMEM lane j (two consecutive keys of the stage): scores to
 //              global memory, and the top-12-bit histogram of the scores (the top-k's first pass),
 //              accumulated per piece in shared memory (16-bit counts; a piece has at most 128
 //              stages) and added to the row's global histogram.
@@ -88,8 +91,8 @@ struct Cfg {
     static constexpr int NQ = Q4 ? HI : 2 * HI;                      // B rows: FP4 queries, or hi + lo rows
     static constexpr uint32_t code_tx = fp4 ? kPair * 32 : kPair * 64;  // global code bytes per stage
     static constexpr int scale_bytes = fp4 ? 2 : 4;                  // per key
-    // stage: codes (128 rows x 128 B, swizzled) | scales (fp4: 512 B, then the 512-byte factor
-    // image the MMA warp builds; e4m3: 1 KB) | record
+    // stage: codes (128 rows x 128 B, swizzled) | scales (e4m3: 1 KB; fp4: the 512-byte factor
+    // image at off_sfa) | record
     static constexpr uint32_t off_scale = 16384;
     static constexpr uint32_t off_sfa = off_scale + 512;
     static constexpr uint32_t off_meta = off_scale + kPair * 4;
@@ -408,8 +411,14 @@ __global__ void __launch_bounds__(kThreads) index_tc_kernel(const __grid_constan
                     const int64_t nk = (Ncap - s0) < kPair ? (Ncap - s0) : kPair;   // Ncap % 8 == 0
                     const uint32_t sbytes = (uint32_t)nk * C::scale_bytes;
                     mbar_arrive_expect_tx(&ms.full[s], C::code_tx + sbytes);
-                    tma_load_2d(sb, &kmap, 0, (int)(key0 / 2), &ms.full[s], pol_stream);
-                    bulk_g2s_hint(sb + C::off_scale, k_scale + key0 * C::scale_bytes, sbytes, &ms.full[s],
+                    if (C::fp4) {
+                        // MMA row R = 32 j + l holds TMA row 4 l + j of the 128 (keys 2(4l+j), +1), so the
+                        // stage's scale bytes, copied as they are stored, form the factor image
+                        tma_load_4d(sb, &kmap, 0, 0, 0, (int)(key0 / kPair), &ms.full[s], pol_stream);
+                    } else {
+                        tma_load_2d(sb, &kmap, 0, (int)(key0 / 2), &ms.full[s], pol_stream);
+                    }
+                    bulk_g2s_hint(sb + (C::fp4 ? C::off_sfa : C::off_scale), k_scale + key0 * C::scale_bytes, sbytes, &ms.full[s],
                                   pol_stream);
                 }
             }
@@ -442,15 +451,6 @@ __global__ void __launch_bounds__(kThreads) index_tc_kernel(const __grid_constan
                     mbar_arrive_cnt(&ms.dfull[d], 2);
                 }
                 break;
-            }
-            if (C::fp4) {
-                // A scale factors of the stage: row r (keys 2r, 2r+1) holds four UE8M0 bytes (even
-                // key blocks 0/1, odd key blocks 0/1); lane l gathers rows l, l+32, l+64, l+96
-                // into line l of the 32 x 16-byte image tcgen05.cp reads
-                const uint32_t* sc = reinterpret_cast<const uint32_t*>(sm + s * C::stage + C::off_scale);
-                *reinterpret_cast<uint4*>(sm + s * C::stage + C::off_sfa + 16 * lane) =
-                    make_uint4(sc[lane], sc[lane + 32], sc[lane + 64], sc[lane + 96]);
-                fence_proxy_async();
             }
             __syncwarp();
             // the accumulator buffer (with its record slot) is free once the epilogue has read it
@@ -599,7 +599,8 @@ __global__ void __launch_bounds__(kThreads) index_tc_kernel(const __grid_constan
             // (at the piece's end) query slot consumed
             __syncwarp();
             if (lane == 0 && (meta.w & kLast)) mbar_arrive(&ms.qfree[qs]);
-            const int64_t key = (int64_t)meta.y + 2 * tid;
+            // keys of TMEM lane tid: e2m1 tiles are loaded permuted (MMA row 32 j + l = TMA row 4 l + j)
+            const int64_t key = (int64_t)meta.y + 2 * (C::fp4 ? 4 * (tid & 31) + (tid >> 5) : tid);
             const bool v0 = key < meta.z, v1 = key + 1 < meta.z;
             float* dst = S + (int64_t)meta.x * Ncap + key;
             if (v1) st_global_v2_hint(dst, acc_e, acc_o, pol_keep);
@@ -648,9 +649,16 @@ cudaError_t launch_index_tc(const void* q_idx, const void* q_scale, const float*
     CUtensorMap kmap;
     std::memset(&kmap, 0, sizeof kmap);
     const uint64_t rows = (uint64_t)B * (uint64_t)Ncap / 2;          // two keys per row of 128 codes
-    const bool ok = C::fp4 ? encode_tmap_2d(&kmap, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, k_codes, 128, rows, 64, 128,
-                                            128)
-                           : encode_tmap_2d(&kmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, k_codes, 128, rows, 128, 128, 128);
+    bool ok;
+    if (C::fp4) {
+        // tiles of 128 TMA rows (256 keys) read as [l 32][j 4] with row 4 l + j landing in smem row 32 j + l
+        const uint64_t dims[4] = {128, 32, 4, rows / 128};
+        const uint64_t strides[3] = {4 * 64, 64, 128 * 64};
+        const uint32_t box[4] = {128, 32, 4, 1};
+        ok = rows % 128 == 0 && encode_tmap_nd(&kmap, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 4, k_codes, dims, strides, box);
+    } else {
+        ok = encode_tmap_2d(&kmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, k_codes, 128, rows, 128, 128, 128);
+    }
     if (!ok) return cudaErrorNotSupported;
     const size_t smem = (size_t)C::smem + 1024;
     // CTAs per SM: shared memory (228 KB per SM, 1 KB reserved per CTA) and TMEM (512 columns)
@@ -673,7 +681,8 @@ cudaError_t launch_index_tc(const void* q_idx, const void* q_scale, const float*
 bool index_tc_supported(int q_dtype, int key_fmt, int H_I, int d_I, int64_t Ncap, const void* k_codes,
                         const void* k_scale, int B, int64_t R) {
     return q_dtype == CSAHCA_BF16 && (key_fmt == CSAHCA_E4M3_ROWSCALE || key_fmt == CSAHCA_E2M1_UE8M0) &&
-           d_I == kDI && (H_I == 16 || H_I == 32 || H_I == 64) && Ncap % 8 == 0 && aligned(k_codes, 32) &&
+           d_I == kDI && (H_I == 16 || H_I == 32 || H_I == 64) &&
+           Ncap % (key_fmt == CSAHCA_E2M1_UE8M0 ? kPair : 8) == 0 && aligned(k_codes, 32) &&
            aligned(k_scale, 16) && (int64_t)B * Ncap / 2 >= 128 && (int64_t)B * Ncap < (1LL << 31) &&
            R * cdiv(Ncap, (int64_t)kChunkStages * kPair) < (1LL << 31);
 }

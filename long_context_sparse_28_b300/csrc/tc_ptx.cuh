@@ -396,3 +396,20 @@ __device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
 
 }  // namespace tc
 }  // namespace csahca
+
+namespace csahca {
+namespace tc {
+
+// 4-D tiled TMA load of the box at element coordinates (x, y, z, w) (see tma_load_2d).
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const void* map, int x, int y, int z, int w, uint64_t* bar,
+                                            uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3, %4, %5}], [%6], %7;"
+        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(smem_u32(bar)),
+          "l"(policy)
+        : "memory");
+}
+
+}  // namespace tc
+}  // namespace csahca

@@ -13,4 +13,10 @@ namespace csahca {
 bool encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType type, const void* base, uint64_t inner, uint64_t rows,
                     uint64_t pitch, uint32_t box_inner, uint32_t box_rows);
 
+// Encodes an N-D tiled map (N <= 5): dims[0] elements innermost, strides[i] = byte stride of
+// dims[i + 1] (any order: a map may visit rows in a permuted order), box[i] per dimension,
+// 128-byte swizzle.  False when the driver rejects it.
+bool encode_tmap_nd(CUtensorMap* map, CUtensorMapDataType type, int rank, const void* base, const uint64_t* dims,
+                    const uint64_t* strides, const uint32_t* box);
+
 }  // namespace csahca

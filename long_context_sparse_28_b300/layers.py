@@ -29,7 +29,7 @@ class CSACache:
     """Compressed sparse attention cache of B sequences (m = 4 by default)."""
 
     def __init__(self, B, Ncap, d, W, d_I, key_fmt, dtype, device="cuda", m=4):
-        Ncap = (Ncap + 7) // 8 * 8      # capacity in multiples of 8 entries (tensor-core indexer tiles)
+        Ncap = (Ncap + 255) // 256 * 256   # capacity in whole 256-key tensor-core indexer stages
         self.B, self.Ncap, self.d, self.W, self.d_I, self.m = B, Ncap, d, W, d_I, m
         self.key_fmt, self.dtype, self.device = key_fmt, dtype, device
         self.ck = torch.zeros(B, Ncap, d, dtype=dtype, device=device)

@@ -63,9 +63,10 @@ def test_hca_prefix_into_a_slot_of_a_running_cache(tmp_path):
 
 
 def test_damaged_or_mismatched_files_are_refused(tmp_path):
-    src = _fill(CSACache(1, 16, 64, 16, 64, L.KEY_FMT["e2m1"], torch.bfloat16, "cpu"), 4)
+    # CSA caches hold whole 256-entry stages: capacity 512 here, 256 for the small one below
+    src = _fill(CSACache(1, 300, 64, 16, 64, L.KEY_FMT["e2m1"], torch.bfloat16, "cpu"), 4)
     p = tmp_path / "a.kv"
-    cache_io.save_prefix(str(p), src, [60])
+    cache_io.save_prefix(str(p), src, [4 * 300])
     raw = p.read_bytes()
     bad = tmp_path / "bad.kv"
     bad.write_bytes(b"XXXXXXXX" + raw[8:])
@@ -77,14 +78,14 @@ def test_damaged_or_mismatched_files_are_refused(tmp_path):
     bad.write_bytes(raw[: len(raw) - 100])
     with pytest.raises(ValueError, match="out of bounds"):
         cache_io.load_prefix(str(bad), device="cpu")
-    other = CSACache(1, 16, 64, 16, 64, L.KEY_FMT["e4m3"], torch.bfloat16, "cpu")
+    other = CSACache(1, 300, 64, 16, 64, L.KEY_FMT["e4m3"], torch.bfloat16, "cpu")
     with pytest.raises(ValueError, match="key_fmt"):
         cache_io.load_prefix_into(str(p), other, 0)
     small = CSACache(1, 8, 64, 16, 64, L.KEY_FMT["e2m1"], torch.bfloat16, "cpu")
     with pytest.raises(ValueError, match="does not fit"):
         cache_io.load_prefix_into(str(p), small, 0)
     with pytest.raises(ValueError, match="do not fit"):
-        cache_io.save_prefix(str(tmp_path / "c.kv"), src, [4 * 17])
+        cache_io.save_prefix(str(tmp_path / "c.kv"), src, [4 * 513])
 
 
 def _rewrite_header(raw: bytes, header: dict) -> bytes:

@@ -169,9 +169,11 @@ def test_bounded_wait_times_out_and_context_survives():
 @pytest.mark.parametrize("fmt,q_dt,Ncap,H_I", [("f32", "f32", 700, 16), ("bf16", "bf16", 700, 16),
                                                ("e4m3", "bf16", 700, 16), ("e2m1", "bf16", 700, 16),
                                                ("e4m3", "bf16", 1000, 16), ("e2m1", "bf16", 1000, 16),
-                                               ("e2m1", "bf16", 1000, 32), ("e4m3", "bf16", 1000, 64)])
+                                               ("e2m1", "bf16", 1024, 16), ("e2m1", "bf16", 1024, 32),
+                                               ("e2m1", "bf16", 1280, 64), ("e4m3", "bf16", 1000, 64)])
 def test_index_scores_and_topk_parity(fmt, q_dt, Ncap, H_I):
-    # Ncap % 8 == 0 (1000) runs the tensor-core indexer for e4m3/e2m1 keys; 700 the generic kernel
+    # the tensor-core indexer runs for e4m3 keys with Ncap % 8 == 0 (1000) and e2m1 keys with
+    # Ncap % 256 == 0 (1024, 1280); the other cases take the generic kernel
     B, T, d_I, m, k = 2, 3, 64, 4, 96
     F = L.KEY_FMT[fmt]
     kin = rnd((B, Ncap, d_I), torch.float32, 21)
@@ -205,7 +207,7 @@ def test_index_scores_and_topk_parity(fmt, q_dt, Ncap, H_I):
 def test_index_fp4_queries_parity(H_I):
     # both indexer operands in FP4: the queries quantised to MX E2M1 (bit-exact with the oracle's
     # rule), then scores against the oracle's scores of the dequantised queries, and the top-k
-    B, T, Ncap, d_I, m, k = 3, 2, 5000, 64, 4, 300
+    B, T, Ncap, d_I, m, k = 3, 2, 5120, 64, 4, 300
     kin = rnd((B, Ncap, d_I), torch.bfloat16, 51)
     kin[1, 7] *= 4
     codes, scales = L.key_storage(B, Ncap, d_I, L.E2M1_UE8M0)
@@ -274,11 +276,11 @@ def test_prefill_indexer_tensor_core_parity(H_I, T):
 
 @pytest.mark.parametrize("fmt", ["e2m1", "e4m3"])
 def test_index_topk_one_bin_over_65536_keys_per_cta(fmt):
-    # 80 rows of 250000 identical index keys: all scores of a row are equal, so the exact top-k
+    # 80 rows of 250112 identical index keys: all scores of a row are equal, so the exact top-k
     # is the first k entries (ties to the lower index) and every key of a row lands in one
     # histogram bin.  The tensor-core indexer's CTAs then stream more than 65536 keys of one row
     # each, which its 16-bit shared-memory counts only survive by being flushed in between.
-    B, Ncap, d_I, H_I, m, k = 80, 250000, 64, 16, 4, 1024
+    B, Ncap, d_I, H_I, m, k = 80, 250112, 64, 16, 4, 1024
     F = L.KEY_FMT[fmt]
     one = rnd((1, 8, d_I), torch.bfloat16, 31)
     c1, s1 = L.key_storage(1, 8, d_I, F)

@@ -49,6 +49,7 @@ class Workload:
     bias_std: float = 0.5
     outlier_frac: float = 0.0
     outlier_mult: float = 4.0
+    index_q: str = "bf16"     # indexer queries: "bf16", or "e2m1" (FP4, the keys' MX form)
     seed: int = 0
 
     def lengths(self) -> list[int]:
@@ -87,6 +88,10 @@ WORKLOADS = {
         d=128, H=64, H_I=16, d_I=64, k=1024, W=128, kv="bf16", key_fmt="e2m1",
         outlier_frac=0.01),
 }
+
+# The 1M-context decode workload with the lightning indexer's queries in FP4 as well.
+WORKLOADS["decode_1m_b32_csa_hca_q4"] = replace(WORKLOADS["decode_1m_b32_csa_hca"], name="decode_1m_b32_csa_hca_q4",
+                                               index_q="e2m1")
 
 KEY_FMT_CODE = {"f32": 0, "bf16": 1, "e4m3": 2, "e2m1": 3}
 
