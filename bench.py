@@ -896,6 +896,121 @@ def run_e2e_prefill(bench, w, n, dev, dist):
                     "(one CUDA graph), D2H copy of both layers' outputs, on one stream"}
 
 
+# ------------------------------------------------------------------------- bulk pooling
+POOL_METRIC = "CSA+HCA bulk pooling of a 1M-token sequence: raw tokens/s on 1 B300"
+
+
+def run_pool(args, dist):
+    """Both compressors over one sequence's raw K/V/gates (m = 4 and m = 128), the caches written;
+    value = raw tokens pooled per second (each token through both compressors)."""
+    import long_context_sparse_28_b300 as L
+    dev = torch.device("cuda", dist.local)
+    torch.cuda.set_device(dev)
+    w = wl.WORKLOADS[args.workload]
+    n = w.L[0]
+    k, v, g = wl.raw_tokens(w, "pool", 0, n, dev)
+    k, v, g = k[None].contiguous(), v[None].contiguous(), g[None].contiguous()
+    cb, hb = wl.layer_bias(w, "csa", w.m_csa, dev), wl.layer_bias(w, "hca", w.m_hca, dev)
+    n_c, n_h = n // w.m_csa, n // w.m_hca
+    ck = torch.empty(1, n_c, w.d, dtype=torch.bfloat16, device=dev)
+    cv = torch.empty_like(ck)
+    hk = torch.empty(1, n_h, w.d, dtype=torch.bfloat16, device=dev)
+    hv = torch.empty_like(hk)
+    p0 = torch.zeros(1, dtype=torch.int64, device=dev)
+    nr = torch.full((1,), n, dtype=torch.int64, device=dev)
+    K, Wm = args.steps, args.warmup
+    stream = torch.cuda.Stream(device=dev)
+
+    def call(i):
+        if i == 0:
+            L.csa_compress(k, v, g, p0, nr, cb, w.m_csa, ck, cv)
+        else:
+            L.hca_compress(k, v, g, p0, nr, hb, w.m_hca, hk, hv)
+
+    with torch.cuda.stream(stream):
+        for _ in range(Wm):
+            call(0)
+            call(1)
+    stream.synchronize()
+    c0 = L.launch_count()
+    evs = [_events(3) for _ in range(K)]
+    sampler = ClockSampler(dev.index if dev.index is not None else 0)
+    dist.barrier()
+    with sampler:
+        with torch.cuda.stream(stream):
+            for s in range(K):
+                _record(evs[s][0], stream)
+                call(0)
+                _record(evs[s][1], stream)
+                call(1)
+                _record(evs[s][2], stream)
+        stream.synchronize()
+    launches = L.launch_count() - c0
+    ms_c = statistics.mean(_elapsed_ms(evs[s][0], evs[s][1]) for s in range(K))
+    ms_h = statistics.mean(_elapsed_ms(evs[s][1], evs[s][2]) for s in range(K))
+    ms_step = dist.max(statistics.mean(_elapsed_ms(evs[s][0], evs[s][2]) for s in range(K)))
+    assert L.device_status(stream) == 0
+    row = w.d * 2
+    bytes_c = n * (2 * row + 4) + n_c * 2 * row          # raw K, V, gates read; entries written
+    bytes_h = n * (2 * row + 4) + n_h * 2 * row
+    peaks = {}
+    try:
+        peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+    except Exception:
+        pass
+    hbm = peaks.get("hbm_gbs", 6400.0)
+    dom, ms_dom, b_dom = ("csa_compress", ms_c, bytes_c) if ms_c >= ms_h else ("hca_compress", ms_h, bytes_h)
+    ach = b_dom / (ms_dom / 1e3) / 1e9
+    roofline = {"bound": "hbm", "kernel": dom, "achieved": round(ach, 1), "peak": hbm, "unit": "GB/s",
+                "frac": round(ach / hbm, 4), "traffic": None, "algorithmic_bytes_per_launch": int(b_dom),
+                "avg_launch_ms": round(ms_dom, 4), "peak_source": "measured" if "hbm_gbs" in peaks else "fallback"}
+    e2e = None
+    if not args.no_e2e:
+        hk_, hv_, hg_ = (t.to("cpu").pin_memory() for t in (k, v, g))
+        out_h = torch.empty(ck.shape, dtype=torch.bfloat16, pin_memory=True)
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        nrep = max(1, min(K, 5))
+        with torch.cuda.stream(stream):
+            t0.record(stream)
+            for _ in range(nrep):
+                k.copy_(hk_, non_blocking=True)
+                v.copy_(hv_, non_blocking=True)
+                g.copy_(hg_, non_blocking=True)
+                call(0)
+                call(1)
+                out_h.copy_(ck, non_blocking=True)
+            t1.record(stream)
+        stream.synchronize()
+        ms_e = dist.max(t0.elapsed_time(t1)) / nrep
+        e2e = {"value": round(n / (ms_e / 1e3), 1), "unit": "raw tokens/s", "ms_per_step": round(ms_e, 4),
+               "h2d_bytes_per_step": int(hk_.numel() * 2 + hv_.numel() * 2 + hg_.numel() * 4),
+               "d2h_bytes_per_step": int(out_h.numel() * 2),
+               "path": "per step: H2D copy of the raw K, V and gates from pinned host memory, both compressors, "
+                       "D2H copy of the CSA keys' cache"}
+    cpu = None
+    if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
+        import oracle
+        nb = 2048                                     # a bounded sample: the first 2048 x 128 tokens
+        K_, V_, G_ = (wl.to_numpy(t[0, :nb * w.m_hca]) for t in (k, v, g))
+        t0c = time.perf_counter()
+        oracle.compress(K_, V_, G_, wl.to_numpy(cb), w.m_csa, oracle.BF16)
+        oracle.compress(K_, V_, G_, wl.to_numpy(hb), w.m_hca, oracle.BF16)
+        dt = time.perf_counter() - t0c
+        cpu = {"value": round(nb * w.m_hca / dt, 1), "unit": "raw tokens/s", "cores": oracle.num_threads(),
+               "kind": "oracle", "sample": f"the first {nb * w.m_hca} of {n} tokens through both compressors "
+                                           f"(fp64 C oracle, OpenMP); {dt:.2f} s"}
+    return {"metric": POOL_METRIC, "value": round(n * dist.world / (ms_step / 1e3), 1), "unit": "raw tokens/s",
+            "n_gpus": dist.world, "steps": K, "warmup": Wm, "ms_per_step": round(ms_step, 5),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": w.name, "L": n, "d": w.d, "m": [w.m_csa, w.m_hca],
+                       "parallelism": f"replicas x{dist.world}",
+                       "l2": "inputs (516 MB) larger than L2; no flush",
+                       "substep_ms": {"csa_compress": round(ms_c, 4), "hca_compress": round(ms_h, 4)},
+                       "algorithmic_bytes": {"csa_compress": int(bytes_c), "hca_compress": int(bytes_h)}},
+            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": int(launches),
+            "clocks": sampler.summary()}
+
+
 # ------------------------------------------------------------------------ reference arm
 def run_reference(args, dist):
     """The CPU oracle as it stands, on the host cores, on a bounded sample of the workload:
@@ -956,6 +1071,8 @@ def main():
             line = run_reference(args, dist)
         elif wl.WORKLOADS[args.workload].kind == "hybrid_prefill":
             line = run_prefill(args, dist)
+        elif wl.WORKLOADS[args.workload].kind == "pool":
+            line = run_pool(args, dist)
         else:
             line = run_ours(args, dist)
         if dist.rank == 0:

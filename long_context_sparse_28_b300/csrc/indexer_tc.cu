@@ -38,9 +38,10 @@
 //              two query slots (the next item's row is loaded one item ahead); per stage (one lane)
 //              the stage's (row, first key, visible count, flags) record, the TMA box of codes and
 //              a bulk copy of the scales;
-//   warp 5     hands the stage's record to the epilogue through the accumulator buffer's slot, then
-//              one thread copies the stage's scale factors (and a new query's) into TMEM and issues
-//              the MMAs into the buffer (up to four buffers, as TMEM allows);
+//   warps 5-6  MMA warps, taking alternate stages (their per-stage waits and issue overlap): hand the
+//              stage's record to the epilogue through the accumulator buffer's slot, then one thread
+//              copies the stage's scale factors (and a new query's) into TMEM and issues the MMAs
+//              into the buffer (up to four buffers, as TMEM allows);
 //   warps 0-3  epilogue: thread j owns TMEM lane j (two consecutive keys of the stage): scores to
 //              global memory, and the top-12-bit histogram of the scores (the top-k's first pass),
 //              accumulated per piece in shared memory (16-bit counts; a piece has at most 128
@@ -63,8 +64,10 @@ constexpr int kDI = 64;
 constexpr int kChunkStages = 8;       // stages per work item: 2048 keys of one query row
 constexpr int kMaxNS = 6;             // shared-memory stages (at most)
 constexpr int kEpi = 128;             // epilogue threads (warps 0-3)
-constexpr int kThreads = kEpi + 64;   // + producer warp + MMA warp
-constexpr int kTerm = 1, kLast = 2;   // stage flags: no more work / last stage of a piece
+constexpr int kMmaWarps = 2;          // MMA-issuing warps, taking alternate stages
+constexpr int kThreads = kEpi + 32 + 32 * kMmaWarps;   // + producer warp + MMA warps
+// stage flags: no more work (kFirstTerm: the record the epilogue receives) / last stage of a piece
+constexpr int kTerm = 1, kLast = 2, kFirstTerm = 4;
 // Longest piece: its keys' histogram is kept in 16-bit shared-memory counts until the piece ends
 constexpr int kMaxPieceStages = 128;  // 32768 keys
 enum : uint32_t { kE4M3 = 0, kE2M1 = 5 };   // kind::f8f6f4 operand formats
@@ -106,11 +109,7 @@ struct Cfg {
     // alignment slack, the static shared memory)
     static constexpr int ns_fit = (int)((114 * 1024 - 1024 - 1024 - sizeof(IdxMisc) - 2 * q_slot -
                                          (fp4 ? 0 : kMaxBuf * kPair * 4)) / stage);
-    static constexpr int NS = ns_fit < 3 ? 3 : (ns_fit > kMaxNS ? kMaxNS : ns_fit);
-    static constexpr uint32_t off_qslots = NS * stage;
-    // e4m3: the row scales of the stage in each accumulator buffer (copied by the MMA warp)
-    static constexpr uint32_t off_dscale = off_qslots + 2 * q_slot;
-    static constexpr uint32_t smem = off_dscale + (fp4 ? 0 : kMaxBuf * kPair * 4);
+    static constexpr int ns_cap = ns_fit < 3 ? 3 : (ns_fit > kMaxNS ? kMaxNS : ns_fit);
     static constexpr uint32_t acc_cols = NQ;                         // one accumulator: hi | lo columns (or FP4 q)
     static constexpr uint32_t d_cols = 2 * acc_cols;                 // even + odd keys
     // fp4: scale factors of A (4 columns per stage slot) and B (4 per query slot)
@@ -119,8 +118,20 @@ struct Cfg {
     // stage nbuf earlier, so more buffers keep more stages between the two in flight; as many as
     // fit in 256 columns (two CTAs per SM), else in 512
     static constexpr int fit256 = (int)((256 - sf_cols) / d_cols), fit512 = (int)((512 - sf_cols) / d_cols);
-    static constexpr int nbuf = fit256 >= 2 ? (fit256 < kMaxBuf ? fit256 : kMaxBuf)
-                                            : (fit512 < kMaxBuf ? (fit512 < 1 ? 1 : fit512) : kMaxBuf);
+    static constexpr int nbuf_fit = fit256 >= 2 ? (fit256 < kMaxBuf ? fit256 : kMaxBuf)
+                                                : (fit512 < kMaxBuf ? (fit512 < 1 ? 1 : fit512) : kMaxBuf);
+    // Two MMA warps take alternate stages.  An mbarrier wait on a phase parity is only sound when
+    // its waiter consumes the barrier's phases one after another, so each warp must own its own
+    // stage slots and accumulator buffers: even counts of both (stage u: slot u % NS and buffer
+    // u % nbuf have the parity of u).  With a single buffer there is one MMA warp.
+    static constexpr int NMW = nbuf_fit >= 2 ? 2 : 1;
+    static constexpr int nbuf = NMW == 2 ? nbuf_fit / 2 * 2 : nbuf_fit;
+    static constexpr int NS = NMW == 2 ? ns_cap / 2 * 2 : ns_cap;
+    static_assert(NMW == 1 || (NS % 2 == 0 && nbuf % 2 == 0), "stage slots and buffers per MMA warp");
+    static constexpr uint32_t off_qslots = NS * stage;
+    // e4m3: the row scales of the stage in each accumulator buffer (copied by the MMA warp)
+    static constexpr uint32_t off_dscale = off_qslots + 2 * q_slot;
+    static constexpr uint32_t smem = off_dscale + (fp4 ? 0 : kMaxBuf * kPair * 4);
     static constexpr uint32_t sfa_col = nbuf * d_cols, sfb_col = sfa_col + 4 * kMaxNS;
     static constexpr uint32_t used_cols = nbuf * d_cols + sf_cols;
     static constexpr uint32_t tmem_cols = used_cols <= 32 ? 32 : used_cols <= 64 ? 64 : used_cols <= 128 ? 128
@@ -230,7 +241,9 @@ __global__ void __launch_bounds__(kThreads) index_tc_kernel(const __grid_constan
             mbar_init(&ms.dfull[d], 2);       // the MMA commit + the MMA warp's record of the stage
             mbar_init(&ms.dfree[d], 4);
         }
-        for (int d = 0; d < 2; ++d) mbar_init(&ms.qfree[d], 5);   // MMA commit + 4 epilogue warps, once per item
+        // 4 epilogue warps, once per item: the epilogue takes the stages in order after their MMAs
+        // completed, so its arrivals at a piece's end imply that every MMA of the piece is done
+        for (int d = 0; d < 2; ++d) mbar_init(&ms.qfree[d], 4);
         fence_mbar_init();
     }
     if (tid < kEpi)
@@ -424,26 +437,32 @@ __global__ void __launch_bounds__(kThreads) index_tc_kernel(const __grid_constan
             }
             u = __shfl_sync(0xffffffffu, u, 0);
         }
-        if (lane == 0) {                      // end of work
-            const uint32_t s = u % C::NS;
-            if (u >= (uint32_t)C::NS) mbar_wait(&ms.empty[s], ((u / C::NS) + 1) & 1, err);
-            *reinterpret_cast<int4*>(sm + s * C::stage + C::off_meta) = make_int4(0, 0, 0, kTerm);
-            mbar_arrive(&ms.full[s]);
+        if (lane == 0) {                      // end of work: one record for each MMA warp
+            for (int j = 0; j < C::NMW; ++j, ++u) {
+                const uint32_t s = u % C::NS;
+                if (u >= (uint32_t)C::NS) mbar_wait(&ms.empty[s], ((u / C::NS) + 1) & 1, err);
+                *reinterpret_cast<int4*>(sm + s * C::stage + C::off_meta) = make_int4(0, 0, 0, kTerm | (j ? 0 : kFirstTerm));
+                mbar_arrive(&ms.full[s]);
+            }
         }
         __syncwarp();
-    } else if (warp == 5) {
+    } else if (warp >= 5 && warp < 5 + kMmaWarps) {
         // ============================================================================= MMA
         constexpr uint32_t af = C::fp4 ? kE2M1 : kE4M3;
         // descriptors of stage 0 and query slot 0; other addresses add (offset >> 4)
         const uint64_t a_desc0 = smem_desc(sbase, 16, 1024);
         const uint64_t b_desc0 = smem_desc(sbase + C::off_qslots, 16, 1024);
-        int prev_piece = -1;                      // piece (low 15 bits) of the previous stage
-        for (uint32_t u = 0;; ++u) {
+        // stages u = mw, mw + kMmaWarps, ...: the two warps' per-stage waits and issue overlap; each
+        // stage's MMAs and commits come from one thread, so the commits track exactly that stage
+        const uint32_t mw = (uint32_t)(warp - 5);
+        int prev_piece = -1;                      // piece (low 15 bits) of this warp's previous stage
+        for (uint32_t u = mw; mw < (uint32_t)C::NMW; u += C::NMW) {
             const uint32_t s = u % C::NS;
             mbar_wait(&ms.full[s], (u / C::NS) & 1, err);
             const int4 meta = *reinterpret_cast<const int4*>(sm + s * C::stage + C::off_meta);
             const uint32_t d = u % C::nbuf, qs = (uint32_t)(meta.w >> 8) & 1u;
             if (meta.w & kTerm) {
+                if (!(meta.w & kFirstTerm)) break;
                 // end of work: hand the record to the epilogue through the next buffer
                 if (u >= (uint32_t)C::nbuf) mbar_wait(&ms.dfree[d], ((u / C::nbuf) + 1) & 1, err);
                 if (lane == 0) {
@@ -495,7 +514,6 @@ __global__ void __launch_bounds__(kThreads) index_tc_kernel(const __grid_constan
                 }
                 mma_commit(&ms.dfull[d]);
                 mma_commit(&ms.empty[s]);
-                if (meta.w & kLast) mma_commit(&ms.qfree[qs]);
             }
             prev_piece = meta.w >> 16;
             __syncwarp();

@@ -24,7 +24,7 @@ import torch
 @dataclass(frozen=True)
 class Workload:
     name: str
-    kind: str                 # "csa_decode" | "hca_decode" | "hybrid_decode" | "hybrid_prefill"
+    kind: str                 # "csa_decode" | "hca_decode" | "hybrid_decode" | "hybrid_prefill" | "pool"
     B: int
     d: int
     H: int
@@ -88,6 +88,10 @@ WORKLOADS = {
         d=128, H=64, H_I=16, d_I=64, k=1024, W=128, kv="bf16", key_fmt="e2m1",
         outlier_frac=0.01),
 }
+
+# Bulk pooling of one 1M-token sequence into both compressed caches (CSA m=4, HCA m=128), bf16, d=128.
+WORKLOADS["pool_1m_bf16"] = Workload(name="pool_1m_bf16", kind="pool", B=1, L=(1 << 20,), d=128, H=64, kv="bf16",
+                                     kv_std=1.0)
 
 # The 1M-context decode workload with the lightning indexer's queries in FP4 as well.
 WORKLOADS["decode_1m_b32_csa_hca_q4"] = replace(WORKLOADS["decode_1m_b32_csa_hca"], name="decode_1m_b32_csa_hca_q4",
