@@ -180,7 +180,8 @@ size_t csa_topk_workspace(int R, int64_t row_stride, int k);
  *     s_i = scale * q[h] . key_i;  out[h] = sum_i softmax(s)_i value_i;  lse[h] = logsumexp(s)
  *   q       : [B][T][H][d] dtype;  out: [B][T][H][d] dtype;  lse: NULL or [B][T][H] float32
  *   ck, cv  : [B][Ncap][d] dtype;  idx: [B][T][k] int32 (-1 entries are skipped; an entry
- *             outside [0, Ncap) is skipped and flags CSAHCA_ERR_BOUNDS on the device)
+ *             outside [0, Ncap) is skipped and flags CSAHCA_ERR_BOUNDS on the device);
+ *             k = 0 (idx may then be NULL) attends over the raw window alone
  *   ring_k, ring_v : [B][ring_cap][d] dtype (token t in slot t % ring_cap)
  *   chunk_k, chunk_v : NULL (decode) or [B][chunk_stride][d] raw tokens starting at position
  *             chunk_pos0[b] (int64, device); window tokens >= chunk_pos0[b] come from here

@@ -302,7 +302,7 @@ csahca_status attend_validate(const AttendArgs& a) {
     if (a.W > 0) CSAHCA_REQUIRE(a.ring_k && a.ring_v && a.ring_cap >= 1);
     if (!a.chunk_k) CSAHCA_REQUIRE(a.W <= a.ring_cap || a.W == 0);
     else CSAHCA_REQUIRE(a.chunk_v && a.chunk_pos0 && a.chunk_stride >= 1);
-    if (a.is_csa) CSAHCA_REQUIRE(a.idx && a.k >= 0);
+    if (a.is_csa) CSAHCA_REQUIRE(a.k >= 0 && (a.idx || a.k == 0));   // k = 0: the window alone
     else CSAHCA_REQUIRE(a.m >= 1);
     const size_t al = (a.dtype == CSAHCA_F32) ? 32 : 16;
     CSAHCA_REQUIRE(aligned(a.q, al) && aligned(a.ck, al) && aligned(a.cv, al));

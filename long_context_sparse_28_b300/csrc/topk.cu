@@ -106,8 +106,8 @@ __device__ __forceinline__ float bin_floor_value(int b) {
 constexpr int kWarpSpan = 1024;    // scores per warp and step of the collect pass (32 per lane)
 constexpr int kSmemWords = 8192;   // bitmap words of a slice kept in shared memory (262144 entries)
 constexpr int kMaxCluster = 8;
-// shared memory: candidates | histogram of this CTA | cluster sums | two bitmaps
-constexpr size_t kSelSmem = (size_t)kCap * 8 + 2 * (size_t)kBins12 * 4 + 2 * (size_t)kSmemWords * 4;
+// shared memory: candidates | the cluster's candidates | two histograms | two bitmaps
+constexpr size_t kSelSmem = 2 * (size_t)kCap * 8 + 2 * (size_t)kBins12 * 4 + 2 * (size_t)kSmemWords * 4;
 
 // Appends the elements >= tv of the warp's span [w0, w0 + cnt_n) of `row` to the shared
 // candidate list (16-byte loads when aligned and full, one shared atomic per warp).
@@ -181,7 +181,8 @@ __global__ void __launch_bounds__(kSelThreads, 1) topk_select_kernel(
     cg::cluster_group cl = cg::this_cluster();
     extern __shared__ __align__(16) unsigned char fsm[];
     uint2* cs = reinterpret_cast<uint2*>(fsm);
-    uint32_t* hmine = reinterpret_cast<uint32_t*>(fsm + (size_t)kCap * 8);
+    uint2* ga = cs + kCap;                             // the whole row's candidates (fast path)
+    uint32_t* hmine = reinterpret_cast<uint32_t*>(fsm + 2 * (size_t)kCap * 8);
     uint32_t* hsum = hmine + kBins12;
     uint32_t* swin = hsum + kBins12;
     uint32_t* stie = swin + kSmemWords;
@@ -224,6 +225,108 @@ __global__ void __launch_bounds__(kSelThreads, 1) topk_select_kernel(
     }
     __syncthreads();
     const int nc = fast ? min(sh_nc, kCap) : 0;
+    if (fast) {
+        // ---- every CTA gathers the row's candidates from the cluster and resolves the row alone
+        cl.sync();                                  // every candidate list is complete
+        int tot = 0;
+        for (int q = 0; q < P; ++q) {
+            const int nq = min(*cl.map_shared_rank(&sh_nc, q), kCap - tot);   // the row holds <= kCap
+            const uint2* src = q == p ? cs : cl.map_shared_rank(cs, q);
+            for (int i = tid; i < nq; i += nthr) ga[tot + i] = src[i];
+            tot += nq;
+        }
+        __syncthreads();
+        // bits 19..8 and 7..0 of the boundary bin's members
+        for (int i = tid; i < tot; i += nthr) {
+            const uint32_t key = ga[i].x;
+            if ((int)(key >> 20) == b1) atomicAdd(&hmine[(key >> 8) & 0xFFFu], 1u);
+        }
+        __syncthreads();
+        int b2;
+        uint32_t above2;
+        find_bin(hmine, kBins12, (uint32_t)k - above1, sh_scan, sh_res, &b2, &above2);
+        const uint32_t pre = ((uint32_t)b1 << 12) | (uint32_t)b2;
+        for (int i = tid; i < kBins12; i += nthr) hsum[i] = 0;
+        __syncthreads();
+        for (int i = tid; i < tot; i += nthr) {
+            const uint32_t key = ga[i].x;
+            if ((key >> 8) == pre) atomicAdd(&hsum[key & 0xFFu], 1u);
+        }
+        __syncthreads();
+        int b3;
+        uint32_t above3;
+        find_bin(hsum, kBins8 < nthr ? nthr : kBins8, (uint32_t)k - above1 - above2, sh_scan, sh_res, &b3, &above3);
+        const uint32_t thr = (pre << 8) | (uint32_t)b3;
+        const int ties_needed = (int)((uint32_t)k - above1 - above2 - above3);
+        // selected entries before this CTA's slice: its output offset, and the ties already taken
+        if (tid == 0) {
+            sh_cnt[0] = 0;
+            sh_cnt[1] = 0;
+        }
+        for (int64_t w = tid; w < sw; w += nthr) {
+            wr[w] = 0u;
+            tr[w] = 0u;
+        }
+        __syncthreads();
+        int a_before = 0, t_before = 0;
+        for (int i = tid; i < tot; i += nthr) {
+            const uint2 e = ga[i];
+            if ((int64_t)e.y < s_lo) {
+                a_before += e.x > thr;
+                t_before += e.x == thr;
+            }
+        }
+        a_before = __reduce_add_sync(0xffffffffu, a_before);
+        t_before = __reduce_add_sync(0xffffffffu, t_before);
+        if (lane == 0) {
+            atomicAdd(&sh_cnt[0], a_before);
+            atomicAdd(&sh_cnt[1], t_before);
+        }
+        // this slice's bitmaps, from its own candidates
+        for (int i = tid; i < nc; i += nthr) {
+            const uint2 e = cs[i];
+            const uint32_t li = e.y - (uint32_t)s_lo;
+            if (e.x > thr) atomicOr(&wr[li >> 5], 1u << (li & 31));
+            else if (e.x == thr) atomicOr(&tr[li >> 5], 1u << (li & 31));
+        }
+        __threadfence_block();
+        __syncthreads();
+        const int out_off = sh_cnt[0] + min(ties_needed, sh_cnt[1]);
+        const int my_ties = max(0, ties_needed - sh_cnt[1]);
+        const int64_t per = (sw + nthr - 1) / nthr;
+        const int64_t v0 = min(sw, (int64_t)tid * per), v1 = min(sw, v0 + per);
+        int nwin = 0, ntie = 0;
+        for (int64_t w = v0; w < v1; ++w) {
+            nwin += __popc(wr[w]);
+            ntie += __popc(tr[w]);
+        }
+        int tot_tie, tot_sel;
+        const int tie_before_local = block_exclusive_scan(ntie, sh_scan, &tot_tie);
+        const int take = max(0, min(my_ties - tie_before_local, ntie));
+        const int pos0 = block_exclusive_scan(nwin + take, sh_scan, &tot_sel);
+        int pos = out_off + pos0, rem = take;
+        for (int64_t w = v0; w < v1; ++w) {
+            uint32_t t = tr[w];
+            uint32_t tsel = 0;
+            while (t && rem > 0) {
+                const uint32_t low = t & (~t + 1u);
+                tsel |= low;
+                t ^= low;
+                --rem;
+            }
+            uint32_t bits = wr[w] | tsel;
+            while (bits) {
+                const int b = __ffs(bits) - 1;
+                if (pos < k) out[pos] = (int32_t)(s_lo + (w * 32 + b));
+                ++pos;
+                bits &= bits - 1;
+            }
+        }
+        cl.sync();                                  // the others have finished reading this CTA's list
+        return;
+    }
+    // ---- the slow path: the boundary bin holds too many entries for the candidate lists; every
+    // pass re-reads the slice and the histograms are summed over the cluster
     // visits (key, index) of this CTA's part: its candidates, or its whole slice
     auto for_each = [&](auto&& f) {
         if (fast) {

@@ -199,3 +199,83 @@ def hybrid_prefill_chunk(csa: CSACache, hca: HCACache, pos0, T, chunk_k, chunk_v
     step = HybridPrefill(csa, hca, T, q_csa.shape[2], k, csa_bias, hca_bias, scale)
     step.set_position(pos0)
     return step.step(chunk_k, chunk_v, chunk_gate, kidx_chunk, q_csa, q_idx, w, q_hca, scores_out=scores_out)
+
+
+# ------------------------------------------------------------------ layer-interleave timeline
+def interleave_kinds(n_layers: int, mtp: bool = True) -> list[str]:
+    """Attention kind of each layer of the stack (pogovet.com article, detail 5): the first two layers
+    HCA, then CSA and HCA alternating (CSA first), and an MTP block whose attention is sliding-window
+    only ("swa")."""
+    kinds = ["hca" if i < 2 else ("csa" if i % 2 == 0 else "hca") for i in range(n_layers)]
+    return kinds + (["swa"] if mtp else [])
+
+
+class SWACache:
+    """Sliding-window-only attention state: the ring of the last W raw tokens."""
+
+    def __init__(self, B, d, W, dtype, device="cuda"):
+        self.B, self.d, self.W, self.dtype, self.device = B, d, W, dtype, device
+        self.ring_k = torch.zeros(B, W, d, dtype=dtype, device=device)
+        self.ring_v = torch.zeros(B, W, d, dtype=dtype, device=device)
+        self.ring_gate = torch.zeros(B, W, dtype=torch.float32, device=device)
+        # attention reads no compressed entry: a one-row placeholder cache and an empty index list
+        self.ck = torch.zeros(B, 1, d, dtype=dtype, device=device)
+        self.cv = torch.zeros(B, 1, d, dtype=dtype, device=device)
+
+    def build_seq(self, b, k_raw, v_raw, gate, n_ctx):
+        _fill_ring(self, b, k_raw, v_raw, gate, n_ctx)
+
+
+class SWADecode:
+    """One decode step of a sliding-window-only layer: the new token into the ring, attention over the
+    W most recent tokens (CSA attention with no selected entry)."""
+
+    def __init__(self, cache: SWACache, H, scale=None):
+        self.c, self.H = cache, H
+        B, d, dev = cache.B, cache.d, cache.device
+        self.scale = 1.0 / math.sqrt(d) if scale is None else scale
+        self.idx = torch.empty(B, 1, 0, dtype=torch.int32, device=dev)
+        self.out = torch.empty(B, 1, H, d, dtype=cache.dtype, device=dev)
+        self.lse = torch.empty(B, 1, H, dtype=torch.float32, device=dev)
+        self.ws = torch.empty(max(256, csa_attend_workspace(B, 1, H, d, 0, cache.W)), dtype=torch.uint8, device=dev)
+
+    def step(self, pos, q, k_new, v_new, gate_new):
+        c = self.c
+        swa_ring_write(k_new, v_new, gate_new, pos, 1, c.ring_k, c.ring_v, c.ring_gate)
+        csa_attend(q, self.scale, c.ck, c.cv, self.idx, c.ring_k, c.ring_v, c.W, pos, self.out, self.lse,
+                   workspace=self.ws)
+        return self.out, self.lse
+
+
+class InterleavedDecode:
+    """One decode step through a stack of attention layers of the kinds given (``interleave_kinds``),
+    each with its own cache: CSA layers append, index, select and attend; HCA layers append and attend
+    densely; the MTP layer attends over its window.  Per layer the step takes that layer's new token
+    (k, v, gate; for CSA also the index-key input), its queries (for CSA also the indexer queries and
+    head weights); the calls of all layers can be captured in one CUDA graph.  The layers' inputs are
+    independent here (no projections between layers): the timeline is the attention path of the stack."""
+
+    def __init__(self, kinds, caches, H, H_I, k, biases, scale=None):
+        assert len(kinds) == len(caches) == len(biases)
+        self.kinds, self.caches = list(kinds), list(caches)
+        self.steps = []
+        for kind, c, bias in zip(kinds, caches, biases):
+            if kind == "csa":
+                self.steps.append(CSADecode(c, H, H_I, k, bias, scale))
+            elif kind == "hca":
+                self.steps.append(HCADecode(c, H, bias, scale))
+            else:
+                self.steps.append(SWADecode(c, H, scale))
+
+    def step(self, pos, inputs):
+        """inputs[i]: dict of layer i's tensors -- q, k_new, v_new, gate_new, and for CSA layers
+        q_idx, w, kidx_new.  Returns the layers' (out, lse)."""
+        outs = []
+        for kind, st, x in zip(self.kinds, self.steps, inputs):
+            if kind == "csa":
+                o, l, _ = st.step(pos, x["q"], x["q_idx"], x["w"], x["k_new"], x["v_new"], x["gate_new"],
+                                  x["kidx_new"])
+            else:
+                o, l = st.step(pos, x["q"], x["k_new"], x["v_new"], x["gate_new"])
+            outs.append((o, l))
+        return outs
