@@ -299,14 +299,14 @@ class DecodeBench:
         self.out_h = torch.empty(B, 1, w.H, w.d, dtype=torch.bfloat16, device=device)
         self.lse_c = torch.empty(B, 1, w.H, dtype=torch.float32, device=device)
         self.lse_h = torch.empty(B, 1, w.H, dtype=torch.float32, device=device)
-        self.ws_topk = torch.empty(L.csa_index_topk_workspace(B, 1, self.Ncap_c, w.k), dtype=torch.uint8,
+        self.ws_topk = torch.zeros(L.csa_index_topk_workspace(B, 1, self.Ncap_c, w.k), dtype=torch.uint8,
                                    device=device)
         if w.index_q == "e2m1":          # FP4 indexer queries: quantised every step
             self.q4c = torch.empty(B, 1, w.H_I, w.d_I // 2, dtype=torch.uint8, device=device)
             self.q4s = torch.empty(B, 1, w.H_I, w.d_I // 32, dtype=torch.uint8, device=device)
-        self.ws_ca = torch.empty(max(256, L.csa_attend_workspace(B, 1, w.H, w.d, w.k, w.W)), dtype=torch.uint8,
+        self.ws_ca = torch.zeros(max(256, L.csa_attend_workspace(B, 1, w.H, w.d, w.k, w.W)), dtype=torch.uint8,
                                  device=device)
-        self.ws_ha = torch.empty(max(256, L.hca_attend_workspace(B, 1, w.H, w.d, self.Ncap_h, w.W, 0)),
+        self.ws_ha = torch.zeros(max(256, L.hca_attend_workspace(B, 1, w.H, w.d, self.Ncap_h, w.W, 0)),
                                  dtype=torch.uint8, device=device)
         self.scale = 1.0 / math.sqrt(w.d)
 

@@ -24,6 +24,12 @@
  *     library never frees, retains or allocates memory; scratch space is a caller-provided
  *     workspace sized by the matching *_workspace() function (256-byte aligned).  The one
  *     exception is hca_attend_noalloc, whose scratch is a fixed array inside the library.
+ *   - The workspaces of csa_index_topk, csa_index_topk_fp4, csa_attend and hca_attend carry
+ *     state between calls: zero-fill a workspace once after allocating it.  Every call leaves
+ *     its state area zero again (per-row histograms that the top-k clears after reading them,
+ *     per-row arrival counters that the row's last CTA resets), so no call spends a launch on
+ *     clearing it.  Zero it again after a call that recorded a device error, and (top-k only)
+ *     before a call with more query rows B*T than the calls it served so far.
  *   - Work is enqueued asynchronously on `stream` (a cudaStream_t; NULL = legacy default),
  *     in stream order.  Kernels are launched with programmatic dependent launch: a kernel may
  *     start while the previous kernel on the stream finishes, but it reads and writes global
@@ -131,7 +137,8 @@ csahca_status csa_index_key_quantize(const void* k_in, csahca_dtype in_dtype, in
  *   idx_out   : [B][T][k] int32
  *   scores_out: NULL, or [B][T][Ncap] float32 receiving the scores of the visible entries
  *               (entries >= n_vis are left untouched)
- *   workspace : csa_index_topk_workspace(B, T, Ncap, k) bytes
+ *   workspace : csa_index_topk_workspace(B, T, Ncap, k) bytes, zero-filled before first use
+ *               (see Conventions)
  * Supported: 1 <= H_I <= 64; 32 <= d_I <= 256, d_I % 32 == 0; H_I*d_I <= 4096; B*T <= 65535;
  * 1 <= k <= 65536 (k larger than the visible entries pads with -1).
  */
@@ -150,7 +157,7 @@ size_t csa_index_topk_workspace(int B, int T, int64_t Ncap, int k);
  *     I(t,s) = sum_{h < H_I} w[t][h] * max(0, qhat[t][h][:] . khat_s),  qhat = 2^(byte-127) * code,
  * exact up to the fp32 accumulation.  Keys are CSAHCA_E2M1_UE8M0.  Top-k, outputs and workspace
  * (csa_index_topk_workspace) as csa_index_topk.  Supported: d_I = 64, H_I in {16, 32, 64},
- * Ncap % 8 == 0, k_codes 32-byte, k_scale and q_codes 16-byte, q_scale 2-byte aligned; otherwise
+ * Ncap % 256 == 0, k_codes 32-byte, k_scale and q_codes 16-byte, q_scale 2-byte aligned; otherwise
  * CSAHCA_ERR_UNSUPPORTED and nothing is enqueued. */
 csahca_status csa_index_topk_fp4(const void* q_codes, const void* q_scale, const float* w,
                                  const void* k_codes, const void* k_scale, int B, int T, int H_I,
@@ -188,7 +195,8 @@ size_t csa_topk_workspace(int R, int64_t row_stride, int k);
  *   W       : window length, 0 <= W <= ring_cap (W <= ring_cap + chunk length for prefill)
  *   q_pos   : [B*T] int64 (device)
  *   dtype   : CSAHCA_F32 or CSAHCA_BF16 (q, caches, ring, chunk and out share it)
- *   workspace : csa_attend_workspace(B, T, H, d, k, W) bytes
+ *   workspace : csa_attend_workspace(B, T, H, d, k, W) bytes, zero-filled before first use
+ *               (see Conventions)
  * An empty key set (no selected entry, W = 0) gives out = 0 and lse = -inf.
  */
 csahca_status csa_attend(const void* q, int B, int T, int H, int d, float scale, const void* ck,
@@ -208,7 +216,8 @@ size_t csa_attend_workspace(int B, int T, int H, int d, int k, int W);
  *     lse = log sum_s exp(lse_s),  o = sum_s exp(lse_s - lse) o_s,
  * in the fixed order s = 0, 1, ... (deterministic).
  * Arguments as csa_attend; `m` is the HCA block size; `splits` = 0 picks the split count.
- * workspace : hca_attend_workspace(B, T, H, d, Ncap, W, splits) bytes.
+ * workspace : hca_attend_workspace(B, T, H, d, Ncap, W, splits) bytes, zero-filled before first
+ *             use (see Conventions).
  */
 csahca_status hca_attend(const void* q, int B, int T, int H, int d, float scale, const void* ck,
                          const void* cv, int64_t Ncap, int m, const void* ring_k,
@@ -225,9 +234,11 @@ size_t hca_attend_workspace(int B, int T, int H, int d, int64_t Ncap, int W, int
  * workspace: the split-K partial results live in one fixed device array of
  * hca_attend_noalloc_scratch_bytes() bytes (16 MiB) inside the library, which every GPU that
  * loads the library keeps until the process exits.  The split count is lowered until the
- * partials fit; if one split per query (B*T*H*(d+1)*4 bytes plus alignment) does not fit,
- * the call returns CSAHCA_ERR_WORKSPACE and enqueues nothing.  Nothing in the array needs to
- * start at zero: every call writes all partials it reads.  All calls on a device share the
+ * partials fit; if one split per query (B*T*H*(d+1)*4 bytes plus alignment, plus the 256 KiB
+ * of per-row arrival counters) does not fit, the call returns CSAHCA_ERR_WORKSPACE and
+ * enqueues nothing.  The array starts zeroed when the library loads, and every call leaves its
+ * counters zero again (after a call that recorded a device error, later results of this entry
+ * point are not guaranteed in that process).  All calls on a device share the
  * array, so calls that may overlap on the GPU (different streams without ordering) race and
  * must be serialised by the caller.  The first call on a device looks up the array's device
  * address (cudaGetSymbolAddress, with that device current); make that first call before any

@@ -110,7 +110,7 @@ def _ws(nbytes: int, device, workspace):
     if workspace is not None:
         assert workspace.numel() * workspace.element_size() >= nbytes
         return workspace, workspace.numel() * workspace.element_size()
-    return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device), max(int(nbytes), 256)
+    return torch.zeros(max(int(nbytes), 256), dtype=torch.uint8, device=device), max(int(nbytes), 256)
 
 
 def status_string(st: int) -> str:

@@ -258,7 +258,7 @@ SplitPlan plan_splits(int R, int64_t total_max, int splits_req) {
 }
 
 size_t attend_workspace_bytes(int R, int H, int d, const SplitPlan& sp) {
-    return align256((size_t)R * sp.S * H * d * 4) + align256((size_t)R * sp.S * H * 4);
+    return kRowCounterBytes + align256((size_t)R * sp.S * H * d * 4) + align256((size_t)R * sp.S * H * 4);
 }
 
 csahca_status attend_run(const AttendArgs& a, int splits_req, void* workspace, size_t ws_bytes,
@@ -267,15 +267,21 @@ csahca_status attend_run(const AttendArgs& a, int splits_req, void* workspace, s
     const SplitPlan sp = plan_splits(R, a.total_max, splits_req);
     if (!workspace || !aligned(workspace, 256) || ws_bytes < attend_workspace_bytes(R, a.H, a.d, sp))
         return CSAHCA_ERR_WORKSPACE;
-    float* o_part = static_cast<float*>(workspace);
-    float* lse_part = reinterpret_cast<float*>(static_cast<char*>(workspace) +
+    unsigned* row_cnt = static_cast<unsigned*>(workspace);
+    float* o_part = reinterpret_cast<float*>(static_cast<char*>(workspace) + kRowCounterBytes);
+    float* lse_part = reinterpret_cast<float*>(static_cast<char*>(workspace) + kRowCounterBytes +
                                                align256((size_t)R * sp.S * a.H * a.d * 4));
     unsigned* err = err_word();
     if (!err) return CSAHCA_ERR_CUDA;
     cudaError_t e;
     if (attend_tc_supported(a)) {
-        e = attend_tc_launch(a, sp.S, sp.kps, o_part, lse_part, err, st);
-    } else if (a.dtype == CSAHCA_F32) {
+        e = attend_tc_launch(a, sp.S, sp.kps, o_part, lse_part, row_cnt, err, st);
+        count_launch();
+        if (e != cudaSuccess) return CSAHCA_ERR_CUDA;
+        CSAHCA_CHECK_LAUNCH();
+        return CSAHCA_OK;
+    }
+    if (a.dtype == CSAHCA_F32) {
         e = dispatch_generic<float>(a, sp.S, sp.kps, o_part, lse_part, err, st);
     } else {
         e = dispatch_generic<__nv_bfloat16>(a, sp.S, sp.kps, o_part, lse_part, err, st);

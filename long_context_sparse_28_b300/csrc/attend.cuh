@@ -99,6 +99,9 @@ struct SplitPlan {
     int kps;   // keys per split (multiple of 128)
 };
 SplitPlan plan_splits(int R, int64_t total_max, int splits_req);
+// Workspace: per-row arrival counters (kRowCounterBytes, zero between calls: the tensor-core path's
+// last CTA of a row merges the row's partials and resets its counter), then the partials.
+constexpr size_t kRowCounterBytes = 65536 * 4;
 size_t attend_workspace_bytes(int R, int H, int d, const SplitPlan& sp);
 // Host-side argument checks and the split + merge launch sequence shared by the entry points.
 csahca_status attend_validate(const AttendArgs& a);
@@ -106,7 +109,10 @@ csahca_status attend_run(const AttendArgs& a, int splits_req, void* workspace, s
 
 // Tensor-core path (bf16, d = 128): availability and launch of the split kernel.
 bool attend_tc_supported(const AttendArgs& a);
-cudaError_t attend_tc_launch(const AttendArgs& a, int S, int kps, float* o_part, float* lse_part, unsigned* err,
+// The kernel also merges each row's partials into a.out / a.lse (the row's last CTA, counted in
+// row_cnt), so no merge launch follows it.
+cudaError_t attend_tc_launch(const AttendArgs& a, int S, int kps, float* o_part, float* lse_part, unsigned* row_cnt,
+                             unsigned* err,
                              cudaStream_t st);
 
 }  // namespace csahca

@@ -22,7 +22,9 @@
 // right after PV(i), so loads, both MMAs and the softmax of the next tile overlap.  With few
 // query rows each CTA takes one near-equal piece of one row's tiles (pieces sized from the rows'
 // actual lengths); otherwise CTAs are persistent over (row, key-split) items.  Partial results
-// (o normalised, lse) go to the split workspace and are merged by the shared merge kernel.
+// (o normalised, lse) go to the split workspace; each item then counts its arrival at its row
+// (an atomic on a per-row counter of the workspace), and the row's last item merges the row's
+// partials exactly and resets the counter, so no second launch is needed and nothing waits.
 #include "attend.cuh"
 #include "tc_ptx.cuh"
 
@@ -44,6 +46,7 @@ constexpr uint32_t kHalf = kKeys * 128;    // [128 rows][64 bf16] swizzled half 
 constexpr uint32_t kTile = 2 * kHalf;      // one K or V tile: 32 KB
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 constexpr int kSchedRows = 256;            // piece schedule for up to this many query rows
+constexpr int kMergeSlots = 16;            // partial slots merged per pass
 
 // Softmax / load threads: one warpgroup (128 threads, one per key row) per 16 heads; then the
 // MMA warp.
@@ -82,12 +85,16 @@ struct alignas(16) Misc {
     int my_empty_row;                // row's slots [my_slots_from, S) it marks empty, a row
     int my_slots_from;               // without tiles whose slots it marks empty (or -1), and
     int64_t my_p;                    // the query position of its row
+    int my_np;                       // pieces (= partial slots) of its row
+    int merge_now;                   // this CTA arrived last at its row: it merges the row
+    alignas(16) float mw[kMergeSlots * 64];   // the merge's per-(slot, head) log-sum-exps, then weights
 };
 static_assert(offsetof(Misc, mrun) % 16 == 0 && offsetof(Misc, mold) % 16 == 0 && offsetof(Misc, alpha) % 16 == 0,
               "float4 fields");
 
 struct ItemTiles {
     int r, b, nt_c, t0, nt, slot;
+    int expect;                      // partial slots of the row, written by as many items
     int64_t p;
     KeyList kl;
 };
@@ -142,6 +149,7 @@ __device__ __noinline__ void piece_schedule(const AttendArgs& a, int S, int nt_w
             ms.my_t0 = t0;
             ms.my_nt = (piece + 1) * nt / np - t0;
             ms.my_p = pq;
+            ms.my_np = np;
             if (piece == 0) ms.my_slots_from = np;
         }
         if (in && np == 0 && lane == c) ms.my_empty_row = lane;   // R <= gridDim.x
@@ -197,6 +205,7 @@ __device__ __noinline__ void piece_schedule(const AttendArgs& a, int S, int nt_w
             ms.my_t0 = t0;
             ms.my_nt = (piece + 1) * nt / np - t0;
             ms.my_p = a.q_pos[q];
+            ms.my_np = np;
             if (piece == 0) ms.my_slots_from = np;
         }
         if (q < R && np == 0 && q == c) ms.my_empty_row = q;   // R <= gridDim.x
@@ -256,10 +265,108 @@ __device__ __forceinline__ void load_tile(const AttendArgs& a, const Maps& maps,
     cp_async_arrive_noinc(bar);
 }
 
+// The row's last item merges the row's partial results: see arrive_and_merge in the kernel.
+// Out of line: it runs once per row and keeps its registers out of the tile loop's allocation.
+template <int H>
+__device__ __noinline__ void merge_row(int r, int ns, int S, const float* __restrict__ lse_part,
+                                       const float* __restrict__ o_part, __nv_bfloat16* __restrict__ out,
+                                       float* __restrict__ lse_out, Misc& ms, int tid) {
+    constexpr int kSoft = Thr<H>::kSoft;
+    const float* lrow = lse_part + (int64_t)r * S * H;
+    const float* orow = o_part + (int64_t)r * S * H * kD;
+    // Every slot [0, ns) holds a finite partial (zeros where it has no keys), so the loads of
+    // the partial outputs need no weights: kMergeSlots slots at a time, their lse into shared
+    // memory and their outputs into registers (units of 4 dims of one head, consecutive
+    // threads on consecutive dims, kMB slots per batch) are issued together; then one
+    // thread per head forms the maxima and sums (rescaled across passes), and the weighted
+    // sums follow.
+    constexpr int kUnits = H * (kD / 4) / kSoft;   // units per thread (4)
+    constexpr int kMB = H == 64 ? 2 : 4;           // slots per batch (registers)
+    float4 acc[kUnits];
+#pragma unroll
+    for (int u = 0; u < kUnits; ++u) acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+    float mx = -INFINITY, tot = 0.0f;              // per head (threads tid < H)
+    for (int s0 = 0; s0 < ns; s0 += kMergeSlots) {
+        const int nsl = min(kMergeSlots, ns - s0);
+        for (int i = tid; i < nsl * H; i += kSoft) ms.mw[i] = __ldcg(lrow + (int64_t)s0 * H + i);
+        for (int sl = 0; sl < nsl; sl += kMB) {
+            float4 v[kMB][kUnits];
+#pragma unroll
+            for (int j = 0; j < kMB; ++j)
+#pragma unroll
+                for (int u = 0; u < kUnits; ++u) {
+                    const int unit = tid + u * kSoft, hh = unit / (kD / 4), c4 = unit % (kD / 4);
+                    v[j][u] = sl + j < nsl ? __ldcg(reinterpret_cast<const float4*>(
+                                                       orow + ((int64_t)(s0 + sl + j) * H + hh) * kD) + c4)
+                                           : make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+            if (sl == 0) {
+                // this pass's maxima, sums and weights (the loads above are in flight)
+                named_barrier_sync(1, kSoft);
+                if (tid < H) {
+                    float m2 = mx;
+                    for (int q = 0; q < nsl; ++q) m2 = fmaxf(m2, ms.mw[q * H + tid]);
+                    const float rs = (m2 == -INFINITY) ? 0.0f : expf(mx - m2);   // 0 on the first pass
+                    tot *= rs;
+                    for (int q = 0; q < nsl; ++q) {
+                        const float ls = ms.mw[q * H + tid];
+                        const float e = ls == -INFINITY ? 0.0f : expf(ls - m2);
+                        tot += e;
+                        ms.mw[q * H + tid] = e;
+                    }
+                    mx = m2;
+                    ms.alpha[tid] = rs;
+                }
+                named_barrier_sync(1, kSoft);
+#pragma unroll
+                for (int u = 0; u < kUnits; ++u) {   // earlier passes' sums move to the new maxima
+                    const float rs = ms.alpha[(tid + u * kSoft) / (kD / 4)];
+                    acc[u].x *= rs;
+                    acc[u].y *= rs;
+                    acc[u].z *= rs;
+                    acc[u].w *= rs;
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < kMB; ++j)
+#pragma unroll
+                for (int u = 0; u < kUnits; ++u) {
+                    const float wgt = sl + j < nsl ? ms.mw[(sl + j) * H + (tid + u * kSoft) / (kD / 4)] : 0.0f;
+                    acc[u].x = fmaf(wgt, v[j][u].x, acc[u].x);
+                    acc[u].y = fmaf(wgt, v[j][u].y, acc[u].y);
+                    acc[u].z = fmaf(wgt, v[j][u].z, acc[u].z);
+                    acc[u].w = fmaf(wgt, v[j][u].w, acc[u].w);
+                }
+        }
+        named_barrier_sync(1, kSoft);              // ms.mw is reused by the next pass
+    }
+    if (tid < H) {
+        ms.linv[tid] = tot > 0.0f ? 1.0f / tot : 0.0f;
+        if (lse_out) lse_out[(int64_t)r * H + tid] = tot > 0.0f ? mx + logf(tot) : -INFINITY;
+    }
+    named_barrier_sync(1, kSoft);
+#pragma unroll
+    for (int u = 0; u < kUnits; ++u) {
+        const float li = ms.linv[(tid + u * kSoft) / (kD / 4)];
+        acc[u].x *= li;
+        acc[u].y *= li;
+        acc[u].z *= li;
+        acc[u].w *= li;
+    }
+    __nv_bfloat16* orow_out = out + (int64_t)r * H * kD;
+#pragma unroll
+    for (int u = 0; u < kUnits; ++u) {
+        const int unit = tid + u * kSoft;
+        reinterpret_cast<uint2*>(orow_out)[unit] =
+            make_uint2(pack_bf16x2(acc[u].x, acc[u].y), pack_bf16x2(acc[u].z, acc[u].w));
+    }
+}
+
 template <int H>
 __global__ void __launch_bounds__(Thr<H>::kThreads, 1)
     attend_tc_kernel(const __grid_constant__ AttendArgs a, int S, int kps, const __grid_constant__ Maps maps, int use_tma_c, int use_tma_w,
-                     int fixed_np, float* __restrict__ o_part, float* __restrict__ lse_part, unsigned* err) {
+                     int fixed_np, float* __restrict__ o_part, float* __restrict__ lse_part,
+                     unsigned* __restrict__ row_cnt, unsigned* err) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                          ~uintptr_t(1023));
@@ -308,6 +415,7 @@ __global__ void __launch_bounds__(Thr<H>::kThreads, 1)
                 ms.my_t0 = piece * nt / fixed_np;
                 ms.my_nt = (piece + 1) * nt / fixed_np - ms.my_t0;
                 ms.my_p = q < R ? a.q_pos[q] : 0;
+                ms.my_np = fixed_np;
             }
         } else {
             piece_schedule(a, S, nt_w, ms, lane);
@@ -331,11 +439,13 @@ __global__ void __launch_bounds__(Thr<H>::kThreads, 1)
             it.nt = ms.my_nt;
             it.slot = ms.my_piece;
             it.p = ms.my_p;
+            it.expect = ms.my_np;
         } else {
             if (cur >= items) return false;
             it.r = cur / S;
             it.slot = cur % S;
             it.t0 = it.slot * tps;
+            it.expect = S;
             cur += gridDim.x;
             it.p = a.q_pos[it.r];
         }
@@ -412,15 +522,31 @@ __global__ void __launch_bounds__(Thr<H>::kThreads, 1)
         const uint64_t pol_stream = l2_policy_evict_first();     // K/V rows are read once per step
         uint32_t g = 0;                                          // tiles processed so far by this CTA
 
-        if (pieces && tid < H) {    // partial slots no piece of this schedule writes: lse = -inf
-            if (ms.my_row >= 0)
-#pragma unroll 1
-                for (int sl = ms.my_slots_from; sl < S; ++sl)
-                    lse_part[((int64_t)ms.my_row * S + sl) * H + tid] = -INFINITY;
-            if (ms.my_empty_row >= 0)
-#pragma unroll 1
-                for (int sl = 0; sl < S; ++sl) lse_part[((int64_t)ms.my_empty_row * S + sl) * H + tid] = -INFINITY;
+        if (pieces && ms.my_empty_row >= 0) {      // a row without keys: o = 0, lse = -inf
+            const int64_t er = ms.my_empty_row;
+            uint4* orow = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out) + er * H * kD);
+            for (int i = tid; i < H * kD / 8; i += kSoft) orow[i] = make_uint4(0u, 0u, 0u, 0u);
+            if (a.lse && tid < H) a.lse[er * H + tid] = -INFINITY;
         }
+        // After an item's partial is written: count the arrival at its row (one release fence,
+        // cumulative over the barrier); the row's last item merges the row's partial results
+        // exactly, slots s = 0, 1, ... in that order (slots with lse = -inf hold no keys):
+        //     lse = log sum_s exp(lse_s),  o = sum_s exp(lse_s - lse) o_s,
+        // and resets the counter.  The partials of other CTAs are read through L2 (ld.global.cg).
+        auto arrive_and_merge = [&](const ItemTiles& itm) {
+            named_barrier_sync(1, kSoft);
+            if (tid == 0) {
+                __threadfence();
+                const bool last = atomicAdd(&row_cnt[itm.r], 1u) + 1u == (unsigned)itm.expect;
+                if (last) __threadfence();
+                ms.merge_now = last;
+            }
+            named_barrier_sync(1, kSoft);
+            if (!ms.merge_now) return;
+            merge_row<H>(itm.r, itm.expect, S, lse_part, o_part, static_cast<__nv_bfloat16*>(a.out), a.lse, ms,
+                         tid);
+            if (tid == 0) row_cnt[itm.r] = 0u;             // ready for the next call
+        };
         ItemTiles it;
         for (int cur = cur0; next_item(cur, it);) {
             const int r = it.r, b = it.b, nt_c = it.nt_c, t0 = it.t0, nt = it.nt;
@@ -429,10 +555,11 @@ __global__ void __launch_bounds__(Thr<H>::kThreads, 1)
             const int64_t obase = ((int64_t)r * S + it.slot) * H;
             const __nv_bfloat16* qr = static_cast<const __nv_bfloat16*>(a.q) + (int64_t)r * H * kD;
 
-            if (nt == 0) {
+            if (nt == 0) {                       // a slot without keys: o = 0 (finite), lse = -inf
 #pragma unroll 1
                 for (int i = tid; i < H * kD; i += kSoft) o_part[obase * kD + i] = 0.0f;
                 if (tid < H) lse_part[obase + tid] = -INFINITY;
+                arrive_and_merge(it);
                 continue;
             }
             if (tid < H) ms.mrun[tid] = -INFINITY;
@@ -633,10 +760,8 @@ __global__ void __launch_bounds__(Thr<H>::kThreads, 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&ms.pready);
             }
-            mbar_wait(&ms.odone, (g + (uint32_t)nt - 1) & 1, err);
-            fence_after_sync();
-            g += (uint32_t)nt;
-            // ---- row sums across the 128 keys, partial lse, normalised partial output
+            // ---- row sums across the 128 keys and the partial lse (while the last PV runs), then
+            // the normalised partial output
             float mine = 0.0f;
 #pragma unroll
             for (int h = 0; h < HG; ++h) {
@@ -655,6 +780,9 @@ __global__ void __launch_bounds__(Thr<H>::kThreads, 1)
                 lse_part[obase + tid] = any ? (m + log2f(l)) * 0.6931471805599453f : -INFINITY;
             }
             named_barrier_sync(1, kSoft);
+            mbar_wait(&ms.odone, (g + (uint32_t)nt - 1) & 1, err);
+            fence_after_sync();
+            g += (uint32_t)nt;
 #pragma unroll
             for (int c0 = 0; c0 < HG; c0 += 16) {
                 uint32_t rr[16];
@@ -667,7 +795,7 @@ __global__ void __launch_bounds__(Thr<H>::kThreads, 1)
                 }
             }
             fence_before_sync();
-            named_barrier_sync(1, kSoft);
+            arrive_and_merge(it);
         }
     }
     __syncwarp();
@@ -685,8 +813,8 @@ bool encode_rows(CUtensorMap* m, const void* base, int64_t rows) {
 }
 
 template <int H>
-cudaError_t launch_tc(const AttendArgs& a, int S, int kps, float* o_part, float* lse_part, unsigned* err,
-                      cudaStream_t st) {
+cudaError_t launch_tc(const AttendArgs& a, int S, int kps, float* o_part, float* lse_part, unsigned* row_cnt,
+                      unsigned* err, cudaStream_t st) {
     Maps maps;
     std::memset(&maps, 0, sizeof maps);
     int use_c = 0, use_w = 0;
@@ -718,21 +846,22 @@ cudaError_t launch_tc(const AttendArgs& a, int S, int kps, float* o_part, float*
         }
     }
     (void)launch_pdl(kern, dim3(grid), dim3(Thr<H>::kThreads), smem, st, a, S, kps, maps, use_c, use_w, fixed_np,
-                     o_part, lse_part, err);
+                     o_part, lse_part, row_cnt, err);
     return cudaGetLastError();
 }
 
 }  // namespace
 
 bool attend_tc_supported(const AttendArgs& a) {
-    return a.dtype == CSAHCA_BF16 && a.d == 128 && (a.H == 32 || a.H == 64) && a.scale > 0.0f;
+    return a.dtype == CSAHCA_BF16 && a.d == 128 && (a.H == 32 || a.H == 64) && a.scale > 0.0f &&
+           aligned(a.out, 16);
 }
 
-cudaError_t attend_tc_launch(const AttendArgs& a, int S, int kps, float* o_part, float* lse_part, unsigned* err,
-                             cudaStream_t st) {
+cudaError_t attend_tc_launch(const AttendArgs& a, int S, int kps, float* o_part, float* lse_part, unsigned* row_cnt,
+                             unsigned* err, cudaStream_t st) {
     switch (a.H) {
-        case 32: return launch_tc<32>(a, S, kps, o_part, lse_part, err, st);
-        case 64: return launch_tc<64>(a, S, kps, o_part, lse_part, err, st);
+        case 32: return launch_tc<32>(a, S, kps, o_part, lse_part, row_cnt, err, st);
+        case 64: return launch_tc<64>(a, S, kps, o_part, lse_part, row_cnt, err, st);
         default: return cudaErrorNotSupported;
     }
 }

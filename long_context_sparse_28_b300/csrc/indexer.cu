@@ -201,11 +201,12 @@ csahca_status csa_index_topk(const void* q_idx, csahca_dtype q_dtype, const floa
     const int R = B * T;
     if (!workspace || !aligned(workspace, 256) || ws_bytes < csa_index_topk_workspace(B, T, Ncap, k))
         return CSAHCA_ERR_WORKSPACE;
+    // workspace: the top-k's histograms (zero between calls: the top-k clears each row's after
+    // use) and bitmaps, then the scores
     char* ws = static_cast<char*>(workspace);
-    float* S = scores_out ? scores_out : reinterpret_cast<float*>(ws);
-    TopkWorkspace tw = topk_carve(ws + align256((size_t)R * Ncap * 4), R, Ncap);
+    TopkWorkspace tw = topk_carve(ws, R, Ncap);
+    float* S = scores_out ? scores_out : reinterpret_cast<float*>(ws + topk_workspace_bytes(R, Ncap));
     cudaStream_t st = (cudaStream_t)stream;
-    if (zero_words(tw.hist1, topk_zero_bytes(R) / 4, st) != cudaSuccess) return CSAHCA_ERR_CUDA;
     bool hist_done = false;
     const csahca_status e = index_scores_launch(q_idx, q_dtype, w, k_codes, k_scale, key_fmt, B, T, H_I, d_I, q_pos,
                                                 Ncap, m, S, tw.hist1, &hist_done, st);
@@ -228,12 +229,11 @@ csahca_status csa_index_topk_fp4(const void* q_codes, const void* q_scale, const
     if (!workspace || !aligned(workspace, 256) || ws_bytes < csa_index_topk_workspace(B, T, Ncap, k))
         return CSAHCA_ERR_WORKSPACE;
     char* ws = static_cast<char*>(workspace);
-    float* S = scores_out ? scores_out : reinterpret_cast<float*>(ws);
-    TopkWorkspace tw = topk_carve(ws + align256((size_t)R * Ncap * 4), R, Ncap);
+    TopkWorkspace tw = topk_carve(ws, R, Ncap);
+    float* S = scores_out ? scores_out : reinterpret_cast<float*>(ws + topk_workspace_bytes(R, Ncap));
     cudaStream_t st = (cudaStream_t)stream;
     unsigned* err = err_word();
     if (!err) return CSAHCA_ERR_CUDA;
-    if (zero_words(tw.hist1, topk_zero_bytes(R) / 4, st) != cudaSuccess) return CSAHCA_ERR_CUDA;
     const cudaError_t e = index_tc_q4_launch(q_codes, q_scale, w, k_codes, k_scale, B, T, H_I, q_pos, Ncap, m, S,
                                              tw.hist1, err, st);
     count_launch();

@@ -173,7 +173,7 @@ __device__ __forceinline__ void cluster_sum(cooperative_groups::cluster_group& c
 // Grid (P, rows), clusters of (P, 1, 1): the CTAs of a cluster share one row.
 __global__ void __launch_bounds__(kSelThreads, 1) topk_select_kernel(
     const float* __restrict__ scores, int64_t stride, const int64_t* __restrict__ n_vis_arr,
-    const int64_t* __restrict__ q_pos, int m, int64_t Ncap, int k, const uint32_t* __restrict__ hist1,
+    const int64_t* __restrict__ q_pos, int m, int64_t Ncap, int k, uint32_t* __restrict__ hist1,
     uint32_t* __restrict__ win, uint32_t* __restrict__ tie, int64_t words, int32_t* __restrict__ idx_out) {
     pdl_wait();
     pdl_trigger();
@@ -194,9 +194,12 @@ __global__ void __launch_bounds__(kSelThreads, 1) topk_select_kernel(
     const int tid = threadIdx.x, nthr = blockDim.x, lane = tid & 31, warp = tid >> 5, nw = nthr >> 5;
     const int64_t n = min(row_nvis(r, n_vis_arr, q_pos, m, Ncap), min(stride, words * 32));
     int32_t* out = idx_out + (int64_t)r * k;
+    uint32_t* hrow = hist1 + (int64_t)r * kBins12;
     if (n <= k) {                                   // every visible entry is selected, in order
-        if (p == 0)
+        if (p == 0) {
             for (int j = tid; j < k; j += nthr) out[j] = j < n ? j : -1;
+            for (int i = tid; i < kBins12; i += nthr) hrow[i] = 0u;   // the histogram, cleared for the next call
+        }
         return;                                     // (the whole cluster takes this branch)
     }
     const float* row = scores + (int64_t)r * stride;
@@ -323,6 +326,8 @@ __global__ void __launch_bounds__(kSelThreads, 1) topk_select_kernel(
             }
         }
         cl.sync();                                  // the others have finished reading this CTA's list
+        if (p == 0)                                 // every CTA has read the histogram: clear it
+            for (int i = tid; i < kBins12; i += nthr) hrow[i] = 0u;
         return;
     }
     // ---- the slow path: the boundary bin holds too many entries for the candidate lists; every
@@ -414,6 +419,8 @@ __global__ void __launch_bounds__(kSelThreads, 1) topk_select_kernel(
         ties_before += tq;
     }
     cl.sync();                                      // the last reads of another CTA's shared memory
+    if (p == 0)                                     // every CTA has read the histogram: clear it
+        for (int i = tid; i < kBins12; i += nthr) hrow[i] = 0u;
     const int my_ties = max(0, min(ties_needed - ties_before, tot_tie));
     const int take = max(0, min(my_ties - tie_before_local, ntie));
     int tot;
@@ -497,7 +504,7 @@ csahca_status topk_launch(const float* scores, int64_t stride, int R, const int6
     cfg.attrs = attr;
     cfg.numAttrs = 2;
     (void)cudaLaunchKernelEx(&cfg, topk_select_kernel, scores, stride, n_vis_arr, q_pos, m, Ncap, k,
-                             (const uint32_t*)tw.hist1, tw.win, tw.tie, tw.words, idx_out);
+                             tw.hist1, tw.win, tw.tie, tw.words, idx_out);
     count_launch();
     CSAHCA_CHECK_LAUNCH();
     return CSAHCA_OK;

@@ -96,8 +96,8 @@ class CSADecode:
         self.idx = torch.empty(B, 1, k, dtype=torch.int32, device=dev)
         self.out = torch.empty(B, 1, H, d, dtype=cache.dtype, device=dev)
         self.lse = torch.empty(B, 1, H, dtype=torch.float32, device=dev)
-        self.ws_topk = torch.empty(csa_index_topk_workspace(B, 1, cache.Ncap, k), dtype=torch.uint8, device=dev)
-        self.ws_att = torch.empty(max(256, csa_attend_workspace(B, 1, H, d, k, cache.W)), dtype=torch.uint8,
+        self.ws_topk = torch.zeros(csa_index_topk_workspace(B, 1, cache.Ncap, k), dtype=torch.uint8, device=dev)
+        self.ws_att = torch.zeros(max(256, csa_attend_workspace(B, 1, H, d, k, cache.W)), dtype=torch.uint8,
                                   device=dev)
 
     def step(self, pos, q, q_idx, w, k_new, v_new, gate_new, kidx_new, scores_out=None):
@@ -124,7 +124,7 @@ class HCADecode:
         self.scale = 1.0 / math.sqrt(d) if scale is None else scale
         self.out = torch.empty(B, 1, H, d, dtype=cache.dtype, device=dev)
         self.lse = torch.empty(B, 1, H, dtype=torch.float32, device=dev)
-        self.ws = torch.empty(max(256, hca_attend_workspace(B, 1, H, d, cache.Ncap, cache.W, splits)),
+        self.ws = torch.zeros(max(256, hca_attend_workspace(B, 1, H, d, cache.Ncap, cache.W, splits)),
                               dtype=torch.uint8, device=dev)
 
     def step(self, pos, q, k_new, v_new, gate_new):
@@ -157,9 +157,9 @@ class HybridPrefill:
         self.lse_c = torch.empty(B, T, H, dtype=torch.float32, device=dev)
         self.out_h = torch.empty(B, T, H, d, dtype=hca.dtype, device=dev)
         self.lse_h = torch.empty(B, T, H, dtype=torch.float32, device=dev)
-        self.ws_topk = torch.empty(csa_index_topk_workspace(B, T, csa.Ncap, k), dtype=torch.uint8, device=dev)
-        self.ws_ca = torch.empty(max(256, csa_attend_workspace(B, T, H, d, k, csa.W)), dtype=torch.uint8, device=dev)
-        self.ws_ha = torch.empty(max(256, hca_attend_workspace(B, T, H, d, hca.Ncap, hca.W, 0)), dtype=torch.uint8,
+        self.ws_topk = torch.zeros(csa_index_topk_workspace(B, T, csa.Ncap, k), dtype=torch.uint8, device=dev)
+        self.ws_ca = torch.zeros(max(256, csa_attend_workspace(B, T, H, d, k, csa.W)), dtype=torch.uint8, device=dev)
+        self.ws_ha = torch.zeros(max(256, hca_attend_workspace(B, T, H, d, hca.Ncap, hca.W, 0)), dtype=torch.uint8,
                                  device=dev)
 
     def set_position(self, pos0):
@@ -237,7 +237,7 @@ class SWADecode:
         self.idx = torch.empty(B, 1, 0, dtype=torch.int32, device=dev)
         self.out = torch.empty(B, 1, H, d, dtype=cache.dtype, device=dev)
         self.lse = torch.empty(B, 1, H, dtype=torch.float32, device=dev)
-        self.ws = torch.empty(max(256, csa_attend_workspace(B, 1, H, d, 0, cache.W)), dtype=torch.uint8, device=dev)
+        self.ws = torch.zeros(max(256, csa_attend_workspace(B, 1, H, d, 0, cache.W)), dtype=torch.uint8, device=dev)
 
     def step(self, pos, q, k_new, v_new, gate_new):
         c = self.c

@@ -71,4 +71,5 @@ def test_workspace_sizes_are_host_only(lib):
     assert n >= 32 * 262144 * 4 + 32 * 4096 * 4 + 2 * 32 * 8192 * 4
     lib.hca_attend_workspace.restype = ctypes.c_size_t
     lib.hca_attend_workspace.argtypes = [ctypes.c_int] * 4 + [ctypes.c_int64, ctypes.c_int, ctypes.c_int]
-    assert lib.hca_attend_workspace(4, 1, 64, 128, 8192, 128, 8) == 4 * 8 * 64 * 128 * 4 + 4 * 8 * 64 * 4
+    # per-row arrival counters (65536 x 4 B) + partial outputs + partial log-sum-exps
+    assert lib.hca_attend_workspace(4, 1, 64, 128, 8192, 128, 8) == 65536 * 4 + 4 * 8 * 64 * 128 * 4 + 4 * 8 * 64 * 4

@@ -501,3 +501,75 @@ def test_decode_step_is_deterministic():
     out1, idx1 = a["out"].clone(), a["idx"].clone()
     b = csa_decode_case(w, [])
     assert torch.equal(out1, b["out"]) and torch.equal(idx1, b["idx"])
+
+
+def test_attend_tensor_core_row_without_keys_gives_zero():
+    # bf16, H = 64: a row with no visible entry and no window (W = 0) is written by the CTA the
+    # schedule gives it (o = 0, lse = -inf); the other row is merged by its last CTA
+    B, H, d, m, Ncap = 2, 64, 128, 128, 8
+    ck, cv, _, _ = _rand_cache(B, Ncap, 1, d, "bf16", 52)
+    q = rnd((B, 1, H, d), torch.bfloat16, 53, d ** -0.5)
+    pos = np.array([5, 128 * 3 + 1])
+    out = torch.full((B, 1, H, d), 9.0, dtype=torch.bfloat16, device="cuda")
+    lse = torch.zeros(B, 1, H, device="cuda")
+    L.hca_attend(q, d ** -0.5, ck, cv, m, None, None, 0, dev_i64(pos), out, lse, splits=2)
+    torch.cuda.synchronize()
+    assert L.device_status() == 0
+    assert (npy(out[0]) == 0).all() and np.isneginf(npy(lse[0])).all()
+    o, ls = oracle.attend(npy(q[1, 0]), d ** -0.5, npy(ck[1]), npy(cv[1]), np.arange(3), None, None, [])
+    assert_close(out[1, 0], o, "bf16", "row with keys")
+    np.testing.assert_allclose(npy(lse[1, 0]), ls, rtol=1e-5, atol=1e-5)
+
+
+def test_workspace_state_is_cleared_by_every_call():
+    # the top-k's per-row histograms and the attention's per-row arrival counters live in the
+    # caller's workspace: after each call they are zero again, so calls on one workspace give the
+    # results of calls on fresh ones
+    B, T, Ncap, d_I, H_I, m, k = 3, 2, 1024, 64, 16, 4, 100
+    F = L.KEY_FMT["e2m1"]
+    R = B * T
+    ws = torch.zeros(L.csa_index_topk_workspace(B, T, Ncap, k), dtype=torch.uint8, device="cuda")
+    ins = []
+    for s in range(2):
+        kin = rnd((B, Ncap, d_I), torch.bfloat16, 70 + s)
+        codes, scales = L.key_storage(B, Ncap, d_I, F)
+        L.csa_index_key_quantize(kin, F, codes, scales)
+        q = rnd((B, T, H_I, d_I), torch.bfloat16, 72 + s, 0.125)
+        w = torch.rand(B, T, H_I, generator=torch.Generator().manual_seed(74 + s)).cuda()
+        pos = dev_i64([4 * Ncap - 1 - 37 * i for i in range(R)])
+        ins.append((q, w, codes, scales, pos))
+
+    def topk(i, wsp):
+        q, w, codes, scales, pos = ins[i]
+        idx = torch.empty(B, T, k, dtype=torch.int32, device="cuda")
+        L.csa_index_topk(q, w, codes, scales, F, pos, m, k, idx, workspace=wsp)
+        return idx
+
+    a1, b1, a2 = topk(0, ws), topk(1, ws), topk(0, ws)
+    torch.cuda.synchronize()
+    assert L.device_status() == 0
+    assert not ws[: R * 4096 * 4].any(), "histograms left behind"
+    fresh = torch.zeros_like(ws)
+    assert torch.equal(a1, a2) and torch.equal(b1, topk(1, fresh))
+    # attention: the same workspace for an HCA and a CSA call, twice
+    H, d, W, Nc = 64, 128, 128, 60
+    ck, cv, rk, rv = _rand_cache(B, Nc, W, d, "bf16", 80)
+    qa = rnd((B, 1, H, d), torch.bfloat16, 81, d ** -0.5)
+    pa = dev_i64([128 * 50 + 3, 128 * 7, 900])
+    sel = torch.arange(k, dtype=torch.int32, device="cuda").remainder(Nc).reshape(1, 1, k).repeat(B, 1, 1)
+    wsa = torch.zeros(max(L.hca_attend_workspace(B, 1, H, d, Nc, W), L.csa_attend_workspace(B, 1, H, d, k, W)),
+                      dtype=torch.uint8, device="cuda")
+
+    def att(wsp):
+        oh, lh = torch.empty_like(qa), torch.empty(B, 1, H, device="cuda")
+        oc, lc = torch.empty_like(qa), torch.empty(B, 1, H, device="cuda")
+        L.hca_attend(qa, d ** -0.5, ck, cv, 128, rk, rv, W, pa, oh, lh, workspace=wsp)
+        L.csa_attend(qa, d ** -0.5, ck, cv, sel, rk, rv, W, pa, oc, lc, workspace=wsp)
+        return oh, lh, oc, lc
+
+    r1, r2, r3 = att(wsa), att(wsa), att(torch.zeros_like(wsa))
+    torch.cuda.synchronize()
+    assert L.device_status() == 0
+    assert not wsa[: 65536 * 4].any(), "arrival counters left behind"
+    for x, y, z in zip(r1, r2, r3):
+        assert torch.equal(x, y) and torch.equal(x, z)
