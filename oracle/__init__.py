@@ -73,6 +73,8 @@ def _L():
             lib.oc_quant_e4m3_rowscale.argtypes = [P, I, I64, I, P, P]
             lib.oc_quant_e2m1_ue8m0.argtypes = [P, I, I64, I, P, P]
             lib.oc_dequant_keys.argtypes = [I, P, P, I64, I, P]
+            lib.oc_quant_kv_fp8.argtypes = [P, I64, I, I, P, P, P]
+            lib.oc_dequant_kv_fp8.argtypes = [P, P, P, I64, I, I, P]
             lib.oc_index_scores.argtypes = [P, I, P, I, I, I, P, I64, P, P]
             lib.oc_topk.argtypes = [P, I64, I, P, I, P]
             lib.oc_attend.argtypes = [P, I, I, I, D, P, P, I, P, I64, P, P, I, P, I64, P, P]
@@ -202,6 +204,30 @@ def dequant_keys(fmt: int, codes: np.ndarray, scales, d: int) -> np.ndarray:
     out = np.empty((rows, d), dtype=np.float64)
     sp = _p(np.ascontiguousarray(scales)) if scales is not None else None
     _L().oc_dequant_keys(fmt, _p(codes), sp, rows, d, _p(out))
+    return out
+
+
+def quant_kv_fp8(x: np.ndarray, d_keep: int):
+    """FP8 storage of compressed K/V rows (see ``oc_quant_kv_fp8``): x [rows, d] (any float dtype,
+    taken as fp64).  Returns (codes uint8 [rows, d - d_keep], scales uint8 [rows, (d - d_keep)/64],
+    keep uint16 BF16 bits [rows, d_keep])."""
+    x = np.ascontiguousarray(to_f64(x) if x.dtype == np.uint16 else x, dtype=np.float64)
+    rows, d = x.shape
+    assert (d - d_keep) % 64 == 0 and 0 <= d_keep <= d
+    codes = np.empty((rows, d - d_keep), dtype=np.uint8)
+    scales = np.empty((rows, (d - d_keep) // 64), dtype=np.uint8)
+    keep = np.zeros((rows, max(d_keep, 1)), dtype=np.uint16)
+    _L().oc_quant_kv_fp8(_p(x), rows, d, d_keep, _p(codes), _p(scales), _p(keep))
+    return codes, scales, keep[:, :d_keep]
+
+
+def dequant_kv_fp8(codes: np.ndarray, scales: np.ndarray, keep: np.ndarray, d: int) -> np.ndarray:
+    codes, scales = np.ascontiguousarray(codes), np.ascontiguousarray(scales)
+    rows = codes.shape[0]
+    d_keep = d - codes.shape[1]
+    kp = np.ascontiguousarray(keep if d_keep else np.zeros((rows, 1), dtype=np.uint16))
+    out = np.empty((rows, d), dtype=np.float64)
+    _L().oc_dequant_kv_fp8(_p(codes), _p(scales), _p(kp), rows, d, d_keep, _p(out))
     return out
 
 

@@ -251,6 +251,61 @@ void oc_dequant_keys(int fmt, const void* codes, const void* scales, int64_t row
     }
 }
 
+/* ------------------------------- f2: FP8 compressed K/V with BF16 RoPE dimensions */
+/*
+ * "Most KV entries are stored in FP8 and only the RoPE dimensions in BF16" (pogovet.com
+ * article, detail 5).  The pages fix neither the RoPE width, the FP8 variant nor the scale;
+ * the reading taken: a row of d values keeps its last d_keep values (the RoPE dims of a K row;
+ * none for a V row) in BF16, rounded to nearest even; every other value is OCP FP8 E4M3 with
+ * one UE8M0 scale 2^e per 64 consecutive values, e = the smallest integer with
+ * amax <= 448 * 2^e (e = 0 for an all-zero block, clamped to [-127, 127]), and
+ * code = RNE_e4m3(x * 2^-e) -- exact scaling, so code * 2^e is the dequantised value and is
+ * exactly a BF16 number.  The values are first rounded to float32, the precision the device
+ * pools in, so both sides take every rounding decision on the same input.
+ * x: [rows][d] fp64;  codes: [rows][d - d_keep];  scales: [rows][(d - d_keep) / 64] biased
+ * bytes e + 127;  keep: [rows][d_keep] BF16 bits (unused when d_keep = 0).
+ */
+static int e4m3_block_exponent(double amax) {
+    if (!(amax > 0.0)) return 0;
+    int ex;
+    frexp(amax, &ex);                                     /* amax in [2^(ex-1), 2^ex) */
+    int e = ex - 10;                                      /* 448 * 2^(ex-10) < 2^(ex-1) */
+    while (ldexp(448.0, e) < amax) ++e;
+    if (e < -127) e = -127;
+    if (e > 127) e = 127;
+    return e;
+}
+
+void oc_quant_kv_fp8(const double* x, int64_t rows, int d, int d_keep, uint8_t* codes, uint8_t* scales,
+                     uint16_t* keep) {
+    const int dq = d - d_keep, nb = dq / 64;
+    for (int64_t r = 0; r < rows; ++r) {
+        for (int b = 0; b < nb; ++b) {
+            double amax = 0.0;
+            for (int c = 0; c < 64; ++c) {
+                double v = fabs((double)(float)x[r * d + b * 64 + c]);
+                if (v > amax) amax = v;
+            }
+            int e = e4m3_block_exponent(amax);
+            scales[r * nb + b] = (uint8_t)(e + 127);
+            for (int c = 0; c < 64; ++c)
+                codes[r * dq + b * 64 + c] = oc_e4m3_encode(ldexp((double)(float)x[r * d + b * 64 + c], -e));
+        }
+        for (int c = 0; c < d_keep; ++c) keep[r * d_keep + c] = oc_double_to_bf16((double)(float)x[r * d + dq + c]);
+    }
+}
+
+/* The dequantised rows, fp64: [rows][d]. */
+void oc_dequant_kv_fp8(const uint8_t* codes, const uint8_t* scales, const uint16_t* keep, int64_t rows, int d,
+                       int d_keep, double* out) {
+    const int dq = d - d_keep, nb = dq / 64;
+    for (int64_t r = 0; r < rows; ++r) {
+        for (int c = 0; c < dq; ++c)
+            out[r * d + c] = ldexp(oc_e4m3_decode(codes[r * dq + c]), (int)scales[r * nb + c / 64] - 127);
+        for (int c = 0; c < d_keep; ++c) out[r * d + dq + c] = bf16_bits_to_double(keep[r * d_keep + c]);
+    }
+}
+
 /* ------------------------------------------------------- a5: indexer scores */
 /*
  * Lightning indexer score: I(t,s) = sum_h w[t,h] * max(0, q[t,h,:] . khat[s,:]).

@@ -20,10 +20,12 @@ from __future__ import annotations
 
 import numpy as np
 
-from . import (BF16, F32, attend, dequant_keys, fp4_query, index_scores, pool, quantize_keys,
-               round_to, topk)
+from . import (BF16, F32, attend, dequant_keys, dequant_kv_fp8, fp4_query, index_scores, pool, quant_kv_fp8,
+               quantize_keys, round_to, topk)
 
-__all__ = ["n_visible", "window_positions", "compress", "csa_queries", "hca_queries"]
+__all__ = ["n_visible", "window_positions", "compress", "compress_kv_fp8", "csa_queries", "hca_queries"]
+
+D_ROPE = 64   # RoPE dimensions of a K row kept in BF16 under FP8 storage (a reading: the pages give no width)
 
 
 def n_visible(pos, m: int, n_entries=None, strict: bool = False):
@@ -45,6 +47,20 @@ def compress(raw_k, raw_v, gate, bias, m: int, store_dtype: int, n_blocks=None):
     pk, _ = pool(raw_k, gate, bias, m, n_blocks)
     pv, _ = pool(raw_v, gate, bias, m, n_blocks)
     return round_to(pk, store_dtype), round_to(pv, store_dtype)
+
+
+def compress_kv_fp8(raw_k, raw_v, gate, bias, m: int, n_blocks=None, d_rope: int = D_ROPE):
+    """Pool like ``compress``, then store the entries in FP8 with the RoPE dims of K in BF16
+    (pogovet.com article, detail 5; ``oc_quant_kv_fp8``).  Returns a dict with the K planes (codes,
+    scales, rope), the V planes (codes, scales) and the dequantised caches ck, cv (fp64 [N, d]),
+    which attention reads."""
+    pk, _ = pool(raw_k, gate, bias, m, n_blocks)
+    pv, _ = pool(raw_v, gate, bias, m, n_blocks)
+    d = pk.shape[1]
+    kc, ks, kr = quant_kv_fp8(pk, d_rope)
+    vc, vs, _ = quant_kv_fp8(pv, 0)
+    return dict(k_codes=kc, k_scales=ks, k_rope=kr, v_codes=vc, v_scales=vs,
+                ck=dequant_kv_fp8(kc, ks, kr, d), cv=dequant_kv_fp8(vc, vs, np.zeros((len(vc), 0), np.uint16), d))
 
 
 def _window_rows(pos: int, W: int, raw_pos0: int):
