@@ -185,7 +185,9 @@ def algorithmic_bytes(w, lens_csa_nvis, lens_hca_nvis, layers="both"):
     queries/outputs -- of the layers the step runs.  Returns dict of per-part bytes."""
     d, H, B = w.d, w.H, w.B
     key_row = {"f32": 4 * w.d_I, "bf16": 2 * w.d_I, "e4m3": w.d_I + 4, "e2m1": w.d_I // 2 + w.d_I // 32}[w.key_fmt]
-    kv_row = 2 * d * 2                                   # one K row + one V row, bf16
+    # one K row + one V row: bf16, or FP8 (K: 64 codes + a scale byte + 64 bf16 RoPE dims; V: 128
+    # codes + 2 scale bytes; the rows' zero padding is not counted)
+    kv_row = 2 * d * 2 if w.kv_cache == "bf16" else (64 + 1 + 128) + (128 + 2)
     csa = layers in ("both", "csa", "index")
     hca = layers in ("both", "hca")
     parts = {
@@ -271,12 +273,13 @@ class DecodeBench:
         self.cb = wl.layer_bias(w, "csa", w.m_csa, device)
         self.hb = wl.layer_bias(w, "hca", w.m_hca, device)
         if layers in ("both", "csa"):
-            self.csa = CSACache(B, self.Ncap_c, w.d, w.W, w.d_I, fmt, torch.bfloat16, device, m=w.m_csa)
+            self.csa = CSACache(B, self.Ncap_c, w.d, w.W, w.d_I, fmt, torch.bfloat16, device, m=w.m_csa,
+                                kv_fp8=w.kv_cache == "fp8")
         elif layers == "index":            # index keys only (no compressed K/V)
             codes, scale = L.key_storage(B, self.Ncap_c, w.d_I, fmt, device)
             self.csa = types.SimpleNamespace(k_codes=codes.zero_(), k_scale=scale.zero_(), key_fmt=fmt, m=w.m_csa)
         if layers in ("both", "hca"):
-            self.hca = HCACache(B, self.Ncap_h, w.d, w.W, torch.bfloat16, device, m=w.m_hca)
+            self.hca = HCACache(B, self.Ncap_h, w.d, w.W, torch.bfloat16, device, m=w.m_hca, kv_fp8=w.kv_cache == "fp8")
         for b, Lb in enumerate(self.lens):
             if layers in ("both", "csa"):
                 k, v, g = wl.raw_tokens(w, "csa", b, Lb - 1, device)
@@ -399,6 +402,14 @@ def load_traffic(kernel: str):
     return None
 
 
+def _oracle_caches(oracle, K, V, G, bias, m, kv_cache):
+    """The oracle's compressed caches: bf16, or FP8 (dequantised, fp64)."""
+    if kv_cache == "fp8":
+        c = oracle.compress_kv_fp8(K, V, G, bias, m)
+        return c["ck"], c["cv"]
+    return oracle.compress(K, V, G, bias, m, oracle.BF16)
+
+
 def cpu_baseline_decode(w, seqs: int, device, layers="both"):
     """The oracle (as it stands) on `seqs` sequences of the workload: one decode query per
     sequence through the step's layers.  Cache construction is setup and not timed."""
@@ -415,14 +426,14 @@ def cpu_baseline_decode(w, seqs: int, device, layers="both"):
             kin = wl.index_key_inputs(w, "csa", b, Lb // w.m_csa + 1, device)
             K, V, G, KIN = (wl.to_numpy(x) for x in (k, v, g, kin))
             cb = wl.to_numpy(wl.layer_bias(w, "csa", w.m_csa, device))
-            ck, cv = oracle.compress(K, V, G, cb, w.m_csa, oracle.BF16)
+            ck, cv = _oracle_caches(oracle, K, V, G, cb, w.m_csa, w.kv_cache)
             codes, sc = oracle.quantize_keys(KIN[: Lb // w.m_csa], fmt)
             del k, v, g, kin
         if layers in ("both", "hca"):
             hk, hv, hg = wl.raw_tokens(w, "hca", b, Lb, device)
             HK, HV, HG = (wl.to_numpy(x) for x in (hk, hv, hg))
             hb = wl.to_numpy(wl.layer_bias(w, "hca", w.m_hca, device))
-            hck, hcv = oracle.compress(HK, HV, HG, hb, w.m_hca, oracle.BF16)
+            hck, hcv = _oracle_caches(oracle, HK, HV, HG, hb, w.m_hca, w.kv_cache)
             del hk, hv, hg
         q = wl.to_numpy(wl.queries(w, "csa", b, 1, device))
         qh = wl.to_numpy(wl.queries(w, "hca", b, 1, device))
@@ -563,7 +574,8 @@ def run_ours(args, dist):
     key_desc = {"e2m1": "e2m1+ue8m0/32", "e4m3": "e4m3+f32 row scale", "bf16": "bf16", "f32": "f32"}[w.key_fmt]
     cfg = {"workload": w.name, "B": w.B,
            "L": f"U[{w.L_range[0]},{w.L_range[1]}] seeded" if w.L_range else w.L[0] if len(set(w.L)) == 1 else list(w.L),
-           "H": w.H, "d": w.d, "layers": layers}
+           "H": w.H, "d": w.d, "layers": layers,
+           "kv_cache": "bf16" if w.kv_cache == "bf16" else "e4m3+ue8m0/64, K RoPE dims 64..127 bf16"}
     if layers in ("both", "csa", "index"):
         cfg["csa"] = {"m": w.m_csa, "k": w.k, "W": w.W, "H_I": w.H_I, "d_I": w.d_I, "index_keys": key_desc,
                       "index_queries": "e2m1+ue8m0/32" if w.index_q == "e2m1" else "bf16"}

@@ -78,11 +78,29 @@ typedef enum {
     CSAHCA_E4M3_ROWSCALE = 2,/* index keys: OCP FP8 E4M3 codes [rows][d_I] (uint8) plus one
                                 float32 scale per row, s = amax/448 (1 for a zero row);
                                 key = s * code                                           */
-    CSAHCA_E2M1_UE8M0 = 3    /* index keys: OCP MX FP4 E2M1 codes, two per byte, the even
+    CSAHCA_E2M1_UE8M0 = 3,   /* index keys: OCP MX FP4 E2M1 codes, two per byte, the even
                                 element in the low nibble: [rows][d_I/2] (uint8), plus one
                                 UE8M0 scale byte (2^(byte-127)) per 32 values:
                                 [rows][d_I/32] (uint8); key = 2^(byte-127) * code        */
+    CSAHCA_KV_FP8 = 4        /* kv_dtype of pooling, appends and attention: compressed K/V
+                                in FP8 with the RoPE dims of K in BF16 (layout below); raw
+                                tokens, ring, queries and outputs stay bfloat16          */
 } csahca_dtype;
+
+/* Compressed K/V in FP8 (pogovet.com article, detail 5: most KV entries are stored in FP8, only
+ * the RoPE dimensions in BF16).  d = 128.  The pages fix neither the RoPE width nor the scale;
+ * the layout takes the last 64 dims of a K row as its RoPE dims and one power-of-two scale per
+ * 64 FP8 values:
+ *   ck: [B][Ncap][208] bytes per K row -- bytes 0..63 the E4M3 codes of dims 0..63, byte 64
+ *       their scale byte, bytes 65..79 zero, bytes 80..207 dims 64..127 as bfloat16;
+ *   cv: [B][Ncap][144] bytes per V row -- bytes 0..127 the E4M3 codes of dims 0..127, bytes
+ *       128 / 129 the scale bytes of dims 0..63 / 64..127, bytes 130..143 zero.
+ * A block of 64 pooled float32 values with largest magnitude amax gets e = the smallest integer
+ * with amax <= 448 * 2^e (0 for an all-zero block; clamped to [-127, 127]), the byte e + 127,
+ * and codes RNE_e4m3(x * 2^-e); a value reads back as code * 2^e (exactly a bfloat16 number).
+ * The bfloat16 dims are the pooled values rounded to nearest even. */
+#define CSAHCA_KV_FP8_K_ROW 208
+#define CSAHCA_KV_FP8_V_ROW 144
 
 /* ------------------------------------------------------------------ a1 / a2: pooling
  * Softmax-gated pooling (pogovet.com article, detail 4; honbul.tistory.com/221 "CSA" and
@@ -99,7 +117,9 @@ typedef enum {
  *   ck, cv       : [B][Ncap][d] kv_dtype; every block lying entirely inside
  *                  [raw_pos0[b], raw_pos0[b]+n_raw[b]) is written at entry j; blocks with
  *                  j >= Ncap are skipped and flag CSAHCA_ERR_BOUNDS on the device.
- *   kv_dtype     : CSAHCA_F32 or CSAHCA_BF16.  d: 1..512, d % 8 == 0.
+ *   kv_dtype     : CSAHCA_F32 or CSAHCA_BF16.  d: 1..512, d % 8 == 0.  Or CSAHCA_KV_FP8: raw
+ *                  tokens bfloat16, ck/cv in the FP8 layout above (the pooled float32 values
+ *                  quantised once), d = 128.  With m = 1 this quantises given rows.
  */
 csahca_status csa_compress(const void* k_raw, const void* v_raw, const float* gate,
                            int64_t raw_stride, const int64_t* raw_pos0, const int64_t* n_raw,
@@ -194,7 +214,9 @@ size_t csa_topk_workspace(int R, int64_t row_stride, int k);
  *             chunk_pos0[b] (int64, device); window tokens >= chunk_pos0[b] come from here
  *   W       : window length, 0 <= W <= ring_cap (W <= ring_cap + chunk length for prefill)
  *   q_pos   : [B*T] int64 (device)
- *   dtype   : CSAHCA_F32 or CSAHCA_BF16 (q, caches, ring, chunk and out share it)
+ *   dtype   : CSAHCA_F32 or CSAHCA_BF16 (q, caches, ring, chunk and out share it), or
+ *             CSAHCA_KV_FP8 (ck/cv in the FP8 layout above; q, ring, chunk and out bfloat16;
+ *             d = 128, H in {32, 64}, else CSAHCA_ERR_UNSUPPORTED)
  *   workspace : csa_attend_workspace(B, T, H, d, k, W) bytes, zero-filled before first use
  *               (see Conventions)
  * An empty key set (no selected entry, W = 0) gives out = 0 and lse = -inf.
@@ -261,7 +283,8 @@ size_t hca_attend_noalloc_scratch_bytes(void);
  * index; for CSA the index key of each completed block (kidx_new row r = the r-th block
  * completed in this call: [B][kidx_rows][d_I], kidx_rows = n_new/m + 1) is quantised into
  * k_codes/k_scale (key_fmt) at the same entry index.
- *   k_new, v_new : [B][n_new][d] kv_dtype;  gate_new: [B][n_new] float32
+ *   k_new, v_new : [B][n_new][d] kv_dtype (bfloat16 for CSAHCA_KV_FP8, whose ck/cv take the
+ *                  FP8 layout above while the ring stays bfloat16);  gate_new: [B][n_new] float32
  *   ring_k, ring_v : [B][ring_cap][d];  ring_gate: [B][ring_cap] float32
  * Pooling reads the ring before the new tokens are written to it.
  */

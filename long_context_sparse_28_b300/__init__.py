@@ -19,6 +19,8 @@ LIB_PATH = os.path.join(_HERE, "libcsahca.so")
 
 F32, BF16, E4M3_ROWSCALE, E2M1_UE8M0 = 0, 1, 2, 3
 KEY_FMT = {"f32": F32, "bf16": BF16, "e4m3": E4M3_ROWSCALE, "e2m1": E2M1_UE8M0}
+# compressed K/V in FP8 with the RoPE dims of K in bf16: caches are uint8 tensors of these row sizes
+KV_FP8, KV_FP8_K_ROW, KV_FP8_V_ROW = 4, 208, 144
 
 # every C entry point and its ctypes signature
 _P, _I64, _I, _F, _SZ = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
@@ -101,6 +103,11 @@ def _dt(t) -> int:
     raise TypeError(f"unsupported dtype {t.dtype}")
 
 
+def _kv_dt(x, ck) -> int:
+    """kv_dtype of a pooling / append / attention call: FP8 caches (uint8 rows), else x's dtype."""
+    return KV_FP8 if ck.dtype == torch.uint8 else _dt(x)
+
+
 def _check(st: int, name: str):
     if st != 0:
         raise CsaHcaError(f"{name}: {library().csahca_status_string(st).decode()} (status {st})")
@@ -154,7 +161,7 @@ def _compress(name, k_raw, v_raw, gate, raw_pos0, n_raw, slot_bias, m, ck, cv, s
     B, stride, d = k_raw.shape
     fn = getattr(library(), name)
     _check(fn(_p(k_raw), _p(v_raw), _p(gate), stride, _p(raw_pos0), _p(n_raw), _p(slot_bias), int(m), B, d,
-              _dt(k_raw), _p(ck), _p(cv), ck.shape[1], _stream(stream)), name)
+              _kv_dt(k_raw, ck), _p(ck), _p(cv), ck.shape[1], _stream(stream)), name)
 
 
 def csa_compress(k_raw, v_raw, gate, raw_pos0, n_raw, slot_bias, m, ck, cv, stream=None):
@@ -248,7 +255,7 @@ def csa_attend(q, scale, ck, cv, idx, ring_k, ring_v, W, q_pos, out, lse=None, c
     ck_, cv_, cp_, cs_ = _chunk_args(chunk_k, chunk_v, chunk_pos0)
     ws, nb = _ws(csa_attend_workspace(B, T, H, d, k, W), q.device, workspace)
     _check(library().csa_attend(_p(q), B, T, H, d, float(scale), _p(ck), _p(cv), ck.shape[1], _p(idx), k, _p(ring_k),
-                           _p(ring_v), ring_cap, int(W), _p(ck_), _p(cv_), _p(cp_), cs_, _p(q_pos), _dt(q), _p(out),
+                           _p(ring_v), ring_cap, int(W), _p(ck_), _p(cv_), _p(cp_), cs_, _p(q_pos), _kv_dt(q, ck), _p(out),
                            _p(lse), _p(ws), nb, _stream(stream)), "csa_attend")
 
 
@@ -261,7 +268,7 @@ def hca_attend(q, scale, ck, cv, m, ring_k, ring_v, W, q_pos, out, lse=None, chu
     ws, nb = _ws(hca_attend_workspace(B, T, H, d, ck.shape[1], W, splits), q.device, workspace)
     _check(library().hca_attend(_p(q), B, T, H, d, float(scale), _p(ck), _p(cv), ck.shape[1], int(m), _p(ring_k),
                            _p(ring_v), ring_cap, int(W), _p(ck_), _p(cv_), _p(cp_), cs_, _p(q_pos), int(splits),
-                           _dt(q), _p(out), _p(lse), _p(ws), nb, _stream(stream)), "hca_attend")
+                           _kv_dt(q, ck), _p(out), _p(lse), _p(ws), nb, _stream(stream)), "hca_attend")
 
 
 def hca_attend_noalloc_scratch_bytes() -> int:
@@ -278,7 +285,7 @@ def hca_attend_noalloc(q, scale, ck, cv, m, ring_k, ring_v, W, q_pos, out, lse=N
     ck_, cv_, cp_, cs_ = _chunk_args(chunk_k, chunk_v, chunk_pos0)
     _check(library().hca_attend_noalloc(_p(q), B, T, H, d, float(scale), _p(ck), _p(cv), ck.shape[1], int(m),
                                         _p(ring_k), _p(ring_v), ring_cap, int(W), _p(ck_), _p(cv_), _p(cp_), cs_,
-                                        _p(q_pos), int(splits), _dt(q), _p(out), _p(lse), _stream(stream)),
+                                        _p(q_pos), int(splits), _kv_dt(q, ck), _p(out), _p(lse), _stream(stream)),
            "hca_attend_noalloc")
 
 
@@ -289,14 +296,14 @@ def csa_cache_append(k_new, v_new, gate_new, kidx_new, pos, slot_bias, m, ring_k
     d_I = kidx_new.shape[-1]
     assert kidx_new.shape[1] == n_new // m + 1
     _check(library().csa_cache_append(_p(k_new), _p(v_new), _p(gate_new), _p(kidx_new), _dt(kidx_new), _p(pos), B, n_new,
-                                 d, _dt(k_new), _p(slot_bias), int(m), _p(ring_k), _p(ring_v), _p(ring_gate),
+                                 d, _kv_dt(k_new, ck), _p(slot_bias), int(m), _p(ring_k), _p(ring_v), _p(ring_gate),
                                  ring_k.shape[1], _p(ck), _p(cv), ck.shape[1], _p(k_codes), _p(k_scale),
                                  int(key_fmt), d_I, _stream(stream)), "csa_cache_append")
 
 
 def hca_cache_append(k_new, v_new, gate_new, pos, slot_bias, m, ring_k, ring_v, ring_gate, ck, cv, stream=None):
     B, n_new, d = k_new.shape
-    _check(library().hca_cache_append(_p(k_new), _p(v_new), _p(gate_new), _p(pos), B, n_new, d, _dt(k_new),
+    _check(library().hca_cache_append(_p(k_new), _p(v_new), _p(gate_new), _p(pos), B, n_new, d, _kv_dt(k_new, ck),
                                  _p(slot_bias), int(m), _p(ring_k), _p(ring_v), _p(ring_gate), ring_k.shape[1],
                                  _p(ck), _p(cv), ck.shape[1], _stream(stream)), "hca_cache_append")
 

@@ -302,7 +302,7 @@ csahca_status attend_run(const AttendArgs& a, int splits_req, void* workspace, s
 
 csahca_status attend_validate(const AttendArgs& a) {
     CSAHCA_REQUIRE(a.q && a.ck && a.cv && a.q_pos && a.out);
-    CSAHCA_REQUIRE(a.dtype == CSAHCA_F32 || a.dtype == CSAHCA_BF16);
+    CSAHCA_REQUIRE(a.dtype == CSAHCA_F32 || a.dtype == CSAHCA_BF16 || a.dtype == CSAHCA_KV_FP8);
     CSAHCA_REQUIRE(a.B >= 1 && a.T >= 1 && (int64_t)a.B * a.T <= 65535 && a.H >= 1 && a.d >= 8);
     CSAHCA_REQUIRE(a.d % 8 == 0 && a.Ncap >= 1 && a.W >= 0);
     if (a.W > 0) CSAHCA_REQUIRE(a.ring_k && a.ring_v && a.ring_cap >= 1);
@@ -315,6 +315,7 @@ csahca_status attend_validate(const AttendArgs& a) {
     if (a.ring_k) CSAHCA_REQUIRE(aligned(a.ring_k, al) && aligned(a.ring_v, al));
     if (a.chunk_k) CSAHCA_REQUIRE(aligned(a.chunk_k, al) && aligned(a.chunk_v, al));
     if (attend_tc_supported(a)) return CSAHCA_OK;
+    if (a.dtype == CSAHCA_KV_FP8) return CSAHCA_ERR_UNSUPPORTED;      // FP8 caches: tensor-core path only
     if (!(a.d == 64 || a.d == 128) || a.H > 64) return CSAHCA_ERR_UNSUPPORTED;
     return CSAHCA_OK;
 }

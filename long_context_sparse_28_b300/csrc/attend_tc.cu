@@ -26,6 +26,7 @@
 // (an atomic on a per-row counter of the workspace), and the row's last item merges the row's
 // partials exactly and resets the counter, so no second launch is needed and nothing waits.
 #include "attend.cuh"
+#include "quant.cuh"
 #include "tc_ptx.cuh"
 
 #include "tmap.cuh"
@@ -50,11 +51,12 @@ constexpr int kMergeSlots = 16;            // partial slots merged per pass
 
 // Softmax / load threads: one warpgroup (128 threads, one per key row) per 16 heads; then the
 // MMA warp.
-template <int H>
+template <int H, bool F8 = false>
 struct Thr {
     static_assert(H % kHG == 0, "heads in groups of 16");
     static constexpr int kSoft = (H / kHG) * kKeys;
-    static constexpr int kThreads = kSoft + 32;
+    static constexpr int kConv = F8 ? 64 : 0;       // FP8 caches: converter threads, two tile rows each
+    static constexpr int kThreads = kSoft + 32 + kConv;
 };
 
 template <int H>
@@ -72,6 +74,7 @@ struct Smem {
 
 struct alignas(16) Misc {
     uint64_t kfull[2], vfull[2], sdone[2], odone, pready;
+    uint64_t k8full[2], v8full[2];   // FP8 caches: a tile's codes have landed (before conversion)
     uint32_t tmem_base;
     int flag[2];                     // per tile (ring of 2): some running maximum moved
     alignas(16) float red[16][32];
@@ -101,6 +104,7 @@ struct ItemTiles {
 
 struct Maps {
     CUtensorMap ck, cv, rk, rv;
+    CUtensorMap k8, kr, v8, vs;      // FP8 caches: K codes + scale, K RoPE dims (bf16), V codes, V scales
 };
 
 // Piece schedule, computed by one warp (no more query rows than CTAs, S >= 2 partial slots per
@@ -265,6 +269,124 @@ __device__ __forceinline__ void load_tile(const AttendArgs& a, const Maps& maps,
     cp_async_arrive_noinc(bar);
 }
 
+// FP8 caches (CSAHCA_KV_FP8).  A compressed K tile lands as 128 rows of 128 bytes (the row's 64
+// codes, its scale byte and the bytes after them) in the slot's first half, dense, and its RoPE
+// dims (bf16) in the second half with the 128-byte swizzle of a bf16 tile; a V tile's codes land
+// as 128 dense rows of 128 bytes in the slot's second half and its scale bytes as rows of 16 bytes
+// in a side buffer.  A converter thread then turns row t into bf16 within row t's own 128-byte
+// rows (the codes it reads are its own), so the conversion needs no barrier.  Contiguous tiles
+// come by TMA (issued by thread 0), selected entries are gathered with cp.async; completion is
+// counted on `bar` as in load_tile.
+constexpr uint32_t kVScale = kKeys * 16;                // V scale rows of one slot: 2 KB
+
+template <int kSoft>
+__device__ __forceinline__ void load_tile_f8(const AttendArgs& a, const Maps& maps, int use_tma, int r, int b,
+                                             int64_t n_c, int ti, bool is_v, uint32_t dst, uint32_t vsc,
+                                             uint64_t* bar, unsigned char* valid, const void* zsrc, uint64_t pol,
+                                             bool track_cp, unsigned* err) {
+    const int tid = threadIdx.x;
+    if (use_tma) {
+        if (!is_v && tid < kKeys) valid[tid] = (int64_t)ti * kKeys + tid < n_c;
+        if (tid == 0) {
+            const int y = (int)((int64_t)b * a.Ncap + (int64_t)ti * kKeys);
+            mbar_expect_tx(bar, is_v ? kHalf + kVScale : 2 * kHalf);
+            if (is_v) {
+                tma_load_2d(dst + kHalf, &maps.v8, 0, y, bar, pol);
+                tma_load_2d(vsc, &maps.vs, 0, y, bar, pol);
+            } else {
+                tma_load_2d(dst, &maps.k8, 0, y, bar, pol);
+                tma_load_2d(dst + kHalf, &maps.kr, 0, y, bar, pol);
+            }
+            if (!track_cp) mbar_arrive_cnt(bar, kSoft);
+        }
+        if (track_cp) cp_async_arrive_noinc(bar);
+        return;
+    }
+    constexpr int kTpr = kSoft / kKeys;                 // threads per row
+    const int rr = tid / kTpr, part = tid % kTpr;
+    const int64_t key = (int64_t)ti * kKeys + rr;
+    const unsigned char* src = nullptr;
+    if (key < n_c) {
+        int64_t e = key;
+        if (a.is_csa) {
+            e = a.idx[(int64_t)r * a.k + key];
+            if (e >= a.Ncap) {
+                flag_error(err, ERRBIT_BOUNDS);
+                e = -1;
+            }
+        }
+        if (e >= 0)
+            src = static_cast<const unsigned char*>(is_v ? a.cv : a.ck) +
+                  ((int64_t)b * a.Ncap + e) * (is_v ? kKv8VRow : kKv8KRow);
+    }
+    if (!is_v && part == 0) valid[rr] = src != nullptr;
+    // K: 5 chunks of codes + scale (dense row rr of the first half), 8 of RoPE dims (swizzled
+    // second half); V: 8 chunks of codes (dense row rr of the second half), 1 of scales
+    const int nch = is_v ? 9 : 13;
+    for (int c = part; c < nch; c += kTpr) {
+        uint32_t d;
+        if (is_v) d = c < 8 ? dst + kHalf + rr * 128 + c * 16 : vsc + rr * 16;
+        else d = c < 5 ? dst + rr * 128 + c * 16 : dst + kHalf + sw128(rr, c - 5);
+        if (src) cp_async16_hint(d, src + c * 16, 16, pol);
+        else cp_async16(d, zsrc, 0);                    // zero fill (no bytes read)
+    }
+    cp_async_arrive_noinc(bar);
+}
+
+// 8 E4M3 codes (two 32-bit words) times 2^e -> 8 bf16 (exact: the product has at most 4
+// significant bits).
+__device__ __forceinline__ uint4 e4m3x8_to_bf16x8(uint32_t w0, uint32_t w1, float sc) {
+    uint32_t o[4];
+    const uint32_t w[2] = {w0, w1};
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+        const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w[h >> 1] >> (16 * (h & 1))), __NV_E4M3);
+        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&hr));
+        o[h] = pack_bf16x2(f.x * sc, f.y * sc);
+    }
+    return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+// 2^(byte - 127) for a UE8M0 scale byte (2^-127 is subnormal; 255 is not produced by the pooling).
+__device__ __forceinline__ float ue8m0_to_f32(uint32_t byte) {
+    return byte ? __uint_as_float(byte << 23) : __uint_as_float(0x00400000u);
+}
+
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+    uint4 c;
+    asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];" : "=r"(c.x), "=r"(c.y), "=r"(c.z), "=r"(c.w) : "r"(addr));
+    return c;
+}
+__device__ __forceinline__ void sts128(uint32_t addr, uint4 u) {
+    asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(u.x), "r"(u.y), "r"(u.z), "r"(u.w) : "memory");
+}
+
+// Row t of a K tile: codes and scale (dense row t of the first half) -> bf16 dims 0..63 in place.
+__device__ __forceinline__ void convert_k_f8(uint32_t slot, int t) {
+    uint4 c[5];
+#pragma unroll
+    for (int i = 0; i < 5; ++i) c[i] = lds128(slot + t * 128 + i * 16);
+    const float sc = ue8m0_to_f32(c[4].x & 0xFFu);
+    const uint32_t* w = reinterpret_cast<const uint32_t*>(c);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) sts128(slot + sw128(t, j), e4m3x8_to_bf16x8(w[2 * j], w[2 * j + 1], sc));
+}
+
+// Row t of a V tile: codes (dense row t of the second half) and scales -> bf16 dims 0..63 (first
+// half) and 64..127 (second half, in place).
+__device__ __forceinline__ void convert_v_f8(uint32_t slot, uint32_t vsc, int t) {
+    uint4 c[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) c[i] = lds128(slot + kHalf + t * 128 + i * 16);
+    uint32_t sb;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(sb) : "r"(vsc + t * 16));
+    const float sc0 = ue8m0_to_f32(sb & 0xFFu), sc1 = ue8m0_to_f32((sb >> 8) & 0xFFu);
+    const uint32_t* w = reinterpret_cast<const uint32_t*>(c);
+#pragma unroll
+    for (int j = 0; j < 16; ++j)
+        sts128(slot + (j >> 3) * kHalf + sw128(t, j & 7), e4m3x8_to_bf16x8(w[2 * j], w[2 * j + 1], j < 8 ? sc0 : sc1));
+}
+
 // The row's last item merges the row's partial results: see arrive_and_merge in the kernel.
 // Out of line: it runs once per row and keeps its registers out of the tile loop's allocation.
 template <int H>
@@ -362,8 +484,8 @@ __device__ __noinline__ void merge_row(int r, int ns, int S, const float* __rest
     }
 }
 
-template <int H>
-__global__ void __launch_bounds__(Thr<H>::kThreads, 1)
+template <int H, bool F8>
+__global__ void __launch_bounds__(Thr<H, F8>::kThreads, 1)
     attend_tc_kernel(const __grid_constant__ AttendArgs a, int S, int kps, const __grid_constant__ Maps maps, int use_tma_c, int use_tma_w,
                      int fixed_np, float* __restrict__ o_part, float* __restrict__ lse_part,
                      unsigned* __restrict__ row_cnt, unsigned* err) {
@@ -383,8 +505,11 @@ __global__ void __launch_bounds__(Thr<H>::kThreads, 1)
     }
     if (tid == 32) {
         for (int i = 0; i < 2; ++i) {
-            mbar_init(&ms.kfull[i], kSoft);
-            mbar_init(&ms.vfull[i], kSoft);
+            // FP8 caches: the loads complete on k8full / v8full and the converters release the tiles
+            mbar_init(&ms.kfull[i], F8 ? Thr<H, F8>::kConv : kSoft);
+            mbar_init(&ms.vfull[i], F8 ? Thr<H, F8>::kConv : kSoft);
+            mbar_init(&ms.k8full[i], kSoft);
+            mbar_init(&ms.v8full[i], kSoft);
             mbar_init(&ms.sdone[i], 1);
             ms.flag[i] = 0;
         }
@@ -512,6 +637,41 @@ __global__ void __launch_bounds__(Thr<H>::kThreads, 1)
             }
         }
         __syncwarp();
+    } else if (F8 && warp > kSoft / 32) {
+        // ======================================================= converter warps (FP8 caches)
+        // In the MMA warp's order of use -- K(0), K(1), then V(i), K(i+2) -- each tile's codes are
+        // waited for, written out as bf16 in place (compressed tiles; window tiles are bf16
+        // already) and released to the MMA warp.
+        const int t = tid - (kSoft + 32);
+        uint32_t g = 0;
+        ItemTiles it;
+        for (int cur = cur0; next_item(cur, it);) {
+            const int nt = it.nt;
+            if (nt == 0) continue;
+            auto conv = [&](int i, bool is_v) {
+                const uint32_t seq = g + (uint32_t)i;
+                mbar_wait(is_v ? &ms.v8full[seq & 1] : &ms.k8full[seq & 1], (seq >> 1) & 1, err);
+                if (it.t0 + i < it.nt_c) {
+                    const uint32_t slot = sbase + (is_v ? L::v : L::k) + (seq & 1) * kTile;
+                    const uint32_t vsc = sbase + L::total + (seq & 1) * kVScale;
+#pragma unroll
+                    for (int rr = t; rr < kKeys; rr += Thr<H, F8>::kConv) {
+                        if (is_v) convert_v_f8(slot, vsc, rr);
+                        else convert_k_f8(slot, rr);
+                    }
+                    fence_proxy_async();                    // the bf16 tile, for the tensor core
+                }
+                mbar_arrive(is_v ? &ms.vfull[seq & 1] : &ms.kfull[seq & 1]);
+            };
+            conv(0, false);
+            if (nt > 1) conv(1, false);
+#pragma unroll 1
+            for (int i = 0; i < nt; ++i) {
+                conv(i, true);
+                if (i + 2 < nt) conv(i + 2, false);
+            }
+            g += (uint32_t)nt;
+        }
     } else {
         // ==================================================================== softmax warps
         constexpr int HG = kHG;                     // heads per warpgroup
@@ -565,12 +725,19 @@ __global__ void __launch_bounds__(Thr<H>::kThreads, 1)
             if (tid < H) ms.mrun[tid] = -INFINITY;
 
             // Tile i's loads are the (g + i)-th of each ring, so slot = (g + i) & 1.
+            // (FP8 caches: every load completes on k8full / v8full, the converters pass it on)
             auto load = [&](int i, bool is_v) {
                 const uint32_t seq = g + (uint32_t)i;
-                load_tile<kSoft>(a, maps, use_tma_c, use_tma_w, r, b, p, kl.n_c, kl.total, nt_c, t0 + i, is_v,
-                                 sbase + (is_v ? L::v : L::k) + (seq & 1) * kTile,
-                                 is_v ? &ms.vfull[seq & 1] : &ms.kfull[seq & 1], ms.valid[seq & 3], qr, pol_stream,
-                                 i == 0 && !is_v, err);
+                const uint32_t dst = sbase + (is_v ? L::v : L::k) + (seq & 1) * kTile;
+                uint64_t* bar = F8 ? (is_v ? &ms.v8full[seq & 1] : &ms.k8full[seq & 1])
+                                   : (is_v ? &ms.vfull[seq & 1] : &ms.kfull[seq & 1]);
+                if (F8 && t0 + i < nt_c)
+                    load_tile_f8<kSoft>(a, maps, use_tma_c, r, b, kl.n_c, t0 + i, is_v, dst,
+                                        sbase + L::total + (seq & 1) * kVScale, bar, ms.valid[seq & 3], qr, pol_stream,
+                                        i == 0 && !is_v, err);
+                else
+                    load_tile<kSoft>(a, maps, use_tma_c, use_tma_w, r, b, p, kl.n_c, kl.total, nt_c, t0 + i, is_v,
+                                     dst, bar, ms.valid[seq & 3], qr, pol_stream, i == 0 && !is_v, err);
             };
 
             // ---- prologue: Q, K(0), K(1), V(0) in flight (K(0) completes only once Q has landed)
@@ -812,23 +979,33 @@ bool encode_rows(CUtensorMap* m, const void* base, int64_t rows) {
     return rows > 0 && encode_tmap_2d(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, base, kD, (uint64_t)rows, kD * 2, 64, kKeys);
 }
 
-template <int H>
+template <int H, bool F8>
 cudaError_t launch_tc(const AttendArgs& a, int S, int kps, float* o_part, float* lse_part, unsigned* row_cnt,
                       unsigned* err, cudaStream_t st) {
     Maps maps;
     std::memset(&maps, 0, sizeof maps);
     int use_c = 0, use_w = 0;
     // HCA entries of a sequence are contiguous; CSA entries are gathered through the index list.
-    if (!a.is_csa && encode_rows(&maps.ck, a.ck, (int64_t)a.B * a.Ncap) &&
-        encode_rows(&maps.cv, a.cv, (int64_t)a.B * a.Ncap))
+    const uint64_t crows = (uint64_t)a.B * (uint64_t)a.Ncap;
+    if (!a.is_csa && !F8 && encode_rows(&maps.ck, a.ck, (int64_t)crows) && encode_rows(&maps.cv, a.cv, (int64_t)crows))
+        use_c = 1;
+    if (!a.is_csa && F8 &&
+        encode_tmap_2d_sw(&maps.k8, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.ck, 128, crows, kKv8KRow, 128, kKeys,
+                          CU_TENSOR_MAP_SWIZZLE_NONE) &&
+        encode_tmap_2d_sw(&maps.kr, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, static_cast<const char*>(a.ck) + 80, 64, crows,
+                          kKv8KRow, 64, kKeys, CU_TENSOR_MAP_SWIZZLE_128B) &&
+        encode_tmap_2d_sw(&maps.v8, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.cv, 128, crows, kKv8VRow, 128, kKeys,
+                          CU_TENSOR_MAP_SWIZZLE_NONE) &&
+        encode_tmap_2d_sw(&maps.vs, CU_TENSOR_MAP_DATA_TYPE_UINT8, static_cast<const char*>(a.cv) + 128, 16, crows,
+                          kKv8VRow, 16, kKeys, CU_TENSOR_MAP_SWIZZLE_NONE))
         use_c = 1;
     // The decode window is the whole ring when it holds exactly one tile of tokens.
     if (a.chunk_k == nullptr && a.W == kKeys && a.ring_cap == kKeys && a.ring_k != nullptr &&
         encode_rows(&maps.rk, a.ring_k, (int64_t)a.B * a.ring_cap) &&
         encode_rows(&maps.rv, a.ring_v, (int64_t)a.B * a.ring_cap))
         use_w = 1;
-    const size_t smem = Smem<H>::total + 1024;
-    auto kern = attend_tc_kernel<H>;
+    const size_t smem = Smem<H>::total + (F8 ? 2 * kVScale : 0) + 1024;
+    auto kern = attend_tc_kernel<H, F8>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const int R = a.B * a.T;
@@ -845,7 +1022,7 @@ cudaError_t launch_tc(const AttendArgs& a, int S, int kps, float* o_part, float*
             fixed_np = (int)cdiv(nt, len);
         }
     }
-    (void)launch_pdl(kern, dim3(grid), dim3(Thr<H>::kThreads), smem, st, a, S, kps, maps, use_c, use_w, fixed_np,
+    (void)launch_pdl(kern, dim3(grid), dim3(Thr<H, F8>::kThreads), smem, st, a, S, kps, maps, use_c, use_w, fixed_np,
                      o_part, lse_part, row_cnt, err);
     return cudaGetLastError();
 }
@@ -853,15 +1030,19 @@ cudaError_t launch_tc(const AttendArgs& a, int S, int kps, float* o_part, float*
 }  // namespace
 
 bool attend_tc_supported(const AttendArgs& a) {
-    return a.dtype == CSAHCA_BF16 && a.d == 128 && (a.H == 32 || a.H == 64) && a.scale > 0.0f &&
-           aligned(a.out, 16);
+    return (a.dtype == CSAHCA_BF16 || a.dtype == CSAHCA_KV_FP8) && a.d == 128 && (a.H == 32 || a.H == 64) &&
+           a.scale > 0.0f && aligned(a.out, 16);
 }
 
 cudaError_t attend_tc_launch(const AttendArgs& a, int S, int kps, float* o_part, float* lse_part, unsigned* row_cnt,
                              unsigned* err, cudaStream_t st) {
     switch (a.H) {
-        case 32: return launch_tc<32>(a, S, kps, o_part, lse_part, row_cnt, err, st);
-        case 64: return launch_tc<64>(a, S, kps, o_part, lse_part, row_cnt, err, st);
+        case 32:
+            return a.dtype == CSAHCA_KV_FP8 ? launch_tc<32, true>(a, S, kps, o_part, lse_part, row_cnt, err, st)
+                                            : launch_tc<32, false>(a, S, kps, o_part, lse_part, row_cnt, err, st);
+        case 64:
+            return a.dtype == CSAHCA_KV_FP8 ? launch_tc<64, true>(a, S, kps, o_part, lse_part, row_cnt, err, st)
+                                            : launch_tc<64, false>(a, S, kps, o_part, lse_part, row_cnt, err, st);
         default: return cudaErrorNotSupported;
     }
 }

@@ -53,10 +53,11 @@ __device__ __forceinline__ float alpha_of(const float (&a)[8], int i) {
 }
 
 // Pool one block with one warp.  rowptr(which, i) -> pointer to token i's row of K (which=0)
-// or V (which=1).  Writes ck_row / cv_row.
-template <typename T, typename RowPtr>
+// or V (which=1).  Writes ck_row / cv_row: rows of T, or (kKv8, d = 128: one pass, every lane
+// active) the entry's FP8 K and V rows.
+template <typename T, bool kKv8, typename RowPtr>
 __device__ __forceinline__ void pool_block_warp(int m, int d, const float (&a)[8], RowPtr rowptr,
-                                                T* ck_row, T* cv_row) {
+                                                void* ck_row, void* cv_row) {
     const int lane = threadIdx.x & 31;
     const int groups = d / 8;                 // 8-channel groups per tensor
     for (int g0 = 0; g0 < 2 * groups; g0 += 32) {
@@ -74,15 +75,18 @@ __device__ __forceinline__ void pool_block_warp(int m, int d, const float (&a)[8
                 for (int c = 0; c < 8; ++c) acc[c] = fmaf(al, x[c], acc[c]);
             }
         }
-        if (active) store8((which ? cv_row : ck_row) + col, acc);
+        if constexpr (kKv8)
+            store_kv8_warp(acc, static_cast<unsigned char*>(ck_row), static_cast<unsigned char*>(cv_row), lane);
+        else if (active)
+            store8(static_cast<T*>(which ? cv_row : ck_row) + col, acc);
     }
 }
 
-template <typename T>
+template <typename T, bool kKv8>
 __global__ void compress_kernel(const T* __restrict__ k_raw, const T* __restrict__ v_raw,
                                 const float* __restrict__ gate, int64_t raw_stride,
                                 const int64_t* __restrict__ raw_pos0, const int64_t* __restrict__ n_raw,
-                                const float* __restrict__ bias, int m, int B, int d, T* ck, T* cv,
+                                const float* __restrict__ bias, int m, int B, int d, void* ck, void* cv,
                                 int64_t Ncap, int64_t max_blocks, unsigned* err) {
     pdl_wait();
     pdl_trigger();
@@ -107,7 +111,12 @@ __global__ void compress_kernel(const T* __restrict__ k_raw, const T* __restrict
         auto rowptr = [&](int which, int i) -> const T* {
             return (which ? v_raw : k_raw) + (row0 + i) * (int64_t)d;
         };
-        pool_block_warp<T>(m, d, a, rowptr, ck + ((int64_t)b * Ncap + j) * d, cv + ((int64_t)b * Ncap + j) * d);
+        const int64_t e = (int64_t)b * Ncap + j;
+        if constexpr (kKv8)
+            pool_block_warp<T, true>(m, d, a, rowptr, static_cast<unsigned char*>(ck) + e * kKv8KRow,
+                                     static_cast<unsigned char*>(cv) + e * kKv8VRow);
+        else
+            pool_block_warp<T, false>(m, d, a, rowptr, static_cast<T*>(ck) + e * d, static_cast<T*>(cv) + e * d);
     }
 }
 
@@ -121,11 +130,11 @@ __global__ void compress_kernel(const T* __restrict__ k_raw, const T* __restrict
 // from one 64-bit remainder per block (ring_cap >= m - 1, so one conditional subtraction).
 constexpr int kAppendThreads = 256;
 
-template <typename T>
+template <typename T, bool kKv8>
 __global__ void __launch_bounds__(kAppendThreads) append_kernel(
     const T* __restrict__ k_new, const T* __restrict__ v_new, const float* __restrict__ gate_new,
     const void* kidx_new, int kidx_dtype, int kidx_rows, const int64_t* __restrict__ pos, int n_new, int d,
-    const float* __restrict__ bias, int m, T* ring_k, T* ring_v, float* ring_gate, int ring_cap, T* ck, T* cv,
+    const float* __restrict__ bias, int m, T* ring_k, T* ring_v, float* ring_gate, int ring_cap, void* ck, void* cv,
     int64_t Ncap, void* k_codes, void* k_scale, int key_fmt, int d_I, unsigned* err) {
     pdl_wait();
     pdl_trigger();
@@ -232,9 +241,15 @@ __global__ void __launch_bounds__(kAppendThreads) append_kernel(
             for (int q = 0; q < NS; ++q)
 #pragma unroll
                 for (int c = 0; c < 8; ++c) o[c] += part[(q * G + tid) * 8 + c];
-            const int wh = (tid < G / 2) ? 0 : 1;
-            const int cl = (tid % (G / 2)) * 8;
-            store8((wh ? cv : ck) + ((int64_t)b * Ncap + j) * d + cl, o);
+            const int64_t e = (int64_t)b * Ncap + j;
+            if constexpr (kKv8) {                           // d = 128: G = 32, warp 0
+                store_kv8_warp(o, static_cast<unsigned char*>(ck) + e * kKv8KRow,
+                               static_cast<unsigned char*>(cv) + e * kKv8VRow, lane);
+            } else {
+                const int wh = (tid < G / 2) ? 0 : 1;
+                const int cl = (tid % (G / 2)) * 8;
+                store8(static_cast<T*>(wh ? cv : ck) + e * d + cl, o);
+            }
         }
         if (quant) {
             const int E = d_I / 32;
@@ -293,7 +308,7 @@ __global__ void ring_write_kernel(const T* __restrict__ k_new, const T* __restri
     }
 }
 
-bool kv_dtype_ok(csahca_dtype t) { return t == CSAHCA_F32 || t == CSAHCA_BF16; }
+bool kv_dtype_ok(csahca_dtype t) { return t == CSAHCA_F32 || t == CSAHCA_BF16 || t == CSAHCA_KV_FP8; }
 
 csahca_status compress_impl(const void* k_raw, const void* v_raw, const float* gate, int64_t raw_stride,
                             const int64_t* raw_pos0, const int64_t* n_raw, const float* bias, int m,
@@ -303,6 +318,7 @@ csahca_status compress_impl(const void* k_raw, const void* v_raw, const float* g
     CSAHCA_REQUIRE(m >= 1 && m <= kMaxM && B >= 1 && d >= 8 && d <= 512 && d % 8 == 0);
     CSAHCA_REQUIRE(raw_stride >= 0 && Ncap >= 0);
     CSAHCA_REQUIRE(kv_dtype_ok(kv));
+    if (kv == CSAHCA_KV_FP8) CSAHCA_REQUIRE(d == 128);
     const size_t al = (kv == CSAHCA_F32) ? 32 : 16;
     CSAHCA_REQUIRE(aligned(k_raw, al) && aligned(v_raw, al) && aligned(ck, al) && aligned(cv, al));
     const int64_t max_blocks = raw_stride / m + 1;
@@ -314,13 +330,17 @@ csahca_status compress_impl(const void* k_raw, const void* v_raw, const float* g
     unsigned* err = err_word();
     if (!err) return CSAHCA_ERR_CUDA;
     if (kv == CSAHCA_F32)
-        (void)launch_pdl(compress_kernel<float>, dim3(grid), dim3(threads), 0, stream, 
+        (void)launch_pdl(compress_kernel<float, false>, dim3(grid), dim3(threads), 0, stream,
             (const float*)k_raw, (const float*)v_raw, gate, raw_stride, raw_pos0, n_raw, bias, m, B, d,
-            (float*)ck, (float*)cv, Ncap, max_blocks, err);
-    else
-        (void)launch_pdl(compress_kernel<__nv_bfloat16>, dim3(grid), dim3(threads), 0, stream, 
+            ck, cv, Ncap, max_blocks, err);
+    else if (kv == CSAHCA_BF16)
+        (void)launch_pdl(compress_kernel<__nv_bfloat16, false>, dim3(grid), dim3(threads), 0, stream,
             (const __nv_bfloat16*)k_raw, (const __nv_bfloat16*)v_raw, gate, raw_stride, raw_pos0, n_raw,
-            bias, m, B, d, (__nv_bfloat16*)ck, (__nv_bfloat16*)cv, Ncap, max_blocks, err);
+            bias, m, B, d, ck, cv, Ncap, max_blocks, err);
+    else
+        (void)launch_pdl(compress_kernel<__nv_bfloat16, true>, dim3(grid), dim3(threads), 0, stream,
+            (const __nv_bfloat16*)k_raw, (const __nv_bfloat16*)v_raw, gate, raw_stride, raw_pos0, n_raw,
+            bias, m, B, d, ck, cv, Ncap, max_blocks, err);
     count_launch();
     CSAHCA_CHECK_LAUNCH();
     return CSAHCA_OK;
@@ -336,6 +356,7 @@ csahca_status append_impl(const void* k_new, const void* v_new, const float* gat
     CSAHCA_REQUIRE((int64_t)n_new * (d / 8) < (1LL << 30) && (int64_t)n_new + ring_cap < (1LL << 30));
     CSAHCA_REQUIRE(ring_cap >= 1 && ring_cap >= m - 1 && Ncap >= 0);
     CSAHCA_REQUIRE(kv_dtype_ok(kv));
+    if (kv == CSAHCA_KV_FP8) CSAHCA_REQUIRE(d == 128);
     const size_t al = (kv == CSAHCA_F32) ? 32 : 16;
     CSAHCA_REQUIRE(aligned(k_new, al) && aligned(v_new, al) && aligned(ring_k, al) && aligned(ring_v, al) &&
                    aligned(ck, al) && aligned(cv, al));
@@ -351,15 +372,20 @@ csahca_status append_impl(const void* k_new, const void* v_new, const float* gat
     if (!err) return CSAHCA_ERR_CUDA;
     const int kidx_rows = n_new / m + 1;
     if (kv == CSAHCA_F32)
-        (void)launch_pdl(append_kernel<float>, dim3(B), dim3(kAppendThreads), 0, stream, 
+        (void)launch_pdl(append_kernel<float, false>, dim3(B), dim3(kAppendThreads), 0, stream,
             (const float*)k_new, (const float*)v_new, gate_new, kidx_new, kidx_dtype, kidx_rows, pos, n_new, d,
-            bias, m, (float*)ring_k, (float*)ring_v, ring_gate, ring_cap, (float*)ck, (float*)cv, Ncap, k_codes,
+            bias, m, (float*)ring_k, (float*)ring_v, ring_gate, ring_cap, ck, cv, Ncap, k_codes,
             k_scale, key_fmt, d_I, err);
-    else
-        (void)launch_pdl(append_kernel<__nv_bfloat16>, dim3(B), dim3(kAppendThreads), 0, stream, 
+    else if (kv == CSAHCA_BF16)
+        (void)launch_pdl(append_kernel<__nv_bfloat16, false>, dim3(B), dim3(kAppendThreads), 0, stream,
             (const __nv_bfloat16*)k_new, (const __nv_bfloat16*)v_new, gate_new, kidx_new, kidx_dtype, kidx_rows,
             pos, n_new, d, bias, m, (__nv_bfloat16*)ring_k, (__nv_bfloat16*)ring_v, ring_gate, ring_cap,
-            (__nv_bfloat16*)ck, (__nv_bfloat16*)cv, Ncap, k_codes, k_scale, key_fmt, d_I, err);
+            ck, cv, Ncap, k_codes, k_scale, key_fmt, d_I, err);
+    else
+        (void)launch_pdl(append_kernel<__nv_bfloat16, true>, dim3(B), dim3(kAppendThreads), 0, stream,
+            (const __nv_bfloat16*)k_new, (const __nv_bfloat16*)v_new, gate_new, kidx_new, kidx_dtype, kidx_rows,
+            pos, n_new, d, bias, m, (__nv_bfloat16*)ring_k, (__nv_bfloat16*)ring_v, ring_gate, ring_cap,
+            ck, cv, Ncap, k_codes, k_scale, key_fmt, d_I, err);
     count_launch();
     CSAHCA_CHECK_LAUNCH();
     return CSAHCA_OK;

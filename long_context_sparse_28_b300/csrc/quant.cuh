@@ -99,4 +99,66 @@ __host__ __device__ inline int64_t key_scale_bytes(int fmt, int d_I) {
     return fmt == CSAHCA_E4M3_ROWSCALE ? 4 : fmt == CSAHCA_E2M1_UE8M0 ? d_I / 32 : 0;
 }
 
+
+// ---------------------------------------------------------------- FP8 compressed K/V
+// Storage of pooled K/V rows of d = 128 in the CSAHCA_KV_FP8 layout (pogovet.com article,
+// detail 5: KV entries in FP8, the RoPE dims in BF16): per 64 values one power-of-two scale 2^e,
+// e = the smallest integer with amax <= 448 * 2^e (amax = f 2^ex, f in [0.5, 1): e = ex - 9 when
+// f <= 0.875 = 448 / 2^9, else ex - 8; 0 for a zero block; clamped to [-127, 127]), codes
+// RNE_e4m3(x * 2^-e) (the scaling is exact); the last 64 dims of K in bfloat16.
+constexpr int kKv8KRow = 208;   // bytes per K row: 64 codes, scale byte, 15 zero bytes, 64 bf16
+constexpr int kKv8VRow = 144;   // bytes per V row: 128 codes, 2 scale bytes, 14 zero bytes
+
+__device__ __forceinline__ int kv8_block_exponent(float amax) {
+    if (!(amax > 0.0f)) return 0;
+    int ex;
+    const float f = frexpf(amax, &ex);
+    const int e = f <= 0.875f ? ex - 9 : ex - 8;
+    return e < -127 ? -127 : (e > 127 ? 127 : e);
+}
+
+// 2^k for k in [-127, 127] as a float (2^-127 is subnormal).
+__device__ __forceinline__ float pow2f(int k) {
+    return k >= -126 ? __int_as_float((127 + k) << 23) : __int_as_float(0x00400000);
+}
+
+// One warp stores one pooled entry: lane L holds 8 consecutive pooled values, lanes 0-15 the K
+// row (dims 8L .. 8L+7), lanes 16-31 the V row (dims 8(L-16) ..).  krow / vrow: the entry's K
+// (kKv8KRow bytes) and V (kKv8VRow bytes) rows, 16-byte aligned.  All 32 lanes take part.
+__device__ __forceinline__ void store_kv8_warp(const float (&x)[8], unsigned char* krow, unsigned char* vrow,
+                                               int lane) {
+    float am = 0.0f;
+#pragma unroll
+    for (int c = 0; c < 8; ++c) am = fmaxf(am, fabsf(x[c]));
+    am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 1));   // the lane's block: 8 aligned lanes
+    am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 2));
+    am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 4));
+    const int e = kv8_block_exponent(am);
+    const int e_v1 = __shfl_sync(0xffffffffu, e, 24);
+    if (lane >= 8 && lane < 16) {                           // K dims 64..127: bfloat16
+        uint4 u;
+        u.x = pack_bf16x2(x[0], x[1]);
+        u.y = pack_bf16x2(x[2], x[3]);
+        u.z = pack_bf16x2(x[4], x[5]);
+        u.w = pack_bf16x2(x[6], x[7]);
+        *reinterpret_cast<uint4*>(krow + 80 + (lane - 8) * 16) = u;
+    } else {
+        const float sc = pow2f(-e);
+        uint32_t w[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const uint32_t c0 = __nv_cvt_float2_to_fp8x2(make_float2(x[4 * h] * sc, x[4 * h + 1] * sc), __NV_SATFINITE,
+                                                         __NV_E4M3);
+            const uint32_t c1 = __nv_cvt_float2_to_fp8x2(make_float2(x[4 * h + 2] * sc, x[4 * h + 3] * sc),
+                                                         __NV_SATFINITE, __NV_E4M3);
+            w[h] = c0 | (c1 << 16);
+        }
+        unsigned char* dst = lane < 8 ? krow + lane * 8 : vrow + (lane - 16) * 8;
+        *reinterpret_cast<uint2*>(dst) = make_uint2(w[0], w[1]);
+    }
+    if (lane == 0) *reinterpret_cast<uint4*>(krow + 64) = make_uint4((uint32_t)(e + 127), 0u, 0u, 0u);
+    if (lane == 16)
+        *reinterpret_cast<uint4*>(vrow + 128) = make_uint4((uint32_t)(e + 127) | ((uint32_t)(e_v1 + 127) << 8), 0u, 0u, 0u);
+}
+
 }  // namespace csahca

@@ -13,6 +13,11 @@ namespace csahca {
 bool encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType type, const void* base, uint64_t inner, uint64_t rows,
                     uint64_t pitch, uint32_t box_inner, uint32_t box_rows);
 
+// The same with the swizzle mode given (CU_TENSOR_MAP_SWIZZLE_NONE lands the box as dense rows)
+// and only the 16-byte base alignment TMA itself asks for (a map may start inside a row).
+bool encode_tmap_2d_sw(CUtensorMap* map, CUtensorMapDataType type, const void* base, uint64_t inner, uint64_t rows,
+                       uint64_t pitch, uint32_t box_inner, uint32_t box_rows, CUtensorMapSwizzle swizzle);
+
 // Encodes an N-D tiled map (N <= 5): dims[0] elements innermost, strides[i] = byte stride of
 // dims[i + 1] (any order: a map may visit rows in a permuted order), box[i] per dimension,
 // 128-byte swizzle.  False when the driver rejects it.

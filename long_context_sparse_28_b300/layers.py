@@ -18,22 +18,32 @@ import torch
 
 from . import (BF16, F32, csa_attend, csa_attend_workspace, csa_cache_append, csa_compress, csa_index_key_quantize,
                csa_index_topk, csa_index_topk_workspace, hca_attend, hca_attend_workspace, hca_cache_append,
-               hca_compress, key_storage, swa_ring_write)
+               hca_compress, key_storage, swa_ring_write, KV_FP8_K_ROW, KV_FP8_V_ROW)
 
 
 def _i64(x, device):
     return torch.as_tensor(x, dtype=torch.int64, device=device).reshape(-1).contiguous()
 
 
+def kv_storage(B, Ncap, d, dtype, kv_fp8, device):
+    """Compressed K and V caches: [B, Ncap, d] of dtype, or with kv_fp8 (d = 128, bfloat16 raw
+    tokens) the FP8 rows of KV_FP8_K_ROW / KV_FP8_V_ROW bytes (pogovet.com detail 5: KV entries in
+    FP8, the RoPE dims in BF16)."""
+    if kv_fp8:
+        assert d == 128 and dtype == torch.bfloat16
+        return (torch.zeros(B, Ncap, KV_FP8_K_ROW, dtype=torch.uint8, device=device),
+                torch.zeros(B, Ncap, KV_FP8_V_ROW, dtype=torch.uint8, device=device))
+    return (torch.zeros(B, Ncap, d, dtype=dtype, device=device), torch.zeros(B, Ncap, d, dtype=dtype, device=device))
+
+
 class CSACache:
     """Compressed sparse attention cache of B sequences (m = 4 by default)."""
 
-    def __init__(self, B, Ncap, d, W, d_I, key_fmt, dtype, device="cuda", m=4):
+    def __init__(self, B, Ncap, d, W, d_I, key_fmt, dtype, device="cuda", m=4, kv_fp8=False):
         Ncap = (Ncap + 255) // 256 * 256   # capacity in whole 256-key tensor-core indexer stages
         self.B, self.Ncap, self.d, self.W, self.d_I, self.m = B, Ncap, d, W, d_I, m
-        self.key_fmt, self.dtype, self.device = key_fmt, dtype, device
-        self.ck = torch.zeros(B, Ncap, d, dtype=dtype, device=device)
-        self.cv = torch.zeros(B, Ncap, d, dtype=dtype, device=device)
+        self.key_fmt, self.dtype, self.device, self.kv_fp8 = key_fmt, dtype, device, kv_fp8
+        self.ck, self.cv = kv_storage(B, Ncap, d, dtype, kv_fp8, device)
         self.ring_k = torch.zeros(B, W, d, dtype=dtype, device=device)
         self.ring_v = torch.zeros(B, W, d, dtype=dtype, device=device)
         self.ring_gate = torch.zeros(B, W, dtype=torch.float32, device=device)
@@ -58,10 +68,10 @@ class CSACache:
 class HCACache:
     """Heavily compressed attention cache of B sequences (m = 128 by default)."""
 
-    def __init__(self, B, Ncap, d, W, dtype, device="cuda", m=128):
+    def __init__(self, B, Ncap, d, W, dtype, device="cuda", m=128, kv_fp8=False):
         self.B, self.Ncap, self.d, self.W, self.m, self.dtype, self.device = B, Ncap, d, W, m, dtype, device
-        self.ck = torch.zeros(B, Ncap, d, dtype=dtype, device=device)
-        self.cv = torch.zeros(B, Ncap, d, dtype=dtype, device=device)
+        self.kv_fp8 = kv_fp8
+        self.ck, self.cv = kv_storage(B, Ncap, d, dtype, kv_fp8, device)
         self.ring_k = torch.zeros(B, W, d, dtype=dtype, device=device)
         self.ring_v = torch.zeros(B, W, d, dtype=dtype, device=device)
         self.ring_gate = torch.zeros(B, W, dtype=torch.float32, device=device)

@@ -164,3 +164,44 @@ def oracle_hca_seq(case, b):
     ck, cv = oracle.compress(h["K"], h["V"], h["G"], npy(case["bias"]), m, sd, n_blocks=Lb // m)
     res = oracle.hca_queries(npy(case["q"][b]), [Lb - 1], ck, cv, h["K"], h["V"], 0, m, w.W, w.scale)
     return res, ck, cv
+
+
+# ----------------------------------------------------------- FP8 compressed K/V (pogovet.com detail 5)
+def kv8_planes(ck, cv):
+    """GPU FP8 caches [N, 208] / [N, 144] uint8 -> the oracle's planes (K codes, scales, RoPE bf16
+    bits; V codes, scales), after checking the zero padding bytes."""
+    k = npy(ck).astype(np.uint8)
+    v = npy(cv).astype(np.uint8)
+    assert not k[:, 65:80].any() and not v[:, 130:144].any(), "padding bytes"
+    return dict(k_codes=k[:, :64], k_scales=k[:, 64:65], k_rope=np.ascontiguousarray(k[:, 80:208]).view(np.uint16),
+                v_codes=v[:, :128], v_scales=v[:, 128:130])
+
+
+def kv8_dequant(pl, d=128):
+    return (oracle.dequant_kv_fp8(pl["k_codes"], pl["k_scales"], pl["k_rope"], d),
+            oracle.dequant_kv_fp8(pl["v_codes"], pl["v_scales"], None, d))
+
+
+def e4m3_step(deq, scale_bytes, block=64):
+    """One E4M3 grid step at each dequantised value, at its block's scale."""
+    e = np.repeat(scale_bytes.astype(np.int64) - 127, block, axis=1)[:, : deq.shape[1]]
+    z = np.abs(deq) * np.ldexp(1.0, -e)
+    k = np.floor(np.log2(np.maximum(z, 2.0 ** -6))).astype(np.int64)
+    return np.ldexp(1.0, np.where(z < 2.0 ** -6, -9, k - 3) + e)
+
+
+def assert_kv8_close(ck, cv, ora, what=""):
+    """Pooled FP8 caches against the oracle's (compress_kv_fp8): the pooled float32 values of the
+    device and the oracle's fp64 ones rounded to float32 may differ in their last bits, so a code
+    may sit one E4M3 step (and a scale one binade) away; the RoPE dims within one bf16 step."""
+    g = kv8_planes(ck, cv)
+    gk, gv = kv8_dequant(g)
+    for name, gd, od, gs, os_ in (("K", gk[:, :64], ora["ck"][:, :64], g["k_scales"], ora["k_scales"]),
+                                  ("V", gv, ora["cv"], g["v_scales"], ora["v_scales"])):
+        tol = np.maximum(e4m3_step(gd, gs), e4m3_step(od, os_))
+        assert (np.abs(gd - od) <= tol).all(), f"{what} {name}: beyond one E4M3 step"
+        assert np.mean(gs == os_) >= 0.99, f"{what} {name}: scale bytes"
+        assert np.abs(gs.astype(int) - os_.astype(int)).max() <= 1, f"{what} {name}: scale off by more than 1"
+    assert np.mean(g["k_codes"] == ora["k_codes"]) >= 0.95 and np.mean(g["v_codes"] == ora["v_codes"]) >= 0.95
+    hu = 2 * bf16_half_ulp(ora["ck"][:, 64:])
+    assert (np.abs(gk[:, 64:] - ora["ck"][:, 64:]) <= hu).all(), f"{what}: RoPE dims"

@@ -50,6 +50,7 @@ class Workload:
     outlier_frac: float = 0.0
     outlier_mult: float = 4.0
     index_q: str = "bf16"     # indexer queries: "bf16", or "e2m1" (FP4, the keys' MX form)
+    kv_cache: str = "bf16"    # compressed K/V storage: "bf16" (= kv), or "fp8" (E4M3, RoPE dims of K in bf16)
     seed: int = 0
 
     def lengths(self) -> list[int]:
@@ -234,3 +235,7 @@ def prefill_inputs(w: Workload, device="cuda", b: int = 0):
     out["q_hca"] = queries(w, "hca", b, w.T, device)
     out["q_idx"], out["w"] = indexer_queries(w, "csa", b, w.T, device)
     return out
+
+# The 1M-context decode workload with the compressed K/V caches in FP8 (the RoPE dims of K in BF16).
+WORKLOADS["decode_1m_b32_csa_hca_kv8"] = replace(WORKLOADS["decode_1m_b32_csa_hca"], name="decode_1m_b32_csa_hca_kv8",
+                                                kv_cache="fp8")
