@@ -55,7 +55,11 @@ template <int H, bool F8 = false>
 struct Thr {
     static_assert(H % kHG == 0, "heads in groups of 16");
     static constexpr int kSoft = (H / kHG) * kKeys;
-    static constexpr int kConv = F8 ? 64 : 0;       // FP8 caches: converter threads, two tile rows each
+    // FP8 caches: converter threads -- one warp for K tiles (four rows each), two for V tiles (two
+    // rows each); 3 warps keep the block at a multiple of 4 warps (the register budget of H = 64)
+    static constexpr int kConvK = F8 ? 32 : 0;
+    static constexpr int kConvV = F8 ? 64 : 0;
+    static constexpr int kConv = kConvK + kConvV;
     static constexpr int kThreads = kSoft + 32 + kConv;
 };
 
@@ -506,8 +510,8 @@ __global__ void __launch_bounds__(Thr<H, F8>::kThreads, 1)
     if (tid == 32) {
         for (int i = 0; i < 2; ++i) {
             // FP8 caches: the loads complete on k8full / v8full and the converters release the tiles
-            mbar_init(&ms.kfull[i], F8 ? Thr<H, F8>::kConv : kSoft);
-            mbar_init(&ms.vfull[i], F8 ? Thr<H, F8>::kConv : kSoft);
+            mbar_init(&ms.kfull[i], F8 ? Thr<H, F8>::kConvK : kSoft);
+            mbar_init(&ms.vfull[i], F8 ? Thr<H, F8>::kConvV : kSoft);
             mbar_init(&ms.k8full[i], kSoft);
             mbar_init(&ms.v8full[i], kSoft);
             mbar_init(&ms.sdone[i], 1);
@@ -639,36 +643,33 @@ __global__ void __launch_bounds__(Thr<H, F8>::kThreads, 1)
         __syncwarp();
     } else if (F8 && warp > kSoft / 32) {
         // ======================================================= converter warps (FP8 caches)
-        // In the MMA warp's order of use -- K(0), K(1), then V(i), K(i+2) -- each tile's codes are
-        // waited for, written out as bf16 in place (compressed tiles; window tiles are bf16
-        // already) and released to the MMA warp.
+        // Two in-order streams, so a late V tile never holds up the next K tile: the K warp takes
+        // K(0), K(1), ..., the V warps V(0), V(1), ...; each tile's codes are waited for, written out
+        // as bf16 in place (compressed tiles; window tiles are bf16 already) and released to the
+        // MMA warp.
         const int t = tid - (kSoft + 32);
+        const bool is_v = t >= Thr<H, F8>::kConvK;
+        const int t0r = is_v ? t - Thr<H, F8>::kConvK : t;
+        const int step = is_v ? Thr<H, F8>::kConvV : Thr<H, F8>::kConvK;
         uint32_t g = 0;
         ItemTiles it;
         for (int cur = cur0; next_item(cur, it);) {
             const int nt = it.nt;
-            if (nt == 0) continue;
-            auto conv = [&](int i, bool is_v) {
+#pragma unroll 1
+            for (int i = 0; i < nt; ++i) {
                 const uint32_t seq = g + (uint32_t)i;
                 mbar_wait(is_v ? &ms.v8full[seq & 1] : &ms.k8full[seq & 1], (seq >> 1) & 1, err);
                 if (it.t0 + i < it.nt_c) {
                     const uint32_t slot = sbase + (is_v ? L::v : L::k) + (seq & 1) * kTile;
                     const uint32_t vsc = sbase + L::total + (seq & 1) * kVScale;
-#pragma unroll
-                    for (int rr = t; rr < kKeys; rr += Thr<H, F8>::kConv) {
+#pragma unroll 1
+                    for (int rr = t0r; rr < kKeys; rr += step) {
                         if (is_v) convert_v_f8(slot, vsc, rr);
                         else convert_k_f8(slot, rr);
                     }
                     fence_proxy_async();                    // the bf16 tile, for the tensor core
                 }
                 mbar_arrive(is_v ? &ms.vfull[seq & 1] : &ms.kfull[seq & 1]);
-            };
-            conv(0, false);
-            if (nt > 1) conv(1, false);
-#pragma unroll 1
-            for (int i = 0; i < nt; ++i) {
-                conv(i, true);
-                if (i + 2 < nt) conv(i + 2, false);
             }
             g += (uint32_t)nt;
         }
