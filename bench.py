@@ -1029,21 +1029,30 @@ def run_reference(args, dist):
     each step = one sequence's decode query through both layers."""
     import oracle
     w = wl.WORKLOADS[args.workload]
+    if not w.kind.endswith("_decode"):
+        return {"impl": "reference", "unavailable": f"the reference arm times the oracle on the decode workloads; "
+                                                    f"{w.name} is a {w.kind} workload"}
+    layers = DEFAULT_LAYERS[w.kind]
+    fmt = {"f32": oracle.KEY_F32, "bf16": oracle.KEY_BF16, "e4m3": oracle.KEY_E4M3, "e2m1": oracle.KEY_E2M1}[w.key_fmt]
     dev = "cuda" if torch.cuda.is_available() else "cpu"
-    nseq = 2
+    nseq = min(2, w.B)
     lens = w.lengths()
     ctx = []
     for b in range(nseq):
         Lb = lens[b]
-        k, v, g = wl.raw_tokens(w, "csa", b, Lb, dev)
-        kin = wl.index_key_inputs(w, "csa", b, Lb // w.m_csa + 1, dev)
-        K, V, G, KIN = (wl.to_numpy(x) for x in (k, v, g, kin))
-        hk, hv, hg = wl.raw_tokens(w, "hca", b, Lb, dev)
-        HK, HV, HG = (wl.to_numpy(x) for x in (hk, hv, hg))
-        ck, cv = oracle.compress(K, V, G, wl.to_numpy(wl.layer_bias(w, "csa", w.m_csa, dev)), w.m_csa, oracle.BF16)
-        codes, sc = oracle.quantize_keys(KIN[: Lb // w.m_csa], oracle.KEY_E2M1)
-        hck, hcv = oracle.compress(HK, HV, HG, wl.to_numpy(wl.layer_bias(w, "hca", w.m_hca, dev)), w.m_hca,
-                                   oracle.BF16)
+        K = V = ck = cv = codes = sc = HK = HV = hck = hcv = None
+        if layers in ("both", "csa"):
+            k, v, g = wl.raw_tokens(w, "csa", b, Lb, dev)
+            kin = wl.index_key_inputs(w, "csa", b, Lb // w.m_csa + 1, dev)
+            K, V, G, KIN = (wl.to_numpy(x) for x in (k, v, g, kin))
+            ck, cv = _oracle_caches(oracle, K, V, G, wl.to_numpy(wl.layer_bias(w, "csa", w.m_csa, dev)), w.m_csa,
+                                    w.kv_cache)
+            codes, sc = oracle.quantize_keys(KIN[: Lb // w.m_csa], fmt)
+        if layers in ("both", "hca"):
+            hk, hv, hg = wl.raw_tokens(w, "hca", b, Lb, dev)
+            HK, HV, HG = (wl.to_numpy(x) for x in (hk, hv, hg))
+            hck, hcv = _oracle_caches(oracle, HK, HV, HG, wl.to_numpy(wl.layer_bias(w, "hca", w.m_hca, dev)),
+                                      w.m_hca, w.kv_cache)
         q = wl.to_numpy(wl.queries(w, "csa", b, 1, dev))
         qh = wl.to_numpy(wl.queries(w, "hca", b, 1, dev))
         qi, ww = (wl.to_numpy(x) for x in wl.indexer_queries(w, "csa", b, 1, dev))
@@ -1051,9 +1060,11 @@ def run_reference(args, dist):
 
     def step(i):
         (Lb, K, V, ck, cv, codes, sc, HK, HV, hck, hcv, q, qh, qi, ww) = ctx[i % len(ctx)]
-        oracle.csa_queries(q, qi, ww, [Lb - 1], ck, cv, codes, sc, oracle.KEY_E2M1, K, V, 0, w.m_csa, w.k, w.W,
-                           w.scale)
-        oracle.hca_queries(qh, [Lb - 1], hck, hcv, HK, HV, 0, w.m_hca, w.W, w.scale)
+        if layers in ("both", "csa"):
+            oracle.csa_queries(q, qi, ww, [Lb - 1], ck, cv, codes, sc, fmt, K, V, 0, w.m_csa, w.k, w.W, w.scale,
+                               q_fp4=w.index_q == "e2m1")
+        if layers in ("both", "hca"):
+            oracle.hca_queries(qh, [Lb - 1], hck, hcv, HK, HV, 0, w.m_hca, w.W, w.scale)
 
     for i in range(args.warmup):
         step(i)
@@ -1063,8 +1074,8 @@ def run_reference(args, dist):
     dt = time.perf_counter() - t0
     value = args.steps / dt
     cpu = {"value": round(value, 4), "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
-           "sample": f"each step = one of {nseq} sequences of {w.name}, one decode query through the CSA and HCA "
-                     f"layers (fp64 C oracle, OpenMP); cache construction untimed"}
+           "sample": f"each step = one of {nseq} sequences of {w.name}, one decode query through the workload's "
+                     f"layers ({layers}; fp64 C oracle, OpenMP); cache construction untimed"}
     return {"metric": METRIC, "impl": "reference", "value": round(value, 4), "unit": UNIT, "n_gpus": dist.world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
