@@ -142,6 +142,19 @@ __global__ void __launch_bounds__(kAppendThreads) append_kernel(
     __shared__ float part[kAppendThreads * 8];
     const int b = blockIdx.x;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    // the new tokens bound for the ring: loaded first (they do not depend on the position) when
+    // one pass of the block covers them (a decode step's token), stored at the end
+    const int first = n_new > ring_cap ? n_new - ring_cap : 0;
+    const int vec = d / 8;
+    const int items = (n_new - first) * vec;
+    const bool pre = items <= kAppendThreads;
+    float yk[8], yv[8], yg = 0.0f;
+    if (pre && tid < items) {
+        const int i = first + tid / vec, c = (tid % vec) * 8;
+        load8_rw(k_new + ((int64_t)b * n_new + i) * d + c, yk);
+        load8_rw(v_new + ((int64_t)b * n_new + i) * d + c, yv);
+        if (c == 0) yg = gate_new[(int64_t)b * n_new + i];
+    }
     const int64_t p = pos[b];
     if (p < 0) {
         if (tid == 0) flag_error(err, ERRBIT_BOUNDS);
@@ -261,12 +274,19 @@ __global__ void __launch_bounds__(kAppendThreads) append_kernel(
     }
     // write the last min(n_new, ring_cap) tokens into the ring (32-bit indices: the host checks
     // that n_new * d / 8 fits)
-    const int first = n_new > ring_cap ? n_new - ring_cap : 0;
-    const int vec = d / 8;
     T* wk = ring_k + (int64_t)b * ring_cap * d;
     T* wv = ring_v + (int64_t)b * ring_cap * d;
     const int base = (int)(p % ring_cap);
-    const int items = (n_new - first) * vec;
+    if (pre) {
+        if (tid < items) {
+            const int i = first + tid / vec, c = (tid % vec) * 8;
+            const int64_t slot = (base + i) % ring_cap;
+            store8(wk + slot * d + c, yk);
+            store8(wv + slot * d + c, yv);
+            if (c == 0) ring_gate[(int64_t)b * ring_cap + slot] = yg;
+        }
+        return;
+    }
     for (int it = tid; it < items; it += blockDim.x) {
         const int i = first + it / vec;
         const int c = (it % vec) * 8;

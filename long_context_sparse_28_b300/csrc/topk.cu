@@ -109,13 +109,12 @@ constexpr int kMaxCluster = 8;
 // shared memory: candidates | the cluster's candidates | two histograms | two bitmaps
 constexpr size_t kSelSmem = 2 * (size_t)kCap * 8 + 2 * (size_t)kBins12 * 4 + 2 * (size_t)kSmemWords * 4;
 
-// Appends the elements >= tv of the warp's span [w0, w0 + cnt_n) of `row` to the shared
-// candidate list (16-byte loads when aligned and full, one shared atomic per warp).
-__device__ __forceinline__ void collect_span(const float* __restrict__ row, int64_t w0, int cnt_n, float tv, uint2* cs,
-                                             int* sh_nc, int lane) {
+// The warp's span [w0, w0 + cnt_n) of `row` into registers: lane element e is entry
+// ((e >> 2) * 32 + lane) * 4 + (e & 3) (16-byte loads when aligned and full; -inf past the end).
+__device__ __forceinline__ void load_span(const float* __restrict__ row, int64_t w0, int cnt_n, int lane,
+                                          float (&v)[32]) {
     const float* src = row + w0;
     const bool vec = ((reinterpret_cast<uintptr_t>(src) & 15) == 0) && cnt_n == kWarpSpan;
-    float v[32];
     if (vec) {
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
@@ -131,6 +130,12 @@ __device__ __forceinline__ void collect_span(const float* __restrict__ row, int6
                 v[4 * j + c] = i < cnt_n ? __ldg(src + i) : -INFINITY;
             }
     }
+}
+
+// Appends the elements >= tv of a loaded span to the shared candidate list (one shared atomic per
+// warp).  Candidates are few (about k per row), so their values are read again from the row.
+__device__ __forceinline__ void collect_loaded(const float* __restrict__ row, int64_t w0, int cnt_n, float tv,
+                                               const float (&v)[32], uint2* cs, int* sh_nc, int lane) {
     uint32_t bits = 0;
 #pragma unroll
     for (int e = 0; e < 32; ++e) {
@@ -149,14 +154,53 @@ __device__ __forceinline__ void collect_span(const float* __restrict__ row, int6
     int base = 0;
     if (lane == 0) base = atomicAdd(sh_nc, total);
     base = __shfl_sync(0xffffffffu, base, 0) + incl - mine;
+    while (bits) {
+        const int e = __ffs(bits) - 1;
+        bits &= bits - 1;
+        const int i = ((e >> 2) * 32 + lane) * 4 + (e & 3);
+        if (base < kCap) cs[base] = make_uint2(ordered_key(__ldg(row + w0 + i)), (uint32_t)(w0 + i));
+        ++base;
+    }
+}
+
+// Exclusive block-wide prefix sums of two counts at once (one pass of barriers).
+__device__ __forceinline__ int2 block_exclusive_scan2(int a, int b, int2* sh) {
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    int x = a, y = b;
 #pragma unroll
-    for (int e = 0; e < 32; ++e) {
-        if (bits & (1u << e)) {
-            const int i = ((e >> 2) * 32 + lane) * 4 + (e & 3);
-            if (base < kCap) cs[base] = make_uint2(ordered_key(v[e]), (uint32_t)(w0 + i));
-            ++base;
+    for (int o = 1; o < 32; o <<= 1) {
+        const int xa = __shfl_up_sync(0xffffffffu, x, o), ya = __shfl_up_sync(0xffffffffu, y, o);
+        if (lane >= o) {
+            x += xa;
+            y += ya;
         }
     }
+    if (lane == 31) sh[wid] = make_int2(x, y);
+    __syncthreads();
+    if (wid == 0) {
+        int2 t = (lane < nw) ? sh[lane] : make_int2(0, 0);
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int xa = __shfl_up_sync(0xffffffffu, t.x, o), ya = __shfl_up_sync(0xffffffffu, t.y, o);
+            if (lane >= o) {
+                t.x += xa;
+                t.y += ya;
+            }
+        }
+        if (lane < nw) sh[lane] = t;
+    }
+    __syncthreads();
+    const int2 base = (wid > 0) ? sh[wid - 1] : make_int2(0, 0);
+    const int2 res = make_int2(base.x + x - a, base.y + y - b);
+    __syncthreads();
+    return res;
+}
+
+__device__ __forceinline__ void cluster_arrive_release() {
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait_acquire() {
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
 // Sums bins [0, nb) of `hist` over the CTAs of the cluster (distributed shared memory) into `out`.
@@ -190,8 +234,12 @@ __global__ void __launch_bounds__(kSelThreads, 1) topk_select_kernel(
     __shared__ int sh_res[2];
     __shared__ int sh_nc;
     __shared__ int sh_cnt[2];                          // this CTA's "above" and "equal" counts
+    __shared__ int2 sh_scan2[32];
     const int r = blockIdx.y, P = (int)cl.num_blocks(), p = (int)cl.block_rank();
     const int tid = threadIdx.x, nthr = blockDim.x, lane = tid & 31, warp = tid >> 5, nw = nthr >> 5;
+    // the row's first histogram into shared memory, loaded together with the row's length
+    for (int i = tid; i < kBins12 / 4; i += nthr)
+        reinterpret_cast<uint4*>(hsum)[i] = reinterpret_cast<const uint4*>(hist1 + (int64_t)r * kBins12)[i];
     const int64_t n = min(row_nvis(r, n_vis_arr, q_pos, m, Ncap), min(stride, words * 32));
     int32_t* out = idx_out + (int64_t)r * k;
     uint32_t* hrow = hist1 + (int64_t)r * kBins12;
@@ -212,9 +260,15 @@ __global__ void __launch_bounds__(kSelThreads, 1) topk_select_kernel(
     uint32_t* wr = smem_bits ? swin : win + (int64_t)r * words + w_lo;
     uint32_t* tr = smem_bits ? stie : tie + (int64_t)r * words + w_lo;
     // ---- boundary bin of the top 12 bits (every CTA, from the row's histogram)
-    const uint32_t* h = hist1 + (int64_t)r * kBins12;
+    const uint32_t* h = hsum;
+    // the warp's first span is loaded while the boundary bin is found
+    float vf[32];
+    const int64_t w00 = s_lo + (int64_t)warp * kWarpSpan;
+    const int n00 = (int)max((int64_t)0, min((int64_t)kWarpSpan, s_hi - w00));
+    if (n00 > 0) load_span(row, w00, n00, lane, vf);
     int b1;
     uint32_t above1;
+    __syncthreads();                                  // the histogram copy
     find_bin(h, kBins12, (uint32_t)k, sh_scan, sh_res, &b1, &above1);
     const bool fast = above1 + h[b1] <= (uint32_t)kCap;
     if (tid == 0) sh_nc = 0;
@@ -223,14 +277,21 @@ __global__ void __launch_bounds__(kSelThreads, 1) topk_select_kernel(
     // ---- candidates of the slice (spans of 1024 entries)
     if (fast) {
         const float tv = bin_floor_value(b1);
-        for (int64_t w0 = s_lo + (int64_t)warp * kWarpSpan; w0 < s_hi; w0 += (int64_t)nw * kWarpSpan)
-            collect_span(row, w0, (int)min((int64_t)kWarpSpan, s_hi - w0), tv, cs, &sh_nc, lane);
+        if (n00 > 0) collect_loaded(row, w00, n00, tv, vf, cs, &sh_nc, lane);
+        for (int64_t w0 = w00 + (int64_t)nw * kWarpSpan; w0 < s_hi; w0 += (int64_t)nw * kWarpSpan) {
+            const int cnt = (int)min((int64_t)kWarpSpan, s_hi - w0);
+            float v[32];
+            load_span(row, w0, cnt, lane, v);
+            collect_loaded(row, w0, cnt, tv, v, cs, &sh_nc, lane);
+        }
     }
     __syncthreads();
     const int nc = fast ? min(sh_nc, kCap) : 0;
     if (fast) {
         // ---- every CTA gathers the row's candidates from the cluster and resolves the row alone
         cl.sync();                                  // every candidate list is complete
+        if (p == 0)                                 // every CTA has its copy: clear the row's histogram
+            for (int i = tid; i < kBins12; i += nthr) hrow[i] = 0u;
         int tot = 0;
         for (int q = 0; q < P; ++q) {
             const int nq = min(*cl.map_shared_rank(&sh_nc, q), kCap - tot);   // the row holds <= kCap
@@ -239,6 +300,7 @@ __global__ void __launch_bounds__(kSelThreads, 1) topk_select_kernel(
             tot += nq;
         }
         __syncthreads();
+        cluster_arrive_release();                   // done with the other CTAs' lists (waited at the end)
         // bits 19..8 and 7..0 of the boundary bin's members
         for (int i = tid; i < tot; i += nthr) {
             const uint32_t key = ga[i].x;
@@ -303,11 +365,11 @@ __global__ void __launch_bounds__(kSelThreads, 1) topk_select_kernel(
             nwin += __popc(wr[w]);
             ntie += __popc(tr[w]);
         }
-        int tot_tie, tot_sel;
-        const int tie_before_local = block_exclusive_scan(ntie, sh_scan, &tot_tie);
-        const int take = max(0, min(my_ties - tie_before_local, ntie));
-        const int pos0 = block_exclusive_scan(nwin + take, sh_scan, &tot_sel);
-        int pos = out_off + pos0, rem = take;
+        // the first my_ties ties of the slice in index order are taken: the takes before a thread
+        // add up to min(my_ties, ties before it)
+        const int2 before = block_exclusive_scan2(nwin, ntie, sh_scan2);
+        const int take = max(0, min(my_ties - before.y, ntie));
+        int pos = out_off + before.x + min(my_ties, before.y), rem = take;
         for (int64_t w = v0; w < v1; ++w) {
             uint32_t t = tr[w];
             uint32_t tsel = 0;
@@ -325,9 +387,7 @@ __global__ void __launch_bounds__(kSelThreads, 1) topk_select_kernel(
                 bits &= bits - 1;
             }
         }
-        cl.sync();                                  // the others have finished reading this CTA's list
-        if (p == 0)                                 // every CTA has read the histogram: clear it
-            for (int i = tid; i < kBins12; i += nthr) hrow[i] = 0u;
+        cluster_wait_acquire();                     // the others have finished reading this CTA's list
         return;
     }
     // ---- the slow path: the boundary bin holds too many entries for the candidate lists; every
