@@ -374,8 +374,8 @@ def _elapsed_ms(a, b):
 _SHARED_SOURCES = ["common.cuh", "tc_ptx.cuh", "tmap.cuh", "tmap.cu", "runtime.cu"]
 CALL_SOURCES = {
     "csa_index_topk": ["indexer.cu", "indexer_tc.cu", "topk.cu", "quant.cuh"] + _SHARED_SOURCES,
-    "hca_attend": ["attend.cu", "attend_tc.cu", "attend.cuh"] + _SHARED_SOURCES,
-    "csa_attend": ["attend.cu", "attend_tc.cu", "attend.cuh"] + _SHARED_SOURCES,
+    "hca_attend": ["attend.cu", "attend_tc.cu", "attend.cuh", "quant.cuh"] + _SHARED_SOURCES,
+    "csa_attend": ["attend.cu", "attend_tc.cu", "attend.cuh", "quant.cuh"] + _SHARED_SOURCES,
 }
 
 
