@@ -79,6 +79,7 @@ struct Smem {
 struct alignas(16) Misc {
     uint64_t kfull[2], vfull[2], sdone[2], odone, pready;
     uint64_t k8full[2], v8full[2];   // FP8 caches: a tile's codes have landed (before conversion)
+    uint64_t mfull;                  // the row merge's partials have landed in shared memory
     uint32_t tmem_base;
     int flag[2];                     // per tile (ring of 2): some running maximum moved
     alignas(16) float red[16][32];
@@ -391,100 +392,90 @@ __device__ __forceinline__ void convert_v_f8(uint32_t slot, uint32_t vsc, int t)
         sts128(slot + (j >> 3) * kHalf + sw128(t, j & 7), e4m3x8_to_bf16x8(w[2 * j], w[2 * j + 1], j < 8 ? sc0 : sc1));
 }
 
-// The row's last item merges the row's partial results: see arrive_and_merge in the kernel.
-// Out of line: it runs once per row and keeps its registers out of the tile loop's allocation.
+// The row's last item merges the row's partial results (see arrive_and_merge in the kernel): up to
+// kMergeStage slots at a time, one thread bulk-copies the slots' partial outputs (32 KB each,
+// contiguous) and log-sum-exps into shared memory -- the tile buffers, idle once the item's MMAs
+// are complete -- so a pass costs one round trip; one thread per head then forms the maxima,
+// sums (rescaled across passes) and weights, and every thread adds its units (4 dims of one head)
+// over the slots.  Out of line: it runs once per row and keeps its registers out of the tile
+// loop's allocation.
+constexpr int kMergeStage = 6;   // 6 x 32 KB of partial outputs in [L::p, L::total)
+
 template <int H>
 __device__ __noinline__ void merge_row(int r, int ns, int S, const float* __restrict__ lse_part,
                                        const float* __restrict__ o_part, __nv_bfloat16* __restrict__ out,
-                                       float* __restrict__ lse_out, Misc& ms, int tid) {
+                                       float* __restrict__ lse_out, Misc& ms, int tid, uint32_t stage,
+                                       uint32_t& mpass, unsigned* err) {
     constexpr int kSoft = Thr<H>::kSoft;
+    constexpr uint32_t kSlotBytes = H * kD * 4;
+    static_assert(kMergeStage * kSlotBytes <= Smem<H>::total - Smem<H>::p, "merge staging fits the tile buffers");
+    static_assert(kMergeStage <= kMergeSlots, "lse staging");
+    constexpr int kUnits = H * (kD / 4) / kSoft;   // units per thread (4)
     const float* lrow = lse_part + (int64_t)r * S * H;
     const float* orow = o_part + (int64_t)r * S * H * kD;
-    // Every slot [0, ns) holds a finite partial (zeros where it has no keys), so the loads of
-    // the partial outputs need no weights: kMergeSlots slots at a time, their lse into shared
-    // memory and their outputs into registers (units of 4 dims of one head, consecutive
-    // threads on consecutive dims, kMB slots per batch) are issued together; then one
-    // thread per head forms the maxima and sums (rescaled across passes), and the weighted
-    // sums follow.
-    constexpr int kUnits = H * (kD / 4) / kSoft;   // units per thread (4)
-    constexpr int kMB = H == 64 ? 2 : 4;           // slots per batch (registers)
     float4 acc[kUnits];
 #pragma unroll
     for (int u = 0; u < kUnits; ++u) acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
     float mx = -INFINITY, tot = 0.0f;              // per head (threads tid < H)
-    for (int s0 = 0; s0 < ns; s0 += kMergeSlots) {
-        const int nsl = min(kMergeSlots, ns - s0);
-        for (int i = tid; i < nsl * H; i += kSoft) ms.mw[i] = __ldcg(lrow + (int64_t)s0 * H + i);
-        for (int sl = 0; sl < nsl; sl += kMB) {
-            float4 v[kMB][kUnits];
-#pragma unroll
-            for (int j = 0; j < kMB; ++j)
-#pragma unroll
-                for (int u = 0; u < kUnits; ++u) {
-                    const int unit = tid + u * kSoft, hh = unit / (kD / 4), c4 = unit % (kD / 4);
-                    v[j][u] = sl + j < nsl ? __ldcg(reinterpret_cast<const float4*>(
-                                                       orow + ((int64_t)(s0 + sl + j) * H + hh) * kD) + c4)
-                                           : make_float4(0.f, 0.f, 0.f, 0.f);
-                }
-            if (sl == 0) {
-                // this pass's maxima, sums and weights (the loads above are in flight)
-                named_barrier_sync(1, kSoft);
-                if (tid < H) {
-                    float m2 = mx;
-                    for (int q = 0; q < nsl; ++q) m2 = fmaxf(m2, ms.mw[q * H + tid]);
-                    const float rs = (m2 == -INFINITY) ? 0.0f : expf(mx - m2);   // 0 on the first pass
-                    tot *= rs;
-                    for (int q = 0; q < nsl; ++q) {
-                        const float ls = ms.mw[q * H + tid];
-                        const float e = ls == -INFINITY ? 0.0f : expf(ls - m2);
-                        tot += e;
-                        ms.mw[q * H + tid] = e;
-                    }
-                    mx = m2;
-                    ms.alpha[tid] = rs;
-                }
-                named_barrier_sync(1, kSoft);
-#pragma unroll
-                for (int u = 0; u < kUnits; ++u) {   // earlier passes' sums move to the new maxima
-                    const float rs = ms.alpha[(tid + u * kSoft) / (kD / 4)];
-                    acc[u].x *= rs;
-                    acc[u].y *= rs;
-                    acc[u].z *= rs;
-                    acc[u].w *= rs;
-                }
-            }
-#pragma unroll
-            for (int j = 0; j < kMB; ++j)
-#pragma unroll
-                for (int u = 0; u < kUnits; ++u) {
-                    const float wgt = sl + j < nsl ? ms.mw[(sl + j) * H + (tid + u * kSoft) / (kD / 4)] : 0.0f;
-                    acc[u].x = fmaf(wgt, v[j][u].x, acc[u].x);
-                    acc[u].y = fmaf(wgt, v[j][u].y, acc[u].y);
-                    acc[u].z = fmaf(wgt, v[j][u].z, acc[u].z);
-                    acc[u].w = fmaf(wgt, v[j][u].w, acc[u].w);
-                }
+    for (int s0 = 0; s0 < ns; s0 += kMergeStage) {
+        const int nsl = min(kMergeStage, ns - s0);
+        if (tid == 0) {
+            fence_proxy_async();                       // the partials, for the bulk copies
+            mbar_arrive_expect_tx(&ms.mfull, (uint32_t)nsl * (kSlotBytes + H * 4));
+            for (int q = 0; q < nsl; ++q)
+                bulk_g2s(stage + q * kSlotBytes, orow + (int64_t)(s0 + q) * H * kD, kSlotBytes, &ms.mfull);
+            bulk_g2s(smem_u32(ms.mw), lrow + (int64_t)s0 * H, (uint32_t)nsl * H * 4, &ms.mfull);
         }
-        named_barrier_sync(1, kSoft);              // ms.mw is reused by the next pass
+        mbar_wait(&ms.mfull, mpass & 1, err);
+        ++mpass;
+        if (tid < H) {
+            float m2 = mx;
+            for (int q = 0; q < nsl; ++q) m2 = fmaxf(m2, ms.mw[q * H + tid]);
+            const float rs = (m2 == -INFINITY) ? 0.0f : expf(mx - m2);   // 0 on the first pass
+            tot *= rs;
+            for (int q = 0; q < nsl; ++q) {
+                const float ls = ms.mw[q * H + tid];
+                const float e = ls == -INFINITY ? 0.0f : expf(ls - m2);
+                tot += e;
+                ms.mw[q * H + tid] = e;
+            }
+            mx = m2;
+            ms.alpha[tid] = rs;
+        }
+        named_barrier_sync(1, kSoft);
+#pragma unroll
+        for (int u = 0; u < kUnits; ++u) {
+            const int unit = tid + u * kSoft, hh = unit / (kD / 4), c4 = unit % (kD / 4);
+            const float rs = ms.alpha[hh];
+            float4 a4 = make_float4(acc[u].x * rs, acc[u].y * rs, acc[u].z * rs, acc[u].w * rs);
+            for (int q = 0; q < nsl; ++q) {
+                const float wgt = ms.mw[q * H + hh];
+                float4 v;
+                asm volatile("ld.shared.v4.f32 {%0,%1,%2,%3}, [%4];"
+                             : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                             : "r"(stage + q * kSlotBytes + (uint32_t)(hh * kD + c4 * 4) * 4));
+                a4.x = fmaf(wgt, v.x, a4.x);
+                a4.y = fmaf(wgt, v.y, a4.y);
+                a4.z = fmaf(wgt, v.z, a4.z);
+                a4.w = fmaf(wgt, v.w, a4.w);
+            }
+            acc[u] = a4;
+        }
+        named_barrier_sync(1, kSoft);                  // the staging is reused by the next pass
     }
     if (tid < H) {
         ms.linv[tid] = tot > 0.0f ? 1.0f / tot : 0.0f;
         if (lse_out) lse_out[(int64_t)r * H + tid] = tot > 0.0f ? mx + logf(tot) : -INFINITY;
     }
     named_barrier_sync(1, kSoft);
-#pragma unroll
-    for (int u = 0; u < kUnits; ++u) {
-        const float li = ms.linv[(tid + u * kSoft) / (kD / 4)];
-        acc[u].x *= li;
-        acc[u].y *= li;
-        acc[u].z *= li;
-        acc[u].w *= li;
-    }
+    fence_proxy_async();              // the staging reads, before the next item's copies into the buffers
     __nv_bfloat16* orow_out = out + (int64_t)r * H * kD;
 #pragma unroll
     for (int u = 0; u < kUnits; ++u) {
         const int unit = tid + u * kSoft;
+        const float li = ms.linv[unit / (kD / 4)];
         reinterpret_cast<uint2*>(orow_out)[unit] =
-            make_uint2(pack_bf16x2(acc[u].x, acc[u].y), pack_bf16x2(acc[u].z, acc[u].w));
+            make_uint2(pack_bf16x2(acc[u].x * li, acc[u].y * li), pack_bf16x2(acc[u].z * li, acc[u].w * li));
     }
 }
 
@@ -519,6 +510,7 @@ __global__ void __launch_bounds__(Thr<H, F8>::kThreads, 1)
         }
         mbar_init(&ms.odone, 1);
         mbar_init(&ms.pready, kSoft / 32);
+        mbar_init(&ms.mfull, 1);
         fence_mbar_init();
     }
     pdl_wait();
@@ -693,7 +685,8 @@ __global__ void __launch_bounds__(Thr<H, F8>::kThreads, 1)
         // cumulative over the barrier); the row's last item merges the row's partial results
         // exactly, slots s = 0, 1, ... in that order (slots with lse = -inf hold no keys):
         //     lse = log sum_s exp(lse_s),  o = sum_s exp(lse_s - lse) o_s,
-        // and resets the counter.  The partials of other CTAs are read through L2 (ld.global.cg).
+        // and resets the counter (merge_row).
+        uint32_t mpass = 0;                         // merge passes so far (the mfull barrier's phase)
         auto arrive_and_merge = [&](const ItemTiles& itm) {
             named_barrier_sync(1, kSoft);
             if (tid == 0) {
@@ -705,7 +698,7 @@ __global__ void __launch_bounds__(Thr<H, F8>::kThreads, 1)
             named_barrier_sync(1, kSoft);
             if (!ms.merge_now) return;
             merge_row<H>(itm.r, itm.expect, S, lse_part, o_part, static_cast<__nv_bfloat16*>(a.out), a.lse, ms,
-                         tid);
+                         tid, sbase + L::p, mpass, err);
             if (tid == 0) row_cnt[itm.r] = 0u;             // ready for the next call
         };
         ItemTiles it;
