@@ -278,16 +278,19 @@ csahca_status attend_run(const AttendArgs& a, int splits_req, void* workspace, s
         e = attend_tc_launch(a, sp.S, sp.kps, o_part, lse_part, row_cnt, err, st);
         count_launch();
         if (e != cudaSuccess) return CSAHCA_ERR_CUDA;
-        CSAHCA_CHECK_LAUNCH();
-        return CSAHCA_OK;
-    }
-    if (a.dtype == CSAHCA_F32) {
-        e = dispatch_generic<float>(a, sp.S, sp.kps, o_part, lse_part, err, st);
+        if (attend_tc_merges(a, sp.S)) {
+            CSAHCA_CHECK_LAUNCH();
+            return CSAHCA_OK;
+        }
     } else {
-        e = dispatch_generic<__nv_bfloat16>(a, sp.S, sp.kps, o_part, lse_part, err, st);
+        if (a.dtype == CSAHCA_F32) {
+            e = dispatch_generic<float>(a, sp.S, sp.kps, o_part, lse_part, err, st);
+        } else {
+            e = dispatch_generic<__nv_bfloat16>(a, sp.S, sp.kps, o_part, lse_part, err, st);
+        }
+        count_launch();
+        if (e != cudaSuccess) return CSAHCA_ERR_CUDA;
     }
-    count_launch();
-    if (e != cudaSuccess) return CSAHCA_ERR_CUDA;
     const unsigned mgrid = (unsigned)cdiv((int64_t)R * a.H, kMergeWarps);
     if (a.dtype == CSAHCA_F32)
         (void)launch_pdl(merge_kernel<float>, dim3(mgrid), dim3(32 * kMergeWarps), 0, st, R, sp.S, a.H, a.d, o_part, lse_part, (float*)a.out,

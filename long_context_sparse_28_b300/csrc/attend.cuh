@@ -109,6 +109,8 @@ csahca_status attend_run(const AttendArgs& a, int splits_req, void* workspace, s
 
 // Tensor-core path (bf16, d = 128): availability and launch of the split kernel.
 bool attend_tc_supported(const AttendArgs& a);
+// True when the tensor-core kernel merges the rows' partials itself (few query rows).
+bool attend_tc_merges(const AttendArgs& a, int S);
 // The kernel also merges each row's partials into a.out / a.lse (the row's last CTA, counted in
 // row_cnt), so no merge launch follows it.
 cudaError_t attend_tc_launch(const AttendArgs& a, int S, int kps, float* o_part, float* lse_part, unsigned* row_cnt,

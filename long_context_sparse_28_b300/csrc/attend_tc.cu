@@ -713,7 +713,7 @@ __global__ void __launch_bounds__(Thr<H, F8>::kThreads, 1)
 #pragma unroll 1
                 for (int i = tid; i < H * kD; i += kSoft) o_part[obase * kD + i] = 0.0f;
                 if (tid < H) lse_part[obase + tid] = -INFINITY;
-                arrive_and_merge(it);
+                if (pieces) arrive_and_merge(it);
                 continue;
             }
             if (tid < H) ms.mrun[tid] = -INFINITY;
@@ -956,7 +956,8 @@ __global__ void __launch_bounds__(Thr<H, F8>::kThreads, 1)
                 }
             }
             fence_before_sync();
-            arrive_and_merge(it);
+            if (pieces) arrive_and_merge(it);
+            else named_barrier_sync(1, kSoft);
         }
     }
     __syncwarp();
@@ -1022,6 +1023,16 @@ cudaError_t launch_tc(const AttendArgs& a, int S, int kps, float* o_part, float*
 }
 
 }  // namespace
+
+bool attend_tc_merges(const AttendArgs& a, int S) {
+    // the kernel's piece schedule (few rows) merges in the row's last CTA; with many rows every
+    // CTA takes (row, split) items and the shared merge kernel follows (it spreads the merges of
+    // many rows over the whole GPU)
+    const int R = a.B * a.T;
+    const int items = R * S;
+    const int grid = items < num_sms() ? items : num_sms();
+    return R <= kSchedRows && R <= grid && S >= 2;
+}
 
 bool attend_tc_supported(const AttendArgs& a) {
     return (a.dtype == CSAHCA_BF16 || a.dtype == CSAHCA_KV_FP8) && a.d == 128 && (a.H == 32 || a.H == 64) &&

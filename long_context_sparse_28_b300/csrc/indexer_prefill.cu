@@ -231,14 +231,12 @@ __global__ void __launch_bounds__(kThreadsP, 1) index_prefill_kernel(
 #pragma unroll
                 for (int j = 0; j < QR / 2; ++j) {
                     const int row = hh * (QR / 2) + j;
-                    if (key < nv[j]) S[(int64_t)(r0 + row) * Ncap + key] = sc[j];
-                    if (hist1 != nullptr) {
-                        // lanes holding the same bin add their count once (shared atomics on one
-                        // address serialise)
-                        const uint32_t bin = key < nv[j] ? ordered_key(sc[j]) >> 20 : 0xFFFFFFFFu;
-                        const uint32_t peers = __match_any_sync(0xffffffffu, bin);
-                        if (bin != 0xFFFFFFFFu && lane == __ffs(peers) - 1)
-                            atomicAdd(&hist[row * 2048 + (bin >> 1)], (uint32_t)__popc(peers) << ((bin & 1) * 16));
+                    if (key < nv[j]) {
+                        S[(int64_t)(r0 + row) * Ncap + key] = sc[j];
+                        if (hist1 != nullptr) {
+                            const uint32_t bin = ordered_key(sc[j]) >> 20;
+                            atomicAdd(&hist[row * 2048 + (bin >> 1)], 1u << ((bin & 1) * 16));
+                        }
                     }
                 }
             }
