@@ -17,6 +17,34 @@ namespace {
 
 constexpr int kMaxM = 256;
 
+// Stores that ask L2 to keep the line (evict-last): the window ring is small and read again by the
+// attention of every step and by the pooling of the next block, while a step streams hundreds of
+// megabytes of caches through L2.
+__device__ __forceinline__ uint64_t keep_policy() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+__device__ __forceinline__ void st_keep(void* ptr, uint4 u, uint64_t pol) {
+    asm volatile("st.global.L2::cache_hint.v4.b32 [%0], {%1,%2,%3,%4}, %5;" ::"l"(ptr), "r"(u.x), "r"(u.y), "r"(u.z),
+                 "r"(u.w), "l"(pol)
+                 : "memory");
+}
+__device__ __forceinline__ void store8_keep(__nv_bfloat16* p, const float (&v)[8], uint64_t pol) {
+    st_keep(p, make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]),
+                          pack_bf16x2(v[6], v[7])),
+            pol);
+}
+__device__ __forceinline__ void store8_keep(float* p, const float (&v)[8], uint64_t pol) {
+    st_keep(p, make_uint4(__float_as_uint(v[0]), __float_as_uint(v[1]), __float_as_uint(v[2]), __float_as_uint(v[3])),
+            pol);
+    st_keep(p + 4, make_uint4(__float_as_uint(v[4]), __float_as_uint(v[5]), __float_as_uint(v[6]), __float_as_uint(v[7])),
+            pol);
+}
+__device__ __forceinline__ void st_keep_f32(float* ptr, float v, uint64_t pol) {
+    asm volatile("st.global.L2::cache_hint.b32 [%0], %1, %2;" ::"l"(ptr), "r"(__float_as_uint(v)), "l"(pol) : "memory");
+}
+
 // Softmax weights of one block, distributed over the warp: lane holds alpha of slots
 // lane + 32*r (r < 8).  `zsrc(i)` returns gate_i + bias_i.
 template <typename Z>
@@ -155,6 +183,16 @@ __global__ void __launch_bounds__(kAppendThreads) append_kernel(
         load8_rw(v_new + ((int64_t)b * n_new + i) * d + c, yv);
         if (c == 0) yg = gate_new[(int64_t)b * n_new + i];
     }
+    // warp 0, for blocks of m <= 32 tokens: the sequence's ring gates (4 slots per lane) and the slot
+    // biases, also loaded before the position is known
+    const bool small_m = m <= 32 && ring_cap <= 128;
+    float rg4[4] = {0.f, 0.f, 0.f, 0.f}, bz = 0.0f;
+    if (warp == 0 && small_m) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+            if (lane * 4 + c < ring_cap) rg4[c] = ring_gate[(int64_t)b * ring_cap + lane * 4 + c];
+        if (lane < m) bz = bias[lane];
+    }
     const int64_t p = pos[b];
     if (p < 0) {
         if (tid == 0) flag_error(err, ERRBIT_BOUNDS);
@@ -206,7 +244,24 @@ __global__ void __launch_bounds__(kAppendThreads) append_kernel(
             const char* row = static_cast<const char*>(kidx_new) + (((int64_t)b * kidx_rows + r) * d_I) * in_bytes;
             load_row_slice(row, kidx_dtype, d_I / 32, kx);
         }
-        if (warp == 0) {
+        if (warp == 0 && small_m) {
+            // lane i < m: slot i's logit, the ring's gate taken from the preloaded registers
+            const int64_t t = t0 + lane;
+            int sl = t0r + (lane < m ? lane : 0);
+            if (sl >= ring_cap) sl -= ring_cap;
+            float g = 0.0f;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const float x = __shfl_sync(0xffffffffu, rg4[c], sl >> 2);
+                if ((sl & 3) == c) g = x;
+            }
+            if (lane < m && t >= p) g = gn[t - p];
+            const float z = lane < m ? g + bz : -INFINITY;
+            const float zmax = warp_max(z);
+            const float e = lane < m ? expf(z - zmax) : 0.0f;
+            const float zs = warp_sum(e);
+            if (lane < m) alpha[lane] = e / zs;
+        } else if (warp == 0) {
             float a[8];
             block_weights(m, [&](int i) {
                 const int64_t t = t0 + i;
@@ -279,11 +334,12 @@ __global__ void __launch_bounds__(kAppendThreads) append_kernel(
     const int base = (int)(p % ring_cap);
     if (pre) {
         if (tid < items) {
+            const uint64_t pol = keep_policy();
             const int i = first + tid / vec, c = (tid % vec) * 8;
             const int64_t slot = (base + i) % ring_cap;
-            store8(wk + slot * d + c, yk);
-            store8(wv + slot * d + c, yv);
-            if (c == 0) ring_gate[(int64_t)b * ring_cap + slot] = yg;
+            store8_keep(wk + slot * d + c, yk, pol);
+            store8_keep(wv + slot * d + c, yv, pol);
+            if (c == 0) st_keep_f32(ring_gate + (int64_t)b * ring_cap + slot, yg, pol);
         }
         return;
     }
