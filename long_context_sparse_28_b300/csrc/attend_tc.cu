@@ -55,12 +55,7 @@ template <int H, bool F8 = false>
 struct Thr {
     static_assert(H % kHG == 0, "heads in groups of 16");
     static constexpr int kSoft = (H / kHG) * kKeys;
-    // FP8 caches: converter threads -- one warp for K tiles (four rows each), two for V tiles (two
-    // rows each); 3 warps keep the block at a multiple of 4 warps (the register budget of H = 64)
-    static constexpr int kConvK = F8 ? 32 : 0;
-    static constexpr int kConvV = F8 ? 64 : 0;
-    static constexpr int kConv = kConvK + kConvV;
-    static constexpr int kThreads = kSoft + 32 + kConv;
+    static constexpr int kThreads = kSoft + 32;
 };
 
 template <int H>
@@ -366,30 +361,58 @@ __device__ __forceinline__ void sts128(uint32_t addr, uint4 u) {
     asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(u.x), "r"(u.y), "r"(u.z), "r"(u.w) : "memory");
 }
 
-// Row t of a K tile: codes and scale (dense row t of the first half) -> bf16 dims 0..63 in place.
-__device__ __forceinline__ void convert_k_f8(uint32_t slot, int t) {
-    uint4 c[5];
+// Part `pt` (of kTpr) of row r of a K tile: its codes (the staged dense row r of the first half)
+// -> bf16 in place.  The kTpr threads of a row sit in one warp: every one reads its codes and the
+// scale byte, then (after __syncwarp) writes its chunks of the row.
+template <int kTpr>
+__device__ __forceinline__ void convert_k_part(uint32_t slot, int r, int pt) {
+    constexpr int kU = 64 / 16 / kTpr;                  // 16-code pieces per part
+    uint4 c[kU];
 #pragma unroll
-    for (int i = 0; i < 5; ++i) c[i] = lds128(slot + t * 128 + i * 16);
-    const float sc = ue8m0_to_f32(c[4].x & 0xFFu);
-    const uint32_t* w = reinterpret_cast<const uint32_t*>(c);
+    for (int i = 0; i < kU; ++i) c[i] = lds128(slot + r * 128 + (pt * kU + i) * 16);
+    uint32_t sb;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(sb) : "r"(slot + r * 128 + 64));
+    __syncwarp();
+    const float sc = ue8m0_to_f32(sb & 0xFFu);
 #pragma unroll
-    for (int j = 0; j < 8; ++j) sts128(slot + sw128(t, j), e4m3x8_to_bf16x8(w[2 * j], w[2 * j + 1], sc));
+    for (int i = 0; i < kU; ++i) {
+        const int j = 2 * (pt * kU + i);                // output chunks j, j + 1 (8 dims each)
+        sts128(slot + sw128(r, j), e4m3x8_to_bf16x8(c[i].x, c[i].y, sc));
+        sts128(slot + sw128(r, j + 1), e4m3x8_to_bf16x8(c[i].z, c[i].w, sc));
+    }
 }
 
-// Row t of a V tile: codes (dense row t of the second half) and scales -> bf16 dims 0..63 (first
-// half) and 64..127 (second half, in place).
-__device__ __forceinline__ void convert_v_f8(uint32_t slot, uint32_t vsc, int t) {
-    uint4 c[8];
+// Part `pt` of row r of a V tile: codes (the staged dense row r of the second half) and scales ->
+// bf16 dims 0..63 (first half) and 64..127 (second half), or zeros for a row that holds no key.
+template <int kTpr>
+__device__ __forceinline__ void convert_v_part(uint32_t slot, uint32_t vsc, int r, int pt, bool zero) {
+    constexpr int kU = 128 / 16 / kTpr;
+    uint4 c[kU];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) c[i] = lds128(slot + kHalf + t * 128 + i * 16);
+    for (int i = 0; i < kU; ++i) c[i] = lds128(slot + kHalf + r * 128 + (pt * kU + i) * 16);
     uint32_t sb;
-    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(sb) : "r"(vsc + t * 16));
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(sb) : "r"(vsc + r * 16));
+    __syncwarp();
     const float sc0 = ue8m0_to_f32(sb & 0xFFu), sc1 = ue8m0_to_f32((sb >> 8) & 0xFFu);
-    const uint32_t* w = reinterpret_cast<const uint32_t*>(c);
 #pragma unroll
-    for (int j = 0; j < 16; ++j)
-        sts128(slot + (j >> 3) * kHalf + sw128(t, j & 7), e4m3x8_to_bf16x8(w[2 * j], w[2 * j + 1], j < 8 ? sc0 : sc1));
+    for (int i = 0; i < kU; ++i) {
+        const int j = 2 * (pt * kU + i);                // output chunks j, j + 1 of the row's 16
+        const float sc = j < 8 ? sc0 : sc1;
+        const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+        sts128(slot + (j >> 3) * kHalf + sw128(r, j & 7), zero ? z : e4m3x8_to_bf16x8(c[i].x, c[i].y, sc));
+        sts128(slot + ((j + 1) >> 3) * kHalf + sw128(r, (j + 1) & 7), zero ? z : e4m3x8_to_bf16x8(c[i].z, c[i].w, sc));
+    }
+}
+
+// Part `pt` of row r of a bf16 V tile: zeros (a row that holds no key of the query).
+template <int kTpr>
+__device__ __forceinline__ void zero_v_part(uint32_t slot, int r, int pt) {
+    constexpr int kC = 16 / kTpr;
+#pragma unroll
+    for (int i = 0; i < kC; ++i) {
+        const int j = pt * kC + i;
+        sts128(slot + (j >> 3) * kHalf + sw128(r, j & 7), make_uint4(0u, 0u, 0u, 0u));
+    }
 }
 
 // The row's last item merges the row's partial results (see arrive_and_merge in the kernel): up to
@@ -500,9 +523,10 @@ __global__ void __launch_bounds__(Thr<H, F8>::kThreads, 1)
     }
     if (tid == 32) {
         for (int i = 0; i < 2; ++i) {
-            // FP8 caches: the loads complete on k8full / v8full and the converters release the tiles
-            mbar_init(&ms.kfull[i], F8 ? Thr<H, F8>::kConvK : kSoft);
-            mbar_init(&ms.vfull[i], F8 ? Thr<H, F8>::kConvV : kSoft);
+            // FP8 caches: the loads complete on k8full / v8full; the softmax warps expand the codes
+            // and release each tile (one arrival per warp)
+            mbar_init(&ms.kfull[i], F8 ? kSoft / 32 : kSoft);
+            mbar_init(&ms.vfull[i], F8 ? kSoft / 32 : kSoft);
             mbar_init(&ms.k8full[i], kSoft);
             mbar_init(&ms.v8full[i], kSoft);
             mbar_init(&ms.sdone[i], 1);
@@ -633,38 +657,6 @@ __global__ void __launch_bounds__(Thr<H, F8>::kThreads, 1)
             }
         }
         __syncwarp();
-    } else if (F8 && warp > kSoft / 32) {
-        // ======================================================= converter warps (FP8 caches)
-        // Two in-order streams, so a late V tile never holds up the next K tile: the K warp takes
-        // K(0), K(1), ..., the V warps V(0), V(1), ...; each tile's codes are waited for, written out
-        // as bf16 in place (compressed tiles; window tiles are bf16 already) and released to the
-        // MMA warp.
-        const int t = tid - (kSoft + 32);
-        const bool is_v = t >= Thr<H, F8>::kConvK;
-        const int t0r = is_v ? t - Thr<H, F8>::kConvK : t;
-        const int step = is_v ? Thr<H, F8>::kConvV : Thr<H, F8>::kConvK;
-        uint32_t g = 0;
-        ItemTiles it;
-        for (int cur = cur0; next_item(cur, it);) {
-            const int nt = it.nt;
-#pragma unroll 1
-            for (int i = 0; i < nt; ++i) {
-                const uint32_t seq = g + (uint32_t)i;
-                mbar_wait(is_v ? &ms.v8full[seq & 1] : &ms.k8full[seq & 1], (seq >> 1) & 1, err);
-                if (it.t0 + i < it.nt_c) {
-                    const uint32_t slot = sbase + (is_v ? L::v : L::k) + (seq & 1) * kTile;
-                    const uint32_t vsc = sbase + L::total + (seq & 1) * kVScale;
-#pragma unroll 1
-                    for (int rr = t0r; rr < kKeys; rr += step) {
-                        if (is_v) convert_v_f8(slot, vsc, rr);
-                        else convert_k_f8(slot, rr);
-                    }
-                    fence_proxy_async();                    // the bf16 tile, for the tensor core
-                }
-                mbar_arrive(is_v ? &ms.vfull[seq & 1] : &ms.kfull[seq & 1]);
-            }
-            g += (uint32_t)nt;
-        }
     } else {
         // ==================================================================== softmax warps
         constexpr int HG = kHG;                     // heads per warpgroup
@@ -734,6 +726,28 @@ __global__ void __launch_bounds__(Thr<H, F8>::kThreads, 1)
                                      dst, bar, ms.valid[seq & 3], qr, pol_stream, i == 0 && !is_v, err);
             };
 
+            // FP8 caches: tile i's codes -> bf16 in place by the softmax warps, then the tile is
+            // released to the MMA warp (K: before MMA1 needs it; V: with the tile's zeroing of rows
+            // that hold no key, before PV)
+            constexpr int kTpr = kSoft / kKeys;
+            auto conv = [&](int i, bool is_v, bool zero_invalid) {
+                const uint32_t seq = g + (uint32_t)i;
+                mbar_wait(is_v ? &ms.v8full[seq & 1] : &ms.k8full[seq & 1], (seq >> 1) & 1, err);
+                const uint32_t slot = sbase + (is_v ? L::v : L::k) + (seq & 1) * kTile;
+                const int cr = tid / kTpr, cp = tid % kTpr;
+                const bool zr = zero_invalid && ms.valid[seq & 3][cr] == 0;
+                if (t0 + i < nt_c) {
+                    if (is_v) convert_v_part<kTpr>(slot, sbase + L::total + (seq & 1) * kVScale, cr, cp, zr);
+                    else convert_k_part<kTpr>(slot, cr, cp);
+                } else if (is_v && zr) {
+                    zero_v_part<kTpr>(slot, cr, cp);
+                }
+                fence_proxy_async();
+                fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(is_v ? &ms.vfull[seq & 1] : &ms.kfull[seq & 1]);
+            };
+
             // ---- prologue: Q, K(0), K(1), V(0) in flight (K(0) completes only once Q has landed)
             for (int c = tid; c < H * 16; c += kSoft) {
                 const int h = c >> 4, cc = c & 15;
@@ -743,6 +757,7 @@ __global__ void __launch_bounds__(Thr<H, F8>::kThreads, 1)
             if (nt > 1) load(1, false);
             load(0, true);
             named_barrier_sync(1, kSoft);                  // valid[] of tiles 0 and 1
+            if constexpr (F8) conv(0, false, false);
 
             float lsum[HG];
 #pragma unroll
@@ -752,6 +767,8 @@ __global__ void __launch_bounds__(Thr<H, F8>::kThreads, 1)
             for (int i = 0; i < nt; ++i) {
                 const uint32_t seq = g + (uint32_t)i;
                 const int ti = t0 + i;
+                if constexpr (F8)
+                    if (i + 1 < nt) conv(i + 1, false, false);   // K(i+1): loaded one tile ago
                 mbar_wait(&ms.sdone[seq & 1], (seq >> 1) & 1, err);
                 fence_after_sync();
                 // Each thread holds one key row of this warpgroup's 16 heads (raw scores; rows that
@@ -901,7 +918,9 @@ __global__ void __launch_bounds__(Thr<H, F8>::kThreads, 1)
                 const bool comp = ti < nt_c;
                 const bool vzero = comp ? (use_tma_c && (int64_t)(ti + 1) * kKeys > kl.n_c)
                                         : (use_tma_w && p < kKeys - 1);
-                if (vzero) {
+                if constexpr (F8) {
+                    conv(i, true, vzero);
+                } else if (vzero) {
                     mbar_wait(&ms.vfull[seq & 1], (seq >> 1) & 1, err);
                     if (tid < kKeys && !valid) {
                         const uint32_t vrow = sbase + L::v + (seq & 1) * kTile + row * 128;
