@@ -91,16 +91,17 @@ typedef enum {
  * the RoPE dimensions in BF16).  d = 128.  The pages fix neither the RoPE width nor the scale;
  * the layout takes the last 64 dims of a K row as its RoPE dims and one power-of-two scale per
  * 64 FP8 values:
- *   ck: [B][Ncap][208] bytes per K row -- bytes 0..63 the E4M3 codes of dims 0..63, byte 64
- *       their scale byte, bytes 65..79 zero, bytes 80..207 dims 64..127 as bfloat16;
- *   cv: [B][Ncap][144] bytes per V row -- bytes 0..127 the E4M3 codes of dims 0..127, bytes
- *       128 / 129 the scale bytes of dims 0..63 / 64..127, bytes 130..143 zero.
+ *   ck: [B][Ncap][224] bytes per K row -- bytes 0..63 the E4M3 codes of dims 0..63, byte 64
+ *       their scale byte, bytes 65 / 66 the scale bytes of the entry's V dims 0..63 / 64..127,
+ *       bytes 67..95 zero, bytes 96..223 dims 64..127 as bfloat16;
+ *   cv: [B][Ncap][128] bytes per V row -- the E4M3 codes of dims 0..127.
+ * (Rows start on 32-byte boundaries; the V row's scales travel with the K row.)
  * A block of 64 pooled float32 values with largest magnitude amax gets e = the smallest integer
  * with amax <= 448 * 2^e (0 for an all-zero block; clamped to [-127, 127]), the byte e + 127,
  * and codes RNE_e4m3(x * 2^-e); a value reads back as code * 2^e (exactly a bfloat16 number).
  * The bfloat16 dims are the pooled values rounded to nearest even. */
-#define CSAHCA_KV_FP8_K_ROW 208
-#define CSAHCA_KV_FP8_V_ROW 144
+#define CSAHCA_KV_FP8_K_ROW 224
+#define CSAHCA_KV_FP8_V_ROW 128
 
 /* ------------------------------------------------------------------ a1 / a2: pooling
  * Softmax-gated pooling (pogovet.com article, detail 4; honbul.tistory.com/221 "CSA" and

@@ -20,7 +20,7 @@ LIB_PATH = os.path.join(_HERE, "libcsahca.so")
 F32, BF16, E4M3_ROWSCALE, E2M1_UE8M0 = 0, 1, 2, 3
 KEY_FMT = {"f32": F32, "bf16": BF16, "e4m3": E4M3_ROWSCALE, "e2m1": E2M1_UE8M0}
 # compressed K/V in FP8 with the RoPE dims of K in bf16: caches are uint8 tensors of these row sizes
-KV_FP8, KV_FP8_K_ROW, KV_FP8_V_ROW = 4, 208, 144
+KV_FP8, KV_FP8_K_ROW, KV_FP8_V_ROW = 4, 224, 128
 
 # every C entry point and its ctypes signature
 _P, _I64, _I, _F, _SZ = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float, ctypes.c_size_t

@@ -104,7 +104,7 @@ struct ItemTiles {
 
 struct Maps {
     CUtensorMap ck, cv, rk, rv;
-    CUtensorMap k8, kr, v8, vs;      // FP8 caches: K codes + scale, K RoPE dims (bf16), V codes, V scales
+    CUtensorMap k8, kr, v8;          // FP8 caches: K codes + scale bytes, K RoPE dims (bf16), V codes
 };
 
 // Piece schedule, computed by one warp (no more query rows than CTAs, S >= 2 partial slots per
@@ -269,14 +269,13 @@ __device__ __forceinline__ void load_tile(const AttendArgs& a, const Maps& maps,
     cp_async_arrive_noinc(bar);
 }
 
-// FP8 caches (CSAHCA_KV_FP8).  A compressed K tile lands as 128 rows of 128 bytes (the row's 64
-// codes, its scale byte and the bytes after them) in the slot's first half, dense, and its RoPE
-// dims (bf16) in the second half with the 128-byte swizzle of a bf16 tile; a V tile's codes land
-// as 128 dense rows of 128 bytes in the slot's second half and its scale bytes as rows of 16 bytes
-// in a side buffer.  A converter thread then turns row t into bf16 within row t's own 128-byte
-// rows (the codes it reads are its own), so the conversion needs no barrier.  Contiguous tiles
-// come by TMA (issued by thread 0), selected entries are gathered with cp.async; completion is
-// counted on `bar` as in load_tile.
+// FP8 caches (CSAHCA_KV_FP8).  A compressed K tile lands as 128 dense rows of 128 bytes (the row's
+// 64 codes, the scale bytes of the K and V rows and the bytes after them) in the slot's first half
+// and its RoPE dims (bf16) in the second half with the 128-byte swizzle of a bf16 tile; a V tile's
+// codes land as 128 dense rows of 128 bytes in the slot's second half.  The V scale bytes reach
+// a side buffer when the K tile is expanded.  The threads of a tile row then turn it into bf16
+// within the row's own 128-byte rows.  Contiguous tiles come by TMA (issued by thread 0),
+// selected entries are gathered with cp.async; completion is counted on `bar` as in load_tile.
 constexpr uint32_t kVScale = kKeys * 16;                // V scale rows of one slot: 2 KB
 
 template <int kSoft>
@@ -289,10 +288,9 @@ __device__ __forceinline__ void load_tile_f8(const AttendArgs& a, const Maps& ma
         if (!is_v && tid < kKeys) valid[tid] = (int64_t)ti * kKeys + tid < n_c;
         if (tid == 0) {
             const int y = (int)((int64_t)b * a.Ncap + (int64_t)ti * kKeys);
-            mbar_expect_tx(bar, is_v ? kHalf + kVScale : 2 * kHalf);
+            mbar_expect_tx(bar, is_v ? kHalf : 2 * kHalf);
             if (is_v) {
                 tma_load_2d(dst + kHalf, &maps.v8, 0, y, bar, pol);
-                tma_load_2d(vsc, &maps.vs, 0, y, bar, pol);
             } else {
                 tma_load_2d(dst, &maps.k8, 0, y, bar, pol);
                 tma_load_2d(dst + kHalf, &maps.kr, 0, y, bar, pol);
@@ -320,13 +318,14 @@ __device__ __forceinline__ void load_tile_f8(const AttendArgs& a, const Maps& ma
                   ((int64_t)b * a.Ncap + e) * (is_v ? kKv8VRow : kKv8KRow);
     }
     if (!is_v && part == 0) valid[rr] = src != nullptr;
-    // K: 5 chunks of codes + scale (dense row rr of the first half), 8 of RoPE dims (swizzled
-    // second half); V: 8 chunks of codes (dense row rr of the second half), 1 of scales
-    const int nch = is_v ? 9 : 13;
+    // K: 6 chunks of codes, scale bytes and zeros (dense row rr of the first half), 8 of RoPE dims
+    // (swizzled second half); V: 8 chunks of codes (dense row rr of the second half)
+    (void)vsc;
+    const int nch = is_v ? 8 : 14;
     for (int c = part; c < nch; c += kTpr) {
         uint32_t d;
-        if (is_v) d = c < 8 ? dst + kHalf + rr * 128 + c * 16 : vsc + rr * 16;
-        else d = c < 5 ? dst + rr * 128 + c * 16 : dst + kHalf + sw128(rr, c - 5);
+        if (is_v) d = dst + kHalf + rr * 128 + c * 16;
+        else d = c < 6 ? dst + rr * 128 + c * 16 : dst + kHalf + sw128(rr, c - 6);
         if (src) cp_async16_hint(d, src + c * 16, 16, pol);
         else cp_async16(d, zsrc, 0);                    // zero fill (no bytes read)
     }
@@ -365,7 +364,7 @@ __device__ __forceinline__ void sts128(uint32_t addr, uint4 u) {
 // -> bf16 in place.  The kTpr threads of a row sit in one warp: every one reads its codes and the
 // scale byte, then (after __syncwarp) writes its chunks of the row.
 template <int kTpr>
-__device__ __forceinline__ void convert_k_part(uint32_t slot, int r, int pt) {
+__device__ __forceinline__ void convert_k_part(uint32_t slot, uint32_t vsc, int r, int pt) {
     constexpr int kU = 64 / 16 / kTpr;                  // 16-code pieces per part
     uint4 c[kU];
 #pragma unroll
@@ -373,6 +372,7 @@ __device__ __forceinline__ void convert_k_part(uint32_t slot, int r, int pt) {
     uint32_t sb;
     asm volatile("ld.shared.u32 %0, [%1];" : "=r"(sb) : "r"(slot + r * 128 + 64));
     __syncwarp();
+    if (pt == 0) asm volatile("st.shared.u32 [%0], %1;" ::"r"(vsc + r * 16), "r"(sb >> 8) : "memory");   // V's two
     const float sc = ue8m0_to_f32(sb & 0xFFu);
 #pragma unroll
     for (int i = 0; i < kU; ++i) {
@@ -738,7 +738,7 @@ __global__ void __launch_bounds__(Thr<H, F8>::kThreads, 1)
                 const bool zr = zero_invalid && ms.valid[seq & 3][cr] == 0;
                 if (t0 + i < nt_c) {
                     if (is_v) convert_v_part<kTpr>(slot, sbase + L::total + (seq & 1) * kVScale, cr, cp, zr);
-                    else convert_k_part<kTpr>(slot, cr, cp);
+                    else convert_k_part<kTpr>(slot, sbase + L::total + (seq & 1) * kVScale, cr, cp);
                 } else if (is_v && zr) {
                     zero_v_part<kTpr>(slot, cr, cp);
                 }
@@ -1006,12 +1006,10 @@ cudaError_t launch_tc(const AttendArgs& a, int S, int kps, float* o_part, float*
     if (!a.is_csa && F8 &&
         encode_tmap_2d_sw(&maps.k8, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.ck, 128, crows, kKv8KRow, 128, kKeys,
                           CU_TENSOR_MAP_SWIZZLE_NONE) &&
-        encode_tmap_2d_sw(&maps.kr, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, static_cast<const char*>(a.ck) + 80, 64, crows,
-                          kKv8KRow, 64, kKeys, CU_TENSOR_MAP_SWIZZLE_128B) &&
+        encode_tmap_2d_sw(&maps.kr, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, static_cast<const char*>(a.ck) + kKv8Rope, 64,
+                          crows, kKv8KRow, 64, kKeys, CU_TENSOR_MAP_SWIZZLE_128B) &&
         encode_tmap_2d_sw(&maps.v8, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.cv, 128, crows, kKv8VRow, 128, kKeys,
-                          CU_TENSOR_MAP_SWIZZLE_NONE) &&
-        encode_tmap_2d_sw(&maps.vs, CU_TENSOR_MAP_DATA_TYPE_UINT8, static_cast<const char*>(a.cv) + 128, 16, crows,
-                          kKv8VRow, 16, kKeys, CU_TENSOR_MAP_SWIZZLE_NONE))
+                          CU_TENSOR_MAP_SWIZZLE_NONE))
         use_c = 1;
     // The decode window is the whole ring when it holds exactly one tile of tokens.
     if (a.chunk_k == nullptr && a.W == kKeys && a.ring_cap == kKeys && a.ring_k != nullptr &&

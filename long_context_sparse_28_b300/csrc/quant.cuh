@@ -106,8 +106,11 @@ __host__ __device__ inline int64_t key_scale_bytes(int fmt, int d_I) {
 // e = the smallest integer with amax <= 448 * 2^e (amax = f 2^ex, f in [0.5, 1): e = ex - 9 when
 // f <= 0.875 = 448 / 2^9, else ex - 8; 0 for a zero block; clamped to [-127, 127]), codes
 // RNE_e4m3(x * 2^-e) (the scaling is exact); the last 64 dims of K in bfloat16.
-constexpr int kKv8KRow = 208;   // bytes per K row: 64 codes, scale byte, 15 zero bytes, 64 bf16
-constexpr int kKv8VRow = 144;   // bytes per V row: 128 codes, 2 scale bytes, 14 zero bytes
+// Rows start on 32-byte sectors: K row (224 bytes) = 64 codes | its scale byte | the V row's two
+// scale bytes | 29 zero bytes | 64 bf16 RoPE dims at byte 96; V row (128 bytes) = 128 codes.
+constexpr int kKv8KRow = 224;
+constexpr int kKv8VRow = 128;
+constexpr int kKv8Rope = 96;    // byte offset of the RoPE dims in a K row
 
 __device__ __forceinline__ int kv8_block_exponent(float amax) {
     if (!(amax > 0.0f)) return 0;
@@ -141,7 +144,7 @@ __device__ __forceinline__ void store_kv8_warp(const float (&x)[8], unsigned cha
         u.y = pack_bf16x2(x[2], x[3]);
         u.z = pack_bf16x2(x[4], x[5]);
         u.w = pack_bf16x2(x[6], x[7]);
-        *reinterpret_cast<uint4*>(krow + 80 + (lane - 8) * 16) = u;
+        *reinterpret_cast<uint4*>(krow + kKv8Rope + (lane - 8) * 16) = u;
     } else {
         const float sc = pow2f(-e);
         uint32_t w[2];
@@ -156,9 +159,12 @@ __device__ __forceinline__ void store_kv8_warp(const float (&x)[8], unsigned cha
         unsigned char* dst = lane < 8 ? krow + lane * 8 : vrow + (lane - 16) * 8;
         *reinterpret_cast<uint2*>(dst) = make_uint2(w[0], w[1]);
     }
-    if (lane == 0) *reinterpret_cast<uint4*>(krow + 64) = make_uint4((uint32_t)(e + 127), 0u, 0u, 0u);
-    if (lane == 16)
-        *reinterpret_cast<uint4*>(vrow + 128) = make_uint4((uint32_t)(e + 127) | ((uint32_t)(e_v1 + 127) << 8), 0u, 0u, 0u);
+    const int e_v0 = __shfl_sync(0xffffffffu, e, 16);
+    if (lane == 0) {
+        *reinterpret_cast<uint4*>(krow + 64) =
+            make_uint4((uint32_t)(e + 127) | ((uint32_t)(e_v0 + 127) << 8) | ((uint32_t)(e_v1 + 127) << 16), 0u, 0u, 0u);
+        *reinterpret_cast<uint4*>(krow + 80) = make_uint4(0u, 0u, 0u, 0u);
+    }
 }
 
 }  // namespace csahca

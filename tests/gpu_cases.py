@@ -168,13 +168,13 @@ def oracle_hca_seq(case, b):
 
 # ----------------------------------------------------------- FP8 compressed K/V (pogovet.com detail 5)
 def kv8_planes(ck, cv):
-    """GPU FP8 caches [N, 208] / [N, 144] uint8 -> the oracle's planes (K codes, scales, RoPE bf16
-    bits; V codes, scales), after checking the zero padding bytes."""
+    """GPU FP8 caches [N, 224] / [N, 128] uint8 -> the oracle's planes (K codes, scales, RoPE bf16
+    bits; V codes, scales -- the V scales travel in the K row), after checking the zero bytes."""
     k = npy(ck).astype(np.uint8)
     v = npy(cv).astype(np.uint8)
-    assert not k[:, 65:80].any() and not v[:, 130:144].any(), "padding bytes"
-    return dict(k_codes=k[:, :64], k_scales=k[:, 64:65], k_rope=np.ascontiguousarray(k[:, 80:208]).view(np.uint16),
-                v_codes=v[:, :128], v_scales=v[:, 128:130])
+    assert k.shape[1] == 224 and v.shape[1] == 128 and not k[:, 67:96].any(), "layout / padding bytes"
+    return dict(k_codes=k[:, :64], k_scales=k[:, 64:65], k_rope=np.ascontiguousarray(k[:, 96:224]).view(np.uint16),
+                v_codes=v[:, :128], v_scales=np.ascontiguousarray(k[:, 65:67]))
 
 
 def kv8_dequant(pl, d=128):
