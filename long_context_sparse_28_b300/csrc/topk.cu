@@ -292,12 +292,31 @@ __global__ void __launch_bounds__(kSelThreads, 1) topk_select_kernel(
         cl.sync();                                  // every candidate list is complete
         if (p == 0)                                 // every CTA has its copy: clear the row's histogram
             for (int i = tid; i < kBins12; i += nthr) hrow[i] = 0u;
-        int tot = 0;
-        for (int q = 0; q < P; ++q) {
-            const int nq = min(*cl.map_shared_rank(&sh_nc, q), kCap - tot);   // the row holds <= kCap
-            const uint2* src = q == p ? cs : cl.map_shared_rank(cs, q);
-            for (int i = tid; i < nq; i += nthr) ga[tot + i] = src[i];
-            tot += nq;
+        // list sizes of all CTAs (one remote read each), then one pass over the concatenation in
+        // which a thread's remote loads are independent (two in flight per iteration)
+        int off[kMaxCluster + 1];
+        off[0] = 0;
+#pragma unroll
+        for (int q = 0; q < kMaxCluster; ++q)
+            off[q + 1] = q < P ? min(off[q] + *cl.map_shared_rank(&sh_nc, q), kCap) : off[q];   // the row holds <= kCap
+        const int tot = off[kMaxCluster];
+        auto src_of = [&](int i) -> const uint2* {
+            int q = 0, start = 0;
+#pragma unroll
+            for (int j = 1; j < kMaxCluster; ++j)
+                if (i >= off[j]) {
+                    q = j;
+                    start = off[j];
+                }
+            const uint2* base = q == p ? cs : cl.map_shared_rank(cs, q);
+            return base + (i - start);
+        };
+        for (int i = tid; i < tot; i += 2 * nthr) {
+            const int i2 = i + nthr;
+            const uint2 x = *src_of(i);
+            const uint2 y = i2 < tot ? *src_of(i2) : make_uint2(0u, 0u);
+            ga[i] = x;
+            if (i2 < tot) ga[i2] = y;
         }
         __syncthreads();
         cluster_arrive_release();                   // done with the other CTAs' lists (waited at the end)
