@@ -19,9 +19,11 @@
 // then rounded, an error below 2^-20 of that largest element; so are heads whose largest element
 // is below 2^-114, whose exponent is capped.)
 //   e2m1 keys (UE8M0 per 32 codes): the MMA applies every scale (kind::mxf8f6f4 block_scale): a
-//     key's factor for its code block is the A scale of its row, 2^-e_h (hi rows) and 2^-(e_h+5)
-//     (lo rows) are the B scales, so the accumulator of a key holds D_hi + D_lo = q . khat per
-//     head directly and the epilogue forms score = sum_h w_h ReLU(D_hi[h] + D_lo[h]).  The scale
+//     key's factor for its code block is the A scale of its row; the hi rows' blocks multiply with
+//     the B factor 2^-e_h and the lo rows' blocks -- issued as further MMAs into the same
+//     accumulator columns -- with 2^-(e_h+5) (bytes 0-1 / 2-3 of the head's factor word), so the
+//     accumulator of a key holds q . khat per head directly (one column per head) and the epilogue
+//     forms score = sum_h w_h ReLU(D[h]).  The scale
 //     factors reach TMEM with tcgen05.cp, which wants an M = 128 operand's factors as 32 lines of
 //     16 bytes (row r's four bytes -- even key blocks 0/1, odd key blocks 0/1 -- in word r / 32 of
 //     line r % 32).  The codes are therefore loaded with a 4-D TMA map that puts TMA row 4 l + j
@@ -110,7 +112,11 @@ struct Cfg {
     static constexpr int ns_fit = (int)((114 * 1024 - 1024 - 1024 - sizeof(IdxMisc) - 2 * q_slot -
                                          (fp4 ? 0 : kMaxBuf * kPair * 4)) / stage);
     static constexpr int ns_cap = ns_fit < 3 ? 3 : (ns_fit > kMaxNS ? kMaxNS : ns_fit);
-    static constexpr uint32_t acc_cols = NQ;                         // one accumulator: hi | lo columns (or FP4 q)
+    // e2m1 keys with bf16 queries: the MMA adds the lo part into the hi part's accumulator (its own
+    // B scale factor 2^-(e_h+5) in bytes 2-3 of the head's factor word), one column per head
+    static constexpr bool fused = fp4 && !Q4;
+    static constexpr bool one_part = fused || Q4;                    // one accumulator column per head
+    static constexpr uint32_t acc_cols = one_part ? HI : NQ;         // hi | lo columns (e4m3 keys)
     static constexpr uint32_t d_cols = 2 * acc_cols;                 // even + odd keys
     // fp4: scale factors of A (4 columns per stage slot) and B (4 per query slot)
     static constexpr uint32_t sf_cols = fp4 ? 4 * kMaxNS + 8 : 0;
@@ -401,9 +407,9 @@ __global__ void __launch_bounds__(kThreads) index_tc_kernel(const __grid_constan
                         // B scale factors (every K block alike): column n's byte in word n / 32 of
                         // line n % 32; hi column h: 2^-e_h, lo column HI + h: 2^-(e_h + 5)
                         uint32_t* sfb = reinterpret_cast<uint32_t*>(qsl + C::off_sfb);
-                        const int nl = HI + h;
-                        sfb[(h & 31) * 4 + (h >> 5)] = (uint32_t)(127 - exq[j]) * 0x01010101u;
-                        sfb[(nl & 31) * 4 + (nl >> 5)] = (uint32_t)(122 - exq[j]) * 0x01010101u;
+                        // (the MMA adds the lo rows into the hi rows' columns: their factor is
+                        // byte 2 + block of column h's word)
+                        sfb[(h & 31) * 4 + (h >> 5)] = (uint32_t)(127 - exq[j]) * 0x0101u | (uint32_t)(122 - exq[j]) * 0x01010000u;
                     }
                 }
             }
@@ -498,11 +504,18 @@ __global__ void __launch_bounds__(kThreads) index_tc_kernel(const __grid_constan
                     for (int e = 0; e < 2; ++e)              // even keys: code columns [0,64); odd: [64,128)
 #pragma unroll
                         for (int blk = 0; blk < 2; ++blk)    // 32-code blocks (one MMA K step each)
+                        {
                             mma_mxf8f6f4_bs(dbuf + e * C::acc_cols, ad0 + (uint64_t)(e * 4 + blk * 2),
                                             bd0 + (uint64_t)(blk * 2),
-                                            idesc_mxf8f6f4_bs(128, C::NQ, af, Q4 ? kE2M1 : kE4M3, 2 * e + blk, blk),
+                                            idesc_mxf8f6f4_bs(128, C::acc_cols, af, Q4 ? kE2M1 : kE4M3, 2 * e + blk, blk),
                                             sfa, sfb,
                                             (uint32_t)(blk > 0));
+                            if constexpr (C::fused)       // the lo rows (row HI on), factor byte 2 + blk
+                                mma_mxf8f6f4_bs(dbuf + e * C::acc_cols, ad0 + (uint64_t)(e * 4 + blk * 2),
+                                                bd0 + (uint64_t)((HI * 128) >> 4) + (uint64_t)(blk * 2),
+                                                idesc_mxf8f6f4_bs(128, C::acc_cols, af, kE4M3, 2 * e + blk, 2 + blk),
+                                                sfa, sfb, 1u);
+                        }
                 } else {
                     const uint32_t id = idesc_f8f6f4(128, 2 * HI, af, kE4M3);
 #pragma unroll
@@ -546,8 +559,8 @@ __global__ void __launch_bounds__(kThreads) index_tc_kernel(const __grid_constan
 #pragma unroll
                 for (int k = 0; k < 16; k += 2) {
                     const uint64_t hp = f2_pack(__uint_as_float(hv[k]), __uint_as_float(hv[k + 1]));
-                    uint64_t v = hp;                                     // FP4 queries: one part
-                    if constexpr (!Q4) {
+                    uint64_t v = hp;                          // one part (fused hi + lo, or FP4 queries)
+                    if constexpr (!C::one_part) {
                         const uint64_t lp = f2_pack(__uint_as_float(lv[k]), __uint_as_float(lv[k + 1]));
                         v = C::fp4 ? f2_add(hp, lp) : f2_fma(Ll, lp, hp);
                     }
@@ -585,7 +598,7 @@ __global__ void __launch_bounds__(kThreads) index_tc_kernel(const __grid_constan
                         uint64_t wv[8];
                         weights16(c0, wv);
                         const int h = key * (int)C::acc_cols + c0;
-                        head_pairs(acc2[key], dv + h, dv + h + (Q4 ? 0 : HI), wv);
+                        head_pairs(acc2[key], dv + h, dv + h + (C::one_part ? 0 : HI), wv);
                     }
             } else {
 #pragma unroll
@@ -597,7 +610,7 @@ __global__ void __launch_bounds__(kThreads) index_tc_kernel(const __grid_constan
                         weights16(c0, wv);
                         uint32_t h0[16], l0[16];
                         tmem_ld16(abase + c0, h0);
-                        if (!Q4) tmem_ld16(abase + HI + c0, l0);
+                        if (!C::one_part) tmem_ld16(abase + HI + c0, l0);
                         tmem_wait_ld();
                         head_pairs(acc2[key], h0, l0, wv);
                     }
