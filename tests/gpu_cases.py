@@ -80,7 +80,7 @@ def csa_decode_case(w: wl.Workload, check_seqs, device="cuda", layer="csa", step
     Ncap = max(lengths) // m + 1
     dtype = wl.torch_dtype(w.kv)
     fmt = L.KEY_FMT[w.key_fmt]
-    cache = CSACache(B, Ncap, w.d, w.W, w.d_I, fmt, dtype, device, m=m)
+    cache = CSACache(B, Ncap, w.d, w.W, w.d_I, fmt, dtype, device, m=m, kv_fp8=w.kv_cache == "fp8")
     bias = wl.layer_bias(w, layer, m, device)
     k_new = torch.empty(B, 1, w.d, dtype=dtype, device=device)
     v_new = torch.empty_like(k_new)
@@ -117,8 +117,13 @@ def oracle_csa_seq(case, b, idx_override=None):
     h = case["host"][b]
     Lb, m = h["L"], w.m_csa
     N = Lb // m
-    sd = oracle.BF16 if w.kv == "bf16" else oracle.F32
-    ck, cv = oracle.compress(h["K"], h["V"], h["G"], npy(case["bias"]), m, sd, n_blocks=N)
+    if w.kv_cache == "fp8":                  # FP8 caches: attention reads the dequantised entries
+        c8 = oracle.compress_kv_fp8(h["K"], h["V"], h["G"], npy(case["bias"]), m, n_blocks=N)
+        ck, cv = c8["ck"], c8["cv"]
+        case.setdefault("kv8", {})[b] = c8
+    else:
+        sd = oracle.BF16 if w.kv == "bf16" else oracle.F32
+        ck, cv = oracle.compress(h["K"], h["V"], h["G"], npy(case["bias"]), m, sd, n_blocks=N)
     codes, scales = oracle.quantize_keys(h["kin"][:N], case["fmt"])
     res = oracle.csa_queries(npy(case["q"][b]), npy(case["q_idx"][b]), npy(case["wts"][b]), [Lb - 1], ck, cv,
                              codes, scales, case["fmt"], h["K"], h["V"], 0, m, w.k, w.W, w.scale,
@@ -133,7 +138,7 @@ def hca_decode_case(w: wl.Workload, check_seqs, device="cuda", layer="hca", spli
     B, m = w.B, w.m_hca
     Ncap = max(lengths) // m + 1
     dtype = wl.torch_dtype(w.kv)
-    cache = HCACache(B, Ncap, w.d, w.W, dtype, device, m=m)
+    cache = HCACache(B, Ncap, w.d, w.W, dtype, device, m=m, kv_fp8=w.kv_cache == "fp8")
     bias = wl.layer_bias(w, layer, m, device)
     k_new = torch.empty(B, 1, w.d, dtype=dtype, device=device)
     v_new = torch.empty_like(k_new)
@@ -160,8 +165,13 @@ def oracle_hca_seq(case, b):
     w = case["w"]
     h = case["host"][b]
     Lb, m = h["L"], w.m_hca
-    sd = oracle.BF16 if w.kv == "bf16" else oracle.F32
-    ck, cv = oracle.compress(h["K"], h["V"], h["G"], npy(case["bias"]), m, sd, n_blocks=Lb // m)
+    if w.kv_cache == "fp8":
+        c8 = oracle.compress_kv_fp8(h["K"], h["V"], h["G"], npy(case["bias"]), m, n_blocks=Lb // m)
+        ck, cv = c8["ck"], c8["cv"]
+        case.setdefault("kv8", {})[b] = c8
+    else:
+        sd = oracle.BF16 if w.kv == "bf16" else oracle.F32
+        ck, cv = oracle.compress(h["K"], h["V"], h["G"], npy(case["bias"]), m, sd, n_blocks=Lb // m)
     res = oracle.hca_queries(npy(case["q"][b]), [Lb - 1], ck, cv, h["K"], h["V"], 0, m, w.W, w.scale)
     return res, ck, cv
 
@@ -198,10 +208,12 @@ def assert_kv8_close(ck, cv, ora, what=""):
     gk, gv = kv8_dequant(g)
     for name, gd, od, gs, os_ in (("K", gk[:, :64], ora["ck"][:, :64], g["k_scales"], ora["k_scales"]),
                                   ("V", gv, ora["cv"], g["v_scales"], ora["v_scales"])):
-        tol = np.maximum(e4m3_step(gd, gs), e4m3_step(od, os_))
+        tol = np.maximum(e4m3_step(gd, gs), e4m3_step(od, os_)) + 1e-4   # (+ the pooling's cancellation error)
         assert (np.abs(gd - od) <= tol).all(), f"{what} {name}: beyond one E4M3 step"
         assert np.mean(gs == os_) >= 0.99, f"{what} {name}: scale bytes"
         assert np.abs(gs.astype(int) - os_.astype(int)).max() <= 1, f"{what} {name}: scale off by more than 1"
     assert np.mean(g["k_codes"] == ora["k_codes"]) >= 0.95 and np.mean(g["v_codes"] == ora["v_codes"]) >= 0.95
-    hu = 2 * bf16_half_ulp(ora["ck"][:, 64:])
+    # one bf16 step, plus the fp32 pooling's own error where the pooled value cancels (inputs of
+    # magnitude <= ~4, up to 128 terms: below 1e-4)
+    hu = 2 * bf16_half_ulp(ora["ck"][:, 64:]) + 1e-4
     assert (np.abs(gk[:, 64:] - ora["ck"][:, 64:]) <= hu).all(), f"{what}: RoPE dims"

@@ -7,8 +7,8 @@ import torch
 
 import oracle
 import workloads as wl
-from tests.gpu_cases import (assert_close, check_index_set, csa_decode_case, hca_decode_case, npy, oracle_csa_seq,
-                             oracle_hca_seq)
+from tests.gpu_cases import (assert_close, assert_kv8_close, check_index_set, csa_decode_case, hca_decode_case, npy,
+                             oracle_csa_seq, oracle_hca_seq)
 
 pytestmark = pytest.mark.gpu
 
@@ -20,8 +20,11 @@ def _check_csa(case, seqs, tol):
         res, ck, cv, codes, scales = oracle_csa_seq(case, b)
         Lb = case["lengths"][b]
         N = Lb // w.m_csa
-        # compressed cache: within one storage ulp of the oracle's
-        assert_close(case["cache"].ck[b, :N], oracle.to_f64(ck), tol, f"ck b{b}")
+        # compressed cache: within one storage ulp (FP8: one E4M3 step) of the oracle's
+        if w.kv_cache == "fp8":
+            assert_kv8_close(case["cache"].ck[b, :N], case["cache"].cv[b, :N], case["kv8"][b], f"ck b{b}")
+        else:
+            assert_close(case["cache"].ck[b, :N], oracle.to_f64(ck), tol, f"ck b{b}")
         # index keys: bit-exact
         np.testing.assert_array_equal(npy(case["cache"].k_codes[b, :N]).view(np.uint8),
                                       np.asarray(codes).view(np.uint8))
@@ -54,7 +57,10 @@ def _check_hca(case, seqs):
     for b in seqs:
         res, ck, cv = oracle_hca_seq(case, b)
         n = case["lengths"][b] // w.m_hca
-        assert_close(case["cache"].ck[b, :n], oracle.to_f64(ck), "bf16", f"hca ck b{b}")
+        if w.kv_cache == "fp8":
+            assert_kv8_close(case["cache"].ck[b, :n], case["cache"].cv[b, :n], case["kv8"][b], f"hca ck b{b}")
+        else:
+            assert_close(case["cache"].ck[b, :n], oracle.to_f64(ck), "bf16", f"hca ck b{b}")
         assert_close(case["out"][b, 0], res["o"][0], "bf16", f"hca out b{b}")
         np.testing.assert_allclose(npy(case["lse"][b, 0]), res["lse"][0], rtol=1e-4, atol=1e-4)
 
@@ -70,6 +76,21 @@ def test_decode_1m_b32_csa_then_hca():
     lens = w.lengths()
     order = np.argsort(lens)
     seqs = sorted({int(order[0]), int(order[len(order) // 3]), int(order[2 * len(order) // 3]), int(order[-1])})
+    csa = csa_decode_case(w, seqs, layer="csa")
+    _check_csa(csa, seqs, "bf16")
+    del csa
+    torch.cuda.empty_cache()
+    hca = hca_decode_case(w, seqs, layer="hca")
+    _check_hca(hca, seqs)
+
+
+def test_decode_1m_b32_with_fp8_caches():
+    # the 1M decode workload with FP8 compressed K/V (the RoPE dims of K in bf16), four sampled
+    # sequences through both layers, at full size in the benchmark's launch configuration
+    w = wl.WORKLOADS["decode_1m_b32_csa_hca_kv8"]
+    lens = w.lengths()
+    order = np.argsort(lens)
+    seqs = sorted({int(order[0]), int(order[len(order) // 2]), int(order[-1])})
     csa = csa_decode_case(w, seqs, layer="csa")
     _check_csa(csa, seqs, "bf16")
     del csa
