@@ -388,14 +388,15 @@ def kernel_source_hash(call: str) -> str:
     return h.hexdigest()[:16]
 
 
-def load_traffic(kernel: str):
+def load_traffic(kernel: str, workload: str):
     """Per-launch DRAM bytes of a call's kernels from the committed ncu summary, if it was taken
-    on the call's current kernel sources."""
+    on this workload and on the call's current kernel sources."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         d = json.load(open(p))
         e = d.get(kernel)
-        if e and kernel in CALL_SOURCES and e.get("source_hash") == kernel_source_hash(kernel):
+        if (e and kernel in CALL_SOURCES and e.get("workload") == workload and
+                e.get("source_hash") == kernel_source_hash(kernel)):
             return e
     except Exception:
         pass
@@ -555,7 +556,7 @@ def run_ours(args, dist):
     per = {DecodeBench.SUBSTEPS[a]: sub_ms[i] for i, a in enumerate(active)}
     dom = max((n for n in kern_bytes if n in per), key=lambda n: per[n])
     dom_gbs = kern_bytes[dom] / (per[dom] / 1e3) / 1e9
-    traffic = load_traffic(dom)
+    traffic = load_traffic(dom, w.name)
     roofline = {"bound": "hbm", "kernel": dom, "achieved": round(dom_gbs, 1), "peak": hbm_peak, "unit": "GB/s",
                 "frac": round(dom_gbs / hbm_peak, 4), "traffic": traffic["dram_bytes_per_launch"] if traffic else None,
                 "algorithmic_bytes_per_launch": int(kern_bytes[dom]), "avg_launch_ms": round(per[dom], 5),
