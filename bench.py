@@ -723,7 +723,8 @@ class PrefillBench:
             L.swa_ring_write(x["ring_k"][None], x["ring_v"][None], x["ring_gate"][None], pos_ring, W, c.ring_k,
                              c.ring_v, c.ring_gate)
         self.x = x
-        self.step_ = HybridPrefill(self.csa, self.hca, T, w.H, w.k, x["csa_bias"], x["hca_bias"])
+        self.step_ = HybridPrefill(self.csa, self.hca, T, w.H, w.k, x["csa_bias"], x["hca_bias"], H_I=w.H_I,
+                                   q_fp4=w.index_q == "e2m1")
         self.step_.set_position(o)
         self.args = (x["chunk_k"][None], x["chunk_v"][None], x["chunk_gate"][None], x["chunk_kidx"][None],
                      x["q_csa"][None], x["q_idx"][None], x["w"][None], x["q_hca"][None])
@@ -749,7 +750,7 @@ def cpu_baseline_prefill(w, rows: int):
     rawk, rawv = np.concatenate([x["ring_k"], x["chunk_k"]]), np.concatenate([x["ring_v"], x["chunk_v"]])
     pos = o + sel
     oracle.csa_queries(x["q_csa"][sel], x["q_idx"][sel], x["w"][sel], pos, ck, cv, codes, sc, fmt, rawk, rawv, o - W,
-                       w.m_csa, w.k, W, w.scale)
+                       w.m_csa, w.k, W, w.scale, q_fp4=w.index_q == "e2m1")
     oracle.hca_queries(x["q_hca"][sel], pos, np.concatenate([x["hca_ck"], hck]), np.concatenate([x["hca_cv"], hcv]),
                        rawk, rawv, o - W, w.m_hca, W, w.scale)
     dt = time.perf_counter() - t0
@@ -811,8 +812,7 @@ def run_prefill(args, dist):
                                           csa.k_codes[0, st.pos0 // csa.m:st.pos0 // csa.m + w.T // csa.m],
                                           None if csa.k_scale is None else
                                           csa.k_scale[0, st.pos0 // csa.m:st.pos0 // csa.m + w.T // csa.m])),
-        lambda: L.csa_index_topk(a[5], a[6], csa.k_codes, csa.k_scale, csa.key_fmt, st.q_pos, csa.m, w.k, st.idx,
-                                 workspace=st.ws_topk),
+        lambda: st.index_topk(a[5], a[6]),
         lambda: L.csa_attend(a[4], st.scale, csa.ck, csa.cv, st.idx, csa.ring_k, csa.ring_v, csa.W, st.q_pos, st.out_c,
                              st.lse_c, chunk_k=a[0], chunk_v=a[1], chunk_pos0=st.p0, workspace=st.ws_ca),
         lambda: L.hca_attend(a[7], st.scale, hca.ck, hca.cv, hca.m, hca.ring_k, hca.ring_v, hca.W, st.q_pos, st.out_h,
@@ -837,11 +837,16 @@ def run_prefill(args, dist):
         pass
     tf_peak = peaks.get("bf16_tflops_sustained", 1400.0)
     dom = max(("csa_index_topk", "csa_attend", "hca_attend"), key=lambda n: per[n])
+    # FP4 x FP4 indexer MMAs (kind::mxf8f6f4) run at the 8-bit rate: 2x bf16 (the nominal 4.5 / 2.25 ratio)
+    fp4_idx = dom == "csa_index_topk" and w.index_q == "e2m1"
+    if fp4_idx:
+        tf_peak = tf_peak * 2
     ach = fl[dom] / (per[dom] / 1e3) / 1e12
     roofline = {"bound": "tensor", "kernel": dom, "achieved": round(ach, 1), "peak": tf_peak, "unit": "TFLOP/s",
                 "frac": round(ach / tf_peak, 4), "traffic": None, "algorithmic_flops_per_launch": fl[dom],
                 "avg_launch_ms": round(per[dom], 4),
-                "peak_source": "measured (sustained)" if "bf16_tflops_sustained" in peaks else "fallback",
+                "peak_source": ("measured (sustained)" if "bf16_tflops_sustained" in peaks else "fallback") +
+                               (": bf16 x 2, the 8-bit MMA rate" if fp4_idx else ""),
                 "step_tflops": round(fl["total"] / (ms_per_step / 1e3) / 1e12, 1)}
     e2e = None if args.no_e2e else run_e2e_prefill(bench, w, K, dev, dist)
     cpu = None
@@ -852,7 +857,8 @@ def run_prefill(args, dist):
         "n_gpus": dist.world, "steps": K, "warmup": Wm, "ms_per_step": round(ms_per_step, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": w.name, "T": w.T, "offset": w.offset, "H": w.H, "d": w.d,
-                   "csa": {"m": w.m_csa, "k": w.k, "W": w.W, "H_I": w.H_I, "d_I": w.d_I, "index_keys": w.key_fmt},
+                   "csa": {"m": w.m_csa, "k": w.k, "W": w.W, "H_I": w.H_I, "d_I": w.d_I, "index_keys": w.key_fmt,
+                           "index_queries": "e2m1+ue8m0/32" if w.index_q == "e2m1" else "bf16"},
                    "hca": {"m": w.m_hca, "W": w.W}, "parallelism": f"replicas x{dist.world}",
                    "l2": "scores (1.09 GB) and gathered keys larger than L2; no flush",
                    "tflop_per_step": round(fl["total"] / 1e12, 4),

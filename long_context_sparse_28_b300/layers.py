@@ -16,8 +16,8 @@ import math
 
 import torch
 
-from . import (BF16, F32, csa_attend, csa_attend_workspace, csa_cache_append, csa_compress, csa_index_key_quantize,
-               csa_index_topk, csa_index_topk_workspace, hca_attend, hca_attend_workspace, hca_cache_append,
+from . import (BF16, E2M1_UE8M0, F32, csa_attend, csa_attend_workspace, csa_cache_append, csa_compress,
+               csa_index_key_quantize, csa_index_topk, csa_index_topk_fp4, csa_index_topk_workspace, hca_attend, hca_attend_workspace, hca_cache_append,
                hca_compress, key_storage, swa_ring_write, KV_FP8_K_ROW, KV_FP8_V_ROW)
 
 
@@ -154,8 +154,15 @@ class HybridPrefill:
     tokens into both rings.  Outputs and workspaces are allocated once, so a chunk's calls can be
     captured in a CUDA graph."""
 
-    def __init__(self, csa: CSACache, hca: HCACache, T, H, k, csa_bias, hca_bias, scale=None):
+    def __init__(self, csa: CSACache, hca: HCACache, T, H, k, csa_bias, hca_bias, scale=None, H_I=None,
+                 q_fp4=False):
         B, d, dev = csa.B, csa.d, csa.device
+        # FP4 indexer queries (the keys' MX E2M1 form, quantised per chunk): e2m1 keys only
+        self.q_fp4 = q_fp4
+        if q_fp4:
+            assert csa.key_fmt == E2M1_UE8M0 and H_I is not None
+            self.q4c = torch.empty(B, T, H_I, csa.d_I // 2, dtype=torch.uint8, device=dev)
+            self.q4s = torch.empty(B, T, H_I, csa.d_I // 32, dtype=torch.uint8, device=dev)
         self.csa, self.hca, self.T, self.H, self.k = csa, hca, T, H, k
         self.csa_bias, self.hca_bias = csa_bias, hca_bias
         self.scale = 1.0 / math.sqrt(d) if scale is None else scale
@@ -180,6 +187,17 @@ class HybridPrefill:
         self.p0.fill_(pos0)
         self.q_pos.copy_((torch.arange(T, device=dev, dtype=torch.int64)[None, :] + pos0).repeat(B, 1).reshape(-1))
 
+    def index_topk(self, q_idx, w, scores_out=None):
+        """The chunk's lightning indexer and top-k (bf16 queries, or FP4 queries quantised here)."""
+        csa = self.csa
+        if self.q_fp4:
+            csa_index_key_quantize(q_idx, E2M1_UE8M0, self.q4c, self.q4s)
+            csa_index_topk_fp4(self.q4c, self.q4s, w, csa.k_codes, csa.k_scale, self.q_pos, csa.m, self.k, self.idx,
+                               scores_out=scores_out, workspace=self.ws_topk)
+        else:
+            csa_index_topk(q_idx, w, csa.k_codes, csa.k_scale, csa.key_fmt, self.q_pos, csa.m, self.k, self.idx,
+                           scores_out=scores_out, workspace=self.ws_topk)
+
     def step(self, chunk_k, chunk_v, chunk_gate, kidx_chunk, q_csa, q_idx, w, q_hca, scores_out=None):
         """chunk_k/v [B, T, d]; chunk_gate [B, T]; kidx_chunk [B, T // m_csa, d_I] (index keys of the
         new CSA entries); q_csa/q_hca [B, T, H, d]; q_idx [B, T, H_I, d_I]; w [B, T, H_I]."""
@@ -190,8 +208,7 @@ class HybridPrefill:
         for b in range(csa.B):
             csa_index_key_quantize(kidx_chunk[b, :nb], csa.key_fmt, csa.k_codes[b, j0:j0 + nb],
                                    None if csa.k_scale is None else csa.k_scale[b, j0:j0 + nb])
-        csa_index_topk(q_idx, w, csa.k_codes, csa.k_scale, csa.key_fmt, self.q_pos, csa.m, self.k, self.idx,
-                       scores_out=scores_out, workspace=self.ws_topk)
+        self.index_topk(q_idx, w, scores_out)
         csa_attend(q_csa, self.scale, csa.ck, csa.cv, self.idx, csa.ring_k, csa.ring_v, csa.W, self.q_pos,
                    self.out_c, self.lse_c, chunk_k=chunk_k, chunk_v=chunk_v, chunk_pos0=self.p0, workspace=self.ws_ca)
         hca_attend(q_hca, self.scale, hca.ck, hca.cv, hca.m, hca.ring_k, hca.ring_v, hca.W, self.q_pos, self.out_h,

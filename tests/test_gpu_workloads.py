@@ -157,3 +157,55 @@ def test_hybrid_prefill_t4096_at_256k():
     # the rings now hold the chunk's last W tokens
     slots = np.arange(o + T - W, o + T) % W
     np.testing.assert_array_equal(npy(csa.ring_k[0])[slots], h["chunk_k"][T - W:])
+
+
+def test_hybrid_prefill_with_fp4_indexer():
+    # the prefill chunk with e2m1 index keys and FP4 (MX E2M1) indexer queries: the indexer runs
+    # both operands in FP4 on the block-scaled tensor core; 64 sampled query rows against the oracle's
+    # FP4-query rule, then CSA attention on the GPU's index sets
+    import long_context_sparse_28_b300 as L
+    from long_context_sparse_28_b300.layers import CSACache, HCACache, HybridPrefill
+    w = wl.WORKLOADS["hybrid_prefill_t4096_at_256k_q4"]
+    x = wl.prefill_inputs(w, "cuda")
+    o, T, W = w.offset, w.T, w.W
+    n_csa, n_hca = o // w.m_csa, o // w.m_hca
+    csa = CSACache(1, (o + T) // w.m_csa, w.d, W, w.d_I, L.E2M1_UE8M0, torch.bfloat16)
+    hca = HCACache(1, (o + T) // w.m_hca, w.d, W, torch.bfloat16)
+    csa.ck[0, :n_csa] = x["csa_ck"]
+    csa.cv[0, :n_csa] = x["csa_cv"]
+    L.csa_index_key_quantize(x["csa_kidx"], L.E2M1_UE8M0, csa.k_codes[0, :n_csa], csa.k_scale[0, :n_csa])
+    hca.ck[0, :n_hca] = x["hca_ck"]
+    hca.cv[0, :n_hca] = x["hca_cv"]
+    pos_ring = torch.tensor([o - W], dtype=torch.int64, device="cuda")
+    for c in (csa, hca):
+        L.swa_ring_write(x["ring_k"][None], x["ring_v"][None], x["ring_gate"][None], pos_ring, W, c.ring_k,
+                         c.ring_v, c.ring_gate)
+    step = HybridPrefill(csa, hca, T, w.H, w.k, x["csa_bias"], x["hca_bias"], H_I=w.H_I, q_fp4=True)
+    step.set_position(o)
+    res = step.step(x["chunk_k"][None], x["chunk_v"][None], x["chunk_gate"][None], x["chunk_kidx"][None],
+                    x["q_csa"][None], x["q_idx"][None], x["w"][None], x["q_hca"][None])
+    torch.cuda.synchronize()
+    assert L.device_status() == 0
+    h = {k: npy(v) for k, v in x.items()}
+    cck, ccv = oracle.compress(h["chunk_k"], h["chunk_v"], h["chunk_gate"], h["csa_bias"], w.m_csa, oracle.BF16)
+    ck_all = np.concatenate([h["csa_ck"], cck])
+    cv_all = np.concatenate([h["csa_cv"], ccv])
+    codes, sc = oracle.quantize_keys(np.concatenate([h["csa_kidx"], h["chunk_kidx"]]), oracle.KEY_E2M1)
+    np.testing.assert_array_equal(npy(csa.k_codes[0, :len(codes)]), codes)   # the chunk's keys, bit-exact
+    rawk = np.concatenate([h["ring_k"], h["chunk_k"]])
+    rawv = np.concatenate([h["ring_v"], h["chunk_v"]])
+    rng = np.random.default_rng(1)
+    edge = [0, 3, 4, 1023, 4095]
+    rows = np.unique(np.concatenate([edge, rng.choice(np.setdiff1d(np.arange(T), edge), 64 - len(edge),
+                                                      replace=False)]))
+    pos = o + rows
+    ores = oracle.csa_queries(h["q_csa"][rows], h["q_idx"][rows], h["w"][rows], pos, ck_all, cv_all, codes, sc,
+                              oracle.KEY_E2M1, rawk, rawv, o - W, w.m_csa, w.k, W, w.scale, q_fp4=True)
+    gidx = npy(res["idx"][0])
+    for i, t in enumerate(rows):
+        nv = (pos[i] + 1) // w.m_csa
+        check_index_set(gidx[t], ores["idx"][i], ores["scores"][i], nv, w.k, f"row {t}")
+    ores2 = oracle.csa_queries(h["q_csa"][rows], h["q_idx"][rows], h["w"][rows], pos, ck_all, cv_all, codes, sc,
+                               oracle.KEY_E2M1, rawk, rawv, o - W, w.m_csa, w.k, W, w.scale, q_fp4=True,
+                               idx_override=gidx[rows])
+    assert_close(res["csa_out"][0, rows], ores2["o"], "bf16", "fp4 prefill csa out")

@@ -239,3 +239,8 @@ def prefill_inputs(w: Workload, device="cuda", b: int = 0):
 # The 1M-context decode workload with the compressed K/V caches in FP8 (the RoPE dims of K in BF16).
 WORKLOADS["decode_1m_b32_csa_hca_kv8"] = replace(WORKLOADS["decode_1m_b32_csa_hca"], name="decode_1m_b32_csa_hca_kv8",
                                                 kv_cache="fp8")
+
+# The prefill chunk with the lightning indexer in FP4 for both operands (e2m1 keys, FP4 queries).
+WORKLOADS["hybrid_prefill_t4096_at_256k_q4"] = replace(WORKLOADS["hybrid_prefill_t4096_at_256k_bf16"],
+                                                      name="hybrid_prefill_t4096_at_256k_q4", key_fmt="e2m1",
+                                                      index_q="e2m1")
