@@ -135,7 +135,7 @@ __device__ __forceinline__ void load_span(const float* __restrict__ row, int64_t
 // Appends the elements >= tv of a loaded span to the shared candidate list (one shared atomic per
 // warp).  Candidates are few (about k per row), so their values are read again from the row.
 __device__ __forceinline__ void collect_loaded(const float* __restrict__ row, int64_t w0, int cnt_n, float tv,
-                                               const float (&v)[32], uint2* cs, int* sh_nc, int lane) {
+                                               const float (&v)[32], uint2* cs, int* sh_nc, int lane, int cap) {
     uint32_t bits = 0;
 #pragma unroll
     for (int e = 0; e < 32; ++e) {
@@ -158,7 +158,7 @@ __device__ __forceinline__ void collect_loaded(const float* __restrict__ row, in
         const int e = __ffs(bits) - 1;
         bits &= bits - 1;
         const int i = ((e >> 2) * 32 + lane) * 4 + (e & 3);
-        if (base < kCap) cs[base] = make_uint2(ordered_key(__ldg(row + w0 + i)), (uint32_t)(w0 + i));
+        if (base < cap) cs[base] = make_uint2(ordered_key(__ldg(row + w0 + i)), (uint32_t)(w0 + i));
         ++base;
     }
 }
@@ -218,18 +218,22 @@ __device__ __forceinline__ void cluster_sum(cooperative_groups::cluster_group& c
 __global__ void __launch_bounds__(kSelThreads, 1) topk_select_kernel(
     const float* __restrict__ scores, int64_t stride, const int64_t* __restrict__ n_vis_arr,
     const int64_t* __restrict__ q_pos, int m, int64_t Ncap, int k, uint32_t* __restrict__ hist1,
-    uint32_t* __restrict__ win, uint32_t* __restrict__ tie, int64_t words, int32_t* __restrict__ idx_out) {
+    uint32_t* __restrict__ win, uint32_t* __restrict__ tie, int64_t words, int32_t* __restrict__ idx_out,
+    int cap, int smem_words) {
     pdl_wait();
     pdl_trigger();
     namespace cg = cooperative_groups;
     cg::cluster_group cl = cg::this_cluster();
     extern __shared__ __align__(16) unsigned char fsm[];
     uint2* cs = reinterpret_cast<uint2*>(fsm);
-    uint2* ga = cs + kCap;                             // the whole row's candidates (fast path)
-    uint32_t* hmine = reinterpret_cast<uint32_t*>(fsm + 2 * (size_t)kCap * 8);
+    // shared memory (sizes from the launch): candidates [cap] | (clusters) the row's candidates [cap] |
+    // two histograms | two bitmaps [smem_words]
+    const bool clustered = cooperative_groups::this_cluster().num_blocks() > 1;
+    uint2* ga = clustered ? cs + cap : cs;             // the whole row's candidates (fast path)
+    uint32_t* hmine = reinterpret_cast<uint32_t*>(fsm + (clustered ? 2 : 1) * (size_t)cap * 8);
     uint32_t* hsum = hmine + kBins12;
     uint32_t* swin = hsum + kBins12;
-    uint32_t* stie = swin + kSmemWords;
+    uint32_t* stie = swin + smem_words;
     __shared__ int sh_scan[33];
     __shared__ int sh_res[2];
     __shared__ int sh_nc;
@@ -256,7 +260,7 @@ __global__ void __launch_bounds__(kSelThreads, 1) topk_select_kernel(
     const int64_t w_lo = nwords * p / P, w_hi = nwords * (p + 1) / P;
     const int64_t s_lo = w_lo * 32, s_hi = min(n, w_hi * 32);
     const int64_t sw = w_hi - w_lo;
-    const bool smem_bits = sw <= kSmemWords;
+    const bool smem_bits = sw <= smem_words;
     uint32_t* wr = smem_bits ? swin : win + (int64_t)r * words + w_lo;
     uint32_t* tr = smem_bits ? stie : tie + (int64_t)r * words + w_lo;
     // ---- boundary bin of the top 12 bits (every CTA, from the row's histogram)
@@ -270,23 +274,23 @@ __global__ void __launch_bounds__(kSelThreads, 1) topk_select_kernel(
     uint32_t above1;
     __syncthreads();                                  // the histogram copy
     find_bin(h, kBins12, (uint32_t)k, sh_scan, sh_res, &b1, &above1);
-    const bool fast = above1 + h[b1] <= (uint32_t)kCap;
+    const bool fast = above1 + h[b1] <= (uint32_t)cap;
     if (tid == 0) sh_nc = 0;
     for (int i = tid; i < kBins12; i += nthr) hmine[i] = 0;
     __syncthreads();
     // ---- candidates of the slice (spans of 1024 entries)
     if (fast) {
         const float tv = bin_floor_value(b1);
-        if (n00 > 0) collect_loaded(row, w00, n00, tv, vf, cs, &sh_nc, lane);
+        if (n00 > 0) collect_loaded(row, w00, n00, tv, vf, cs, &sh_nc, lane, cap);
         for (int64_t w0 = w00 + (int64_t)nw * kWarpSpan; w0 < s_hi; w0 += (int64_t)nw * kWarpSpan) {
             const int cnt = (int)min((int64_t)kWarpSpan, s_hi - w0);
             float v[32];
             load_span(row, w0, cnt, lane, v);
-            collect_loaded(row, w0, cnt, tv, v, cs, &sh_nc, lane);
+            collect_loaded(row, w0, cnt, tv, v, cs, &sh_nc, lane, cap);
         }
     }
     __syncthreads();
-    const int nc = fast ? min(sh_nc, kCap) : 0;
+    const int nc = fast ? min(sh_nc, cap) : 0;
     if (fast) {
         // ---- every CTA gathers the row's candidates from the cluster and resolves the row alone
         cl.sync();                                  // every candidate list is complete
@@ -298,7 +302,7 @@ __global__ void __launch_bounds__(kSelThreads, 1) topk_select_kernel(
         off[0] = 0;
 #pragma unroll
         for (int q = 0; q < kMaxCluster; ++q)
-            off[q + 1] = q < P ? min(off[q] + *cl.map_shared_rank(&sh_nc, q), kCap) : off[q];   // the row holds <= kCap
+            off[q + 1] = q < P ? min(off[q] + *cl.map_shared_rank(&sh_nc, q), cap) : off[q];   // the row holds <= cap
         const int tot = off[kMaxCluster];
         auto src_of = [&](int i) -> const uint2* {
             int q = 0, start = 0;
@@ -311,7 +315,7 @@ __global__ void __launch_bounds__(kSelThreads, 1) topk_select_kernel(
             const uint2* base = q == p ? cs : cl.map_shared_rank(cs, q);
             return base + (i - start);
         };
-        for (int i = tid; i < tot; i += 2 * nthr) {
+        for (int i = tid; clustered && i < tot; i += 2 * nthr) {   // (one CTA: its list is the row's)
             const int i2 = i + nthr;
             const uint2 x = *src_of(i);
             const uint2 y = i2 < tot ? *src_of(i2) : make_uint2(0u, 0u);
@@ -568,10 +572,17 @@ csahca_status topk_launch(const float* scores, int64_t stride, int R, const int6
     const int64_t spans = std::max<int64_t>(1, cdiv(stride, (int64_t)kWarpSpan * (kSelThreads / 32)));
     int P = (int)std::max<int64_t>(1, std::min<int64_t>(std::min<int64_t>(num_sms() / R, kMaxCluster), spans));
     while (P & (P - 1)) --P;                         // a power of two
+    // One CTA per row (many rows, short rows): a lean form -- 512 threads, 4096 candidates, bitmaps
+    // sized to the row, no gathered copy -- so that two CTAs share an SM.
+    const bool lean = P == 1 && tw.words <= 4096;
+    const int threads = lean ? 512 : kSelThreads;
+    const int cap = lean ? 4096 : kCap;
+    const int smem_words = lean ? (int)tw.words : kSmemWords;
+    const size_t smem = (size_t)(P > 1 ? 2 : 1) * cap * 8 + 2 * (size_t)kBins12 * 4 + 2 * (size_t)smem_words * 4;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)P, (unsigned)R);
-    cfg.blockDim = dim3(kSelThreads);
-    cfg.dynamicSmemBytes = kSelSmem;
+    cfg.blockDim = dim3(threads);
+    cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -583,7 +594,7 @@ csahca_status topk_launch(const float* scores, int64_t stride, int R, const int6
     cfg.attrs = attr;
     cfg.numAttrs = 2;
     (void)cudaLaunchKernelEx(&cfg, topk_select_kernel, scores, stride, n_vis_arr, q_pos, m, Ncap, k,
-                             tw.hist1, tw.win, tw.tie, tw.words, idx_out);
+                             tw.hist1, tw.win, tw.tie, tw.words, idx_out, cap, smem_words);
     count_launch();
     CSAHCA_CHECK_LAUNCH();
     return CSAHCA_OK;
