@@ -49,6 +49,8 @@ def _geometry(cache) -> dict:
          "dtype": _NAMES[cache.dtype]}
     if g["kind"] == "csa":
         g.update(d_I=int(cache.d_I), key_fmt=int(cache.key_fmt))
+    if getattr(cache, "kv_fp8", False):       # compressed K/V rows in FP8 (recorded only when set)
+        g["kv_fp8"] = True
     return g
 
 
@@ -137,6 +139,8 @@ def _check_schema(path: str, h) -> None:
         bad("kind")
     if h.get("dtype") not in _DTYPES:
         bad("dtype")
+    if "kv_fp8" in h and not isinstance(h["kv_fp8"], bool):
+        bad("kv_fp8")
     for key in ("m", "d", "W") + (("d_I", "key_fmt") if h["kind"] == "csa" else ()):
         if not _is_int(h.get(key)) or h[key] < 0:
             bad(key)
@@ -190,6 +194,8 @@ def load_prefix_into(path: str, cache, b: int, seq: int = 0) -> int:
     for key, val in g.items():
         if header.get(key) != val:
             raise ValueError(f"{path}: {key} = {header.get(key)!r}, the cache has {val!r}")
+    if bool(header.get("kv_fp8", False)) != bool(g.get("kv_fp8", False)):
+        raise ValueError(f"{path}: kv_fp8 = {header.get('kv_fp8', False)!r}, the cache has {g.get('kv_fp8', False)!r}")
     if not 0 <= seq < len(header["seqs"]):
         raise ValueError(f"{path}: no saved sequence {seq}")
     if not 0 <= b < cache.B:
@@ -222,11 +228,12 @@ def load_prefix(path: str, device="cuda", Ncap: int | None = None):
     Ncap = max(ns + [1]) if Ncap is None else int(Ncap)
     dt = _DTYPES[header["dtype"]]
     B = len(ns)
+    fp8 = bool(header.get("kv_fp8", False))
     if header["kind"] == "csa":
         cache = CSACache(B, Ncap, header["d"], header["W"], header["d_I"], header["key_fmt"], dt, device,
-                         m=header["m"])
+                         m=header["m"], kv_fp8=fp8)
     elif header["kind"] == "hca":
-        cache = HCACache(B, Ncap, header["d"], header["W"], dt, device, m=header["m"])
+        cache = HCACache(B, Ncap, header["d"], header["W"], dt, device, m=header["m"], kv_fp8=fp8)
     else:
         raise ValueError(f"{path}: unknown cache kind {header['kind']!r}")
     return cache, [load_prefix_into(path, cache, i, i) for i in range(B)]

@@ -132,3 +132,34 @@ def test_malformed_headers_are_refused_with_value_error(tmp_path, edit):
     dst = HCACache(2, 8, 64, 16, torch.bfloat16, "cpu", m=128)
     with pytest.raises(ValueError):
         cache_io.load_prefix_into(str(bad), dst, 0)
+
+
+def test_fp8_cache_round_trip_and_mismatch(tmp_path):
+    # FP8 compressed K/V rows (uint8) are saved and restored as bytes; the flag travels in the
+    # header, and a bf16 cache refuses an FP8 file
+    src = _fill(CSACache(2, 40, 128, 16, 64, L.KEY_FMT["e2m1"], torch.bfloat16, "cpu", kv_fp8=True), 7)
+    assert src.ck.dtype == torch.uint8 and src.ck.shape[-1] == L.KV_FP8_K_ROW
+    p = str(tmp_path / "fp8.kv")
+    cache_io.save_prefix(p, src, [4 * 33 + 1, 9])
+    dst, got = cache_io.load_prefix(p, device="cpu")
+    assert dst.kv_fp8 and got == [4 * 33 + 1, 9]
+    for b, n in enumerate(got):
+        _same(_state(src, b, n), _state(dst, b, n))
+    plain = CSACache(2, 40, 128, 16, 64, L.KEY_FMT["e2m1"], torch.bfloat16, "cpu")
+    with pytest.raises(ValueError, match="kv_fp8"):
+        cache_io.load_prefix_into(p, plain, 0)
+    p2 = str(tmp_path / "bf16.kv")
+    cache_io.save_prefix(p2, _fill(plain, 8), [4 * 20, 0])
+    with pytest.raises(ValueError, match="kv_fp8"):
+        cache_io.load_prefix_into(p2, src, 0)
+
+
+def test_fp8_hca_prefix_into_a_slot(tmp_path):
+    src = _fill(HCACache(2, 9, 128, 128, torch.bfloat16, "cpu", kv_fp8=True), 8)
+    p = str(tmp_path / "hca8.kv")
+    cache_io.save_prefix(p, src, [128 * 6 + 3, 128])
+    dst = _fill(HCACache(3, 12, 128, 128, torch.bfloat16, "cpu", kv_fp8=True), 9)
+    n = cache_io.load_prefix_into(p, dst, 2, seq=0)
+    assert n == 128 * 6 + 3
+    _same(_state(src, 0, n), _state(dst, 2, n))
+    assert not dst.ck[2, 6:].any() and not dst.cv[2, 6:].any()
