@@ -111,15 +111,35 @@ struct Maps {
 // row): every row is cut into ceil(tiles / L) pieces of near-equal length, L the smallest length
 // >= the average tiles per CTA for which all pieces fit the grid and no row has more than S
 // pieces; CTA c takes the c-th piece (row by row), whose partial result goes to slot = piece
-// index.  Kept out of line: it runs once per CTA and its code should not crowd the tile loop.
-__device__ __noinline__ void piece_schedule(const AttendArgs& a, int S, int nt_w, Misc& ms, int lane) {
-    const int R = a.B * a.T;
+// index.  The general form is kept out of line (it runs once per CTA and its code should not crowd
+// the tile loop); its inputs come by value: the kernel's parameters, read through a reference in
+// an out-of-line call, take a generic load each (about 0.5 us for the schedule's few fields).
+struct SchedIn {
+    const int64_t* q_pos;
+    int64_t Ncap;
+    int R, m, k, is_csa;
+};
+
+__device__ __forceinline__ int compressed_tiles(const SchedIn& si, int64_t p) {
+    int64_t n;
+    if (si.is_csa) {
+        n = si.k;
+    } else {
+        n = (p < 0) ? 0 : ((si.m & (si.m - 1)) == 0 ? (p + 1) >> (__ffs(si.m) - 1) : (p + 1) / si.m);
+        n = n < si.Ncap ? n : si.Ncap;
+    }
+    return (int)cdiv(n, kKeys);
+}
+
+// Up to 32 rows (the decode batches), one row per lane: the same schedule in registers and
+// shuffles, inlined (the out-of-line call's first instruction fetch costs about 0.4 us).
+__device__ __forceinline__ void piece_schedule_rows32(const SchedIn& si, int S, int nt_w, Misc& ms, int lane) {
+    const int R = si.R;
     const int G = (int)gridDim.x, c = (int)blockIdx.x;
-    if (R <= 32) {
-        // one row per lane (the decode batches): the same schedule in registers and shuffles
+    {
         const bool in = lane < R;
-        const int64_t pq = in ? a.q_pos[lane] : 0;
-        const int nt = in ? (int)cdiv(key_list(a, lane, 0, pq).n_c, kKeys) + nt_w : 0;
+        const int64_t pq = in ? si.q_pos[lane] : 0;
+        const int nt = in ? compressed_tiles(si, pq) + nt_w : 0;
         int total = nt, ntmax = nt;
         for (int o = 16; o > 0; o >>= 1) {
             total += __shfl_xor_sync(0xffffffffu, total, o);
@@ -157,12 +177,21 @@ __device__ __noinline__ void piece_schedule(const AttendArgs& a, int S, int nt_w
             if (piece == 0) ms.my_slots_from = np;
         }
         if (in && np == 0 && lane == c) ms.my_empty_row = lane;   // R <= gridDim.x
-        return;
     }
+}
+
+// (out of line where inlining it would push the tile loop's registers into spills)
+__device__ __noinline__ void piece_schedule_rows32_ool(const SchedIn si, int S, int nt_w, Misc& ms, int lane) {
+    piece_schedule_rows32(si, S, nt_w, ms, lane);
+}
+
+__device__ __noinline__ void piece_schedule(const SchedIn si, int S, int nt_w, Misc& ms, int lane) {
+    const int R = si.R;
+    const int G = (int)gridDim.x, c = (int)blockIdx.x;
     int total = 0, ntmax = 0;
 #pragma unroll 1
     for (int q = lane; q < R; q += 32) {
-        const int n = (int)cdiv(key_list(a, q, 0, a.q_pos[q]).n_c, kKeys) + nt_w;
+        const int n = compressed_tiles(si, si.q_pos[q]) + nt_w;
         ms.snt[q] = n;
         total += n;
         ntmax = max(ntmax, n);
@@ -208,7 +237,7 @@ __device__ __noinline__ void piece_schedule(const AttendArgs& a, int S, int nt_w
             ms.my_piece = piece;
             ms.my_t0 = t0;
             ms.my_nt = (piece + 1) * nt / np - t0;
-            ms.my_p = a.q_pos[q];
+            ms.my_p = si.q_pos[q];
             ms.my_np = np;
             if (piece == 0) ms.my_slots_from = np;
         }
@@ -563,7 +592,13 @@ __global__ void __launch_bounds__(Thr<H, F8>::kThreads, 1)
                 ms.my_np = fixed_np;
             }
         } else {
-            piece_schedule(a, S, nt_w, ms, lane);
+            const SchedIn si{a.q_pos, a.Ncap, R, a.m, a.k, a.is_csa};
+            if (R <= 32) {
+                if constexpr (F8) piece_schedule_rows32_ool(si, S, nt_w, ms, lane);
+                else piece_schedule_rows32(si, S, nt_w, ms, lane);
+            } else {
+                piece_schedule(si, S, nt_w, ms, lane);
+            }
         }
     }
     fence_before_sync();
@@ -673,8 +708,8 @@ __global__ void __launch_bounds__(Thr<H, F8>::kThreads, 1)
             for (int i = tid; i < H * kD / 8; i += kSoft) orow[i] = make_uint4(0u, 0u, 0u, 0u);
             if (a.lse && tid < H) a.lse[er * H + tid] = -INFINITY;
         }
-        // After an item's partial is written: count the arrival at its row (one release fence,
-        // cumulative over the barrier); the row's last item merges the row's partial results
+        // After an item's partial is written: count the arrival at its row (one acquire-release
+        // atomic, cumulative over the barrier); the row's last item merges the row's partial results
         // exactly, slots s = 0, 1, ... in that order (slots with lse = -inf hold no keys):
         //     lse = log sum_s exp(lse_s),  o = sum_s exp(lse_s - lse) o_s,
         // and resets the counter (merge_row).
@@ -682,10 +717,12 @@ __global__ void __launch_bounds__(Thr<H, F8>::kThreads, 1)
         auto arrive_and_merge = [&](const ItemTiles& itm) {
             named_barrier_sync(1, kSoft);
             if (tid == 0) {
-                __threadfence();
-                const bool last = atomicAdd(&row_cnt[itm.r], 1u) + 1u == (unsigned)itm.expect;
-                if (last) __threadfence();
-                ms.merge_now = last;
+                // acq_rel: releases this CTA's partial (the barrier above orders every thread's
+                // stores before it) and, for the last arrival, acquires the other items' partials
+                unsigned before;
+                asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;"
+                             : "=r"(before) : "l"(&row_cnt[itm.r]) : "memory");
+                ms.merge_now = before + 1u == (unsigned)itm.expect;
             }
             named_barrier_sync(1, kSoft);
             if (!ms.merge_now) return;
