@@ -195,39 +195,53 @@ __global__ void __launch_bounds__(kThreadsP, 1) index_prefill_kernel(
             const int4 itm = ms.item[qs];
             if (itm.w) break;
             const int r0 = itm.x, key0 = itm.y;
+            // this thread's rows hh QR/2 + j, j < QR/2, own the 64 consecutive accumulator columns
+            // [64 hh, 64 hh + 64) of a tile (QR/2 rows x H_I heads): their head weights, in registers
+            // for the whole item
+            constexpr int kCols = (QR / 2) * HI;
+            static_assert(kCols == 64, "64 columns per epilogue thread");
             int nv[QR / 2];
 #pragma unroll
             for (int j = 0; j < QR / 2; ++j) nv[j] = ms.nvis[qs][hh * (QR / 2) + j];
+            uint64_t wv[kCols / 2];
+#pragma unroll
+            for (int k = 0; k < kCols; k += 2) {
+                const float2 x = *reinterpret_cast<const float2*>(&ms.w[qs][hh * kCols + k]);
+                wv[k / 2] = f2_pack(x.x, x.y);
+            }
             for (int t = 0; t < itm.z; ++t, ++dn) {
                 const uint32_t d = dn & 1;
                 mbar_wait(&ms.dfull[d], (dn >> 1) & 1, err);
                 fence_after_sync();
                 const int key = key0 + t * kKeysT + key_l;
+                // all 64 columns in one round trip, then the accumulator goes back to the MMA warp
+                uint32_t v[kCols];
+#pragma unroll
+                for (int c = 0; c < kCols; c += 16) {
+                    uint32_t t16[16];
+                    tmem_ld16(tmem + d * 128 + lane_off + hh * kCols + c, t16);
+#pragma unroll
+                    for (int k = 0; k < 16; ++k) v[c + k] = t16[k];
+                }
+                tmem_wait_ld();
+                fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&ms.dfree[d]);
                 float sc[QR / 2];
 #pragma unroll
                 for (int j = 0; j < QR / 2; ++j) {
-                    const int row = hh * (QR / 2) + j;
                     uint64_t acc = f2_pack(0.0f, 0.0f);
 #pragma unroll
-                    for (int c0 = 0; c0 < HI; c0 += 16) {
-                        uint32_t v[16];
-                        tmem_ld16(tmem + d * 128 + lane_off + row * HI + c0, v);
-                        tmem_wait_ld();
-#pragma unroll
-                        for (int k = 0; k < 16; k += 2) {
-                            const float2 wv = *reinterpret_cast<const float2*>(&ms.w[qs][row * HI + c0 + k]);
-                            acc = f2_fma(f2_pack(wv.x, wv.y),
-                                         f2_pack(fmaxf(__uint_as_float(v[k]), 0.0f), fmaxf(__uint_as_float(v[k + 1]), 0.0f)),
-                                         acc);
-                        }
+                    for (int k = 0; k < HI; k += 2) {
+                        const int c = j * HI + k;
+                        acc = f2_fma(wv[c / 2],
+                                     f2_pack(fmaxf(__uint_as_float(v[c]), 0.0f), fmaxf(__uint_as_float(v[c + 1]), 0.0f)),
+                                     acc);
                     }
                     float a0, a1;
                     f2_unpack(acc, a0, a1);
                     sc[j] = a0 + a1;
                 }
-                fence_before_sync();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&ms.dfree[d]);
 #pragma unroll
                 for (int j = 0; j < QR / 2; ++j) {
                     const int row = hh * (QR / 2) + j;
