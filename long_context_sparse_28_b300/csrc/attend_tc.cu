@@ -575,6 +575,9 @@ __global__ void __launch_bounds__(Thr<H, F8>::kThreads, 1)
     // With few query rows each CTA takes one piece of one row (piece_schedule); otherwise items
     // are (row, split) pairs, split s holding tiles [s kps, (s+1) kps).
     const bool pieces = R <= kSchedRows && R <= (int)gridDim.x && S >= 2;
+    // one split per row (many rows): each item is a whole row, written as the final output (bf16,
+    // and the lse) with no merge
+    const bool direct = !pieces && S == 1;
     if (pieces && warp == 0) {
         if (fixed_np > 0) {
             // every row has the same tiles (CSA: k selected entries + the window); the host cut
@@ -739,9 +742,14 @@ __global__ void __launch_bounds__(Thr<H, F8>::kThreads, 1)
             const __nv_bfloat16* qr = static_cast<const __nv_bfloat16*>(a.q) + (int64_t)r * H * kD;
 
             if (nt == 0) {                       // a slot without keys: o = 0 (finite), lse = -inf
-#pragma unroll 1
-                for (int i = tid; i < H * kD; i += kSoft) o_part[obase * kD + i] = 0.0f;
-                if (tid < H) lse_part[obase + tid] = -INFINITY;
+                if (direct) {
+                    __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(a.out) + obase * kD;
+                    for (int i = tid; i < H * kD; i += kSoft) orow[i] = __float2bfloat16(0.0f);
+                    if (a.lse && tid < H) a.lse[obase + tid] = -INFINITY;
+                } else {
+                    for (int i = tid; i < H * kD; i += kSoft) o_part[obase * kD + i] = 0.0f;
+                    if (tid < H) lse_part[obase + tid] = -INFINITY;
+                }
                 if (pieces) arrive_and_merge(it);
                 continue;
             }
@@ -994,7 +1002,9 @@ __global__ void __launch_bounds__(Thr<H, F8>::kThreads, 1)
                 const float m = ms.mrun[tid];
                 const bool any = (l > 0.0f) && (m != -INFINITY);
                 ms.linv[tid] = any ? 1.0f / l : 0.0f;
-                lse_part[obase + tid] = any ? (m + log2f(l)) * 0.6931471805599453f : -INFINITY;
+                const float lse = any ? (m + log2f(l)) * 0.6931471805599453f : -INFINITY;
+                if (!direct) lse_part[obase + tid] = lse;
+                else if (a.lse) a.lse[obase + tid] = lse;
             }
             named_barrier_sync(1, kSoft);
             mbar_wait(&ms.odone, (g + (uint32_t)nt - 1) & 1, err);
@@ -1008,7 +1018,9 @@ __global__ void __launch_bounds__(Thr<H, F8>::kThreads, 1)
 #pragma unroll
                 for (int k = 0; k < 16; ++k) {
                     const int h = wg * HG + c0 + k;
-                    o_part[(obase + h) * kD + row] = __uint_as_float(rr[k]) * ms.linv[h];
+                    const float o = __uint_as_float(rr[k]) * ms.linv[h];
+                    if (direct) static_cast<__nv_bfloat16*>(a.out)[(obase + h) * kD + row] = __float2bfloat16(o);
+                    else o_part[(obase + h) * kD + row] = o;
                 }
             }
             fence_before_sync();
@@ -1081,11 +1093,11 @@ cudaError_t launch_tc(const AttendArgs& a, int S, int kps, float* o_part, float*
 bool attend_tc_merges(const AttendArgs& a, int S) {
     // the kernel's piece schedule (few rows) merges in the row's last CTA; with many rows every
     // CTA takes (row, split) items and the shared merge kernel follows (it spreads the merges of
-    // many rows over the whole GPU)
+    // many rows over the whole GPU), unless a row is one split, written out directly
     const int R = a.B * a.T;
     const int items = R * S;
     const int grid = items < num_sms() ? items : num_sms();
-    return R <= kSchedRows && R <= grid && S >= 2;
+    return S == 1 || (R <= kSchedRows && R <= grid && S >= 2);
 }
 
 bool attend_tc_supported(const AttendArgs& a) {
