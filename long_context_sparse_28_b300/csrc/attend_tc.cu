@@ -83,6 +83,7 @@ struct alignas(16) Misc {
     alignas(16) float alpha[64];     // read as float4
     float linv[64];
     unsigned char valid[4][kKeys];   // per tile (ring of 4): row holds a key of this query
+    int32_t eidx[4][kKeys];          // per tile (ring of 4), CSA: the row's selected entry (-1: none)
     int snt[kSchedRows];             // piece schedule: tiles of each query row
     int my_row, my_piece, my_t0, my_nt;  // piece schedule: this CTA's piece (row -1: none), its
     int my_empty_row;                // row's slots [my_slots_from, S) it marks empty, a row
@@ -252,11 +253,17 @@ __device__ __noinline__ void piece_schedule(const SchedIn si, int S, int nt_w, M
 // thread 0; otherwise the rows are gathered with cp.async (kSoft / 128 threads per row).  With
 // `track_cp` every thread's arrival waits for all its earlier cp.async copies (the query tile
 // loaded just before), else a TMA tile's arrivals are made at once by thread 0.
+// CSA selected entries: a K tile records each row's entry in e_dst[row]; a V tile reads them from
+// e_src (its K tile's record) instead of the index list, and a K tile takes the thread's row's
+// entry from e_pre when the caller loaded it ahead (else kNoEntry: read here).
+constexpr int32_t kNoEntry = INT32_MIN;
+
 template <int kSoft>
 __device__ __forceinline__ void load_tile(const AttendArgs& a, const Maps& maps, int use_tma_c, int use_tma_w, int r,
                                        int b, int64_t p, int64_t n_c, int64_t total, int nt_c, int ti, bool is_v,
                                        uint32_t dst, uint64_t* bar, unsigned char* valid, const void* zsrc,
-                                       uint64_t pol, bool track_cp, unsigned* err) {
+                                       uint64_t pol, bool track_cp, unsigned* err, int32_t* e_dst = nullptr,
+                                       const int32_t* e_src = nullptr, int32_t e_pre = kNoEntry) {
     const int tid = threadIdx.x;
     const bool comp = ti < nt_c;
     if (comp ? use_tma_c : use_tma_w) {
@@ -282,11 +289,29 @@ __device__ __forceinline__ void load_tile(const AttendArgs& a, const Maps& maps,
     const bool in = key < (comp ? n_c : total);
     const __nv_bfloat16* kp = nullptr;
     const __nv_bfloat16* vp = nullptr;
-    KeyList kl;
-    kl.n_c = n_c;
-    kl.total = total;
-    if (in) key_rows<__nv_bfloat16>(a, kl, r, b, p, key, &kp, &vp, err);
-    if (!is_v && part == 0) valid[rr] = kp != nullptr;
+    int32_t e = -1;
+    if (in && comp && a.is_csa) {
+        // (the selected-entry path of key_rows, with the entry possibly known already)
+        e = e_src ? e_src[rr] : (e_pre != kNoEntry ? e_pre : a.idx[(int64_t)r * a.k + key]);
+        if (e >= a.Ncap) {
+            flag_error(err, ERRBIT_BOUNDS);
+            e = -1;
+        }
+        if (e >= 0) {
+            const int64_t off = ((int64_t)b * a.Ncap + e) * a.d;
+            kp = static_cast<const __nv_bfloat16*>(a.ck) + off;
+            vp = static_cast<const __nv_bfloat16*>(a.cv) + off;
+        }
+    } else if (in) {
+        KeyList kl;
+        kl.n_c = n_c;
+        kl.total = total;
+        key_rows<__nv_bfloat16>(a, kl, r, b, p, key, &kp, &vp, err);
+    }
+    if (!is_v && part == 0) {
+        valid[rr] = kp != nullptr;
+        if (e_dst) e_dst[rr] = e < 0 ? -1 : e;
+    }
     const __nv_bfloat16* src = is_v ? vp : kp;
 #pragma unroll
     for (int c = 0; c < kCpt; ++c) {
@@ -757,6 +782,7 @@ __global__ void __launch_bounds__(Thr<H, F8>::kThreads, 1)
 
             // Tile i's loads are the (g + i)-th of each ring, so slot = (g + i) & 1.
             // (FP8 caches: every load completes on k8full / v8full, the converters pass it on)
+            int32_t e_next = kNoEntry;               // (CSA) this thread's row's entry of the next K gather
             auto load = [&](int i, bool is_v) {
                 const uint32_t seq = g + (uint32_t)i;
                 const uint32_t dst = sbase + (is_v ? L::v : L::k) + (seq & 1) * kTile;
@@ -768,7 +794,18 @@ __global__ void __launch_bounds__(Thr<H, F8>::kThreads, 1)
                                         i == 0 && !is_v, err);
                 else
                     load_tile<kSoft>(a, maps, use_tma_c, use_tma_w, r, b, p, kl.n_c, kl.total, nt_c, t0 + i, is_v,
-                                     dst, bar, ms.valid[seq & 3], qr, pol_stream, i == 0 && !is_v, err);
+                                     dst, bar, ms.valid[seq & 3], qr, pol_stream, i == 0 && !is_v, err,
+                                     is_v ? nullptr : ms.eidx[seq & 3],
+                                     (is_v && i > 0) ? ms.eidx[seq & 3] : nullptr,   // (V(0): its K record is
+                                     is_v ? kNoEntry : e_next);                       //  not visible yet)
+            };
+            // CSA gathers: the entry of this thread's row in the tile after next, loaded one tile
+            // ahead (the K gather then issues without waiting on the index list)
+            const int kTprL = kSoft / kKeys;
+            auto entry_ahead = [&](int i) -> int32_t {
+                const int64_t key = (int64_t)(t0 + i) * kKeys + tid / kTprL;
+                if (F8 || !a.is_csa || i >= nt || t0 + i >= nt_c || key >= kl.n_c) return kNoEntry;
+                return a.idx[(int64_t)r * a.k + key];
             };
 
             // FP8 caches: tile i's codes -> bf16 in place by the softmax warps, then the tile is
@@ -798,9 +835,11 @@ __global__ void __launch_bounds__(Thr<H, F8>::kThreads, 1)
                 const int h = c >> 4, cc = c & 15;
                 cp_async16(sbase + L::q + (cc >> 3) * L::q_half + sw128(h, cc & 7), qr + h * kD + cc * 8, 16);
             }
+            e_next = kNoEntry;
             load(0, false);
             if (nt > 1) load(1, false);
             load(0, true);
+            e_next = entry_ahead(2);
             named_barrier_sync(1, kSoft);                  // valid[] of tiles 0 and 1
             if constexpr (F8) conv(0, false, false);
 
@@ -846,6 +885,7 @@ __global__ void __launch_bounds__(Thr<H, F8>::kThreads, 1)
                 };
                 // K slot of tile i is free (MMA1(i) complete)
                 if (i + 2 < nt) load(i + 2, false);
+                e_next = entry_ahead(i + 3);
                 // ---- P = 2^(s c - m) with the running maxima m, exponents capped at the threshold.
                 // When some score exceeds its head's running maximum by more than the threshold
                 // (always on an item's first tile, which skips this pass) the maxima are raised
