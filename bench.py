@@ -869,50 +869,81 @@ def run_prefill(args, dist):
 
 
 def run_e2e_prefill(bench, w, n, dev, dist):
-    """The public API end to end: each step copies the chunk's inputs from pinned host memory,
-    runs the chunk's calls (one CUDA graph) and reads both layers' outputs back into pinned host
-    memory, all inside the timed region."""
+    """The public API end to end, as a serving loop would drive it: each step copies the chunk's
+    inputs from pinned host memory, runs the chunk's calls (one CUDA graph per buffer) and reads
+    both layers' outputs back into pinned host memory, all inside the timed region.  Inputs and
+    outputs are double-buffered: the copy-in of step i+1 and the read-back of step i-1 run on their
+    own streams (copy engines) while step i computes."""
     L = bench.L
-    host = [t.to("cpu").pin_memory() for t in bench.args]
-    dev_in = [torch.empty_like(t) for t in bench.args]
-    out_host = [torch.empty(bench.step_.out_c.shape, dtype=torch.bfloat16, pin_memory=True) for _ in range(2)]
-    stream = torch.cuda.Stream(device=dev)
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.stream(stream):
-        for d_, h_ in zip(dev_in, host):
-            d_.copy_(h_)
-        bench.step(dev_in)
-        stream.synchronize()
-        with torch.cuda.graph(g, stream=stream, capture_error_mode="relaxed"):
-            bench.step(dev_in)
+    st = bench.step_
+    host = [t.to("cpu").pin_memory() for t in bench.args]          # the chunk, re-sent every step
+    dev_in = [[torch.empty_like(t) for t in bench.args] for _ in range(2)]
+    outs = [(torch.empty_like(st.out_c), torch.empty_like(st.out_h)) for _ in range(2)]
+    out_host = [[torch.empty(st.out_c.shape, dtype=torch.bfloat16, pin_memory=True) for _ in range(2)]
+                for _ in range(2)]
+    cs, hs, ds = (torch.cuda.Stream(device=dev) for _ in range(3))
+    saved = (st.out_c, st.out_h)
+    graphs = []
+    with torch.cuda.stream(cs):
+        for b in range(2):
+            for d_, h_ in zip(dev_in[b], host):
+                d_.copy_(h_)
+            st.out_c, st.out_h = outs[b]
+            bench.step(dev_in[b])
+            cs.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=cs, capture_error_mode="relaxed"):
+                bench.step(dev_in[b])
+            graphs.append(g)
+    st.out_c, st.out_h = saved
     torch.cuda.synchronize()
+    h2d_done = [torch.cuda.Event() for _ in range(2)]
+    comp_done = [torch.cuda.Event() for _ in range(2)]
+    d2h_done = [torch.cuda.Event() for _ in range(2)]
 
-    def one():
-        for d_, h_ in zip(dev_in, host):
-            d_.copy_(h_, non_blocking=True)
-        g.replay()
-        out_host[0].copy_(bench.step_.out_c, non_blocking=True)
-        out_host[1].copy_(bench.step_.out_h, non_blocking=True)
+    def run(i0, i1, start_ev):
+        hs.wait_event(start_ev)
+        for i in range(i0, i1):
+            b = i & 1
+            if i - i0 >= 2:
+                hs.wait_event(comp_done[b])            # step i-2 has consumed this input buffer
+            with torch.cuda.stream(hs):
+                for d_, h_ in zip(dev_in[b], host):
+                    d_.copy_(h_, non_blocking=True)
+                h2d_done[b].record(hs)
+            cs.wait_event(h2d_done[b])
+            if i - i0 >= 2:
+                cs.wait_event(d2h_done[b])             # step i-2's outputs have been read back
+            graphs[b].replay()
+            comp_done[b].record(cs)
+            ds.wait_event(comp_done[b])
+            with torch.cuda.stream(ds):
+                out_host[b][0].copy_(outs[b][0], non_blocking=True)
+                out_host[b][1].copy_(outs[b][1], non_blocking=True)
+                d2h_done[b].record(ds)
+        cs.wait_event(d2h_done[(i1 - 1) & 1])
+        cs.wait_event(d2h_done[(i1 - 2) & 1])
 
-    with torch.cuda.stream(stream):
-        for _ in range(2):
-            one()
+    with torch.cuda.stream(cs):
+        ev = torch.cuda.Event()
+        ev.record(cs)
+        run(0, 2, ev)
     torch.cuda.synchronize()
     dist.barrier()
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        t0.record(stream)
-        for _ in range(n):
-            one()
-        t1.record(stream)
+    with torch.cuda.stream(cs):
+        t0.record(cs)
+        run(2, 2 + n, t0)
+        t1.record(cs)
     torch.cuda.synchronize()
     ms = dist.max(t0.elapsed_time(t1)) / n
     assert L.device_status() == 0
     return {"value": round(w.T * dist.world / (ms / 1e3), 1), "unit": "query tokens/s", "ms_per_step": round(ms, 4),
             "h2d_bytes_per_step": int(sum(t.numel() * t.element_size() for t in host)),
-            "d2h_bytes_per_step": int(sum(t.numel() * t.element_size() for t in out_host)),
+            "d2h_bytes_per_step": int(sum(t.numel() * t.element_size() for t in out_host[0])),
             "path": "per step: H2D copy of the chunk's inputs from pinned host memory, the chunk's C-ABI calls "
-                    "(one CUDA graph), D2H copy of both layers' outputs, on one stream"}
+                    "(one CUDA graph per buffer), D2H copy of both layers' outputs; inputs and outputs "
+                    "double-buffered on copy streams"}
 
 
 # ------------------------------------------------------------------------- bulk pooling
