@@ -521,6 +521,32 @@ def test_attend_tensor_core_row_without_keys_gives_zero():
     np.testing.assert_allclose(npy(lse[1, 0]), ls, rtol=1e-5, atol=1e-5)
 
 
+def test_attend_many_rows_one_split_written_directly():
+    # more rows than the piece schedule takes and one split per row: every row is one item whose
+    # CTA writes the bf16 output and lse itself (no partials, no merge launch); rows without keys
+    # (no complete block, W = 0) give o = 0, lse = -inf
+    B, H, d, m, Ncap = 300, 64, 128, 128, 8
+    ck, cv, _, _ = _rand_cache(B, Ncap, 1, d, "bf16", 54)
+    q = rnd((B, 1, H, d), torch.bfloat16, 55, d ** -0.5)
+    rng = np.random.default_rng(56)
+    pos = rng.integers(0, m * Ncap, size=B)
+    pos[::7] = rng.integers(0, m - 1, size=len(pos[::7]))      # no complete block yet
+    out = torch.full((B, 1, H, d), 9.0, dtype=torch.bfloat16, device="cuda")
+    lse = torch.zeros(B, 1, H, device="cuda")
+    L.hca_attend(q, d ** -0.5, ck, cv, m, None, None, 0, dev_i64(pos), out, lse)
+    torch.cuda.synchronize()
+    assert L.device_status() == 0
+    o_g, l_g = npy(out), npy(lse)
+    for b in range(B):
+        n = (int(pos[b]) + 1) // m
+        if n == 0:
+            assert (o_g[b] == 0).all() and np.isneginf(l_g[b]).all(), b
+            continue
+        o, ls = oracle.attend(npy(q[b, 0]), d ** -0.5, npy(ck[b]), npy(cv[b]), np.arange(n), None, None, [])
+        assert_close(out[b, 0], o, "bf16", f"row {b}")
+        np.testing.assert_allclose(l_g[b, 0], ls, rtol=1e-5, atol=1e-5)
+
+
 def test_workspace_state_is_cleared_by_every_call():
     # the top-k's per-row histograms and the attention's per-row arrival counters live in the
     # caller's workspace: after each call they are zero again, so calls on one workspace give the
