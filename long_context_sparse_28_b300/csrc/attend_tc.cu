@@ -493,7 +493,9 @@ __device__ __noinline__ void merge_row(int r, int ns, int S, const float* __rest
     float4 acc[kUnits];
 #pragma unroll
     for (int u = 0; u < kUnits; ++u) acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-    float mx = -INFINITY, tot = 0.0f;              // per head (threads tid < H)
+    static_assert(kSoft == 8 * H && kMergeStage <= 8, "eight merging threads per head, one slot each");
+    const int wh = tid >> 3, wq = tid & 7;         // head wh, slot wq of a pass (kMergeStage <= 8)
+    float mx = -INFINITY, tot = 0.0f;              // per head (its eight threads hold the same values)
     for (int s0 = 0; s0 < ns; s0 += kMergeStage) {
         const int nsl = min(kMergeStage, ns - s0);
         if (tid == 0) {
@@ -505,19 +507,24 @@ __device__ __noinline__ void merge_row(int r, int ns, int S, const float* __rest
         }
         mbar_wait(&ms.mfull, mpass & 1, err);
         ++mpass;
-        if (tid < H) {
-            float m2 = mx;
-            for (int q = 0; q < nsl; ++q) m2 = fmaxf(m2, ms.mw[q * H + tid]);
+        {
+            // a head's slots over its eight threads: the maximum by shuffles, one exponential per
+            // thread, then the sum in slot order (as one thread would add them)
+            const float ls = wq < nsl ? ms.mw[wq * H + wh] : -INFINITY;
+            float m2 = fmaxf(mx, ls);
+#pragma unroll
+            for (int o = 1; o < 8; o <<= 1) m2 = fmaxf(m2, __shfl_xor_sync(0xffffffffu, m2, o));
             const float rs = (m2 == -INFINITY) ? 0.0f : expf(mx - m2);   // 0 on the first pass
+            const float e = ls == -INFINITY ? 0.0f : expf(ls - m2);
             tot *= rs;
-            for (int q = 0; q < nsl; ++q) {
-                const float ls = ms.mw[q * H + tid];
-                const float e = ls == -INFINITY ? 0.0f : expf(ls - m2);
-                tot += e;
-                ms.mw[q * H + tid] = e;
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                const float eq = __shfl_sync(0xffffffffu, e, (tid & ~7) | q);
+                if (q < nsl) tot += eq;
             }
             mx = m2;
-            ms.alpha[tid] = rs;
+            if (wq < nsl) ms.mw[wq * H + wh] = e;
+            if (wq == 0) ms.alpha[wh] = rs;
         }
         named_barrier_sync(1, kSoft);
 #pragma unroll
@@ -540,9 +547,9 @@ __device__ __noinline__ void merge_row(int r, int ns, int S, const float* __rest
         }
         named_barrier_sync(1, kSoft);                  // the staging is reused by the next pass
     }
-    if (tid < H) {
-        ms.linv[tid] = tot > 0.0f ? 1.0f / tot : 0.0f;
-        if (lse_out) lse_out[(int64_t)r * H + tid] = tot > 0.0f ? mx + logf(tot) : -INFINITY;
+    if (wq == 0) {
+        ms.linv[wh] = tot > 0.0f ? 1.0f / tot : 0.0f;
+        if (lse_out) lse_out[(int64_t)r * H + wh] = tot > 0.0f ? mx + logf(tot) : -INFINITY;
     }
     named_barrier_sync(1, kSoft);
     fence_proxy_async();              // the staging reads, before the next item's copies into the buffers
