@@ -186,12 +186,11 @@ cudaError_t index_tc_q4_launch(const void* q_codes, const void* q_scale, const f
                                const void* k_scale, int B, int T, int H_I, const int64_t* q_pos, int64_t Ncap, int m,
                                float* S, uint32_t* hist1, unsigned* err, cudaStream_t st);
 // Tensor-core indexer scores for chunked prefill (bf16 keys and queries, d_I = 64, T a multiple of
-// 128 / H_I); hist1 as above.
+// 128 / H_I); scores only (the top-k forms its first histogram in a pass of its own).
 bool index_prefill_supported(int q_dtype, int key_fmt, int H_I, int d_I, int64_t Ncap, const void* q_idx,
                              const void* k_codes, int B, int T);
 cudaError_t index_prefill_launch(const void* q_idx, const float* w, const void* k_codes, int B, int T, int H_I,
-                                 const int64_t* q_pos, int64_t Ncap, int m, float* S, uint32_t* hist1, unsigned* err,
-                                 cudaStream_t st);
+                                 const int64_t* q_pos, int64_t Ncap, int m, float* S, unsigned* err, cudaStream_t st);
 
 // Top-k over float32 scores (rows of `stride`, n_vis per row from q_pos or n_vis arrays).
 struct TopkWorkspace {

@@ -137,8 +137,9 @@ static csahca_status index_validate(const void* q_idx, csahca_dtype q_dtype, con
     return CSAHCA_OK;
 }
 
-// Launches the scores kernel; with a non-null hist1 the tensor-core kernel also accumulates the
-// top-k histogram (*hist_done = true), the generic kernel does not.
+// Launches the scores kernel; with a non-null hist1 the decode tensor-core kernel also accumulates
+// the top-k histogram (*hist_done = true); the prefill and generic kernels do not (the top-k then
+// forms it in a pass of its own).
 static csahca_status index_scores_launch(const void* q_idx, csahca_dtype q_dtype, const float* w,
                                          const void* k_codes, const void* k_scale, csahca_dtype key_fmt, int B,
                                          int T, int H_I, int d_I, const int64_t* q_pos, int64_t Ncap, int m,
@@ -159,10 +160,9 @@ static csahca_status index_scores_launch(const void* q_idx, csahca_dtype q_dtype
     if (index_prefill_supported(q_dtype, key_fmt, H_I, d_I, Ncap, q_idx, k_codes, B, T)) {
         unsigned* err = err_word();
         if (!err) return CSAHCA_ERR_CUDA;
-        const cudaError_t e = index_prefill_launch(q_idx, w, k_codes, B, T, H_I, q_pos, Ncap, m, S, hist1, err, st);
+        const cudaError_t e = index_prefill_launch(q_idx, w, k_codes, B, T, H_I, q_pos, Ncap, m, S, err, st);
         if (e != cudaErrorNotSupported) {
             count_launch();
-            if (hist_done) *hist_done = hist1 != nullptr;
             return e == cudaSuccess ? CSAHCA_OK : CSAHCA_ERR_CUDA;
         }
     }

@@ -17,10 +17,10 @@
 //              accumulators;
 //   warps 0-7  epilogue: warp e reads TMEM lanes 32 (e % 4) .. (the tile's keys) and the columns of
 //              query rows [(e / 4) QR/2, (e / 4 + 1) QR/2): per key and row the score
-//              sum_h w_h ReLU(D[row, h]), stored to S (consecutive lanes, consecutive keys) and
-//              counted in the row's 12-bit histogram (16-bit counts in shared memory, added to the
-//              row's global histogram at the end of the item -- the top-k's first pass).
-// Scores of keys a row does not see (s >= its visible count) are neither stored nor counted.
+//              sum_h w_h ReLU(D[row, h]), stored to S (consecutive lanes, consecutive keys).
+// Scores of keys a row does not see (s >= its visible count) are not stored.  The top-k's first
+// histogram is not formed here: with thousands of rows a separate histogram pass over the scores
+// costs less than the epilogue's shared-memory atomics (one per key and row) did.
 #include "common.cuh"
 #include "tc_ptx.cuh"
 #include "tmap.cuh"
@@ -36,7 +36,7 @@ using namespace tc;
 
 constexpr int kKeysT = 128;          // keys per tile (MMA M)
 constexpr int kDI = 64;              // index dim (128 bytes of bf16: one swizzled row)
-constexpr int kChunkTiles = 64;      // tiles per item: 8192 keys, so 16-bit histogram counts cannot overflow
+constexpr int kChunkTiles = 64;      // tiles per item: 8192 keys
 constexpr int kNS = 4;               // key-tile stages
 constexpr int kEpiWarps = 8;
 constexpr int kThreadsP = 32 * kEpiWarps + 64;
@@ -47,8 +47,7 @@ template <int HI>
 struct PCfg {
     static constexpr int QR = 128 / HI;                        // query rows per item
     static constexpr uint32_t off_q = kNS * kTileBytes;        // two query slots
-    static constexpr uint32_t off_hist = off_q + 2 * kQBytes;  // [QR][2048] words: two 16-bit bins each
-    static constexpr uint32_t smem = off_hist + QR * 2048 * 4;
+    static constexpr uint32_t smem = off_q + 2 * kQBytes;
     static_assert(HI == 16 || HI == 32 || HI == 64, "heads");
 };
 
@@ -68,7 +67,7 @@ template <int HI>
 __global__ void __launch_bounds__(kThreadsP, 1) index_prefill_kernel(
     const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap qmap, const float* __restrict__ w,
     int T, const int64_t* __restrict__ q_pos, int64_t Ncap, int m, int R, float* __restrict__ S,
-    uint32_t* __restrict__ hist1, unsigned* err) {
+    unsigned* err) {
     using C = PCfg<HI>;
     constexpr int QR = C::QR;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -77,7 +76,6 @@ __global__ void __launch_bounds__(kThreadsP, 1) index_prefill_kernel(
     __shared__ PMisc ms;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t sbase = smem_u32(sm);
-    uint32_t* hist = reinterpret_cast<uint32_t*>(sm + C::off_hist);
 
     if (warp == 0) {
         tmem_alloc(&ms.tmem_base, 256);
@@ -96,7 +94,6 @@ __global__ void __launch_bounds__(kThreadsP, 1) index_prefill_kernel(
         }
         fence_mbar_init();
     }
-    for (int i = tid; i < QR * 2048; i += blockDim.x) hist[i] = 0u;
     pdl_wait();
     pdl_trigger();
     fence_before_sync();
@@ -245,28 +242,8 @@ __global__ void __launch_bounds__(kThreadsP, 1) index_prefill_kernel(
 #pragma unroll
                 for (int j = 0; j < QR / 2; ++j) {
                     const int row = hh * (QR / 2) + j;
-                    if (key < nv[j]) {
-                        S[(int64_t)(r0 + row) * Ncap + key] = sc[j];
-                        if (hist1 != nullptr) {
-                            const uint32_t bin = ordered_key(sc[j]) >> 20;
-                            atomicAdd(&hist[row * 2048 + (bin >> 1)], 1u << ((bin & 1) * 16));
-                        }
-                    }
+                    if (key < nv[j]) S[(int64_t)(r0 + row) * Ncap + key] = sc[j];
                 }
-            }
-            // item done: add the rows' histograms to the global ones and clear them
-            if (hist1 != nullptr) {
-            named_barrier_sync(1, 32 * kEpiWarps);
-            for (int i = tid; i < QR * 2048; i += 32 * kEpiWarps) {
-                const uint32_t v = hist[i];
-                if (v) {
-                    uint32_t* gh = hist1 + (int64_t)(r0 + i / 2048) * 4096 + 2 * (i % 2048);
-                    if (v & 0xFFFFu) atomicAdd(gh, v & 0xFFFFu);
-                    if (v >> 16) atomicAdd(gh + 1, v >> 16);
-                    hist[i] = 0u;
-                }
-            }
-            named_barrier_sync(1, 32 * kEpiWarps);
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&ms.qfree[qs]);
@@ -281,7 +258,7 @@ __global__ void __launch_bounds__(kThreadsP, 1) index_prefill_kernel(
 
 template <int HI>
 cudaError_t launch_prefill(const void* q_idx, const float* w, const void* k_codes, int B, int T, const int64_t* q_pos,
-                           int64_t Ncap, int m, float* S, uint32_t* hist1, unsigned* err, cudaStream_t st) {
+                           int64_t Ncap, int m, float* S, unsigned* err, cudaStream_t st) {
     using C = PCfg<HI>;
     CUtensorMap kmap, qmap;
     std::memset(&kmap, 0, sizeof kmap);
@@ -296,7 +273,7 @@ cudaError_t launch_prefill(const void* q_idx, const float* w, const void* k_code
     if (e != cudaSuccess) return e;
     const int64_t items = (int64_t)(R / C::QR) * cdiv(Ncap, (int64_t)kChunkTiles * kKeysT);
     const int grid = (int)std::min<int64_t>(items, num_sms());
-    (void)launch_pdl(kern, dim3(grid), dim3(kThreadsP), smem, st, kmap, qmap, w, T, q_pos, Ncap, m, R, S, hist1, err);
+    (void)launch_pdl(kern, dim3(grid), dim3(kThreadsP), smem, st, kmap, qmap, w, T, q_pos, Ncap, m, R, S, err);
     return cudaGetLastError();
 }
 
@@ -313,12 +290,12 @@ bool index_prefill_supported(int q_dtype, int key_fmt, int H_I, int d_I, int64_t
 }
 
 cudaError_t index_prefill_launch(const void* q_idx, const float* w, const void* k_codes, int B, int T, int H_I,
-                                 const int64_t* q_pos, int64_t Ncap, int m, float* S, uint32_t* hist1, unsigned* err,
+                                 const int64_t* q_pos, int64_t Ncap, int m, float* S, unsigned* err,
                                  cudaStream_t st) {
     switch (H_I) {
-        case 16: return launch_prefill<16>(q_idx, w, k_codes, B, T, q_pos, Ncap, m, S, hist1, err, st);
-        case 32: return launch_prefill<32>(q_idx, w, k_codes, B, T, q_pos, Ncap, m, S, hist1, err, st);
-        case 64: return launch_prefill<64>(q_idx, w, k_codes, B, T, q_pos, Ncap, m, S, hist1, err, st);
+        case 16: return launch_prefill<16>(q_idx, w, k_codes, B, T, q_pos, Ncap, m, S, err, st);
+        case 32: return launch_prefill<32>(q_idx, w, k_codes, B, T, q_pos, Ncap, m, S, err, st);
+        case 64: return launch_prefill<64>(q_idx, w, k_codes, B, T, q_pos, Ncap, m, S, err, st);
         default: return cudaErrorNotSupported;
     }
 }
