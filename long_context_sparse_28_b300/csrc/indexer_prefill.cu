@@ -37,7 +37,7 @@ using namespace tc;
 constexpr int kKeysT = 128;          // keys per tile (MMA M)
 constexpr int kDI = 64;              // index dim (128 bytes of bf16: one swizzled row)
 constexpr int kChunkTiles = 64;      // tiles per item: 8192 keys
-constexpr int kNS = 4;               // key-tile stages
+constexpr int kNS = 8;               // key-tile stages (the keys come from L2: more in flight helps)
 constexpr int kEpiWarps = 8;
 constexpr int kThreadsP = 32 * kEpiWarps + 64;
 constexpr uint32_t kTileBytes = kKeysT * 128;   // 16 KB
