@@ -62,10 +62,6 @@ inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, siz
     return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
 }
 
-// Zeroes n 32-bit words (a kernel rather than a memset node, so the launch chain stays
-// programmatic).
-cudaError_t zero_words(uint32_t* p, size_t n, cudaStream_t st);
-
 // ------------------------------------------------------------------------- vector I/O
 // 8 consecutive elements <-> float[8]; p must be 16-byte (bf16) / 32-byte (f32) aligned.
 __device__ __forceinline__ void load8(const float* p, float (&o)[8]) {
@@ -201,10 +197,10 @@ struct TopkWorkspace {
 };
 size_t topk_workspace_bytes(int64_t R, int64_t stride);
 TopkWorkspace topk_carve(void* ws, int64_t R, int64_t stride);
-// Bytes at the start of the workspace that must be zero before a histogram is accumulated.
-size_t topk_zero_bytes(int64_t R);
 // n_vis for row r is either n_vis_arr[r] (if non-NULL) or min(Ncap, (q_pos[r]+1)/m).
-// hist_ready: hist1/cand_n were zeroed and hist1 filled by the caller (the fused indexer).
+// hist_ready: hist1 was filled by the caller (the fused indexer); else a histogram pass fills it
+// (hist1 is zero on entry either way: the workspace starts zero-filled and every call clears
+// the rows it used).
 csahca_status topk_launch(const float* scores, int64_t stride, int R, const int64_t* n_vis_arr,
                           const int64_t* q_pos, int m, int64_t Ncap, int k, int32_t* idx_out,
                           const TopkWorkspace& tw, bool hist_ready, cudaStream_t stream);

@@ -45,15 +45,6 @@ int num_sms() {
 void count_launch(int n) { g_launches += (uint64_t)n; }
 
 namespace {
-__global__ void zero_words_kernel(uint32_t* __restrict__ p, size_t n) {
-    pdl_wait();
-    pdl_trigger();
-    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x)
-        p[i] = 0u;
-}
-}  // namespace
-
-namespace {
 // One warp waits on an mbarrier that nothing ever arrives on, through the same bounded wait the
 // tensor-core kernels use; the wait gives up after limit_ns, flags CSAHCA_ERR_TIMEOUT in the
 // error word and the kernel returns normally.
@@ -67,14 +58,6 @@ __global__ void bounded_wait_kernel(uint64_t limit_ns, unsigned* err) {
     (void)tc::mbar_wait(&bar, 0, err, limit_ns);
 }
 }  // namespace
-
-cudaError_t zero_words(uint32_t* p, size_t n, cudaStream_t st) {
-    if (n == 0) return cudaSuccess;
-    const size_t blocks = (n + 255) / 256;
-    const unsigned grid = (unsigned)(blocks < (size_t)num_sms() * 4 ? blocks : (size_t)num_sms() * 4);
-    count_launch();
-    return launch_pdl(zero_words_kernel, dim3(grid), dim3(256), 0, st, p, n);
-}
 
 }  // namespace csahca
 

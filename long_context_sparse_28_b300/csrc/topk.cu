@@ -26,7 +26,7 @@ namespace {
 
 constexpr int kBins12 = 4096;
 constexpr int kBins8 = 256;
-constexpr int kSlice = 8192;       // scores per histogram CTA
+constexpr int kSlice = 32768;      // scores per histogram CTA
 constexpr int kCap = 8192;         // candidate-list capacity per row
 constexpr int kThreads = 256;      // histogram pass
 constexpr int kSelThreads = 1024;  // select pass
@@ -90,7 +90,20 @@ __global__ void __launch_bounds__(kThreads) topk_hist_kernel(const float* __rest
     for (int i = threadIdx.x; i < kBins12; i += blockDim.x) sh[i] = 0;
     __syncthreads();
     const float* row = scores + (int64_t)r * stride;
-    for (int64_t s = s0 + threadIdx.x; s < s1; s += blockDim.x) atomicAdd(&sh[ordered_key(row[s]) >> 20], 1u);
+    int64_t s = s0;
+    if ((reinterpret_cast<uintptr_t>(row + s0) & 15) == 0) {      // 16-byte loads
+        const float4* r4 = reinterpret_cast<const float4*>(row + s0);
+        const int64_t n4 = (s1 - s0) / 4;
+        for (int64_t i = threadIdx.x; i < n4; i += blockDim.x) {
+            const float4 x = __ldg(r4 + i);
+            atomicAdd(&sh[ordered_key(x.x) >> 20], 1u);
+            atomicAdd(&sh[ordered_key(x.y) >> 20], 1u);
+            atomicAdd(&sh[ordered_key(x.z) >> 20], 1u);
+            atomicAdd(&sh[ordered_key(x.w) >> 20], 1u);
+        }
+        s = s0 + n4 * 4;
+    }
+    for (s += threadIdx.x; s < s1; s += blockDim.x) atomicAdd(&sh[ordered_key(row[s]) >> 20], 1u);
     __syncthreads();
     uint32_t* gh = hist1 + (int64_t)r * kBins12;
     for (int i = threadIdx.x; i < kBins12; i += blockDim.x)
@@ -545,14 +558,14 @@ TopkWorkspace topk_carve(void* ws, int64_t R, int64_t stride) {
     return t;
 }
 
-size_t topk_zero_bytes(int64_t R) { return align256((size_t)R * kBins12 * 4); }
 
 csahca_status topk_launch(const float* scores, int64_t stride, int R, const int64_t* n_vis_arr,
                           const int64_t* q_pos, int m, int64_t Ncap, int k, int32_t* idx_out,
                           const TopkWorkspace& tw, bool hist_ready, cudaStream_t stream) {
     if (!hist_ready) {
+        // (the histograms are zero here: the workspace starts zero-filled and every call's select
+        // pass clears the rows it used)
         const int64_t P = std::max<int64_t>(1, cdiv(stride, kSlice));
-        if (zero_words(tw.hist1, topk_zero_bytes(R) / 4, stream) != cudaSuccess) return CSAHCA_ERR_CUDA;
         (void)launch_pdl(topk_hist_kernel, dim3((unsigned)P, (unsigned)R), dim3(kThreads), 0, stream, scores, stride,
                          n_vis_arr, q_pos, m, Ncap, tw.hist1);
         count_launch();
