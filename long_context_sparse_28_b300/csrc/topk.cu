@@ -232,7 +232,7 @@ __global__ void __launch_bounds__(kSelThreads, 1) topk_select_kernel(
     const float* __restrict__ scores, int64_t stride, const int64_t* __restrict__ n_vis_arr,
     const int64_t* __restrict__ q_pos, int m, int64_t Ncap, int k, uint32_t* __restrict__ hist1,
     uint32_t* __restrict__ win, uint32_t* __restrict__ tie, int64_t words, int32_t* __restrict__ idx_out,
-    int cap, int smem_words) {
+    int cap, int smem_words, int self_hist) {
     pdl_wait();
     pdl_trigger();
     namespace cg = cooperative_groups;
@@ -254,10 +254,32 @@ __global__ void __launch_bounds__(kSelThreads, 1) topk_select_kernel(
     __shared__ int2 sh_scan2[32];
     const int r = blockIdx.y, P = (int)cl.num_blocks(), p = (int)cl.block_rank();
     const int tid = threadIdx.x, nthr = blockDim.x, lane = tid & 31, warp = tid >> 5, nw = nthr >> 5;
-    // the row's first histogram into shared memory, loaded together with the row's length
-    for (int i = tid; i < kBins12 / 4; i += nthr)
-        reinterpret_cast<uint4*>(hsum)[i] = reinterpret_cast<const uint4*>(hist1 + (int64_t)r * kBins12)[i];
+    // the row's first histogram into shared memory, loaded together with the row's length; or
+    // (self_hist: one CTA per row and no histogram from the indexer) formed here from the row's
+    // scores, which the collect pass below then reads again from L2
     const int64_t n = min(row_nvis(r, n_vis_arr, q_pos, m, Ncap), min(stride, words * 32));
+    if (self_hist) {
+        for (int i = tid; i < kBins12; i += nthr) hsum[i] = 0u;
+        __syncthreads();
+        const float* srow = scores + (int64_t)r * stride;
+        int64_t s = 0;
+        if ((reinterpret_cast<uintptr_t>(srow) & 15) == 0) {
+            const float4* r4 = reinterpret_cast<const float4*>(srow);
+            const int64_t n4 = n / 4;
+            for (int64_t i = tid; i < n4; i += nthr) {
+                const float4 x = __ldg(r4 + i);
+                atomicAdd(&hsum[ordered_key(x.x) >> 20], 1u);
+                atomicAdd(&hsum[ordered_key(x.y) >> 20], 1u);
+                atomicAdd(&hsum[ordered_key(x.z) >> 20], 1u);
+                atomicAdd(&hsum[ordered_key(x.w) >> 20], 1u);
+            }
+            s = n4 * 4;
+        }
+        for (s += tid; s < n; s += nthr) atomicAdd(&hsum[ordered_key(srow[s]) >> 20], 1u);
+    } else {
+        for (int i = tid; i < kBins12 / 4; i += nthr)
+            reinterpret_cast<uint4*>(hsum)[i] = reinterpret_cast<const uint4*>(hist1 + (int64_t)r * kBins12)[i];
+    }
     int32_t* out = idx_out + (int64_t)r * k;
     uint32_t* hrow = hist1 + (int64_t)r * kBins12;
     if (n <= k) {                                   // every visible entry is selected, in order
@@ -562,15 +584,6 @@ TopkWorkspace topk_carve(void* ws, int64_t R, int64_t stride) {
 csahca_status topk_launch(const float* scores, int64_t stride, int R, const int64_t* n_vis_arr,
                           const int64_t* q_pos, int m, int64_t Ncap, int k, int32_t* idx_out,
                           const TopkWorkspace& tw, bool hist_ready, cudaStream_t stream) {
-    if (!hist_ready) {
-        // (the histograms are zero here: the workspace starts zero-filled and every call's select
-        // pass clears the rows it used)
-        const int64_t P = std::max<int64_t>(1, cdiv(stride, kSlice));
-        (void)launch_pdl(topk_hist_kernel, dim3((unsigned)P, (unsigned)R), dim3(kThreads), 0, stream, scores, stride,
-                         n_vis_arr, q_pos, m, Ncap, tw.hist1);
-        count_launch();
-        CSAHCA_CHECK_LAUNCH();
-    }
     static bool attr_set[64] = {false};
     int dev = 0;
     cudaGetDevice(&dev);
@@ -588,6 +601,17 @@ csahca_status topk_launch(const float* scores, int64_t stride, int R, const int6
     // One CTA per row (many rows, short rows): a lean form -- 512 threads, 4096 candidates, bitmaps
     // sized to the row, no gathered copy -- so that two CTAs share an SM.
     const bool lean = P == 1 && tw.words <= 4096;
+    // Without the indexer's histogram: one CTA per row forms its row's histogram itself; several
+    // CTAs per row need the row's histogram first (a pass of its own).  (The histograms are zero
+    // on entry: the workspace starts zero-filled and every select pass clears the rows it used.)
+    const int self_hist = (!hist_ready && P == 1) ? 1 : 0;
+    if (!hist_ready && !self_hist) {
+        const int64_t HP = std::max<int64_t>(1, cdiv(stride, kSlice));
+        (void)launch_pdl(topk_hist_kernel, dim3((unsigned)HP, (unsigned)R), dim3(kThreads), 0, stream, scores, stride,
+                         n_vis_arr, q_pos, m, Ncap, tw.hist1);
+        count_launch();
+        CSAHCA_CHECK_LAUNCH();
+    }
     const int threads = lean ? 512 : kSelThreads;
     const int cap = lean ? 4096 : kCap;
     const int smem_words = lean ? (int)tw.words : kSmemWords;
@@ -607,7 +631,7 @@ csahca_status topk_launch(const float* scores, int64_t stride, int R, const int6
     cfg.attrs = attr;
     cfg.numAttrs = 2;
     (void)cudaLaunchKernelEx(&cfg, topk_select_kernel, scores, stride, n_vis_arr, q_pos, m, Ncap, k,
-                             tw.hist1, tw.win, tw.tie, tw.words, idx_out, cap, smem_words);
+                             tw.hist1, tw.win, tw.tie, tw.words, idx_out, cap, smem_words, self_hist);
     count_launch();
     CSAHCA_CHECK_LAUNCH();
     return CSAHCA_OK;
