@@ -37,7 +37,7 @@ using namespace tc;
 constexpr int kKeysT = 128;          // keys per tile (MMA M)
 constexpr int kDI = 64;              // index dim (128 bytes of bf16: one swizzled row)
 constexpr int kChunkTiles = 64;      // tiles per item: 8192 keys
-constexpr int kNS = 8;               // key-tile stages (the keys come from L2: more in flight helps)
+constexpr int kNS = 4;               // key-tile stages (two CTAs per SM: 2 x 96 KB of shared memory)
 constexpr int kEpiWarps = 8;
 constexpr int kThreadsP = 32 * kEpiWarps + 64;
 constexpr uint32_t kTileBytes = kKeysT * 128;   // 16 KB
@@ -64,7 +64,7 @@ static_assert(offsetof(PMisc, w) % 16 == 0 && offsetof(PMisc, item) % 16 == 0, "
 // [c * 8192, c * 8192 + 128 * tiles) of the group's sequence, tiles limited by the group's largest
 // visible count.
 template <int HI>
-__global__ void __launch_bounds__(kThreadsP, 1) index_prefill_kernel(
+__global__ void __launch_bounds__(kThreadsP, 2) index_prefill_kernel(
     const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap qmap, const float* __restrict__ w,
     int T, const int64_t* __restrict__ q_pos, int64_t Ncap, int m, int R, float* __restrict__ S,
     unsigned* err) {
@@ -193,19 +193,14 @@ __global__ void __launch_bounds__(kThreadsP, 1) index_prefill_kernel(
             if (itm.w) break;
             const int r0 = itm.x, key0 = itm.y;
             // this thread's rows hh QR/2 + j, j < QR/2, own the 64 consecutive accumulator columns
-            // [64 hh, 64 hh + 64) of a tile (QR/2 rows x H_I heads): their head weights, in registers
-            // for the whole item
+            // [64 hh, 64 hh + 64) of a tile (QR/2 rows x H_I heads); their head weights are read
+            // from shared memory (broadcast) so that two CTAs' registers fit an SM
             constexpr int kCols = (QR / 2) * HI;
             static_assert(kCols == 64, "64 columns per epilogue thread");
             int nv[QR / 2];
 #pragma unroll
             for (int j = 0; j < QR / 2; ++j) nv[j] = ms.nvis[qs][hh * (QR / 2) + j];
-            uint64_t wv[kCols / 2];
-#pragma unroll
-            for (int k = 0; k < kCols; k += 2) {
-                const float2 x = *reinterpret_cast<const float2*>(&ms.w[qs][hh * kCols + k]);
-                wv[k / 2] = f2_pack(x.x, x.y);
-            }
+            const float2* wsm = reinterpret_cast<const float2*>(&ms.w[qs][hh * kCols]);
             for (int t = 0; t < itm.z; ++t, ++dn) {
                 const uint32_t d = dn & 1;
                 mbar_wait(&ms.dfull[d], (dn >> 1) & 1, err);
@@ -231,7 +226,7 @@ __global__ void __launch_bounds__(kThreadsP, 1) index_prefill_kernel(
 #pragma unroll
                     for (int k = 0; k < HI; k += 2) {
                         const int c = j * HI + k;
-                        acc = f2_fma(wv[c / 2],
+                        acc = f2_fma(f2_pack(wsm[c / 2].x, wsm[c / 2].y),
                                      f2_pack(fmaxf(__uint_as_float(v[c]), 0.0f), fmaxf(__uint_as_float(v[c + 1]), 0.0f)),
                                      acc);
                     }
@@ -272,7 +267,7 @@ cudaError_t launch_prefill(const void* q_idx, const float* w, const void* k_code
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const int64_t items = (int64_t)(R / C::QR) * cdiv(Ncap, (int64_t)kChunkTiles * kKeysT);
-    const int grid = (int)std::min<int64_t>(items, num_sms());
+    const int grid = (int)std::min<int64_t>(items, 2 * num_sms());   // two CTAs per SM
     (void)launch_pdl(kern, dim3(grid), dim3(kThreadsP), smem, st, kmap, qmap, w, T, q_pos, Ncap, m, R, S, err);
     return cudaGetLastError();
 }
