@@ -148,6 +148,76 @@ __global__ void compress_kernel(const T* __restrict__ k_raw, const T* __restrict
     }
 }
 
+// Large blocks (m >= 64) with one CTA of four warps per block: warp q sums tokens
+// [q m / 4, (q + 1) m / 4) of every channel group (the same per-token weights), the partial sums
+// meet in shared memory and warp 0 adds them in quarter order and stores the entry.  Four times
+// the loads in flight of the one-warp form, for the few large blocks of a prefill chunk.
+template <typename T, bool kKv8>
+__global__ void __launch_bounds__(128) compress_split_kernel(
+    const T* __restrict__ k_raw, const T* __restrict__ v_raw, const float* __restrict__ gate, int64_t raw_stride,
+    const int64_t* __restrict__ raw_pos0, const int64_t* __restrict__ n_raw, const float* __restrict__ bias, int m,
+    int B, int d, void* ck, void* cv, int64_t Ncap, int64_t max_blocks, unsigned* err) {
+    pdl_wait();
+    pdl_trigger();
+    __shared__ float part[4][4][32][8];       // [quarter][channel-group pass (d <= 512)][lane][channel]
+    const int q = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int groups = d / 8;                 // 8-channel groups per tensor
+    const int64_t total = (int64_t)B * max_blocks;
+    for (int64_t bid = blockIdx.x; bid < total; bid += gridDim.x) {
+        const int b = (int)(bid / max_blocks);
+        const int64_t jl = bid % max_blocks;
+        const int64_t p0 = raw_pos0[b], n = n_raw[b];
+        const int64_t j = (p0 + m - 1) / m + jl;          // first block fully inside + jl
+        if ((j + 1) * m > p0 + n) continue;
+        if (j >= Ncap || (j + 1) * m - p0 > raw_stride || p0 < 0) {
+            if (threadIdx.x == 0) flag_error(err, ERRBIT_BOUNDS);
+            continue;
+        }
+        const int64_t row0 = (int64_t)b * raw_stride + (j * m - p0);
+        const float* g = gate + row0;
+        float a[8];
+        block_weights(m, [&](int i) { return g[i] + bias[i]; }, a);
+        const int i0 = q * m / 4, i1 = (q + 1) * m / 4;
+        for (int g0 = 0, it = 0; g0 < 2 * groups; g0 += 32, ++it) {
+            const int gi = g0 + lane;
+            const bool active = gi < 2 * groups;
+            const T* base = (gi < groups ? k_raw : v_raw) + (gi % groups) * 8;
+            float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+            for (int i = i0; i < i1; ++i) {
+                const float al = alpha_of(a, i);  // warp-uniform loop: all lanes shuffle
+                if (active) {
+                    float x[8];
+                    load8_rw(base + (row0 + i) * (int64_t)d, x);
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) acc[c] = fmaf(al, x[c], acc[c]);
+                }
+            }
+#pragma unroll
+            for (int c = 0; c < 8; ++c) part[q][it][lane][c] = acc[c];
+        }
+        __syncthreads();
+        if (q == 0) {
+            const int64_t e = (int64_t)b * Ncap + j;
+            for (int g0 = 0, it = 0; g0 < 2 * groups; g0 += 32, ++it) {
+                const int gi = g0 + lane;
+                float acc[8];
+#pragma unroll
+                for (int c = 0; c < 8; ++c)
+                    acc[c] = ((part[0][it][lane][c] + part[1][it][lane][c]) + part[2][it][lane][c]) +
+                             part[3][it][lane][c];
+                if constexpr (kKv8) {
+                    store_kv8_warp(acc, static_cast<unsigned char*>(ck) + e * kKv8KRow,
+                                   static_cast<unsigned char*>(cv) + e * kKv8VRow, lane);
+                } else if (gi < 2 * groups) {
+                    T* dst = static_cast<T*>(gi < groups ? ck : cv) + e * d + (gi % groups) * 8;
+                    store8(dst, acc);
+                }
+            }
+        }
+        __syncthreads();                      // the partial sums are reused by the next block
+    }
+}
+
 // One CTA per sequence: pool completed blocks (reading old tokens from the ring), then write
 // the new tokens into the ring.  A completed block is pooled by the whole CTA: warp 0 computes
 // the m softmax weights into shared memory, then every thread sums a subset of the m tokens for
@@ -400,11 +470,29 @@ csahca_status compress_impl(const void* k_raw, const void* v_raw, const float* g
     const int64_t max_blocks = raw_stride / m + 1;
     const int64_t warps = (int64_t)B * max_blocks;
     if (warps == 0 || Ncap == 0 || raw_stride == 0) return CSAHCA_OK;
+    unsigned* err = err_word();
+    if (!err) return CSAHCA_ERR_CUDA;
+    if (m >= 64) {                            // four warps per block
+        const int grid = (int)std::min<int64_t>(warps, (int64_t)num_sms() * 16);
+        if (kv == CSAHCA_F32)
+            (void)launch_pdl(compress_split_kernel<float, false>, dim3(grid), dim3(128), 0, stream,
+                (const float*)k_raw, (const float*)v_raw, gate, raw_stride, raw_pos0, n_raw, bias, m, B, d,
+                ck, cv, Ncap, max_blocks, err);
+        else if (kv == CSAHCA_BF16)
+            (void)launch_pdl(compress_split_kernel<__nv_bfloat16, false>, dim3(grid), dim3(128), 0, stream,
+                (const __nv_bfloat16*)k_raw, (const __nv_bfloat16*)v_raw, gate, raw_stride, raw_pos0, n_raw,
+                bias, m, B, d, ck, cv, Ncap, max_blocks, err);
+        else
+            (void)launch_pdl(compress_split_kernel<__nv_bfloat16, true>, dim3(grid), dim3(128), 0, stream,
+                (const __nv_bfloat16*)k_raw, (const __nv_bfloat16*)v_raw, gate, raw_stride, raw_pos0, n_raw,
+                bias, m, B, d, ck, cv, Ncap, max_blocks, err);
+        count_launch();
+        CSAHCA_CHECK_LAUNCH();
+        return CSAHCA_OK;
+    }
     const int threads = 256;
     const int64_t want = cdiv(warps, threads / 32);
     const int grid = (int)std::min<int64_t>(want, (int64_t)num_sms() * 16);
-    unsigned* err = err_word();
-    if (!err) return CSAHCA_ERR_CUDA;
     if (kv == CSAHCA_F32)
         (void)launch_pdl(compress_kernel<float, false>, dim3(grid), dim3(threads), 0, stream,
             (const float*)k_raw, (const float*)v_raw, gate, raw_stride, raw_pos0, n_raw, bias, m, B, d,
