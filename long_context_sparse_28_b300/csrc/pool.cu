@@ -95,7 +95,8 @@ __device__ __forceinline__ void pool_block_warp(int m, int d, const float (&a)[8
         const int col = (g % groups) * 8;
         float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
         for (int i = 0; i < m; ++i) {
-            const float al = alpha_of(a, i);  // warp-uniform loop: all lanes shuffle
+            // warp-uniform loop: all lanes shuffle (one shuffle when every weight is in a[0])
+            const float al = m <= 32 ? __shfl_sync(0xffffffffu, a[0], i) : alpha_of(a, i);
             if (active) {
                 float x[8];
                 load8_rw(rowptr(which, i) + col, x);
