@@ -169,6 +169,9 @@ csahca_status csa_index_topk(const void* q_idx, csahca_dtype q_dtype, const floa
                              int m, int k, int32_t* idx_out, float* scores_out, void* workspace,
                              size_t ws_bytes, csahca_stream_t stream);
 size_t csa_index_topk_workspace(int B, int T, int64_t Ncap, int k);
+/* Workspace bytes of csa_index_topk_fp4 that allow its prefill form (see there): the bytes of
+ * csa_index_topk_workspace, plus B*Ncap*128 + B*T*H_I*128 (rounded to 256) when the form applies. */
+size_t csa_index_topk_fp4_workspace(int B, int T, int H_I, int64_t Ncap, int k);
 
 /* The lightning indexer with FP4 queries as well as FP4 keys (pogovet.com detail 5: the indexer runs
  * in FP4; honbul.tistory.com/221: FP4 QAT of the CSA indexer's query-key path).  The queries come in
@@ -176,10 +179,14 @@ size_t csa_index_topk_workspace(int B, int T, int64_t Ncap, int k);
  * the low nibble) and q_scale [B][T][H_I][d_I/32] UE8M0 bytes, as csa_index_key_quantize produces
  * from bf16 queries with key_fmt CSAHCA_E2M1_UE8M0 -- and the score is
  *     I(t,s) = sum_{h < H_I} w[t][h] * max(0, qhat[t][h][:] . khat_s),  qhat = 2^(byte-127) * code,
- * exact up to the fp32 accumulation.  Keys are CSAHCA_E2M1_UE8M0.  Top-k, outputs and workspace
- * (csa_index_topk_workspace) as csa_index_topk.  Supported: d_I = 64, H_I in {16, 32, 64},
- * Ncap % 256 == 0, k_codes 32-byte, k_scale and q_codes 16-byte, q_scale 2-byte aligned; otherwise
- * CSAHCA_ERR_UNSUPPORTED and nothing is enqueued. */
+ * exact up to the fp32 accumulation.  Keys are CSAHCA_E2M1_UE8M0.  Top-k and outputs as
+ * csa_index_topk.  Workspace: csa_index_topk_workspace(B, T, Ncap, k) bytes at least; with
+ * csa_index_topk_fp4_workspace(B, T, H_I, Ncap, k) bytes and more than 256 query rows (chunked
+ * prefill, T a multiple of 128 / H_I) the keys and queries are first expanded to bf16 in the
+ * workspace -- exactly, for block scales up to 2^125 -- and scored 128 / H_I query rows per tensor-
+ * core tile; otherwise one query row per work item on the block-scaled MMA.  Supported: d_I = 64,
+ * H_I in {16, 32, 64}, Ncap % 256 == 0, k_codes 32-byte, k_scale and q_codes 16-byte, q_scale
+ * 2-byte aligned; otherwise CSAHCA_ERR_UNSUPPORTED and nothing is enqueued. */
 csahca_status csa_index_topk_fp4(const void* q_codes, const void* q_scale, const float* w,
                                  const void* k_codes, const void* k_scale, int B, int T, int H_I,
                                  int d_I, const int64_t* q_pos, int64_t Ncap, int m, int k,

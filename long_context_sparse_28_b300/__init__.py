@@ -30,6 +30,7 @@ _SIGS = {
     "csa_index_key_quantize": ([_P, _I, _I64, _I, _I, _P, _P, _P], _I),
     "csa_index_topk": ([_P, _I, _P, _P, _P, _I, _I, _I, _I, _I, _P, _I64, _I, _I, _P, _P, _P, _SZ, _P], _I),
     "csa_index_topk_workspace": ([_I, _I, _I64, _I], _SZ),
+    "csa_index_topk_fp4_workspace": ([_I, _I, _I, _I64, _I], _SZ),
     "csa_index_topk_fp4": ([_P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _I64, _I, _I, _P, _P, _P, _SZ, _P], _I),
     "csa_index_scores": ([_P, _I, _P, _P, _P, _I, _I, _I, _I, _I, _P, _I64, _I, _P, _P], _I),
     "csa_topk_from_scores": ([_P, _I64, _I, _P, _I, _P, _P, _SZ, _P], _I),
@@ -185,6 +186,10 @@ def csa_index_topk_workspace(B, T, Ncap, k) -> int:
     return int(library().csa_index_topk_workspace(B, T, Ncap, k))
 
 
+def csa_index_topk_fp4_workspace(B, T, H_I, Ncap, k) -> int:
+    return int(library().csa_index_topk_fp4_workspace(B, T, H_I, Ncap, k))
+
+
 def csa_index_topk(q_idx, w, k_codes, k_scale, key_fmt, q_pos, m, k, idx_out, scores_out=None,
                    workspace=None, stream=None):
     """q_idx [B, T, H_I, d_I]; w [B, T, H_I]; k_codes/k_scale index keys [B, Ncap, ...];
@@ -204,7 +209,7 @@ def csa_index_topk_fp4(q_codes, q_scale, w, k_codes, k_scale, q_pos, m, k, idx_o
     B, T, H_I, half = q_codes.shape
     d_I = 2 * half
     Ncap = k_codes.shape[1]
-    ws, nb = _ws(csa_index_topk_workspace(B, T, Ncap, k), q_codes.device, workspace)
+    ws, nb = _ws(csa_index_topk_fp4_workspace(B, T, H_I, Ncap, k), q_codes.device, workspace)
     _check(library().csa_index_topk_fp4(_p(q_codes), _p(q_scale), _p(w), _p(k_codes), _p(k_scale), B, T, H_I, d_I,
                                         _p(q_pos), Ncap, int(m), int(k), _p(idx_out), _p(scores_out), _p(ws), nb,
                                         _stream(stream)), "csa_index_topk_fp4")

@@ -109,11 +109,58 @@ __global__ void __launch_bounds__(256) index_score_kernel(
 }
 
 }  // namespace
+// OCP MX FP4 (E2M1 codes, UE8M0 per 32) rows of 64 values -> bf16, exactly: e2m1 values have at
+// most two significant bits and the scale is a power of two, so every product is a bf16 value
+// while the scale exponent stays within bf16's range (byte - 127 <= 125, i.e. inputs below ~1e38).
+// One thread per 8 values (4 code bytes).
+__global__ void __launch_bounds__(256) expand_e2m1_rows_kernel(const uint8_t* __restrict__ codes,
+                                                               const uint8_t* __restrict__ scales, int64_t rows,
+                                                               __nv_bfloat16* __restrict__ out) {
+    pdl_wait();
+    pdl_trigger();
+    const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (t >= rows * 8) return;
+    const int64_t row = t >> 3;
+    const int part = (int)(t & 7);                       // values 8 part .. 8 part + 7
+    const uint32_t c4 = *reinterpret_cast<const uint32_t*>(codes + row * 32 + part * 4);
+    const float sc = ldexpf(1.0f, (int)scales[row * 2 + (part >> 2)] - 127);
+    // E2M1 code s e1 e0 m: |x| = m / 2 for e = 0, (1 + m / 2) 2^(e - 1) otherwise
+    auto e2m1 = [](uint32_t c) {
+        const uint32_t e = (c >> 1) & 3u, mb = c & 1u;
+        const float mag = e == 0 ? 0.5f * (float)mb : ldexpf(1.0f + 0.5f * (float)mb, (int)e - 1);
+        return (c & 8u) ? -mag : mag;
+    };
+    uint32_t o[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const uint32_t byte = (c4 >> (8 * j)) & 0xFFu;   // the even element in the low nibble
+        o[j] = pack_bf16x2(e2m1(byte & 0xFu) * sc, e2m1(byte >> 4) * sc);
+    }
+    *reinterpret_cast<uint4*>(out + row * 64 + part * 8) = make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+// FP4 queries with many rows (chunked prefill): the rows' keys and queries are expanded exactly to
+// bf16 in the workspace and scored by the bf16 prefill indexer, whose tiles serve 128 / H_I query
+// rows at once (the block-scaled decode indexer takes one query row per work item).
+bool fp4_prefill_form(int B, int T, int H_I, int d_I, int64_t Ncap) {
+    return (int64_t)B * T > 256 && d_I == 64 && (H_I == 16 || H_I == 32 || H_I == 64) && T % (128 / H_I) == 0 &&
+           Ncap >= 1;
+}
+size_t fp4_prefill_scratch_bytes(int B, int T, int H_I, int64_t Ncap) {
+    return align256((size_t)B * Ncap * 64 * 2) + align256((size_t)B * T * H_I * 64 * 2);
+}
+
 }  // namespace csahca
 
 using namespace csahca;
 
 extern "C" {
+
+size_t csa_index_topk_fp4_workspace(int B, int T, int H_I, int64_t Ncap, int k) {
+    const size_t base = csa_index_topk_workspace(B, T, Ncap, k);
+    if (base == 0 || !fp4_prefill_form(B, T, H_I, 64, Ncap)) return base;
+    return base + fp4_prefill_scratch_bytes(B, T, H_I, Ncap);
+}
 
 size_t csa_index_topk_workspace(int B, int T, int64_t Ncap, int k) {
     (void)k;
@@ -234,6 +281,25 @@ csahca_status csa_index_topk_fp4(const void* q_codes, const void* q_scale, const
     cudaStream_t st = (cudaStream_t)stream;
     unsigned* err = err_word();
     if (!err) return CSAHCA_ERR_CUDA;
+    const size_t base = csa_index_topk_workspace(B, T, Ncap, k);
+    if (fp4_prefill_form(B, T, H_I, d_I, Ncap) && ws_bytes >= base + fp4_prefill_scratch_bytes(B, T, H_I, Ncap)) {
+        __nv_bfloat16* kb = reinterpret_cast<__nv_bfloat16*>(ws + base);
+        __nv_bfloat16* qb = reinterpret_cast<__nv_bfloat16*>(ws + base + align256((size_t)B * Ncap * 64 * 2));
+        const int64_t krows = (int64_t)B * Ncap, qrows = (int64_t)R * H_I;
+        if (index_prefill_supported(CSAHCA_BF16, CSAHCA_BF16, H_I, d_I, Ncap, qb, kb, B, T)) {
+            (void)launch_pdl(expand_e2m1_rows_kernel, dim3((unsigned)cdiv(krows * 8, 256)), dim3(256), 0, st,
+                             static_cast<const uint8_t*>(k_codes), static_cast<const uint8_t*>(k_scale), krows, kb);
+            (void)launch_pdl(expand_e2m1_rows_kernel, dim3((unsigned)cdiv(qrows * 8, 256)), dim3(256), 0, st,
+                             static_cast<const uint8_t*>(q_codes), static_cast<const uint8_t*>(q_scale), qrows, qb);
+            count_launch(2);
+            const cudaError_t ep = index_prefill_launch(qb, w, kb, B, T, H_I, q_pos, Ncap, m, S, err, st);
+            if (ep == cudaSuccess) {
+                count_launch();
+                return topk_launch(S, Ncap, R, nullptr, q_pos, m, Ncap, k, idx_out, tw, false, st);
+            }
+            if (ep != cudaErrorNotSupported) return CSAHCA_ERR_CUDA;
+        }
+    }
     const cudaError_t e = index_tc_q4_launch(q_codes, q_scale, w, k_codes, k_scale, B, T, H_I, q_pos, Ncap, m, S,
                                              tw.hist1, err, st);
     count_launch();

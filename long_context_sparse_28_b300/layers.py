@@ -17,7 +17,8 @@ import math
 import torch
 
 from . import (BF16, E2M1_UE8M0, F32, csa_attend, csa_attend_workspace, csa_cache_append, csa_compress,
-               csa_index_key_quantize, csa_index_topk, csa_index_topk_fp4, csa_index_topk_workspace, hca_attend, hca_attend_workspace, hca_cache_append,
+               csa_index_key_quantize, csa_index_topk, csa_index_topk_fp4, csa_index_topk_fp4_workspace,
+               csa_index_topk_workspace, hca_attend, hca_attend_workspace, hca_cache_append,
                hca_compress, key_storage, swa_ring_write, KV_FP8_K_ROW, KV_FP8_V_ROW)
 
 
@@ -174,7 +175,9 @@ class HybridPrefill:
         self.lse_c = torch.empty(B, T, H, dtype=torch.float32, device=dev)
         self.out_h = torch.empty(B, T, H, d, dtype=hca.dtype, device=dev)
         self.lse_h = torch.empty(B, T, H, dtype=torch.float32, device=dev)
-        self.ws_topk = torch.zeros(csa_index_topk_workspace(B, T, csa.Ncap, k), dtype=torch.uint8, device=dev)
+        ws_topk = (csa_index_topk_fp4_workspace(B, T, H_I, csa.Ncap, k) if q_fp4 else
+                   csa_index_topk_workspace(B, T, csa.Ncap, k))
+        self.ws_topk = torch.zeros(ws_topk, dtype=torch.uint8, device=dev)
         self.ws_ca = torch.zeros(max(256, csa_attend_workspace(B, T, H, d, k, csa.W)), dtype=torch.uint8, device=dev)
         self.ws_ha = torch.zeros(max(256, hca_attend_workspace(B, T, H, d, hca.Ncap, hca.W, 0)), dtype=torch.uint8,
                                  device=dev)

@@ -240,6 +240,46 @@ def test_index_fp4_queries_parity(H_I):
             check_index_set(npy(idx[b, t]), ref[t], S[t], int(nv[t]), k, f"b{b}t{t}")
 
 
+@pytest.mark.parametrize("H_I", [16, 64])
+def test_index_fp4_queries_prefill_form(H_I):
+    # more than 256 query rows with the FP4 workspace: keys and queries expanded to bf16 in the
+    # workspace (exact), scored by the prefill indexer, top-k with its own histogram; scores and
+    # index sets against the oracle's FP4 rule
+    from torch.profiler import ProfilerActivity, profile
+    B, T, Ncap, d_I, m, k = 1, 320, 2048, 64, 4, 150
+    kin = rnd((B, Ncap, d_I), torch.bfloat16, 61)
+    kin[0, 11] *= 16
+    codes, scales = L.key_storage(B, Ncap, d_I, L.E2M1_UE8M0)
+    L.csa_index_key_quantize(kin, L.E2M1_UE8M0, codes, scales)
+    q = rnd((B, T, H_I, d_I), torch.bfloat16, 62, 0.125)
+    q[0, 5, 1] *= 64
+    qc = torch.empty(B, T, H_I, d_I // 2, dtype=torch.uint8, device="cuda")
+    qs = torch.empty(B, T, H_I, d_I // 32, dtype=torch.uint8, device="cuda")
+    L.csa_index_key_quantize(q, L.E2M1_UE8M0, qc, qs)
+    w = torch.rand(B, T, H_I, generator=torch.Generator().manual_seed(63)).cuda()
+    pos_np = np.arange(4 * Ncap - 1 - 23 * (T - 1), 4 * Ncap, 23)          # visibility grows along the rows
+    pos = dev_i64(pos_np)
+    idx = torch.empty(B, T, k, dtype=torch.int32, device="cuda")
+    sc = torch.full((B, T, Ncap), float("nan"), device="cuda")
+    ws = torch.zeros(L.csa_index_topk_fp4_workspace(B, T, H_I, Ncap, k), dtype=torch.uint8, device="cuda")
+    assert ws.numel() > L.csa_index_topk_workspace(B, T, Ncap, k)          # the form applies
+    with profile(activities=[ProfilerActivity.CUDA]) as prof:
+        L.csa_index_topk_fp4(qc, qs, w, codes, scales, pos, m, k, idx, scores_out=sc, workspace=ws)
+        torch.cuda.synchronize()
+    names = " ".join(e.name for e in prof.events())
+    assert "expand_e2m1_rows_kernel" in names and "index_prefill_kernel" in names
+    assert L.device_status() == 0
+    kc, ks = oracle.quantize_keys(npy(kin[0]), oracle.KEY_E2M1)
+    khat = oracle.dequant_keys(oracle.KEY_E2M1, kc, ks, d_I)
+    nv = np.minimum(Ncap, (pos_np + 1) // m)
+    S = oracle.index_scores(oracle.fp4_query(npy(q[0])), npy(w[0]), khat, nv)
+    ref = oracle.topk(S, nv, k)
+    for t in range(0, T, 7):
+        got = npy(sc[0, t])[: nv[t]].astype(np.float64)
+        assert np.abs(got - S[t, : nv[t]]).max() <= 1e-5 * np.abs(S[t, : nv[t]]).max() + 1e-6
+        check_index_set(npy(idx[0, t]), ref[t], S[t], int(nv[t]), k, f"t{t}")
+
+
 @pytest.mark.parametrize("H_I,T", [(16, 24), (32, 12), (64, 6)])
 def test_prefill_indexer_tensor_core_parity(H_I, T):
     # bf16 keys and queries with T a multiple of 128 / H_I: the tensor-core prefill kernel (query
