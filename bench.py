@@ -837,8 +837,10 @@ def run_prefill(args, dist):
         pass
     tf_peak = peaks.get("bf16_tflops_sustained", 1400.0)
     dom = max(("csa_index_topk", "csa_attend", "hca_attend"), key=lambda n: per[n])
-    # FP4 x FP4 indexer MMAs (kind::mxf8f6f4) run at the 8-bit rate: 2x bf16 (the nominal 4.5 / 2.25 ratio)
-    fp4_idx = dom == "csa_index_topk" and w.index_q == "e2m1"
+    # FP4 x FP4 indexer MMAs (kind::mxf8f6f4) run at the 8-bit rate: 2x bf16 (the nominal 4.5 / 2.25
+    # ratio); with more than 256 query rows the FP4 operands are expanded exactly to bf16 and scored
+    # on the bf16 MMA, so the bf16 peak applies
+    fp4_idx = dom == "csa_index_topk" and w.index_q == "e2m1" and w.T <= 256
     if fp4_idx:
         tf_peak = tf_peak * 2
     ach = fl[dom] / (per[dom] / 1e3) / 1e12
