@@ -76,7 +76,7 @@ struct alignas(16) Misc {
     uint64_t k8full[2], v8full[2];   // FP8 caches: a tile's codes have landed (before conversion)
     uint64_t mfull;                  // the row merge's partials have landed in shared memory
     uint32_t tmem_base;
-    int flag[2];                     // per tile (ring of 2): some running maximum moved
+    int flag[4][2];                  // per warpgroup and tile (ring of 2): one of its maxima moved
     alignas(16) float red[16][32];
     alignas(16) float mrun[64];      // read as float4
     alignas(16) float mold[64];      // running maxima before the tile's update (float4)
@@ -591,7 +591,7 @@ __global__ void __launch_bounds__(Thr<H, F8>::kThreads, 1)
             mbar_init(&ms.k8full[i], kSoft);
             mbar_init(&ms.v8full[i], kSoft);
             mbar_init(&ms.sdone[i], 1);
-            ms.flag[i] = 0;
+            for (int w4 = 0; w4 < 4; ++w4) ms.flag[w4][i] = 0;
         }
         mbar_init(&ms.odone, 1);
         mbar_init(&ms.pready, kSoft / 32);
@@ -918,11 +918,11 @@ __global__ void __launch_bounds__(Thr<H, F8>::kThreads, 1)
                         }
                     }
                     store_p(pp);
-                    grow = named_barrier_or(1, kSoft, need && valid);
+                    grow = named_barrier_or(2 + wg, 128, need && valid);   // this warpgroup's heads
                 }
                 // everyone is done with tile i-1's flag (the barrier above, or on an item's first
                 // tile the previous item's closing barriers)
-                if (tid == 0) ms.flag[(seq + 1) & 1] = 0;
+                if ((tid & 127) == 0) ms.flag[wg][(seq + 1) & 1] = 0;
                 bool rescale = false;
                 if (grow) {
                     // tile maxima per head: a warp reduction, then a 4-way merge over the warpgroup
@@ -938,24 +938,25 @@ __global__ void __launch_bounds__(Thr<H, F8>::kThreads, 1)
                         }
                     }
                     ms.red[warp][lane] = mine;
-                    named_barrier_sync(1, kSoft);
-                    if (tid < H) {
-                        const int gq = tid / HG, hh = tid % HG;
-                        const float traw = fmaxf(fmaxf(ms.red[4 * gq][hh], ms.red[4 * gq + 1][hh]),
-                                                 fmaxf(ms.red[4 * gq + 2][hh], ms.red[4 * gq + 3][hh]));
+                    // (the warpgroup owns its heads' maxima: its own barriers suffice)
+                    named_barrier_sync(2 + wg, 128);
+                    if ((tid & 127) < HG) {
+                        const int hh = tid & 127, hd = wg * HG + hh;
+                        const float traw = fmaxf(fmaxf(ms.red[4 * wg][hh], ms.red[4 * wg + 1][hh]),
+                                                 fmaxf(ms.red[4 * wg + 2][hh], ms.red[4 * wg + 3][hh]));
                         const float tmax = traw * c_log2;
-                        const float mo = ms.mrun[tid];
+                        const float mo = ms.mrun[hd];
                         float al = 1.0f;
                         if (tmax > mo + kRescaleThreshold || (mo == -INFINITY && tmax != -INFINITY)) {
                             al = (mo == -INFINITY) ? 0.0f : ex2_approx(mo - tmax);
-                            ms.mrun[tid] = tmax;
-                            ms.flag[seq & 1] = 1;
+                            ms.mrun[hd] = tmax;
+                            ms.flag[wg][seq & 1] = 1;
                         }
-                        ms.mold[tid] = mo;
-                        ms.alpha[tid] = al;
+                        ms.mold[hd] = mo;
+                        ms.alpha[hd] = al;
                     }
-                    named_barrier_sync(1, kSoft);
-                    rescale = ms.flag[seq & 1] != 0;
+                    named_barrier_sync(2 + wg, 128);
+                    rescale = ms.flag[wg][seq & 1] != 0;
                     // P again with the new maxima; the row sums drop the first pass's term
                     // (recomputed exactly as it was added) and are rescaled
                     uint32_t rr[16];
