@@ -66,8 +66,7 @@ constexpr int kDI = 64;
 constexpr int kChunkStages = 8;       // stages per work item: 2048 keys of one query row
 constexpr int kMaxNS = 6;             // shared-memory stages (at most)
 constexpr int kEpi = 128;             // epilogue threads (warps 0-3)
-constexpr int kMmaWarps = 2;          // MMA-issuing warps, taking alternate stages
-constexpr int kThreads = kEpi + 32 + 32 * kMmaWarps;   // + producer warp + MMA warps
+constexpr int kMaxMmaWarps = 5;       // MMA-issuing warps (at most), taking the stages in turn
 // stage flags: no more work (kFirstTerm: the record the epilogue receives) / last stage of a piece
 constexpr int kTerm = 1, kLast = 2, kFirstTerm = 4;
 // Longest piece: its keys' histogram is kept in 16-bit shared-memory counts until the piece ends
@@ -76,7 +75,7 @@ enum : uint32_t { kE4M3 = 0, kE2M1 = 5 };   // kind::f8f6f4 operand formats
 constexpr float kLoScale = 0.03125f;         // lo rows of the query operand carry 32 x the remainder
 
 constexpr int kSchedRows = 256;       // balanced piece schedule for up to this many query rows
-constexpr int kMaxBuf = 4;            // TMEM accumulator buffers (at most)
+constexpr int kMaxBuf = 5;            // TMEM accumulator buffers (at most)
 
 struct alignas(16) IdxMisc {
     alignas(16) uint32_t hist[2048];      // top-12-bit histogram of the scores since the last flush:
@@ -126,14 +125,18 @@ struct Cfg {
     static constexpr int fit256 = (int)((256 - sf_cols) / d_cols), fit512 = (int)((512 - sf_cols) / d_cols);
     static constexpr int nbuf_fit = fit256 >= 2 ? (fit256 < kMaxBuf ? fit256 : kMaxBuf)
                                                 : (fit512 < kMaxBuf ? (fit512 < 1 ? 1 : fit512) : kMaxBuf);
-    // Two MMA warps take alternate stages.  An mbarrier wait on a phase parity is only sound when
-    // its waiter consumes the barrier's phases one after another, so each warp must own its own
-    // stage slots and accumulator buffers: even counts of both (stage u: slot u % NS and buffer
-    // u % nbuf have the parity of u).  With a single buffer there is one MMA warp.
-    static constexpr int NMW = nbuf_fit >= 2 ? 2 : 1;
-    static constexpr int nbuf = NMW == 2 ? nbuf_fit / 2 * 2 : nbuf_fit;
-    static constexpr int NS = NMW == 2 ? ns_cap / 2 * 2 : ns_cap;
-    static_assert(NMW == 1 || (NS % 2 == 0 && nbuf % 2 == 0), "stage slots and buffers per MMA warp");
+    // NMW MMA warps take the stages in turn (warp u % NMW issues stage u).  An mbarrier wait on a
+    // phase parity is only sound when its waiter consumes the barrier's phases one after another,
+    // so each warp must own its own stage slots and accumulator buffers: both counts multiples of
+    // NMW (stage u: slot u % NS and buffer u % nbuf are congruent to u mod NMW).  Five warps with
+    // one slot and one buffer each where five of both fit (a slot count two warps cannot share
+    // evenly), else two warps, or one with a single buffer.
+    static constexpr int NMW = (ns_cap >= 5 && nbuf_fit >= 5) ? 5 : nbuf_fit >= 2 ? 2 : 1;
+    static constexpr int nbuf = nbuf_fit / NMW * NMW;
+    static constexpr int NS = ns_cap / NMW * NMW;
+    static_assert(NMW <= kMaxMmaWarps && NS >= NMW && nbuf >= NMW && NS % NMW == 0 && nbuf % NMW == 0,
+                  "stage slots and buffers per MMA warp");
+    static constexpr int threads = kEpi + 32 + 32 * NMW;   // + producer warp + MMA warps
     static constexpr uint32_t off_qslots = NS * stage;
     // e4m3: the row scales of the stage in each accumulator buffer (copied by the MMA warp)
     static constexpr uint32_t off_dscale = off_qslots + 2 * q_slot;
@@ -217,7 +220,7 @@ __device__ __forceinline__ void load_q_raw(const __nv_bfloat16* __restrict__ q_r
 }
 
 template <int FMT, int HI, bool Q4>
-__global__ void __launch_bounds__(kThreads) index_tc_kernel(const __grid_constant__ CUtensorMap kmap,
+__global__ void __launch_bounds__(Cfg<FMT, HI, Q4>::threads) index_tc_kernel(const __grid_constant__ CUtensorMap kmap,
                                                             const __nv_bfloat16* __restrict__ q_idx,
                                                             const uint8_t* __restrict__ q_scale,
                                                             const float* __restrict__ w,
@@ -452,13 +455,13 @@ __global__ void __launch_bounds__(kThreads) index_tc_kernel(const __grid_constan
             }
         }
         __syncwarp();
-    } else if (warp >= 5 && warp < 5 + kMmaWarps) {
+    } else if (warp >= 5 && warp < 5 + C::NMW) {
         // ============================================================================= MMA
         constexpr uint32_t af = C::fp4 ? kE2M1 : kE4M3;
         // descriptors of stage 0 and query slot 0; other addresses add (offset >> 4)
         const uint64_t a_desc0 = smem_desc(sbase, 16, 1024);
         const uint64_t b_desc0 = smem_desc(sbase + C::off_qslots, 16, 1024);
-        // stages u = mw, mw + kMmaWarps, ...: the two warps' per-stage waits and issue overlap; each
+        // stages u = mw, mw + NMW, ...: the warps' per-stage waits and issue overlap; each
         // stage's MMAs and commits come from one thread, so the commits track exactly that stage
         const uint32_t mw = (uint32_t)(warp - 5);
         int prev_piece = -1;                      // piece (low 15 bits) of this warp's previous stage
@@ -701,7 +704,7 @@ cudaError_t launch_index_tc(const void* q_idx, const void* q_scale, const float*
     const int R = B * T;
     const int64_t items = (int64_t)R * cdiv(Ncap, (int64_t)kChunkStages * kPair);
     const int grid = (int)std::min<int64_t>(items, (int64_t)num_sms() * occ);
-    (void)launch_pdl(kern, dim3(grid), dim3(kThreads), smem, st, kmap, static_cast<const __nv_bfloat16*>(q_idx),
+    (void)launch_pdl(kern, dim3(grid), dim3(C::threads), smem, st, kmap, static_cast<const __nv_bfloat16*>(q_idx),
                      static_cast<const uint8_t*>(q_scale), w,
                                        static_cast<const uint8_t*>(k_scale), T, q_pos, Ncap, m, R, S, hist1, err);
     return cudaGetLastError();
