@@ -130,8 +130,9 @@ struct Cfg {
     // so each warp must own its own stage slots and accumulator buffers: both counts multiples of
     // NMW (stage u: slot u % NS and buffer u % nbuf are congruent to u mod NMW).  Five warps with
     // one slot and one buffer each where five of both fit (a slot count two warps cannot share
-    // evenly), else two warps, or one with a single buffer.
-    static constexpr int NMW = (ns_cap >= 5 && nbuf_fit >= 5) ? 5 : nbuf_fit >= 2 ? 2 : 1;
+    // evenly) and the queries are bf16 (two operand parts per stage; with FP4 queries a stage is
+    // half the MMA work and five warps measured slower), else two warps, or one with a single buffer.
+    static constexpr int NMW = (!Q4 && ns_cap >= 5 && nbuf_fit >= 5) ? 5 : nbuf_fit >= 2 ? 2 : 1;
     static constexpr int nbuf = nbuf_fit / NMW * NMW;
     static constexpr int NS = ns_cap / NMW * NMW;
     static_assert(NMW <= kMaxMmaWarps && NS >= NMW && nbuf >= NMW && NS % NMW == 0 && nbuf % NMW == 0,
